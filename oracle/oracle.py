@@ -1,0 +1,159 @@
+"""Python binding of the plain CPU oracle (``spec_verify_oracle.c``).
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.  Only the test suite, the
+smoke check and the CPU-baseline leg of the benchmark import this module.  It
+shares no code with the CUDA library and never imports it.
+
+The arithmetic lives in C (fp64); this file only builds the shared object with
+gcc, marshals numpy arrays and names the rules.  Logits are numpy ``float32``
+arrays, or ``uint16`` arrays holding bf16 bit patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "spec_verify_oracle.c")
+LIBRARY = os.path.join(HERE, "liboracle.so")
+
+F32, BF16 = 0, 1
+RULE_MU = 0
+RULE_ORIGINAL_GATE = 1
+RULE_SAMPLER_MATCH = 2
+RULE_ARGMAX = 3
+RULE_RESAMPLE_P = 4
+RULE_RENORM_MU = 5
+RULE_RESIDUAL_Q = 6
+
+FLAG_UNREACHED, FLAG_ACCEPT, FLAG_REJECT, FLAG_NULL, FLAG_INVALID = 0, 1, 2, 3, 4
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction, so x86
+    and aarch64 hosts evaluate the same expressions)."""
+    with _lock:
+        fresh = os.path.exists(LIBRARY) and os.path.getmtime(LIBRARY) >= max(
+            os.path.getmtime(SOURCE), os.path.getmtime(os.path.join(HERE, "spec_verify_oracle.h")))
+        if force or not fresh:
+            tmp = LIBRARY + f".tmp{os.getpid()}"
+            subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-ffp-contract=off",
+                            "-fno-fast-math", "-fPIC", "-shared", SOURCE, "-o", tmp, "-lm",
+                            "-lpthread"], check=True)
+            os.replace(tmp, LIBRARY)
+    return LIBRARY
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(LIBRARY)
+        P = ctypes.c_void_p
+        L.oracle_philox4x32_10.argtypes = [P, P, P]
+        L.oracle_philox4x32_10.restype = None
+        L.oracle_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32]
+        L.oracle_uniform.restype = ctypes.c_double
+        L.oracle_softmax_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P]
+        L.oracle_softmax_row.restype = ctypes.c_int
+        L.oracle_inverse_cdf.argtypes = [P, ctypes.c_int64, ctypes.c_double, P]
+        L.oracle_inverse_cdf.restype = ctypes.c_int64
+        L.oracle_verify.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int64, ctypes.c_double, P, P, ctypes.c_uint64,
+                                    ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P,
+                                    ctypes.c_int]
+        L.oracle_verify.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return F32
+    if a.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"logits must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, seq: int, pos: int, draw: int) -> float:
+    return lib().oracle_uniform(seed, seq, pos, draw)
+
+
+def softmax_row(logits: np.ndarray, T: float):
+    """Returns (p, row_max, row_lse, valid)."""
+    x = np.ascontiguousarray(logits)
+    p = np.zeros(x.shape[-1], dtype=np.float64)
+    mx = np.zeros(1, dtype=np.float64)
+    lse = np.zeros(1, dtype=np.float64)
+    bad = lib().oracle_softmax_row(_ptr(x), _dtype_code(x), x.shape[-1], float(T), _ptr(p),
+                                   _ptr(mx), _ptr(lse))
+    return p, float(mx[0]), float(lse[0]), bad == 0
+
+
+def inverse_cdf(r: np.ndarray, u: float):
+    """Returns (index, margin)."""
+    w = np.ascontiguousarray(r, dtype=np.float64)
+    m = np.zeros(1, dtype=np.float64)
+    v = lib().oracle_inverse_cdf(_ptr(w), w.shape[0], float(u), _ptr(m))
+    return int(v), float(m[0])
+
+
+def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, seed: int = 0,
+           seq_offset: int = 0, u0=None, u1=None, rule: int = RULE_MU, nthreads: int = 1):
+    """Run the oracle on a batch.
+
+    Lt [B, k+1, V], Ld [B, k, V] (float32, or uint16 bf16 bits), D [B, k] int32.
+    ``gate`` and ``tau`` are per-sequence arrays (or scalars broadcast to B).
+    ``u0`` [B, k] / ``u1`` [B] give explicit uniforms instead of Philox draws.
+    Returns a dict of numpy arrays: accepted_len, tokens, alpha, flags,
+    row_stats [B, 2k+1, 2] (max, lse of L/T), margin, degenerate.
+    """
+    Lt = np.ascontiguousarray(Lt)
+    Ld = np.ascontiguousarray(Ld)
+    B, k1, V = Lt.shape
+    k = k1 - 1
+    if Ld.shape != (B, k, V):
+        raise ValueError(f"draft logits shape {Ld.shape} != {(B, k, V)}")
+    D = np.ascontiguousarray(D, dtype=np.int32).reshape(B, k)
+    gate = np.ascontiguousarray(np.broadcast_to(np.asarray(gate, dtype=np.uint8), (B,)))
+    tau = np.ascontiguousarray(np.broadcast_to(np.asarray(tau, dtype=np.float64), (B,)))
+    if u0 is not None:
+        u0 = np.ascontiguousarray(u0, dtype=np.float64).reshape(B, k)
+    if u1 is not None:
+        u1 = np.ascontiguousarray(u1, dtype=np.float64).reshape(B)
+    out = dict(
+        accepted_len=np.zeros(B, dtype=np.int32),
+        tokens=np.zeros((B, k + 1), dtype=np.int32),
+        alpha=np.zeros((B, k), dtype=np.float64),
+        flags=np.zeros((B, k), dtype=np.int8),
+        row_stats=np.zeros((B, 2 * k + 1, 2), dtype=np.float64),
+        margin=np.zeros(B, dtype=np.float64),
+        degenerate=np.zeros(B, dtype=np.int32),
+    )
+    rc = lib().oracle_verify(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B, k, V,
+                             float(T), _ptr(gate), _ptr(tau), int(seed), int(seq_offset), _ptr(u0),
+                             _ptr(u1), int(rule), _ptr(out["accepted_len"]), _ptr(out["tokens"]),
+                             _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
+                             _ptr(out["margin"]), _ptr(out["degenerate"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify rejected its arguments")
+    return out

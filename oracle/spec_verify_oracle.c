@@ -1,0 +1,445 @@
+/*
+ * spec_verify_oracle.c -- plain CPU oracle (fp64) for batched speculative-
+ * decoding verification.  TEST INFRASTRUCTURE: see spec_verify_oracle.h for
+ * the contract, the sources and who may call it.  Every step is written out
+ * the way the pages state it, one sequence at a time, with no fusion.
+ */
+#include "spec_verify_oracle.h"
+
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- Philox */
+
+/* Philox4x32-10 [P]: each round multiplies words 0 and 2 by the two round
+ * multipliers, mixes the high halves with words 1 and 3 and the key, and the
+ * key advances by the two Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const uint32_t mult0 = 0xD2511F53u, mult1 = 0xCD9E8D57u;
+  const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += weyl0;
+      k1 += weyl1;
+    }
+    uint64_t prod0 = (uint64_t)mult0 * (uint64_t)x0;
+    uint64_t prod1 = (uint64_t)mult1 * (uint64_t)x2;
+    uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+    uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+    uint32_t y0 = hi1 ^ x1 ^ k0;
+    uint32_t y1 = lo1;
+    uint32_t y2 = hi0 ^ x3 ^ k1;
+    uint32_t y3 = lo0;
+    x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+double oracle_uniform(uint64_t seed, uint64_t seq, uint32_t pos, uint32_t draw) {
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t ctr[4] = {(uint32_t)seq, pos, draw, (uint32_t)(seq >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  /* 24 high bits, scaled by 2^-24: exact in float and double */
+  return (double)(out[0] >> 8) * (1.0 / 16777216.0);
+}
+
+/* -------------------------------------------------------------- softmax */
+
+static double logit_at(const void* L, int dt, int64_t i) {
+  if (dt == ORACLE_F32) return (double)((const float*)L)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)L)[i] << 16; /* bf16 -> f32 is exact */
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* p = softmax(L / T) [M "What changed": the effective distribution is the
+ * temperature softmax over the full vocabulary].  Reading: -inf logits are
+ * allowed (p = 0); NaN, +inf or an all -inf row make the row invalid, the
+ * "non-finite observations fail closed" rule of [R]. */
+int oracle_softmax_row(const void* logits, int dt, int64_t V, double T,
+                       double* p, double* row_max, double* row_lse) {
+  double m = -INFINITY;
+  int bad = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    double x = logit_at(logits, dt, v);
+    if (isnan(x) || (isinf(x) && x > 0)) bad = 1;
+    double xs = x / T;
+    if (xs > m) m = xs;
+  }
+  if (row_max) *row_max = m;
+  if (bad || m == -INFINITY) {
+    if (row_lse) *row_lse = NAN;
+    return 1;
+  }
+  double s = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    double e = exp(logit_at(logits, dt, v) / T - m);
+    if (p) p[v] = e;
+    s += e;
+  }
+  if (p)
+    for (int64_t v = 0; v < V; ++v) p[v] /= s;
+  if (row_lse) *row_lse = m + log(s);
+  return 0;
+}
+
+/* ------------------------------------------------------------ sampling */
+
+/* Inverse-CDF pick: the smallest v with prefix(v) > u * Z.  Reading: the
+ * strict comparison means a zero-weight token is never picked, so the
+ * residual never emits a token with p <= mu ([M] "Where chi-square is
+ * blind").  If rounding left no such v, take the last v with weight > 0. */
+int64_t oracle_inverse_cdf(const double* r, int64_t V, double u, double* margin) {
+  double Z = 0.0;
+  for (int64_t v = 0; v < V; ++v) Z += r[v];
+  if (!(Z > 0.0)) {
+    if (margin) *margin = 0.0;
+    return -1;
+  }
+  double y = u * Z;
+  double before = 0.0, upto = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    before = upto;
+    upto += r[v];
+    if (upto > y) {
+      if (margin) *margin = fmin(fabs(u - before / Z), fabs(u - upto / Z));
+      return v;
+    }
+  }
+  for (int64_t v = V - 1; v >= 0; --v)
+    if (r[v] > 0.0) {
+      if (margin) *margin = 0.0;
+      return v;
+    }
+  return -1;
+}
+
+static int64_t argmax_first(const double* p, int64_t V) {
+  int64_t best = 0;
+  for (int64_t v = 1; v < V; ++v)
+    if (p[v] > p[best]) best = v;
+  return best;
+}
+
+/* ------------------------------------------------------ one sequence */
+
+typedef struct {
+  const void* Lt; int tdt;
+  const void* Ld; int ddt;
+  const int32_t* D;
+  int B, k;
+  int64_t V;
+  double T;
+  const uint8_t* gate;
+  const double* tau;
+  uint64_t seed, seq_offset;
+  const double* u0;
+  const double* u1;
+  int rule;
+  int32_t* accepted_len; int32_t* tokens; double* alpha; int8_t* flags;
+  double* row_stats; double* margin; int32_t* degenerate;
+} job_t;
+
+typedef struct {
+  double* P;   /* [k+1][V] target distributions p_j */
+  double* Q;   /* [k][V]   draft distributions q_j */
+  double* mu;  /* [V]      retained measure of one row */
+  double* r;   /* [V]      residual weights */
+} scratch_t;
+
+static double u_accept(const job_t* J, int b, int j) {
+  if (J->u0) return J->u0[(int64_t)b * J->k + j];
+  return oracle_uniform(J->seed, J->seq_offset + (uint64_t)b, (uint32_t)j, 0u);
+}
+
+static double u_residual(const job_t* J, int b, int jstar) {
+  if (J->u1) return J->u1[b];
+  return oracle_uniform(J->seed, J->seq_offset + (uint64_t)b, (uint32_t)jstar, 1u);
+}
+
+/* mu_j for the rule: plain mode mu = q; gated mode [S "Approach"]: q kept on
+ * admitted tokens (q >= tau, equality passes [R]) and NOT renormalised.  The
+ * RENORM_MU control renormalises it (the plausible mistake). */
+static void retained_measure(const job_t* J, int gated, double tau, const double* q, double* mu) {
+  int64_t V = J->V;
+  if (!gated) {
+    memcpy(mu, q, (size_t)V * sizeof(double));
+    return;
+  }
+  double kept = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    mu[v] = (q[v] >= tau) ? q[v] : 0.0;
+    kept += mu[v];
+  }
+  if (J->rule == ORACLE_RULE_RENORM_MU && kept > 0.0)
+    for (int64_t v = 0; v < V; ++v) mu[v] /= kept;
+}
+
+static void verify_one(const job_t* J, int b, scratch_t* S) {
+  const int k = J->k;
+  const int64_t V = J->V;
+  const int gated = J->gate[b] != 0;
+  const double tau = J->tau[b];
+  int32_t* tok = J->tokens + (int64_t)b * (k + 1);
+  double* al = J->alpha + (int64_t)b * k;
+  int8_t* fl = J->flags + (int64_t)b * k;
+  const int32_t* Db = J->D + (int64_t)b * k;
+  const int esz_t = J->tdt == ORACLE_BF16 ? 2 : 4, esz_d = J->ddt == ORACLE_BF16 ? 2 : 4;
+
+  /* step 1: the row distributions p_0..p_k and q_0..q_{k-1} */
+  int invalid = 0;
+  for (int j = 0; j <= k; ++j) {
+    const char* row = (const char*)J->Lt + ((int64_t)b * (k + 1) + j) * V * esz_t;
+    double mx, lse;
+    invalid |= oracle_softmax_row(row, J->tdt, V, J->T, S->P + (int64_t)j * V, &mx, &lse);
+    if (J->row_stats) {
+      J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 0] = mx;
+      J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 1] = lse;
+    }
+  }
+  for (int j = 0; j < k; ++j) {
+    const char* row = (const char*)J->Ld + ((int64_t)b * k + j) * V * esz_d;
+    double mx, lse;
+    invalid |= oracle_softmax_row(row, J->ddt, V, J->T, S->Q + (int64_t)j * V, &mx, &lse);
+    if (J->row_stats) {
+      J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 0] = mx;
+      J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 1] = lse;
+    }
+  }
+  for (int j = 0; j < k; ++j)
+    if (Db[j] < 0 || (int64_t)Db[j] >= V) invalid = 1;
+
+  double marg = INFINITY;
+  if (J->degenerate) J->degenerate[b] = 0;
+  if (invalid) {
+    J->accepted_len[b] = -1;
+    for (int j = 0; j <= k; ++j) tok[j] = -1;
+    for (int j = 0; j < k; ++j) {
+      al[j] = 0.0;
+      fl[j] = ORACLE_FLAG_INVALID;
+    }
+    if (J->margin) J->margin[b] = marg;
+    return;
+  }
+
+  /* step 2: acceptance probability of every position (also past j*).
+   * alpha = min(1, p(D)/mu(D)); NULL -> 0; mu(D) = 0 < p(D) -> 1; p(D) = 0 -> 0. */
+  for (int j = 0; j < k; ++j) {
+    const double pd = S->P[(int64_t)j * V + Db[j]];
+    const double qd = S->Q[(int64_t)j * V + Db[j]];
+    double a;
+    if (J->rule == ORACLE_RULE_ORIGINAL_GATE && gated && !(qd >= tau)) {
+      a = 0.0; /* failed gate: a target sample, no acceptance */
+    } else if (J->rule == ORACLE_RULE_ORIGINAL_GATE || J->rule == ORACLE_RULE_SAMPLER_MATCH ||
+               J->rule == ORACLE_RULE_ARGMAX) {
+      a = qd > 0.0 ? fmin(1.0, pd / qd) : (pd > 0.0 ? 1.0 : 0.0);
+    } else if (gated && !(qd >= tau)) {
+      a = 0.0; /* explicit NULL row */
+    } else {
+      retained_measure(J, gated, tau, S->Q + (int64_t)j * V, S->mu);
+      const double md = S->mu[Db[j]];
+      a = md > 0.0 ? fmin(1.0, pd / md) : (pd > 0.0 ? 1.0 : 0.0);
+    }
+    al[j] = a;
+    fl[j] = ORACLE_FLAG_UNREACHED;
+  }
+
+  /* step 3: walk the chain, stop at the first position not accepted [M] */
+  int jstar = k;
+  int resid_from_p = 0;   /* stop position samples p itself */
+  int resid_argmax = 0;   /* argmax control emits argmax p */
+  int64_t direct_token = -1; /* sampler-match control emits its own draw */
+  for (int j = 0; j < k; ++j) {
+    const double* pj = S->P + (int64_t)j * V;
+    const double* qj = S->Q + (int64_t)j * V;
+    const int32_t d = Db[j];
+    const double u = u_accept(J, b, j);
+
+    if (J->rule == ORACLE_RULE_SAMPLER_MATCH) {
+      /* [M] sampler-match: a fresh target draw; accept iff it equals D */
+      double m;
+      int64_t x = oracle_inverse_cdf(pj, V, u, &m);
+      marg = fmin(marg, m);
+      if (x == d) {
+        fl[j] = ORACLE_FLAG_ACCEPT;
+        continue;
+      }
+      fl[j] = ORACLE_FLAG_REJECT;
+      jstar = j;
+      direct_token = x;
+      break;
+    }
+    if (J->rule == ORACLE_RULE_ARGMAX) {
+      /* [M] argmax-against-argmax: accept iff D is the target argmax */
+      if ((int64_t)d == argmax_first(pj, V)) {
+        fl[j] = ORACLE_FLAG_ACCEPT;
+        continue;
+      }
+      fl[j] = ORACLE_FLAG_REJECT;
+      jstar = j;
+      resid_argmax = 1;
+      break;
+    }
+    if (J->rule == ORACLE_RULE_ORIGINAL_GATE) {
+      /* [S "Problem and result"]: the gate filters drafts, acceptance uses
+       * the unfiltered q, and a failed gate becomes a plain target sample */
+      if (gated) {
+        marg = fmin(marg, fabs(qj[d] - tau));
+        if (!(qj[d] >= tau)) {
+          fl[j] = ORACLE_FLAG_NULL;
+          jstar = j;
+          resid_from_p = 1;
+          break;
+        }
+      }
+      if (qj[d] > 0.0 && pj[d] < qj[d]) marg = fmin(marg, fabs(u - pj[d] / qj[d]));
+      if (pj[d] > 0.0 && u * qj[d] <= pj[d]) {
+        fl[j] = ORACLE_FLAG_ACCEPT;
+        continue;
+      }
+      fl[j] = ORACLE_FLAG_REJECT;
+      jstar = j;
+      break;
+    }
+
+    /* the method (and the RESAMPLE_P / RENORM_MU / RESIDUAL_Q controls) */
+    if (gated) {
+      marg = fmin(marg, fabs(qj[d] - tau));
+      if (!(qj[d] >= tau)) { /* failed gate: explicit NULL row [S "Approach"] */
+        fl[j] = ORACLE_FLAG_NULL;
+        jstar = j;
+        break;
+      }
+    }
+    retained_measure(J, gated, tau, qj, S->mu);
+    const double md = S->mu[d];
+    if (md > 0.0 && pj[d] < md) marg = fmin(marg, fabs(u - pj[d] / md));
+    /* accept test p(D) > 0 && u * mu(D) <= p(D) [M "What changed"] */
+    if (pj[d] > 0.0 && u * md <= pj[d]) {
+      fl[j] = ORACLE_FLAG_ACCEPT;
+      continue;
+    }
+    fl[j] = ORACLE_FLAG_REJECT;
+    jstar = j;
+    break;
+  }
+  if (J->rule == ORACLE_RULE_RESAMPLE_P && jstar < k) resid_from_p = 1;
+
+  /* step 4/5: what the stop row emits */
+  int64_t pick;
+  if (direct_token >= 0) {
+    pick = direct_token;
+  } else if (resid_argmax || (J->rule == ORACLE_RULE_ARGMAX && jstar == k)) {
+    pick = argmax_first(S->P + (int64_t)jstar * V, V);
+  } else {
+    const double* pst = S->P + (int64_t)jstar * V;
+    const double u = u_residual(J, b, jstar);
+    if (jstar == k || resid_from_p) {
+      /* ordinary bonus sample of p [S "Approach"] (and the p-resampling controls) */
+      memcpy(S->r, pst, (size_t)V * sizeof(double));
+    } else {
+      /* residual (p - mu)+ [S "Approach"]; plain mode mu = q [M] */
+      const double* qst = S->Q + (int64_t)jstar * V;
+      if (J->rule == ORACLE_RULE_ORIGINAL_GATE || J->rule == ORACLE_RULE_RESIDUAL_Q) {
+        memcpy(S->mu, qst, (size_t)V * sizeof(double));
+      } else {
+        retained_measure(J, gated, tau, qst, S->mu);
+      }
+      if (gated)
+        for (int64_t v = 0; v < V; ++v) marg = fmin(marg, fabs(qst[v] - tau));
+      double Z = 0.0;
+      for (int64_t v = 0; v < V; ++v) {
+        double d = pst[v] - S->mu[v];
+        S->r[v] = d > 0.0 ? d : 0.0;
+        Z += S->r[v];
+      }
+      if (!(Z > 0.0)) {
+        /* reading: a residual with no mass falls back to sampling p */
+        memcpy(S->r, pst, (size_t)V * sizeof(double));
+        if (J->degenerate) J->degenerate[b] = 1;
+      }
+    }
+    double m;
+    pick = oracle_inverse_cdf(S->r, V, u, &m);
+    marg = fmin(marg, m);
+  }
+
+  /* step 6: outputs */
+  J->accepted_len[b] = jstar;
+  for (int j = 0; j < jstar; ++j) tok[j] = Db[j];
+  tok[jstar] = (int32_t)pick;
+  for (int j = jstar + 1; j <= k; ++j) tok[j] = -1;
+  if (J->margin) J->margin[b] = marg;
+}
+
+/* ------------------------------------------------------------- batch */
+
+typedef struct {
+  const job_t* J;
+  int first, stride;
+  int err;
+} worker_t;
+
+static void* worker_main(void* arg) {
+  worker_t* w = (worker_t*)arg;
+  const job_t* J = w->J;
+  scratch_t S;
+  const size_t V = (size_t)J->V;
+  S.P = (double*)malloc((size_t)(J->k + 1) * V * sizeof(double));
+  S.Q = (double*)malloc((size_t)(J->k > 0 ? J->k : 1) * V * sizeof(double));
+  S.mu = (double*)malloc(V * sizeof(double));
+  S.r = (double*)malloc(V * sizeof(double));
+  if (!S.P || !S.Q || !S.mu || !S.r) {
+    w->err = 1;
+  } else {
+    for (int b = w->first; b < J->B; b += w->stride) verify_one(J, b, &S);
+  }
+  free(S.P); free(S.Q); free(S.mu); free(S.r);
+  return NULL;
+}
+
+int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                  int B, int k, int64_t V, double T,
+                  const uint8_t* gate, const double* tau,
+                  uint64_t seed, uint64_t seq_offset,
+                  const double* u0, const double* u1, int rule,
+                  int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                  double* row_stats, double* margin, int32_t* degenerate,
+                  int nthreads) {
+  if (B < 0 || k < 1 || V < 1 || !(T > 0.0) || isinf(T)) return 1;
+  if (B == 0) return 0;
+  if (!Lt || !Ld || !D || !gate || !tau || !accepted_len || !tokens || !alpha || !flags) return 1;
+  if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
+  if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_RESIDUAL_Q) return 1;
+  job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
+             accepted_len, tokens, alpha, flags, row_stats, margin, degenerate};
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > B) nthreads = B;
+  worker_t* ws = (worker_t*)calloc((size_t)nthreads, sizeof(worker_t));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!ws || !th) {
+    free(ws); free(th);
+    return 1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    ws[t].J = &J;
+    ws[t].first = t;
+    ws[t].stride = nthreads;
+  }
+  int err = 0;
+  if (nthreads == 1) {
+    worker_main(&ws[0]);
+  } else {
+    for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, worker_main, &ws[t]);
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  }
+  for (int t = 0; t < nthreads; ++t) err |= ws[t].err;
+  free(ws); free(th);
+  return err ? 1 : 0;
+}

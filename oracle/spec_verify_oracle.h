@@ -1,0 +1,111 @@
+/*
+ * spec_verify_oracle.h -- plain CPU oracle for batched speculative-decoding
+ * verification (modified rejection sampling, plain and mu/NULL-gated modes).
+ *
+ * TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark load this code.
+ * It shares no source with the CUDA library: its Philox generator, softmax,
+ * decision rule and inverse-CDF sampler are written out here independently,
+ * in double precision, one sequence at a time, with no blocking or fusion.
+ *
+ * Sources the arithmetic follows (web pages, cited by title and section):
+ *   [S]  Strata PR #3416 "[Engine] Preserve target probabilities in gated
+ *        MTP" -- sections "Problem and result" (the worked example and the
+ *        biased original gate) and "Approach" (retained measure mu, explicit
+ *        NULL row, min(1, p(D)/mu(D)) acceptance, residual (p - mu)+,
+ *        ordinary bonus sample).
+ *   [M]  mlxcel PR #992 "modified rejection sampling" -- sections "The
+ *        acceptance ceiling" (sum min(p,q) = 1 - TV, sampler-match sum p*q,
+ *        argmax rule), "What changed" (accept test p(t) > 0 && u*q(t) <= p(t),
+ *        residual normalise(relu(p - q)), fp32 effective distribution) and
+ *        "Two metric corrections" (a chain stops at its first rejection).
+ *   [R]  regolith audit "rank-1 moce and step-aware speculative retention",
+ *        section "schedule behavior" (equality passes the gate; a failed gate
+ *        ends the contiguous prefix).
+ *   [P]  J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel random
+ *        numbers: as easy as 1, 2, 3", SC'11 -- the Philox4x32 bijection.
+ *
+ * Readings where the pages are silent are listed beside each function.
+ */
+#ifndef SPEC_VERIFY_ORACLE_H
+#define SPEC_VERIFY_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element types of the logits arrays */
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* decision rules.  ORACLE_RULE_MU is the method; the others are controls
+ * (known-correct or known-wrong rules) that the statistical tests need. */
+enum {
+  ORACLE_RULE_MU = 0,            /* plain MRS (gate off) / mu-NULL rule (gate on) */
+  ORACLE_RULE_ORIGINAL_GATE = 1, /* [S] biased: unfiltered q, failed gate samples p */
+  ORACLE_RULE_SAMPLER_MATCH = 2, /* [M] lossless: accept iff a fresh p draw equals D */
+  ORACLE_RULE_ARGMAX = 3,        /* [M] biased: accept iff D == argmax p, emit argmax */
+  ORACLE_RULE_RESAMPLE_P = 4,    /* [M] biased: on rejection sample p, not the residual */
+  ORACLE_RULE_RENORM_MU = 5,     /* plausible mistake: mu renormalised over admitted set */
+  ORACLE_RULE_RESIDUAL_Q = 6     /* plausible mistake: gated residual uses (p - q)+ */
+};
+
+/* per-position flags (same values as the CUDA library's outputs) */
+enum {
+  ORACLE_FLAG_UNREACHED = 0,
+  ORACLE_FLAG_ACCEPT = 1,
+  ORACLE_FLAG_REJECT = 2,
+  ORACLE_FLAG_NULL = 3,
+  ORACLE_FLAG_INVALID = 4
+};
+
+/* Philox4x32 with 10 rounds [P]: out = bijection_key(ctr). */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* U(seed, seq, pos, draw): key = (seed lo32, seed hi32), counter =
+ * (seq lo32, pos, draw, seq hi32); u = (out[0] >> 8) * 2^-24, in [0, 1). */
+double oracle_uniform(uint64_t seed, uint64_t seq, uint32_t pos, uint32_t draw);
+
+/* Temperature softmax of one row of V logits (element type dt):
+ * p[v] = exp(L[v]/T - m) / sum_w exp(L[w]/T - m), m = max_v L[v]/T.
+ * Writes p (may be NULL), *row_max = m and *row_lse = m + ln(sum).
+ * Returns 0, or 1 when the row is invalid (a NaN or +inf logit, or every
+ * logit -inf). */
+int oracle_softmax_row(const void* logits, int dt, int64_t V, double T,
+                       double* p, double* row_max, double* row_lse);
+
+/* Inverse-CDF pick over the weights r[0..V): the smallest v whose inclusive
+ * prefix sum exceeds u * Z (Z = sum r); if rounding leaves none, the last v
+ * with r[v] > 0; -1 if every weight is zero.  *margin (may be NULL) receives
+ * the distance of u to the two edges of the chosen interval, in units of Z. */
+int64_t oracle_inverse_cdf(const double* r, int64_t V, double u, double* margin);
+
+/*
+ * Verify a batch.  Shapes (row-major, V innermost):
+ *   Lt [B, k+1, V] (dt tdt), Ld [B, k, V] (dt ddt), D [B, k] int32.
+ *   gate[B]   0 = plain, 1 = mu/NULL gated;  tau[B] thresholds (gated rows).
+ *   u0 [B, k], u1 [B]: explicit uniforms, or NULL to draw them from Philox:
+ *     u0[b,j] = U(seed, seq_offset + b, j, 0), u1[b] = U(seed, seq_offset+b, j*, 1).
+ * Outputs (all host):
+ *   accepted_len[B] (-1 for an invalid sequence), tokens[B, k+1] (-1 padded),
+ *   alpha[B, k] (acceptance probability of every position, also past j*),
+ *   flags[B, k], and optionally row_stats[B, 2k+1, 2] = (max, lse) of L/T for
+ *   target rows 0..k then draft rows 0..k-1, margin[B] = the smallest distance
+ *   of a used uniform (or of q(D), or of any q on the residual row) to its
+ *   decision boundary, degenerate[B] = 1 when the residual had zero mass.
+ * nthreads >= 1 threads split the sequences.  Returns 0, or 1 on bad args.
+ */
+int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                  int B, int k, int64_t V, double T,
+                  const uint8_t* gate, const double* tau,
+                  uint64_t seed, uint64_t seq_offset,
+                  const double* u0, const double* u1, int rule,
+                  int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                  double* row_stats, double* margin, int32_t* degenerate,
+                  int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,381 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these tests compares the oracle with a retyped copy of itself: each
+checks a printed value (the gated worked example, the Philox known answers,
+the chi-square threshold), a closed form (sum min(p, q) = 1 - TV, sum p*q), a
+library routine (scipy's logsumexp), an exact law obtained by enumeration, or
+a zero-tolerance support property.  Known-wrong control rules show that each
+law test has the power to reject a plausible mistake.
+"""
+import os
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+from scipy.stats import chi2
+
+from oracle import oracle as O
+from tests.law import distributions, exact_law, position_marginals
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ Philox
+
+def test_philox_known_answers():
+    for row in _golden_rows("philox4x32_10_kat.txt"):
+        w = [int(x, 16) for x in row]
+        out = O.philox4x32_10(w[0:4], w[4:6])
+        assert [int(x) for x in out] == w[6:10]
+
+
+def test_uniform_maps_seed_sequence_position_draw_onto_key_and_counter():
+    # key = (seed lo, seed hi), counter = (seq lo, pos, draw, seq hi), u = (out0 >> 8) 2^-24
+    rows = [[int(x, 16) for x in r] for r in _golden_rows("philox4x32_10_kat.txt")]
+    for c0, c1, c2, c3, k0, k1, o0, *_ in rows:
+        seed = k0 | (k1 << 32)
+        seq = c0 | (c3 << 32)
+        assert O.uniform(seed, seq, c1, c2) == (o0 >> 8) / 2.0 ** 24
+
+
+def test_uniforms_are_24_bit_grid_points_and_look_uniform():
+    u = np.array([O.uniform(12345, b, j, d) for b in range(200) for j in range(5) for d in range(2)])
+    assert np.all((u >= 0) & (u < 1))
+    assert np.all(u * 2 ** 24 == np.floor(u * 2 ** 24))
+    # Kolmogorov-Smirnov distance against U[0,1) for 2000 draws: 1.95/sqrt(n) is alpha ~ 1e-3
+    s = np.sort(u)
+    n = len(s)
+    ks = max(np.max(np.arange(1, n + 1) / n - s), np.max(s - np.arange(n) / n))
+    assert ks < 1.95 / np.sqrt(n)
+
+
+# ------------------------------------------------------------------ softmax
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 1.5])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_softmax_row_matches_library_logsumexp(T, bf16):
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(1000) * 4).astype(np.float32)
+    if bf16:
+        bits = x.view(np.uint32) >> 16
+        arr = bits.astype(np.uint16)
+        x = (bits << 16).astype(np.uint32).view(np.float32)
+    else:
+        arr = x
+    p, mx, lse, ok = O.softmax_row(arr, T)
+    xs = x.astype(np.float64) / T
+    assert ok
+    assert mx == np.max(xs)
+    assert abs(lse - logsumexp(xs)) <= 1e-12 * abs(logsumexp(xs))
+    np.testing.assert_allclose(p, softmax(xs), rtol=1e-12, atol=0)
+
+
+def test_softmax_row_invalid_and_minus_inf():
+    x = np.array([0.0, -np.inf, 1.0], dtype=np.float32)
+    p, _, _, ok = O.softmax_row(x, 1.0)
+    assert ok and p[1] == 0.0 and abs(p.sum() - 1) < 1e-15
+    for bad in ([0.0, np.nan, 1.0], [0.0, np.inf, 1.0], [-np.inf, -np.inf]):
+        _, _, _, ok = O.softmax_row(np.array(bad, dtype=np.float32), 1.0)
+        assert not ok
+
+
+# ------------------------------------------------------------- inverse CDF
+
+def test_inverse_cdf_law_and_zero_weights():
+    r = np.array([0.0, 0.2, 0.0, 0.5, 0.3, 0.0])
+    # law over a fine u grid equals r / Z; zero-weight tokens never picked
+    us = (np.arange(100000) + 0.5) / 100000
+    picks = np.array([O.inverse_cdf(r, u)[0] for u in us[::10]])
+    freq = np.bincount(picks, minlength=6) / len(picks)
+    np.testing.assert_allclose(freq, r / r.sum(), atol=2e-4)
+    assert O.inverse_cdf(r, 0.0)[0] == 1  # u = 0 must not pick the leading zero-weight token
+    assert O.inverse_cdf(r, 1.0 - 2.0 ** -24)[0] == 4
+    assert O.inverse_cdf(np.zeros(4), 0.3)[0] == -1
+
+
+# ---------------------------------------------------------- exact laws
+
+def _check_lossless(law, P, Q, gated, tau, tol=1e-10):
+    k = Q.shape[0]
+    V = P.shape[1]
+    reach, emit, passed = position_marginals(law, k, V)
+    assert abs(sum(law.values()) - 1.0) < tol
+    for j in range(k + 1):
+        if reach[j] > 1e-9:
+            np.testing.assert_allclose(emit[j] / reach[j], P[j], atol=tol / reach[j])
+    for j in range(k):
+        if reach[j] > 1e-9:
+            mu = Q[j] * (Q[j] >= tau) if gated else Q[j]
+            assert abs(passed[j] / reach[j] - np.minimum(P[j], mu).sum()) < tol / reach[j]
+
+
+def _worked_example():
+    g = {r[0]: [float(x) for x in r[1:]] for r in _golden_rows("gated_worked_example.txt")}
+    p, q = np.array(g["p"]), np.array(g["q"])
+    Lt = np.log(np.stack([p, p])).astype(np.float32)  # k = 1: position 0 and the bonus row
+    Ld = np.log(q)[None, :].astype(np.float32)
+    return g, Lt, Ld
+
+
+def test_worked_example_mu_rule_emits_p():
+    g, Lt, Ld = _worked_example()
+    law = exact_law(Lt, Ld, 1.0, True, g["threshold"][0], rule=O.RULE_MU)
+    _, emit, _ = position_marginals(law, 1, 2)
+    # the first emitted token's law is printed on the page; exact up to fp32 logits
+    np.testing.assert_allclose(emit[0], g["emitted_mu_rule"], atol=1e-12)
+
+
+def test_worked_example_original_gate_is_biased_as_printed():
+    g, Lt, Ld = _worked_example()
+    law = exact_law(Lt, Ld, 1.0, True, g["threshold"][0], rule=O.RULE_ORIGINAL_GATE)
+    _, emit, _ = position_marginals(law, 1, 2)
+    # fp32 logits move q by ~1e-8 from (0.875, 0.125); the biased law moves with it
+    np.testing.assert_allclose(emit[0], g["emitted_original_gate"], atol=1e-7)
+
+
+def _random_case(rng, V, k, scale=2.0, noise=1.0):
+    Lt = (rng.standard_normal((k + 1, V)) * scale).astype(np.float32)
+    Ld = (Lt[:k] + rng.standard_normal((k, V)) * noise).astype(np.float32)
+    return Lt, Ld
+
+
+@pytest.mark.parametrize("V,k", [(2, 1), (3, 2), (5, 2), (8, 3)])
+@pytest.mark.parametrize("gated,tau", [(False, 0.5), (True, 0.5), (True, 0.3)])
+def test_exact_law_is_lossless(V, k, gated, tau):
+    rng = np.random.default_rng(100 * V + 10 * k + int(gated) + int(tau * 10))
+    for trial in range(2):
+        Lt, Ld = _random_case(rng, V, k, scale=2.0 + trial)
+        T = 1.0 if trial == 0 else 0.7
+        law = exact_law(Lt, Ld, T, gated, tau)
+        P, Q = distributions(Lt, Ld, T)
+        _check_lossless(law, P, Q, gated, tau)
+
+
+def test_exact_law_plain_pass_rate_is_one_minus_tv():
+    rng = np.random.default_rng(7)
+    Lt, Ld = _random_case(rng, 6, 2)
+    law = exact_law(Lt, Ld, 1.0, False, 0.5)
+    P, Q = distributions(Lt, Ld, 1.0)
+    reach, _, passed = position_marginals(law, 2, 6)
+    for j in range(2):
+        tv = 0.5 * np.abs(P[j] - Q[j]).sum()
+        assert abs(passed[j] / reach[j] - (1.0 - tv)) < 1e-10
+        assert passed[j] / reach[j] >= (P[j] * Q[j]).sum()
+
+
+@pytest.mark.parametrize("rule", [O.RULE_ORIGINAL_GATE, O.RULE_RESAMPLE_P, O.RULE_ARGMAX,
+                                  O.RULE_RENORM_MU, O.RULE_RESIDUAL_Q])
+def test_exact_law_rejects_known_wrong_rules(rule):
+    # p = (0.5, 0.25, 0.25), q = (0.6, 0.35, 0.05), tau = 0.5: each mistake moves the law
+    p = np.array([0.5, 0.25, 0.25])
+    q = np.array([0.6, 0.35, 0.05])
+    Lt = np.log(np.stack([p, p])).astype(np.float32)
+    Ld = np.log(q)[None, :].astype(np.float32)
+    law = exact_law(Lt, Ld, 1.0, True, 0.5, rule=rule)
+    _, emit, _ = position_marginals(law, 1, 3)
+    assert np.max(np.abs(emit[0] - p)) > 1e-2
+
+
+def test_exact_law_sampler_match_control_is_lossless_with_sum_pq():
+    # sampler-match: accept iff a fresh target draw equals D; acceptance sum p*q [mlxcel #992]
+    rng = np.random.default_rng(11)
+    V, k, n = 5, 1, 200000
+    Lt, Ld = _random_case(rng, V, k)
+    P, Q = distributions(Lt, Ld, 1.0)
+    D = rng.choice(V, size=(n, k), p=Q[0])
+    out = O.verify(np.broadcast_to(Lt, (n, k + 1, V)), np.broadcast_to(Ld, (n, k, V)), D, 1.0, 0, 0.5,
+                   seed=5, rule=O.RULE_SAMPLER_MATCH, nthreads=4)
+    acc = (out["accepted_len"] >= 1).mean()
+    spq = (P[0] * Q[0]).sum()
+    assert abs(acc - spq) < 4 * np.sqrt(spq * (1 - spq) / n)
+    assert spq <= np.minimum(P[0], Q[0]).sum()
+    counts = np.bincount(out["tokens"][:, 0], minlength=V)
+    stat = ((counts - n * P[0]) ** 2 / (n * P[0])).sum()
+    assert stat < chi2.ppf(1 - 1e-4, V - 1)
+
+
+def test_alpha_averages_to_sum_min_closed_form():
+    # E_{D~q}[alpha(D)] = sum_x min(p, mu): pins alpha = min(1, p/mu) on every token
+    rng = np.random.default_rng(5)
+    V = 7
+    Lt, Ld = _random_case(rng, V, 1)
+    P, Q = distributions(Lt, Ld, 1.0)
+    D = np.arange(V, dtype=np.int32)[:, None]
+    for gated, tau in [(False, 0.5), (True, 0.2), (True, 0.45)]:
+        out = O.verify(np.broadcast_to(Lt, (V, 2, V)), np.broadcast_to(Ld, (V, 1, V)), D, 1.0,
+                       int(gated), tau, seed=1)
+        mu = Q[0] * (Q[0] >= tau) if gated else Q[0]
+        assert abs((Q[0] * out["alpha"][:, 0]).sum() - np.minimum(P[0], mu).sum()) < 1e-14
+
+
+# ---------------------------------------------------------------- chi-square
+
+def test_page_chi_square_threshold_is_the_library_quantile():
+    g = {r[0]: float(r[1]) for r in _golden_rows("chi_square_threshold.txt")}
+    assert abs(chi2.ppf(1 - g["alpha"], int(g["dof"])) - g["threshold"]) < 1e-4
+
+
+def _tiny_config(rng, n):
+    # tiny config: V=8, k=3, target ~ N(0, 2^2), draft = target + N(0, 1), T = 1
+    V, k = 8, 3
+    Lt, Ld = _random_case(rng, V, k)
+    _, Q = distributions(Lt, Ld, 1.0)
+    D = np.stack([rng.choice(V, size=n, p=Q[j]) for j in range(k)], axis=1).astype(np.int32)
+    return Lt, Ld, D
+
+
+def _chi_square_position0(out, P0):
+    n = out["tokens"].shape[0]
+    counts = np.bincount(out["tokens"][:, 0], minlength=len(P0))
+    return ((counts - n * P0) ** 2 / (n * P0)).sum()
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_chi_square_emitted_tokens_follow_p(gated):
+    rng = np.random.default_rng(21 + gated)
+    n = 100000
+    Lt, Ld, D = _tiny_config(rng, n)
+    P, Q = distributions(Lt, Ld, 1.0)
+    out = O.verify(np.broadcast_to(Lt, (n, 4, 8)), np.broadcast_to(Ld, (n, 3, 8)), D, 1.0, int(gated),
+                   0.5, seed=2024, nthreads=4)
+    thr = chi2.ppf(1 - 1e-4, 7)
+    assert _chi_square_position0(out, P[0]) < thr
+    # every later position, conditional on being reached, also follows p_j
+    for j in range(1, 4):
+        sel = out["accepted_len"] >= j
+        if sel.sum() > 2000:
+            counts = np.bincount(out["tokens"][sel, j], minlength=8)
+            m = sel.sum()
+            assert ((counts - m * P[j]) ** 2 / (m * P[j])).sum() < thr
+
+
+@pytest.mark.parametrize("rule", [O.RULE_RESAMPLE_P, O.RULE_ARGMAX, O.RULE_ORIGINAL_GATE])
+def test_chi_square_rejects_known_wrong_rules(rule):
+    rng = np.random.default_rng(40 + rule)
+    n = 100000
+    if rule == O.RULE_ORIGINAL_GATE:
+        p, q = np.array([0.5, 0.5]), np.array([0.875, 0.125])
+        Lt = np.log(np.stack([p, p])).astype(np.float32)
+        Ld = np.log(q)[None, :].astype(np.float32)
+        D = rng.choice(2, size=(n, 1), p=q).astype(np.int32)
+        k, V = 1, 2
+    else:
+        Lt, Ld, D = _tiny_config(rng, n)
+        k, V = 3, 8
+    P, _ = distributions(Lt, Ld, 1.0)
+    out = O.verify(np.broadcast_to(Lt, (n, k + 1, V)), np.broadcast_to(Ld, (n, k, V)), D, 1.0, 1,
+                   0.5, seed=7, rule=rule, nthreads=4)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        assert _chi_square_position0(out, P[0]) > chi2.ppf(1 - 1e-4, V - 1)
+
+
+# ----------------------------------------------------------- support, edges
+
+def test_zero_target_mass_is_never_accepted_or_emitted():
+    # token 0 has p = 0 (target logit -inf); the drafter offers it, sometimes with q = 0 too
+    rng = np.random.default_rng(9)
+    n, V = 4000, 4
+    Lt = np.tile(np.array([-np.inf, 0.0, 0.5, -1.0], dtype=np.float32), (n, 2, 1))
+    Ld = np.tile(np.array([1.0, 0.0, 0.0, 0.0], dtype=np.float32), (n, 1, 1))
+    Ld[: n // 2, 0, 0] = -np.inf  # underflowed proposal mass: u * 0 <= 0 must not accept
+    D = np.zeros((n, 1), dtype=np.int32)
+    for gated in (0, 1):
+        out = O.verify(Lt, Ld, D, 1.0, gated, 0.3, seed=rng.integers(1 << 60))
+        assert np.all(out["accepted_len"] == 0)
+        assert np.all(out["tokens"][:, 0] != 0)
+        assert np.all(out["alpha"][:, 0] == 0.0)
+
+
+def test_residual_never_emits_tokens_where_p_le_mu():
+    rng = np.random.default_rng(13)
+    n, V = 20000, 6
+    Lt, Ld = _random_case(rng, V, 1, scale=1.5, noise=1.5)
+    P, Q = distributions(Lt, Ld, 1.0)
+    D = rng.choice(V, size=(n, 1), p=Q[0]).astype(np.int32)
+    for gated, tau in [(0, 0.5), (1, 0.25)]:
+        out = O.verify(np.broadcast_to(Lt, (n, 2, V)), np.broadcast_to(Ld, (n, 1, V)), D, 1.0, gated,
+                       tau, seed=3)
+        mu = Q[0] * (Q[0] >= tau) if gated else Q[0]
+        stopped = out["accepted_len"] == 0
+        assert stopped.any()
+        assert np.all(P[0][out["tokens"][stopped, 0]] > mu[out["tokens"][stopped, 0]])
+
+
+def test_gate_equality_passes():
+    # q = (0.5, 0.5) exactly (equal logits); threshold 0.5: the offered token is admitted, not NULL
+    Lt = np.zeros((1, 2, 2), dtype=np.float32)
+    Ld = np.zeros((1, 1, 2), dtype=np.float32)
+    out = O.verify(Lt, Ld, np.array([[1]]), 1.0, 1, 0.5, u0=np.array([[0.999]]), u1=np.array([0.1]))
+    assert out["flags"][0, 0] == O.FLAG_ACCEPT and out["alpha"][0, 0] == 1.0
+
+
+def test_null_row_ends_the_chain_and_samples_the_residual():
+    # gated, q(D) < tau: flag NULL, alpha 0, later positions unreached
+    p = np.array([0.5, 0.5])
+    q = np.array([0.875, 0.125])
+    Lt = np.log(np.stack([p, p, p])).astype(np.float32)[None]
+    Ld = np.log(np.stack([q, q])).astype(np.float32)[None]
+    out = O.verify(Lt, Ld, np.array([[1, 0]]), 1.0, 1, 0.5, u0=np.array([[0.0, 0.0]]),
+                   u1=np.array([0.0]))
+    assert out["accepted_len"][0] == 0
+    assert list(out["flags"][0]) == [O.FLAG_NULL, O.FLAG_UNREACHED]
+    assert out["tokens"][0, 0] == 1  # residual (p - mu)+ = (0, 0.5): only token 1
+    assert list(out["tokens"][0, 1:]) == [-1, -1]
+    assert out["alpha"][0, 0] == 0.0 and out["alpha"][0, 1] > 0.5
+
+
+def test_invalid_sequences_fail_closed():
+    rng = np.random.default_rng(1)
+    Lt, Ld = _random_case(rng, 5, 2)
+    Lt = np.stack([Lt] * 4)
+    Ld = np.stack([Ld] * 4)
+    D = np.zeros((4, 2), dtype=np.int32)
+    Lt[1, 2, 3] = np.nan       # NaN in the bonus row
+    Ld[2, 0, :] = -np.inf      # all -inf draft row
+    D[3, 1] = 5                # token out of range
+    out = O.verify(Lt, Ld, D, 1.0, 0, 0.5, seed=1)
+    assert out["accepted_len"][0] >= 0
+    for b in (1, 2, 3):
+        assert out["accepted_len"][b] == -1
+        assert np.all(out["tokens"][b] == -1)
+        assert np.all(out["flags"][b] == O.FLAG_INVALID)
+
+
+def test_sequence_offset_and_threads_do_not_change_results():
+    rng = np.random.default_rng(8)
+    B, k, V = 24, 3, 16
+    Lt = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    Ld = (Lt[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    D = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    gate = (np.arange(B) % 2).astype(np.uint8)
+    full = O.verify(Lt, Ld, D, 0.8, gate, 0.3, seed=99, nthreads=1)
+    thr = O.verify(Lt, Ld, D, 0.8, gate, 0.3, seed=99, nthreads=5)
+    for key in full:
+        np.testing.assert_array_equal(full[key], thr[key])
+    half = O.verify(Lt[12:], Ld[12:], D[12:], 0.8, gate[12:], 0.3, seed=99, seq_offset=12)
+    for key in full:
+        np.testing.assert_array_equal(full[key][12:], half[key])
+
+
+def test_margin_reports_draws_near_a_boundary():
+    p = np.array([0.5, 0.5])
+    q = np.array([0.8, 0.2])
+    Lt = np.log(np.stack([p, p])).astype(np.float32)[None]
+    Ld = np.log(q).astype(np.float32)[None, None]
+    P, Q = distributions(Lt[0], Ld[0], 1.0)
+    ratio = P[0, 0] / Q[0, 0]
+    near = O.verify(Lt, Ld, np.array([[0]]), 1.0, 0, 0.5, u0=np.array([[ratio + 3e-7]]),
+                    u1=np.array([0.5]))
+    far = O.verify(Lt, Ld, np.array([[0]]), 1.0, 0, 0.5, u0=np.array([[ratio + 0.1]]),
+                   u1=np.array([0.5]))
+    assert near["margin"][0] < 1e-6 and far["margin"][0] > 1e-3
