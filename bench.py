@@ -1,0 +1,378 @@
+"""Benchmark of batched speculative-decoding verification on GB300.
+
+One step = one spec_verify_run call (the whole hot path: row statistics,
+gate/accept decisions, residual or bonus sampling) over one batch of the
+synthetic workload, inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the fp64 CPU oracle on the host cores (the baseline
+arm); under torchrun only rank 0 runs it.  Multi-GPU runs shard sequences
+across ranks (weak scaling, Philox keys stay global via seq_offset).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "verified draft positions/sec and logits GB/s (fraction of GB300 HBM peak)"
+DEFAULT_WORKLOAD = "b64_v128256_zipf_gated"
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 126 * 1024 * 1024
+PROFILE = os.path.join(ROOT, "profiles", "verify_kernel_b64_v128256_zipf_gated.md")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--seed", type=int, default=1234)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of load (timed region plus untimed steps) seen by the clock sampler")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_online_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(pkg, "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith(("kernel_hash", "traffic_bytes_per_launch")):
+            key, val = line.split(":", 1)
+            vals[key.strip(" -*`")] = val.strip(" `\n")
+    if vals.get("kernel_hash") != kernel_hash():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), hw=f[5], hwt=f[6], swt=f[7],
+                                 pcap=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def cpu_oracle_rate(w, seconds: float, nthreads: int):
+    """Time the fp64 oracle on the workload's sequences for about `seconds`."""
+    from oracle import oracle as O
+    Lt = workloads.to_numpy_logits(w.Lt)
+    Ld = workloads.to_numpy_logits(w.Ld)
+    D = w.D.cpu().numpy()
+    gate = w.gate.cpu().numpy()
+    tau = w.tau.cpu().numpy().astype(np.float64)
+    O.verify(Lt[:1], Ld[:1], D[:1], w.T, gate[:1], tau[:1], seed=w.philox_seed)  # build + warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=nthreads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return reps * w.B * w.k / el, reps, el
+
+
+def run_reference(args, ws, rank):
+    """The baseline arm: the fp64 CPU oracle on host cores."""
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    cfg = workloads.CONFIGS[args.workload]
+    sample_B = max(1, min(cfg["B"], 8))
+    w = workloads.make(args.workload, seed=args.seed, device="cpu", B=sample_B)
+    Lt = workloads.to_numpy_logits(w.Lt)
+    Ld = workloads.to_numpy_logits(w.Ld)
+    D = w.D.cpu().numpy()
+    gate = w.gate.cpu().numpy()
+    tau = w.tau.cpu().numpy().astype(np.float64)
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+    t_step = time.perf_counter() - t0
+    # a deliberately slow program: bound the whole run to a few minutes
+    budget = 150.0
+    steps = args.steps
+    warm = args.warmup
+    if (steps + warm) * t_step > budget:
+        warm = min(warm, 3)
+        steps = max(1, int(budget / t_step) - warm)
+    for _ in range(warm):
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+    el = time.perf_counter() - t0
+    value = steps * sample_B * w.k / el
+    sample = (f"{sample_B} of {cfg['B']} sequences of {args.workload} per step; "
+              f"{steps} of {args.steps} requested steps timed")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "B_sample": sample_B, "k": w.k, "V": w.V,
+                   "logits_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo" if args.impl == "reference" else "nccl")
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import speculative_decoding_verification_online_gb300 as sv
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workloads.CONFIGS[args.workload]
+    B = cfg["B"]
+    # inputs larger than L2 for the big configs; rotate copies so each step reads
+    # logits that the previous steps have evicted
+    per_set = None
+    sets = []
+    nsets = 1
+    for i in range(8):
+        w = workloads.make(args.workload, seed=args.seed + 1000 * rank + 7 * i, device=dev)
+        sets.append(w)
+        per_set = w.logits_bytes()
+        nsets = len(sets)
+        if nsets * per_set >= 3 * L2_BYTES and nsets >= 2:
+            break
+    w0 = sets[0]
+    k, V = w0.k, w0.V
+    ver = sv.SpecVerifier(B, k, V, device=local)
+    outs = [ver.outputs(B) for _ in range(nsets)]
+    seq_offset = rank * B
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        w = sets[i % nsets]
+        ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]),
+                gate_per_seq=w.gate, threshold_per_seq=w.tau, seed=w.philox_seed,
+                seq_offset=seq_offset, out=outs[i % nsets])
+
+    sampler = ClockSampler(local)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if ws > 1:
+        dist.barrier()
+    # keep the GPU busy (untimed) until the sampler has seen ~1 s under load
+    t_extra = time.perf_counter()
+    while t_wall + (time.perf_counter() - t_extra) < args.clock_window:
+        for i in range(1000):
+            step(i)
+        torch.cuda.synchronize(dev)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    el = torch.tensor([ms], dtype=torch.float64)
+    if ws > 1:
+        el_t = el.to(dev)
+        dist.all_reduce(el_t, op=dist.ReduceOp.MAX)
+        el = el_t.cpu()
+    ms_total = float(el[0])
+    sec = ms_total / 1e3
+    positions = ws * args.steps * B * k
+    value = positions / sec
+    logits_bytes = per_set  # per step per rank
+    launch_s = sec / args.steps  # one kernel per step
+    achieved_gbs = logits_bytes / launch_s / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # e2e through the host-buffer entry point: pinned inputs, H2D + verify + D2H per step
+    e2e = None
+    if rank == 0 or ws > 1:
+        wh = sets[0]
+        Lt_h = wh.Lt.cpu().pin_memory()
+        Ld_h = wh.Ld.cpu().pin_memory()
+        D_h = wh.D.cpu().pin_memory()
+        g_h = wh.gate.cpu().pin_memory()
+        tau_h = wh.tau.cpu().pin_memory()
+        out_h = dict(accepted_len=torch.empty(B, dtype=torch.int32).pin_memory(),
+                     tokens=torch.empty(B, k + 1, dtype=torch.int32).pin_memory(),
+                     accept_prob=torch.empty(B, k, dtype=torch.float32).pin_memory(),
+                     flags=torch.empty(B, k, dtype=torch.int8).pin_memory())
+
+        def hstep():
+            ver.run_host(Lt_h, Ld_h, D_h, wh.T, gate_mode=sv.SV_GATED_MU,
+                         threshold=float(cfg["tau"]), gate_per_seq=g_h, threshold_per_seq=tau_h,
+                         seed=wh.philox_seed, out=out_h)
+        for _ in range(3):
+            hstep()
+        n_e2e = max(1, args.e2e_steps)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            hstep()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        h2d = (Lt_h.numel() * Lt_h.element_size() + Ld_h.numel() * Ld_h.element_size() +
+               D_h.numel() * 4 + g_h.numel() + tau_h.numel() * 4)
+        d2h = sum(t.numel() * t.element_size() for t in out_h.values())
+        e2e = {"value": ws * B * k / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0:
+        cores = os.cpu_count() or 1
+        small = workloads.make(args.workload, seed=args.seed, device="cpu",
+                               B=min(B, 16 if V > 100000 else B))
+        rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores)
+        cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
+               "sample": f"{small.B} sequences of {args.workload} x {reps} repetitions "
+                         f"({cel:.1f} s)"}
+
+    if rank == 0:
+        clocks = sampler.summary()
+        traffic = profile_traffic()
+        line = {
+            "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
+                       "logits_dtype": w0.dtype, "T": w0.T, "gate": cfg["gate"],
+                       "threshold": cfg["tau"],
+                       "l2": f"inputs larger than L2: {nsets} rotated copies of "
+                             f"{per_set / 1e6:.1f} MB logits",
+                       "parallelism": f"replicas x{ws} (sequence shards)"},
+            "logits_gbs": achieved_gbs,
+            "logits_frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": achieved_gbs / peak, "peak_kind": peak_kind,
+                         "traffic": traffic, "kernel": "verify_kernel",
+                         "algorithmic_bytes_per_launch": logits_bytes},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * sv.spec_verify_launches_per_run(),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    ver.close()
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-decoding
+ * verifier: modified rejection sampling in plain and mu/NULL-gated modes.
+ *
+ * What one call computes, for every sequence b of a batch of B sequences with
+ * k draft positions over a vocabulary of V tokens:
+ *
+ *   p_j = softmax(Lt[b,j,:] / T), j = 0..k      (target rows, temperature T)
+ *   q_j = softmax(Ld[b,j,:] / T), j = 0..k-1    (draft rows)
+ *     -- the effective distributions are full-vocabulary temperature softmaxes
+ *        evaluated in fp32 (mlxcel PR #992, "What changed").
+ *   mu_j = q_j in plain mode; in gated mode mu_j(x) = q_j(x) on admitted tokens
+ *     (q_j(x) >= threshold, equality passes) and 0 elsewhere, NOT renormalised
+ *     (Strata PR #3416 "Preserve target probabilities in gated MTP", section
+ *     "Approach"; equality rule: regolith audit, "schedule behavior").
+ *   For j = 0, 1, ...: gated and q_j(D_j) < threshold -> explicit NULL row,
+ *     stop; otherwise accept D_j iff p_j(D_j) > 0 and u0 * mu_j(D_j) <= p_j(D_j)
+ *     (mlxcel PR #992, "What changed": the accept test and its load-bearing
+ *     p > 0 conjunct); stop at the first position not accepted (mlxcel PR
+ *     #992, "Two metric corrections").
+ *   At the stop position j* < k (rejection or NULL) emit a sample of the
+ *     normalised positive part of p_j* - mu_j*; when all k drafts pass emit an
+ *     ordinary bonus sample of p_k (Strata PR #3416, "Approach").  Samples are
+ *     inverse-CDF picks in token order: the smallest v whose inclusive prefix
+ *     sum exceeds u1 * Z.  A residual with no mass falls back to sampling p.
+ *   Uniforms: u = Philox4x32-10 (Salmon et al., SC'11) with key = (seed lo32,
+ *     seed hi32) and counter = (s lo32, j, draw, s hi32), s = seq_offset + b;
+ *     u = (out.x >> 8) * 2^-24.  u0 uses draw 0 at position j, u1 draw 1 at j*.
+ *
+ * Outputs per sequence: accepted_len = j*, tokens = D_0..D_{j*-1}, the
+ * residual/bonus token, then -1 padding; accept_prob[j] = min(1, p/mu) for
+ * every position (0 for a NULL row, also filled past j*); optional flags and
+ * batch counters.
+ *
+ * Memory: every logits, token and output pointer is DEVICE memory owned by the
+ * caller (except the *_host entry point); rows are contiguous, row-major, V
+ * innermost.  The handle owns only its workspace.  Calls are asynchronous on
+ * the given stream; one handle must not run two calls at once.
+ *
+ * Errors: arguments the host can check are validated before any launch and
+ * yield a non-zero sv_status with nothing launched.  Problems only the device
+ * sees -- a draft token outside [0, V), a row with a NaN or +inf logit or with
+ * every logit -inf, a per-sequence threshold outside (0, 1] -- never trap: that
+ * sequence gets accepted_len = -1, tokens = -1, flags = SV_FLAG_INVALID,
+ * accept_prob = 0, and counters[SV_CNT_INVALID] is incremented.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spec_verify_s* spec_verify_t; /* opaque handle */
+
+typedef enum {
+  SV_OK = 0,
+  SV_EINVAL = 1,        /* bad argument (shape, pointer, temperature, threshold, dtype) */
+  SV_ENOMEM = 2,        /* device or host allocation failed */
+  SV_ECUDA = 3,         /* a CUDA runtime call or a launch failed */
+  SV_EUNSUPPORTED = 4   /* a size outside the library's limits (see SV_MAX_K, SV_MAX_V) */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum { SV_PLAIN = 0, SV_GATED_MU = 1 } sv_gate;
+
+/* per-position flags written to `flags` */
+enum {
+  SV_FLAG_UNREACHED = 0, /* past the stop position */
+  SV_FLAG_ACCEPT = 1,
+  SV_FLAG_REJECT = 2,
+  SV_FLAG_NULL = 3,      /* gated mode: the offered token failed the gate */
+  SV_FLAG_INVALID = 4    /* the sequence was rejected as invalid input */
+};
+
+/* slots of the optional `counters` output (uint64, accumulated: the caller zeroes them) */
+enum {
+  SV_CNT_TESTED = 0,     /* positions tested: accepted ones plus each stop position < k */
+  SV_CNT_ACCEPTED = 1,   /* accepted draft tokens */
+  SV_CNT_NULL = 2,       /* NULL rows */
+  SV_CNT_REJECTED = 3,   /* rejections */
+  SV_CNT_BONUS = 4,      /* sequences that accepted all k drafts */
+  SV_CNT_BOUNDARY = 5,   /* draws whose uniform (or gated q(D)) lay within 1e-6 of its boundary */
+  SV_CNT_INVALID = 6,    /* sequences rejected as invalid input */
+  SV_CNT_DEGENERATE = 7, /* residuals with no mass that fell back to sampling p */
+  SV_NUM_COUNTERS = 8
+};
+
+#define SV_MAX_K 32            /* draft positions per sequence */
+#define SV_MAX_V (1 << 22)     /* vocabulary size */
+
+/* Create a verifier for batches of up to max_B sequences, k draft positions and
+ * vocabulary V on CUDA device `device`.  Allocates the device workspace
+ * (about max_B * (2k+1) * ceil(V / 8192) * 8 bytes plus candidate lists).
+ * Returns SV_EINVAL for max_B < 1, k < 1 or V < 1, SV_EUNSUPPORTED beyond
+ * SV_MAX_K / SV_MAX_V, SV_ENOMEM or SV_ECUDA on CUDA failures; *out is set to
+ * NULL on any error. */
+sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int device);
+
+/* Verify a batch (the spec call).
+ *   target_logits [B, k+1, V] of dtype tdt, draft_logits [B, k, V] of dtype ddt,
+ *   draft_tokens [B, k] int32 -- device, read-only.
+ *   temperature: finite, > 0.
+ *   gate_mode / threshold: the default mode and threshold of every sequence;
+ *     threshold must lie in (0, 1] when gate_mode is SV_GATED_MU.
+ *   gate_mode_per_seq [B] uint8 (0 plain, 1 gated) and threshold_per_seq [B]
+ *     float: optional device arrays overriding the defaults (NULL = use them).
+ *   seed / Philox key; uniforms are keyed on the sequence index b.
+ *   accepted_len [B] int32, tokens [B, k+1] int32, accept_prob [B, k] float:
+ *     required device outputs.  flags [B, k] int8 and counters [8] uint64
+ *     (accumulated, see SV_CNT_*): optional device outputs (NULL = skip).
+ *   cuda_stream: a cudaStream_t (NULL = legacy default stream).
+ * B = 0 is a no-op.  Asynchronous: returns once the work is enqueued. */
+sv_status spec_verify_run(spec_verify_t h,
+                          const void* target_logits, sv_dtype tdt,
+                          const void* draft_logits, sv_dtype ddt,
+                          const int32_t* draft_tokens,
+                          int B, float temperature,
+                          sv_gate gate_mode, float threshold,
+                          const uint8_t* gate_mode_per_seq,
+                          const float* threshold_per_seq,
+                          uint64_t seed,
+                          int32_t* accepted_len, int32_t* tokens, float* accept_prob,
+                          int8_t* flags, uint64_t* counters,
+                          void* cuda_stream);
+
+/* spec_verify_run with three extras:
+ *   seq_offset: the Philox counter uses s = seq_offset + b, so a batch split
+ *     across calls (or GPUs) draws the same uniforms as the whole batch.
+ *   u_accept [B, k] / u_residual [B]: optional device arrays of explicit
+ *     uniforms in [0, 1) that replace the Philox draws u0 and u1 (a test hook
+ *     for probing decisions away from their boundaries); NULL = Philox.
+ *   row_stats [B, 2k+1, 2] float: optional device output, (max, log-sum-exp)
+ *     of L/T for target rows 0..k then draft rows 0..k-1 of each sequence. */
+sv_status spec_verify_run_ex(spec_verify_t h,
+                             const void* target_logits, sv_dtype tdt,
+                             const void* draft_logits, sv_dtype ddt,
+                             const int32_t* draft_tokens,
+                             int B, float temperature,
+                             sv_gate gate_mode, float threshold,
+                             const uint8_t* gate_mode_per_seq,
+                             const float* threshold_per_seq,
+                             uint64_t seed, uint64_t seq_offset,
+                             const float* u_accept, const float* u_residual,
+                             int32_t* accepted_len, int32_t* tokens, float* accept_prob,
+                             int8_t* flags, uint64_t* counters, float* row_stats,
+                             void* cuda_stream);
+
+/* spec_verify_run with HOST buffers for every input and output (same shapes;
+ * gate_mode_per_seq / threshold_per_seq / flags / counters optional, host).
+ * Copies the inputs to device staging buffers, verifies, copies the outputs
+ * back and synchronises the stream before returning; counters are overwritten,
+ * not accumulated.  The staging buffers (sized for max_B) are allocated on the
+ * first call and kept by the handle.  Pinned host memory makes the copies
+ * asynchronous DMA; pageable memory works but is slower. */
+sv_status spec_verify_run_host(spec_verify_t h,
+                               const void* target_logits, sv_dtype tdt,
+                               const void* draft_logits, sv_dtype ddt,
+                               const int32_t* draft_tokens,
+                               int B, float temperature,
+                               sv_gate gate_mode, float threshold,
+                               const uint8_t* gate_mode_per_seq,
+                               const float* threshold_per_seq,
+                               uint64_t seed,
+                               int32_t* accepted_len, int32_t* tokens, float* accept_prob,
+                               int8_t* flags, uint64_t* counters,
+                               void* cuda_stream);
+
+/* Release the handle and its device memory (NULL is a no-op).  Synchronises
+ * the handle's device first. */
+sv_status spec_verify_free(spec_verify_t h);
+
+/* Static, never-NULL description of a status code. */
+const char* spec_verify_status_string(sv_status s);
+
+/* Number of kernel launches one spec_verify_run call makes (for launch
+ * accounting in benchmarks). */
+int spec_verify_launches_per_run(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,298 @@
+// Host side of the C ABI declared in include/spec_verify.h: handle and
+// workspace management, argument validation and the single fused launch.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "spec_verify.h"
+#include "verify_kernel.cuh"
+
+struct spec_verify_s {
+  int device = 0;
+  int max_B = 0, k = 0, V = 0, nchunk = 0;
+  int num_sms = 0;
+  int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [target is bf16][draft is bf16]
+  void* ws = nullptr;                          // one device allocation for the workspace
+  float2* part = nullptr;
+  float* cand_v = nullptr;
+  int* cand_i = nullptr;
+  int* cand_n = nullptr;
+  unsigned* seq_done = nullptr;
+  // staging for spec_verify_run_host (allocated on first use)
+  void* stage = nullptr;
+  size_t stage_bytes = 0;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
+
+bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
+
+template <typename TT, typename TD>
+sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
+  long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
+  if (grid > P.total_items) grid = P.total_items;
+  if (grid < 1) grid = 1;
+  sv::verify_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, 0, st>>>(P);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_verify_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_EINVAL: return "invalid argument";
+    case SV_ENOMEM: return "out of memory";
+    case SV_ECUDA: return "CUDA error";
+    case SV_EUNSUPPORTED: return "unsupported size";
+  }
+  return "unknown status";
+}
+
+int spec_verify_launches_per_run(void) { return 1; }
+
+sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int device) {
+  if (!out) return SV_EINVAL;
+  *out = nullptr;
+  if (max_B < 1 || k < 1 || V < 1) return SV_EINVAL;
+  if (k > SV_MAX_K || V > SV_MAX_V) return SV_EUNSUPPORTED;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return SV_ECUDA;
+  DeviceGuard g(device);
+  if (!g.ok) return SV_ECUDA;
+
+  spec_verify_s* h = new (std::nothrow) spec_verify_s();
+  if (!h) return SV_ENOMEM;
+  h->device = device;
+  h->max_B = max_B;
+  h->k = k;
+  h->V = V;
+  h->nchunk = (V + sv::kChunk - 1) / sv::kChunk;
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete h;
+    return SV_ECUDA;
+  }
+  cudaError_t e = cudaSuccess;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[0][0], sv::verify_kernel<float, float>, sv::kThreads, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[0][1], sv::verify_kernel<float, uint16_t>, sv::kThreads, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[1][0], sv::verify_kernel<uint16_t, float>, sv::kThreads, 0);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[1][1], sv::verify_kernel<uint16_t, uint16_t>, sv::kThreads, 0);
+  if (e != cudaSuccess) {
+    delete h;
+    return SV_ECUDA;
+  }
+
+  const size_t rows = 2 * static_cast<size_t>(k) + 1;
+  const size_t n_part = static_cast<size_t>(max_B) * rows * h->nchunk;
+  const size_t n_cand = static_cast<size_t>(max_B) * k * h->nchunk;
+  size_t off = 0;
+  const size_t o_part = off; off = align_up(off + n_part * sizeof(float2), 256);
+  const size_t o_cv = off;   off = align_up(off + n_cand * sv::kTopM * sizeof(float), 256);
+  const size_t o_ci = off;   off = align_up(off + n_cand * sv::kTopM * sizeof(int), 256);
+  const size_t o_cn = off;   off = align_up(off + n_cand * sizeof(int), 256);
+  const size_t o_sd = off;   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  if (cudaMalloc(&h->ws, off) != cudaSuccess) {
+    delete h;
+    return SV_ENOMEM;
+  }
+  char* base = static_cast<char*>(h->ws);
+  h->part = reinterpret_cast<float2*>(base + o_part);
+  h->cand_v = reinterpret_cast<float*>(base + o_cv);
+  h->cand_i = reinterpret_cast<int*>(base + o_ci);
+  h->cand_n = reinterpret_cast<int*>(base + o_cn);
+  h->seq_done = reinterpret_cast<unsigned*>(base + o_sd);
+  if (cudaMemset(h->ws, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return SV_ECUDA;
+  }
+  *out = h;
+  return SV_OK;
+}
+
+sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                             const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens,
+                             int B, float temperature, sv_gate gate_mode, float threshold,
+                             const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                             uint64_t seed, uint64_t seq_offset, const float* u_accept,
+                             const float* u_residual, int32_t* accepted_len, int32_t* tokens,
+                             float* accept_prob, int8_t* flags, uint64_t* counters,
+                             float* row_stats, void* cuda_stream) {
+  if (!h) return SV_EINVAL;
+  if (B < 0 || B > h->max_B) return SV_EINVAL;
+  if (!valid_dtype(tdt) || !valid_dtype(ddt)) return SV_EINVAL;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_EINVAL;
+  if (gate_mode != SV_PLAIN && gate_mode != SV_GATED_MU) return SV_EINVAL;
+  const bool default_tau_used = (gate_mode == SV_GATED_MU || gate_mode_per_seq) && !threshold_per_seq;
+  if (default_tau_used && !(threshold > 0.f && threshold <= 1.f)) return SV_EINVAL;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !accepted_len || !tokens || !accept_prob)
+    return SV_EINVAL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return SV_ECUDA;
+
+  const int k = h->k, V = h->V;
+  sv::Params P{};
+  P.Lt = target_logits;
+  P.Ld = draft_logits;
+  P.D = draft_tokens;
+  P.B = B;
+  P.k = k;
+  P.V = V;
+  P.nchunk = h->nchunk;
+  P.rows = 2 * k + 1;
+  P.items_per_seq = P.rows * h->nchunk;
+  P.total_items = static_cast<long long>(B) * P.items_per_seq;
+  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.T = temperature;
+  P.gate_default = gate_mode == SV_GATED_MU ? 1 : 0;
+  P.tau_default = threshold;
+  P.gate_per_seq = gate_mode_per_seq;
+  P.tau_per_seq = threshold_per_seq;
+  P.seed = seed;
+  P.seq_offset = seq_offset;
+  P.u0 = u_accept;
+  P.u1 = u_residual;
+  P.accepted_len = accepted_len;
+  P.tokens = tokens;
+  P.alpha = accept_prob;
+  P.flags = flags;
+  P.counters = reinterpret_cast<unsigned long long*>(counters);
+  P.row_stats = row_stats;
+  P.part = h->part;
+  P.cand_v = h->cand_v;
+  P.cand_i = h->cand_i;
+  P.cand_n = h->cand_n;
+  P.seq_done = h->seq_done;
+  const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
+  const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
+  P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);
+  P.vec_d = (row_d % 16 == 0) && (reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
+
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
+  const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
+  if (tb && db) return launch<uint16_t, uint16_t>(h, P, bps, st);
+  if (tb && !db) return launch<uint16_t, float>(h, P, bps, st);
+  if (!tb && db) return launch<float, uint16_t>(h, P, bps, st);
+  return launch<float, float>(h, P, bps, st);
+}
+
+sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                          const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens,
+                          int B, float temperature, sv_gate gate_mode, float threshold,
+                          const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                          uint64_t seed, int32_t* accepted_len, int32_t* tokens,
+                          float* accept_prob, int8_t* flags, uint64_t* counters,
+                          void* cuda_stream) {
+  return spec_verify_run_ex(h, target_logits, tdt, draft_logits, ddt, draft_tokens, B, temperature,
+                            gate_mode, threshold, gate_mode_per_seq, threshold_per_seq, seed, 0,
+                            nullptr, nullptr, accepted_len, tokens, accept_prob, flags, counters,
+                            nullptr, cuda_stream);
+}
+
+sv_status spec_verify_run_host(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                               const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens,
+                               int B, float temperature, sv_gate gate_mode, float threshold,
+                               const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                               uint64_t seed, int32_t* accepted_len, int32_t* tokens,
+                               float* accept_prob, int8_t* flags, uint64_t* counters,
+                               void* cuda_stream) {
+  if (!h) return SV_EINVAL;
+  if (B < 0 || B > h->max_B || !valid_dtype(tdt) || !valid_dtype(ddt)) return SV_EINVAL;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !draft_tokens || !accepted_len || !tokens || !accept_prob)
+    return SV_EINVAL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return SV_ECUDA;
+  const size_t k = h->k, V = h->V, mB = h->max_B;
+  // staging layout sized for max_B and fp32 logits (the larger element type)
+  size_t off = 0;
+  const size_t o_t = off; off = align_up(off + mB * (k + 1) * V * 4, 256);
+  const size_t o_d = off; off = align_up(off + mB * k * V * 4, 256);
+  const size_t o_D = off; off = align_up(off + mB * k * 4, 256);
+  const size_t o_g = off; off = align_up(off + mB, 256);
+  const size_t o_tau = off; off = align_up(off + mB * 4, 256);
+  const size_t o_al = off; off = align_up(off + mB * 4, 256);
+  const size_t o_tok = off; off = align_up(off + mB * (k + 1) * 4, 256);
+  const size_t o_ap = off; off = align_up(off + mB * k * 4, 256);
+  const size_t o_fl = off; off = align_up(off + mB * k, 256);
+  const size_t o_cnt = off; off = align_up(off + SV_NUM_COUNTERS * 8, 256);
+  if (!h->stage) {
+    if (cudaMalloc(&h->stage, off) != cudaSuccess) {
+      h->stage = nullptr;
+      return SV_ENOMEM;
+    }
+    h->stage_bytes = off;
+  }
+  char* s = static_cast<char*>(h->stage);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const size_t bt = static_cast<size_t>(B) * (k + 1) * V * elem_size(tdt);
+  const size_t bd = static_cast<size_t>(B) * k * V * elem_size(ddt);
+  bool ok = true;
+  ok = ok && cudaMemcpyAsync(s + o_t, target_logits, bt, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(s + o_d, draft_logits, bd, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(s + o_D, draft_tokens, static_cast<size_t>(B) * k * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (gate_mode_per_seq)
+    ok = ok && cudaMemcpyAsync(s + o_g, gate_mode_per_seq, static_cast<size_t>(B), cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (threshold_per_seq)
+    ok = ok && cudaMemcpyAsync(s + o_tau, threshold_per_seq, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (counters) ok = ok && cudaMemsetAsync(s + o_cnt, 0, SV_NUM_COUNTERS * 8, st) == cudaSuccess;
+  if (!ok) return SV_ECUDA;
+  sv_status rc = spec_verify_run_ex(
+      h, s + o_t, tdt, s + o_d, ddt, reinterpret_cast<const int32_t*>(s + o_D), B, temperature,
+      gate_mode, threshold, gate_mode_per_seq ? reinterpret_cast<const uint8_t*>(s + o_g) : nullptr,
+      threshold_per_seq ? reinterpret_cast<const float*>(s + o_tau) : nullptr, seed, 0, nullptr,
+      nullptr, reinterpret_cast<int32_t*>(s + o_al), reinterpret_cast<int32_t*>(s + o_tok),
+      reinterpret_cast<float*>(s + o_ap), flags ? reinterpret_cast<int8_t*>(s + o_fl) : nullptr,
+      counters ? reinterpret_cast<uint64_t*>(s + o_cnt) : nullptr, nullptr, cuda_stream);
+  if (rc != SV_OK) return rc;
+  ok = ok && cudaMemcpyAsync(accepted_len, s + o_al, static_cast<size_t>(B) * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(tokens, s + o_tok, static_cast<size_t>(B) * (k + 1) * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(accept_prob, s + o_ap, static_cast<size_t>(B) * k * 4, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  if (flags) ok = ok && cudaMemcpyAsync(flags, s + o_fl, static_cast<size_t>(B) * k, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  if (counters) ok = ok && cudaMemcpyAsync(counters, s + o_cnt, SV_NUM_COUNTERS * 8, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+  ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+  return ok ? SV_OK : SV_ECUDA;
+}
+
+sv_status spec_verify_free(spec_verify_t h) {
+  if (!h) return SV_OK;
+  sv_status rc = SV_OK;
+  {
+    DeviceGuard g(h->device);
+    if (!g.ok || cudaDeviceSynchronize() != cudaSuccess) rc = SV_ECUDA;
+    if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = SV_ECUDA;
+    if (h->stage && cudaFree(h->stage) != cudaSuccess) rc = SV_ECUDA;
+  }
+  delete h;
+  return rc;
+}
+
+}  // extern "C"

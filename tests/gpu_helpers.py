@@ -1,0 +1,79 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path and the oracle on
+the same seeded inputs and compare them the way the tolerances demand.
+
+Comparison rules:
+  * accepted lengths and emitted tokens are compared bit for bit on every
+    sequence whose oracle margin (the distance of any used uniform, or of a
+    gated q, to its decision boundary) is at least 1e-6; sequences below that
+    margin are boundary draws, counted and excluded;
+  * acceptance probabilities agree within 1e-5 relative (fp32 against fp64),
+    except on positions whose gated q(D) lies within 1e-6 of the threshold
+    (there the NULL decision itself is a boundary case);
+  * flags of reached positions are compared like the tokens.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads
+
+BOUNDARY = 1e-6
+ALPHA_RTOL = 1e-5
+ALPHA_ATOL = 1e-30
+
+
+def oracle_for(w: workloads.Workload, idx=None, nthreads=8, u0=None, u1=None):
+    """Oracle outputs for workload w (all sequences, or the listed ones)."""
+    gate = w.gate.cpu().numpy()
+    tau = w.tau.cpu().numpy().astype(np.float64)
+    if idx is None:
+        return O.verify(workloads.to_numpy_logits(w.Lt), workloads.to_numpy_logits(w.Ld),
+                        w.D.cpu().numpy(), w.T, gate, tau, seed=w.philox_seed,
+                        u0=u0, u1=u1, nthreads=nthreads)
+    parts = []
+    for b in idx:
+        parts.append(O.verify(workloads.to_numpy_logits(w.Lt[b:b + 1]),
+                              workloads.to_numpy_logits(w.Ld[b:b + 1]), w.D[b:b + 1].cpu().numpy(),
+                              w.T, gate[b:b + 1], tau[b:b + 1], seed=w.philox_seed,
+                              seq_offset=int(b), nthreads=1))
+    return {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
+
+
+def gated_q_of_drafts(w: workloads.Workload, ref, idx=None):
+    """q_j(D_j) in fp64 from the oracle's row statistics (for excluding gate-boundary alphas)."""
+    sel = slice(None) if idx is None else torch.as_tensor(idx)
+    Ld = w.Ld[sel].float().cpu().double()
+    D = w.D[sel].cpu().long()
+    k = w.k
+    x = torch.gather(Ld, 2, D.unsqueeze(-1)).squeeze(-1) / w.T
+    lse = torch.as_tensor(ref["row_stats"][:, k + 1:, 1])
+    return torch.exp(x - lse).numpy()
+
+
+def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
+    """Assert parity; returns (n_compared, n_boundary)."""
+    sel = slice(None) if idx is None else np.asarray(idx)
+    g_len = got["accepted_len"].cpu().numpy()[sel]
+    g_tok = got["tokens"].cpu().numpy()[sel]
+    g_alpha = got["accept_prob"].cpu().numpy()[sel].astype(np.float64)
+    g_flags = got["flags"].cpu().numpy()[sel] if "flags" in got else None
+    margin = ref["margin"]
+    ok = margin >= BOUNDARY
+    n_boundary = int((~ok).sum())
+    bad = np.nonzero(ok & ((g_len != ref["accepted_len"]) | np.any(g_tok != ref["tokens"], axis=1)))[0]
+    assert bad.size == 0, (
+        f"{what}: {bad.size} non-boundary mismatches, first b={bad[:5]}: "
+        f"gpu len {g_len[bad[:3]]} tok {g_tok[bad[:3]]} | oracle len {ref['accepted_len'][bad[:3]]} "
+        f"tok {ref['tokens'][bad[:3]]} margin {margin[bad[:3]]}")
+    if g_flags is not None:
+        assert np.array_equal(g_flags[ok], ref["flags"][ok]), what
+    gate = w.gate.cpu().numpy()[sel].astype(bool)
+    keep = np.ones_like(g_alpha, dtype=bool)
+    if gate.any():
+        qd = gated_q_of_drafts(w, ref, idx)
+        tau = w.tau.cpu().numpy()[sel][:, None]
+        keep &= ~(gate[:, None] & (np.abs(qd - tau) < BOUNDARY))
+    np.testing.assert_allclose(g_alpha[keep], ref["alpha"][keep], rtol=ALPHA_RTOL, atol=ALPHA_ATOL,
+                               err_msg=what)
+    return int(ok.sum()), n_boundary
