@@ -17,11 +17,15 @@ struct spec_verify_s {
   int num_sms = 0;
   int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [target is bf16][draft is bf16]
   void* ws = nullptr;                          // one device allocation for the workspace
+  size_t ws_bytes = 0;
   float2* part = nullptr;
+  float* xD = nullptr;
   float* cand_v = nullptr;
   int* cand_i = nullptr;
-  int* cand_n = nullptr;
+  unsigned* cand_n = nullptr;
   unsigned* seq_done = nullptr;
+  unsigned* work = nullptr;
+  unsigned* exit_count = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
   void* stage = nullptr;
   size_t stage_bytes = 0;
@@ -36,11 +40,26 @@ size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
 template <typename TT, typename TD>
+constexpr int dyn_smem() {
+  return sv::Stages<TT, TD>::kDepth * sv::Stages<TT, TD>::kBytes;
+}
+
+// opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
+template <typename TT, typename TD>
+cudaError_t configure(int* blocks_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(sv::verify_kernel<TT, TD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::verify_kernel<TT, TD>,
+                                                       sv::kThreads, dyn_smem<TT, TD>());
+}
+
+template <typename TT, typename TD>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   if (grid > P.total_items) grid = P.total_items;
   if (grid < 1) grid = 1;
-  sv::verify_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, 0, st>>>(P);
+  sv::verify_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, dyn_smem<TT, TD>(), st>>>(P);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -98,11 +117,10 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
     delete h;
     return SV_ECUDA;
   }
-  cudaError_t e = cudaSuccess;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[0][0], sv::verify_kernel<float, float>, sv::kThreads, 0);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[0][1], sv::verify_kernel<float, uint16_t>, sv::kThreads, 0);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[1][0], sv::verify_kernel<uint16_t, float>, sv::kThreads, 0);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&h->blocks_per_sm[1][1], sv::verify_kernel<uint16_t, uint16_t>, sv::kThreads, 0);
+  cudaError_t e = configure<float, float>(&h->blocks_per_sm[0][0]);
+  if (e == cudaSuccess) e = configure<float, uint16_t>(&h->blocks_per_sm[0][1]);
+  if (e == cudaSuccess) e = configure<uint16_t, float>(&h->blocks_per_sm[1][0]);
+  if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&h->blocks_per_sm[1][1]);
   if (e != cudaSuccess) {
     delete h;
     return SV_ECUDA;
@@ -110,23 +128,29 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
 
   const size_t rows = 2 * static_cast<size_t>(k) + 1;
   const size_t n_part = static_cast<size_t>(max_B) * rows * h->nchunk;
-  const size_t n_cand = static_cast<size_t>(max_B) * k * h->nchunk;
+  const size_t n_rowc = static_cast<size_t>(max_B) * k;
   size_t off = 0;
   const size_t o_part = off; off = align_up(off + n_part * sizeof(float2), 256);
-  const size_t o_cv = off;   off = align_up(off + n_cand * sv::kTopM * sizeof(float), 256);
-  const size_t o_ci = off;   off = align_up(off + n_cand * sv::kTopM * sizeof(int), 256);
-  const size_t o_cn = off;   off = align_up(off + n_cand * sizeof(int), 256);
+  const size_t o_xd = off;   off = align_up(off + static_cast<size_t>(max_B) * rows * sizeof(float), 256);
+  const size_t o_cv = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(float), 256);
+  const size_t o_ci = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(int), 256);
+  const size_t o_cn = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
   const size_t o_sd = off;   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  const size_t o_wk = off;   off = align_up(off + 2 * sizeof(unsigned), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
   }
+  h->ws_bytes = off;
   char* base = static_cast<char*>(h->ws);
   h->part = reinterpret_cast<float2*>(base + o_part);
+  h->xD = reinterpret_cast<float*>(base + o_xd);
   h->cand_v = reinterpret_cast<float*>(base + o_cv);
   h->cand_i = reinterpret_cast<int*>(base + o_ci);
-  h->cand_n = reinterpret_cast<int*>(base + o_cn);
+  h->cand_n = reinterpret_cast<unsigned*>(base + o_cn);
   h->seq_done = reinterpret_cast<unsigned*>(base + o_sd);
+  h->work = reinterpret_cast<unsigned*>(base + o_wk);
+  h->exit_count = h->work + 1;
   if (cudaMemset(h->ws, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -168,7 +192,9 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.nchunk = h->nchunk;
   P.rows = 2 * k + 1;
   P.items_per_seq = P.rows * h->nchunk;
-  P.total_items = static_cast<long long>(B) * P.items_per_seq;
+  const long long total = static_cast<long long>(B) * P.items_per_seq;
+  if (total >= (1ll << 31)) return SV_EUNSUPPORTED;
+  P.total_items = static_cast<unsigned>(total);
   P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.T = temperature;
   P.gate_default = gate_mode == SV_GATED_MU ? 1 : 0;
@@ -186,10 +212,13 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.counters = reinterpret_cast<unsigned long long*>(counters);
   P.row_stats = row_stats;
   P.part = h->part;
+  P.xD = h->xD;
   P.cand_v = h->cand_v;
   P.cand_i = h->cand_i;
   P.cand_n = h->cand_n;
   P.seq_done = h->seq_done;
+  P.work = h->work;
+  P.exit_count = h->exit_count;
   const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
   const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
   P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);

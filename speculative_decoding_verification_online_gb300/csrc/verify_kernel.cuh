@@ -3,18 +3,23 @@
 // One launch verifies a whole batch.  Work is a list of items (sequence b,
 // row r, chunk c) in sequence-major order, where rows 0..k are the target
 // rows and rows k+1..2k the draft rows of b, and a chunk is kChunk = 8192
-// consecutive vocabulary entries.  Persistent CTAs take items round-robin:
+// consecutive vocabulary entries.  Persistent CTAs pull items from a global
+// counter (so a CTA that is busy finishing a sequence simply takes fewer
+// items) and run a cp.async pipeline of S chunk stages in shared memory:
 //
-//   1. stream the chunk once (128-bit read-only loads, lane-contiguous per
-//      instruction), take the chunk max m and s = sum exp((L - m) / T) -- the
-//      one-read row statistics of the temperature softmax (mlxcel PR #992,
-//      "What changed": p and q are full-vocabulary temperature softmaxes in
-//      fp32); for draft rows of gated sequences also keep the (at most
-//      floor(1/threshold)) tokens whose in-chunk probability reaches the gate,
-//      a superset of the tokens the gate admits;
-//   2. publish (m, s) and bump the sequence's completion counter; the CTA that
-//      completes the last item of sequence b finishes b (no CTA ever waits for
-//      another, so nothing can hang):
+//   1. stream the chunk once (16-byte cp.async per thread, each warp copying
+//      512 contiguous bytes per instruction; every thread later reads back
+//      exactly the pieces it copied, so the pipeline needs no extra barrier),
+//      take the chunk max m and s = sum exp((L - m) / T) -- the one-read row
+//      statistics of the temperature softmax (mlxcel PR #992, "What changed":
+//      p and q are full-vocabulary temperature softmaxes in fp32); record the
+//      logit at the drafted token when it lies in the chunk; for draft rows
+//      of gated sequences keep the tokens whose in-chunk probability reaches
+//      the gate (at most floor(1/threshold) of them, a superset of the tokens
+//      the gate admits) in a per-row candidate list;
+//   2. publish (m, s) and bump the sequence's completion counter with an
+//      acq_rel atomic; the CTA that completes the last item of sequence b
+//      finishes b (no CTA ever waits for another, so nothing can hang):
 //   3. combine the chunk partials into row max / sum, evaluate every draft
 //      position -- gate, retained measure mu, alpha = min(1, p(D)/mu(D)),
 //      Philox u0, the accept test p > 0 && u0 * mu <= p (Strata PR #3416,
@@ -23,10 +28,10 @@
 //   4. sample the stop row: the normalised positive part of p - mu after a
 //      rejection or NULL, p itself for the bonus row.  Chunk sums of the
 //      residual come from the partials (minus the admitted tokens' min(p, q)
-//      in gated mode), an fp64 prefix over chunks finds the chunk holding
-//      u1 * Z, and one re-read of that chunk with a block-wide fp64 scan finds
-//      the token.  Plain-mode rejections need q everywhere, so they re-read
-//      the stop row pair once to form the chunk sums.
+//      in gated mode), a prefix over chunks finds the chunk holding u1 * Z,
+//      and one re-read of that chunk with a block-wide scan finds the token.
+//      Plain-mode rejections need q everywhere, so they re-read the stop row
+//      pair once to form the chunk sums.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -43,9 +48,11 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kEPT = 32;                    // elements per thread per chunk
 constexpr int kChunk = kThreads * kEPT;     // vocabulary entries per work item
-constexpr int kTopM = 4;                    // gate-candidate slots per draft chunk
+constexpr int kTopM = 4;                    // gate candidates per chunk / admitted tokens per row
+constexpr int kRowCap = 64;                 // gate candidates kept per draft row
 constexpr int kMaxChunks = (SV_MAX_V + kChunk - 1) / kChunk;
 constexpr int kMaxRows = 2 * SV_MAX_K + 1;
+constexpr int kRing = 8;                    // fetched item indices kept per CTA
 constexpr float kBoundary = 1e-6f;
 // Candidates are kept against a threshold lowered by this factor so that
 // rounding cannot drop an admitted token; the gated fast path needs
@@ -57,7 +64,7 @@ struct Params {
   const void* Ld;  // [B, k, V]
   const int32_t* D;
   int B, k, V, nchunk, rows, items_per_seq;
-  long long total_items;
+  unsigned total_items;
   float c;     // log2(e) / T, rounded once
   float T;
   int gate_default;
@@ -74,11 +81,14 @@ struct Params {
   unsigned long long* counters;
   float* row_stats;
   // workspace
-  float2* part;    // [B, rows, nchunk] (chunk max of raw logits, sum of exp2((L - m) c))
-  float* cand_v;   // [B, k, nchunk, kTopM] raw logits of gate candidates
-  int* cand_i;     // [B, k, nchunk, kTopM] their token ids
-  int* cand_n;     // [B, k, nchunk] candidate count (> kTopM: overflow)
-  unsigned* seq_done;  // [B] completion counters, reset by the finishing CTA
+  float2* part;        // [B, rows, nchunk] (chunk max of raw logits, sum of exp2((L - m) c))
+  float* xD;           // [B, rows] raw logit at the drafted token (rows j < k and draft rows)
+  float* cand_v;       // [B, k, kRowCap] raw logits of gate candidates
+  int* cand_i;         // [B, k, kRowCap] their token ids
+  unsigned* cand_n;    // [B, k] candidates appended (> kRowCap: overflow); reset by the finisher
+  unsigned* seq_done;  // [B] completion counters, reset by the finisher
+  unsigned* work;      // [1] next item to hand out, reset by the last CTA to exit
+  unsigned* exit_count;  // [1]
   int vec_t, vec_d;    // rows allow 16-byte vector loads
 };
 
@@ -87,12 +97,20 @@ struct Params {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ __forceinline__ float2 ldcg_f2(const float2* p) { return __ldcg(p); }
@@ -149,6 +167,14 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
 __device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -174,7 +200,7 @@ template <>
 __device__ __forceinline__ void load8<uint16_t>(const uint16_t* row, int v0, int V, bool vec,
                                                 float (&x)[8]) {
   if (vec && v0 + 8 <= V) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + v0));
+    const uint4 u = __ldcg(reinterpret_cast<const uint4*>(row + v0));
     x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x); x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
     x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z); x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
   } else {
@@ -186,8 +212,8 @@ template <>
 __device__ __forceinline__ void load8<float>(const float* row, int v0, int V, bool vec,
                                              float (&x)[8]) {
   if (vec && v0 + 8 <= V) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(row + v0));
-    const float4 b = __ldg(reinterpret_cast<const float4*>(row + v0) + 1);
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(row + v0));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(row + v0) + 1);
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
   } else {
@@ -208,23 +234,35 @@ __device__ __forceinline__ bool gate_fast_path(float tau) {
 
 // ------------------------------------------------------- chunk registers
 //
-// Thread t = 32 w + l holds NV 16-byte slots of the chunk: slot i is vector
-// index w * 32 NV + 32 i + l (so each load instruction of a warp reads 512
-// contiguous bytes).  bf16: 4 slots of 8 entries kept packed; f32: 8 slots of 4.
+// Thread t = 32 w + l owns NV 16-byte slots of the chunk: slot i is vector
+// index w * 32 NV + 32 i + l (each copy instruction of a warp moves 512
+// contiguous bytes).  bf16: 4 slots of 8 entries kept packed; f32: 8 slots of
+// 4.  A slot that lies wholly inside the row of an aligned tensor travels by
+// cp.async into the stage; other slots (ragged tail, unaligned rows) are read
+// directly, entries past V reading as -inf.
 
 template <typename T> struct Chunk;
 
 template <> struct Chunk<uint16_t> {
   static constexpr int kNV = 4, kVE = 8;
   uint32_t w[16];
-  __device__ __forceinline__ static int elem(int slot_vec, int e) { return slot_vec * kVE + e; }
-  __device__ __forceinline__ void load(const uint16_t* row, int c0, int V, bool vec, int warp, int lane) {
+  __device__ __forceinline__ static void issue(const uint16_t* row, unsigned char* stage, int c0, int V,
+                                               int warp, int lane) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int sv = warp * 32 * kNV + 32 * i + lane;
+      const int v0 = c0 + sv * kVE;
+      if (v0 + kVE <= V) cp_async16(stage + sv * 16, row + v0);
+    }
+  }
+  __device__ __forceinline__ void load(const uint16_t* row, const unsigned char* stage, int c0, int V,
+                                       bool vec, int warp, int lane) {
 #pragma unroll
     for (int i = 0; i < kNV; ++i) {
       const int sv = warp * 32 * kNV + 32 * i + lane;
       const int v0 = c0 + sv * kVE;
       if (vec && v0 + kVE <= V) {
-        const uint4 u = ldg_stream(row + v0);
+        const uint4 u = *reinterpret_cast<const uint4*>(stage + sv * 16);
         w[4 * i + 0] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
       } else {
 #pragma unroll
@@ -273,15 +311,24 @@ template <> struct Chunk<uint16_t> {
 template <> struct Chunk<float> {
   static constexpr int kNV = 8, kVE = 4;
   float x[32];
-  __device__ __forceinline__ void load(const float* row, int c0, int V, bool vec, int warp, int lane) {
+  __device__ __forceinline__ static void issue(const float* row, unsigned char* stage, int c0, int V,
+                                               int warp, int lane) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const int sv = warp * 32 * kNV + 32 * i + lane;
+      const int v0 = c0 + sv * kVE;
+      if (v0 + kVE <= V) cp_async16(stage + sv * 16, row + v0);
+    }
+  }
+  __device__ __forceinline__ void load(const float* row, const unsigned char* stage, int c0, int V,
+                                       bool vec, int warp, int lane) {
 #pragma unroll
     for (int i = 0; i < kNV; ++i) {
       const int sv = warp * 32 * kNV + 32 * i + lane;
       const int v0 = c0 + sv * kVE;
       if (vec && v0 + kVE <= V) {
-        const uint4 u = ldg_stream(row + v0);
-        x[4 * i + 0] = __uint_as_float(u.x); x[4 * i + 1] = __uint_as_float(u.y);
-        x[4 * i + 2] = __uint_as_float(u.z); x[4 * i + 3] = __uint_as_float(u.w);
+        const float4 u = *reinterpret_cast<const float4*>(stage + sv * 16);
+        x[4 * i + 0] = u.x; x[4 * i + 1] = u.y; x[4 * i + 2] = u.z; x[4 * i + 3] = u.w;
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e) x[4 * i + e] = v0 + e < V ? __ldg(row + v0 + e) : -INFINITY;
@@ -327,24 +374,31 @@ struct Shared {
   int ncand;
   float cand_v[kTopM];
   int cand_i[kTopM];
+  unsigned ring[kRing];
+  int fin_b;
   // finishing phase
   float rowM[kMaxRows];
   float rowInvS[kMaxRows];
   double rowS[kMaxRows];
+  float xD[kMaxRows];
+  int Dv[SV_MAX_K];
+  unsigned candn[SV_MAX_K];
   double tile[kMaxChunks];
-  double wtot[kWarps];
+  double wbase[kWarps];
+  float wtot[kWarps];
   int bad;
   int jstar;
   int stop_flag;
   int boundary;
-  int nadm;
-  int overflow;
-  int adm_i[kTopM];
-  float adm_q[kTopM];
+  unsigned overflow_rows;
   int tstar;
   double before;
   int pick;
   int last_pos;
+  int nadm[SV_MAX_K];
+  int adm_i[SV_MAX_K][kTopM];
+  float adm_q[SV_MAX_K][kTopM];
+  float adm_p[SV_MAX_K][kTopM];
 };
 
 __device__ __forceinline__ bool seq_gated(const Params& P, int b) {
@@ -357,9 +411,9 @@ __device__ __forceinline__ float seq_tau(const Params& P, int b) {
 // ------------------------------------------------------------ finishing
 
 // residual weight of token v with target logit xt (and draft logit xd in the
-// dense mode).  mode 0: p (bonus row, or degenerate residual); mode 1: p minus
-// min(p, q) on the admitted list; mode 2: max(0, p - mu) with mu from the draft
-// logit (mu = q, or q on q >= tau in gated mode).
+// dense mode).  mode 0: p (bonus row, or degenerate residual); mode 1: p, or
+// max(0, p - q) on the admitted list; mode 2: max(0, p - mu) with mu from the
+// draft logit (mu = q, or q on q >= tau in gated mode).
 struct ResidualEval {
   int mode;
   float Mt, invSt, Md, invSd, c, tau;
@@ -383,23 +437,46 @@ struct ResidualEval {
 
 template <typename TT, typename TD>
 __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
   const bool gated = seq_gated(P, b);
   const float tau = seq_tau(P, b);
+  const bool fastgate = gated && gate_fast_path(tau);
   const float c = P.c;
   const uint64_t s_idx = P.seq_offset + static_cast<uint64_t>(b);
+  const TT* Lt = static_cast<const TT*>(P.Lt);
+  const TD* Ld = static_cast<const TD*>(P.Ld);
 
+  // phase A: everything the decisions need, in one round of loads
   if (tid == 0) {
     sh.bad = (gated && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
-    sh.nadm = 0;
-    sh.overflow = 0;
     sh.boundary = 0;
     sh.pick = -1;
     sh.last_pos = -1;
+    sh.overflow_rows = 0u;
   }
-  __syncthreads();
-
+  if (tid < R) sh.xD[tid] = __ldcg(P.xD + static_cast<int64_t>(b) * R + tid);
+  if (tid < k) {
+    sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
+    sh.candn[tid] = fastgate ? __ldcg(P.cand_n + static_cast<int64_t>(b) * k + tid) : 0u;
+    sh.nadm[tid] = 0;
+  }
+  // candidate entries of every draft row, read before the counts are known
+  // (slots past kCandPerThread * kThreads, i.e. k > 8, are read in phase B)
+  constexpr int kCandPerThread = 2;
+  float cv[kCandPerThread];
+  int ci[kCandPerThread];
+  if (fastgate) {
+#pragma unroll
+    for (int u = 0; u < kCandPerThread; ++u) {
+      const int e = tid + u * kThreads;
+      if (e < k * kRowCap) {
+        cv[u] = __ldcg(P.cand_v + static_cast<int64_t>(b) * k * kRowCap + e);
+        ci[u] = __ldcg(P.cand_i + static_cast<int64_t>(b) * k * kRowCap + e);
+      }
+    }
+  }
   // F1: row max / sum from the chunk partials (fp64 accumulation)
   for (int r = warp; r < R; r += kWarps) {
     const float2* pr = P.part + (static_cast<int64_t>(b) * R + r) * nch;
@@ -419,31 +496,59 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       sh.rowInvS[r] = static_cast<float>(1.0 / S);
       if (M == -INFINITY || !isfinite(S) || !(S > 0.0)) sh.bad = 1;
       if (P.row_stats) {
-        const int out_row = r;  // target rows 0..k, then draft rows
         const float mo = M / P.T;
-        P.row_stats[(static_cast<int64_t>(b) * R + out_row) * 2 + 0] = mo;
-        P.row_stats[(static_cast<int64_t>(b) * R + out_row) * 2 + 1] =
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = mo;
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] =
             static_cast<float>(static_cast<double>(mo) + log(S));
       }
     }
   }
   __syncthreads();
 
+  // phase B: admitted tokens of every draft row and their target probability
+  // (one more round of loads, overlapping the decisions below)
+  if (fastgate && !sh.bad) {
+    auto admit = [&](int e, float x, int v) {
+      const int j = e / kRowCap, s = e - j * kRowCap;
+      const unsigned n = sh.candn[j];
+      if (n > static_cast<unsigned>(kRowCap)) {
+        if (s == 0) atomicOr(&sh.overflow_rows, 1u << j);
+        return;
+      }
+      if (s >= static_cast<int>(n)) return;
+      const int rd = k + 1 + j;
+      const float q = prob_of(x, sh.rowM[rd], c, sh.rowInvS[rd]);
+      if (q >= tau) {
+        const int a = atomicAdd(&sh.nadm[j], 1);
+        if (a < kTopM) {
+          const float xt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + j) * V, v);
+          sh.adm_i[j][a] = v;
+          sh.adm_q[j][a] = q;
+          sh.adm_p[j][a] = prob_of(xt, sh.rowM[j], c, sh.rowInvS[j]);
+        } else {
+          atomicOr(&sh.overflow_rows, 1u << j);
+        }
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < kCandPerThread; ++u)
+      if (tid + u * kThreads < k * kRowCap) admit(tid + u * kThreads, cv[u], ci[u]);
+    for (int e = tid + kCandPerThread * kThreads; e < k * kRowCap; e += kThreads)
+      admit(e, __ldcg(P.cand_v + static_cast<int64_t>(b) * k * kRowCap + e),
+            __ldcg(P.cand_i + static_cast<int64_t>(b) * k * kRowCap + e));
+  }
+
   // F2: every draft position (one lane each): gate, mu, alpha, accept test
   if (warp == 0) {
-    const TT* Lt = static_cast<const TT*>(P.Lt);
-    const TD* Ld = static_cast<const TD*>(P.Ld);
     bool ok = true, acc = false, is_null = false, near = false;
     float alpha = 0.f;
     if (lane < k) {
-      const int d = P.D[static_cast<int64_t>(b) * k + lane];
+      const int d = sh.Dv[lane];
       ok = d >= 0 && d < V;
       if (ok && !sh.bad) {
         const int rt = lane, rd = k + 1 + lane;
-        const float xt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + lane) * V, d);
-        const float xd = logit_at<TD>(Ld + (static_cast<int64_t>(b) * k + lane) * V, d);
-        const float p = prob_of(xt, sh.rowM[rt], c, sh.rowInvS[rt]);
-        const float q = prob_of(xd, sh.rowM[rd], c, sh.rowInvS[rd]);
+        const float p = prob_of(sh.xD[rt], sh.rowM[rt], c, sh.rowInvS[rt]);
+        const float q = prob_of(sh.xD[rd], sh.rowM[rd], c, sh.rowInvS[rd]);
         const bool admitted = !gated || q >= tau;
         const float mu = admitted ? q : 0.f;
         is_null = !admitted;
@@ -485,6 +590,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
 
   const int jstar = sh.jstar;
   int32_t* tok = P.tokens + static_cast<int64_t>(b) * (k + 1);
+  if (fastgate && tid < k) P.cand_n[static_cast<int64_t>(b) * k + tid] = 0u;  // ready for the next call
   if (sh.bad) {
     if (tid <= k) tok[tid] = -1;
     if (tid == 0) {
@@ -496,43 +602,16 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
 
   // F3: the stop row's residual (or bonus) weights, chunk by chunk
   const int rt = jstar, rd = k + 1 + jstar;
-  const TT* trow = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
-  const TD* drow = jstar < k ? static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + jstar) * V
-                             : nullptr;
+  const TT* trow = Lt + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
+  const TD* drow = jstar < k ? Ld + (static_cast<int64_t>(b) * k + jstar) * V : nullptr;
   int mode = 0;
-  if (jstar < k) mode = (gated && gate_fast_path(tau)) ? 1 : 2;
-
-  if (mode == 1) {
-    // admitted tokens of the stop row from the per-chunk gate candidates
-    const int64_t cbase = (static_cast<int64_t>(b) * k + jstar) * nch;
-    for (int ch = tid; ch < nch; ch += kThreads) {
-      const int n = __ldcg(P.cand_n + cbase + ch);
-      if (n > kTopM) {
-        sh.overflow = 1;
-        continue;
-      }
-      for (int sl = 0; sl < n; ++sl) {
-        const float x = __ldcg(P.cand_v + (cbase + ch) * kTopM + sl);
-        const int v = __ldcg(P.cand_i + (cbase + ch) * kTopM + sl);
-        const float q = prob_of(x, sh.rowM[rd], c, sh.rowInvS[rd]);
-        if (q >= tau) {
-          const int a = atomicAdd(&sh.nadm, 1);
-          if (a < kTopM) {
-            sh.adm_i[a] = v;
-            sh.adm_q[a] = q;
-          } else {
-            sh.overflow = 1;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    if (sh.overflow) mode = 2;
-  }
+  if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
+  const int nadm = mode == 1 ? min(sh.nadm[jstar], kTopM) : 0;
 
   const ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
                         jstar < k ? sh.rowM[rd] : 0.f, jstar < k ? sh.rowInvS[rd] : 0.f,
-                        c, tau, gated, sh.nadm < kTopM ? sh.nadm : kTopM, sh.adm_i, sh.adm_q};
+                        c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
+                        jstar < k ? sh.adm_q[jstar] : sh.adm_q[0]};
 
   auto chunk_sums_from_partials = [&](int use_mode) {
     const float2* pr = P.part + (static_cast<int64_t>(b) * R + rt) * nch;
@@ -543,12 +622,9 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
                      : static_cast<double>(ms.y) * static_cast<double>(exp2f((ms.x - ev.Mt) * c)) *
                            (1.0 / sh.rowS[rt]);
       if (use_mode == 1) {
-        for (int a = 0; a < ev.nadm; ++a)
-          if (ev.adm_i[a] / kChunk == ch) {
-            const float xt = logit_at<TT>(trow, ev.adm_i[a]);
-            const float p = prob_of(xt, ev.Mt, c, ev.invSt);
-            t -= static_cast<double>(fminf(p, ev.adm_q[a]));
-          }
+        for (int a = 0; a < nadm; ++a)
+          if (sh.adm_i[jstar][a] / kChunk == ch)
+            t -= static_cast<double>(fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]));
         if (t < 0.0) t = 0.0;
       }
       sh.tile[ch] = t;
@@ -560,15 +636,17 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
     for (int ch = warp; ch < nch; ch += kWarps) {
       float acc = 0.f;
       const int c0 = ch * kChunk;
-      for (int g = lane; g < kChunk / 8; g += 32) {
-        const int v0 = c0 + g * 8;
-        if (v0 >= V) break;
-        float xt[8], xd[8];
-        load8<TT>(trow, v0, V, P.vec_t != 0, xt);
-        load8<TD>(drow, v0, V, P.vec_d != 0, xd);
+#pragma unroll 4
+      for (int u = 0; u < kChunk / 8 / 32; ++u) {
+        const int v0 = c0 + (u * 32 + lane) * 8;
+        if (v0 < V) {
+          float xt[8], xd[8];
+          load8<TT>(trow, v0, V, P.vec_t != 0, xt);
+          load8<TD>(drow, v0, V, P.vec_d != 0, xd);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (v0 + e < V) acc += ev(v0 + e, xt[e], xd[e]);
+          for (int e = 0; e < 8; ++e)
+            if (v0 + e < V) acc += ev(v0 + e, xt[e], xd[e]);
+        }
       }
       const double t = warp_sum_d(static_cast<double>(acc));
       if (lane == 0) sh.tile[ch] = t;
@@ -579,7 +657,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
   __syncthreads();
 
   // total mass; a residual without mass falls back to p
-  double Z = 0.0;
+  double Z;
   {
     double z = 0.0;
     for (int ch = lane; ch < nch; ch += 32) z += sh.tile[ch];
@@ -640,7 +718,6 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
     const int e0 = c0 + tid * kEPT;
     const double yl = y - sh.before;
     float r[kEPT];
-    double tot = 0.0;
 #pragma unroll
     for (int g = 0; g < kEPT / 8; ++g) {
       float xt[8], xd[8];
@@ -650,40 +727,55 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       for (int e = 0; e < 8; ++e) {
         const int v = e0 + 8 * g + e;
         r[8 * g + e] = v < V ? ev2(v, xt[e], ev2.mode == 2 ? xd[e] : 0.f) : 0.f;
-        tot += static_cast<double>(r[8 * g + e]);
       }
     }
-    // block scan of the per-thread totals (fp64).  Thread i's range is
-    // [lo_i, hi_i) with lo_{i+1} == hi_i bit for bit, so exactly one thread
-    // claims any y below the chunk total.
-    const double wincl = warp_incl_scan_d(tot, lane);
-    double wexcl = __shfl_up_sync(0xffffffffu, wincl, 1);
-    if (lane == 0) wexcl = 0.0;
+    // per-thread total (pairwise), warp scan in fp32, block offsets in fp64.
+    // Thread i's range is [lo_i, hi_i) with lo_{i+1} == hi_i bit for bit, so
+    // exactly one thread claims any y below the chunk total.
+    float pw[kEPT / 2];
+#pragma unroll
+    for (int e = 0; e < kEPT / 2; ++e) pw[e] = r[2 * e] + r[2 * e + 1];
+#pragma unroll
+    for (int w = kEPT / 4; w >= 1; w >>= 1)
+#pragma unroll
+      for (int e = 0; e < w; ++e) pw[e] = pw[2 * e] + pw[2 * e + 1];
+    const float tot = pw[0];
+    const float wincl = warp_incl_scan(tot, lane);
+    float wexcl = __shfl_up_sync(0xffffffffu, wincl, 1);
+    if (lane == 0) wexcl = 0.f;
     if (lane == 31) sh.wtot[warp] = wincl;
     __syncthreads();
-    double wbase = 0.0;
-    for (int w = 0; w < warp; ++w) wbase += sh.wtot[w];
-    const double lo = wbase + wexcl, hi = wbase + wincl;
+    if (lane == 0) {
+      double base = 0.0;
+      for (int w = 0; w < warp; ++w) base += static_cast<double>(sh.wtot[w]);
+      sh.wbase[warp] = base;
+    }
+    __syncwarp();
+    const double wbase = sh.wbase[warp];
+    const double lo = wbase + static_cast<double>(wexcl), hi = wbase + static_cast<double>(wincl);
     int lastpos = -1;
+#pragma unroll
     for (int e = 0; e < kEPT; ++e)
       if (r[e] > 0.f) lastpos = e0 + e;
     if (lo <= yl && yl < hi) {
-      double run = lo;
+      const float target = static_cast<float>(yl - lo);
+      float run = 0.f, prev = 0.f;
       int pick = lastpos;  // rounding inside the thread: its last positive entry
-      double prev = lo;
+      bool hit = false;
       for (int e = 0; e < kEPT; ++e) {
         prev = run;
-        run += static_cast<double>(r[e]);
-        if (run > yl) {
+        run += r[e];
+        if (run > target) {
           pick = e0 + e;
+          hit = true;
           break;
         }
       }
-      if (run <= yl) prev = run = hi;
+      if (!hit) prev = run = static_cast<float>(hi - lo);
       sh.pick = pick;
-      const float cl = static_cast<float>((sh.before + prev) / Z);
-      const float ch2 = static_cast<float>((sh.before + run) / Z);
-      if (fabsf(u1 - cl) < kBoundary || fabsf(u1 - ch2) < kBoundary) sh.boundary += 1;
+      const double cl = (sh.before + lo + static_cast<double>(prev)) / Z;
+      const double chh = (sh.before + lo + static_cast<double>(run)) / Z;
+      if (fabs(u1 - cl) < kBoundary || fabs(u1 - chh) < kBoundary) sh.boundary += 1;
     }
     atomicMax(&sh.last_pos, lastpos);
   }
@@ -709,113 +801,206 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       if (degenerate) atomicAdd(P.counters + SV_CNT_DEGENERATE, 1ull);
     }
   }
-  if (tid < jstar) tok[tid] = P.D[static_cast<int64_t>(b) * k + tid];
+  if (tid < jstar) tok[tid] = sh.Dv[tid];
   if (tid > jstar && tid <= k) tok[tid] = -1;
 }
 
 // ----------------------------------------------------------- the kernel
 
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const Params P) {
+struct Stages {
+  static constexpr int kBytes = kChunk * static_cast<int>(sizeof(TT) > sizeof(TD) ? sizeof(TT) : sizeof(TD));
+  static constexpr int kDepth = kBytes <= 16384 ? 4 : 3;
+  static constexpr int kMinBlocks = kBytes <= 16384 ? 3 : 2;
+};
+
+template <typename TT, typename TD>
+__device__ __forceinline__ void issue_item(const Params& P, unsigned item, unsigned char* stage,
+                                           int warp, int lane) {
+  const int b = static_cast<int>(item / static_cast<unsigned>(P.items_per_seq));
+  const int rem = static_cast<int>(item - static_cast<unsigned>(b) * P.items_per_seq);
+  const int r = rem / P.nchunk;
+  const int c0 = (rem - r * P.nchunk) * kChunk;
+  if (r <= P.k) {
+    if (P.vec_t)
+      Chunk<TT>::issue(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V,
+                       stage, c0, P.V, warp, lane);
+  } else {
+    if (P.vec_d)
+      Chunk<TD>::issue(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V,
+                       stage, c0, P.V, warp, lane);
+  }
+}
+
+// one work item: chunk statistics, drafted-token logit, gate candidates, and
+// the publication of all of it.  On entry *ticket / ticket_b (thread 0) hold
+// the completion count the previous item observed and its sequence; *fin_out
+// returns, to every thread, the sequence that previous item completed (or -1),
+// and *ticket the count this item observes.
+template <typename T>
+__device__ __forceinline__ void process_item(const Params& P, Shared& sh, const T* row,
+                                             const unsigned char* stage, int b, int r, int ch,
+                                             bool is_draft, int tid, int warp, int lane,
+                                             unsigned* ticket, int ticket_b, int* fin_out) {
+  const int k = P.k;
+  const int c0 = ch * kChunk;
+  const bool vec = is_draft ? P.vec_d != 0 : P.vec_t != 0;
+  const int j = is_draft ? r - k - 1 : r;
+  int d = -1;
+  if (tid == 0 && j < k) d = __ldg(P.D + static_cast<int64_t>(b) * k + j);
+
+  Chunk<T> regs;
+  regs.load(row, stage, c0, P.V, vec, warp, lane);
+  const float mine = regs.max();
+  const float mw = warp_max(mine);
+  if (lane == 0) sh.red_max[warp] = mw;
+  __syncthreads();
+  float m_c = sh.red_max[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) m_c = fmaxf(m_c, sh.red_max[w]);
+  const float s_t = warp_sum(regs.expsum(m_c == -INFINITY ? 0.f : m_c, P.c));
+  if (lane == 0) sh.red_sum[warp] = s_t;
+  if (tid == 0)  // the previous item's completion count has had a whole item to return
+    sh.fin_b = (ticket_b >= 0 && *ticket == static_cast<unsigned>(P.items_per_seq - 1)) ? ticket_b : -1;
+  __syncthreads();
+  float s_c = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) s_c += sh.red_sum[w];
+  *fin_out = sh.fin_b;
+
+  bool want_cand = false;
+  if (is_draft) {
+    const float tau = seq_tau(P, b);
+    want_cand = seq_gated(P, b) && gate_fast_path(tau);
+    if (want_cand) {
+      // tokens with in-chunk probability >= slack * tau: a superset of the
+      // admitted set (q <= in-chunk probability), at most 1/(slack tau) of them
+      float thr = INFINITY;
+      if (s_c > 0.f && isfinite(s_c)) thr = m_c + log2f(tau * kGateSlack * s_c) / P.c;
+      if (mine >= thr) {
+        regs.for_each(c0, warp, lane, [&](int v, float x) {
+          if (x >= thr && v < P.V) {
+            const int slot = atomicAdd(&sh.ncand, 1);
+            if (slot < kTopM) {
+              sh.cand_v[slot] = x;
+              sh.cand_i[slot] = v;
+            }
+          }
+        });
+      }
+      __syncthreads();
+    }
+  }
+
+  if (tid == 0) {
+    const int R = P.rows;
+    P.part[(static_cast<int64_t>(b) * R + r) * P.nchunk + ch] = make_float2(m_c, s_c);
+    if (d >= c0 && d < c0 + kChunk && d < P.V) {
+      constexpr int kVE = Chunk<T>::kVE;
+      const int v0 = d - (d - c0) % kVE;
+      const float x = (vec && v0 + kVE <= P.V) ? (sizeof(T) == 2
+                          ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[d - c0]) << 16)
+                          : reinterpret_cast<const float*>(stage)[d - c0])
+                                              : logit_at<T>(row, d);
+      P.xD[static_cast<int64_t>(b) * R + r] = x;
+    }
+    if (want_cand) {
+      const int n = sh.ncand;
+      if (n > 0) {
+        const int64_t rowc = static_cast<int64_t>(b) * k + j;
+        const unsigned add = n > kTopM ? static_cast<unsigned>(kRowCap + 1) : static_cast<unsigned>(n);
+        const unsigned base = atomicAdd(P.cand_n + rowc, add);
+        if (n <= kTopM)
+          for (int s = 0; s < n; ++s)
+            if (base + s < static_cast<unsigned>(kRowCap)) {
+              P.cand_v[rowc * kRowCap + base + s] = sh.cand_v[s];
+              P.cand_i[rowc * kRowCap + base + s] = sh.cand_i[s];
+            }
+      }
+      sh.ncand = 0;
+    }
+    *ticket = atom_add_acq_rel(P.seq_done + b, 1u);
+  }
+}
+
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(kThreads, Stages<TT, TD>::kMinBlocks) verify_kernel(const Params P) {
+  constexpr int S = Stages<TT, TD>::kDepth;
+  constexpr int kStage = Stages<TT, TD>::kBytes;
+  extern __shared__ __align__(128) unsigned char stages[];
   __shared__ Shared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) sh.ncand = 0;
+  const unsigned total = P.total_items;
   const int k = P.k, nch = P.nchunk;
 
-  for (long long item = blockIdx.x; item < P.total_items; item += gridDim.x) {
-    const int b = static_cast<int>(item / P.items_per_seq);
-    const int rem = static_cast<int>(item - static_cast<long long>(b) * P.items_per_seq);
+  if (tid == 0) {
+    sh.ncand = 0;
+    sh.fin_b = -1;
+    for (int s = 0; s <= S; ++s) sh.ring[s] = atomicAdd(P.work, 1u);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const unsigned it_idx = sh.ring[s];
+    if (it_idx < total) issue_item<TT, TD>(P, it_idx, stages + s * kStage, warp, lane);
+    cp_async_commit();
+  }
+
+  unsigned pending = 0;   // thread 0: item index fetched one iteration ago
+  unsigned ticket = 0;    // thread 0: completion count seen by the last item
+  int ticket_b = -1;      // thread 0: sequence of the last item
+  int fin = -1;           // sequence to finish (broadcast during the next item)
+  for (int it = 0;; ++it) {
+    const unsigned cur = sh.ring[it % kRing];
+    if (cur >= total) break;
+    {
+      const unsigned nx = sh.ring[(it + S - 1) % kRing];
+      if (nx < total) issue_item<TT, TD>(P, nx, stages + ((it + S - 1) % S) * kStage, warp, lane);
+      cp_async_commit();
+    }
+    if (tid == 0) {
+      if (it > 0) sh.ring[(it + S) % kRing] = pending;
+      pending = atomicAdd(P.work, 1u);
+    }
+    cp_async_wait<S - 1>();
+
+    const int b = static_cast<int>(cur / static_cast<unsigned>(P.items_per_seq));
+    const int rem = static_cast<int>(cur - static_cast<unsigned>(b) * P.items_per_seq);
     const int r = rem / nch;
     const int ch = rem - r * nch;
-    const bool is_draft = r > k;
-    const int c0 = ch * kChunk;
-
-    float m_t, s_t;
-    float m_c, s_c;
-    bool want_cand = false;
-    float thr = INFINITY;
-    if (!is_draft) {
-      Chunk<TT> regs;
+    const unsigned char* stage = stages + (it % S) * kStage;
+    if (r <= k) {
       const TT* row = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + r) * P.V;
-      regs.load(row, c0, P.V, P.vec_t != 0, warp, lane);
-      m_t = regs.max();
-      m_t = warp_max(m_t);
-      if (lane == 0) sh.red_max[warp] = m_t;
-      __syncthreads();
-      m_c = sh.red_max[0];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) m_c = fmaxf(m_c, sh.red_max[w]);
-      s_t = regs.expsum(m_c == -INFINITY ? 0.f : m_c, P.c);
-      s_t = warp_sum(s_t);
-      if (lane == 0) sh.red_sum[warp] = s_t;
-      __syncthreads();
-      s_c = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) s_c += sh.red_sum[w];
+      process_item<TT>(P, sh, row, stage, b, r, ch, false, tid, warp, lane, &ticket, ticket_b, &fin);
     } else {
-      const int j = r - k - 1;
-      Chunk<TD> regs;
-      const TD* row = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + j) * P.V;
-      regs.load(row, c0, P.V, P.vec_d != 0, warp, lane);
-      const float mine = regs.max();
-      m_t = warp_max(mine);
-      if (lane == 0) sh.red_max[warp] = m_t;
-      __syncthreads();
-      m_c = sh.red_max[0];
-#pragma unroll
-      for (int w = 1; w < kWarps; ++w) m_c = fmaxf(m_c, sh.red_max[w]);
-      s_t = regs.expsum(m_c == -INFINITY ? 0.f : m_c, P.c);
-      s_t = warp_sum(s_t);
-      if (lane == 0) sh.red_sum[warp] = s_t;
-      __syncthreads();
-      s_c = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) s_c += sh.red_sum[w];
-      const float tau = seq_tau(P, b);
-      want_cand = seq_gated(P, b) && gate_fast_path(tau);
-      if (want_cand) {
-        // tokens with in-chunk probability >= slack * tau: a superset of the
-        // admitted set (q <= in-chunk probability), at most 1/(slack tau) of them
-        if (s_c > 0.f && isfinite(s_c)) thr = m_c + log2f(tau * kGateSlack * s_c) / P.c;
-        if (mine >= thr) {
-          regs.for_each(c0, warp, lane, [&](int v, float x) {
-            if (x >= thr && v < P.V) {
-              const int slot = atomicAdd(&sh.ncand, 1);
-              if (slot < kTopM) {
-                sh.cand_v[slot] = x;
-                sh.cand_i[slot] = v;
-              }
-            }
-          });
-        }
-        __syncthreads();
-      }
+      const TD* row = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + (r - k - 1)) * P.V;
+      process_item<TD>(P, sh, row, stage, b, r, ch, true, tid, warp, lane, &ticket, ticket_b, &fin);
     }
-
-    bool last = false;
-    if (tid == 0) {
-      const int64_t pidx = (static_cast<int64_t>(b) * P.rows + r) * nch + ch;
-      P.part[pidx] = make_float2(m_c, s_c);
-      if (want_cand) {
-        const int j = r - k - 1;
-        const int64_t cidx = (static_cast<int64_t>(b) * k + j) * nch + ch;
-        const int n = sh.ncand;
-        P.cand_n[cidx] = n;
-        for (int s = 0; s < n && s < kTopM; ++s) {
-          P.cand_v[cidx * kTopM + s] = sh.cand_v[s];
-          P.cand_i[cidx * kTopM + s] = sh.cand_i[s];
-        }
-        sh.ncand = 0;
-      }
-      __threadfence();
-      const unsigned prev = atomicAdd(P.seq_done + b, 1u);
-      last = prev == static_cast<unsigned>(P.items_per_seq - 1);
-    }
-    if (__syncthreads_or(last)) {
-      __threadfence();
-      finish_sequence<TT, TD>(P, b, sh);
-      if (tid == 0) P.seq_done[b] = 0u;  // ready for the next call
+    if (tid == 0) ticket_b = b;
+    if (fin >= 0) {  // uniform: every thread read sh.fin_b after the same barrier
+      finish_sequence<TT, TD>(P, fin, sh);
+      if (tid == 0) P.seq_done[fin] = 0u;  // ready for the next call
       __syncthreads();
+    }
+  }
+  // the last item's completion
+  if (tid == 0) {
+    sh.fin_b = (ticket_b >= 0 && ticket == static_cast<unsigned>(P.items_per_seq - 1)) ? ticket_b : -1;
+    sh.ring[0] = pending;  // consume the outstanding fetch
+  }
+  __syncthreads();
+  fin = sh.fin_b;
+  if (fin >= 0) {
+    finish_sequence<TT, TD>(P, fin, sh);
+    if (tid == 0) P.seq_done[fin] = 0u;
+  }
+  cp_async_wait<0>();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned e = atomicAdd(P.exit_count, 1u);
+    if (e == gridDim.x - 1) {  // every CTA has stopped fetching: reset for the next call
+      atomicExch(P.work, 0u);
+      atomicExch(P.exit_count, 0u);
     }
   }
 }

@@ -17,6 +17,7 @@ import numpy as np
 import torch
 
 import workloads
+from oracle import oracle as O
 
 BOUNDARY = 1e-6
 ALPHA_RTOL = 1e-5
