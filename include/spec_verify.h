@@ -181,6 +181,14 @@ const char* spec_verify_status_string(sv_status s);
  * accounting in benchmarks). */
 int spec_verify_launches_per_run(void);
 
+/* Timing aid: the next spec_verify_run* call on this handle records
+ * ev_before / ev_after (cudaEvent_t values created by the caller on the
+ * handle's device) on its stream immediately before and after its first
+ * launch, the bandwidth-bound stream pass, so that pass can be timed alone.
+ * One-shot: the marks are cleared by that call.  Passing NULL for both clears
+ * pending marks.  Returns SV_EINVAL for a NULL handle or only one NULL event. */
+sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after);
+
 #ifdef __cplusplus
 }
 #endif

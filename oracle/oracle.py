@@ -67,7 +67,7 @@ def lib() -> ctypes.CDLL:
         L.oracle_inverse_cdf.restype = ctypes.c_int64
         L.oracle_verify.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int64, ctypes.c_double, P, P, ctypes.c_uint64,
-                                    ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P,
+                                    ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P, P,
                                     ctypes.c_int]
         L.oracle_verify.restype = ctypes.c_int
         _lib = L
@@ -125,7 +125,8 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
     ``gate`` and ``tau`` are per-sequence arrays (or scalars broadcast to B).
     ``u0`` [B, k] / ``u1`` [B] give explicit uniforms instead of Philox draws.
     Returns a dict of numpy arrays: accepted_len, tokens, alpha, flags,
-    row_stats [B, 2k+1, 2] (max, lse of L/T), margin, degenerate.
+    row_stats [B, 2k+1, 2] (max, lse of L/T), margin (all used draws),
+    margin_pick (the residual / bonus pick alone), degenerate.
     """
     Lt = np.ascontiguousarray(Lt)
     Ld = np.ascontiguousarray(Ld)
@@ -147,13 +148,15 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
         flags=np.zeros((B, k), dtype=np.int8),
         row_stats=np.zeros((B, 2 * k + 1, 2), dtype=np.float64),
         margin=np.zeros(B, dtype=np.float64),
+        margin_pick=np.zeros(B, dtype=np.float64),
         degenerate=np.zeros(B, dtype=np.int32),
     )
     rc = lib().oracle_verify(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B, k, V,
                              float(T), _ptr(gate), _ptr(tau), int(seed), int(seq_offset), _ptr(u0),
                              _ptr(u1), int(rule), _ptr(out["accepted_len"]), _ptr(out["tokens"]),
                              _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
-                             _ptr(out["margin"]), _ptr(out["degenerate"]), int(nthreads))
+                             _ptr(out["margin"]), _ptr(out["margin_pick"]),
+                             _ptr(out["degenerate"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out

@@ -143,7 +143,7 @@ typedef struct {
   const double* u1;
   int rule;
   int32_t* accepted_len; int32_t* tokens; double* alpha; int8_t* flags;
-  double* row_stats; double* margin; int32_t* degenerate;
+  double* row_stats; double* margin; double* margin_pick; int32_t* degenerate;
 } job_t;
 
 typedef struct {
@@ -215,7 +215,8 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   for (int j = 0; j < k; ++j)
     if (Db[j] < 0 || (int64_t)Db[j] >= V) invalid = 1;
 
-  double marg = INFINITY;
+  double marg = INFINITY;      /* accept tests and gates of tested positions */
+  double marg_pick = INFINITY; /* the residual / bonus pick */
   if (J->degenerate) J->degenerate[b] = 0;
   if (invalid) {
     J->accepted_len[b] = -1;
@@ -225,6 +226,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
       fl[j] = ORACLE_FLAG_INVALID;
     }
     if (J->margin) J->margin[b] = marg;
+    if (J->margin_pick) J->margin_pick[b] = marg_pick;
     return;
   }
 
@@ -265,7 +267,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
       /* [M] sampler-match: a fresh target draw; accept iff it equals D */
       double m;
       int64_t x = oracle_inverse_cdf(pj, V, u, &m);
-      marg = fmin(marg, m);
+      marg_pick = fmin(marg_pick, m);
       if (x == d) {
         fl[j] = ORACLE_FLAG_ACCEPT;
         continue;
@@ -352,7 +354,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
         retained_measure(J, gated, tau, qst, S->mu);
       }
       if (gated)
-        for (int64_t v = 0; v < V; ++v) marg = fmin(marg, fabs(qst[v] - tau));
+        for (int64_t v = 0; v < V; ++v) marg_pick = fmin(marg_pick, fabs(qst[v] - tau));
       double Z = 0.0;
       for (int64_t v = 0; v < V; ++v) {
         double d = pst[v] - S->mu[v];
@@ -367,7 +369,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     }
     double m;
     pick = oracle_inverse_cdf(S->r, V, u, &m);
-    marg = fmin(marg, m);
+    marg_pick = fmin(marg_pick, m);
   }
 
   /* step 6: outputs */
@@ -375,7 +377,8 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   for (int j = 0; j < jstar; ++j) tok[j] = Db[j];
   tok[jstar] = (int32_t)pick;
   for (int j = jstar + 1; j <= k; ++j) tok[j] = -1;
-  if (J->margin) J->margin[b] = marg;
+  if (J->margin) J->margin[b] = fmin(marg, marg_pick);
+  if (J->margin_pick) J->margin_pick[b] = marg_pick;
 }
 
 /* ------------------------------------------------------------- batch */
@@ -410,15 +413,15 @@ int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_
                   uint64_t seed, uint64_t seq_offset,
                   const double* u0, const double* u1, int rule,
                   int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
-                  double* row_stats, double* margin, int32_t* degenerate,
-                  int nthreads) {
+                  double* row_stats, double* margin, double* margin_pick,
+                  int32_t* degenerate, int nthreads) {
   if (B < 0 || k < 1 || V < 1 || !(T > 0.0) || isinf(T)) return 1;
   if (B == 0) return 0;
   if (!Lt || !Ld || !D || !gate || !tau || !accepted_len || !tokens || !alpha || !flags) return 1;
   if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
   if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_RESIDUAL_Q) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
-             accepted_len, tokens, alpha, flags, row_stats, margin, degenerate};
+             accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate};
   if (nthreads < 1) nthreads = 1;
   if (nthreads > B) nthreads = B;
   worker_t* ws = (worker_t*)calloc((size_t)nthreads, sizeof(worker_t));

@@ -93,7 +93,10 @@ int64_t oracle_inverse_cdf(const double* r, int64_t V, double u, double* margin)
  *   flags[B, k], and optionally row_stats[B, 2k+1, 2] = (max, lse) of L/T for
  *   target rows 0..k then draft rows 0..k-1, margin[B] = the smallest distance
  *   of a used uniform (or of q(D), or of any q on the residual row) to its
- *   decision boundary, degenerate[B] = 1 when the residual had zero mass.
+ *   decision boundary, margin_pick[B] = the part of that minimum that comes
+ *   from the residual / bonus pick (its interval edges and, in gated mode, the
+ *   gate membership of the residual row's tokens), degenerate[B] = 1 when the
+ *   residual had zero mass.
  * nthreads >= 1 threads split the sequences.  Returns 0, or 1 on bad args.
  */
 int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
@@ -102,8 +105,8 @@ int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_
                   uint64_t seed, uint64_t seq_offset,
                   const double* u0, const double* u1, int rule,
                   int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
-                  double* row_stats, double* margin, int32_t* degenerate,
-                  int nthreads);
+                  double* row_stats, double* margin, double* margin_pick,
+                  int32_t* degenerate, int nthreads);
 
 #ifdef __cplusplus
 }

@@ -1,11 +1,13 @@
 """GB300 (sm_103a) batched speculative-decoding verification.
 
-Modified rejection sampling in plain and mu/NULL-gated modes, as one fused
-CUDA kernel behind the C ABI of ``include/spec_verify.h``; this package holds
-the CUDA sources (``csrc/``), the build step and the ctypes binding.
+Modified rejection sampling in plain and mu/NULL-gated modes: a streaming
+kernel and a per-sequence finishing kernel behind the C ABI of
+``include/spec_verify.h``.  This package holds the CUDA sources (``csrc/``),
+the build step, the ctypes binding and the sequence-sharding helper.
 """
 from .spec_verify import (  # noqa: F401
     COUNTER_NAMES, SV_BF16, SV_F32, SV_FLAG_ACCEPT, SV_FLAG_INVALID, SV_FLAG_NULL, SV_FLAG_REJECT,
     SV_FLAG_UNREACHED, SV_GATED_MU, SV_PLAIN, SpecVerifier, SpecVerifyError, load,
-    spec_verify_free, spec_verify_init, spec_verify_launches_per_run, spec_verify_run,
+    spec_verify_free, spec_verify_init, spec_verify_launches_per_run, spec_verify_mark_next,
+    spec_verify_run,
     spec_verify_run_ex, spec_verify_run_host, spec_verify_status_string)

@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/spec_verify.h: handle and
-// workspace management, argument validation and the single fused launch.
+// workspace management, argument validation, and the two launches of a call
+// (the stream pass, then the finishing pass as a programmatic dependent launch).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -23,9 +24,8 @@ struct spec_verify_s {
   float* cand_v = nullptr;
   int* cand_i = nullptr;
   unsigned* cand_n = nullptr;
-  unsigned* seq_done = nullptr;
-  unsigned* work = nullptr;
-  unsigned* exit_count = nullptr;
+  // one-shot timing marks around the next stream pass
+  cudaEvent_t mark_before = nullptr, mark_after = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
   void* stage = nullptr;
   size_t stage_bytes = 0;
@@ -47,10 +47,10 @@ constexpr int dyn_smem() {
 // opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
 template <typename TT, typename TD>
 cudaError_t configure(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(sv::verify_kernel<TT, TD>,
+  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::verify_kernel<TT, TD>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::stream_kernel<TT, TD>,
                                                        sv::kThreads, dyn_smem<TT, TD>());
 }
 
@@ -59,7 +59,28 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaSt
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   if (grid > P.total_items) grid = P.total_items;
   if (grid < 1) grid = 1;
-  sv::verify_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, dyn_smem<TT, TD>(), st>>>(P);
+  const bool marked = h->mark_before != nullptr;
+  if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
+  sv::stream_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, dyn_smem<TT, TD>(), st>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
+  if (marked) {
+    const cudaError_t e = cudaEventRecord(h->mark_after, st);
+    h->mark_before = h->mark_after = nullptr;
+    if (e != cudaSuccess) return SV_ECUDA;
+  }
+  // the finishing pass: one CTA per sequence, allowed to launch while the
+  // stream pass drains; it waits (griddepcontrol.wait) before reading its output
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(P.B));
+  cfg.blockDim = dim3(sv::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD>, P) != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -94,7 +115,14 @@ const char* spec_verify_status_string(sv_status s) {
   return "unknown status";
 }
 
-int spec_verify_launches_per_run(void) { return 1; }
+int spec_verify_launches_per_run(void) { return 2; }
+
+sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after) {
+  if (!h || (ev_before == nullptr) != (ev_after == nullptr)) return SV_EINVAL;
+  h->mark_before = static_cast<cudaEvent_t>(ev_before);
+  h->mark_after = static_cast<cudaEvent_t>(ev_after);
+  return SV_OK;
+}
 
 sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int device) {
   if (!out) return SV_EINVAL;
@@ -135,8 +163,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   const size_t o_cv = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(float), 256);
   const size_t o_ci = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(int), 256);
   const size_t o_cn = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
-  const size_t o_sd = off;   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
-  const size_t o_wk = off;   off = align_up(off + 2 * sizeof(unsigned), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
@@ -148,9 +174,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   h->cand_v = reinterpret_cast<float*>(base + o_cv);
   h->cand_i = reinterpret_cast<int*>(base + o_ci);
   h->cand_n = reinterpret_cast<unsigned*>(base + o_cn);
-  h->seq_done = reinterpret_cast<unsigned*>(base + o_sd);
-  h->work = reinterpret_cast<unsigned*>(base + o_wk);
-  h->exit_count = h->work + 1;
   if (cudaMemset(h->ws, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
@@ -216,9 +239,6 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.cand_v = h->cand_v;
   P.cand_i = h->cand_i;
   P.cand_n = h->cand_n;
-  P.seq_done = h->seq_done;
-  P.work = h->work;
-  P.exit_count = h->exit_count;
   const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
   const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
   P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);

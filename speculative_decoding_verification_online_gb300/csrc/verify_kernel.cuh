@@ -1,37 +1,40 @@
-// Fused batched speculative-decoding verification kernel for sm_103a.
+// Batched speculative-decoding verification kernels for sm_103a.
 //
-// One launch verifies a whole batch.  Work is a list of items (sequence b,
-// row r, chunk c) in sequence-major order, where rows 0..k are the target
-// rows and rows k+1..2k the draft rows of b, and a chunk is kChunk = 8192
-// consecutive vocabulary entries.  Persistent CTAs pull items from a global
-// counter (so a CTA that is busy finishing a sequence simply takes fewer
-// items) and run a cp.async pipeline of S chunk stages in shared memory:
+// A call is two launches on one stream:
 //
-//   1. stream the chunk once (16-byte cp.async per thread, each warp copying
-//      512 contiguous bytes per instruction; every thread later reads back
-//      exactly the pieces it copied, so the pipeline needs no extra barrier),
-//      take the chunk max m and s = sum exp((L - m) / T) -- the one-read row
-//      statistics of the temperature softmax (mlxcel PR #992, "What changed":
-//      p and q are full-vocabulary temperature softmaxes in fp32); record the
-//      logit at the drafted token when it lies in the chunk; for draft rows
-//      of gated sequences keep the tokens whose in-chunk probability reaches
-//      the gate (at most floor(1/threshold) of them, a superset of the tokens
-//      the gate admits) in a per-row candidate list;
-//   2. publish (m, s) and bump the sequence's completion counter with an
-//      acq_rel atomic; the CTA that completes the last item of sequence b
-//      finishes b (no CTA ever waits for another, so nothing can hang):
-//   3. combine the chunk partials into row max / sum, evaluate every draft
-//      position -- gate, retained measure mu, alpha = min(1, p(D)/mu(D)),
-//      Philox u0, the accept test p > 0 && u0 * mu <= p (Strata PR #3416,
-//      "Approach"; mlxcel PR #992, "What changed") -- and stop at the first
-//      position not accepted;
-//   4. sample the stop row: the normalised positive part of p - mu after a
-//      rejection or NULL, p itself for the bonus row.  Chunk sums of the
-//      residual come from the partials (minus the admitted tokens' min(p, q)
-//      in gated mode), a prefix over chunks finds the chunk holding u1 * Z,
-//      and one re-read of that chunk with a block-wide scan finds the token.
-//      Plain-mode rejections need q everywhere, so they re-read the stop row
-//      pair once to form the chunk sums.
+// stream_kernel -- the bandwidth-bound pass.  Work is a list of items (sequence
+//   b, row r, chunk c), where rows 0..k are the target rows and rows k+1..2k the
+//   draft rows of b and a chunk is kChunk = 8192 consecutive vocabulary entries.
+//   Persistent CTAs take items round-robin through a cp.async pipeline of S
+//   chunk stages in shared memory (16-byte copies, each warp moving 512
+//   contiguous bytes per instruction; every thread later reads back exactly the
+//   pieces it copied, so the pipeline needs no barrier of its own).  Per item
+//   it reads the chunk once and publishes the chunk statistics of the
+//   temperature softmax (mlxcel PR #992, "What changed": p and q are
+//   full-vocabulary temperature softmaxes in fp32), the logit at the drafted
+//   token when that token lies in the chunk, and -- for draft rows of gated
+//   sequences -- the tokens whose in-chunk probability reaches the gate (at
+//   most floor(1/threshold) per chunk, a superset of the tokens the gate
+//   admits) appended to a per-row candidate list.
+//
+// finish_kernel -- one CTA per sequence, launched as a programmatic dependent
+//   launch so that its start-up overlaps the end of the stream pass.  It
+//   combines the chunk statistics into row statistics, evaluates every draft
+//   position -- gate, retained measure mu, alpha = min(1, p(D)/mu(D)), Philox
+//   u0, the accept test p > 0 && u0 * mu <= p (Strata PR #3416, "Approach";
+//   mlxcel PR #992, "What changed") -- stops at the first position not
+//   accepted, and samples the stop row: the normalised positive part of p - mu
+//   after a rejection or NULL, p itself for the bonus row.  Chunk sums of the
+//   residual come from the chunk statistics (minus the admitted tokens'
+//   min(p, q) in gated mode), a prefix over chunks finds the chunk holding
+//   u1 * Z, and one re-read of that chunk with a block-wide scan finds the
+//   token.  Plain-mode rejections need q everywhere, so they re-read the stop
+//   row pair once to form the chunk sums.
+//
+// Row statistics live in a scaled log2 domain: with c = log2(e) / T, a chunk
+// with raw maximum m stores mc = fl(m * c) and s = sum_v exp2(fma(x_v, c, -mc)),
+// and a token's probability is exp2(fma(x, c, -Mc)) / S for the row's (Mc, S).
+// One FFMA per entry, and the stored reference mc is exactly the one removed.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -46,13 +49,12 @@ namespace sv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kEPT = 32;                    // elements per thread per chunk
+constexpr int kEPT = 32;                    // entries per thread per chunk
 constexpr int kChunk = kThreads * kEPT;     // vocabulary entries per work item
 constexpr int kTopM = 4;                    // gate candidates per chunk / admitted tokens per row
 constexpr int kRowCap = 64;                 // gate candidates kept per draft row
 constexpr int kMaxChunks = (SV_MAX_V + kChunk - 1) / kChunk;
 constexpr int kMaxRows = 2 * SV_MAX_K + 1;
-constexpr int kRing = 8;                    // fetched item indices kept per CTA
 constexpr float kBoundary = 1e-6f;
 // Candidates are kept against a threshold lowered by this factor so that
 // rounding cannot drop an admitted token; the gated fast path needs
@@ -81,14 +83,11 @@ struct Params {
   unsigned long long* counters;
   float* row_stats;
   // workspace
-  float2* part;        // [B, rows, nchunk] (chunk max of raw logits, sum of exp2((L - m) c))
+  float2* part;        // [B, rows, nchunk] (mc, s) per chunk
   float* xD;           // [B, rows] raw logit at the drafted token (rows j < k and draft rows)
   float* cand_v;       // [B, k, kRowCap] raw logits of gate candidates
   int* cand_i;         // [B, k, kRowCap] their token ids
   unsigned* cand_n;    // [B, k] candidates appended (> kRowCap: overflow); reset by the finisher
-  unsigned* seq_done;  // [B] completion counters, reset by the finisher
-  unsigned* work;      // [1] next item to hand out, reset by the last CTA to exit
-  unsigned* exit_count;  // [1]
   int vec_t, vec_d;    // rows allow 16-byte vector loads
 };
 
@@ -107,12 +106,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 __device__ __forceinline__ float2 ldcg_f2(const float2* p) { return __ldcg(p); }
 
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
@@ -125,31 +118,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 pk(float a, float b) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk(f32x2 v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -222,10 +190,10 @@ __device__ __forceinline__ void load8<float>(const float* row, int v0, int V, bo
   }
 }
 
-// probability of a token with raw logit x in a row with raw max M and
-// 1/sum invS: exp2((x - M) * c) * invS.  Every decision uses this one formula.
-__device__ __forceinline__ float prob_of(float x, float M, float c, float invS) {
-  return exp2f((x - M) * c) * invS;
+// probability of a token with raw logit x in a row with scaled max Mc and
+// 1/sum invS: exp2(fma(x, c, -Mc)) * invS.  Every decision uses this formula.
+__device__ __forceinline__ float prob_of(float x, float Mc, float c, float invS) {
+  return exp2f(fmaf(x, c, -Mc)) * invS;
 }
 
 __device__ __forceinline__ bool gate_fast_path(float tau) {
@@ -235,11 +203,10 @@ __device__ __forceinline__ bool gate_fast_path(float tau) {
 // ------------------------------------------------------- chunk registers
 //
 // Thread t = 32 w + l owns NV 16-byte slots of the chunk: slot i is vector
-// index w * 32 NV + 32 i + l (each copy instruction of a warp moves 512
-// contiguous bytes).  bf16: 4 slots of 8 entries kept packed; f32: 8 slots of
-// 4.  A slot that lies wholly inside the row of an aligned tensor travels by
-// cp.async into the stage; other slots (ragged tail, unaligned rows) are read
-// directly, entries past V reading as -inf.
+// index w * 32 NV + 32 i + l.  bf16: 4 slots of 8 entries kept packed; f32: 8
+// slots of 4.  A slot that lies wholly inside the row of an aligned tensor
+// travels by cp.async into the stage; other slots (ragged tail, unaligned
+// rows) are read directly, entries past V reading as -inf.
 
 template <typename T> struct Chunk;
 
@@ -281,18 +248,17 @@ template <> struct Chunk<uint16_t> {
     for (int q = 1; q < 16; ++q) m = bmax2(m, w[q]);
     return fmaxf(bf16_lo(m), bf16_hi(m));
   }
-  __device__ __forceinline__ float expsum(float m, float c) const {
-    const f32x2 mm = pk(m, m), cc = pk(c, c);
-    f32x2 acc = pk(0.f, 0.f);
+  // sum_v exp2(fma(x_v, c, nmc)), four independent accumulators
+  __device__ __forceinline__ float expsum(float c, float nmc) const {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      float a, b;
-      upk(mul2(sub2(pk(bf16_lo(w[q]), bf16_hi(w[q])), mm), cc), a, b);
-      acc = add2(acc, pk(ex2_approx(a), ex2_approx(b)));
+    for (int q = 0; q < 16; q += 2) {
+      a0 += ex2_approx(fmaf(bf16_lo(w[q]), c, nmc));
+      a1 += ex2_approx(fmaf(bf16_hi(w[q]), c, nmc));
+      a2 += ex2_approx(fmaf(bf16_lo(w[q + 1]), c, nmc));
+      a3 += ex2_approx(fmaf(bf16_hi(w[q + 1]), c, nmc));
     }
-    float s0, s1;
-    upk(acc, s0, s1);
-    return s0 + s1;
+    return (a0 + a1) + (a2 + a3);
   }
   template <typename F>
   __device__ __forceinline__ void for_each(int c0, int warp, int lane, F&& f) const {
@@ -336,23 +302,24 @@ template <> struct Chunk<float> {
     }
   }
   __device__ __forceinline__ float max() const {
-    float m = x[0];
+    float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]);
 #pragma unroll
-    for (int e = 1; e < 32; ++e) m = fmaxf(m, x[e]);
-    return m;
-  }
-  __device__ __forceinline__ float expsum(float m, float c) const {
-    const f32x2 mm = pk(m, m), cc = pk(c, c);
-    f32x2 acc = pk(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      float a, b;
-      upk(mul2(sub2(pk(x[e], x[e + 1]), mm), cc), a, b);
-      acc = add2(acc, pk(ex2_approx(a), ex2_approx(b)));
+    for (int e = 4; e < 32; e += 4) {
+      m0 = fmaxf(m0, fmaxf(x[e], x[e + 1]));
+      m1 = fmaxf(m1, fmaxf(x[e + 2], x[e + 3]));
     }
-    float s0, s1;
-    upk(acc, s0, s1);
-    return s0 + s1;
+    return fmaxf(m0, m1);
+  }
+  __device__ __forceinline__ float expsum(float c, float nmc) const {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      a0 += ex2_approx(fmaf(x[e], c, nmc));
+      a1 += ex2_approx(fmaf(x[e + 1], c, nmc));
+      a2 += ex2_approx(fmaf(x[e + 2], c, nmc));
+      a3 += ex2_approx(fmaf(x[e + 3], c, nmc));
+    }
+    return (a0 + a1) + (a2 + a3);
   }
   template <typename F>
   __device__ __forceinline__ void for_each(int c0, int warp, int lane, F&& f) const {
@@ -365,19 +332,192 @@ template <> struct Chunk<float> {
   }
 };
 
-// ---------------------------------------------------------- shared state
+__device__ __forceinline__ bool seq_gated(const Params& P, int b) {
+  return P.gate_per_seq ? (P.gate_per_seq[b] != 0) : (P.gate_default != 0);
+}
+__device__ __forceinline__ float seq_tau(const Params& P, int b) {
+  return P.tau_per_seq ? P.tau_per_seq[b] : P.tau_default;
+}
 
-struct Shared {
-  // streaming phase
-  float red_max[kWarps];
-  float red_sum[kWarps];
+// ------------------------------------------------------- stream kernel
+
+template <typename TT, typename TD>
+struct Stages {
+  static constexpr int kBytes = kChunk * static_cast<int>(sizeof(TT) > sizeof(TD) ? sizeof(TT) : sizeof(TD));
+  static constexpr int kDepth = kBytes <= 16384 ? 4 : 3;
+  static constexpr int kMinBlocks = kBytes <= 16384 ? 3 : 2;
+};
+
+struct StreamShared {
+  __align__(16) float red_max[kWarps];
+  __align__(16) float red_sum[kWarps];
   int ncand;
   float cand_v[kTopM];
   int cand_i[kTopM];
-  unsigned ring[kRing];
-  int fin_b;
-  // finishing phase
-  float rowM[kMaxRows];
+};
+
+__device__ __forceinline__ void decode_item(const Params& P, unsigned item, int& b, int& r, int& ch) {
+  b = static_cast<int>(item / static_cast<unsigned>(P.items_per_seq));
+  const int rem = static_cast<int>(item - static_cast<unsigned>(b) * P.items_per_seq);
+  r = rem / P.nchunk;
+  ch = rem - r * P.nchunk;
+}
+
+template <typename TT, typename TD>
+__device__ __forceinline__ void issue_item(const Params& P, unsigned item, unsigned char* stage,
+                                           int warp, int lane) {
+  int b, r, ch;
+  decode_item(P, item, b, r, ch);
+  const int c0 = ch * kChunk;
+  if (r <= P.k) {
+    if (P.vec_t)
+      Chunk<TT>::issue(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V,
+                       stage, c0, P.V, warp, lane);
+  } else {
+    if (P.vec_d)
+      Chunk<TD>::issue(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V,
+                       stage, c0, P.V, warp, lane);
+  }
+}
+
+// one work item: chunk statistics, drafted-token logit, gate candidates
+template <typename T>
+__device__ __forceinline__ void process_item(const Params& P, StreamShared& sh, const T* row,
+                                             const unsigned char* stage, int b, int r, int ch,
+                                             bool is_draft, int tid, int warp, int lane) {
+  const int k = P.k;
+  const int c0 = ch * kChunk;
+  const bool vec = is_draft ? P.vec_d != 0 : P.vec_t != 0;
+  const int j = is_draft ? r - k - 1 : r;
+  int d = -1;
+  if (tid == 0 && j < k) d = __ldg(P.D + static_cast<int64_t>(b) * k + j);
+
+  Chunk<T> regs;
+  regs.load(row, stage, c0, P.V, vec, warp, lane);
+  const float mine = regs.max();
+  const float mw = warp_max(mine);
+  if (lane == 0) sh.red_max[warp] = mw;
+  __syncthreads();
+  const float4 ma = *reinterpret_cast<const float4*>(&sh.red_max[0]);
+  const float4 mb = *reinterpret_cast<const float4*>(&sh.red_max[4]);
+  const float m_c = fmaxf(fmaxf(fmaxf(ma.x, ma.y), fmaxf(ma.z, ma.w)), fmaxf(fmaxf(mb.x, mb.y), fmaxf(mb.z, mb.w)));
+  // scaled reference: mc = fl(m c); an all -inf chunk uses 0 so that -inf entries give 0
+  const float mc = m_c == -INFINITY ? -INFINITY : m_c * P.c;
+  const float nmc = m_c == -INFINITY ? 0.f : -mc;
+  const float s_t = warp_sum(regs.expsum(P.c, nmc));
+  if (lane == 0) sh.red_sum[warp] = s_t;
+  __syncthreads();
+  const float4 sa = *reinterpret_cast<const float4*>(&sh.red_sum[0]);
+  const float4 sb = *reinterpret_cast<const float4*>(&sh.red_sum[4]);
+  const float s_c = ((sa.x + sa.y) + (sa.z + sa.w)) + ((sb.x + sb.y) + (sb.z + sb.w));
+
+  bool want_cand = false;
+  if (is_draft) {
+    const float tau = seq_tau(P, b);
+    want_cand = seq_gated(P, b) && gate_fast_path(tau);
+    if (want_cand) {
+      // in-chunk probability exp2(x c - mc) / s >= slack * tau: a superset of
+      // the admitted set (q <= in-chunk probability), at most 1/(slack tau) tokens
+      float thr = INFINITY;
+      if (s_c > 0.f && isfinite(s_c)) thr = (mc + log2f(tau * kGateSlack * s_c)) / P.c;
+      if (mine >= thr) {
+        regs.for_each(c0, warp, lane, [&](int v, float x) {
+          if (x >= thr && v < P.V) {
+            const int slot = atomicAdd(&sh.ncand, 1);
+            if (slot < kTopM) {
+              sh.cand_v[slot] = x;
+              sh.cand_i[slot] = v;
+            }
+          }
+        });
+      }
+      __syncthreads();
+    }
+  }
+
+  if (tid == 0) {
+    const int R = P.rows;
+    P.part[(static_cast<int64_t>(b) * R + r) * P.nchunk + ch] = make_float2(mc, s_c);
+    if (d >= c0 && d < c0 + kChunk && d < P.V) {
+      constexpr int kVE = Chunk<T>::kVE;
+      const int v0 = d - (d - c0) % kVE;
+      float x;
+      if (vec && v0 + kVE <= P.V) {
+        if (sizeof(T) == 2)
+          x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[d - c0]) << 16);
+        else
+          x = reinterpret_cast<const float*>(stage)[d - c0];
+      } else {
+        x = logit_at<T>(row, d);
+      }
+      P.xD[static_cast<int64_t>(b) * R + r] = x;
+    }
+    if (want_cand) {
+      const int n = sh.ncand;
+      if (n > 0) {
+        const int64_t rowc = static_cast<int64_t>(b) * k + j;
+        const unsigned add = n > kTopM ? static_cast<unsigned>(kRowCap + 1) : static_cast<unsigned>(n);
+        const unsigned base = atomicAdd(P.cand_n + rowc, add);
+        if (n <= kTopM)
+          for (int s = 0; s < n; ++s)
+            if (base + s < static_cast<unsigned>(kRowCap)) {
+              P.cand_v[rowc * kRowCap + base + s] = sh.cand_v[s];
+              P.cand_i[rowc * kRowCap + base + s] = sh.cand_i[s];
+            }
+      }
+      sh.ncand = 0;
+    }
+  }
+}
+
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(kThreads, Stages<TT, TD>::kMinBlocks) stream_kernel(const Params P) {
+  constexpr int S = Stages<TT, TD>::kDepth;
+  constexpr int kStage = Stages<TT, TD>::kBytes;
+  extern __shared__ __align__(128) unsigned char stages[];
+  __shared__ StreamShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned total = P.total_items;
+  const unsigned G = gridDim.x;
+  const int k = P.k;
+  if (tid == 0) sh.ncand = 0;
+
+  // prologue: the first S - 1 items of this CTA in flight
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) {
+    const unsigned item = blockIdx.x + static_cast<unsigned>(s) * G;
+    if (item < total) issue_item<TT, TD>(P, item, stages + s * kStage, warp, lane);
+    cp_async_commit();
+  }
+  int it = 0;
+  for (unsigned item = blockIdx.x; item < total; item += G, ++it) {
+    {
+      const unsigned nx = item + static_cast<unsigned>(S - 1) * G;
+      if (nx < total) issue_item<TT, TD>(P, nx, stages + ((it + S - 1) % S) * kStage, warp, lane);
+      cp_async_commit();
+    }
+    cp_async_wait<S - 1>();
+    int b, r, ch;
+    decode_item(P, item, b, r, ch);
+    const unsigned char* stage = stages + (it % S) * kStage;
+    if (r <= k) {
+      const TT* row = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + r) * P.V;
+      process_item<TT>(P, sh, row, stage, b, r, ch, false, tid, warp, lane);
+    } else {
+      const TD* row = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + (r - k - 1)) * P.V;
+      process_item<TD>(P, sh, row, stage, b, r, ch, true, tid, warp, lane);
+    }
+  }
+  cp_async_wait<0>();
+  // let the finishing grid start its prologue; its griddepcontrol.wait still
+  // waits for this grid to complete and its memory to be visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------ finishing
+
+struct FinishShared {
+  float rowM[kMaxRows];      // scaled row max Mc
   float rowInvS[kMaxRows];
   double rowS[kMaxRows];
   float xD[kMaxRows];
@@ -400,15 +540,6 @@ struct Shared {
   float adm_q[SV_MAX_K][kTopM];
   float adm_p[SV_MAX_K][kTopM];
 };
-
-__device__ __forceinline__ bool seq_gated(const Params& P, int b) {
-  return P.gate_per_seq ? (P.gate_per_seq[b] != 0) : (P.gate_default != 0);
-}
-__device__ __forceinline__ float seq_tau(const Params& P, int b) {
-  return P.tau_per_seq ? P.tau_per_seq[b] : P.tau_default;
-}
-
-// ------------------------------------------------------------ finishing
 
 // residual weight of token v with target logit xt (and draft logit xd in the
 // dense mode).  mode 0: p (bonus row, or degenerate residual); mode 1: p, or
@@ -436,8 +567,7 @@ struct ResidualEval {
 };
 
 template <typename TT, typename TD>
-__device__ void finish_sequence(const Params& P, int b, Shared& sh) {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+__device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
   const bool gated = seq_gated(P, b);
@@ -477,7 +607,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       }
     }
   }
-  // F1: row max / sum from the chunk partials (fp64 accumulation)
+  // row statistics from the chunk statistics (fp64 accumulation)
   for (int r = warp; r < R; r += kWarps) {
     const float2* pr = P.part + (static_cast<int64_t>(b) * R + r) * nch;
     float M = -INFINITY;
@@ -487,7 +617,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
     for (int ch = lane; ch < nch; ch += 32) {
       const float2 ms = ldcg_f2(pr + ch);
       S += (ms.x == -INFINITY) ? static_cast<double>(ms.y * 0.f)
-                               : static_cast<double>(ms.y) * static_cast<double>(exp2f((ms.x - M) * c));
+                               : static_cast<double>(ms.y) * static_cast<double>(exp2f(ms.x - M));
     }
     S = warp_sum_d(S);
     if (lane == 0) {
@@ -496,10 +626,10 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       sh.rowInvS[r] = static_cast<float>(1.0 / S);
       if (M == -INFINITY || !isfinite(S) || !(S > 0.0)) sh.bad = 1;
       if (P.row_stats) {
-        const float mo = M / P.T;
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = mo;
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] =
-            static_cast<float>(static_cast<double>(mo) + log(S));
+        // (max, log-sum-exp) of L / T: Mc ln 2 and Mc ln 2 + ln S
+        const double mo = static_cast<double>(M) * 0.6931471805599453;
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = static_cast<float>(mo);
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = static_cast<float>(mo + log(S));
       }
     }
   }
@@ -538,7 +668,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
             __ldcg(P.cand_i + static_cast<int64_t>(b) * k * kRowCap + e));
   }
 
-  // F2: every draft position (one lane each): gate, mu, alpha, accept test
+  // every draft position (one lane each): gate, mu, alpha, accept test
   if (warp == 0) {
     bool ok = true, acc = false, is_null = false, near = false;
     float alpha = 0.f;
@@ -600,7 +730,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
     return;
   }
 
-  // F3: the stop row's residual (or bonus) weights, chunk by chunk
+  // the stop row's residual (or bonus) weights, chunk by chunk
   const int rt = jstar, rd = k + 1 + jstar;
   const TT* trow = Lt + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
   const TD* drow = jstar < k ? Ld + (static_cast<int64_t>(b) * k + jstar) * V : nullptr;
@@ -619,7 +749,7 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
       const float2 ms = ldcg_f2(pr + ch);
       double t = (ms.x == -INFINITY)
                      ? 0.0
-                     : static_cast<double>(ms.y) * static_cast<double>(exp2f((ms.x - ev.Mt) * c)) *
+                     : static_cast<double>(ms.y) * static_cast<double>(exp2f(ms.x - ev.Mt)) *
                            (1.0 / sh.rowS[rt]);
       if (use_mode == 1) {
         for (int a = 0; a < nadm; ++a)
@@ -805,204 +935,12 @@ __device__ void finish_sequence(const Params& P, int b, Shared& sh) {
   if (tid > jstar && tid <= k) tok[tid] = -1;
 }
 
-// ----------------------------------------------------------- the kernel
-
 template <typename TT, typename TD>
-struct Stages {
-  static constexpr int kBytes = kChunk * static_cast<int>(sizeof(TT) > sizeof(TD) ? sizeof(TT) : sizeof(TD));
-  static constexpr int kDepth = kBytes <= 16384 ? 4 : 3;
-  static constexpr int kMinBlocks = kBytes <= 16384 ? 3 : 2;
-};
-
-template <typename TT, typename TD>
-__device__ __forceinline__ void issue_item(const Params& P, unsigned item, unsigned char* stage,
-                                           int warp, int lane) {
-  const int b = static_cast<int>(item / static_cast<unsigned>(P.items_per_seq));
-  const int rem = static_cast<int>(item - static_cast<unsigned>(b) * P.items_per_seq);
-  const int r = rem / P.nchunk;
-  const int c0 = (rem - r * P.nchunk) * kChunk;
-  if (r <= P.k) {
-    if (P.vec_t)
-      Chunk<TT>::issue(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V,
-                       stage, c0, P.V, warp, lane);
-  } else {
-    if (P.vec_d)
-      Chunk<TD>::issue(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V,
-                       stage, c0, P.V, warp, lane);
-  }
-}
-
-// one work item: chunk statistics, drafted-token logit, gate candidates, and
-// the publication of all of it.  On entry *ticket / ticket_b (thread 0) hold
-// the completion count the previous item observed and its sequence; *fin_out
-// returns, to every thread, the sequence that previous item completed (or -1),
-// and *ticket the count this item observes.
-template <typename T>
-__device__ __forceinline__ void process_item(const Params& P, Shared& sh, const T* row,
-                                             const unsigned char* stage, int b, int r, int ch,
-                                             bool is_draft, int tid, int warp, int lane,
-                                             unsigned* ticket, int ticket_b, int* fin_out) {
-  const int k = P.k;
-  const int c0 = ch * kChunk;
-  const bool vec = is_draft ? P.vec_d != 0 : P.vec_t != 0;
-  const int j = is_draft ? r - k - 1 : r;
-  int d = -1;
-  if (tid == 0 && j < k) d = __ldg(P.D + static_cast<int64_t>(b) * k + j);
-
-  Chunk<T> regs;
-  regs.load(row, stage, c0, P.V, vec, warp, lane);
-  const float mine = regs.max();
-  const float mw = warp_max(mine);
-  if (lane == 0) sh.red_max[warp] = mw;
-  __syncthreads();
-  float m_c = sh.red_max[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) m_c = fmaxf(m_c, sh.red_max[w]);
-  const float s_t = warp_sum(regs.expsum(m_c == -INFINITY ? 0.f : m_c, P.c));
-  if (lane == 0) sh.red_sum[warp] = s_t;
-  if (tid == 0)  // the previous item's completion count has had a whole item to return
-    sh.fin_b = (ticket_b >= 0 && *ticket == static_cast<unsigned>(P.items_per_seq - 1)) ? ticket_b : -1;
-  __syncthreads();
-  float s_c = 0.f;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) s_c += sh.red_sum[w];
-  *fin_out = sh.fin_b;
-
-  bool want_cand = false;
-  if (is_draft) {
-    const float tau = seq_tau(P, b);
-    want_cand = seq_gated(P, b) && gate_fast_path(tau);
-    if (want_cand) {
-      // tokens with in-chunk probability >= slack * tau: a superset of the
-      // admitted set (q <= in-chunk probability), at most 1/(slack tau) of them
-      float thr = INFINITY;
-      if (s_c > 0.f && isfinite(s_c)) thr = m_c + log2f(tau * kGateSlack * s_c) / P.c;
-      if (mine >= thr) {
-        regs.for_each(c0, warp, lane, [&](int v, float x) {
-          if (x >= thr && v < P.V) {
-            const int slot = atomicAdd(&sh.ncand, 1);
-            if (slot < kTopM) {
-              sh.cand_v[slot] = x;
-              sh.cand_i[slot] = v;
-            }
-          }
-        });
-      }
-      __syncthreads();
-    }
-  }
-
-  if (tid == 0) {
-    const int R = P.rows;
-    P.part[(static_cast<int64_t>(b) * R + r) * P.nchunk + ch] = make_float2(m_c, s_c);
-    if (d >= c0 && d < c0 + kChunk && d < P.V) {
-      constexpr int kVE = Chunk<T>::kVE;
-      const int v0 = d - (d - c0) % kVE;
-      const float x = (vec && v0 + kVE <= P.V) ? (sizeof(T) == 2
-                          ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[d - c0]) << 16)
-                          : reinterpret_cast<const float*>(stage)[d - c0])
-                                              : logit_at<T>(row, d);
-      P.xD[static_cast<int64_t>(b) * R + r] = x;
-    }
-    if (want_cand) {
-      const int n = sh.ncand;
-      if (n > 0) {
-        const int64_t rowc = static_cast<int64_t>(b) * k + j;
-        const unsigned add = n > kTopM ? static_cast<unsigned>(kRowCap + 1) : static_cast<unsigned>(n);
-        const unsigned base = atomicAdd(P.cand_n + rowc, add);
-        if (n <= kTopM)
-          for (int s = 0; s < n; ++s)
-            if (base + s < static_cast<unsigned>(kRowCap)) {
-              P.cand_v[rowc * kRowCap + base + s] = sh.cand_v[s];
-              P.cand_i[rowc * kRowCap + base + s] = sh.cand_i[s];
-            }
-      }
-      sh.ncand = 0;
-    }
-    *ticket = atom_add_acq_rel(P.seq_done + b, 1u);
-  }
-}
-
-template <typename TT, typename TD>
-__global__ void __launch_bounds__(kThreads, Stages<TT, TD>::kMinBlocks) verify_kernel(const Params P) {
-  constexpr int S = Stages<TT, TD>::kDepth;
-  constexpr int kStage = Stages<TT, TD>::kBytes;
-  extern __shared__ __align__(128) unsigned char stages[];
-  __shared__ Shared sh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned total = P.total_items;
-  const int k = P.k, nch = P.nchunk;
-
-  if (tid == 0) {
-    sh.ncand = 0;
-    sh.fin_b = -1;
-    for (int s = 0; s <= S; ++s) sh.ring[s] = atomicAdd(P.work, 1u);
-  }
-  __syncthreads();
-#pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
-    const unsigned it_idx = sh.ring[s];
-    if (it_idx < total) issue_item<TT, TD>(P, it_idx, stages + s * kStage, warp, lane);
-    cp_async_commit();
-  }
-
-  unsigned pending = 0;   // thread 0: item index fetched one iteration ago
-  unsigned ticket = 0;    // thread 0: completion count seen by the last item
-  int ticket_b = -1;      // thread 0: sequence of the last item
-  int fin = -1;           // sequence to finish (broadcast during the next item)
-  for (int it = 0;; ++it) {
-    const unsigned cur = sh.ring[it % kRing];
-    if (cur >= total) break;
-    {
-      const unsigned nx = sh.ring[(it + S - 1) % kRing];
-      if (nx < total) issue_item<TT, TD>(P, nx, stages + ((it + S - 1) % S) * kStage, warp, lane);
-      cp_async_commit();
-    }
-    if (tid == 0) {
-      if (it > 0) sh.ring[(it + S) % kRing] = pending;
-      pending = atomicAdd(P.work, 1u);
-    }
-    cp_async_wait<S - 1>();
-
-    const int b = static_cast<int>(cur / static_cast<unsigned>(P.items_per_seq));
-    const int rem = static_cast<int>(cur - static_cast<unsigned>(b) * P.items_per_seq);
-    const int r = rem / nch;
-    const int ch = rem - r * nch;
-    const unsigned char* stage = stages + (it % S) * kStage;
-    if (r <= k) {
-      const TT* row = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + r) * P.V;
-      process_item<TT>(P, sh, row, stage, b, r, ch, false, tid, warp, lane, &ticket, ticket_b, &fin);
-    } else {
-      const TD* row = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + (r - k - 1)) * P.V;
-      process_item<TD>(P, sh, row, stage, b, r, ch, true, tid, warp, lane, &ticket, ticket_b, &fin);
-    }
-    if (tid == 0) ticket_b = b;
-    if (fin >= 0) {  // uniform: every thread read sh.fin_b after the same barrier
-      finish_sequence<TT, TD>(P, fin, sh);
-      if (tid == 0) P.seq_done[fin] = 0u;  // ready for the next call
-      __syncthreads();
-    }
-  }
-  // the last item's completion
-  if (tid == 0) {
-    sh.fin_b = (ticket_b >= 0 && ticket == static_cast<unsigned>(P.items_per_seq - 1)) ? ticket_b : -1;
-    sh.ring[0] = pending;  // consume the outstanding fetch
-  }
-  __syncthreads();
-  fin = sh.fin_b;
-  if (fin >= 0) {
-    finish_sequence<TT, TD>(P, fin, sh);
-    if (tid == 0) P.seq_done[fin] = 0u;
-  }
-  cp_async_wait<0>();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned e = atomicAdd(P.exit_count, 1u);
-    if (e == gridDim.x - 1) {  // every CTA has stopped fetching: reset for the next call
-      atomicExch(P.work, 0u);
-      atomicExch(P.exit_count, 0u);
-    }
-  }
+__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const Params P) {
+  __shared__ FinishShared sh;
+  // wait for the stream pass (programmatic dependent launch) before reading its output
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  finish_sequence<TT, TD>(P, blockIdx.x, sh);
 }
 
 }  // namespace sv

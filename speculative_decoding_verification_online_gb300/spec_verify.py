@@ -58,6 +58,8 @@ def load() -> ctypes.CDLL:
     L.spec_verify_status_string.restype = ctypes.c_char_p
     L.spec_verify_launches_per_run.argtypes = []
     L.spec_verify_launches_per_run.restype = I
+    L.spec_verify_mark_next.argtypes = [P, P, P]
+    L.spec_verify_mark_next.restype = I
     _lib = L
     return L
 
@@ -110,6 +112,11 @@ def spec_verify_launches_per_run() -> int:
     return load().spec_verify_launches_per_run()
 
 
+def spec_verify_mark_next(h, ev_before, ev_after) -> int:
+    """Record two CUDA events (raw cudaEvent_t handles) around the next call's stream pass."""
+    return load().spec_verify_mark_next(h, ev_before, ev_after)
+
+
 # ------------------------------------------------------ torch marshalling
 
 def _dt(t: torch.Tensor) -> int:
@@ -153,6 +160,12 @@ class SpecVerifier:
             self.close()
         except Exception:
             pass
+
+    def mark_next(self, ev_before: torch.cuda.Event, ev_after: torch.cuda.Event):
+        """Time the next call's stream pass with two torch CUDA events (enable_timing=True)."""
+        rc = spec_verify_mark_next(self.handle, ev_before.cuda_event, ev_after.cuda_event)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_mark_next")
 
     def outputs(self, B: int):
         dev = self.device

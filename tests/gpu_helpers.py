@@ -2,14 +2,18 @@
 the same seeded inputs and compare them the way the tolerances demand.
 
 Comparison rules:
-  * accepted lengths and emitted tokens are compared bit for bit on every
-    sequence whose oracle margin (the distance of any used uniform, or of a
-    gated q, to its decision boundary) is at least 1e-6; sequences below that
-    margin are boundary draws, counted and excluded;
+  * accepted lengths, emitted tokens and flags are compared bit for bit on
+    every sequence whose oracle margin (the distance of every used uniform, or
+    gated q, to its decision boundary) is at least 1e-6; a mismatch there fails;
+  * sequences below that margin are boundary draws: they are counted, and so
+    are the mismatches among them.  Draws of the accept test and the gate must
+    number under 1e-5 of those draws (plus a small allowance for small
+    samples); the residual / bonus pick over V tokens has V interval edges,
+    so at large V many picks sit within 1e-6 of an edge whatever the
+    arithmetic -- those are reported, and mismatches among them bounded;
   * acceptance probabilities agree within 1e-5 relative (fp32 against fp64),
     except on positions whose gated q(D) lies within 1e-6 of the threshold
-    (there the NULL decision itself is a boundary case);
-  * flags of reached positions are compared like the tokens.
+    (there the NULL decision itself is a boundary case).
 """
 from __future__ import annotations
 
@@ -53,7 +57,8 @@ def gated_q_of_drafts(w: workloads.Workload, ref, idx=None):
 
 
 def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
-    """Assert parity; returns (n_compared, n_boundary)."""
+    """Assert parity; returns a dict of counts (compared, boundary, boundary_decision,
+    boundary_pick, boundary_mismatch, draws)."""
     sel = slice(None) if idx is None else np.asarray(idx)
     g_len = got["accepted_len"].cpu().numpy()[sel]
     g_tok = got["tokens"].cpu().numpy()[sel]
@@ -61,14 +66,14 @@ def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
     g_flags = got["flags"].cpu().numpy()[sel] if "flags" in got else None
     margin = ref["margin"]
     ok = margin >= BOUNDARY
-    n_boundary = int((~ok).sum())
-    bad = np.nonzero(ok & ((g_len != ref["accepted_len"]) | np.any(g_tok != ref["tokens"], axis=1)))[0]
+    mism = (g_len != ref["accepted_len"]) | np.any(g_tok != ref["tokens"], axis=1)
+    if g_flags is not None:
+        mism |= np.any(g_flags != ref["flags"], axis=1)
+    bad = np.nonzero(ok & mism)[0]
     assert bad.size == 0, (
         f"{what}: {bad.size} non-boundary mismatches, first b={bad[:5]}: "
         f"gpu len {g_len[bad[:3]]} tok {g_tok[bad[:3]]} | oracle len {ref['accepted_len'][bad[:3]]} "
         f"tok {ref['tokens'][bad[:3]]} margin {margin[bad[:3]]}")
-    if g_flags is not None:
-        assert np.array_equal(g_flags[ok], ref["flags"][ok]), what
     gate = w.gate.cpu().numpy()[sel].astype(bool)
     keep = np.ones_like(g_alpha, dtype=bool)
     if gate.any():
@@ -77,4 +82,15 @@ def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
         keep &= ~(gate[:, None] & (np.abs(qd - tau) < BOUNDARY))
     np.testing.assert_allclose(g_alpha[keep], ref["alpha"][keep], rtol=ALPHA_RTOL, atol=ALPHA_ATOL,
                                err_msg=what)
-    return int(ok.sum()), n_boundary
+    valid = ref["accepted_len"] >= 0
+    tested = np.where(valid, np.minimum(ref["accepted_len"] + 1, w.k), 0)
+    pick_bnd = ref["margin_pick"] < BOUNDARY
+    dec_bnd = ~ok & ~pick_bnd
+    stats = dict(compared=int(ok.sum()), boundary=int((~ok).sum()),
+                 boundary_decision=int(dec_bnd.sum()), boundary_pick=int(pick_bnd.sum()),
+                 boundary_mismatch=int((~ok & mism).sum()),
+                 draws=int((tested + valid).sum()))
+    print(f"[parity] {what}: {stats}")
+    assert stats["boundary_decision"] <= 1e-5 * stats["draws"] + 2, (what, stats)
+    assert stats["boundary_mismatch"] <= 0.1 * max(stats["boundary"], 1) + 1, (what, stats)
+    return stats

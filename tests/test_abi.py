@@ -44,7 +44,7 @@ def test_status_strings_and_launch_count(library):
     assert sv.spec_verify_status_string(0) == "ok"
     assert sv.spec_verify_status_string(1) == "invalid argument"
     assert "unknown" in sv.spec_verify_status_string(99)
-    assert sv.spec_verify_launches_per_run() == 1
+    assert sv.spec_verify_launches_per_run() == 2
 
 
 def test_init_rejects_bad_sizes_before_touching_the_device(library):

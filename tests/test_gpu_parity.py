@@ -61,8 +61,7 @@ def test_parity_small_shapes_ragged_tails(sv, dtype, V):
     ver = _verifier(sv, w)
     out = _run(sv, ver, w, row_stats=True)
     ref = oracle_for(w)
-    n, nb = compare(w, out, ref, what=f"V={V} {dtype}")
-    assert n >= B - 2
+    compare(w, out, ref, what=f"V={V} {dtype}")
     rs = out["row_stats"].cpu().numpy().astype(np.float64)
     np.testing.assert_allclose(rs[..., 0], ref["row_stats"][..., 0], rtol=1e-6, atol=1e-6)
     np.testing.assert_allclose(rs[..., 1], ref["row_stats"][..., 1], rtol=1e-5, atol=1e-5)
@@ -124,9 +123,9 @@ def test_tiny_config_1e5_trials_bit_exact_and_chi_square(sv, gated):
     cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
     out = _run(sv, ver, w, counters=cnt)
     ref = oracle_for(w)
-    ncmp, nbnd = compare(w, out, ref, what=f"tiny gated={gated}")
-    draws = int((np.minimum(ref["accepted_len"] + 1, 3) + 1).sum())  # u0 per tested position + u1
-    assert nbnd < max(1, 1e-5 * draws) + 3
+    st = compare(w, out, ref, what=f"tiny gated={gated}")
+    # V = 8: every boundary kind is rare; all of them together stay under 1e-5 of draws
+    assert st["boundary"] <= 1e-5 * st["draws"] + 3
     # emitted tokens at position 0 follow p_0 (Pearson, alpha = 1e-4, dof 7)
     p0 = torch.softmax(Lt[0, 0].double() / base.T, dim=-1).cpu().numpy()
     tok0 = out["tokens"][:, 0].cpu().numpy()
@@ -168,8 +167,7 @@ def test_full_size_configs(sv, name, B, sample):
         rng = np.random.default_rng(7)
         idx = np.sort(rng.choice(w.B, size=sample, replace=False))
         ref = oracle_for(w, idx=idx)
-    n, nb = compare(w, out, ref, idx=idx, what=name)
-    assert n >= (w.B if idx is None else len(idx)) - 2
+    compare(w, out, ref, idx=idx, what=name)
     # whole-batch invariants at full size
     al = out["accepted_len"].cpu().numpy()
     tok = out["tokens"].cpu().numpy()
