@@ -294,6 +294,9 @@ def main():
     n_mark = args.steps
     marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
              for _ in range(n_mark)]
+    for a, b in marks:  # torch creates the CUDA events on their first record
+        a.record(stream)
+        b.record(stream)
     torch.cuda.synchronize(dev)
     for i in range(n_mark):
         ver.mark_next(*marks[i])

@@ -94,8 +94,9 @@ enum {
 #define SV_MAX_V (1 << 22)     /* vocabulary size */
 
 /* Create a verifier for batches of up to max_B sequences, k draft positions and
- * vocabulary V on CUDA device `device`.  Allocates the device workspace
- * (about max_B * (2k+1) * ceil(V / 8192) * 8 bytes plus candidate lists).
+ * vocabulary V on CUDA device `device`.  Allocates the device workspace:
+ * max_B * (2k+1) * ceil(V / 2048) * 8 bytes of chunk statistics plus
+ * max_B * k * ceil(V / 2048) * 32 bytes of gate-candidate slots.
  * Returns SV_EINVAL for max_B < 1, k < 1 or V < 1, SV_EUNSUPPORTED beyond
  * SV_MAX_K / SV_MAX_V, SV_ENOMEM or SV_ECUDA on CUDA failures; *out is set to
  * NULL on any error. */

@@ -21,9 +21,9 @@ struct spec_verify_s {
   size_t ws_bytes = 0;
   float2* part = nullptr;
   float* xD = nullptr;
-  float* cand_v = nullptr;
-  int* cand_i = nullptr;
-  unsigned* cand_n = nullptr;
+  sv::Cand* cand = nullptr;
+  unsigned* cand_over = nullptr;
+  unsigned* work = nullptr;
   // one-shot timing marks around the next stream pass
   cudaEvent_t mark_before = nullptr, mark_after = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
@@ -39,9 +39,10 @@ size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 
 bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
+// every warp of a stream CTA owns a ring of kDepth chunk stages
 template <typename TT, typename TD>
 constexpr int dyn_smem() {
-  return sv::Stages<TT, TD>::kDepth * sv::Stages<TT, TD>::kBytes;
+  return sv::Stages<TT, TD>::kWarpsPerCta * sv::Stages<TT, TD>::kDepth * sv::Stages<TT, TD>::kBytes;
 }
 
 // opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
@@ -50,18 +51,26 @@ cudaError_t configure(int* blocks_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(sv::finish_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(sizeof(sv::FinishShared)));
+  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::stream_kernel<TT, TD>,
-                                                       sv::kThreads, dyn_smem<TT, TD>());
+                                                       sv::Stages<TT, TD>::kThreadsPerCta,
+                                                       dyn_smem<TT, TD>());
 }
 
 template <typename TT, typename TD>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
-  if (grid > P.total_items) grid = P.total_items;
+  // a warp takes whole work units, so more than total_units / warps-per-CTA CTAs idle
+  const long long need = (static_cast<long long>(P.total_units) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
+                         sv::Stages<TT, TD>::kWarpsPerCta;
+  if (grid > need) grid = need;
   if (grid < 1) grid = 1;
   const bool marked = h->mark_before != nullptr;
   if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
-  sv::stream_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::kThreads, dyn_smem<TT, TD>(), st>>>(P);
+  sv::stream_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::Stages<TT, TD>::kThreadsPerCta,
+                              dyn_smem<TT, TD>(), st>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
   if (marked) {
     const cudaError_t e = cudaEventRecord(h->mark_after, st);
@@ -71,9 +80,11 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaSt
   // the finishing pass: one CTA per sequence, allowed to launch while the
   // stream pass drains; it waits (griddepcontrol.wait) before reading its output
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(P.B));
-  cfg.blockDim = dim3(sv::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  // one CTA per sequence up to two per SM; larger batches loop (warm instruction cache)
+  const int fin_grid = P.B < 2 * h->num_sms ? P.B : 2 * h->num_sms;
+  cfg.gridDim = dim3(static_cast<unsigned>(fin_grid));
+  cfg.blockDim = dim3(sv::kFinThreads);
+  cfg.dynamicSmemBytes = sizeof(sv::FinishShared);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -160,9 +171,10 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   size_t off = 0;
   const size_t o_part = off; off = align_up(off + n_part * sizeof(float2), 256);
   const size_t o_xd = off;   off = align_up(off + static_cast<size_t>(max_B) * rows * sizeof(float), 256);
-  const size_t o_cv = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(float), 256);
-  const size_t o_ci = off;   off = align_up(off + n_rowc * sv::kRowCap * sizeof(int), 256);
-  const size_t o_cn = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
+  const size_t n_cand = n_rowc * h->nchunk * sv::kTopM;
+  const size_t o_cd = off;   off = align_up(off + n_cand * sizeof(sv::Cand), 256);
+  const size_t o_co = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
+  const size_t o_wk = off;   off = align_up(off + sizeof(unsigned), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
@@ -171,10 +183,14 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   char* base = static_cast<char*>(h->ws);
   h->part = reinterpret_cast<float2*>(base + o_part);
   h->xD = reinterpret_cast<float*>(base + o_xd);
-  h->cand_v = reinterpret_cast<float*>(base + o_cv);
-  h->cand_i = reinterpret_cast<int*>(base + o_ci);
-  h->cand_n = reinterpret_cast<unsigned*>(base + o_cn);
-  if (cudaMemset(h->ws, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  h->cand = reinterpret_cast<sv::Cand*>(base + o_cd);
+  h->cand_over = reinterpret_cast<unsigned*>(base + o_co);
+  h->work = reinterpret_cast<unsigned*>(base + o_wk);
+  // everything starts at zero except the candidate slots, which start empty
+  // (all bits set: token id -1); the finishing pass restores both after use
+  if (cudaMemset(h->ws, 0, off) != cudaSuccess ||
+      cudaMemset(h->cand, 0xFF, n_cand * sizeof(sv::Cand)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->ws);
     delete h;
     return SV_ECUDA;
@@ -214,10 +230,11 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.V = V;
   P.nchunk = h->nchunk;
   P.rows = 2 * k + 1;
-  P.items_per_seq = P.rows * h->nchunk;
-  const long long total = static_cast<long long>(B) * P.items_per_seq;
+  P.nunit = (h->nchunk + sv::kUnit - 1) / sv::kUnit;
+  P.units_per_seq = P.rows * P.nunit;
+  const long long total = static_cast<long long>(B) * P.units_per_seq;
   if (total >= (1ll << 31)) return SV_EUNSUPPORTED;
-  P.total_items = static_cast<unsigned>(total);
+  P.total_units = static_cast<unsigned>(total);
   P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.T = temperature;
   P.gate_default = gate_mode == SV_GATED_MU ? 1 : 0;
@@ -236,9 +253,9 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.row_stats = row_stats;
   P.part = h->part;
   P.xD = h->xD;
-  P.cand_v = h->cand_v;
-  P.cand_i = h->cand_i;
-  P.cand_n = h->cand_n;
+  P.cand = h->cand;
+  P.cand_over = h->cand_over;
+  P.work = h->work;
   const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
   const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
   P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);

@@ -2,20 +2,19 @@
 //
 // A call is two launches on one stream:
 //
-// stream_kernel -- the bandwidth-bound pass.  Work is a list of items (sequence
-//   b, row r, chunk c), where rows 0..k are the target rows and rows k+1..2k the
-//   draft rows of b and a chunk is kChunk = 8192 consecutive vocabulary entries.
-//   Persistent CTAs take items round-robin through a cp.async pipeline of S
-//   chunk stages in shared memory (16-byte copies, each warp moving 512
-//   contiguous bytes per instruction; every thread later reads back exactly the
-//   pieces it copied, so the pipeline needs no barrier of its own).  Per item
-//   it reads the chunk once and publishes the chunk statistics of the
-//   temperature softmax (mlxcel PR #992, "What changed": p and q are
-//   full-vocabulary temperature softmaxes in fp32), the logit at the drafted
-//   token when that token lies in the chunk, and -- for draft rows of gated
-//   sequences -- the tokens whose in-chunk probability reaches the gate (at
-//   most floor(1/threshold) per chunk, a superset of the tokens the gate
-//   admits) appended to a per-row candidate list.
+// stream_kernel -- the bandwidth-bound pass.  Rows are cut into chunks of
+//   kChunk = 2048 vocabulary entries; rows 0..k of a sequence are its target
+//   rows, rows k+1..2k its draft rows.  Every warp works on its own: it takes
+//   work units of kUnit consecutive chunks of one row from a global counter (one
+//   atomic per unit, in sequence-major order), streams them through a private
+//   cp.async ring of S chunk stages in shared memory (each lane copies and later
+//   reads back its own 16-byte slots, so no barrier is involved anywhere), and
+//   per chunk publishes the chunk statistics of the temperature softmax
+//   (mlxcel PR #992, "What changed": p and q are full-vocabulary temperature
+//   softmaxes in fp32), the logit at the drafted token when that token lies in
+//   the chunk, and -- for draft rows of gated sequences -- the tokens whose
+//   in-chunk probability reaches the gate (at most floor(1/threshold) of them, a
+//   superset of the tokens the gate admits).
 //
 // finish_kernel -- one CTA per sequence, launched as a programmatic dependent
 //   launch so that its start-up overlaps the end of the stream pass.  It
@@ -47,12 +46,9 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kEPT = 32;                    // entries per thread per chunk
-constexpr int kChunk = kThreads * kEPT;     // vocabulary entries per work item
-constexpr int kTopM = 4;                    // gate candidates per chunk / admitted tokens per row
-constexpr int kRowCap = 64;                 // gate candidates kept per draft row
+constexpr int kChunk = 2048;                // vocabulary entries per chunk statistic
+constexpr int kUnit = 4;                    // chunks per work unit (one atomic fetch)
+constexpr int kTopM = 4;                    // gate candidate slots per chunk / admitted tokens per row
 constexpr int kMaxChunks = (SV_MAX_V + kChunk - 1) / kChunk;
 constexpr int kMaxRows = 2 * SV_MAX_K + 1;
 constexpr float kBoundary = 1e-6f;
@@ -61,12 +57,17 @@ constexpr float kBoundary = 1e-6f;
 // slack * threshold * (kTopM + 1) > 1, i.e. threshold > ~0.2002.
 constexpr float kGateSlack = 1.0f - 1.0f / 1024.0f;
 
+struct Cand {  // a gate candidate: raw logit and token id (id -1: empty slot)
+  float x;
+  int v;
+};
+
 struct Params {
   const void* Lt;  // [B, k+1, V]
   const void* Ld;  // [B, k, V]
   const int32_t* D;
-  int B, k, V, nchunk, rows, items_per_seq;
-  unsigned total_items;
+  int B, k, V, nchunk, rows, nunit, units_per_seq;
+  unsigned total_units;
   float c;     // log2(e) / T, rounded once
   float T;
   int gate_default;
@@ -85,9 +86,9 @@ struct Params {
   // workspace
   float2* part;        // [B, rows, nchunk] (mc, s) per chunk
   float* xD;           // [B, rows] raw logit at the drafted token (rows j < k and draft rows)
-  float* cand_v;       // [B, k, kRowCap] raw logits of gate candidates
-  int* cand_i;         // [B, k, kRowCap] their token ids
-  unsigned* cand_n;    // [B, k] candidates appended (> kRowCap: overflow); reset by the finisher
+  Cand* cand;          // [B, k, nchunk, kTopM] gate candidates of draft rows; emptied by the finisher
+  unsigned* cand_over; // [B, k] a chunk had more than kTopM candidates; cleared by the finisher
+  unsigned* work;      // [1] next work unit to hand out; reset by the finishing pass
   int vec_t, vec_d;    // rows allow 16-byte vector loads
 };
 
@@ -99,6 +100,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -130,26 +135,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+__device__ __forceinline__ int warp_excl_scan_int(int v, int lane, int& total) {
+  int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
   }
-  return v;
-}
-__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - v;
 }
 
 // one logit as float
@@ -200,59 +194,76 @@ __device__ __forceinline__ bool gate_fast_path(float tau) {
   return tau * kGateSlack * static_cast<float>(kTopM + 1) > 1.0f;
 }
 
+__device__ __forceinline__ bool seq_gated(const Params& P, int b) {
+  return P.gate_per_seq ? (P.gate_per_seq[b] != 0) : (P.gate_default != 0);
+}
+__device__ __forceinline__ float seq_tau(const Params& P, int b) {
+  return P.tau_per_seq ? P.tau_per_seq[b] : P.tau_default;
+}
+
 // ------------------------------------------------------- chunk registers
 //
-// Thread t = 32 w + l owns NV 16-byte slots of the chunk: slot i is vector
-// index w * 32 NV + 32 i + l.  bf16: 4 slots of 8 entries kept packed; f32: 8
-// slots of 4.  A slot that lies wholly inside the row of an aligned tensor
-// travels by cp.async into the stage; other slots (ragged tail, unaligned
-// rows) are read directly, entries past V reading as -inf.
+// A warp holds one chunk: lane l owns NV 16-byte slots, slot i being vector
+// index 32 i + l of the chunk (each copy instruction of the warp moves 512
+// contiguous bytes).  bf16 entries stay packed in pairs.  The stage always ends
+// up holding the whole chunk: 16-byte slots inside the row arrive by cp.async,
+// slots past V are filled with -inf, and a partial last slot -- or every slot
+// of a row that is not 16-byte aligned -- is read directly.
 
-template <typename T> struct Chunk;
+template <typename T> struct Lane;
 
-template <> struct Chunk<uint16_t> {
-  static constexpr int kNV = 4, kVE = 8;
-  uint32_t w[16];
+template <> struct Lane<uint16_t> {
+  static constexpr int kVE = 8;
+  static constexpr int kNV = kChunk / 32 / kVE;  // 8 slots, 64 entries
+  uint32_t w[4 * kNV];
   __device__ __forceinline__ static void issue(const uint16_t* row, unsigned char* stage, int c0, int V,
-                                               int warp, int lane) {
+                                               bool vec, int lane) {
+    if (vec && c0 + kChunk <= V) {
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      const int sv = warp * 32 * kNV + 32 * i + lane;
-      const int v0 = c0 + sv * kVE;
-      if (v0 + kVE <= V) cp_async16(stage + sv * 16, row + v0);
+      for (int i = 0; i < kNV; ++i) cp_async16(stage + (32 * i + lane) * 16, row + c0 + (32 * i + lane) * kVE);
+      return;
     }
-  }
-  __device__ __forceinline__ void load(const uint16_t* row, const unsigned char* stage, int c0, int V,
-                                       bool vec, int warp, int lane) {
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < kNV; ++i) {
-      const int sv = warp * 32 * kNV + 32 * i + lane;
+      const int sv = 32 * i + lane;
       const int v0 = c0 + sv * kVE;
       if (vec && v0 + kVE <= V) {
-        const uint4 u = *reinterpret_cast<const uint4*>(stage + sv * 16);
-        w[4 * i + 0] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+        cp_async16(stage + sv * 16, row + v0);
       } else {
+        uint32_t t[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int a = v0 + 2 * q;
           const uint32_t lo = a < V ? static_cast<uint32_t>(__ldg(row + a)) : 0xFF80u;
           const uint32_t hi = a + 1 < V ? static_cast<uint32_t>(__ldg(row + a + 1)) : 0xFF80u;
-          w[4 * i + q] = lo | (hi << 16);
+          t[q] = lo | (hi << 16);
         }
+        *reinterpret_cast<uint4*>(stage + sv * 16) = make_uint4(t[0], t[1], t[2], t[3]);
       }
     }
   }
-  __device__ __forceinline__ float max() const {
-    uint32_t m = w[0];
+  __device__ __forceinline__ void load(const unsigned char* stage, int lane) {
 #pragma unroll
-    for (int q = 1; q < 16; ++q) m = bmax2(m, w[q]);
+    for (int i = 0; i < kNV; ++i) {
+      const uint4 u = *reinterpret_cast<const uint4*>(stage + (32 * i + lane) * 16);
+      w[4 * i + 0] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+    }
+  }
+  __device__ __forceinline__ float max() const {
+    uint32_t m0 = w[0], m1 = w[1];
+#pragma unroll
+    for (int q = 2; q < 4 * kNV; q += 2) {
+      m0 = bmax2(m0, w[q]);
+      m1 = bmax2(m1, w[q + 1]);
+    }
+    const uint32_t m = bmax2(m0, m1);
     return fmaxf(bf16_lo(m), bf16_hi(m));
   }
   // sum_v exp2(fma(x_v, c, nmc)), four independent accumulators
   __device__ __forceinline__ float expsum(float c, float nmc) const {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (int q = 0; q < 16; q += 2) {
+    for (int q = 0; q < 4 * kNV; q += 2) {
       a0 += ex2_approx(fmaf(bf16_lo(w[q]), c, nmc));
       a1 += ex2_approx(fmaf(bf16_hi(w[q]), c, nmc));
       a2 += ex2_approx(fmaf(bf16_lo(w[q + 1]), c, nmc));
@@ -260,51 +271,54 @@ template <> struct Chunk<uint16_t> {
     }
     return (a0 + a1) + (a2 + a3);
   }
-  template <typename F>
-  __device__ __forceinline__ void for_each(int c0, int warp, int lane, F&& f) const {
+  // entries x of slot i with fma(x, c, nmc) >= lts, as a bit mask
+  __device__ __forceinline__ unsigned slot_hits(int i, float c, float nmc, float lts) const {
+    unsigned m = 0;
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      const int v0 = c0 + (warp * 32 * kNV + 32 * i + lane) * kVE;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        f(v0 + 2 * q, bf16_lo(w[4 * i + q]));
-        f(v0 + 2 * q + 1, bf16_hi(w[4 * i + q]));
-      }
+    for (int q = 0; q < 4; ++q) {
+      m |= (fmaf(bf16_lo(w[4 * i + q]), c, nmc) >= lts ? 1u : 0u) << (2 * q);
+      m |= (fmaf(bf16_hi(w[4 * i + q]), c, nmc) >= lts ? 1u : 0u) << (2 * q + 1);
     }
+    return m;
   }
 };
 
-template <> struct Chunk<float> {
-  static constexpr int kNV = 8, kVE = 4;
-  float x[32];
+template <> struct Lane<float> {
+  static constexpr int kVE = 4;
+  static constexpr int kNV = kChunk / 32 / kVE;  // 16 slots, 64 entries
+  float x[4 * kNV];
   __device__ __forceinline__ static void issue(const float* row, unsigned char* stage, int c0, int V,
-                                               int warp, int lane) {
+                                               bool vec, int lane) {
+    if (vec && c0 + kChunk <= V) {
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      const int sv = warp * 32 * kNV + 32 * i + lane;
-      const int v0 = c0 + sv * kVE;
-      if (v0 + kVE <= V) cp_async16(stage + sv * 16, row + v0);
+      for (int i = 0; i < kNV; ++i) cp_async16(stage + (32 * i + lane) * 16, row + c0 + (32 * i + lane) * kVE);
+      return;
     }
-  }
-  __device__ __forceinline__ void load(const float* row, const unsigned char* stage, int c0, int V,
-                                       bool vec, int warp, int lane) {
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < kNV; ++i) {
-      const int sv = warp * 32 * kNV + 32 * i + lane;
+      const int sv = 32 * i + lane;
       const int v0 = c0 + sv * kVE;
       if (vec && v0 + kVE <= V) {
-        const float4 u = *reinterpret_cast<const float4*>(stage + sv * 16);
-        x[4 * i + 0] = u.x; x[4 * i + 1] = u.y; x[4 * i + 2] = u.z; x[4 * i + 3] = u.w;
+        cp_async16(stage + sv * 16, row + v0);
       } else {
+        float t[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) x[4 * i + e] = v0 + e < V ? __ldg(row + v0 + e) : -INFINITY;
+        for (int e = 0; e < 4; ++e) t[e] = v0 + e < V ? __ldg(row + v0 + e) : -INFINITY;
+        *reinterpret_cast<float4*>(stage + sv * 16) = make_float4(t[0], t[1], t[2], t[3]);
       }
+    }
+  }
+  __device__ __forceinline__ void load(const unsigned char* stage, int lane) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+      const float4 u = *reinterpret_cast<const float4*>(stage + (32 * i + lane) * 16);
+      x[4 * i + 0] = u.x; x[4 * i + 1] = u.y; x[4 * i + 2] = u.z; x[4 * i + 3] = u.w;
     }
   }
   __device__ __forceinline__ float max() const {
     float m0 = fmaxf(x[0], x[1]), m1 = fmaxf(x[2], x[3]);
 #pragma unroll
-    for (int e = 4; e < 32; e += 4) {
+    for (int e = 4; e < 4 * kNV; e += 4) {
       m0 = fmaxf(m0, fmaxf(x[e], x[e + 1]));
       m1 = fmaxf(m1, fmaxf(x[e + 2], x[e + 3]));
     }
@@ -313,7 +327,7 @@ template <> struct Chunk<float> {
   __device__ __forceinline__ float expsum(float c, float nmc) const {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 32; e += 4) {
+    for (int e = 0; e < 4 * kNV; e += 4) {
       a0 += ex2_approx(fmaf(x[e], c, nmc));
       a1 += ex2_approx(fmaf(x[e + 1], c, nmc));
       a2 += ex2_approx(fmaf(x[e + 2], c, nmc));
@@ -321,192 +335,214 @@ template <> struct Chunk<float> {
     }
     return (a0 + a1) + (a2 + a3);
   }
-  template <typename F>
-  __device__ __forceinline__ void for_each(int c0, int warp, int lane, F&& f) const {
+  __device__ __forceinline__ unsigned slot_hits(int i, float c, float nmc, float lts) const {
+    unsigned m = 0;
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-      const int v0 = c0 + (warp * 32 * kNV + 32 * i + lane) * kVE;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) f(v0 + e, x[4 * i + e]);
-    }
+    for (int e = 0; e < 4; ++e) m |= (fmaf(x[4 * i + e], c, nmc) >= lts ? 1u : 0u) << e;
+    return m;
   }
 };
-
-__device__ __forceinline__ bool seq_gated(const Params& P, int b) {
-  return P.gate_per_seq ? (P.gate_per_seq[b] != 0) : (P.gate_default != 0);
-}
-__device__ __forceinline__ float seq_tau(const Params& P, int b) {
-  return P.tau_per_seq ? P.tau_per_seq[b] : P.tau_default;
-}
 
 // ------------------------------------------------------- stream kernel
 
+// launch shape of the stream pass: 4 independent warps per CTA, each with a
+// ring of kDepth chunk stages
 template <typename TT, typename TD>
 struct Stages {
+  static constexpr int kWarpsPerCta = 4;
+  static constexpr int kThreadsPerCta = 32 * kWarpsPerCta;
   static constexpr int kBytes = kChunk * static_cast<int>(sizeof(TT) > sizeof(TD) ? sizeof(TT) : sizeof(TD));
-  static constexpr int kDepth = kBytes <= 16384 ? 4 : 3;
-  static constexpr int kMinBlocks = kBytes <= 16384 ? 3 : 2;
+  static constexpr int kDepth = 3;
+  static constexpr int kMinBlocks = kBytes <= 4096 ? 4 : 2;
 };
 
-struct StreamShared {
-  __align__(16) float red_max[kWarps];
-  __align__(16) float red_sum[kWarps];
-  int ncand;
-  float cand_v[kTopM];
-  int cand_i[kTopM];
+constexpr int kURing = 8;  // work units known to a warp: being consumed, being issued, fetched
+
+struct WarpQueue {
+  int4 unit[kURing];  // (b, r, first chunk, chunk count); count 0 = no more work
+  int d[kURing];      // the drafted token of the unit's row (rows j < k), copied asynchronously
 };
 
-__device__ __forceinline__ void decode_item(const Params& P, unsigned item, int& b, int& r, int& ch) {
-  b = static_cast<int>(item / static_cast<unsigned>(P.items_per_seq));
-  const int rem = static_cast<int>(item - static_cast<unsigned>(b) * P.items_per_seq);
-  r = rem / P.nchunk;
-  ch = rem - r * P.nchunk;
+// lane 0: decode a work-unit index; count 0 past the end of the work
+__device__ __forceinline__ int4 decode_unit(const Params& P, unsigned u) {
+  if (u >= P.total_units) return make_int4(0, 0, 0, 0);
+  const int b = static_cast<int>(u / static_cast<unsigned>(P.units_per_seq));
+  const int rem = static_cast<int>(u - static_cast<unsigned>(b) * P.units_per_seq);
+  const int r = rem / P.nunit;
+  const int c0 = (rem - r * P.nunit) * kUnit;
+  const int n = P.nchunk - c0 < kUnit ? P.nchunk - c0 : kUnit;
+  return make_int4(b, r, c0, n);
 }
 
-template <typename TT, typename TD>
-__device__ __forceinline__ void issue_item(const Params& P, unsigned item, unsigned char* stage,
-                                           int warp, int lane) {
-  int b, r, ch;
-  decode_item(P, item, b, r, ch);
-  const int c0 = ch * kChunk;
-  if (r <= P.k) {
-    if (P.vec_t)
-      Chunk<TT>::issue(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V,
-                       stage, c0, P.V, warp, lane);
-  } else {
-    if (P.vec_d)
-      Chunk<TD>::issue(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V,
-                       stage, c0, P.V, warp, lane);
+// lane 0: put work unit `slot` of the warp's queue in place (decode it and
+// start the asynchronous copy of its drafted token)
+__device__ __forceinline__ void enqueue_unit(const Params& P, WarpQueue& Q, int slot, unsigned u) {
+  const int4 q = decode_unit(P, u);
+  Q.unit[slot] = q;
+  if (q.w > 0) {
+    const int j = q.y <= P.k ? q.y : q.y - P.k - 1;
+    if (j < P.k) cp_async4(&Q.d[slot], P.D + static_cast<int64_t>(q.x) * P.k + j);
   }
 }
 
-// one work item: chunk statistics, drafted-token logit, gate candidates
+template <typename TT, typename TD>
+__device__ __forceinline__ void issue_chunk(const Params& P, int b, int r, int ch, unsigned char* stage,
+                                            int lane) {
+  const int c0 = ch * kChunk;
+  if (r <= P.k)
+    Lane<TT>::issue(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V,
+                    stage, c0, P.V, P.vec_t != 0, lane);
+  else
+    Lane<TD>::issue(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V,
+                    stage, c0, P.V, P.vec_d != 0, lane);
+}
+
+// entry o of a staged chunk as float
 template <typename T>
-__device__ __forceinline__ void process_item(const Params& P, StreamShared& sh, const T* row,
-                                             const unsigned char* stage, int b, int r, int ch,
-                                             bool is_draft, int tid, int warp, int lane) {
+__device__ __forceinline__ float stage_logit(const unsigned char* stage, int o) {
+  if constexpr (sizeof(T) == 2)
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[o]) << 16);
+  else
+    return reinterpret_cast<const float*>(stage)[o];
+}
+
+// one chunk, by one warp: statistics, drafted-token logit, gate candidates
+template <typename T>
+__device__ __forceinline__ void process_chunk(const Params& P, const unsigned char* stage, int b, int r,
+                                              int ch, int d, int lane) {
   const int k = P.k;
   const int c0 = ch * kChunk;
-  const bool vec = is_draft ? P.vec_d != 0 : P.vec_t != 0;
+  const bool is_draft = r > k;
   const int j = is_draft ? r - k - 1 : r;
-  int d = -1;
-  if (tid == 0 && j < k) d = __ldg(P.D + static_cast<int64_t>(b) * k + j);
 
-  Chunk<T> regs;
-  regs.load(row, stage, c0, P.V, vec, warp, lane);
+  Lane<T> regs;
+  regs.load(stage, lane);
+  // each lane sums against its own reference fl(m_l c); the warp then merges
   const float mine = regs.max();
-  const float mw = warp_max(mine);
-  if (lane == 0) sh.red_max[warp] = mw;
-  __syncthreads();
-  const float4 ma = *reinterpret_cast<const float4*>(&sh.red_max[0]);
-  const float4 mb = *reinterpret_cast<const float4*>(&sh.red_max[4]);
-  const float m_c = fmaxf(fmaxf(fmaxf(ma.x, ma.y), fmaxf(ma.z, ma.w)), fmaxf(fmaxf(mb.x, mb.y), fmaxf(mb.z, mb.w)));
-  // scaled reference: mc = fl(m c); an all -inf chunk uses 0 so that -inf entries give 0
-  const float mc = m_c == -INFINITY ? -INFINITY : m_c * P.c;
-  const float nmc = m_c == -INFINITY ? 0.f : -mc;
-  const float s_t = warp_sum(regs.expsum(P.c, nmc));
-  if (lane == 0) sh.red_sum[warp] = s_t;
-  __syncthreads();
-  const float4 sa = *reinterpret_cast<const float4*>(&sh.red_sum[0]);
-  const float4 sb = *reinterpret_cast<const float4*>(&sh.red_sum[4]);
-  const float s_c = ((sa.x + sa.y) + (sa.z + sa.w)) + ((sb.x + sb.y) + (sb.z + sb.w));
+  const float mct = mine == -INFINITY ? -INFINITY : mine * P.c;
+  float s_l = regs.expsum(P.c, mine == -INFINITY ? 0.f : -mct);
+  const float mc = warp_max(mct);
+  s_l = mct == -INFINITY ? s_l * 0.f : s_l * ex2_approx(mct - mc);
+  const float s = warp_sum(s_l);
+  if (lane == 0) P.part[(static_cast<int64_t>(b) * P.rows + r) * P.nchunk + ch] = make_float2(mc, s);
 
-  bool want_cand = false;
-  if (is_draft) {
-    const float tau = seq_tau(P, b);
-    want_cand = seq_gated(P, b) && gate_fast_path(tau);
-    if (want_cand) {
-      // in-chunk probability exp2(x c - mc) / s >= slack * tau: a superset of
-      // the admitted set (q <= in-chunk probability), at most 1/(slack tau) tokens
-      float thr = INFINITY;
-      if (s_c > 0.f && isfinite(s_c)) thr = (mc + log2f(tau * kGateSlack * s_c)) / P.c;
-      if (mine >= thr) {
-        regs.for_each(c0, warp, lane, [&](int v, float x) {
-          if (x >= thr && v < P.V) {
-            const int slot = atomicAdd(&sh.ncand, 1);
-            if (slot < kTopM) {
-              sh.cand_v[slot] = x;
-              sh.cand_i[slot] = v;
-            }
-          }
-        });
-      }
-      __syncthreads();
-    }
+  // the logit at the drafted token, written by the lane whose slot holds it
+  if (j < k && d >= c0 && d < c0 + kChunk && d < P.V) {
+    const int sv = (d - c0) / Lane<T>::kVE;
+    if ((sv & 31) == lane) P.xD[static_cast<int64_t>(b) * P.rows + r] = stage_logit<T>(stage, d - c0);
   }
 
-  if (tid == 0) {
-    const int R = P.rows;
-    P.part[(static_cast<int64_t>(b) * R + r) * P.nchunk + ch] = make_float2(mc, s_c);
-    if (d >= c0 && d < c0 + kChunk && d < P.V) {
-      constexpr int kVE = Chunk<T>::kVE;
-      const int v0 = d - (d - c0) % kVE;
-      float x;
-      if (vec && v0 + kVE <= P.V) {
-        if (sizeof(T) == 2)
-          x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[d - c0]) << 16);
-        else
-          x = reinterpret_cast<const float*>(stage)[d - c0];
-      } else {
-        x = logit_at<T>(row, d);
-      }
-      P.xD[static_cast<int64_t>(b) * R + r] = x;
-    }
-    if (want_cand) {
-      const int n = sh.ncand;
-      if (n > 0) {
-        const int64_t rowc = static_cast<int64_t>(b) * k + j;
-        const unsigned add = n > kTopM ? static_cast<unsigned>(kRowCap + 1) : static_cast<unsigned>(n);
-        const unsigned base = atomicAdd(P.cand_n + rowc, add);
-        if (n <= kTopM)
-          for (int s = 0; s < n; ++s)
-            if (base + s < static_cast<unsigned>(kRowCap)) {
-              P.cand_v[rowc * kRowCap + base + s] = sh.cand_v[s];
-              P.cand_i[rowc * kRowCap + base + s] = sh.cand_i[s];
+  if (is_draft) {
+    const float tau = seq_tau(P, b);
+    if (seq_gated(P, b) && gate_fast_path(tau) && s > 0.f && isfinite(s)) {
+      // a token's in-chunk probability exp2(fma(x, c, -mc)) / s reaches
+      // slack * tau iff fma(x, c, -mc) >= lts = log2(slack tau s); that set is a
+      // superset of the admitted tokens (q <= in-chunk probability) and holds
+      // at most 1/(slack tau) tokens.  lts <= 0 is needed for any token at all,
+      // which rules out almost every chunk at once (s is warp-uniform).
+      const float lts = log2f(tau * kGateSlack * s);
+      if (lts <= 0.f) {
+        // lanes whose own maximum could reach it (a small margin absorbs the
+        // rounding of mct - mc against the fused form)
+        const bool maybe = mct - mc >= lts - 1.0f / 256.0f;
+        int mine_n = 0;
+        unsigned hits[Lane<T>::kNV];
+#pragma unroll
+        for (int i = 0; i < Lane<T>::kNV; ++i) {
+          hits[i] = maybe ? regs.slot_hits(i, P.c, -mc, lts) : 0u;
+          mine_n += __popc(hits[i]);
+        }
+        int total;
+        int slot = warp_excl_scan_int(mine_n, lane, total);
+        const int64_t base = ((static_cast<int64_t>(b) * k + j) * P.nchunk + ch) * kTopM;
+        if (mine_n > 0) {
+#pragma unroll
+          for (int i = 0; i < Lane<T>::kNV; ++i) {
+            unsigned m = hits[i];
+            while (m) {
+              const int e = __ffs(m) - 1;
+              m &= m - 1;
+              // the value comes from the stage (a register array indexed by a
+              // run-time entry would go through local memory)
+              const int o = (32 * i + lane) * Lane<T>::kVE + e;
+              if (slot < kTopM) P.cand[base + slot] = Cand{stage_logit<T>(stage, o), c0 + o};
+              ++slot;
             }
+          }
+        }
+        if (lane == 0 && total > kTopM) P.cand_over[static_cast<int64_t>(b) * k + j] = 1u;
       }
-      sh.ncand = 0;
     }
   }
 }
 
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(kThreads, Stages<TT, TD>::kMinBlocks) stream_kernel(const Params P) {
+__global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
+    stream_kernel(const Params P) {
   constexpr int S = Stages<TT, TD>::kDepth;
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
-  __shared__ StreamShared sh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned total = P.total_items;
-  const unsigned G = gridDim.x;
+  __shared__ WarpQueue queues[Stages<TT, TD>::kWarpsPerCta];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* ring = stages + warp * S * kStage;
+  WarpQueue& Q = queues[warp];
   const int k = P.k;
-  if (tid == 0) sh.ncand = 0;
 
-  // prologue: the first S - 1 items of this CTA in flight
-#pragma unroll
-  for (int s = 0; s < S - 1; ++s) {
-    const unsigned item = blockIdx.x + static_cast<unsigned>(s) * G;
-    if (item < total) issue_item<TT, TD>(P, item, stages + s * kStage, warp, lane);
-    cp_async_commit();
+  // the warp's work: its first two units are fixed (warp g of G takes units g
+  // and G + g, so the start needs no atomics and neighbouring warps read
+  // neighbouring memory); later units come from a global counter counting
+  // from 2G.  Lane 0 keeps one fetch in flight beyond the two units it has
+  // queued; units are consumed chunk by chunk, and chunks are issued S - 1
+  // ahead of their use.
+  const unsigned G = gridDim.x * Stages<TT, TD>::kWarpsPerCta;
+  const unsigned g = blockIdx.x * Stages<TT, TD>::kWarpsPerCta + warp;
+  unsigned pending = 0;
+  if (lane == 0) {
+    enqueue_unit(P, Q, 0, g);
+    enqueue_unit(P, Q, 1, G + g);
+    pending = 2 * G + atomicAdd(P.work, 1u);
   }
-  int it = 0;
-  for (unsigned item = blockIdx.x; item < total; item += G, ++it) {
-    {
-      const unsigned nx = item + static_cast<unsigned>(S - 1) * G;
-      if (nx < total) issue_item<TT, TD>(P, nx, stages + ((it + S - 1) % S) * kStage, warp, lane);
-      cp_async_commit();
+  __syncwarp();
+  int iu = 0, ic = 0, issued = 0;  // issue cursor: unit, chunk within it
+  int cu = 0, cc = 0, used = 0;    // consume cursor
+  auto issue_next = [&]() {
+    const int4 u = Q.unit[iu % kURing];
+    if (u.w > 0) {
+      issue_chunk<TT, TD>(P, u.x, u.y, u.z + ic, ring + (issued % S) * kStage, lane);
+      ++issued;
+      if (++ic == u.w) {
+        ic = 0;
+        ++iu;
+        if (lane == 0) {  // unit iu + 1 enters the queue; the next fetch goes out
+          enqueue_unit(P, Q, (iu + 1) % kURing, pending);
+          pending = 2 * G + atomicAdd(P.work, 1u);
+        }
+      }
     }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int s = 0; s < S - 1; ++s) issue_next();
+  __syncwarp();
+  for (;;) {
+    const int4 u = Q.unit[cu % kURing];
+    if (u.w <= 0) break;
+    issue_next();
     cp_async_wait<S - 1>();
-    int b, r, ch;
-    decode_item(P, item, b, r, ch);
-    const unsigned char* stage = stages + (it % S) * kStage;
-    if (r <= k) {
-      const TT* row = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + r) * P.V;
-      process_item<TT>(P, sh, row, stage, b, r, ch, false, tid, warp, lane);
-    } else {
-      const TD* row = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + (r - k - 1)) * P.V;
-      process_item<TD>(P, sh, row, stage, b, r, ch, true, tid, warp, lane);
+    __syncwarp();
+    const unsigned char* stage = ring + (used % S) * kStage;
+    const int ch = u.z + cc;
+    const int d = Q.d[cu % kURing];
+    if (u.y <= k)
+      process_chunk<TT>(P, stage, u.x, u.y, ch, d, lane);
+    else
+      process_chunk<TD>(P, stage, u.x, u.y, ch, d, lane);
+    ++used;
+    if (++cc == u.w) {
+      cc = 0;
+      ++cu;
     }
+    __syncwarp();
   }
   cp_async_wait<0>();
   // let the finishing grid start its prologue; its griddepcontrol.wait still
@@ -515,36 +551,97 @@ __global__ void __launch_bounds__(kThreads, Stages<TT, TD>::kMinBlocks) stream_k
 }
 
 // ------------------------------------------------------------ finishing
+//
+// The finishing pass runs once per sequence over a long, mostly straight code
+// path, so it is written compactly (rolled loops, partials and residual
+// weights staged in shared memory).  Its sums are float-float (an fp32 pair
+// with ~2^-44 relative error, built from error-free two-sums): fp64 would be
+// as precise, but fp64 is a narrow, long-latency pipe on this part and this
+// path is all dependent steps.
+
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinPartCap = 4096;  // chunk statistics of a sequence staged in shared memory
+
+struct dfloat {
+  float hi, lo;
+};
+__device__ __forceinline__ dfloat df(float a) { return {a, 0.f}; }
+// error-free sum (Knuth's two-sum), renormalised
+__device__ __forceinline__ dfloat df_add(dfloat a, dfloat b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb) + (a.lo + b.lo);
+  const float hi = s + e;
+  return {hi, e - (hi - s)};
+}
+__device__ __forceinline__ dfloat df_sub(dfloat a, dfloat b) { return df_add(a, {-b.hi, -b.lo}); }
+__device__ __forceinline__ dfloat df_mul(dfloat a, float b) {
+  const float p = a.hi * b;
+  const float e = fmaf(a.lo, b, fmaf(a.hi, b, -p));
+  const float hi = p + e;
+  return {hi, e - (hi - p)};
+}
+__device__ __forceinline__ bool df_lt(dfloat a, dfloat b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ bool df_le(dfloat a, dfloat b) { return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo); }
+__device__ __forceinline__ float df_f(dfloat a) { return a.hi + a.lo; }
+__device__ __forceinline__ dfloat shfl_xor_df(dfloat v, int o) {
+  return {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ dfloat shfl_up_df(dfloat v, int o) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ dfloat shfl_df(dfloat v, int src) {
+  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+__device__ __forceinline__ dfloat warp_sum_df(dfloat v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
+  return v;
+}
+__device__ __forceinline__ dfloat warp_incl_scan_df(dfloat v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const dfloat n = shfl_up_df(v, o);
+    if (lane >= o) v = df_add(v, n);
+  }
+  return v;
+}
 
 struct FinishShared {
+  float2 part[kFinPartCap];  // the sequence's chunk statistics (when they fit)
+  float tile[kMaxChunks];    // residual mass of every chunk of the stop row
   float rowM[kMaxRows];      // scaled row max Mc
   float rowInvS[kMaxRows];
-  double rowS[kMaxRows];
+  dfloat rowS[kMaxRows];
   float xD[kMaxRows];
   int Dv[SV_MAX_K];
-  unsigned candn[SV_MAX_K];
-  double tile[kMaxChunks];
-  double wbase[kWarps];
-  float wtot[kWarps];
+  dfloat wtot[kFinWarps];
+  dfloat wbase[kFinWarps];
+  int wlast[kFinWarps];
   int bad;
   int jstar;
   int stop_flag;
   int boundary;
   unsigned overflow_rows;
   int tstar;
-  double before;
+  int degenerate;
+  int mode;
+  dfloat before;
+  dfloat Z;
+  dfloat y;
+  float u1;
   int pick;
-  int last_pos;
   int nadm[SV_MAX_K];
   int adm_i[SV_MAX_K][kTopM];
   float adm_q[SV_MAX_K][kTopM];
   float adm_p[SV_MAX_K][kTopM];
 };
 
-// residual weight of token v with target logit xt (and draft logit xd in the
-// dense mode).  mode 0: p (bonus row, or degenerate residual); mode 1: p, or
-// max(0, p - q) on the admitted list; mode 2: max(0, p - mu) with mu from the
-// draft logit (mu = q, or q on q >= tau in gated mode).
+// residual weights of eight consecutive entries [v0, v0 + 8).  mode 0: p (bonus
+// row, or degenerate residual); mode 1: p, or max(0, p - q) on the admitted
+// list; mode 2: max(0, p - mu) with mu from the draft logits (mu = q, or q on
+// q >= tau in gated mode).  Entries past V weigh 0.
 struct ResidualEval {
   int mode;
   float Mt, invSt, Md, invSd, c, tau;
@@ -552,19 +649,33 @@ struct ResidualEval {
   int nadm;
   const int* adm_i;
   const float* adm_q;
-  __device__ __forceinline__ float operator()(int v, float xt, float xd) const {
-    const float p = prob_of(xt, Mt, c, invSt);
-    if (mode == 0) return p;
-    if (mode == 1) {
-      for (int a = 0; a < nadm; ++a)
-        if (adm_i[a] == v) return fmaxf(p - adm_q[a], 0.f);
-      return p;
-    }
-    const float q = prob_of(xd, Md, c, invSd);
-    const float mu = (!gated || q >= tau) ? q : 0.f;
-    return fmaxf(p - mu, 0.f);
-  }
 };
+
+__device__ __forceinline__ void residual8(const ResidualEval& e, const float (&xt)[8], const float (&xd)[8],
+                                          int v0, int V, float (&r)[8]) {
+  if (e.mode == 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float p = prob_of(xt[i], e.Mt, e.c, e.invSt);
+      const float q = prob_of(xd[i], e.Md, e.c, e.invSd);
+      const float mu = (!e.gated || q >= e.tau) ? q : 0.f;
+      r[i] = v0 + i < V ? fmaxf(p - mu, 0.f) : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = v0 + i < V ? prob_of(xt[i], e.Mt, e.c, e.invSt) : 0.f;
+    if (e.mode == 1) {
+      for (int a = 0; a < e.nadm; ++a) {
+        const int o = e.adm_i[a] - v0;
+        if (o >= 0 && o < 8) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i == o) r[i] = fmaxf(r[i] - e.adm_q[a], 0.f);
+        }
+      }
+    }
+  }
+}
 
 template <typename TT, typename TD>
 __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
@@ -577,95 +688,90 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   const uint64_t s_idx = P.seq_offset + static_cast<uint64_t>(b);
   const TT* Lt = static_cast<const TT*>(P.Lt);
   const TD* Ld = static_cast<const TD*>(P.Ld);
+  const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
+  const bool staged = R * nch <= kFinPartCap;
 
-  // phase A: everything the decisions need, in one round of loads
+  // phase A: what the decisions need, in one round of loads
   if (tid == 0) {
     sh.bad = (gated && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
     sh.boundary = 0;
     sh.pick = -1;
-    sh.last_pos = -1;
     sh.overflow_rows = 0u;
   }
   if (tid < R) sh.xD[tid] = __ldcg(P.xD + static_cast<int64_t>(b) * R + tid);
   if (tid < k) {
     sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
-    sh.candn[tid] = fastgate ? __ldcg(P.cand_n + static_cast<int64_t>(b) * k + tid) : 0u;
     sh.nadm[tid] = 0;
   }
-  // candidate entries of every draft row, read before the counts are known
-  // (slots past kCandPerThread * kThreads, i.e. k > 8, are read in phase B)
-  constexpr int kCandPerThread = 2;
-  float cv[kCandPerThread];
-  int ci[kCandPerThread];
-  if (fastgate) {
-#pragma unroll
-    for (int u = 0; u < kCandPerThread; ++u) {
-      const int e = tid + u * kThreads;
-      if (e < k * kRowCap) {
-        cv[u] = __ldcg(P.cand_v + static_cast<int64_t>(b) * k * kRowCap + e);
-        ci[u] = __ldcg(P.cand_i + static_cast<int64_t>(b) * k * kRowCap + e);
-      }
-    }
+  __syncthreads();
+  if (tid < k && fastgate && __ldcg(P.cand_over + static_cast<int64_t>(b) * k + tid)) {
+    atomicOr(&sh.overflow_rows, 1u << tid);
+    P.cand_over[static_cast<int64_t>(b) * k + tid] = 0u;
   }
-  // row statistics from the chunk statistics (fp64 accumulation)
-  for (int r = warp; r < R; r += kWarps) {
-    const float2* pr = P.part + (static_cast<int64_t>(b) * R + r) * nch;
+  if (staged) {
+#pragma unroll 4
+    for (int e = tid; e < R * nch; e += kFinThreads) sh.part[e] = ldcg_f2(seq_part + e);
+  }
+  __syncthreads();
+  auto part_at = [&](int r, int ch) -> float2 {
+    return staged ? sh.part[r * nch + ch] : ldcg_f2(seq_part + static_cast<int64_t>(r) * nch + ch);
+  };
+
+  // row statistics (a warp per row): merge the chunk (mc, s) pairs
+#pragma unroll 1
+  for (int r = warp; r < R; r += kFinWarps) {
     float M = -INFINITY;
-    for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, ldcg_f2(pr + ch).x);
+#pragma unroll 1
+    for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, part_at(r, ch).x);
     M = warp_max(M);
-    double S = 0.0;
+    dfloat S = df(0.f);
+#pragma unroll 1
     for (int ch = lane; ch < nch; ch += 32) {
-      const float2 ms = ldcg_f2(pr + ch);
-      S += (ms.x == -INFINITY) ? static_cast<double>(ms.y * 0.f)
-                               : static_cast<double>(ms.y) * static_cast<double>(exp2f(ms.x - M));
+      const float2 ms = part_at(r, ch);
+      S = df_add(S, df(ms.x == -INFINITY ? ms.y * 0.f : ms.y * exp2f(ms.x - M)));
     }
-    S = warp_sum_d(S);
+    S = warp_sum_df(S);
     if (lane == 0) {
       sh.rowM[r] = M;
       sh.rowS[r] = S;
-      sh.rowInvS[r] = static_cast<float>(1.0 / S);
-      if (M == -INFINITY || !isfinite(S) || !(S > 0.0)) sh.bad = 1;
+      // 1 / (hi + lo) to float precision
+      sh.rowInvS[r] = (1.f / S.hi) * (1.f - S.lo / S.hi);
+      if (M == -INFINITY || !isfinite(S.hi) || !(S.hi > 0.f)) sh.bad = 1;
       if (P.row_stats) {
         // (max, log-sum-exp) of L / T: Mc ln 2 and Mc ln 2 + ln S
-        const double mo = static_cast<double>(M) * 0.6931471805599453;
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = static_cast<float>(mo);
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = static_cast<float>(mo + log(S));
+        const float mo = M * 0.69314718f;
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = mo;
+        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = mo + (logf(S.hi) + S.lo / S.hi);
       }
     }
   }
   __syncthreads();
 
   // phase B: admitted tokens of every draft row and their target probability
-  // (one more round of loads, overlapping the decisions below)
-  if (fastgate && !sh.bad) {
-    auto admit = [&](int e, float x, int v) {
-      const int j = e / kRowCap, s = e - j * kRowCap;
-      const unsigned n = sh.candn[j];
-      if (n > static_cast<unsigned>(kRowCap)) {
-        if (s == 0) atomicOr(&sh.overflow_rows, 1u << j);
-        return;
-      }
-      if (s >= static_cast<int>(n)) return;
+  // (the candidate slots are emptied for the next call as they are read)
+  if (fastgate) {
+    Cand* sc = P.cand + static_cast<int64_t>(b) * k * nch * kTopM;
+#pragma unroll 4
+    for (int e = tid; e < k * nch * kTopM; e += kFinThreads) {
+      const Cand cd = sc[e];
+      if (cd.v < 0) continue;
+      sc[e].v = -1;
+      const int j = e / (nch * kTopM);
+      if (sh.bad || cd.v >= V) continue;
       const int rd = k + 1 + j;
-      const float q = prob_of(x, sh.rowM[rd], c, sh.rowInvS[rd]);
+      const float q = prob_of(cd.x, sh.rowM[rd], c, sh.rowInvS[rd]);
       if (q >= tau) {
         const int a = atomicAdd(&sh.nadm[j], 1);
         if (a < kTopM) {
-          const float xt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + j) * V, v);
-          sh.adm_i[j][a] = v;
+          const float xt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + j) * V, cd.v);
+          sh.adm_i[j][a] = cd.v;
           sh.adm_q[j][a] = q;
           sh.adm_p[j][a] = prob_of(xt, sh.rowM[j], c, sh.rowInvS[j]);
         } else {
           atomicOr(&sh.overflow_rows, 1u << j);
         }
       }
-    };
-#pragma unroll
-    for (int u = 0; u < kCandPerThread; ++u)
-      if (tid + u * kThreads < k * kRowCap) admit(tid + u * kThreads, cv[u], ci[u]);
-    for (int e = tid + kCandPerThread * kThreads; e < k * kRowCap; e += kThreads)
-      admit(e, __ldcg(P.cand_v + static_cast<int64_t>(b) * k * kRowCap + e),
-            __ldcg(P.cand_i + static_cast<int64_t>(b) * k * kRowCap + e));
+    }
   }
 
   // every draft position (one lane each): gate, mu, alpha, accept test
@@ -714,13 +820,13 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
       sh.stop_flag = jstar < k ? (((nullm >> jstar) & 1u) ? SV_FLAG_NULL : SV_FLAG_REJECT)
                                : SV_FLAG_ACCEPT;
       sh.boundary = __popc(nearm);
+      sh.u1 = P.u1 ? P.u1[b] : philox_uniform(P.seed, s_idx, static_cast<uint32_t>(jstar), 1u);
     }
   }
   __syncthreads();
 
   const int jstar = sh.jstar;
   int32_t* tok = P.tokens + static_cast<int64_t>(b) * (k + 1);
-  if (fastgate && tid < k) P.cand_n[static_cast<int64_t>(b) * k + tid] = 0u;  // ready for the next call
   if (sh.bad) {
     if (tid <= k) tok[tid] = -1;
     if (tid == 0) {
@@ -737,184 +843,183 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   int mode = 0;
   if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
   const int nadm = mode == 1 ? min(sh.nadm[jstar], kTopM) : 0;
-
-  const ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
-                        jstar < k ? sh.rowM[rd] : 0.f, jstar < k ? sh.rowInvS[rd] : 0.f,
-                        c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
-                        jstar < k ? sh.adm_q[jstar] : sh.adm_q[0]};
-
-  auto chunk_sums_from_partials = [&](int use_mode) {
-    const float2* pr = P.part + (static_cast<int64_t>(b) * R + rt) * nch;
-    for (int ch = tid; ch < nch; ch += kThreads) {
-      const float2 ms = ldcg_f2(pr + ch);
-      double t = (ms.x == -INFINITY)
-                     ? 0.0
-                     : static_cast<double>(ms.y) * static_cast<double>(exp2f(ms.x - ev.Mt)) *
-                           (1.0 / sh.rowS[rt]);
-      if (use_mode == 1) {
-        for (int a = 0; a < nadm; ++a)
-          if (sh.adm_i[jstar][a] / kChunk == ch)
-            t -= static_cast<double>(fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]));
-        if (t < 0.0) t = 0.0;
-      }
-      sh.tile[ch] = t;
-    }
-  };
+  ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
+                  jstar < k ? sh.rowM[rd] : 0.f, jstar < k ? sh.rowInvS[rd] : 0.f,
+                  c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
+                  jstar < k ? sh.adm_q[jstar] : sh.adm_q[0]};
+  const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
+  constexpr int kLaneGroups = kChunk / 8 / 32;  // 8-entry groups per lane when a warp reads a chunk
 
   if (mode == 2) {
-    // dense: one re-read of the stop row pair, a warp per chunk
-    for (int ch = warp; ch < nch; ch += kWarps) {
-      float acc = 0.f;
+    // dense: one re-read of the stop row pair, a warp per chunk (each lane
+    // 8-entry groups lane, lane + 32, ...: 16-byte coalesced loads, all issued
+    // before use); no barrier until every chunk is summed
+#pragma unroll 1
+    for (int ch = warp; ch < nch; ch += kFinWarps) {
       const int c0 = ch * kChunk;
-#pragma unroll 4
-      for (int u = 0; u < kChunk / 8 / 32; ++u) {
-        const int v0 = c0 + (u * 32 + lane) * 8;
-        if (v0 < V) {
-          float xt[8], xd[8];
-          load8<TT>(trow, v0, V, P.vec_t != 0, xt);
-          load8<TD>(drow, v0, V, P.vec_d != 0, xd);
+      float acc = 0.f;
+#pragma unroll 1
+      for (int h = 0; h < kLaneGroups; h += 4) {
+        float xt[4][8], xd[4][8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (v0 + e < V) acc += ev(v0 + e, xt[e], xd[e]);
+        for (int u = 0; u < 4; ++u) {
+          load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
+          load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float rr[8];
+          residual8(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
+          acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
         }
       }
-      const double t = warp_sum_d(static_cast<double>(acc));
-      if (lane == 0) sh.tile[ch] = t;
+      acc = warp_sum(acc);
+      if (lane == 0) sh.tile[ch] = acc;
     }
-  } else {
-    chunk_sums_from_partials(mode);
-  }
-  __syncthreads();
-
-  // total mass; a residual without mass falls back to p
-  double Z;
-  {
-    double z = 0.0;
-    for (int ch = lane; ch < nch; ch += 32) z += sh.tile[ch];
-    Z = warp_sum_d(z);
-  }
-  int degenerate = 0;
-  ResidualEval ev2 = ev;
-  if (!(Z > 0.0)) {
     __syncthreads();
-    chunk_sums_from_partials(0);
-    __syncthreads();
-    double z = 0.0;
-    for (int ch = lane; ch < nch; ch += 32) z += sh.tile[ch];
-    Z = warp_sum_d(z);
-    ev2.mode = 0;
-    degenerate = 1;
   }
 
-  const float u1 = P.u1 ? P.u1[b] : philox_uniform(P.seed, s_idx, static_cast<uint32_t>(jstar), 1u);
-  const double y = static_cast<double>(u1) * Z;
-
-  // the chunk holding y: first chunk whose inclusive prefix exceeds y
+  // warp 0: chunk sums (from the chunk statistics in modes 0 / 1), the total
+  // mass Z (a residual without mass falls back to p), and the chunk holding
+  // y = u1 Z: the first chunk whose inclusive prefix exceeds y
   if (warp == 0) {
-    double carry = 0.0;
-    int found = -1;
-    double before = 0.0;
-    for (int g0 = 0; g0 < nch && found < 0; g0 += 32) {
+    const float invS = sh.rowInvS[rt];
+    auto chunk_sums = [&](int use_mode) {
+#pragma unroll 1
+      for (int ch = lane; ch < nch; ch += 32) {
+        const float2 ms = part_at(rt, ch);
+        float t = ms.x == -INFINITY ? 0.f : ms.y * exp2f(ms.x - ev.Mt) * invS;
+        if (use_mode == 1) {
+          for (int a = 0; a < nadm; ++a)
+            if (sh.adm_i[jstar][a] / kChunk == ch) t -= fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]);
+          t = fmaxf(t, 0.f);
+        }
+        sh.tile[ch] = t;
+      }
+      __syncwarp();
+    };
+    auto total = [&]() {
+      dfloat z = df(0.f);
+#pragma unroll 1
+      for (int ch = lane; ch < nch; ch += 32) z = df_add(z, df(sh.tile[ch]));
+      return warp_sum_df(z);
+    };
+    if (mode != 2) chunk_sums(mode);
+    dfloat Z = total();
+    int degenerate = 0;
+    if (!(Z.hi > 0.f)) {
+      chunk_sums(0);
+      Z = total();
+      degenerate = 1;
+    }
+    const dfloat y = df_mul(Z, sh.u1);
+    dfloat carry = df(0.f), before = df(0.f);
+    int found = -1, last = -1;
+#pragma unroll 1
+    for (int g0 = 0; g0 < nch; g0 += 32) {
       const int ch = g0 + lane;
-      const double t = ch < nch ? sh.tile[ch] : 0.0;
-      const double incl = warp_incl_scan_d(t, lane) + carry;
-      const unsigned m = __ballot_sync(0xffffffffu, ch < nch && incl > y);
-      if (m) {
+      const float t = ch < nch ? sh.tile[ch] : 0.f;
+      if (t > 0.f) last = ch;
+      const dfloat incl = df_add(warp_incl_scan_df(df(t), lane), carry);
+      const unsigned m = __ballot_sync(0xffffffffu, ch < nch && df_lt(y, incl));
+      if (found < 0 && m) {
         const int src = __ffs(m) - 1;
         found = g0 + src;
-        before = __shfl_sync(0xffffffffu, incl - t, src);
+        before = shfl_df(df_sub(incl, df(t)), src);
       }
-      carry = __shfl_sync(0xffffffffu, incl, 31);
+      carry = shfl_df(incl, 31);
     }
-    if (found < 0) {
-      // rounding left y at or past the total: take the last chunk with mass
-      int last = -1;
-      for (int ch = lane; ch < nch; ch += 32)
-        if (sh.tile[ch] > 0.0) last = ch;
-      for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (found < 0) {  // rounding left y at or past the total: the last chunk with mass
       found = last < 0 ? 0 : last;
-      before = INFINITY;  // forces the last-positive fallback inside the chunk
+      before = df(INFINITY);  // forces the last-positive fallback inside the chunk
     }
     if (lane == 0) {
       sh.tstar = found;
       sh.before = before;
+      sh.Z = Z;
+      sh.y = y;
+      sh.degenerate = degenerate;
+      sh.mode = degenerate ? 0 : mode;
     }
   }
   __syncthreads();
+  ev.mode = sh.mode;
 
-  // one re-read of the chosen chunk: thread i owns entries [c0 + 32 i, c0 + 32 i + 32)
+  // one re-read of the chosen chunk: thread i evaluates entries [8 i, 8 i + 8)
+  const int c0 = sh.tstar * kChunk;
+  const int e0 = tid * 8;
+  float r8[8];
   {
-    const int c0 = sh.tstar * kChunk;
-    const int e0 = c0 + tid * kEPT;
-    const double yl = y - sh.before;
-    float r[kEPT];
+    float xt[8], xd[8];
+    load8<TT>(trow, c0 + e0, V, vt, xt);
+    if (ev.mode == 2) load8<TD>(drow, c0 + e0, V, vd, xd);
+    residual8(ev, xt, xd, c0 + e0, V, r8);
+  }
+
+  // block scan: thread i owns entries [8 i, 8 i + 8) of the chunk.  Thread i's
+  // range is [lo_i, hi_i) with lo_{i+1} == hi_i bit for bit (the same
+  // float-float sums), so exactly one thread claims any y below the chunk total.
+  {
+    int lastpos = -1;
+    float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-    for (int g = 0; g < kEPT / 8; ++g) {
-      float xt[8], xd[8];
-      load8<TT>(trow, e0 + 8 * g, V, P.vec_t != 0, xt);
-      if (ev2.mode == 2) load8<TD>(drow, e0 + 8 * g, V, P.vec_d != 0, xd);
+    for (int e = 0; e < 8; ++e) {
+      if (e & 1) t1 += r8[e]; else t0 += r8[e];
+      if (r8[e] > 0.f) lastpos = c0 + e0 + e;
+    }
+    const dfloat tot = df_add(df(t0), df(t1));
+    const dfloat wincl = warp_incl_scan_df(tot, lane);
+    dfloat wexcl = shfl_up_df(wincl, 1);
+    if (lane == 0) wexcl = df(0.f);
+    int wl = lastpos;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int v = e0 + 8 * g + e;
-        r[8 * g + e] = v < V ? ev2(v, xt[e], ev2.mode == 2 ? xd[e] : 0.f) : 0.f;
+    for (int o = 16; o > 0; o >>= 1) wl = max(wl, __shfl_xor_sync(0xffffffffu, wl, o));
+    if (lane == 31) sh.wtot[warp] = wincl;
+    if (lane == 0) sh.wlast[warp] = wl;
+    __syncthreads();
+    if (tid == 0) {
+      dfloat base = df(0.f);
+      for (int w = 0; w < kFinWarps; ++w) {
+        sh.wbase[w] = base;
+        base = df_add(base, sh.wtot[w]);
       }
     }
-    // per-thread total (pairwise), warp scan in fp32, block offsets in fp64.
-    // Thread i's range is [lo_i, hi_i) with lo_{i+1} == hi_i bit for bit, so
-    // exactly one thread claims any y below the chunk total.
-    float pw[kEPT / 2];
-#pragma unroll
-    for (int e = 0; e < kEPT / 2; ++e) pw[e] = r[2 * e] + r[2 * e + 1];
-#pragma unroll
-    for (int w = kEPT / 4; w >= 1; w >>= 1)
-#pragma unroll
-      for (int e = 0; e < w; ++e) pw[e] = pw[2 * e] + pw[2 * e + 1];
-    const float tot = pw[0];
-    const float wincl = warp_incl_scan(tot, lane);
-    float wexcl = __shfl_up_sync(0xffffffffu, wincl, 1);
-    if (lane == 0) wexcl = 0.f;
-    if (lane == 31) sh.wtot[warp] = wincl;
     __syncthreads();
-    if (lane == 0) {
-      double base = 0.0;
-      for (int w = 0; w < warp; ++w) base += static_cast<double>(sh.wtot[w]);
-      sh.wbase[warp] = base;
-    }
-    __syncwarp();
-    const double wbase = sh.wbase[warp];
-    const double lo = wbase + static_cast<double>(wexcl), hi = wbase + static_cast<double>(wincl);
-    int lastpos = -1;
-#pragma unroll
-    for (int e = 0; e < kEPT; ++e)
-      if (r[e] > 0.f) lastpos = e0 + e;
-    if (lo <= yl && yl < hi) {
-      const float target = static_cast<float>(yl - lo);
+    const dfloat wbase = sh.wbase[warp];
+    const dfloat lo = df_add(wbase, wexcl), hi = df_add(wbase, wincl);
+    const dfloat yl = df_sub(sh.y, sh.before);
+    if (df_le(lo, yl) && df_lt(yl, hi)) {
+      const float target = df_f(df_sub(yl, lo));
       float run = 0.f, prev = 0.f;
       int pick = lastpos;  // rounding inside the thread: its last positive entry
       bool hit = false;
-      for (int e = 0; e < kEPT; ++e) {
-        prev = run;
-        run += r[e];
-        if (run > target) {
-          pick = e0 + e;
-          hit = true;
-          break;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (!hit) {
+          prev = run;
+          run += r8[e];
+          if (run > target) {
+            pick = c0 + e0 + e;
+            hit = true;
+          }
         }
       }
-      if (!hit) prev = run = static_cast<float>(hi - lo);
+      if (!hit) prev = run = df_f(df_sub(hi, lo));
       sh.pick = pick;
-      const double cl = (sh.before + lo + static_cast<double>(prev)) / Z;
-      const double chh = (sh.before + lo + static_cast<double>(run)) / Z;
-      if (fabs(u1 - cl) < kBoundary || fabs(u1 - chh) < kBoundary) sh.boundary += 1;
+      const float Zf = df_f(sh.Z);
+      const float cl = df_f(df_add(df_add(sh.before, lo), df(prev))) / Zf;
+      const float chh = df_f(df_add(df_add(sh.before, lo), df(run))) / Zf;
+      if (fabsf(sh.u1 - cl) < kBoundary || fabsf(sh.u1 - chh) < kBoundary) sh.boundary += 1;
     }
-    atomicMax(&sh.last_pos, lastpos);
   }
   __syncthreads();
 
   if (tid == 0) {
     int pick = sh.pick;
     if (pick < 0) {
-      pick = sh.last_pos;
+      for (int w = 0; w < kFinWarps; ++w) pick = max(pick, sh.wlast[w]);
       sh.boundary += 1;
     }
     P.accepted_len[b] = jstar;
@@ -928,7 +1033,7 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
         atomicAdd(P.counters + SV_CNT_BONUS, 1ull);
       }
       if (sh.boundary) atomicAdd(P.counters + SV_CNT_BOUNDARY, static_cast<unsigned long long>(sh.boundary));
-      if (degenerate) atomicAdd(P.counters + SV_CNT_DEGENERATE, 1ull);
+      if (sh.degenerate) atomicAdd(P.counters + SV_CNT_DEGENERATE, 1ull);
     }
   }
   if (tid < jstar) tok[tid] = sh.Dv[tid];
@@ -936,11 +1041,17 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
 }
 
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const Params P) {
-  __shared__ FinishShared sh;
+__global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char fin_smem[];
+  FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
   // wait for the stream pass (programmatic dependent launch) before reading its output
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  finish_sequence<TT, TD>(P, blockIdx.x, sh);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *P.work = 0u;  // the stream pass's unit counter
+#pragma unroll 1
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    finish_sequence<TT, TD>(P, b, sh);
+    __syncthreads();
+  }
 }
 
 }  // namespace sv

@@ -162,7 +162,10 @@ class SpecVerifier:
             pass
 
     def mark_next(self, ev_before: torch.cuda.Event, ev_after: torch.cuda.Event):
-        """Time the next call's stream pass with two torch CUDA events (enable_timing=True)."""
+        """Time the next call's stream pass with two torch CUDA events (enable_timing=True,
+        already recorded once so that torch has created them)."""
+        if not ev_before.cuda_event or not ev_after.cuda_event:
+            raise ValueError("record both events once before passing them (torch creates them lazily)")
         rc = spec_verify_mark_next(self.handle, ev_before.cuda_event, ev_after.cuda_event)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_mark_next")
