@@ -23,7 +23,6 @@ struct spec_verify_s {
   float* xD = nullptr;
   sv::Cand* cand = nullptr;
   unsigned* cand_over = nullptr;
-  unsigned* work = nullptr;
   // one-shot timing marks around the next stream pass
   cudaEvent_t mark_before = nullptr, mark_after = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
@@ -62,8 +61,8 @@ cudaError_t configure(int* blocks_per_sm) {
 template <typename TT, typename TD>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
-  // a warp takes whole work units, so more than total_units / warps-per-CTA CTAs idle
-  const long long need = (static_cast<long long>(P.total_units) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
+  // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
+  const long long need = (static_cast<long long>(P.total_chunks) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
                          sv::Stages<TT, TD>::kWarpsPerCta;
   if (grid > need) grid = need;
   if (grid < 1) grid = 1;
@@ -174,7 +173,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   const size_t n_cand = n_rowc * h->nchunk * sv::kTopM;
   const size_t o_cd = off;   off = align_up(off + n_cand * sizeof(sv::Cand), 256);
   const size_t o_co = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
-  const size_t o_wk = off;   off = align_up(off + sizeof(unsigned), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
@@ -185,7 +183,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   h->xD = reinterpret_cast<float*>(base + o_xd);
   h->cand = reinterpret_cast<sv::Cand*>(base + o_cd);
   h->cand_over = reinterpret_cast<unsigned*>(base + o_co);
-  h->work = reinterpret_cast<unsigned*>(base + o_wk);
   // everything starts at zero except the candidate slots, which start empty
   // (all bits set: token id -1); the finishing pass restores both after use
   if (cudaMemset(h->ws, 0, off) != cudaSuccess ||
@@ -230,11 +227,11 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.V = V;
   P.nchunk = h->nchunk;
   P.rows = 2 * k + 1;
-  P.nunit = (h->nchunk + sv::kUnit - 1) / sv::kUnit;
-  P.units_per_seq = P.rows * P.nunit;
-  const long long total = static_cast<long long>(B) * P.units_per_seq;
+  const long long total = static_cast<long long>(B) * P.rows * h->nchunk;
   if (total >= (1ll << 31)) return SV_EUNSUPPORTED;
-  P.total_units = static_cast<unsigned>(total);
+  P.total_chunks = static_cast<unsigned>(total);
+  P.div_nchunk = sv::make_fastdiv(static_cast<unsigned>(h->nchunk));
+  P.div_rows = sv::make_fastdiv(static_cast<unsigned>(P.rows));
   P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.T = temperature;
   P.gate_default = gate_mode == SV_GATED_MU ? 1 : 0;
@@ -255,7 +252,6 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.xD = h->xD;
   P.cand = h->cand;
   P.cand_over = h->cand_over;
-  P.work = h->work;
   const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
   const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
   P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);

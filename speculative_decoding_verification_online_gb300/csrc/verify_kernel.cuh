@@ -4,16 +4,16 @@
 //
 // stream_kernel -- the bandwidth-bound pass.  Rows are cut into chunks of
 //   kChunk = 2048 vocabulary entries; rows 0..k of a sequence are its target
-//   rows, rows k+1..2k its draft rows.  Every warp works on its own: it takes
-//   work units of kUnit consecutive chunks of one row from a global counter (one
-//   atomic per unit, in sequence-major order), streams them through a private
-//   cp.async ring of S chunk stages in shared memory (each lane copies and later
-//   reads back its own 16-byte slots, so no barrier is involved anywhere), and
-//   per chunk publishes the chunk statistics of the temperature softmax
-//   (mlxcel PR #992, "What changed": p and q are full-vocabulary temperature
-//   softmaxes in fp32), the logit at the drafted token when that token lies in
-//   the chunk, and -- for draft rows of gated sequences -- the tokens whose
-//   in-chunk probability reaches the gate (at most floor(1/threshold) of them, a
+//   rows, rows k+1..2k its draft rows.  One CTA per SM; every warp works on
+//   its own: it takes its CTA's chunks one at a time from a shared-memory
+//   counter, streams them through a private cp.async ring of S chunk stages
+//   in shared memory (each lane copies and later reads back its own 16-byte
+//   slots, so no barrier is involved after the start), and per
+//   chunk publishes the chunk statistics of the temperature softmax (mlxcel PR
+//   #992, "What changed": p and q are full-vocabulary temperature softmaxes in
+//   fp32), the logit at the drafted token when that token lies in the chunk,
+//   and -- for draft rows of gated sequences -- the tokens whose in-chunk
+//   probability reaches the gate (at most floor(1/threshold) of them, a
 //   superset of the tokens the gate admits).
 //
 // finish_kernel -- one CTA per sequence, launched as a programmatic dependent
@@ -47,7 +47,6 @@
 namespace sv {
 
 constexpr int kChunk = 2048;                // vocabulary entries per chunk statistic
-constexpr int kUnit = 4;                    // chunks per work unit (one atomic fetch)
 constexpr int kTopM = 4;                    // gate candidate slots per chunk / admitted tokens per row
 constexpr int kMaxChunks = (SV_MAX_V + kChunk - 1) / kChunk;
 constexpr int kMaxRows = 2 * SV_MAX_K + 1;
@@ -62,12 +61,31 @@ struct Cand {  // a gate candidate: raw logit and token id (id -1: empty slot)
   int v;
 };
 
+// floor(n / d) for a divisor fixed per call, as a multiply-high and a shift
+// (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the round-up variant): with s = ceil(log2 d)
+// and m = floor(2^32 (2^s - d) / d) + 1, floor(n / d) = (mulhi(n, m) + n) >> s
+// for every 32-bit n.
+struct FastDiv {
+  unsigned d, m, s;
+};
+__host__ __device__ inline FastDiv make_fastdiv(unsigned d) {
+  unsigned s = 0;
+  while ((1ull << s) < d) ++s;
+  const unsigned long long m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  return FastDiv{d, static_cast<unsigned>(m), s};
+}
+__device__ __forceinline__ unsigned fastdiv(unsigned n, const FastDiv& f) {
+  return static_cast<unsigned>((static_cast<unsigned long long>(__umulhi(n, f.m)) + n) >> f.s);
+}
+
 struct Params {
   const void* Lt;  // [B, k+1, V]
   const void* Ld;  // [B, k, V]
   const int32_t* D;
-  int B, k, V, nchunk, rows, nunit, units_per_seq;
-  unsigned total_units;
+  int B, k, V, nchunk, rows;
+  unsigned total_chunks;  // B * rows * nchunk
+  FastDiv div_nchunk, div_rows;
   float c;     // log2(e) / T, rounded once
   float T;
   int gate_default;
@@ -88,7 +106,6 @@ struct Params {
   float* xD;           // [B, rows] raw logit at the drafted token (rows j < k and draft rows)
   Cand* cand;          // [B, k, nchunk, kTopM] gate candidates of draft rows; emptied by the finisher
   unsigned* cand_over; // [B, k] a chunk had more than kTopM candidates; cleared by the finisher
-  unsigned* work;      // [1] next work unit to hand out; reset by the finishing pass
   int vec_t, vec_d;    // rows allow 16-byte vector loads
 };
 
@@ -349,40 +366,57 @@ template <> struct Lane<float> {
 // ring of kDepth chunk stages
 template <typename TT, typename TD>
 struct Stages {
-  static constexpr int kWarpsPerCta = 4;
-  static constexpr int kThreadsPerCta = 32 * kWarpsPerCta;
   static constexpr int kBytes = kChunk * static_cast<int>(sizeof(TT) > sizeof(TD) ? sizeof(TT) : sizeof(TD));
   static constexpr int kDepth = 3;
-  static constexpr int kMinBlocks = kBytes <= 4096 ? 4 : 2;
+  // one CTA per SM holding 192 KB of rings: 16 warps of 4 KB stages (bf16
+  // rows), 8 warps of 8 KB stages otherwise
+  static constexpr int kWarpsPerCta = kBytes <= 4096 ? 16 : 8;
+  static constexpr int kThreadsPerCta = 32 * kWarpsPerCta;
+  static constexpr int kMinBlocks = 1;
 };
 
-constexpr int kURing = 8;  // work units known to a warp: being consumed, being issued, fetched
+// ---- work distribution
+//
+// The stream pass's work is the list of all chunks, sequence-major: chunk
+// index x = (b * rows + r) * nchunk + ch.  The grid holds one CTA per SM, and
+// CTA c owns chunks c, c + NC, c + 2 NC, ... (NC CTAs), so the grid sweeps
+// memory front to back and every SM gets the same share.  Inside a CTA the
+// warps take the CTA's chunks one at a time from a shared-memory counter.
+// Measured on this part: SMs given equal shares finish within about a
+// microsecond of each other, while warps on one SM drift apart by several, so
+// balancing is needed inside the SM only; no global atomics are involved (a
+// stream of global atomics issued alongside the logits traffic sees replies
+// delayed by tens of microseconds).
+
+constexpr int kItemRing = 8;       // decoded chunks known to a warp (in flight or next)
+constexpr unsigned kNoWork = 0xffffffffu;
 
 struct WarpQueue {
-  int4 unit[kURing];  // (b, r, first chunk, chunk count); count 0 = no more work
-  int d[kURing];      // the drafted token of the unit's row (rows j < k), copied asynchronously
+  int4 item[kItemRing];  // (b, r, ch, 1) of a chunk to stream; w = 0: no more work
+  int d[kItemRing];      // the drafted token of the chunk's row (rows j < k), copied asynchronously
 };
 
-// lane 0: decode a work-unit index; count 0 past the end of the work
-__device__ __forceinline__ int4 decode_unit(const Params& P, unsigned u) {
-  if (u >= P.total_units) return make_int4(0, 0, 0, 0);
-  const int b = static_cast<int>(u / static_cast<unsigned>(P.units_per_seq));
-  const int rem = static_cast<int>(u - static_cast<unsigned>(b) * P.units_per_seq);
-  const int r = rem / P.nunit;
-  const int c0 = (rem - r * P.nunit) * kUnit;
-  const int n = P.nchunk - c0 < kUnit ? P.nchunk - c0 : kUnit;
-  return make_int4(b, r, c0, n);
+// lane 0: the warp's next chunk index, or kNoWork
+__device__ __forceinline__ unsigned next_chunk(const Params& P, unsigned* cta_next) {
+  const unsigned i = atomicAdd(cta_next, 1u);
+  const unsigned long long x = blockIdx.x + static_cast<unsigned long long>(i) * gridDim.x;
+  return x < P.total_chunks ? static_cast<unsigned>(x) : kNoWork;
 }
 
-// lane 0: put work unit `slot` of the warp's queue in place (decode it and
-// start the asynchronous copy of its drafted token)
-__device__ __forceinline__ void enqueue_unit(const Params& P, WarpQueue& Q, int slot, unsigned u) {
-  const int4 q = decode_unit(P, u);
-  Q.unit[slot] = q;
-  if (q.w > 0) {
-    const int j = q.y <= P.k ? q.y : q.y - P.k - 1;
-    if (j < P.k) cp_async4(&Q.d[slot], P.D + static_cast<int64_t>(q.x) * P.k + j);
+// lane 0: decode chunk index x into item slot `slot` and start the copy of
+// its drafted token
+__device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot, unsigned x) {
+  if (x == kNoWork) {
+    Q.item[slot] = make_int4(0, 0, 0, 0);
+    return;
   }
+  const unsigned rg = fastdiv(x, P.div_nchunk);
+  const int ch = static_cast<int>(x - rg * static_cast<unsigned>(P.nchunk));
+  const unsigned b = fastdiv(rg, P.div_rows);
+  const int r = static_cast<int>(rg - b * static_cast<unsigned>(P.rows));
+  Q.item[slot] = make_int4(static_cast<int>(b), r, ch, 1);
+  const int j = r <= P.k ? r : r - P.k - 1;
+  if (j < P.k) cp_async4(&Q.d[slot], P.D + static_cast<int64_t>(b) * P.k + j);
 }
 
 template <typename TT, typename TD>
@@ -483,65 +517,43 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
   __shared__ WarpQueue queues[Stages<TT, TD>::kWarpsPerCta];
+  __shared__ unsigned cta_next;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* ring = stages + warp * S * kStage;
   WarpQueue& Q = queues[warp];
   const int k = P.k;
 
-  // the warp's work: its first two units are fixed (warp g of G takes units g
-  // and G + g, so the start needs no atomics and neighbouring warps read
-  // neighbouring memory); later units come from a global counter counting
-  // from 2G.  Lane 0 keeps one fetch in flight beyond the two units it has
-  // queued; units are consumed chunk by chunk, and chunks are issued S - 1
-  // ahead of their use.
-  const unsigned G = gridDim.x * Stages<TT, TD>::kWarpsPerCta;
-  const unsigned g = blockIdx.x * Stages<TT, TD>::kWarpsPerCta + warp;
-  unsigned pending = 0;
-  if (lane == 0) {
-    enqueue_unit(P, Q, 0, g);
-    enqueue_unit(P, Q, 1, G + g);
-    pending = 2 * G + atomicAdd(P.work, 1u);
-  }
+  // item n (the warp's n-th chunk) is decoded at step n - 1, issued into ring
+  // slot n % S at step n (S - 1 steps ahead of its use) and consumed at loop
+  // iteration n; the copy of its drafted token rides in the commit group of
+  // step n - 1, so it has landed when the chunk has.
+  if (threadIdx.x == 0) cta_next = 0u;
+  __syncthreads();
+  if (lane == 0) put_item(P, Q, 0, next_chunk(P, &cta_next));
   __syncwarp();
-  int iu = 0, ic = 0, issued = 0;  // issue cursor: unit, chunk within it
-  int cu = 0, cc = 0, used = 0;    // consume cursor
+  int issued = 0;
   auto issue_next = [&]() {
-    const int4 u = Q.unit[iu % kURing];
-    if (u.w > 0) {
-      issue_chunk<TT, TD>(P, u.x, u.y, u.z + ic, ring + (issued % S) * kStage, lane);
-      ++issued;
-      if (++ic == u.w) {
-        ic = 0;
-        ++iu;
-        if (lane == 0) {  // unit iu + 1 enters the queue; the next fetch goes out
-          enqueue_unit(P, Q, (iu + 1) % kURing, pending);
-          pending = 2 * G + atomicAdd(P.work, 1u);
-        }
-      }
-    }
+    const int4 it = Q.item[issued % kItemRing];
+    if (it.w > 0) issue_chunk<TT, TD>(P, it.x, it.y, it.z, ring + (issued % S) * kStage, lane);
+    if (lane == 0) put_item(P, Q, (issued + 1) % kItemRing, it.w > 0 ? next_chunk(P, &cta_next) : kNoWork);
+    ++issued;
     cp_async_commit();
+    __syncwarp();
   };
 #pragma unroll
   for (int s = 0; s < S - 1; ++s) issue_next();
-  __syncwarp();
-  for (;;) {
-    const int4 u = Q.unit[cu % kURing];
-    if (u.w <= 0) break;
+  for (int n = 0;; ++n) {
+    const int4 it = Q.item[n % kItemRing];
+    if (it.w <= 0) break;
     issue_next();
     cp_async_wait<S - 1>();
     __syncwarp();
-    const unsigned char* stage = ring + (used % S) * kStage;
-    const int ch = u.z + cc;
-    const int d = Q.d[cu % kURing];
-    if (u.y <= k)
-      process_chunk<TT>(P, stage, u.x, u.y, ch, d, lane);
+    const int d = Q.d[n % kItemRing];  // landed with the commit group of step n - 1
+    const unsigned char* stage = ring + (n % S) * kStage;
+    if (it.y <= k)
+      process_chunk<TT>(P, stage, it.x, it.y, it.z, d, lane);
     else
-      process_chunk<TD>(P, stage, u.x, u.y, ch, d, lane);
-    ++used;
-    if (++cc == u.w) {
-      cc = 0;
-      ++cu;
-    }
+      process_chunk<TD>(P, stage, it.x, it.y, it.z, d, lane);
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -1046,7 +1058,6 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) 
   FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
   // wait for the stream pass (programmatic dependent launch) before reading its output
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (blockIdx.x == 0 && threadIdx.x == 0) *P.work = 0u;  // the stream pass's unit counter
 #pragma unroll 1
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
     finish_sequence<TT, TD>(P, b, sh);
