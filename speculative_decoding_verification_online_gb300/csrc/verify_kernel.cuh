@@ -529,6 +529,10 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // step n - 1, so it has landed when the chunk has.
   if (threadIdx.x == 0) cta_next = 0u;
   __syncthreads();
+  // the finishing grid may launch at once: its CTAs take SMs as this grid's
+  // CTAs retire, run their input-only prologue, and wait (griddepcontrol.wait)
+  // for this grid to complete and its memory to be visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0) put_item(P, Q, 0, next_chunk(P, &cta_next));
   __syncwarp();
   int issued = 0;
@@ -557,9 +561,6 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     __syncwarp();
   }
   cp_async_wait<0>();
-  // let the finishing grid start its prologue; its griddepcontrol.wait still
-  // waits for this grid to complete and its memory to be visible
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------ finishing
@@ -574,6 +575,7 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
 constexpr int kFinThreads = 256;
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kFinPartCap = 4096;  // chunk statistics of a sequence staged in shared memory
+constexpr int kCandCap = 256;      // gate candidates of a sequence gathered in shared memory
 
 struct dfloat {
   float hi, lo;
@@ -623,37 +625,46 @@ __device__ __forceinline__ dfloat warp_incl_scan_df(dfloat v, int lane) {
 struct FinishShared {
   float2 part[kFinPartCap];  // the sequence's chunk statistics (when they fit)
   float tile[kMaxChunks];    // residual mass of every chunk of the stop row
+  dfloat prefix[kMaxChunks]; // inclusive prefix sums of tile
   float rowM[kMaxRows];      // scaled row max Mc
   float rowInvS[kMaxRows];
   dfloat rowS[kMaxRows];
   float xD[kMaxRows];
+  // inputs read before the stream pass has finished
   int Dv[SV_MAX_K];
+  float u0[SV_MAX_K];
+  float u1[SV_MAX_K + 1];    // the residual draw for every possible stop position
+  int gated;
+  float tau;
+  // gate candidates gathered from the per-chunk slots
+  int ncand;
+  int cand_j[kCandCap];
+  int cand_v[kCandCap];
+  float cand_x[kCandCap];
+  int nadm[SV_MAX_K];
+  int adm_i[SV_MAX_K][kTopM];
+  float adm_q[SV_MAX_K][kTopM];
+  float adm_p[SV_MAX_K][kTopM];
+  unsigned overflow_rows;    // draft rows whose admitted set is not fully known
   dfloat wtot[kFinWarps];
-  dfloat wbase[kFinWarps];
   int wlast[kFinWarps];
   int bad;
   int jstar;
   int stop_flag;
   int boundary;
-  unsigned overflow_rows;
   int tstar;
   int degenerate;
   int mode;
+  int pick;
   dfloat before;
   dfloat Z;
   dfloat y;
-  float u1;
-  int pick;
-  int nadm[SV_MAX_K];
-  int adm_i[SV_MAX_K][kTopM];
-  float adm_q[SV_MAX_K][kTopM];
-  float adm_p[SV_MAX_K][kTopM];
 };
 
-// residual weights of eight consecutive entries [v0, v0 + 8).  mode 0: p (bonus
-// row, or degenerate residual); mode 1: p, or max(0, p - q) on the admitted
-// list; mode 2: max(0, p - mu) with mu from the draft logits (mu = q, or q on
-// q >= tau in gated mode).  Entries past V weigh 0.
+// residual weights of eight consecutive entries [v0, v0 + 8): max(0, p - mu)
+// with mu = 0 (mode 0: the bonus row, or a residual without mass), mu = q on
+// the admitted tokens listed (mode 1), or mu from the draft logits (mode 2:
+// q, or q on q >= tau in gated mode).  Entries past V weigh 0.
 struct ResidualEval {
   int mode;
   float Mt, invSt, Md, invSd, c, tau;
@@ -665,27 +676,62 @@ struct ResidualEval {
 
 __device__ __forceinline__ void residual8(const ResidualEval& e, const float (&xt)[8], const float (&xd)[8],
                                           int v0, int V, float (&r)[8]) {
-  if (e.mode == 2) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float p = prob_of(xt[i], e.Mt, e.c, e.invSt);
+  for (int i = 0; i < 8; ++i) {
+    const float p = prob_of(xt[i], e.Mt, e.c, e.invSt);
+    float mu = 0.f;
+    if (e.mode == 2) {
       const float q = prob_of(xd[i], e.Md, e.c, e.invSd);
-      const float mu = (!e.gated || q >= e.tau) ? q : 0.f;
-      r[i] = v0 + i < V ? fmaxf(p - mu, 0.f) : 0.f;
+      mu = (!e.gated || q >= e.tau) ? q : 0.f;
     }
-  } else {
+    r[i] = v0 + i < V ? fmaxf(p - mu, 0.f) : 0.f;
+  }
+  if (e.mode == 1) {
+#pragma unroll 1
+    for (int a = 0; a < e.nadm; ++a) {
+      const int o = e.adm_i[a] - v0;
+      if (o >= 0 && o < 8) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) r[i] = v0 + i < V ? prob_of(xt[i], e.Mt, e.c, e.invSt) : 0.f;
-    if (e.mode == 1) {
-      for (int a = 0; a < e.nadm; ++a) {
-        const int o = e.adm_i[a] - v0;
-        if (o >= 0 && o < 8) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i == o) r[i] = fmaxf(r[i] - e.adm_q[a], 0.f);
-        }
+        for (int i = 0; i < 8; ++i)
+          if (i == o) r[i] = fmaxf(r[i] - e.adm_q[a], 0.f);
       }
     }
+  }
+}
+
+// what the finishing pass of sequence b needs from the inputs alone: drafted
+// tokens, the Philox draws (or the explicit uniforms), the gate.  Runs before
+// the wait on the stream pass.
+__device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishShared& sh) {
+  const int tid = threadIdx.x, k = P.k;
+  const uint64_t s_idx = P.seq_offset + static_cast<uint64_t>(b);
+  if (tid <= k) {
+    // draw 0 at position tid (the accept test), draw 1 at position tid (the
+    // residual or bonus sample, should the sequence stop there)
+#pragma unroll 1
+    for (int draw = 0; draw < 2; ++draw) {
+      float u;
+      if (draw == 0 && P.u0) u = tid < k ? P.u0[static_cast<int64_t>(b) * k + tid] : 0.f;
+      else if (draw == 1 && P.u1) u = P.u1[b];
+      else u = philox_uniform(P.seed, s_idx, static_cast<uint32_t>(tid), static_cast<uint32_t>(draw));
+      if (draw == 0 && tid < k) sh.u0[tid] = u;
+      if (draw == 1) sh.u1[tid] = u;
+    }
+  }
+  if (tid < k) {
+    sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
+    sh.nadm[tid] = 0;
+  }
+  if (tid == 0) {
+    const bool gated = seq_gated(P, b);
+    const float tau = seq_tau(P, b);
+    sh.gated = gated ? 1 : 0;
+    sh.tau = tau;
+    sh.bad = (gated && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
+    sh.ncand = 0;
+    sh.overflow_rows = 0u;
+    sh.boundary = 0;
+    sh.pick = -1;
   }
 }
 
@@ -693,100 +739,129 @@ template <typename TT, typename TD>
 __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
-  const bool gated = seq_gated(P, b);
-  const float tau = seq_tau(P, b);
+  const bool gated = sh.gated != 0;
+  const float tau = sh.tau;
   const bool fastgate = gated && gate_fast_path(tau);
   const float c = P.c;
-  const uint64_t s_idx = P.seq_offset + static_cast<uint64_t>(b);
   const TT* Lt = static_cast<const TT*>(P.Lt);
   const TD* Ld = static_cast<const TD*>(P.Ld);
   const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
   const bool staged = R * nch <= kFinPartCap;
 
-  // phase A: what the decisions need, in one round of loads
-  if (tid == 0) {
-    sh.bad = (gated && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
-    sh.boundary = 0;
-    sh.pick = -1;
-    sh.overflow_rows = 0u;
-  }
+  // step 1: what the stream pass left -- drafted-token logits, chunk
+  // statistics, and (gated) the candidate slots, gathered into a list and
+  // emptied for the next call -- in one round of independent loads
   if (tid < R) sh.xD[tid] = __ldcg(P.xD + static_cast<int64_t>(b) * R + tid);
-  if (tid < k) {
-    sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
-    sh.nadm[tid] = 0;
-  }
-  __syncthreads();
-  if (tid < k && fastgate && __ldcg(P.cand_over + static_cast<int64_t>(b) * k + tid)) {
+  if (fastgate && tid < k && __ldcg(P.cand_over + static_cast<int64_t>(b) * k + tid)) {
     atomicOr(&sh.overflow_rows, 1u << tid);
     P.cand_over[static_cast<int64_t>(b) * k + tid] = 0u;
   }
-  if (staged) {
-#pragma unroll 4
-    for (int e = tid; e < R * nch; e += kFinThreads) sh.part[e] = ldcg_f2(seq_part + e);
+  {
+    // up to kBatch chunk statistics and kBatch candidate slots per thread per
+    // round, all loads issued before any is used (one round trip)
+    constexpr int kBatch = 8;
+    const int np = staged ? R * nch : 0;
+    const int ns = fastgate ? k * nch * kTopM : 0;
+    Cand* sc = P.cand + static_cast<int64_t>(b) * k * nch * kTopM;
+    const int nmax = np > ns ? np : ns;
+#pragma unroll 1
+    for (int base = 0; base < nmax; base += kBatch * kFinThreads) {
+      float2 pv[kBatch], cd[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int e = base + i * kFinThreads + tid;
+        if (e < np) pv[i] = ldcg_f2(seq_part + e);
+        cd[i] = e < ns ? ldcg_f2(reinterpret_cast<const float2*>(sc + e)) : make_float2(0.f, __int_as_float(-1));
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int e = base + i * kFinThreads + tid;
+        if (e < np) sh.part[e] = pv[i];
+        const int v = __float_as_int(cd[i].y);
+        if (v >= 0) {  // a candidate: gather it and empty the slot for the next call
+          sc[e].v = -1;
+          const int j = e / (nch * kTopM);
+          const int n = atomicAdd(&sh.ncand, 1);
+          if (n < kCandCap && v < V) {
+            sh.cand_j[n] = j;
+            sh.cand_v[n] = v;
+            sh.cand_x[n] = cd[i].x;
+          } else {
+            atomicOr(&sh.overflow_rows, 1u << j);
+          }
+        }
+      }
+    }
   }
   __syncthreads();
   auto part_at = [&](int r, int ch) -> float2 {
     return staged ? sh.part[r * nch + ch] : ldcg_f2(seq_part + static_cast<int64_t>(r) * nch + ch);
   };
 
-  // row statistics (a warp per row): merge the chunk (mc, s) pairs
+  // step 2: the target logits of the candidates go out (a candidate thread
+  // uses them in step 3) while half-warps merge the chunk statistics of
+  // rows r0 + 0 and r0 + 1 (both halves of a warp loop together)
+  const int nc = min(sh.ncand, kCandCap);
+  int cj = 0, cv = 0;
+  float cx = 0.f, cxt = 0.f;
+  if (tid < nc) {
+    cj = sh.cand_j[tid];
+    cv = sh.cand_v[tid];
+    cx = sh.cand_x[tid];
+    cxt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + cj) * V, cv);
+  }
+  {
+    const int half = lane >> 4, l16 = lane & 15;
 #pragma unroll 1
-  for (int r = warp; r < R; r += kFinWarps) {
-    float M = -INFINITY;
+    for (int r0 = 2 * warp; r0 < R; r0 += 2 * kFinWarps) {
+      const int r = r0 + half;
+      const bool live = r < R;
+      float M = -INFINITY;
 #pragma unroll 1
-    for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, part_at(r, ch).x);
-    M = warp_max(M);
-    dfloat S = df(0.f);
+      for (int ch = l16; live && ch < nch; ch += 16) M = fmaxf(M, part_at(r, ch).x);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      dfloat S = df(0.f);
 #pragma unroll 1
-    for (int ch = lane; ch < nch; ch += 32) {
-      const float2 ms = part_at(r, ch);
-      S = df_add(S, df(ms.x == -INFINITY ? ms.y * 0.f : ms.y * exp2f(ms.x - M)));
-    }
-    S = warp_sum_df(S);
-    if (lane == 0) {
-      sh.rowM[r] = M;
-      sh.rowS[r] = S;
-      // 1 / (hi + lo) to float precision
-      sh.rowInvS[r] = (1.f / S.hi) * (1.f - S.lo / S.hi);
-      if (M == -INFINITY || !isfinite(S.hi) || !(S.hi > 0.f)) sh.bad = 1;
-      if (P.row_stats) {
-        // (max, log-sum-exp) of L / T: Mc ln 2 and Mc ln 2 + ln S
-        const float mo = M * 0.69314718f;
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = mo;
-        P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = mo + (logf(S.hi) + S.lo / S.hi);
+      for (int ch = l16; live && ch < nch; ch += 16) {
+        const float2 ms = part_at(r, ch);
+        S = df_add(S, df(ms.x == -INFINITY ? ms.y * 0.f : ms.y * exp2f(ms.x - M)));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) S = df_add(S, shfl_xor_df(S, o));
+      if (live && l16 == 0) {
+        sh.rowM[r] = M;
+        sh.rowS[r] = S;
+        sh.rowInvS[r] = (1.f / S.hi) * (1.f - S.lo / S.hi);  // 1 / (hi + lo) to float precision
+        if (M == -INFINITY || !isfinite(S.hi) || !(S.hi > 0.f)) sh.bad = 1;
+        if (P.row_stats) {
+          // (max, log-sum-exp) of L / T: Mc ln 2 and Mc ln 2 + ln S
+          const float mo = M * 0.69314718f;
+          P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = mo;
+          P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = mo + (logf(S.hi) + S.lo / S.hi);
+        }
       }
     }
   }
   __syncthreads();
 
-  // phase B: admitted tokens of every draft row and their target probability
-  // (the candidate slots are emptied for the next call as they are read)
-  if (fastgate) {
-    Cand* sc = P.cand + static_cast<int64_t>(b) * k * nch * kTopM;
-#pragma unroll 4
-    for (int e = tid; e < k * nch * kTopM; e += kFinThreads) {
-      const Cand cd = sc[e];
-      if (cd.v < 0) continue;
-      sc[e].v = -1;
-      const int j = e / (nch * kTopM);
-      if (sh.bad || cd.v >= V) continue;
-      const int rd = k + 1 + j;
-      const float q = prob_of(cd.x, sh.rowM[rd], c, sh.rowInvS[rd]);
-      if (q >= tau) {
-        const int a = atomicAdd(&sh.nadm[j], 1);
-        if (a < kTopM) {
-          const float xt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + j) * V, cd.v);
-          sh.adm_i[j][a] = cd.v;
-          sh.adm_q[j][a] = q;
-          sh.adm_p[j][a] = prob_of(xt, sh.rowM[j], c, sh.rowInvS[j]);
-        } else {
-          atomicOr(&sh.overflow_rows, 1u << j);
-        }
+  // step 3: the admitted tokens (q >= tau) among the candidates, with their
+  // target probability; and, in warp 0, every draft position: gate, mu,
+  // alpha, accept test
+  if (tid < nc && !sh.bad) {
+    const int rd = k + 1 + cj;
+    const float q = prob_of(cx, sh.rowM[rd], c, sh.rowInvS[rd]);
+    if (q >= tau) {
+      const int a = atomicAdd(&sh.nadm[cj], 1);
+      if (a < kTopM) {
+        sh.adm_i[cj][a] = cv;
+        sh.adm_q[cj][a] = q;
+        sh.adm_p[cj][a] = prob_of(cxt, sh.rowM[cj], c, sh.rowInvS[cj]);
+      } else {
+        atomicOr(&sh.overflow_rows, 1u << cj);
       }
     }
   }
-
-  // every draft position (one lane each): gate, mu, alpha, accept test
   if (warp == 0) {
     bool ok = true, acc = false, is_null = false, near = false;
     float alpha = 0.f;
@@ -801,8 +876,7 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
         const float mu = admitted ? q : 0.f;
         is_null = !admitted;
         alpha = is_null ? 0.f : (mu > 0.f ? fminf(1.f, p / mu) : (p > 0.f ? 1.f : 0.f));
-        const float u0 = P.u0 ? P.u0[static_cast<int64_t>(b) * k + lane]
-                              : philox_uniform(P.seed, s_idx, static_cast<uint32_t>(lane), 0u);
+        const float u0 = sh.u0[lane];
         acc = !is_null && p > 0.f && u0 * mu <= p;
         near = (gated && fabsf(q - tau) < kBoundary) ||
                (!is_null && mu > 0.f && p < mu && fabsf(u0 - p / mu) < kBoundary);
@@ -832,7 +906,6 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
       sh.stop_flag = jstar < k ? (((nullm >> jstar) & 1u) ? SV_FLAG_NULL : SV_FLAG_REJECT)
                                : SV_FLAG_ACCEPT;
       sh.boundary = __popc(nearm);
-      sh.u1 = P.u1 ? P.u1[b] : philox_uniform(P.seed, s_idx, static_cast<uint32_t>(jstar), 1u);
     }
   }
   __syncthreads();
@@ -848,13 +921,14 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
     return;
   }
 
-  // the stop row's residual (or bonus) weights, chunk by chunk
+  // step 4: the stop row's residual (or bonus) mass per chunk
   const int rt = jstar, rd = k + 1 + jstar;
   const TT* trow = Lt + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
   const TD* drow = jstar < k ? Ld + (static_cast<int64_t>(b) * k + jstar) * V : nullptr;
   int mode = 0;
   if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
   const int nadm = mode == 1 ? min(sh.nadm[jstar], kTopM) : 0;
+  const float u1 = sh.u1[jstar];
   ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
                   jstar < k ? sh.rowM[rd] : 0.f, jstar < k ? sh.rowInvS[rd] : 0.f,
                   c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
@@ -864,8 +938,8 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
 
   if (mode == 2) {
     // dense: one re-read of the stop row pair, a warp per chunk (each lane
-    // 8-entry groups lane, lane + 32, ...: 16-byte coalesced loads, all issued
-    // before use); no barrier until every chunk is summed
+    // 8-entry groups lane, lane + 32, ...: 16-byte coalesced loads, four
+    // groups of both rows issued before use); no barrier until every chunk is summed
 #pragma unroll 1
     for (int ch = warp; ch < nch; ch += kFinWarps) {
       const int c0 = ch * kChunk;
@@ -891,8 +965,8 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
     __syncthreads();
   }
 
-  // warp 0: chunk sums (from the chunk statistics in modes 0 / 1), the total
-  // mass Z (a residual without mass falls back to p), and the chunk holding
+  // warp 0: chunk masses (from the chunk statistics in modes 0 / 1), the total
+  // Z (a residual without mass falls back to p), and the chunk holding
   // y = u1 Z: the first chunk whose inclusive prefix exceeds y
   if (warp == 0) {
     const float invS = sh.rowInvS[rt];
@@ -902,6 +976,7 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
         const float2 ms = part_at(rt, ch);
         float t = ms.x == -INFINITY ? 0.f : ms.y * exp2f(ms.x - ev.Mt) * invS;
         if (use_mode == 1) {
+#pragma unroll 1
           for (int a = 0; a < nadm; ++a)
             if (sh.adm_i[jstar][a] / kChunk == ch) t -= fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]);
           t = fmaxf(t, 0.f);
@@ -910,36 +985,43 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
       }
       __syncwarp();
     };
-    auto total = [&]() {
-      dfloat z = df(0.f);
+    // one pass gives every chunk's inclusive prefix (float-float) and the total
+    auto scan_all = [&]() {
+      dfloat carry = df(0.f);
 #pragma unroll 1
-      for (int ch = lane; ch < nch; ch += 32) z = df_add(z, df(sh.tile[ch]));
-      return warp_sum_df(z);
+      for (int g0 = 0; g0 < nch; g0 += 32) {
+        const int ch = g0 + lane;
+        const float t = ch < nch ? sh.tile[ch] : 0.f;
+        const dfloat incl = df_add(warp_incl_scan_df(df(t), lane), carry);
+        if (ch < nch) sh.prefix[ch] = incl;
+        carry = shfl_df(incl, 31);
+      }
+      __syncwarp();
+      return carry;
     };
     if (mode != 2) chunk_sums(mode);
-    dfloat Z = total();
+    dfloat Z = scan_all();
     int degenerate = 0;
     if (!(Z.hi > 0.f)) {
       chunk_sums(0);
-      Z = total();
+      Z = scan_all();
       degenerate = 1;
     }
-    const dfloat y = df_mul(Z, sh.u1);
-    dfloat carry = df(0.f), before = df(0.f);
+    // the first chunk whose inclusive prefix exceeds y = u1 Z, and the last
+    // chunk with mass
+    const dfloat y = df_mul(Z, u1);
+    dfloat before = df(0.f);
     int found = -1, last = -1;
 #pragma unroll 1
     for (int g0 = 0; g0 < nch; g0 += 32) {
       const int ch = g0 + lane;
-      const float t = ch < nch ? sh.tile[ch] : 0.f;
-      if (t > 0.f) last = ch;
-      const dfloat incl = df_add(warp_incl_scan_df(df(t), lane), carry);
-      const unsigned m = __ballot_sync(0xffffffffu, ch < nch && df_lt(y, incl));
+      const bool in = ch < nch;
+      if (in && sh.tile[ch] > 0.f) last = ch;
+      const unsigned m = __ballot_sync(0xffffffffu, in && df_lt(y, sh.prefix[ch]));
       if (found < 0 && m) {
-        const int src = __ffs(m) - 1;
-        found = g0 + src;
-        before = shfl_df(df_sub(incl, df(t)), src);
+        found = g0 + __ffs(m) - 1;
+        before = df_sub(sh.prefix[found], df(sh.tile[found]));
       }
-      carry = shfl_df(incl, 31);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
@@ -959,7 +1041,10 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   __syncthreads();
   ev.mode = sh.mode;
 
-  // one re-read of the chosen chunk: thread i evaluates entries [8 i, 8 i + 8)
+  // step 5: one re-read of the chosen chunk; thread i evaluates entries
+  // [8 i, 8 i + 8), then a block-wide scan.  Thread i's range is [lo_i, hi_i)
+  // with lo_{i+1} == hi_i bit for bit (the same float-float sums), so exactly
+  // one thread claims any y below the chunk total.
   const int c0 = sh.tstar * kChunk;
   const int e0 = tid * 8;
   float r8[8];
@@ -969,10 +1054,6 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
     if (ev.mode == 2) load8<TD>(drow, c0 + e0, V, vd, xd);
     residual8(ev, xt, xd, c0 + e0, V, r8);
   }
-
-  // block scan: thread i owns entries [8 i, 8 i + 8) of the chunk.  Thread i's
-  // range is [lo_i, hi_i) with lo_{i+1} == hi_i bit for bit (the same
-  // float-float sums), so exactly one thread claims any y below the chunk total.
   {
     int lastpos = -1;
     float t0 = 0.f, t1 = 0.f;
@@ -991,15 +1072,10 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
     if (lane == 31) sh.wtot[warp] = wincl;
     if (lane == 0) sh.wlast[warp] = wl;
     __syncthreads();
-    if (tid == 0) {
-      dfloat base = df(0.f);
-      for (int w = 0; w < kFinWarps; ++w) {
-        sh.wbase[w] = base;
-        base = df_add(base, sh.wtot[w]);
-      }
-    }
-    __syncthreads();
-    const dfloat wbase = sh.wbase[warp];
+    // every thread forms its warp's base from the (at most 8) warp totals
+    dfloat wbase = df(0.f);
+#pragma unroll 1
+    for (int w = 0; w < warp; ++w) wbase = df_add(wbase, sh.wtot[w]);
     const dfloat lo = df_add(wbase, wexcl), hi = df_add(wbase, wincl);
     const dfloat yl = df_sub(sh.y, sh.before);
     if (df_le(lo, yl) && df_lt(yl, hi)) {
@@ -1023,11 +1099,12 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
       const float Zf = df_f(sh.Z);
       const float cl = df_f(df_add(df_add(sh.before, lo), df(prev))) / Zf;
       const float chh = df_f(df_add(df_add(sh.before, lo), df(run))) / Zf;
-      if (fabsf(sh.u1 - cl) < kBoundary || fabsf(sh.u1 - chh) < kBoundary) sh.boundary += 1;
+      if (fabsf(u1 - cl) < kBoundary || fabsf(u1 - chh) < kBoundary) atomicAdd(&sh.boundary, 1);
     }
   }
   __syncthreads();
 
+  // step 6: outputs
   if (tid == 0) {
     int pick = sh.pick;
     if (pick < 0) {
@@ -1056,12 +1133,19 @@ template <typename TT, typename TD>
 __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
-  // wait for the stream pass (programmatic dependent launch) before reading its output
+  // the first sequence's input-only work overlaps the end of the stream pass;
+  // then wait for the stream pass (programmatic dependent launch) before
+  // reading its output
+  if (blockIdx.x < P.B) finish_prologue(P, blockIdx.x, sh);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    finish_sequence<TT, TD>(P, b, sh);
+    if (b != static_cast<int>(blockIdx.x)) {
+      __syncthreads();
+      finish_prologue(P, b, sh);
+    }
     __syncthreads();
+    finish_sequence<TT, TD>(P, b, sh);
   }
 }
 
