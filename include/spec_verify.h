@@ -190,6 +190,54 @@ int spec_verify_launches_per_run(void);
  * pending marks.  Returns SV_EINVAL for a NULL handle or only one NULL event. */
 sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free entry point.  The pages have no counterpart of this call; it
+ * exists for callers that may not allocate device memory where they verify --
+ * a serving loop whose device memory is reserved up front by its own caching
+ * allocator, or one that must not call cudaMalloc / cudaFree between decode
+ * steps because they synchronise the device.  spec_verify_init allocates the
+ * handle's workspace, so such callers cannot create a handle at that point.
+ *
+ * spec_verify_run_noalloc verifies exactly like spec_verify_run (same kernels,
+ * same arguments plus k and V, same results bit for bit) on the CURRENT CUDA
+ * device.  Its workspace is a static device buffer of SV_NOALLOC_SCRATCH_BYTES
+ * compiled into the library; it calls no allocating CUDA or library function.
+ * Sizes beyond the buffer return SV_EUNSUPPORTED with nothing launched:
+ *   B * k * ceil(V / 2048) * 4 <= SV_NOALLOC_MAX_CAND_SLOTS
+ *   B * k                      <= SV_NOALLOC_MAX_ROWS
+ *   B * (2k+1) * ceil(V / 2048) * 8 + B * (2k+1) * 4 (each rounded up to 256)
+ *                              <= SV_NOALLOC_STATS_BYTES
+ * (B = 64, k = 5, V = 128256 uses 80,640 slots and 0.36 MiB of statistics;
+ * B = 256, k = 8, V = 151936 does not fit.)
+ *
+ * Set-up: the first call on a device (per process) looks up the buffer's
+ * device address, sets the kernels' attributes and fills the candidate slots
+ * with their empty marker (a synchronous memset).  Make that first call
+ * outside any stream capture.  What must hold before every call: every
+ * candidate slot empty (all bits set) and every row-overflow flag zero; set-up
+ * establishes it and every call that completes restores it.
+ *
+ * Concurrency: all calls on a device share the one buffer, so they must not
+ * overlap -- issue them on one stream or otherwise order them.  Two calls in
+ * flight at once race on the buffer and produce wrong results.
+ *
+ * Other errors as spec_verify_run; SV_EINVAL also for k < 1 or V < 1. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define SV_NOALLOC_MAX_CAND_SLOTS (1u << 19)                 /* 4 MiB of 8-byte slots */
+#define SV_NOALLOC_MAX_ROWS (1u << 14)                       /* 64 KiB of flags */
+#define SV_NOALLOC_STATS_BYTES (SV_NOALLOC_SCRATCH_BYTES - (4u << 20) - (64u << 10))
+sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype tdt,
+                                  const void* draft_logits, sv_dtype ddt,
+                                  const int32_t* draft_tokens,
+                                  int B, int k, int V, float temperature,
+                                  sv_gate gate_mode, float threshold,
+                                  const uint8_t* gate_mode_per_seq,
+                                  const float* threshold_per_seq,
+                                  uint64_t seed,
+                                  int32_t* accepted_len, int32_t* tokens, float* accept_prob,
+                                  int8_t* flags, uint64_t* counters,
+                                  void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

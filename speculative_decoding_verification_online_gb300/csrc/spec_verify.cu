@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "spec_verify.h"
@@ -358,3 +359,119 @@ sv_status spec_verify_free(spec_verify_t h) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (spec_verify_run_noalloc).
+//
+// For callers that may not allocate device memory at the point where they
+// verify (device memory reserved up front by their own allocator, or no
+// cudaMalloc / cudaFree between decode steps because those synchronise the
+// device): the workspace lives in one static device buffer instead of a
+// handle's allocation, and the call goes through the same validation and the
+// same two launches as spec_verify_run_ex, on a handle built on the stack.
+//
+// Buffer layout (fixed, so that the candidate slots keep their empty marker
+// from one call to the next whatever the shapes):
+//   [0, 4 MiB)                  candidate slots, all bits set when empty
+//   [4 MiB, 4 MiB + 64 KiB)     row-overflow flags, zero when clear
+//   [4 MiB + 64 KiB, 8 MiB)     chunk statistics, then drafted-token logits
+// The finishing pass empties every slot and clears every flag it reads, so a
+// completed call leaves the buffer as set-up left it.  Calls on one device
+// share the buffer and must not overlap.
+
+namespace {
+
+constexpr size_t kNaCandBytes = static_cast<size_t>(SV_NOALLOC_MAX_CAND_SLOTS) * sizeof(sv::Cand);
+constexpr size_t kNaOverBytes = static_cast<size_t>(SV_NOALLOC_MAX_ROWS) * sizeof(unsigned);
+static_assert(kNaCandBytes == (4u << 20), "candidate region is 4 MiB");
+static_assert(kNaCandBytes + kNaOverBytes + SV_NOALLOC_STATS_BYTES == SV_NOALLOC_SCRATCH_BYTES,
+              "scratch layout");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocDevice {
+  bool ready = false;
+  unsigned char* base = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+  int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};
+};
+constexpr int kNaMaxDevices = 64;
+NoallocDevice g_na[kNaMaxDevices];
+std::mutex g_na_mutex;
+
+// once per device, with that device current: the buffer's address, the
+// kernels' attributes, and the empty marker in every candidate slot
+sv_status noalloc_setup(int dev, NoallocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  NoallocDevice& d = g_na[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SV_ECUDA;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SV_ECUDA;
+    cudaError_t e = configure<float, float>(&d.blocks_per_sm[0][0]);
+    if (e == cudaSuccess) e = configure<float, uint16_t>(&d.blocks_per_sm[0][1]);
+    if (e == cudaSuccess) e = configure<uint16_t, float>(&d.blocks_per_sm[1][0]);
+    if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&d.blocks_per_sm[1][1]);
+    if (e != cudaSuccess) return SV_ECUDA;
+    unsigned char* base = static_cast<unsigned char*>(p);
+    if (cudaMemset(base, 0xFF, kNaCandBytes) != cudaSuccess ||
+        cudaMemset(base + kNaCandBytes, 0, kNaOverBytes) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return SV_ECUDA;
+    d.base = base;
+    d.ready = true;
+  }
+  *out = &d;
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype tdt,
+                                             const void* draft_logits, sv_dtype ddt,
+                                             const int32_t* draft_tokens, int B, int k, int V,
+                                             float temperature, sv_gate gate_mode, float threshold,
+                                             const uint8_t* gate_mode_per_seq,
+                                             const float* threshold_per_seq, uint64_t seed,
+                                             int32_t* accepted_len, int32_t* tokens,
+                                             float* accept_prob, int8_t* flags, uint64_t* counters,
+                                             void* cuda_stream) {
+  if (B < 0 || k < 1 || V < 1) return SV_EINVAL;
+  if (k > SV_MAX_K || V > SV_MAX_V) return SV_EUNSUPPORTED;
+  // sizes against the fixed buffer, before anything touches the device
+  const size_t nchunk = (static_cast<size_t>(V) + sv::kChunk - 1) / sv::kChunk;
+  const size_t rows = 2 * static_cast<size_t>(k) + 1;
+  const size_t slots = static_cast<size_t>(B) * k * nchunk * sv::kTopM;
+  const size_t part_bytes = align_up(static_cast<size_t>(B) * rows * nchunk * sizeof(float2), 256);
+  const size_t xd_bytes = align_up(static_cast<size_t>(B) * rows * sizeof(float), 256);
+  if (slots > SV_NOALLOC_MAX_CAND_SLOTS || static_cast<size_t>(B) * k > SV_NOALLOC_MAX_ROWS ||
+      part_bytes + xd_bytes > SV_NOALLOC_STATS_BYTES)
+    return SV_EUNSUPPORTED;
+  if (B == 0) return SV_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ECUDA;
+  if (dev < 0 || dev >= kNaMaxDevices) return SV_EUNSUPPORTED;
+  NoallocDevice* d = nullptr;
+  const sv_status st = noalloc_setup(dev, &d);
+  if (st != SV_OK) return st;
+
+  // a handle on the stack whose workspace points into the buffer
+  spec_verify_s h;
+  h.device = dev;
+  h.max_B = B;
+  h.k = k;
+  h.V = V;
+  h.nchunk = static_cast<int>(nchunk);
+  h.num_sms = d->num_sms;
+  for (int a = 0; a < 2; ++a)
+    for (int b = 0; b < 2; ++b) h.blocks_per_sm[a][b] = d->blocks_per_sm[a][b];
+  h.cand = reinterpret_cast<sv::Cand*>(d->base);
+  h.cand_over = reinterpret_cast<unsigned*>(d->base + kNaCandBytes);
+  h.part = reinterpret_cast<float2*>(d->base + kNaCandBytes + kNaOverBytes);
+  h.xD = reinterpret_cast<float*>(d->base + kNaCandBytes + kNaOverBytes + part_bytes);
+  return spec_verify_run_ex(&h, target_logits, tdt, draft_logits, ddt, draft_tokens, B, temperature,
+                            gate_mode, threshold, gate_mode_per_seq, threshold_per_seq, seed, 0,
+                            nullptr, nullptr, accepted_len, tokens, accept_prob, flags, counters,
+                            nullptr, cuda_stream);
+}

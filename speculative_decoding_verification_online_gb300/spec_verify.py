@@ -60,6 +60,8 @@ def load() -> ctypes.CDLL:
     L.spec_verify_launches_per_run.restype = I
     L.spec_verify_mark_next.argtypes = [P, P, P]
     L.spec_verify_mark_next.restype = I
+    L.spec_verify_run_noalloc.argtypes = [P, I, P, I, P, I, I, I, F, I, F, P, P, U64, P, P, P, P, P, P]
+    L.spec_verify_run_noalloc.restype = I
     _lib = L
     return L
 
@@ -115,6 +117,16 @@ def spec_verify_launches_per_run() -> int:
 def spec_verify_mark_next(h, ev_before, ev_after) -> int:
     """Record two CUDA events (raw cudaEvent_t handles) around the next call's stream pass."""
     return load().spec_verify_mark_next(h, ev_before, ev_after)
+
+
+def spec_verify_run_noalloc(Lt, tdt, Ld, ddt, D, B, k, V, temperature, gate_mode, threshold,
+                            gate_per_seq, threshold_per_seq, seed, accepted_len, tokens, accept_prob,
+                            flags, counters, stream) -> int:
+    """Raw call of the allocation-free entry point (current device); returns the status."""
+    return load().spec_verify_run_noalloc(Lt, tdt, Ld, ddt, D, B, k, V, temperature, gate_mode,
+                                          threshold, gate_per_seq, threshold_per_seq, seed,
+                                          accepted_len, tokens, accept_prob, flags, counters,
+                                          stream)
 
 
 # ------------------------------------------------------ torch marshalling
@@ -238,3 +250,34 @@ class SpecVerifier:
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_run_host")
         return out
+
+
+def run_noalloc(Lt, Ld, D, temperature, gate_mode=SV_PLAIN, threshold=0.5, gate_per_seq=None,
+                threshold_per_seq=None, seed=0, out=None, counters=None, stream=None):
+    """Verify device tensors through the allocation-free entry point on their device.
+
+    The outputs are the caller's tensors (``out``, or new ones made here by
+    torch); the library itself allocates nothing.  Calls on one device must
+    not overlap."""
+    B, k1, V = Lt.shape
+    k = k1 - 1
+    dev = Lt.device
+    _check(Lt, "target_logits", (B, k + 1, V), device=dev)
+    _check(Ld, "draft_logits", (B, k, V), device=dev)
+    _check(D, "draft_tokens", (B, k), torch.int32, dev)
+    if out is None:
+        out = dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+                   tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev),
+                   accept_prob=torch.empty(B, k, dtype=torch.float32, device=dev),
+                   flags=torch.empty(B, k, dtype=torch.int8, device=dev))
+    with torch.cuda.device(dev):
+        st = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream
+        rc = spec_verify_run_noalloc(Lt.data_ptr(), _dt(Lt), Ld.data_ptr(), _dt(Ld), D.data_ptr(), B,
+                                     k, V, float(temperature), int(gate_mode), float(threshold),
+                                     _ptr(gate_per_seq), _ptr(threshold_per_seq), int(seed),
+                                     out["accepted_len"].data_ptr(), out["tokens"].data_ptr(),
+                                     out["accept_prob"].data_ptr(), _ptr(out.get("flags")),
+                                     _ptr(counters), st)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_run_noalloc")
+    return out
