@@ -466,7 +466,11 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
     if ((sv & 31) == lane) P.xD[static_cast<int64_t>(b) * P.rows + r] = stage_logit<T>(stage, d - c0);
   }
 
-  if (is_draft) {
+  // gated draft rows keep candidates only on the fast path (slack tau (kTopM + 1)
+  // > 1), and a chunk can hold one only if s <= 1 / (slack tau) (the chunk's
+  // largest term contributes 1 to s): s < kTopM + 1 rules out almost every
+  // chunk before the row's gate settings are even read
+  if (is_draft && s < static_cast<float>(kTopM + 1)) {
     const float tau = seq_tau(P, b);
     if (seq_gated(P, b) && gate_fast_path(tau) && s > 0.f && isfinite(s)) {
       // a token's in-chunk probability exp2(fma(x, c, -mc)) / s reaches
