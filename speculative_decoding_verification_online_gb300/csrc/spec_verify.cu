@@ -37,6 +37,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 
+constexpr int kFinCluster = 4;  // CTAs sharing a sequence's dense residual
+
 bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
 // every warp of a stream CTA owns a ring of kDepth chunk stages
@@ -60,7 +62,8 @@ cudaError_t configure(int* blocks_per_sm) {
 }
 
 template <typename TT, typename TD>
-sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
+sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
+                 cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
   const long long need = (static_cast<long long>(P.total_chunks) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
@@ -80,17 +83,33 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaSt
   // the finishing pass: one CTA per sequence, allowed to launch while the
   // stream pass drains; it waits (griddepcontrol.wait) before reading its output
   cudaLaunchConfig_t cfg = {};
-  // one CTA per sequence up to two per SM; larger batches loop (warm instruction cache)
-  const int fin_grid = P.B < 2 * h->num_sms ? P.B : 2 * h->num_sms;
-  cfg.gridDim = dim3(static_cast<unsigned>(fin_grid));
+  // a cluster of CTAs per sequence at a time (two CTAs per SM at most; larger
+  // batches loop).  When dense residuals are likely (plain rows, or gated rows
+  // off the candidate fast path) and the whole batch fits at once, clusters of
+  // up to kFinCluster CTAs share the re-read of the stop row pair; otherwise
+  // one CTA per sequence (more sequences in flight beats wider sequences)
+  int csize = 1;
+  if (dense_likely)
+    for (int c = kFinCluster; c > 1; c /= 2)
+      if (static_cast<long long>(P.B) * c <= 2ll * h->num_sms) {
+        csize = c;
+        break;
+      }
+  const int max_clusters = 2 * h->num_sms / csize;
+  const int clusters = P.B < max_clusters ? P.B : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize));
   cfg.blockDim = dim3(sv::kFinThreads);
   cfg.dynamicSmemBytes = sizeof(sv::FinishShared);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = csize > 1 ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD>, P) != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
@@ -261,10 +280,15 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
   const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
-  if (tb && db) return launch<uint16_t, uint16_t>(h, P, bps, st);
-  if (tb && !db) return launch<uint16_t, float>(h, P, bps, st);
-  if (!tb && db) return launch<float, uint16_t>(h, P, bps, st);
-  return launch<float, float>(h, P, bps, st);
+  // dense residuals are likely unless every row is gated on the candidate fast
+  // path (per-sequence settings are device data: their presence counts as likely)
+  const bool all_fast_gated = gate_mode == SV_GATED_MU && !gate_mode_per_seq && !threshold_per_seq &&
+                              threshold * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
+  const bool dense_likely = !all_fast_gated;
+  if (tb && db) return launch<uint16_t, uint16_t>(h, P, bps, dense_likely, st);
+  if (tb && !db) return launch<uint16_t, float>(h, P, bps, dense_likely, st);
+  if (!tb && db) return launch<float, uint16_t>(h, P, bps, dense_likely, st);
+  return launch<float, float>(h, P, bps, dense_likely, st);
 }
 
 sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,

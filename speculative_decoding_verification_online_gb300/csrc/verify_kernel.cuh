@@ -41,10 +41,14 @@
 #include <cmath>
 #include <cstdint>
 
+#include <cooperative_groups.h>
+
 #include "philox.cuh"
 #include "spec_verify.h"
 
 namespace sv {
+
+namespace cg = cooperative_groups;
 
 constexpr int kChunk = 2048;                // vocabulary entries per chunk statistic
 constexpr int kTopM = 4;                    // gate candidate slots per chunk / admitted tokens per row
@@ -663,6 +667,7 @@ struct FinishShared {
   dfloat before;
   dfloat Z;
   dfloat y;
+  int fmode;  // the stop row's sampling mode (-1: the sequence is done)
 };
 
 // residual weights of eight consecutive entries [v0, v0 + 8): max(0, p - mu)
@@ -740,7 +745,7 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
 }
 
 template <typename TT, typename TD>
-__device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
+__device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
   const bool gated = sh.gated != 0;
@@ -748,7 +753,6 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   const bool fastgate = gated && gate_fast_path(tau);
   const float c = P.c;
   const TT* Lt = static_cast<const TT*>(P.Lt);
-  const TD* Ld = static_cast<const TD*>(P.Ld);
   const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
   const bool staged = R * nch <= kFinPartCap;
 
@@ -921,16 +925,84 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
     if (tid == 0) {
       P.accepted_len[b] = -1;
       if (P.counters) atomicAdd(P.counters + SV_CNT_INVALID, 1ull);
+      sh.fmode = -1;  // done: nothing left to sample
     }
     return;
   }
 
-  // step 4: the stop row's residual (or bonus) mass per chunk
+  // the stop row's sampling mode: 0 the bonus row (p), 1 a gated row whose
+  // admitted set is known (p minus the admitted tokens' q), 2 the dense
+  // residual (q everywhere: the stop row pair is re-read)
+  if (tid == 0) {
+    int mode = 0;
+    if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
+    sh.fmode = mode;
+  }
+}
+
+// The dense residual's chunk masses sum max(0, p - mu) over the stop row pair
+// of sequence b (mu = q, or q on q >= tau when gated), one warp per chunk: the
+// CTAs of a cluster share the chunks (CTA r of n takes chunks r * 8 + w, then
+// every 8 n) and write the masses into the leading CTA's shared memory.  Lanes
+// take 8-entry groups lane, lane + 32, ... (16-byte coalesced loads), four
+// groups of both rows issued before use.
+template <typename TT, typename TD>
+__device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lead, float* lead_tile,
+                                 int rank, int csize) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int k = P.k, V = P.V, nch = P.nchunk;
+  const int jstar = lead.jstar;
+  const int rt = jstar, rd = k + 1 + jstar;
+  const TT* trow = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
+  const TD* drow = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + jstar) * V;
+  const ResidualEval ev{2, lead.rowM[rt], lead.rowInvS[rt], lead.rowM[rd], lead.rowInvS[rd], P.c, lead.tau,
+                        lead.gated != 0, 0, nullptr, nullptr};
+  const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
+  constexpr int kLaneGroups = kChunk / 8 / 32;
+#pragma unroll 1
+  for (int ch = rank * kFinWarps + warp; ch < nch; ch += csize * kFinWarps) {
+    const int c0 = ch * kChunk;
+    float acc = 0.f;
+#pragma unroll 1
+    for (int h = 0; h < kLaneGroups; h += 4) {
+      float xt[4][8], xd[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
+        load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float rr[8];
+        residual8(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
+        acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) lead_tile[ch] = acc;
+  }
+}
+
+template <typename TT, typename TD>
+__device__ void finish_back(const Params& P, int b, FinishShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
+  const bool gated = sh.gated != 0;
+  const float tau = sh.tau;
+  const float c = P.c;
+  const TT* Lt = static_cast<const TT*>(P.Lt);
+  const TD* Ld = static_cast<const TD*>(P.Ld);
+  const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
+  const bool staged = R * nch <= kFinPartCap;
+  auto part_at = [&](int r, int ch) -> float2 {
+    return staged ? sh.part[r * nch + ch] : ldcg_f2(seq_part + static_cast<int64_t>(r) * nch + ch);
+  };
+  const int jstar = sh.jstar;
+  int32_t* tok = P.tokens + static_cast<int64_t>(b) * (k + 1);
   const int rt = jstar, rd = k + 1 + jstar;
   const TT* trow = Lt + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
   const TD* drow = jstar < k ? Ld + (static_cast<int64_t>(b) * k + jstar) * V : nullptr;
-  int mode = 0;
-  if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
+  const int mode = sh.fmode;
   const int nadm = mode == 1 ? min(sh.nadm[jstar], kTopM) : 0;
   const float u1 = sh.u1[jstar];
   ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
@@ -938,36 +1010,6 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
                   c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
                   jstar < k ? sh.adm_q[jstar] : sh.adm_q[0]};
   const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
-  constexpr int kLaneGroups = kChunk / 8 / 32;  // 8-entry groups per lane when a warp reads a chunk
-
-  if (mode == 2) {
-    // dense: one re-read of the stop row pair, a warp per chunk (each lane
-    // 8-entry groups lane, lane + 32, ...: 16-byte coalesced loads, four
-    // groups of both rows issued before use); no barrier until every chunk is summed
-#pragma unroll 1
-    for (int ch = warp; ch < nch; ch += kFinWarps) {
-      const int c0 = ch * kChunk;
-      float acc = 0.f;
-#pragma unroll 1
-      for (int h = 0; h < kLaneGroups; h += 4) {
-        float xt[4][8], xd[4][8];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
-          load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float rr[8];
-          residual8(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
-          acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
-        }
-      }
-      acc = warp_sum(acc);
-      if (lane == 0) sh.tile[ch] = acc;
-    }
-    __syncthreads();
-  }
 
   // warp 0: chunk masses (from the chunk statistics in modes 0 / 1), the total
   // Z (a residual without mass falls back to p), and the chunk holding
@@ -1133,23 +1175,41 @@ __device__ void finish_sequence(const Params& P, int b, FinishShared& sh) {
   if (tid > jstar && tid <= k) tok[tid] = -1;
 }
 
+// The finishing grid runs in clusters of one or more CTAs (a cluster per
+// sequence at a time).  The leading CTA does all the work of a sequence except
+// the dense residual's chunk masses, which every CTA of the cluster shares.
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int csize = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int cid = static_cast<int>(blockIdx.x) / csize;
+  const int ncl = static_cast<int>(gridDim.x) / csize;
+  FinishShared* lead = csize > 1 ? cluster.map_shared_rank(&sh, 0) : &sh;
   // the first sequence's input-only work overlaps the end of the stream pass;
   // then wait for the stream pass (programmatic dependent launch) before
   // reading its output
-  if (blockIdx.x < P.B) finish_prologue(P, blockIdx.x, sh);
+  if (rank == 0 && cid < P.B) finish_prologue(P, cid, sh);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
-  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    if (b != static_cast<int>(blockIdx.x)) {
+  for (int b = cid; b < P.B; b += ncl) {
+    if (rank == 0) {
+      if (b != cid) {
+        __syncthreads();
+        finish_prologue(P, b, sh);
+      }
       __syncthreads();
-      finish_prologue(P, b, sh);
+      finish_front<TT, TD>(P, b, sh);
+      __syncthreads();
     }
-    __syncthreads();
-    finish_sequence<TT, TD>(P, b, sh);
+    if (csize > 1) cluster.sync();  // the leading CTA's decision, visible to the cluster
+    const int fmode = lead->fmode;
+    if (fmode == 2) dense_chunk_sums<TT, TD>(P, b, *lead, lead->tile, rank, csize);
+    if (csize > 1) cluster.sync();  // every chunk mass is in the leading CTA
+    else __syncthreads();
+    if (rank == 0 && fmode >= 0) finish_back<TT, TD>(P, b, sh);
   }
 }
 
