@@ -64,6 +64,34 @@ static double logit_at(const void* L, int dt, int64_t i) {
  * "non-finite observations fail closed" rule of [R]. */
 int oracle_softmax_row(const void* logits, int dt, int64_t V, double T,
                        double* p, double* row_max, double* row_lse) {
+  if (T == 0.0) {
+    /* Reading for temperature 0 (greedy decoding): the distribution is the
+     * T -> 0 limit of the temperature softmax, one-hot at the largest logit;
+     * among equal largest logits, the first (smallest index).  Reported row
+     * statistics: (max L, max L), the limit of T * (max, lse) of L / T. */
+    double m = -INFINITY;
+    int64_t best = -1;
+    int bad = 0;
+    for (int64_t v = 0; v < V; ++v) {
+      double x = logit_at(logits, dt, v);
+      if (isnan(x) || (isinf(x) && x > 0)) bad = 1;
+      if (x > m) {
+        m = x;
+        best = v;
+      }
+    }
+    if (row_max) *row_max = m;
+    if (bad || best < 0) {
+      if (row_lse) *row_lse = NAN;
+      return 1;
+    }
+    if (p) {
+      for (int64_t v = 0; v < V; ++v) p[v] = 0.0;
+      p[best] = 1.0;
+    }
+    if (row_lse) *row_lse = m;
+    return 0;
+  }
   double m = -INFINITY;
   int bad = 0;
   for (int64_t v = 0; v < V; ++v) {
@@ -415,7 +443,7 @@ int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_
                   int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                   double* row_stats, double* margin, double* margin_pick,
                   int32_t* degenerate, int nthreads) {
-  if (B < 0 || k < 1 || V < 1 || !(T > 0.0) || isinf(T)) return 1;
+  if (B < 0 || k < 1 || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
   if (B == 0) return 0;
   if (!Lt || !Ld || !D || !gate || !tau || !accepted_len || !tokens || !alpha || !flags) return 1;
   if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;

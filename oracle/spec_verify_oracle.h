@@ -69,6 +69,8 @@ double oracle_uniform(uint64_t seed, uint64_t seq, uint32_t pos, uint32_t draw);
 
 /* Temperature softmax of one row of V logits (element type dt):
  * p[v] = exp(L[v]/T - m) / sum_w exp(L[w]/T - m), m = max_v L[v]/T.
+ * T = 0 is greedy decoding: p is one-hot at the first largest logit, and
+ * *row_max = *row_lse = max_v L[v].
  * Writes p (may be NULL), *row_max = m and *row_lse = m + ln(sum).
  * Returns 0, or 1 when the row is invalid (a NaN or +inf logit, or every
  * logit -inf). */
@@ -97,6 +99,8 @@ int64_t oracle_inverse_cdf(const double* r, int64_t V, double u, double* margin)
  *   from the residual / bonus pick (its interval edges and, in gated mode, the
  *   gate membership of the residual row's tokens), degenerate[B] = 1 when the
  *   residual had zero mass.
+ * T = 0 runs the same rule on the one-hot (greedy) distributions of
+ * oracle_softmax_row.
  * nthreads >= 1 threads split the sequences.  Returns 0, or 1 on bad args.
  */
 int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,

@@ -379,3 +379,77 @@ def test_margin_reports_draws_near_a_boundary():
     far = O.verify(Lt, Ld, np.array([[0]]), 1.0, 0, 0.5, u0=np.array([[ratio + 0.1]]),
                    u1=np.array([0.5]))
     assert near["margin"][0] < 1e-6 and far["margin"][0] > 1e-3
+
+
+# --------------------------------------------------- temperature 0 (greedy)
+
+def _greedy_case(rng, B, k, V, ties=True):
+    """Integer-valued logits (many exact ties) and drafted tokens that often
+    equal a row's argmax."""
+    Lt = rng.integers(-3, 4, size=(B, k + 1, V)).astype(np.float32)
+    Ld = (Lt[:, :k] + rng.integers(-1, 2, size=(B, k, V))).astype(np.float32)
+    if not ties:
+        Lt += rng.permutation(V)[None, None, :].astype(np.float32) * 1e-3
+        Ld += rng.permutation(V)[None, None, :].astype(np.float32) * 1e-3
+    D = np.where(rng.random((B, k)) < 0.7, np.argmax(Lt[:, :k], axis=2),
+                 np.where(rng.random((B, k)) < 0.5, np.argmax(Ld, axis=2),
+                          rng.integers(0, V, size=(B, k)))).astype(np.int32)
+    return Lt, Ld, D
+
+
+@pytest.mark.parametrize("gated", [0, 1])
+def test_greedy_is_the_argmax_chain(gated):
+    # T = 0: p and q are one-hot at the first largest logit (numpy's argmax
+    # convention), so the rule reduces to: NULL (gated) where D differs from
+    # the draft argmax, reject where it differs from the target argmax, and
+    # emit the target argmax of the stop row
+    rng = np.random.default_rng(41 + gated)
+    B, k, V = 400, 4, 9
+    Lt, Ld, D = _greedy_case(rng, B, k, V)
+    out = O.verify(Lt, Ld, D, 0.0, gated, 0.5, seed=5)
+    tstar = np.argmax(Lt, axis=2)
+    dstar = np.argmax(Ld, axis=2)
+    for b in range(B):
+        j = 0
+        flags = []
+        while j < k:
+            if gated and D[b, j] != dstar[b, j]:
+                flags.append(O.FLAG_NULL)
+                break
+            if D[b, j] != tstar[b, j]:
+                flags.append(O.FLAG_REJECT)
+                break
+            flags.append(O.FLAG_ACCEPT)
+            j += 1
+        assert out["accepted_len"][b] == j
+        assert list(out["tokens"][b, :j]) == list(D[b, :j])
+        assert out["tokens"][b, j] == tstar[b, j]
+        assert all(t == -1 for t in out["tokens"][b, j + 1:])
+        assert list(out["flags"][b, :len(flags)]) == flags
+        admitted = (D[b] == dstar[b]) if gated else np.ones(k, bool)
+        assert np.array_equal(out["alpha"][b], (admitted & (D[b] == tstar[b, :k])).astype(float))
+
+
+def test_greedy_ties_take_the_first_maximum():
+    Lt = np.array([[[1.0, 3.0, 3.0, 2.0], [0.0, 5.0, 0.0, 5.0]]], dtype=np.float32)
+    Ld = np.array([[[3.0, 3.0, 0.0, 0.0]]], dtype=np.float32)
+    out = O.verify(Lt, Ld, np.array([[1]]), 0.0, 0, 0.5)
+    assert out["accepted_len"][0] == 1 and list(out["tokens"][0]) == [1, 1]
+    out = O.verify(Lt, Ld, np.array([[2]]), 0.0, 0, 0.5)
+    assert out["accepted_len"][0] == 0 and list(out["tokens"][0]) == [1, -1]
+    out = O.verify(Lt, Ld, np.array([[1]]), 0.0, 1, 0.5)  # draft argmax is token 0: NULL
+    assert out["flags"][0, 0] == O.FLAG_NULL and list(out["tokens"][0]) == [1, -1]
+
+
+@pytest.mark.parametrize("gated", [0, 1])
+def test_greedy_is_the_low_temperature_limit(gated):
+    # with every maximum ahead of the runner-up by at least 1e-3, T = 1e-7
+    # makes every probability but the largest exp(-1e4): zero in double, so
+    # the ordinary rule at that temperature must do what the greedy rule does
+    rng = np.random.default_rng(7 + gated)
+    Lt, Ld, D = _greedy_case(rng, 300, 3, 12, ties=False)
+    g = O.verify(Lt, Ld, D, 0.0, gated, 0.5, seed=11)
+    t = O.verify(Lt, Ld, D, 1e-7, gated, 0.5, seed=11)
+    for key in ("accepted_len", "tokens", "flags"):
+        assert np.array_equal(g[key], t[key]), key
+    assert np.allclose(g["alpha"], t["alpha"], atol=1e-12)
