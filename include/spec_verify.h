@@ -105,7 +105,11 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
 /* Verify a batch (the spec call).
  *   target_logits [B, k+1, V] of dtype tdt, draft_logits [B, k, V] of dtype ddt,
  *   draft_tokens [B, k] int32 -- device, read-only.
- *   temperature: finite, > 0.
+ *   temperature: finite, >= 0.  0 is greedy decoding: p_j and q_j are one-hot
+ *     at the row's first largest logit (the T -> 0 limit), so a position is
+ *     accepted iff D_j is the target argmax (gated: NULL iff D_j is not the
+ *     draft argmax), alpha is 1 or 0, the stop row emits its target argmax,
+ *     no uniform is drawn, and row_stats holds (max L, max L).
  *   gate_mode / threshold: the default mode and threshold of every sequence;
  *     threshold must lie in (0, 1] when gate_mode is SV_GATED_MU.
  *   gate_mode_per_seq [B] uint8 (0 plain, 1 gated) and threshold_per_seq [B]

@@ -48,20 +48,28 @@ constexpr int dyn_smem() {
 }
 
 // opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
-template <typename TT, typename TD>
-cudaError_t configure(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD>,
+template <typename TT, typename TD, bool G>
+cudaError_t configure_one() {
+  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(sv::finish_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(sizeof(sv::FinishShared)));
+  return cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(sizeof(sv::FinishShared)));
+}
+
+// both variants (sampling and greedy) of a dtype pair: opt the kernels into
+// their dynamic shared memory and ask how many stream CTAs fit on an SM
+template <typename TT, typename TD>
+cudaError_t configure(int* blocks_per_sm) {
+  cudaError_t e = configure_one<TT, TD, false>();
+  if (e == cudaSuccess) e = configure_one<TT, TD, true>();
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::stream_kernel<TT, TD>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::stream_kernel<TT, TD, false>,
                                                        sv::Stages<TT, TD>::kThreadsPerCta,
                                                        dyn_smem<TT, TD>());
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool G>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
                  cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
@@ -72,8 +80,8 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   if (grid < 1) grid = 1;
   const bool marked = h->mark_before != nullptr;
   if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
-  sv::stream_kernel<TT, TD><<<static_cast<unsigned>(grid), sv::Stages<TT, TD>::kThreadsPerCta,
-                              dyn_smem<TT, TD>(), st>>>(P);
+  sv::stream_kernel<TT, TD, G><<<static_cast<unsigned>(grid), sv::Stages<TT, TD>::kThreadsPerCta,
+                                 dyn_smem<TT, TD>(), st>>>(P);
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
   if (marked) {
     const cudaError_t e = cudaEventRecord(h->mark_after, st);
@@ -110,7 +118,7 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD>, P) != cudaSuccess) return SV_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G>, P) != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -227,7 +235,7 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   if (!h) return SV_EINVAL;
   if (B < 0 || B > h->max_B) return SV_EINVAL;
   if (!valid_dtype(tdt) || !valid_dtype(ddt)) return SV_EINVAL;
-  if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_EINVAL;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_EINVAL;
   if (gate_mode != SV_PLAIN && gate_mode != SV_GATED_MU) return SV_EINVAL;
   const bool default_tau_used = (gate_mode == SV_GATED_MU || gate_mode_per_seq) && !threshold_per_seq;
   if (default_tau_used && !(threshold > 0.f && threshold <= 1.f)) return SV_EINVAL;
@@ -252,7 +260,8 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.total_chunks = static_cast<unsigned>(total);
   P.div_nchunk = sv::make_fastdiv(static_cast<unsigned>(h->nchunk));
   P.div_rows = sv::make_fastdiv(static_cast<unsigned>(P.rows));
-  P.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  P.greedy = temperature == 0.f ? 1 : 0;
+  P.c = P.greedy ? 0.f : static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
   P.T = temperature;
   P.gate_default = gate_mode == SV_GATED_MU ? 1 : 0;
   P.tau_default = threshold;
@@ -284,11 +293,17 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   // path (per-sequence settings are device data: their presence counts as likely)
   const bool all_fast_gated = gate_mode == SV_GATED_MU && !gate_mode_per_seq && !threshold_per_seq &&
                               threshold * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
-  const bool dense_likely = !all_fast_gated;
-  if (tb && db) return launch<uint16_t, uint16_t>(h, P, bps, dense_likely, st);
-  if (tb && !db) return launch<uint16_t, float>(h, P, bps, dense_likely, st);
-  if (!tb && db) return launch<float, uint16_t>(h, P, bps, dense_likely, st);
-  return launch<float, float>(h, P, bps, dense_likely, st);
+  const bool dense_likely = !all_fast_gated && !P.greedy;
+  if (P.greedy) {
+    if (tb && db) return launch<uint16_t, uint16_t, true>(h, P, bps, false, st);
+    if (tb && !db) return launch<uint16_t, float, true>(h, P, bps, false, st);
+    if (!tb && db) return launch<float, uint16_t, true>(h, P, bps, false, st);
+    return launch<float, float, true>(h, P, bps, false, st);
+  }
+  if (tb && db) return launch<uint16_t, uint16_t, false>(h, P, bps, dense_likely, st);
+  if (tb && !db) return launch<uint16_t, float, false>(h, P, bps, dense_likely, st);
+  if (!tb && db) return launch<float, uint16_t, false>(h, P, bps, dense_likely, st);
+  return launch<float, float, false>(h, P, bps, dense_likely, st);
 }
 
 sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,

@@ -90,8 +90,9 @@ struct Params {
   int B, k, V, nchunk, rows;
   unsigned total_chunks;  // B * rows * nchunk
   FastDiv div_nchunk, div_rows;
-  float c;     // log2(e) / T, rounded once
+  float c;     // log2(e) / T, rounded once (0 when greedy)
   float T;
+  int greedy;  // T = 0: one-hot p and q at each row's first largest logit
   int gate_default;
   float tau_default;
   const uint8_t* gate_per_seq;
@@ -280,6 +281,17 @@ template <> struct Lane<uint16_t> {
     const uint32_t m = bmax2(m0, m1);
     return fmaxf(bf16_lo(m), bf16_hi(m));
   }
+  // f(slot, entry, value) for every entry, in increasing index order
+  template <class F>
+  __device__ __forceinline__ void visit(F&& f) const {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f(i, 2 * q, bf16_lo(w[4 * i + q]));
+        f(i, 2 * q + 1, bf16_hi(w[4 * i + q]));
+      }
+  }
   // sum_v exp2(fma(x_v, c, nmc)), four independent accumulators
   __device__ __forceinline__ float expsum(float c, float nmc) const {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -344,6 +356,13 @@ template <> struct Lane<float> {
       m1 = fmaxf(m1, fmaxf(x[e + 2], x[e + 3]));
     }
     return fmaxf(m0, m1);
+  }
+  template <class F>
+  __device__ __forceinline__ void visit(F&& f) const {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f(i, e, x[4 * i + e]);
   }
   __device__ __forceinline__ float expsum(float c, float nmc) const {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -444,6 +463,30 @@ __device__ __forceinline__ float stage_logit(const unsigned char* stage, int o) 
     return reinterpret_cast<const float*>(stage)[o];
 }
 
+// one chunk of a greedy call (temperature 0), by one warp: the chunk's largest
+// logit and the first index holding it, or index -1 when the chunk holds a
+// NaN or +inf logit (!(x <= FLT_MAX) holds exactly for those; -inf is allowed)
+template <typename T>
+__device__ __forceinline__ void process_chunk_greedy(const Params& P, const unsigned char* stage, int b,
+                                                     int r, int ch, int lane) {
+  Lane<T> regs;
+  regs.load(stage, lane);
+  const float m = warp_max(regs.max());
+  int first = kChunk;
+  bool nonfinite = false;
+  regs.visit([&](int i, int e, float x) {
+    const int o = (32 * i + lane) * Lane<T>::kVE + e;
+    if (x == m && o < first) first = o;
+    nonfinite |= !(x <= 3.402823466e38f);
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+  const bool bad = __any_sync(0xffffffffu, nonfinite);
+  if (lane == 0)
+    P.part[(static_cast<int64_t>(b) * P.rows + r) * P.nchunk + ch] =
+        make_float2(m, __int_as_float(bad ? -1 : ch * kChunk + first));
+}
+
 // one chunk, by one warp: statistics, drafted-token logit, gate candidates
 template <typename T>
 __device__ __forceinline__ void process_chunk(const Params& P, const unsigned char* stage, int b, int r,
@@ -518,7 +561,7 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   }
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kGreedy>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
     stream_kernel(const Params P) {
   constexpr int S = Stages<TT, TD>::kDepth;
@@ -562,10 +605,14 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     __syncwarp();
     const int d = Q.d[n % kItemRing];  // landed with the commit group of step n - 1
     const unsigned char* stage = ring + (n % S) * kStage;
-    if (it.y <= k)
+    if constexpr (kGreedy) {
+      if (it.y <= k) process_chunk_greedy<TT>(P, stage, it.x, it.y, it.z, lane);
+      else process_chunk_greedy<TD>(P, stage, it.x, it.y, it.z, lane);
+    } else if (it.y <= k) {
       process_chunk<TT>(P, stage, it.x, it.y, it.z, d, lane);
-    else
+    } else {
       process_chunk<TD>(P, stage, it.x, it.y, it.z, d, lane);
+    }
     __syncwarp();
   }
   cp_async_wait<0>();
@@ -668,6 +715,7 @@ struct FinishShared {
   dfloat Z;
   dfloat y;
   int fmode;  // the stop row's sampling mode (-1: the sequence is done)
+  int targ[kMaxRows];  // greedy calls: each row's first largest logit
 };
 
 // residual weights of eight consecutive entries [v0, v0 + 8): max(0, p - mu)
@@ -940,6 +988,126 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   }
 }
 
+// A greedy call (temperature 0): p and q are one-hot at each row's first
+// largest logit t*_j (target) and d*_j (draft), so the rule reduces to: a
+// gated position is NULL where D differs from d*_j, a position is accepted
+// where D equals t*_j (alpha is 1 there, 0 elsewhere), and the stop row emits
+// t*_{j*} -- the residual (p - mu)+ is one-hot at t*_{j*}, or empty when
+// t*_{j*} = d*_{j*}, which falls back to p: the same token.  No uniform is used.
+template <typename TT, typename TD>
+__device__ void finish_greedy(const Params& P, int b, FinishShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
+  const bool gated = sh.gated != 0;
+  const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
+  const bool staged = R * nch <= kFinPartCap;
+  if (staged) {
+#pragma unroll 4
+    for (int e = tid; e < R * nch; e += kFinThreads) sh.part[e] = ldcg_f2(seq_part + e);
+  }
+  __syncthreads();
+  auto part_at = [&](int r, int ch) -> float2 {
+    return staged ? sh.part[r * nch + ch] : ldcg_f2(seq_part + static_cast<int64_t>(r) * nch + ch);
+  };
+  // each row's largest logit and the first chunk holding it (half-warps)
+  {
+    const int half = lane >> 4, l16 = lane & 15;
+#pragma unroll 1
+    for (int r0 = 2 * warp; r0 < R; r0 += 2 * kFinWarps) {
+      const int r = r0 + half;
+      const bool live = r < R;
+      float M = -INFINITY;
+      int bc = nch;
+      bool bad = false;
+#pragma unroll 1
+      for (int ch = l16; live && ch < nch; ch += 16) {
+        const float2 ms = part_at(r, ch);
+        if (__float_as_int(ms.y) < 0) bad = true;
+        if (ms.x > M) {
+          M = ms.x;
+          bc = ch;
+        }
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        const float oM = __shfl_xor_sync(0xffffffffu, M, o);
+        const int obc = __shfl_xor_sync(0xffffffffu, bc, o);
+        if (oM > M || (oM == M && obc < bc)) {
+          M = oM;
+          bc = obc;
+        }
+      }
+      const unsigned badm = __ballot_sync(0xffffffffu, live && bad);
+      const bool anybad = ((badm >> (16 * half)) & 0xffffu) != 0u;
+      if (live && l16 == 0) {
+        if (anybad || M == -INFINITY || bc >= nch) {
+          sh.bad = 1;
+          sh.targ[r] = -1;
+        } else {
+          sh.targ[r] = __float_as_int(part_at(r, bc).y);
+        }
+        if (P.row_stats) {
+          P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 0] = M;
+          P.row_stats[(static_cast<int64_t>(b) * R + r) * 2 + 1] = M;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  int32_t* tok = P.tokens + static_cast<int64_t>(b) * (k + 1);
+  if (warp == 0) {
+    bool ok = true, acc = false, is_null = false;
+    if (lane < k) {
+      const int d = sh.Dv[lane];
+      ok = d >= 0 && d < V;
+      is_null = gated && d != sh.targ[k + 1 + lane];
+      acc = ok && !is_null && d == sh.targ[lane];
+    }
+    const bool any_bad = __any_sync(0xffffffffu, !ok) || sh.bad;
+    const unsigned accm = __ballot_sync(0xffffffffu, lane < k && acc);
+    int jstar = __ffs(~accm) - 1;
+    if (jstar > k || jstar < 0) jstar = k;
+    const unsigned nullm = __ballot_sync(0xffffffffu, lane < k && is_null);
+    if (lane < k) {
+      const int64_t o = static_cast<int64_t>(b) * k + lane;
+      P.alpha[o] = (!any_bad && acc) ? 1.f : 0.f;
+      if (P.flags) {
+        int8_t f;
+        if (any_bad) f = SV_FLAG_INVALID;
+        else if (lane < jstar) f = SV_FLAG_ACCEPT;
+        else if (lane == jstar) f = is_null ? SV_FLAG_NULL : SV_FLAG_REJECT;
+        else f = SV_FLAG_UNREACHED;
+        P.flags[o] = f;
+      }
+    }
+    if (any_bad) {
+      if (lane <= k) tok[lane] = -1;
+      if (lane == 0) {
+        P.accepted_len[b] = -1;
+        if (P.counters) atomicAdd(P.counters + SV_CNT_INVALID, 1ull);
+      }
+    } else {
+      if (lane < jstar) tok[lane] = sh.Dv[lane];
+      if (lane == jstar) tok[lane] = sh.targ[jstar];
+      if (lane > jstar && lane <= k) tok[lane] = -1;
+      if (lane == 0) {
+        P.accepted_len[b] = jstar;
+        if (P.counters) {
+          atomicAdd(P.counters + SV_CNT_TESTED, static_cast<unsigned long long>(jstar < k ? jstar + 1 : k));
+          atomicAdd(P.counters + SV_CNT_ACCEPTED, static_cast<unsigned long long>(jstar));
+          if (jstar < k) {
+            atomicAdd(P.counters + (((nullm >> jstar) & 1u) ? SV_CNT_NULL : SV_CNT_REJECTED), 1ull);
+            if (sh.targ[jstar] == sh.targ[k + 1 + jstar]) atomicAdd(P.counters + SV_CNT_DEGENERATE, 1ull);
+          } else {
+            atomicAdd(P.counters + SV_CNT_BONUS, 1ull);
+          }
+        }
+      }
+    }
+  }
+  if (tid == 0) sh.fmode = -1;  // nothing left to sample
+}
+
 // The dense residual's chunk masses sum max(0, p - mu) over the stop row pair
 // of sequence b (mu = q, or q on q >= tau when gated), one warp per chunk: the
 // CTAs of a cluster share the chunks (CTA r of n takes chunks r * 8 + w, then
@@ -1178,7 +1346,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
 // The finishing grid runs in clusters of one or more CTAs (a cluster per
 // sequence at a time).  The leading CTA does all the work of a sequence except
 // the dense residual's chunk masses, which every CTA of the cluster shares.
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kGreedy>
 __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) {
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
@@ -1201,7 +1369,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) 
         finish_prologue(P, b, sh);
       }
       __syncthreads();
-      finish_front<TT, TD>(P, b, sh);
+      if constexpr (kGreedy) finish_greedy<TT, TD>(P, b, sh);
+      else finish_front<TT, TD>(P, b, sh);
       __syncthreads();
     }
     if (csize > 1) cluster.sync();  // the leading CTA's decision, visible to the cluster

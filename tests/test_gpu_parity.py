@@ -283,7 +283,9 @@ def test_host_side_argument_errors(sv):
     w = _custom(4, 2, 100, "f32", 1.0, 0, 0.5, seed=1)
     ver = _verifier(sv, w)
     with pytest.raises(sv.SpecVerifyError):
-        ver.run(w.Lt, w.Ld, w.D, 0.0)
+        ver.run(w.Lt, w.Ld, w.D, -1.0)
+    with pytest.raises(sv.SpecVerifyError):
+        ver.run(w.Lt, w.Ld, w.D, float("nan"))
     with pytest.raises(sv.SpecVerifyError):
         ver.run(w.Lt, w.Ld, w.D, float("inf"))
     with pytest.raises(sv.SpecVerifyError):
@@ -313,3 +315,60 @@ def test_host_buffer_entry_point_matches_device_path(sv):
     for key in ("accepted_len", "tokens", "accept_prob", "flags"):
         assert torch.equal(dev[key].cpu(), host[key]), key
     ver.close()
+
+
+# ------------------------------------------------------ temperature 0 (greedy)
+
+def _greedy_custom(B, k, V, dtype, seed, gate):
+    """Integer-valued logits (exact ties across and inside chunks) with drafted
+    tokens that often equal a row's argmax."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    t = torch.randint(-6, 7, (B, k + 1, V), generator=g, device="cuda").float()
+    d = t[:, :k] + torch.randint(-1, 2, (B, k, V), generator=g, device="cuda").float()
+    ta, da = torch.argmax(t[:, :k], dim=2), torch.argmax(d, dim=2)
+    r = torch.rand(B, k, generator=g, device="cuda")
+    rnd = torch.randint(0, V, (B, k), generator=g, device="cuda")
+    D = torch.where(r < 0.7, ta, torch.where(r < 0.85, da, rnd)).to(torch.int32)
+    gate_t = torch.as_tensor(np.broadcast_to(np.asarray(gate, dtype=np.uint8), (B,)).copy(), device="cuda")
+    tau_t = torch.full((B,), 0.5, dtype=torch.float32, device="cuda")
+    return workloads.Workload(name="greedy", Lt=t.to(dt), Ld=d.to(dt), D=D, T=0.0, gate=gate_t, tau=tau_t,
+                              philox_seed=seed + 2, B=B, k=k, V=V, dtype=dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [20000, 4096, 67, 1])
+def test_greedy_parity(sv, dtype, V):
+    B, k = 48, 5
+    gate = (np.arange(B) % 2).astype(np.uint8)
+    w = _greedy_custom(B, k, V, dtype, seed=V + 3 * (dtype == "f32"), gate=gate)
+    ver = _verifier(sv, w)
+    cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
+    rs = ver.run(w.Lt, w.Ld, w.D, 0.0, gate_mode=sv.SV_GATED_MU, threshold=0.5, gate_per_seq=w.gate,
+                 threshold_per_seq=w.tau, seed=w.philox_seed, counters=cnt, row_stats=True)
+    torch.cuda.synchronize()
+    ref = oracle_for(w)
+    compare(w, rs, ref, what=f"greedy {dtype} V={V}")
+    # alpha is exactly 0 or 1, row statistics are (max L, max L)
+    a = rs["accept_prob"].cpu().numpy()
+    assert np.all((a == 0.0) | (a == 1.0))
+    np.testing.assert_array_equal(rs["row_stats"].cpu().numpy().astype(np.float64), ref["row_stats"])
+    c = cnt.cpu().numpy()
+    assert c[1] == ref["accepted_len"].sum() and c[5] == 0 and c[7] == ref["degenerate"].sum()
+    ver.close()
+
+
+def test_greedy_full_size_128k(sv):
+    w = workloads.make("b64_v128256_zipf_gated", seed=1234, device="cuda")
+    w.T = 0.0
+    for gate in (None, "plain"):
+        if gate is not None:
+            w = workloads.make("b64_v128256_zipf_gated", seed=1234, device="cuda", gate=gate)
+            w.T = 0.0
+        ver = _verifier(sv, w)
+        out = ver.run(w.Lt, w.Ld, w.D, 0.0, gate_mode=sv.SV_GATED_MU, threshold=0.5,
+                      gate_per_seq=w.gate, threshold_per_seq=w.tau, seed=w.philox_seed)
+        torch.cuda.synchronize()
+        compare(w, out, oracle_for(w, nthreads=16), what=f"greedy 128k {gate}")
+        ver.close()
