@@ -5,7 +5,10 @@ gate/accept decisions, residual or bonus sampling) over one batch of the
 synthetic workload, inputs resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--temperature T] [--gate plain|gated|half]
+
+--temperature and --gate override the workload's temperature (0 = greedy
+decoding) and gate recipe; the logits and drafted tokens stay the same.
 
 --impl reference times the fp64 CPU oracle on the host cores (the baseline
 arm); under torchrun only rank 0 runs it.  Multi-GPU runs shard sequences
@@ -46,6 +49,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--seed", type=int, default=1234)
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="override the workload's temperature (0 = greedy decoding)")
+    ap.add_argument("--gate", choices=["plain", "gated", "half"], default=None,
+                    help="override the workload's gate recipe")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=1.0,
@@ -58,6 +65,18 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def make_workload(args, seed, device, B=None):
+    """The named workload with the command line's temperature / gate overrides."""
+    w = workloads.make(args.workload, seed=seed, device=device, B=B, gate=args.gate)
+    if args.temperature is not None:
+        w.T = float(args.temperature)
+    return w
+
+
+def overridden(args) -> bool:
+    return args.temperature is not None or args.gate is not None
 
 
 def kernel_hash() -> str:
@@ -176,7 +195,7 @@ def run_reference(args, ws, rank):
     from oracle import oracle as O
     cfg = workloads.CONFIGS[args.workload]
     sample_B = max(1, min(cfg["B"], 8))
-    w = workloads.make(args.workload, seed=args.seed, device="cpu", B=sample_B)
+    w = make_workload(args, args.seed, "cpu", B=sample_B)
     Lt = workloads.to_numpy_logits(w.Lt)
     Ld = workloads.to_numpy_logits(w.Ld)
     D = w.D.cpu().numpy()
@@ -208,7 +227,8 @@ def run_reference(args, ws, rank):
         "ms_per_step": 1e3 * el / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "B_sample": sample_B, "k": w.k, "V": w.V,
-                   "logits_dtype": w.dtype},
+                   "logits_dtype": w.dtype, "T": w.T,
+                   "gate": args.gate or workloads.CONFIGS[args.workload]["gate"]},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -241,7 +261,7 @@ def main():
     sets = []
     nsets = 1
     for i in range(8):
-        w = workloads.make(args.workload, seed=args.seed + 1000 * rank + 7 * i, device=dev)
+        w = make_workload(args, args.seed + 1000 * rank + 7 * i, dev)
         sets.append(w)
         per_set = w.logits_bytes()
         nsets = len(sets)
@@ -351,8 +371,7 @@ def main():
     cpu = None
     if rank == 0:
         cores = os.cpu_count() or 1
-        small = workloads.make(args.workload, seed=args.seed, device="cpu",
-                               B=min(B, 16 if V > 100000 else B))
+        small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
         rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores)
         cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
                "sample": f"{small.B} sequences of {args.workload} x {reps} repetitions "
@@ -360,14 +379,16 @@ def main():
 
     if rank == 0:
         clocks = sampler.summary()
-        traffic = profile_traffic()
+        # the committed ncu summary covers the default configuration only
+        traffic = (profile_traffic() if args.workload == DEFAULT_WORKLOAD and not overridden(args)
+                   else None)
         line = {
             "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
-                       "logits_dtype": w0.dtype, "T": w0.T, "gate": cfg["gate"],
+                       "logits_dtype": w0.dtype, "T": w0.T, "gate": args.gate or cfg["gate"],
                        "threshold": cfg["tau"],
                        "l2": f"inputs larger than L2: {nsets} rotated copies of "
                              f"{per_set / 1e6:.1f} MB logits",

@@ -29,6 +29,7 @@ RULE_ARGMAX = 3
 RULE_RESAMPLE_P = 4
 RULE_RENORM_MU = 5
 RULE_RESIDUAL_Q = 6
+RULE_MU_STEP_ONLY = 7
 
 FLAG_UNREACHED, FLAG_ACCEPT, FLAG_REJECT, FLAG_NULL, FLAG_INVALID = 0, 1, 2, 3, 4
 
@@ -70,6 +71,12 @@ def lib() -> ctypes.CDLL:
                                     ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P, P,
                                     ctypes.c_int]
         L.oracle_verify.restype = ctypes.c_int
+        L.oracle_verify_policy.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
+                                           ctypes.c_int, ctypes.c_double, ctypes.c_uint64,
+                                           ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P,
+                                           P, ctypes.c_int]
+        L.oracle_verify_policy.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -118,12 +125,16 @@ def inverse_cdf(r: np.ndarray, u: float):
 
 
 def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, seed: int = 0,
-           seq_offset: int = 0, u0=None, u1=None, rule: int = RULE_MU, nthreads: int = 1):
+           seq_offset: int = 0, u0=None, u1=None, rule: int = RULE_MU, nthreads: int = 1,
+           tau_sched=None, min_cum: float = 0.0):
     """Run the oracle on a batch.
 
     Lt [B, k+1, V], Ld [B, k, V] (float32, or uint16 bf16 bits), D [B, k] int32.
     ``gate`` and ``tau`` are per-sequence arrays (or scalars broadcast to B).
     ``u0`` [B, k] / ``u1`` [B] give explicit uniforms instead of Philox draws.
+    ``tau_sched`` (a sequence of per-step thresholds, the last repeating) and
+    ``min_cum`` (the cumulative floor, 0 = off) are the gate policy of gated
+    sequences (``oracle_verify_policy``).
     Returns a dict of numpy arrays: accepted_len, tokens, alpha, flags,
     row_stats [B, 2k+1, 2] (max, lse of L/T), margin (all used draws),
     margin_pick (the residual / bonus pick alone), degenerate.
@@ -151,12 +162,15 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
         margin_pick=np.zeros(B, dtype=np.float64),
         degenerate=np.zeros(B, dtype=np.int32),
     )
-    rc = lib().oracle_verify(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B, k, V,
-                             float(T), _ptr(gate), _ptr(tau), int(seed), int(seq_offset), _ptr(u0),
-                             _ptr(u1), int(rule), _ptr(out["accepted_len"]), _ptr(out["tokens"]),
-                             _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
-                             _ptr(out["margin"]), _ptr(out["margin_pick"]),
-                             _ptr(out["degenerate"]), int(nthreads))
+    sched = None if tau_sched is None else np.ascontiguousarray(tau_sched, dtype=np.float64).ravel()
+    n_sched = 0 if sched is None else int(sched.shape[0])
+    rc = lib().oracle_verify_policy(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B,
+                                    k, V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
+                                    float(min_cum), int(seed), int(seq_offset), _ptr(u0), _ptr(u1),
+                                    int(rule), _ptr(out["accepted_len"]), _ptr(out["tokens"]),
+                                    _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
+                                    _ptr(out["margin"]), _ptr(out["margin_pick"]),
+                                    _ptr(out["degenerate"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out

@@ -172,6 +172,8 @@ typedef struct {
   int rule;
   int32_t* accepted_len; int32_t* tokens; double* alpha; int8_t* flags;
   double* row_stats; double* margin; double* margin_pick; int32_t* degenerate;
+  const double* tau_sched; int n_sched; /* per-step thresholds (NULL: tau[b] at every step) */
+  double min_cum;                       /* cumulative floor (0: no cumulative gate) */
 } job_t;
 
 typedef struct {
@@ -191,10 +193,42 @@ static double u_residual(const job_t* J, int b, int jstar) {
   return oracle_uniform(J->seed, J->seq_offset + (uint64_t)b, (uint32_t)jstar, 1u);
 }
 
+/* The gate threshold of step j of sequence b [R "schedule behavior"]: a
+ * supplied schedule overrides the sequence's threshold at every step, its last
+ * entry repeating for later steps; without one the sequence's threshold is the
+ * floor of every step. */
+static double step_threshold(const job_t* J, int b, int j) {
+  if (J->tau_sched) return J->tau_sched[j < J->n_sched ? j : J->n_sched - 1];
+  return J->tau[b];
+}
+
+/* Gate admission of a token with draft probability qv at a step whose
+ * threshold is tau_j, behind a drafted prefix whose draft probabilities
+ * multiply to cprev [R "schedule behavior"]: the per-step floor qv >= tau_j
+ * and, when the cumulative floor is positive, the prefix product including
+ * this token, cprev * qv >= min_cum -- both must hold, equality passes.  A zero
+ * floor disables the cumulative gate. */
+static int admitted(const job_t* J, double tau_j, double cprev, double qv) {
+  if (!(qv >= tau_j)) return 0;
+  if (J->min_cum > 0.0 && !(cprev * qv >= J->min_cum)) return 0;
+  return 1;
+}
+
+/* distance of a gate decision to its boundaries: |qv - tau_j| (a zero step
+ * floor admits every token whatever the rounding: no boundary) and, with a
+ * cumulative floor, |cprev * qv - min_cum| (both in probability units) */
+static double gate_margin(const job_t* J, double tau_j, double cprev, double qv) {
+  double m = tau_j > 0.0 ? fabs(qv - tau_j) : INFINITY;
+  if (J->min_cum > 0.0) m = fmin(m, fabs(cprev * qv - J->min_cum));
+  return m;
+}
+
 /* mu_j for the rule: plain mode mu = q; gated mode [S "Approach"]: q kept on
- * admitted tokens (q >= tau, equality passes [R]) and NOT renormalised.  The
- * RENORM_MU control renormalises it (the plausible mistake). */
-static void retained_measure(const job_t* J, int gated, double tau, const double* q, double* mu) {
+ * the tokens the gate would admit at this step (same predicate as the offered
+ * token's gate) and NOT renormalised.  The RENORM_MU control renormalises it
+ * (the plausible mistake). */
+static void retained_measure(const job_t* J, int gated, double tau_j, double cprev, const double* q,
+                             double* mu) {
   int64_t V = J->V;
   if (!gated) {
     memcpy(mu, q, (size_t)V * sizeof(double));
@@ -202,7 +236,8 @@ static void retained_measure(const job_t* J, int gated, double tau, const double
   }
   double kept = 0.0;
   for (int64_t v = 0; v < V; ++v) {
-    mu[v] = (q[v] >= tau) ? q[v] : 0.0;
+    const int in = J->rule == ORACLE_RULE_MU_STEP_ONLY ? (q[v] >= tau_j) : admitted(J, tau_j, cprev, q[v]);
+    mu[v] = in ? q[v] : 0.0;
     kept += mu[v];
   }
   if (J->rule == ORACLE_RULE_RENORM_MU && kept > 0.0)
@@ -213,7 +248,6 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   const int k = J->k;
   const int64_t V = J->V;
   const int gated = J->gate[b] != 0;
-  const double tau = J->tau[b];
   int32_t* tok = J->tokens + (int64_t)b * (k + 1);
   double* al = J->alpha + (int64_t)b * k;
   int8_t* fl = J->flags + (int64_t)b * k;
@@ -258,21 +292,30 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     return;
   }
 
+  /* the drafted prefix's product of draft probabilities in front of each
+   * step, reset to 1 for every verification round [R "schedule behavior"]:
+   * cprev[j] = prod_{i<j} q_i(D_i) */
+  double cprev[ORACLE_MAX_K + 1];
+  cprev[0] = 1.0;
+  for (int j = 0; j < k; ++j) cprev[j + 1] = cprev[j] * S->Q[(int64_t)j * V + Db[j]];
+
   /* step 2: acceptance probability of every position (also past j*).
    * alpha = min(1, p(D)/mu(D)); NULL -> 0; mu(D) = 0 < p(D) -> 1; p(D) = 0 -> 0. */
   for (int j = 0; j < k; ++j) {
     const double pd = S->P[(int64_t)j * V + Db[j]];
     const double qd = S->Q[(int64_t)j * V + Db[j]];
+    const double tau = step_threshold(J, b, j);
+    const int pass = admitted(J, tau, cprev[j], qd);
     double a;
-    if (J->rule == ORACLE_RULE_ORIGINAL_GATE && gated && !(qd >= tau)) {
+    if (J->rule == ORACLE_RULE_ORIGINAL_GATE && gated && !pass) {
       a = 0.0; /* failed gate: a target sample, no acceptance */
     } else if (J->rule == ORACLE_RULE_ORIGINAL_GATE || J->rule == ORACLE_RULE_SAMPLER_MATCH ||
                J->rule == ORACLE_RULE_ARGMAX) {
       a = qd > 0.0 ? fmin(1.0, pd / qd) : (pd > 0.0 ? 1.0 : 0.0);
-    } else if (gated && !(qd >= tau)) {
+    } else if (gated && !pass) {
       a = 0.0; /* explicit NULL row */
     } else {
-      retained_measure(J, gated, tau, S->Q + (int64_t)j * V, S->mu);
+      retained_measure(J, gated, tau, cprev[j], S->Q + (int64_t)j * V, S->mu);
       const double md = S->mu[Db[j]];
       a = md > 0.0 ? fmin(1.0, pd / md) : (pd > 0.0 ? 1.0 : 0.0);
     }
@@ -290,6 +333,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     const double* qj = S->Q + (int64_t)j * V;
     const int32_t d = Db[j];
     const double u = u_accept(J, b, j);
+    const double tau = step_threshold(J, b, j);
 
     if (J->rule == ORACLE_RULE_SAMPLER_MATCH) {
       /* [M] sampler-match: a fresh target draw; accept iff it equals D */
@@ -320,8 +364,8 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
       /* [S "Problem and result"]: the gate filters drafts, acceptance uses
        * the unfiltered q, and a failed gate becomes a plain target sample */
       if (gated) {
-        marg = fmin(marg, fabs(qj[d] - tau));
-        if (!(qj[d] >= tau)) {
+        marg = fmin(marg, gate_margin(J, tau, cprev[j], qj[d]));
+        if (!admitted(J, tau, cprev[j], qj[d])) {
           fl[j] = ORACLE_FLAG_NULL;
           jstar = j;
           resid_from_p = 1;
@@ -340,14 +384,14 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
 
     /* the method (and the RESAMPLE_P / RENORM_MU / RESIDUAL_Q controls) */
     if (gated) {
-      marg = fmin(marg, fabs(qj[d] - tau));
-      if (!(qj[d] >= tau)) { /* failed gate: explicit NULL row [S "Approach"] */
+      marg = fmin(marg, gate_margin(J, tau, cprev[j], qj[d]));
+      if (!admitted(J, tau, cprev[j], qj[d])) { /* failed gate: explicit NULL row [S "Approach"] */
         fl[j] = ORACLE_FLAG_NULL;
         jstar = j;
         break;
       }
     }
-    retained_measure(J, gated, tau, qj, S->mu);
+    retained_measure(J, gated, tau, cprev[j], qj, S->mu);
     const double md = S->mu[d];
     if (md > 0.0 && pj[d] < md) marg = fmin(marg, fabs(u - pj[d] / md));
     /* accept test p(D) > 0 && u * mu(D) <= p(D) [M "What changed"] */
@@ -376,13 +420,15 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     } else {
       /* residual (p - mu)+ [S "Approach"]; plain mode mu = q [M] */
       const double* qst = S->Q + (int64_t)jstar * V;
+      const double tau = step_threshold(J, b, jstar);
       if (J->rule == ORACLE_RULE_ORIGINAL_GATE || J->rule == ORACLE_RULE_RESIDUAL_Q) {
         memcpy(S->mu, qst, (size_t)V * sizeof(double));
       } else {
-        retained_measure(J, gated, tau, qst, S->mu);
+        retained_measure(J, gated, tau, cprev[jstar], qst, S->mu);
       }
       if (gated)
-        for (int64_t v = 0; v < V; ++v) marg_pick = fmin(marg_pick, fabs(qst[v] - tau));
+        for (int64_t v = 0; v < V; ++v)
+          marg_pick = fmin(marg_pick, gate_margin(J, tau, cprev[jstar], qst[v]));
       double Z = 0.0;
       for (int64_t v = 0; v < V; ++v) {
         double d = pst[v] - S->mu[v];
@@ -443,13 +489,30 @@ int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_
                   int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                   double* row_stats, double* margin, double* margin_pick,
                   int32_t* degenerate, int nthreads) {
-  if (B < 0 || k < 1 || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
+  return oracle_verify_policy(Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, NULL, 0, 0.0, seed,
+                              seq_offset, u0, u1, rule, accepted_len, tokens, alpha, flags,
+                              row_stats, margin, margin_pick, degenerate, nthreads);
+}
+
+int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                         int B, int k, int64_t V, double T,
+                         const uint8_t* gate, const double* tau,
+                         const double* tau_sched, int n_sched, double min_cum,
+                         uint64_t seed, uint64_t seq_offset,
+                         const double* u0, const double* u1, int rule,
+                         int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                         double* row_stats, double* margin, double* margin_pick,
+                         int32_t* degenerate, int nthreads) {
+  if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
+  if (tau_sched && n_sched < 1) return 1;
+  if (!(min_cum >= 0.0 && min_cum <= 1.0)) return 1;
   if (B == 0) return 0;
   if (!Lt || !Ld || !D || !gate || !tau || !accepted_len || !tokens || !alpha || !flags) return 1;
   if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
-  if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_RESIDUAL_Q) return 1;
+  if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_MU_STEP_ONLY) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
-             accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate};
+             accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate,
+             tau_sched, n_sched, min_cum};
   if (nthreads < 1) nthreads = 1;
   if (nthreads > B) nthreads = B;
   worker_t* ws = (worker_t*)calloc((size_t)nthreads, sizeof(worker_t));

@@ -21,7 +21,9 @@
  *        "Two metric corrections" (a chain stops at its first rejection).
  *   [R]  regolith audit "rank-1 moce and step-aware speculative retention",
  *        section "schedule behavior" (equality passes the gate; a failed gate
- *        ends the contiguous prefix).
+ *        ends the contiguous prefix; per-step threshold schedules whose last
+ *        entry repeats; the cumulative prefix-product floor; both floors
+ *        composed by logical and).
  *   [P]  J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel random
  *        numbers: as easy as 1, 2, 3", SC'11 -- the Philox4x32 bijection.
  *
@@ -36,6 +38,9 @@
 extern "C" {
 #endif
 
+/* largest k the oracle accepts */
+#define ORACLE_MAX_K 64
+
 /* element types of the logits arrays */
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 
@@ -48,7 +53,8 @@ enum {
   ORACLE_RULE_ARGMAX = 3,        /* [M] biased: accept iff D == argmax p, emit argmax */
   ORACLE_RULE_RESAMPLE_P = 4,    /* [M] biased: on rejection sample p, not the residual */
   ORACLE_RULE_RENORM_MU = 5,     /* plausible mistake: mu renormalised over admitted set */
-  ORACLE_RULE_RESIDUAL_Q = 6     /* plausible mistake: gated residual uses (p - q)+ */
+  ORACLE_RULE_RESIDUAL_Q = 6,    /* plausible mistake: gated residual uses (p - q)+ */
+  ORACLE_RULE_MU_STEP_ONLY = 7   /* plausible mistake: mu ignores the cumulative floor */
 };
 
 /* per-position flags (same values as the CUDA library's outputs) */
@@ -111,6 +117,31 @@ int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_
                   int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                   double* row_stats, double* margin, double* margin_pick,
                   int32_t* degenerate, int nthreads);
+
+/*
+ * oracle_verify with the gate policy of [R] "schedule behavior" for the gated
+ * sequences (gate[b] = 1):
+ *   tau_sched [n_sched] (n_sched >= 1, or NULL): per-step thresholds that
+ *     replace tau[b]; step j uses tau_sched[min(j, n_sched - 1)] (the last
+ *     entry repeats).  Entries may be 0 (no per-step floor at that step).
+ *   min_cum in [0, 1]: the cumulative floor; when positive, step j also needs
+ *     prod_{i<j} q_i(D_i) * q_j(x) >= min_cum (products in double, reset to 1
+ *     for every sequence).  0 disables it.
+ * Both floors must hold (logical and); equality passes.  The retained measure
+ * mu_j keeps q_j on every token x that the same predicate admits at step j
+ * (with the drafted prefix's product), so a failed gate is still an explicit
+ * NULL row and the residual is (p_j - mu_j)+.  margin also covers the
+ * cumulative decision, |product - min_cum|.  Returns 1 on bad args.
+ */
+int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                         int B, int k, int64_t V, double T,
+                         const uint8_t* gate, const double* tau,
+                         const double* tau_sched, int n_sched, double min_cum,
+                         uint64_t seed, uint64_t seq_offset,
+                         const double* u0, const double* u1, int rule,
+                         int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                         double* row_stats, double* margin, double* margin_pick,
+                         int32_t* degenerate, int nthreads);
 
 #ifdef __cplusplus
 }

@@ -34,17 +34,36 @@ def distributions(Lt: np.ndarray, Ld: np.ndarray, T: float):
     return P, Q
 
 
-def _u1_edges(P, Q, gated, tau, grid):
-    k = Q.shape[0]
+def _step_tau(tau, tau_sched, s):
+    if tau_sched is None:
+        return tau
+    return tau_sched[min(s, len(tau_sched) - 1)]
+
+
+def _u1_edges(P, Q, gated, tau, grid, tau_sched=None, min_cum=0.0):
+    """Cell edges of u1: the cumulative sums of every distribution a stop row
+    could sample.  With a cumulative floor the admitted set of step s depends
+    on the drafted prefix, so every prefix's product contributes its own."""
+    k, V = Q.shape
     edges = set(np.linspace(0.0, 1.0, grid + 1).tolist())
     for s in range(k + 1):
         cands = [P[s]]
         if s < k:
-            mu = Q[s] * (Q[s] >= tau) if gated else Q[s]
-            cands.append(np.maximum(P[s] - mu, 0.0))
+            ts = _step_tau(tau, tau_sched, s)
+            prods = {1.0}
+            if min_cum > 0.0:
+                prods = {float(np.prod(Q[np.arange(s), list(pre)])) if s else 1.0
+                         for pre in itertools.product(range(V), repeat=s)}
+            for c in sorted(prods):
+                keep = Q[s] >= ts
+                mus = [Q[s] * keep]
+                if min_cum > 0.0:
+                    mus.append(Q[s] * (keep & (c * Q[s] >= min_cum)))
+                for mu in (mus if gated else [Q[s]]):
+                    cands.append(np.maximum(P[s] - mu, 0.0))
+                    if gated and mu.sum() > 0:
+                        cands.append(np.maximum(P[s] - mu / mu.sum(), 0.0))
             cands.append(np.maximum(P[s] - Q[s], 0.0))
-            if gated and mu.sum() > 0:
-                cands.append(np.maximum(P[s] - mu / mu.sum(), 0.0))
         for w in cands:
             Z = w.sum()
             if Z > 0:
@@ -56,11 +75,13 @@ def _u1_edges(P, Q, gated, tau, grid):
     return e
 
 
-def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32):
+def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32, tau_sched=None, min_cum=0.0):
     """Law of (accepted_len, tokens) for one sequence, as a dict -> probability.
 
-    Lt [k+1, V], Ld [k, V] float32 (one sequence).
+    Lt [k+1, V], Ld [k, V] float32 (one sequence); tau_sched / min_cum: the
+    gate policy passed through to the oracle.
     """
+    pol = dict(tau_sched=tau_sched, min_cum=min_cum)
     Lt = np.asarray(Lt, dtype=np.float32)
     Ld = np.asarray(Ld, dtype=np.float32)
     k1, V = Lt.shape
@@ -72,10 +93,10 @@ def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32):
 
     # the oracle's acceptance probability of every position for every draft outcome
     base = O.verify(np.broadcast_to(Lt, (nD, k1, V)), np.broadcast_to(Ld, (nD, k, V)), drafts, T,
-                    gated, tau, u0=np.full((nD, k), 0.5), u1=np.full(nD, 0.5), rule=rule)
+                    gated, tau, u0=np.full((nD, k), 0.5), u1=np.full(nD, 0.5), rule=rule, **pol)
     alpha = base["alpha"]
 
-    edges = _u1_edges(P, Q, gated, tau, grid)
+    edges = _u1_edges(P, Q, gated, tau, grid, tau_sched, min_cum)
     lo, hi = edges[:-1], edges[1:]
     mids = 0.5 * (lo + hi)
     vols = hi - lo
@@ -104,7 +125,7 @@ def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32):
     pw = np.concatenate(probes_w)
     n = pd.shape[0]
     out = O.verify(np.broadcast_to(Lt, (n, k1, V)), np.broadcast_to(Ld, (n, k, V)), drafts[pd], T,
-                   gated, tau, u0=pu0, u1=pu1, rule=rule, nthreads=4)
+                   gated, tau, u0=pu0, u1=pu1, rule=rule, nthreads=4, **pol)
     law: dict = {}
     for acc, toks, w in zip(out["accepted_len"], out["tokens"], pw):
         key = (int(acc), tuple(int(t) for t in toks))

@@ -453,3 +453,154 @@ def test_greedy_is_the_low_temperature_limit(gated):
     for key in ("accepted_len", "tokens", "flags"):
         assert np.array_equal(g[key], t[key]), key
     assert np.allclose(g["alpha"], t["alpha"], atol=1e-12)
+
+
+# ------------------------------------------- gate policy: schedules, cumulative floor
+
+def _policy_rows(qs, V=10):
+    """One gated sequence whose drafted token at step j has draft probability
+    exactly qs[j] (1/n for n equal logits, the rest -inf) and whose target rows
+    equal its draft rows, so every admitted draft is accepted (alpha = 1) and
+    the accepted length counts the drafts the gate retains."""
+    k = len(qs)
+    Ld = np.full((1, k, V), -np.inf, dtype=np.float32)
+    for j, q in enumerate(qs):
+        n = int(round(1.0 / q))
+        assert abs(n * q - 1.0) < 1e-12
+        Ld[0, j, :n] = 0.0
+    Lt = np.concatenate([Ld, Ld[:, :1]], axis=1)  # bonus row: any valid row
+    D = np.zeros((1, k), dtype=np.int32)
+    return Lt, Ld, D
+
+
+def _floats(text):
+    return [float(x) for x in text.split(",")]
+
+
+@pytest.mark.parametrize("row", range(8))
+def test_gate_policy_worked_examples_retain_as_printed(row):
+    rows = _golden_rows("gate_schedule_example.txt")
+    kind, qs, sched, cum, want = rows[row]
+    Lt, Ld, D = _policy_rows(_floats(qs))
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.99, seed=3, tau_sched=_floats(sched), min_cum=float(cum))
+    got = int(out["accepted_len"][0])
+    if want.startswith(">="):
+        assert got >= int(want[2:])
+    else:
+        assert got == int(want), (kind, qs, sched, cum)
+    k = len(_floats(qs))
+    if got < k:  # the failed gate is an explicit NULL row that ends the prefix
+        assert out["flags"][0, got] == O.FLAG_NULL
+        assert np.all(out["flags"][0, got + 1:] == O.FLAG_UNREACHED)
+        assert out["alpha"][0, got] == 0.0
+    assert np.all(out["flags"][0, :got] == O.FLAG_ACCEPT)
+
+
+def test_gate_policy_cumulative_floor_just_above_a_product_fails():
+    # the survival rows meet their floors exactly; the next double up fails
+    Lt, Ld, D = _policy_rows([0.5, 0.5, 0.5])
+    for floor, want in ((0.5, 0), (0.25, 1), (0.125, 2)):
+        out = O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.0], min_cum=np.nextafter(floor, 1.0))
+        assert out["accepted_len"][0] == want
+
+
+def test_gate_policy_last_threshold_repeats():
+    # schedule (0.1, 0.6): steps 2 and 3 use 0.6 as well
+    Lt, Ld, D = _policy_rows([0.5, 1.0, 1.0, 0.5])
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.99, tau_sched=[0.1, 0.6])
+    assert out["accepted_len"][0] == 3 and out["flags"][0, 3] == O.FLAG_NULL
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.99, tau_sched=[0.1, 0.6, 0.6, 0.5])
+    assert out["accepted_len"][0] == 4
+
+
+def test_gate_policy_floors_compose_by_logical_and():
+    Lt, Ld, D = _policy_rows([0.5, 0.5, 0.5])
+    # the step floor passes every step, the cumulative floor fails step 2
+    assert O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.35], min_cum=0.2)["accepted_len"][0] == 2
+    # the cumulative floor passes step 0 (0.25 >= 0.2), the step floor fails it
+    Lt, Ld, D = _policy_rows([0.25, 1.0])
+    assert O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.35], min_cum=0.2)["accepted_len"][0] == 0
+    assert O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.2], min_cum=0.2)["accepted_len"][0] == 2
+
+
+def test_gate_policy_special_cases_reduce_to_the_plain_and_flat_rules():
+    rng = np.random.default_rng(77)
+    B, k, V = 300, 4, 40
+    Lt = (rng.standard_normal((B, k + 1, V)) * 2.5).astype(np.float32)
+    Ld = (Lt[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    D = np.argmax(Ld + rng.gumbel(size=Ld.shape), axis=2).astype(np.int32)
+    keys = ("accepted_len", "tokens", "flags", "alpha")
+    # schedule 0 and floor 0: every token is admitted, mu = q -- plain mode
+    a = O.verify(Lt, Ld, D, 1.0, 1, 0.9, seed=9, tau_sched=[0.0], min_cum=0.0)
+    b = O.verify(Lt, Ld, D, 1.0, 0, 0.9, seed=9)
+    for key in keys:
+        assert np.array_equal(a[key], b[key]), key
+    # a flat one-entry schedule overrides every sequence's own threshold
+    a = O.verify(Lt, Ld, D, 1.0, 1, rng.uniform(0.05, 1.0, B), seed=9, tau_sched=[0.3])
+    b = O.verify(Lt, Ld, D, 1.0, 1, 0.3, seed=9)
+    for key in keys:
+        assert np.array_equal(a[key], b[key]), key
+    # a cumulative floor never admits more than the step floor alone
+    a = O.verify(Lt, Ld, D, 1.0, 1, 0.3, seed=9, min_cum=0.05)
+    assert np.all(a["accepted_len"] <= b["accepted_len"])
+    # plain sequences ignore the policy
+    a = O.verify(Lt, Ld, D, 1.0, 0, 0.3, seed=9, tau_sched=[0.9, 0.1], min_cum=0.5)
+    c = O.verify(Lt, Ld, D, 1.0, 0, 0.3, seed=9)
+    for key in keys:
+        assert np.array_equal(a[key], c[key]), key
+
+
+def _check_emits_p(law, P, tol=1e-10):
+    k = P.shape[0] - 1
+    reach, emit, _ = position_marginals(law, k, P.shape[1])
+    assert abs(sum(law.values()) - 1.0) < tol
+    for j in range(k + 1):
+        if reach[j] > 1e-9:
+            np.testing.assert_allclose(emit[j] / reach[j], P[j], atol=tol / reach[j])
+
+
+@pytest.mark.parametrize("V,k,sched,cum", [(3, 2, [0.0], 0.2), (4, 3, [0.1, 0.3], 0.05),
+                                           (4, 2, [0.25], 0.1), (5, 2, [0.3, 0.0], 0.0)])
+def test_exact_law_is_lossless_under_gate_policy(V, k, sched, cum):
+    # [S "Approach"]: keeping q on the admitted set, the failed gate as a NULL
+    # row and the residual (p - mu)+ preserve p whatever the admitted set, as
+    # long as it depends on the committed prefix only -- here the schedule and
+    # the prefix product
+    rng = np.random.default_rng(1000 * V + 100 * k + int(100 * cum))
+    for trial in range(2):
+        Lt, Ld = _random_case(rng, V, k, scale=1.5 + trial)
+        law = exact_law(Lt, Ld, 1.0, True, 0.99, tau_sched=sched, min_cum=cum)
+        P, _ = distributions(Lt, Ld, 1.0)
+        _check_emits_p(law, P)
+
+
+def test_exact_law_rejects_mu_without_the_cumulative_floor():
+    # p = q on step 0 and step 1; step 1's admitted set shrinks when the
+    # prefix product is low, and a mu that ignores it is no longer lossless
+    p0 = np.array([0.45, 0.35, 0.2])
+    p1 = np.array([0.6, 0.3, 0.1])
+    q1 = np.array([0.7, 0.2, 0.1])
+    Lt = np.log(np.stack([p0, p1, p1])).astype(np.float32)
+    Ld = np.log(np.stack([p0, q1])).astype(np.float32)
+    P, _ = distributions(Lt, Ld, 1.0)
+    good = exact_law(Lt, Ld, 1.0, True, 0.99, tau_sched=[0.0], min_cum=0.2)
+    _check_emits_p(good, P)
+    bad = exact_law(Lt, Ld, 1.0, True, 0.99, tau_sched=[0.0], min_cum=0.2, rule=O.RULE_MU_STEP_ONLY)
+    _, emit, _ = position_marginals(bad, 2, 3)
+    reach, _, _ = position_marginals(bad, 2, 3)
+    assert np.max(np.abs(emit[1] / reach[1] - P[1])) > 1e-3
+
+
+def test_gate_policy_margin_covers_the_cumulative_decision():
+    Lt, Ld, D = _policy_rows([0.5, 0.5])
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.0], min_cum=0.25 + 3e-7)
+    assert out["margin"][0] < 1e-6 and out["accepted_len"][0] == 1
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.0], min_cum=0.3)
+    assert out["margin"][0] > 1e-3
+
+
+def test_gate_policy_bad_arguments_are_rejected():
+    Lt, Ld, D = _policy_rows([0.5])
+    for kw in (dict(tau_sched=[]), dict(min_cum=-0.1), dict(min_cum=1.5), dict(min_cum=np.nan)):
+        with pytest.raises(ValueError):
+            O.verify(Lt, Ld, D, 1.0, 1, 0.5, **kw)
