@@ -6,9 +6,12 @@ synthetic workload, inputs resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--temperature T] [--gate plain|gated|half]
+                  [--gate-schedule T0,T1,...] [--min-cum F]
 
 --temperature and --gate override the workload's temperature (0 = greedy
 decoding) and gate recipe; the logits and drafted tokens stay the same.
+--gate-schedule / --min-cum set the gate policy of the gated sequences
+(per-step thresholds, the last repeating; the cumulative prefix-product floor).
 
 --impl reference times the fp64 CPU oracle on the host cores (the baseline
 arm); under torchrun only rank 0 runs it.  Multi-GPU runs shard sequences
@@ -53,6 +56,10 @@ def parse():
                     help="override the workload's temperature (0 = greedy decoding)")
     ap.add_argument("--gate", choices=["plain", "gated", "half"], default=None,
                     help="override the workload's gate recipe")
+    ap.add_argument("--gate-schedule", default=None,
+                    help="per-step gate thresholds, comma-separated (the last repeats)")
+    ap.add_argument("--min-cum", type=float, default=0.0,
+                    help="cumulative floor on the drafted prefix's product of draft probabilities")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=1.0,
@@ -76,7 +83,15 @@ def make_workload(args, seed, device, B=None):
 
 
 def overridden(args) -> bool:
-    return args.temperature is not None or args.gate is not None
+    return (args.temperature is not None or args.gate is not None or args.gate_schedule is not None
+            or args.min_cum > 0)
+
+
+def gate_policy(args):
+    sched = None
+    if args.gate_schedule is not None:
+        sched = [float(x) for x in args.gate_schedule.split(",")]
+    return sched, float(args.min_cum)
 
 
 def kernel_hash() -> str:
@@ -169,7 +184,7 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def cpu_oracle_rate(w, seconds: float, nthreads: int):
+def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
     """Time the fp64 oracle on the workload's sequences for about `seconds`."""
     from oracle import oracle as O
     Lt = workloads.to_numpy_logits(w.Lt)
@@ -177,10 +192,11 @@ def cpu_oracle_rate(w, seconds: float, nthreads: int):
     D = w.D.cpu().numpy()
     gate = w.gate.cpu().numpy()
     tau = w.tau.cpu().numpy().astype(np.float64)
-    O.verify(Lt[:1], Ld[:1], D[:1], w.T, gate[:1], tau[:1], seed=w.philox_seed)  # build + warm
+    pol = dict(tau_sched=sched, min_cum=cum)
+    O.verify(Lt[:1], Ld[:1], D[:1], w.T, gate[:1], tau[:1], seed=w.philox_seed, **pol)  # build + warm
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=nthreads)
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=nthreads, **pol)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -202,8 +218,10 @@ def run_reference(args, ws, rank):
     gate = w.gate.cpu().numpy()
     tau = w.tau.cpu().numpy().astype(np.float64)
     cores = os.cpu_count() or 1
+    sched, cum = gate_policy(args)
+    pol = dict(tau_sched=sched, min_cum=cum)
     t0 = time.perf_counter()
-    O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+    O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
     t_step = time.perf_counter() - t0
     # a deliberately slow program: bound the whole run to a few minutes
     budget = 150.0
@@ -213,10 +231,10 @@ def run_reference(args, ws, rank):
         warm = min(warm, 3)
         steps = max(1, int(budget / t_step) - warm)
     for _ in range(warm):
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
     t0 = time.perf_counter()
     for _ in range(steps):
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores)
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
     el = time.perf_counter() - t0
     value = steps * sample_B * w.k / el
     sample = (f"{sample_B} of {cfg['B']} sequences of {args.workload} per step; "
@@ -228,7 +246,8 @@ def run_reference(args, ws, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "B_sample": sample_B, "k": w.k, "V": w.V,
                    "logits_dtype": w.dtype, "T": w.T,
-                   "gate": args.gate or workloads.CONFIGS[args.workload]["gate"]},
+                   "gate": args.gate or workloads.CONFIGS[args.workload]["gate"],
+                   "gate_schedule": sched, "min_cum": cum},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -270,6 +289,9 @@ def main():
     w0 = sets[0]
     k, V = w0.k, w0.V
     ver = sv.SpecVerifier(B, k, V, device=local)
+    sched, cum = gate_policy(args)
+    if sched is not None or cum > 0:
+        ver.set_gate_policy(sched, cum)
     outs = [ver.outputs(B) for _ in range(nsets)]
     seq_offset = rank * B
     stream = torch.cuda.current_stream(dev)
@@ -372,7 +394,7 @@ def main():
     if rank == 0:
         cores = os.cpu_count() or 1
         small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
-        rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores)
+        rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores, sched, cum)
         cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
                "sample": f"{small.B} sequences of {args.workload} x {reps} repetitions "
                          f"({cel:.1f} s)"}
@@ -389,6 +411,7 @@ def main():
             "data": "synthetic",
             "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
                        "logits_dtype": w0.dtype, "T": w0.T, "gate": args.gate or cfg["gate"],
+                       "gate_schedule": sched, "min_cum": cum,
                        "threshold": cfg["tau"],
                        "l2": f"inputs larger than L2: {nsets} rotated copies of "
                              f"{per_set / 1e6:.1f} MB logits",

@@ -84,7 +84,8 @@ enum {
   SV_CNT_NULL = 2,       /* NULL rows */
   SV_CNT_REJECTED = 3,   /* rejections */
   SV_CNT_BONUS = 4,      /* sequences that accepted all k drafts */
-  SV_CNT_BOUNDARY = 5,   /* draws whose uniform (or gated q(D)) lay within 1e-6 of its boundary */
+  SV_CNT_BOUNDARY = 5,   /* draws whose uniform (or gated q(D), or the prefix product of the
+                            cumulative floor) lay within 1e-6 of its boundary */
   SV_CNT_INVALID = 6,    /* sequences rejected as invalid input */
   SV_CNT_DEGENERATE = 7, /* residuals with no mass that fell back to sampling p */
   SV_NUM_COUNTERS = 8
@@ -174,6 +175,30 @@ sv_status spec_verify_run_host(spec_verify_t h,
                                int32_t* accepted_len, int32_t* tokens, float* accept_prob,
                                int8_t* flags, uint64_t* counters,
                                void* cuda_stream);
+
+/* Gate policy of the gated sequences of every later call on this handle
+ * (regolith audit "rank-1 moce and step-aware speculative retention", section
+ * "schedule behavior"):
+ *   schedule [n_schedule] host floats, each finite and in [0, 1], with
+ *     1 <= n_schedule <= SV_MAX_K; or NULL with n_schedule = 0 for none.
+ *     Step j uses schedule[min(j, n_schedule - 1)] (the last entry repeats)
+ *     IN PLACE OF the sequence's threshold, which is then neither used nor
+ *     checked; 0 removes the per-step floor at that step.
+ *   min_cum: finite, in [0, 1].  When positive, step j also requires the
+ *     drafted prefix's product of draft probabilities to stay at or above it:
+ *     prod_{i<j} q_i(D_i) * q_j(x) >= min_cum (reset to 1 for every sequence
+ *     and call).  0 disables this floor.
+ * Both floors must hold (logical and); equality passes.  A failed gate is the
+ * explicit NULL row as before, and mu_j keeps q_j on every token x the same
+ * predicate admits at step j, so the output law stays p.  Temperature 0 uses
+ * the same predicate on one-hot q.  The host copies the schedule; later calls
+ * carry the policy in their launch arguments, so calls already enqueued keep
+ * the policy they were issued with.  Default: no schedule, min_cum = 0.
+ * Returns SV_EINVAL for a NULL handle or a malformed policy, and then leaves
+ * the previous policy in place.  spec_verify_run_noalloc has no handle and
+ * always runs without a policy. */
+sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, int n_schedule,
+                                      float min_cum);
 
 /* Release the handle and its device memory (NULL is a no-op).  Synchronises
  * the handle's device first. */

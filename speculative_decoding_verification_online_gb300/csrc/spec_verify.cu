@@ -29,6 +29,10 @@ struct spec_verify_s {
   // staging for spec_verify_run_host (allocated on first use)
   void* stage = nullptr;
   size_t stage_bytes = 0;
+  // gate policy (spec_verify_set_gate_policy): schedule entries, cumulative floor
+  int n_sched = 0;
+  float sched[SV_MAX_K] = {};
+  float min_cum = 0.f;
 };
 
 namespace {
@@ -48,7 +52,7 @@ constexpr int dyn_smem() {
 }
 
 // opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
-template <typename TT, typename TD, bool G>
+template <typename TT, typename TD, int G>
 cudaError_t configure_one() {
   cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
@@ -57,19 +61,22 @@ cudaError_t configure_one() {
                               static_cast<int>(sizeof(sv::FinishShared)));
 }
 
-// both variants (sampling and greedy) of a dtype pair: opt the kernels into
-// their dynamic shared memory and ask how many stream CTAs fit on an SM
+// every variant (sampling, sampling with a gate policy, greedy) of a dtype
+// pair: opt the kernels into their dynamic shared memory and ask how many
+// stream CTAs fit on an SM
 template <typename TT, typename TD>
 cudaError_t configure(int* blocks_per_sm) {
-  cudaError_t e = configure_one<TT, TD, false>();
-  if (e == cudaSuccess) e = configure_one<TT, TD, true>();
+  cudaError_t e = configure_one<TT, TD, sv::kModeSample>();
+  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>();
+  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>();
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, sv::stream_kernel<TT, TD, false>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
+                                                       sv::stream_kernel<TT, TD, sv::kModeSample>,
                                                        sv::Stages<TT, TD>::kThreadsPerCta,
                                                        dyn_smem<TT, TD>());
 }
 
-template <typename TT, typename TD, bool G>
+template <typename TT, typename TD, int G>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
                  cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
@@ -120,6 +127,16 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   cfg.numAttrs = csize > 1 ? 2 : 1;
   if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G>, P) != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+// the kernel variant G for the call's logits types (tb / db: bf16)
+template <int G>
+sv_status launch_mode(spec_verify_t h, const sv::Params& P, int bps, bool dense_likely, bool tb, bool db,
+                      cudaStream_t st) {
+  if (tb && db) return launch<uint16_t, uint16_t, G>(h, P, bps, dense_likely, st);
+  if (tb && !db) return launch<uint16_t, float, G>(h, P, bps, dense_likely, st);
+  if (!tb && db) return launch<float, uint16_t, G>(h, P, bps, dense_likely, st);
+  return launch<float, float, G>(h, P, bps, dense_likely, st);
 }
 
 struct DeviceGuard {
@@ -237,7 +254,9 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   if (!valid_dtype(tdt) || !valid_dtype(ddt)) return SV_EINVAL;
   if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_EINVAL;
   if (gate_mode != SV_PLAIN && gate_mode != SV_GATED_MU) return SV_EINVAL;
-  const bool default_tau_used = (gate_mode == SV_GATED_MU || gate_mode_per_seq) && !threshold_per_seq;
+  // a schedule replaces the sequences' thresholds, which then go unchecked
+  const bool default_tau_used =
+      (gate_mode == SV_GATED_MU || gate_mode_per_seq) && !threshold_per_seq && h->n_sched == 0;
   if (default_tau_used && !(threshold > 0.f && threshold <= 1.f)) return SV_EINVAL;
   if (B == 0) return SV_OK;
   if (!target_logits || !draft_logits || !draft_tokens || !accepted_len || !tokens || !accept_prob)
@@ -267,6 +286,10 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.tau_default = threshold;
   P.gate_per_seq = gate_mode_per_seq;
   P.tau_per_seq = threshold_per_seq;
+  P.has_sched = h->n_sched > 0 ? 1 : 0;
+  P.min_cum = h->min_cum;
+  for (int j = 0; j < k; ++j)
+    P.tau_step[j] = h->n_sched > 0 ? h->sched[j < h->n_sched ? j : h->n_sched - 1] : 0.f;
   P.seed = seed;
   P.seq_offset = seq_offset;
   P.u0 = u_accept;
@@ -291,19 +314,16 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
   // dense residuals are likely unless every row is gated on the candidate fast
   // path (per-sequence settings are device data: their presence counts as likely)
-  const bool all_fast_gated = gate_mode == SV_GATED_MU && !gate_mode_per_seq && !threshold_per_seq &&
-                              threshold * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
+  auto fast_floor = [&](float t) {
+    return std::max(t, P.min_cum) * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
+  };
+  bool all_fast_gated = gate_mode == SV_GATED_MU && !gate_mode_per_seq &&
+                        (P.has_sched || (!threshold_per_seq && fast_floor(threshold)));
+  for (int j = 0; P.has_sched && j < k; ++j) all_fast_gated = all_fast_gated && fast_floor(P.tau_step[j]);
   const bool dense_likely = !all_fast_gated && !P.greedy;
-  if (P.greedy) {
-    if (tb && db) return launch<uint16_t, uint16_t, true>(h, P, bps, false, st);
-    if (tb && !db) return launch<uint16_t, float, true>(h, P, bps, false, st);
-    if (!tb && db) return launch<float, uint16_t, true>(h, P, bps, false, st);
-    return launch<float, float, true>(h, P, bps, false, st);
-  }
-  if (tb && db) return launch<uint16_t, uint16_t, false>(h, P, bps, dense_likely, st);
-  if (tb && !db) return launch<uint16_t, float, false>(h, P, bps, dense_likely, st);
-  if (!tb && db) return launch<float, uint16_t, false>(h, P, bps, dense_likely, st);
-  return launch<float, float, false>(h, P, bps, dense_likely, st);
+  if (P.greedy) return launch_mode<sv::kModeGreedy>(h, P, bps, false, tb, db, st);
+  if (P.has_sched || P.min_cum > 0.f) return launch_mode<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
+  return launch_mode<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
 }
 
 sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,
@@ -382,6 +402,19 @@ sv_status spec_verify_run_host(spec_verify_t h, const void* target_logits, sv_dt
   if (counters) ok = ok && cudaMemcpyAsync(counters, s + o_cnt, SV_NUM_COUNTERS * 8, cudaMemcpyDeviceToHost, st) == cudaSuccess;
   ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
   return ok ? SV_OK : SV_ECUDA;
+}
+
+sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, int n_schedule,
+                                      float min_cum) {
+  if (!h) return SV_EINVAL;
+  if (schedule ? (n_schedule < 1 || n_schedule > SV_MAX_K) : n_schedule != 0) return SV_EINVAL;
+  for (int j = 0; j < n_schedule; ++j)
+    if (!(schedule[j] >= 0.f && schedule[j] <= 1.f)) return SV_EINVAL;
+  if (!(min_cum >= 0.f && min_cum <= 1.f)) return SV_EINVAL;
+  h->n_sched = n_schedule;
+  for (int j = 0; j < SV_MAX_K; ++j) h->sched[j] = j < n_schedule ? schedule[j] : 0.f;
+  h->min_cum = min_cum;
+  return SV_OK;
 }
 
 sv_status spec_verify_free(spec_verify_t h) {

@@ -60,6 +60,12 @@ constexpr float kBoundary = 1e-6f;
 // slack * threshold * (kTopM + 1) > 1, i.e. threshold > ~0.2002.
 constexpr float kGateSlack = 1.0f - 1.0f / 1024.0f;
 
+// Kernel variants, chosen per call on the host: the sampling rule, the same
+// with a gate policy (per-step thresholds and/or a cumulative floor), and
+// greedy decoding (temperature 0, which honours the policy too).  Each is its
+// own instantiation, so the plain sampling path carries no policy code.
+enum : int { kModeSample = 0, kModePolicy = 1, kModeGreedy = 2 };
+
 struct Cand {  // a gate candidate: raw logit and token id (id -1: empty slot)
   float x;
   int v;
@@ -97,6 +103,12 @@ struct Params {
   float tau_default;
   const uint8_t* gate_per_seq;
   const float* tau_per_seq;
+  // gate policy of the gated sequences: per-step thresholds that replace the
+  // sequence's own (has_sched), and the cumulative floor on the drafted
+  // prefix's product of draft probabilities (0: off)
+  int has_sched;
+  float min_cum;
+  float tau_step[SV_MAX_K];
   uint64_t seed, seq_offset;
   const float* u0;
   const float* u1;
@@ -221,6 +233,23 @@ __device__ __forceinline__ bool seq_gated(const Params& P, int b) {
 }
 __device__ __forceinline__ float seq_tau(const Params& P, int b) {
   return P.tau_per_seq ? P.tau_per_seq[b] : P.tau_default;
+}
+// the gate threshold of step j of sequence b: the schedule's entry when the
+// policy has one, else the sequence's threshold
+__device__ __forceinline__ float step_tau(const Params& P, int b, int j) {
+  return P.has_sched ? P.tau_step[j] : seq_tau(P, b);
+}
+// a floor under everything the gate can require of q at step j: q >= tau_j,
+// and q >= cprev * q >= min_cum because the prefix product cprev is at most 1;
+// the stream pass keeps candidates against it
+__device__ __forceinline__ float step_floor(const Params& P, int b, int j) {
+  return fmaxf(step_tau(P, b, j), P.min_cum);
+}
+// gate admission of a token with draft probability q at a step with
+// threshold tau behind a prefix product cprev: both floors, equality passes
+// (cum: the policy has a cumulative floor)
+__device__ __forceinline__ bool gate_admits(float q, float tau, float cprev, bool cum, float min_cum) {
+  return q >= tau && (!cum || cprev * q >= min_cum);
 }
 
 // ------------------------------------------------------- chunk registers
@@ -488,7 +517,7 @@ __device__ __forceinline__ void process_chunk_greedy(const Params& P, const unsi
 }
 
 // one chunk, by one warp: statistics, drafted-token logit, gate candidates
-template <typename T>
+template <typename T, bool kPol>
 __device__ __forceinline__ void process_chunk(const Params& P, const unsigned char* stage, int b, int r,
                                               int ch, int d, int lane) {
   const int k = P.k;
@@ -518,7 +547,7 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   // largest term contributes 1 to s): s < kTopM + 1 rules out almost every
   // chunk before the row's gate settings are even read
   if (is_draft && s < static_cast<float>(kTopM + 1)) {
-    const float tau = seq_tau(P, b);
+    const float tau = kPol ? step_floor(P, b, j) : seq_tau(P, b);
     if (seq_gated(P, b) && gate_fast_path(tau) && s > 0.f && isfinite(s)) {
       // a token's in-chunk probability exp2(fma(x, c, -mc)) / s reaches
       // slack * tau iff fma(x, c, -mc) >= lts = log2(slack tau s); that set is a
@@ -561,9 +590,10 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   }
 }
 
-template <typename TT, typename TD, bool kGreedy>
+template <typename TT, typename TD, int kMode>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
-    stream_kernel(const Params P) {
+    stream_kernel(const __grid_constant__ Params P) {
+  constexpr bool kPol = kMode == kModePolicy;
   constexpr int S = Stages<TT, TD>::kDepth;
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
@@ -605,13 +635,13 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     __syncwarp();
     const int d = Q.d[n % kItemRing];  // landed with the commit group of step n - 1
     const unsigned char* stage = ring + (n % S) * kStage;
-    if constexpr (kGreedy) {
+    if constexpr (kMode == kModeGreedy) {
       if (it.y <= k) process_chunk_greedy<TT>(P, stage, it.x, it.y, it.z, lane);
       else process_chunk_greedy<TD>(P, stage, it.x, it.y, it.z, lane);
     } else if (it.y <= k) {
-      process_chunk<TT>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TT, kPol>(P, stage, it.x, it.y, it.z, d, lane);
     } else {
-      process_chunk<TD>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TD, kPol>(P, stage, it.x, it.y, it.z, d, lane);
     }
     __syncwarp();
   }
@@ -690,7 +720,10 @@ struct FinishShared {
   float u0[SV_MAX_K];
   float u1[SV_MAX_K + 1];    // the residual draw for every possible stop position
   int gated;
-  float tau;
+  float tau;                 // the sequence's threshold (no policy)
+  float tau_j[SV_MAX_K];     // each step's gate threshold (policy, greedy)
+  float cprev[SV_MAX_K];     // product of q_i(D_i) over i < j (cumulative floor only)
+  unsigned fast_rows;        // draft rows whose admitted set comes from candidates
   // gate candidates gathered from the per-chunk slots
   int ncand;
   int cand_j[kCandCap];
@@ -721,16 +754,18 @@ struct FinishShared {
 // residual weights of eight consecutive entries [v0, v0 + 8): max(0, p - mu)
 // with mu = 0 (mode 0: the bonus row, or a residual without mass), mu = q on
 // the admitted tokens listed (mode 1), or mu from the draft logits (mode 2:
-// q, or q on q >= tau in gated mode).  Entries past V weigh 0.
+// q where q >= tau and, with a policy, cprev q >= min_cum -- the gate's
+// predicate; a plain row, or a policy without a cumulative floor, sets the
+// unused floors to -1, which every q passes).  Entries past V weigh 0.
 struct ResidualEval {
   int mode;
-  float Mt, invSt, Md, invSd, c, tau;
-  bool gated;
+  float Mt, invSt, Md, invSd, c, tau, cprev, min_cum;
   int nadm;
   const int* adm_i;
   const float* adm_q;
 };
 
+template <bool kPol>
 __device__ __forceinline__ void residual8(const ResidualEval& e, const float (&xt)[8], const float (&xd)[8],
                                           int v0, int V, float (&r)[8]) {
 #pragma unroll
@@ -739,7 +774,8 @@ __device__ __forceinline__ void residual8(const ResidualEval& e, const float (&x
     float mu = 0.f;
     if (e.mode == 2) {
       const float q = prob_of(xd[i], e.Md, e.c, e.invSd);
-      mu = (!e.gated || q >= e.tau) ? q : 0.f;
+      if constexpr (kPol) mu = (q >= e.tau && e.cprev * q >= e.min_cum) ? q : 0.f;
+      else mu = q >= e.tau ? q : 0.f;
     }
     r[i] = v0 + i < V ? fmaxf(p - mu, 0.f) : 0.f;
   }
@@ -759,6 +795,7 @@ __device__ __forceinline__ void residual8(const ResidualEval& e, const float (&x
 // what the finishing pass of sequence b needs from the inputs alone: drafted
 // tokens, the Philox draws (or the explicit uniforms), the gate.  Runs before
 // the wait on the stream pass.
+template <int kMode>
 __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, k = P.k;
   const uint64_t s_idx = P.seq_offset + static_cast<uint64_t>(b);
@@ -778,13 +815,28 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
   if (tid < k) {
     sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
     sh.nadm[tid] = 0;
+    if constexpr (kMode != kModeSample) {
+      sh.tau_j[tid] = step_tau(P, b, tid);
+      sh.cprev[tid] = 1.f;
+    }
+  }
+  if constexpr (kMode == kModePolicy) {
+    if (tid < 32) {
+      // rows whose admitted set the stream pass collected (same predicate there)
+      const bool fast = tid < k && seq_gated(P, b) && gate_fast_path(step_floor(P, b, tid));
+      const unsigned m = __ballot_sync(0xffffffffu, fast);
+      if (tid == 0) sh.fast_rows = m;
+    }
   }
   if (tid == 0) {
     const bool gated = seq_gated(P, b);
     const float tau = seq_tau(P, b);
     sh.gated = gated ? 1 : 0;
     sh.tau = tau;
-    sh.bad = (gated && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
+    if constexpr (kMode == kModeSample)
+      sh.fast_rows = (gated && gate_fast_path(tau)) ? (k >= 32 ? 0xffffffffu : (1u << k) - 1u) : 0u;
+    // the sequence's own threshold is checked where it is used (no schedule)
+    sh.bad = (gated && !P.has_sched && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
     sh.ncand = 0;
     sh.overflow_rows = 0u;
     sh.boundary = 0;
@@ -792,13 +844,13 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
   }
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kPol>
 __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
   const bool gated = sh.gated != 0;
-  const float tau = sh.tau;
-  const bool fastgate = gated && gate_fast_path(tau);
+  const unsigned fast_rows = sh.fast_rows;
+  const bool cum = kPol && P.min_cum > 0.f;
   const float c = P.c;
   const TT* Lt = static_cast<const TT*>(P.Lt);
   const float2* seq_part = P.part + static_cast<int64_t>(b) * R * nch;
@@ -808,7 +860,7 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   // statistics, and (gated) the candidate slots, gathered into a list and
   // emptied for the next call -- in one round of independent loads
   if (tid < R) sh.xD[tid] = __ldcg(P.xD + static_cast<int64_t>(b) * R + tid);
-  if (fastgate && tid < k && __ldcg(P.cand_over + static_cast<int64_t>(b) * k + tid)) {
+  if (tid < k && ((fast_rows >> tid) & 1u) && __ldcg(P.cand_over + static_cast<int64_t>(b) * k + tid)) {
     atomicOr(&sh.overflow_rows, 1u << tid);
     P.cand_over[static_cast<int64_t>(b) * k + tid] = 0u;
   }
@@ -817,7 +869,7 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
     // round, all loads issued before any is used (one round trip)
     constexpr int kBatch = 8;
     const int np = staged ? R * nch : 0;
-    const int ns = fastgate ? k * nch * kTopM : 0;
+    const int ns = fast_rows ? k * nch * kTopM : 0;
     Cand* sc = P.cand + static_cast<int64_t>(b) * k * nch * kTopM;
     const int nmax = np > ns ? np : ns;
 #pragma unroll 1
@@ -901,42 +953,65 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   }
   __syncthreads();
 
-  // step 3: the admitted tokens (q >= tau) among the candidates, with their
-  // target probability; and, in warp 0, every draft position: gate, mu,
-  // alpha, accept test
-  if (tid < nc && !sh.bad) {
-    const int rd = k + 1 + cj;
-    const float q = prob_of(cx, sh.rowM[rd], c, sh.rowInvS[rd]);
-    if (q >= tau) {
-      const int a = atomicAdd(&sh.nadm[cj], 1);
-      if (a < kTopM) {
-        sh.adm_i[cj][a] = cv;
-        sh.adm_q[cj][a] = q;
-        sh.adm_p[cj][a] = prob_of(cxt, sh.rowM[cj], c, sh.rowInvS[cj]);
-      } else {
-        atomicOr(&sh.overflow_rows, 1u << cj);
+  // step 3: the admitted tokens among the candidates, with their target
+  // probability; and, in warp 0, every draft position: gate, mu, alpha, accept
+  // test.  With a cumulative floor a candidate's admission needs the prefix
+  // product of its step, which warp 0 computes first.
+  auto admit_candidates = [&]() {
+    if (tid < nc && !sh.bad) {
+      const int rd = k + 1 + cj;
+      const float q = prob_of(cx, sh.rowM[rd], c, sh.rowInvS[rd]);
+      if (kPol ? gate_admits(q, sh.tau_j[cj], sh.cprev[cj], cum, P.min_cum) : q >= sh.tau) {
+        const int a = atomicAdd(&sh.nadm[cj], 1);
+        if (a < kTopM) {
+          sh.adm_i[cj][a] = cv;
+          sh.adm_q[cj][a] = q;
+          sh.adm_p[cj][a] = prob_of(cxt, sh.rowM[cj], c, sh.rowInvS[cj]);
+        } else {
+          atomicOr(&sh.overflow_rows, 1u << cj);
+        }
       }
     }
-  }
+  };
+  if (!cum) admit_candidates();
   if (warp == 0) {
     bool ok = true, acc = false, is_null = false, near = false;
-    float alpha = 0.f;
+    float alpha = 0.f, p = 0.f, q = 1.f;
     if (lane < k) {
       const int d = sh.Dv[lane];
       ok = d >= 0 && d < V;
       if (ok && !sh.bad) {
         const int rt = lane, rd = k + 1 + lane;
-        const float p = prob_of(sh.xD[rt], sh.rowM[rt], c, sh.rowInvS[rt]);
-        const float q = prob_of(sh.xD[rd], sh.rowM[rd], c, sh.rowInvS[rd]);
-        const bool admitted = !gated || q >= tau;
-        const float mu = admitted ? q : 0.f;
-        is_null = !admitted;
-        alpha = is_null ? 0.f : (mu > 0.f ? fminf(1.f, p / mu) : (p > 0.f ? 1.f : 0.f));
-        const float u0 = sh.u0[lane];
-        acc = !is_null && p > 0.f && u0 * mu <= p;
-        near = (gated && fabsf(q - tau) < kBoundary) ||
-               (!is_null && mu > 0.f && p < mu && fabsf(u0 - p / mu) < kBoundary);
+        p = prob_of(sh.xD[rt], sh.rowM[rt], c, sh.rowInvS[rt]);
+        q = prob_of(sh.xD[rd], sh.rowM[rd], c, sh.rowInvS[rd]);
       }
+    }
+    float cprev = 1.f;
+    if (cum) {
+      // exclusive prefix product of q_i(D_i) over the positions (lanes past k
+      // hold 1)
+      float incl = q;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl *= y;
+      }
+      cprev = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) cprev = 1.f;
+      if (lane < k) sh.cprev[lane] = cprev;
+    }
+    if (lane < k && ok && !sh.bad) {
+      const float tau = kPol ? sh.tau_j[lane] : sh.tau;
+      const bool admitted = !gated || gate_admits(q, tau, cprev, cum, P.min_cum);
+      const float mu = admitted ? q : 0.f;
+      is_null = !admitted;
+      alpha = is_null ? 0.f : (mu > 0.f ? fminf(1.f, p / mu) : (p > 0.f ? 1.f : 0.f));
+      const float u0 = sh.u0[lane];
+      acc = !is_null && p > 0.f && u0 * mu <= p;
+      bool gate_near = fabsf(q - tau) < kBoundary;
+      if constexpr (kPol)
+        gate_near = (tau > 0.f && gate_near) || (cum && fabsf(cprev * q - P.min_cum) < kBoundary);
+      near = (gated && gate_near) || (!is_null && mu > 0.f && p < mu && fabsf(u0 - p / mu) < kBoundary);
     }
     const bool any_bad = __any_sync(0xffffffffu, !ok) || sh.bad;
     const unsigned accm = __ballot_sync(0xffffffffu, lane < k && acc);
@@ -964,6 +1039,10 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
       sh.boundary = __popc(nearm);
     }
   }
+  if (cum) {
+    __syncthreads();  // the prefix products
+    admit_candidates();
+  }
   __syncthreads();
 
   const int jstar = sh.jstar;
@@ -983,7 +1062,7 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   // residual (q everywhere: the stop row pair is re-read)
   if (tid == 0) {
     int mode = 0;
-    if (jstar < k) mode = (fastgate && !((sh.overflow_rows >> jstar) & 1u)) ? 1 : 2;
+    if (jstar < k) mode = (((fast_rows & ~sh.overflow_rows) >> jstar) & 1u) ? 1 : 2;
     sh.fmode = mode;
   }
 }
@@ -1057,10 +1136,16 @@ __device__ void finish_greedy(const Params& P, int b, FinishShared& sh) {
   int32_t* tok = P.tokens + static_cast<int64_t>(b) * (k + 1);
   if (warp == 0) {
     bool ok = true, acc = false, is_null = false;
+    // one-hot q: q_j(D_j) is 1 where D_j is the draft argmax, else 0, and the
+    // prefix product in front of step j is 1 iff every earlier draft is
+    const bool hit = lane < k && sh.Dv[lane] == sh.targ[k + 1 + lane];
+    const unsigned hitm = __ballot_sync(0xffffffffu, hit);
     if (lane < k) {
       const int d = sh.Dv[lane];
       ok = d >= 0 && d < V;
-      is_null = gated && d != sh.targ[k + 1 + lane];
+      const float q = hit ? 1.f : 0.f;
+      const float cprev = ((~hitm) & ((1u << lane) - 1u)) == 0u ? 1.f : 0.f;
+      is_null = gated && !gate_admits(q, sh.tau_j[lane], cprev, P.min_cum > 0.f, P.min_cum);
       acc = ok && !is_null && d == sh.targ[lane];
     }
     const bool any_bad = __any_sync(0xffffffffu, !ok) || sh.bad;
@@ -1114,7 +1199,7 @@ __device__ void finish_greedy(const Params& P, int b, FinishShared& sh) {
 // every 8 n) and write the masses into the leading CTA's shared memory.  Lanes
 // take 8-entry groups lane, lane + 32, ... (16-byte coalesced loads), four
 // groups of both rows issued before use.
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kPol>
 __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lead, float* lead_tile,
                                  int rank, int csize) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1123,8 +1208,11 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
   const int rt = jstar, rd = k + 1 + jstar;
   const TT* trow = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + jstar) * V;
   const TD* drow = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + jstar) * V;
-  const ResidualEval ev{2, lead.rowM[rt], lead.rowInvS[rt], lead.rowM[rd], lead.rowInvS[rd], P.c, lead.tau,
-                        lead.gated != 0, 0, nullptr, nullptr};
+  const bool gated = lead.gated != 0;
+  const ResidualEval ev{2, lead.rowM[rt], lead.rowInvS[rt], lead.rowM[rd], lead.rowInvS[rd], P.c,
+                        gated ? (kPol ? lead.tau_j[jstar] : lead.tau) : -1.f,
+                        kPol ? lead.cprev[jstar] : 1.f,
+                        kPol && gated && P.min_cum > 0.f ? P.min_cum : -1.f, 0, nullptr, nullptr};
   const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
   constexpr int kLaneGroups = kChunk / 8 / 32;
 #pragma unroll 1
@@ -1142,7 +1230,7 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float rr[8];
-        residual8(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
+        residual8<kPol>(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
         acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
       }
     }
@@ -1151,12 +1239,11 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
   }
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kPol>
 __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
   const bool gated = sh.gated != 0;
-  const float tau = sh.tau;
   const float c = P.c;
   const TT* Lt = static_cast<const TT*>(P.Lt);
   const TD* Ld = static_cast<const TD*>(P.Ld);
@@ -1175,7 +1262,10 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
   const float u1 = sh.u1[jstar];
   ResidualEval ev{mode, sh.rowM[rt], sh.rowInvS[rt],
                   jstar < k ? sh.rowM[rd] : 0.f, jstar < k ? sh.rowInvS[rd] : 0.f,
-                  c, tau, gated, nadm, jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
+                  c, gated && jstar < k ? (kPol ? sh.tau_j[jstar] : sh.tau) : -1.f,
+                  kPol && jstar < k ? sh.cprev[jstar] : 1.f,
+                  kPol && gated && P.min_cum > 0.f ? P.min_cum : -1.f, nadm,
+                  jstar < k ? sh.adm_i[jstar] : sh.adm_i[0],
                   jstar < k ? sh.adm_q[jstar] : sh.adm_q[0]};
   const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
 
@@ -1266,7 +1356,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
     float xt[8], xd[8];
     load8<TT>(trow, c0 + e0, V, vt, xt);
     if (ev.mode == 2) load8<TD>(drow, c0 + e0, V, vd, xd);
-    residual8(ev, xt, xd, c0 + e0, V, r8);
+    residual8<kPol>(ev, xt, xd, c0 + e0, V, r8);
   }
   {
     int lastpos = -1;
@@ -1346,8 +1436,9 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
 // The finishing grid runs in clusters of one or more CTAs (a cluster per
 // sequence at a time).  The leading CTA does all the work of a sequence except
 // the dense residual's chunk masses, which every CTA of the cluster shares.
-template <typename TT, typename TD, bool kGreedy>
-__global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) {
+template <typename TT, typename TD, int kMode>
+__global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_constant__ Params P) {
+  constexpr bool kPol = kMode == kModePolicy;
   extern __shared__ __align__(16) unsigned char fin_smem[];
   FinishShared& sh = *reinterpret_cast<FinishShared*>(fin_smem);
   cg::cluster_group cluster = cg::this_cluster();
@@ -1359,26 +1450,26 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const Params P) 
   // the first sequence's input-only work overlaps the end of the stream pass;
   // then wait for the stream pass (programmatic dependent launch) before
   // reading its output
-  if (rank == 0 && cid < P.B) finish_prologue(P, cid, sh);
+  if (rank == 0 && cid < P.B) finish_prologue<kMode>(P, cid, sh);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
   for (int b = cid; b < P.B; b += ncl) {
     if (rank == 0) {
       if (b != cid) {
         __syncthreads();
-        finish_prologue(P, b, sh);
+        finish_prologue<kMode>(P, b, sh);
       }
       __syncthreads();
-      if constexpr (kGreedy) finish_greedy<TT, TD>(P, b, sh);
-      else finish_front<TT, TD>(P, b, sh);
+      if constexpr (kMode == kModeGreedy) finish_greedy<TT, TD>(P, b, sh);
+      else finish_front<TT, TD, kPol>(P, b, sh);
       __syncthreads();
     }
     if (csize > 1) cluster.sync();  // the leading CTA's decision, visible to the cluster
     const int fmode = lead->fmode;
-    if (fmode == 2) dense_chunk_sums<TT, TD>(P, b, *lead, lead->tile, rank, csize);
+    if (fmode == 2) dense_chunk_sums<TT, TD, kPol>(P, b, *lead, lead->tile, rank, csize);
     if (csize > 1) cluster.sync();  // every chunk mass is in the leading CTA
     else __syncthreads();
-    if (rank == 0 && fmode >= 0) finish_back<TT, TD>(P, b, sh);
+    if (rank == 0 && fmode >= 0) finish_back<TT, TD, kPol>(P, b, sh);
   }
 }
 

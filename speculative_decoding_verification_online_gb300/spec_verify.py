@@ -62,6 +62,8 @@ def load() -> ctypes.CDLL:
     L.spec_verify_mark_next.restype = I
     L.spec_verify_run_noalloc.argtypes = [P, I, P, I, P, I, I, I, F, I, F, P, P, U64, P, P, P, P, P, P]
     L.spec_verify_run_noalloc.restype = I
+    L.spec_verify_set_gate_policy.argtypes = [P, P, I, F]
+    L.spec_verify_set_gate_policy.restype = I
     _lib = L
     return L
 
@@ -108,6 +110,11 @@ def spec_verify_run_host(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode, thre
 
 def spec_verify_free(h) -> int:
     return load().spec_verify_free(h)
+
+
+def spec_verify_set_gate_policy(h, schedule, n_schedule, min_cum) -> int:
+    """Raw call: schedule is a ctypes float array (or None), min_cum a float."""
+    return load().spec_verify_set_gate_policy(h, schedule, n_schedule, min_cum)
 
 
 def spec_verify_launches_per_run() -> int:
@@ -181,6 +188,20 @@ class SpecVerifier:
         rc = spec_verify_mark_next(self.handle, ev_before.cuda_event, ev_after.cuda_event)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_mark_next")
+
+    def set_gate_policy(self, schedule=None, min_cum: float = 0.0):
+        """Per-step thresholds (a sequence of floats in [0, 1], the last one
+        repeating; None for none) and the cumulative floor (0 = off) of the
+        gated sequences of later calls.  Raises on a malformed policy, which
+        then leaves the previous one in place."""
+        arr, n = None, 0
+        if schedule is not None:
+            vals = [float(x) for x in schedule]
+            n = len(vals)
+            arr = (ctypes.c_float * max(n, 1))(*vals)
+        rc = spec_verify_set_gate_policy(self.handle, arr, n, float(min_cum))
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_set_gate_policy")
 
     def outputs(self, B: int):
         dev = self.device

@@ -28,20 +28,23 @@ ALPHA_RTOL = 1e-5
 ALPHA_ATOL = 1e-30
 
 
-def oracle_for(w: workloads.Workload, idx=None, nthreads=8, u0=None, u1=None):
-    """Oracle outputs for workload w (all sequences, or the listed ones)."""
+def oracle_for(w: workloads.Workload, idx=None, nthreads=8, u0=None, u1=None, tau_sched=None,
+               min_cum=0.0):
+    """Oracle outputs for workload w (all sequences, or the listed ones), with
+    an optional gate policy (per-step schedule, cumulative floor)."""
     gate = w.gate.cpu().numpy()
     tau = w.tau.cpu().numpy().astype(np.float64)
+    pol = dict(tau_sched=tau_sched, min_cum=min_cum)
     if idx is None:
         return O.verify(workloads.to_numpy_logits(w.Lt), workloads.to_numpy_logits(w.Ld),
                         w.D.cpu().numpy(), w.T, gate, tau, seed=w.philox_seed,
-                        u0=u0, u1=u1, nthreads=nthreads)
+                        u0=u0, u1=u1, nthreads=nthreads, **pol)
     parts = []
     for b in idx:
         parts.append(O.verify(workloads.to_numpy_logits(w.Lt[b:b + 1]),
                               workloads.to_numpy_logits(w.Ld[b:b + 1]), w.D[b:b + 1].cpu().numpy(),
                               w.T, gate[b:b + 1], tau[b:b + 1], seed=w.philox_seed,
-                              seq_offset=int(b), nthreads=1))
+                              seq_offset=int(b), nthreads=1, **pol))
     return {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
 
 
@@ -56,9 +59,31 @@ def gated_q_of_drafts(w: workloads.Workload, ref, idx=None):
     return torch.exp(x - lse).numpy()
 
 
-def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
+def gate_near_boundary(w: workloads.Workload, ref, idx=None, tau_sched=None, min_cum=0.0):
+    """[B, k] mask of gated positions whose gate decision lies within 1e-6 of a
+    boundary: |q(D) - tau_j| (tau_j > 0) or, with a cumulative floor,
+    |prod_{i<j} q_i(D_i) * q_j(D_j) - min_cum| (q in fp64 from the oracle)."""
+    sel = slice(None) if idx is None else np.asarray(idx)
+    gate = w.gate.cpu().numpy()[sel].astype(bool)
+    qd = gated_q_of_drafts(w, ref, idx)
+    k = w.k
+    if tau_sched is None:
+        tau = np.broadcast_to(w.tau.cpu().numpy()[sel].astype(np.float64)[:, None], qd.shape)
+    else:
+        tau = np.broadcast_to(np.array([tau_sched[min(j, len(tau_sched) - 1)] for j in range(k)]),
+                              qd.shape)
+    near = (tau > 0) & (np.abs(qd - tau) < BOUNDARY)
+    if min_cum > 0:
+        incl = np.cumprod(qd, axis=1)
+        near |= np.abs(incl - min_cum) < BOUNDARY
+    return gate[:, None] & near
+
+
+def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what="", tau_sched=None,
+            min_cum=0.0):
     """Assert parity; returns a dict of counts (compared, boundary, boundary_decision,
-    boundary_pick, boundary_mismatch, draws)."""
+    boundary_pick, boundary_mismatch, draws).  tau_sched / min_cum: the gate
+    policy both sides ran with."""
     sel = slice(None) if idx is None else np.asarray(idx)
     g_len = got["accepted_len"].cpu().numpy()[sel]
     g_tok = got["tokens"].cpu().numpy()[sel]
@@ -77,9 +102,7 @@ def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what=""):
     gate = w.gate.cpu().numpy()[sel].astype(bool)
     keep = np.ones_like(g_alpha, dtype=bool)
     if gate.any():
-        qd = gated_q_of_drafts(w, ref, idx)
-        tau = w.tau.cpu().numpy()[sel][:, None]
-        keep &= ~(gate[:, None] & (np.abs(qd - tau) < BOUNDARY))
+        keep &= ~gate_near_boundary(w, ref, idx, tau_sched, min_cum)
     np.testing.assert_allclose(g_alpha[keep], ref["alpha"][keep], rtol=ALPHA_RTOL, atol=ALPHA_ATOL,
                                err_msg=what)
     valid = ref["accepted_len"] >= 0
