@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P, P,
                                            P, ctypes.c_int]
         L.oracle_verify_policy.restype = ctypes.c_int
+        L.oracle_diagnostics.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
+                                         ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int]
+        L.oracle_diagnostics.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -173,4 +177,34 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
                                     _ptr(out["degenerate"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
+    return out
+
+
+def diagnostics(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, tau_sched=None,
+                min_cum: float = 0.0, nthreads: int = 1):
+    """Closed-form acceptance of every draft position (``oracle_diagnostics``).
+
+    Returns a dict of numpy arrays: min_sum [B, k] (sum min(p, mu)), pq_sum
+    [B, k] (sum p q), argmax_q [B, k] (q at the first largest p), margin [B]
+    (gated sequences: the closest q(x) to a gate boundary).
+    """
+    Lt = np.ascontiguousarray(Lt)
+    Ld = np.ascontiguousarray(Ld)
+    B, k1, V = Lt.shape
+    k = k1 - 1
+    if Ld.shape != (B, k, V):
+        raise ValueError(f"draft logits shape {Ld.shape} != {(B, k, V)}")
+    D = np.ascontiguousarray(D, dtype=np.int32).reshape(B, k)
+    gate = np.ascontiguousarray(np.broadcast_to(np.asarray(gate, dtype=np.uint8), (B,)))
+    tau = np.ascontiguousarray(np.broadcast_to(np.asarray(tau, dtype=np.float64), (B,)))
+    sched = None if tau_sched is None else np.ascontiguousarray(tau_sched, dtype=np.float64).ravel()
+    n_sched = 0 if sched is None else int(sched.shape[0])
+    out = dict(min_sum=np.zeros((B, k)), pq_sum=np.zeros((B, k)), argmax_q=np.zeros((B, k)),
+               margin=np.zeros(B))
+    rc = lib().oracle_diagnostics(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B, k,
+                                  V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
+                                  float(min_cum), _ptr(out["min_sum"]), _ptr(out["pq_sum"]),
+                                  _ptr(out["argmax_q"]), _ptr(out["margin"]), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_diagnostics rejected its arguments")
     return out

@@ -174,6 +174,9 @@ typedef struct {
   double* row_stats; double* margin; double* margin_pick; int32_t* degenerate;
   const double* tau_sched; int n_sched; /* per-step thresholds (NULL: tau[b] at every step) */
   double min_cum;                       /* cumulative floor (0: no cumulative gate) */
+  /* oracle_diagnostics outputs (diagnose = 1 runs diagnose_one instead of verify_one) */
+  int diagnose;
+  double* diag_min; double* diag_pq; double* diag_argq;
 } job_t;
 
 typedef struct {
@@ -455,6 +458,62 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   if (J->margin_pick) J->margin_pick[b] = marg_pick;
 }
 
+/* Closed-form acceptance of every draft position of sequence b [M "The
+ * acceptance ceiling"]: when the draft is drawn from q_j, modified rejection
+ * sampling accepts with probability sum_x min(p_j(x), mu_j(x)) (plain mode:
+ * the maximal-coupling bound sum_x min(p, q) = 1 - TV), sampler-match with
+ * sum_x p_j(x) q_j(x), and the argmax rule with q_j(argmax p_j).  mu_j is the
+ * retained measure of the gate (its threshold, schedule and cumulative floor
+ * with the drafted prefix D_0..D_{j-1}).  A position whose rows p_j, q_j (or,
+ * with a cumulative floor, an earlier draft row or drafted token) are invalid
+ * gets NaN, as does every position of a gated sequence with a threshold
+ * outside (0, 1] and no schedule. */
+static void diagnose_one(const job_t* J, int b, scratch_t* S) {
+  const int k = J->k;
+  const int64_t V = J->V;
+  const int gated = J->gate[b] != 0;
+  const int32_t* Db = J->D + (int64_t)b * k;
+  const int esz_t = J->tdt == ORACLE_BF16 ? 2 : 4, esz_d = J->ddt == ORACLE_BF16 ? 2 : 4;
+  int bad_t[ORACLE_MAX_K], bad_d[ORACLE_MAX_K];
+  double mx, lse;
+  for (int j = 0; j < k; ++j) {
+    const char* rt = (const char*)J->Lt + ((int64_t)b * (k + 1) + j) * V * esz_t;
+    const char* rd = (const char*)J->Ld + ((int64_t)b * k + j) * V * esz_d;
+    bad_t[j] = oracle_softmax_row(rt, J->tdt, V, J->T, S->P + (int64_t)j * V, &mx, &lse);
+    bad_d[j] = oracle_softmax_row(rd, J->ddt, V, J->T, S->Q + (int64_t)j * V, &mx, &lse);
+  }
+  const int cum = gated && J->min_cum > 0.0;
+  const int bad_tau = gated && !J->tau_sched && !(J->tau[b] > 0.0 && J->tau[b] <= 1.0);
+  double marg = INFINITY;
+  double cprev = 1.0;   /* prod_{i<j} q_i(D_i) */
+  int prefix_bad = 0;   /* an earlier draft row or drafted token the product needs is invalid */
+  for (int j = 0; j < k; ++j) {
+    const int64_t o = (int64_t)b * k + j;
+    const double* pj = S->P + (int64_t)j * V;
+    const double* qj = S->Q + (int64_t)j * V;
+    if (bad_t[j] || bad_d[j] || bad_tau || (cum && prefix_bad)) {
+      if (J->diag_min) J->diag_min[o] = NAN;
+      if (J->diag_pq) J->diag_pq[o] = NAN;
+      if (J->diag_argq) J->diag_argq[o] = NAN;
+    } else {
+      const double tau = step_threshold(J, b, j);
+      retained_measure(J, gated, tau, cprev, qj, S->mu);
+      double smin = 0.0, spq = 0.0;
+      for (int64_t v = 0; v < V; ++v) {
+        smin += fmin(pj[v], S->mu[v]);
+        spq += pj[v] * qj[v];
+        if (gated) marg = fmin(marg, gate_margin(J, tau, cprev, qj[v]));
+      }
+      if (J->diag_min) J->diag_min[o] = smin;
+      if (J->diag_pq) J->diag_pq[o] = spq;
+      if (J->diag_argq) J->diag_argq[o] = qj[argmax_first(pj, V)];
+    }
+    if (bad_d[j] || Db[j] < 0 || (int64_t)Db[j] >= V) prefix_bad = 1;
+    else cprev *= qj[Db[j]];
+  }
+  if (J->margin) J->margin[b] = marg;
+}
+
 /* ------------------------------------------------------------- batch */
 
 typedef struct {
@@ -475,11 +534,16 @@ static void* worker_main(void* arg) {
   if (!S.P || !S.Q || !S.mu || !S.r) {
     w->err = 1;
   } else {
-    for (int b = w->first; b < J->B; b += w->stride) verify_one(J, b, &S);
+    for (int b = w->first; b < J->B; b += w->stride) {
+      if (J->diagnose) diagnose_one(J, b, &S);
+      else verify_one(J, b, &S);
+    }
   }
   free(S.P); free(S.Q); free(S.mu); free(S.r);
   return NULL;
 }
+
+static int run_jobs(const job_t* Jp, int nthreads);
 
 int oracle_verify(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
                   int B, int k, int64_t V, double T,
@@ -512,7 +576,32 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
   if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_MU_STEP_ONLY) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
              accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate,
-             tau_sched, n_sched, min_cum};
+             tau_sched, n_sched, min_cum, 0, NULL, NULL, NULL};
+  return run_jobs(&J, nthreads);
+}
+
+int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                       int B, int k, int64_t V, double T,
+                       const uint8_t* gate, const double* tau,
+                       const double* tau_sched, int n_sched, double min_cum,
+                       double* min_sum, double* pq_sum, double* argmax_q, double* margin,
+                       int nthreads) {
+  if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
+  if (tau_sched && n_sched < 1) return 1;
+  if (!(min_cum >= 0.0 && min_cum <= 1.0)) return 1;
+  if (B == 0) return 0;
+  if (!Lt || !Ld || !D || !gate || !tau) return 1;
+  if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
+  job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, 0, 0, NULL, NULL, ORACLE_RULE_MU,
+             NULL, NULL, NULL, NULL, NULL, margin, NULL, NULL,
+             tau_sched, n_sched, min_cum, 1, min_sum, pq_sum, argmax_q};
+  return run_jobs(&J, nthreads);
+}
+
+/* the sequences of a job split over nthreads worker threads */
+static int run_jobs(const job_t* Jp, int nthreads) {
+  const job_t J = *Jp;
+  const int B = J.B;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > B) nthreads = B;
   worker_t* ws = (worker_t*)calloc((size_t)nthreads, sizeof(worker_t));

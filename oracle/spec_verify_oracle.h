@@ -143,6 +143,30 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
                          double* row_stats, double* margin, double* margin_pick,
                          int32_t* degenerate, int nthreads);
 
+/*
+ * Closed-form acceptance of every draft position [M] "The acceptance ceiling":
+ * for a draft drawn from q_j,
+ *   min_sum[b, j]  = sum_x min(p_j(x), mu_j(x))  -- modified rejection sampling
+ *                    (plain mode mu = q: the maximal-coupling bound 1 - TV);
+ *   pq_sum[b, j]   = sum_x p_j(x) q_j(x)         -- sampler-match;
+ *   argmax_q[b, j] = q_j(argmax p_j)             -- the argmax rule (first
+ *                    largest p_j).
+ * mu_j follows the sequence's gate and the policy of oracle_verify_policy
+ * (the cumulative floor uses the drafted prefix D_0..D_{j-1}).  Outputs
+ * [B, k] (each may be NULL); margin[B] (may be NULL) = the smallest distance
+ * of any q_j(x) of a gated sequence to its gate boundaries.  A position whose
+ * rows p_j or q_j are invalid (NaN or +inf logit, all -inf), or -- with a
+ * cumulative floor -- behind an invalid earlier draft row or drafted token,
+ * gets NaN; so does every position of a gated sequence with a threshold
+ * outside (0, 1] and no schedule.  Returns 1 on bad args.
+ */
+int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                       int B, int k, int64_t V, double T,
+                       const uint8_t* gate, const double* tau,
+                       const double* tau_sched, int n_sched, double min_cum,
+                       double* min_sum, double* pq_sum, double* argmax_q, double* margin,
+                       int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -604,3 +604,102 @@ def test_gate_policy_bad_arguments_are_rejected():
     for kw in (dict(tau_sched=[]), dict(min_cum=-0.1), dict(min_cum=1.5), dict(min_cum=np.nan)):
         with pytest.raises(ValueError):
             O.verify(Lt, Ld, D, 1.0, 1, 0.5, **kw)
+
+
+# ------------------------------------------------- closed-form acceptance diagnostics
+
+def test_diagnostics_reproduce_the_printed_ceiling_example():
+    g = {r[0]: [float(x) for x in r[1:]] for r in _golden_rows("acceptance_ceiling_example.txt")}
+    p, q = np.array(g["p"]), np.array(g["q"])
+    with np.errstate(divide="ignore"):
+        Lt = np.log(np.stack([p, p]))[None].astype(np.float32)
+        Ld = np.log(q)[None, None].astype(np.float32)
+    d = O.diagnostics(Lt, Ld, np.zeros((1, 1)), 1.0, 0, 0.5)
+    assert abs(d["argmax_q"][0, 0] - g["argmax_q"][0]) < 1e-7
+    assert abs(d["min_sum"][0, 0] - g["ceiling"][0]) < 1e-7
+    assert abs(d["pq_sum"][0, 0] - g["sampler_match"][0]) < 1e-7
+
+
+@pytest.mark.parametrize("gated,tau,sched", [(False, 0.5, None), (True, 0.3, None), (True, 0.99, [0.2, 0.0])])
+def test_diagnostics_are_the_exact_pass_rates_of_the_three_rules(gated, tau, sched):
+    # without a cumulative floor mu_j does not depend on the prefix, so the
+    # enumerated law's pass rate at every reached position is the closed form
+    rng = np.random.default_rng(31 + int(gated) + (sched is not None))
+    V, k = 4, 2
+    Lt, Ld = _random_case(rng, V, k, scale=1.5)
+    d = O.diagnostics(Lt[None], Ld[None], np.zeros((1, k)), 1.0, int(gated), tau, tau_sched=sched)
+    for rule, key in ((O.RULE_MU, "min_sum"), (O.RULE_ARGMAX, "argmax_q")):
+        g, t = (gated, tau) if rule == O.RULE_MU else (False, 0.5)
+        law = exact_law(Lt, Ld, 1.0, g, t, rule=rule, tau_sched=sched if rule == O.RULE_MU else None)
+        reach, _, passed = position_marginals(law, k, V)
+        for j in range(k):
+            assert abs(passed[j] / reach[j] - d[key][0, j]) < 1e-9, (key, j)
+    # sampler-match draws a fresh target token with u0: its pass rate at step 0
+    # over the cells of u0 cut at p_0's cumulative sums, for every draft D_0
+    P, Q = distributions(Lt, Ld, 1.0)
+    edges = np.concatenate([[0.0], np.cumsum(P[0])])
+    edges[-1] = 1.0
+    mids, vols = 0.5 * (edges[:-1] + edges[1:]), np.diff(edges)
+    keep = vols > 0
+    mids, vols = mids[keep], vols[keep]
+    n = V * len(mids)
+    D = np.zeros((n, k), dtype=np.int32)
+    D[:, 0] = np.repeat(np.arange(V), len(mids))
+    u0 = np.full((n, k), 0.5)
+    u0[:, 0] = np.tile(mids, V)
+    out = O.verify(np.broadcast_to(Lt, (n, k + 1, V)), np.broadcast_to(Ld, (n, k, V)), D, 1.0, 0, 0.5,
+                   u0=u0, u1=np.full(n, 0.5), rule=O.RULE_SAMPLER_MATCH)
+    acc = (out["accepted_len"] >= 1).astype(float)
+    rate = float((acc * np.tile(vols, V) * np.repeat(Q[0], len(mids))).sum())
+    assert abs(rate - d["pq_sum"][0, 0]) < 1e-12
+
+
+@pytest.mark.parametrize("sched,cum", [([0.0], 0.2), ([0.1, 0.3], 0.1), (None, 0.3)])
+def test_diagnostics_min_sum_is_the_mean_acceptance_probability(sched, cum):
+    # E over D_j ~ q_j of the oracle's alpha_j, the drafted prefix held fixed,
+    # is sum_x min(p_j, mu_j) -- also with a cumulative floor, whose mu_j
+    # depends on the prefix
+    rng = np.random.default_rng(int(100 * cum) + len(sched or []))
+    V, k = 6, 3
+    Lt, Ld = _random_case(rng, V, k, scale=1.5)
+    _, Q = distributions(Lt, Ld, 1.0)
+    prefix = rng.integers(0, V, size=k)
+    d = O.diagnostics(Lt[None], Ld[None], prefix[None], 1.0, 1, 0.4, tau_sched=sched, min_cum=cum)
+    for j in range(k):
+        D = np.broadcast_to(prefix, (V, k)).copy()
+        D[:, j] = np.arange(V)
+        a = O.verify(np.broadcast_to(Lt, (V, k + 1, V)), np.broadcast_to(Ld, (V, k, V)), D, 1.0, 1, 0.4,
+                     tau_sched=sched, min_cum=cum)["alpha"][:, j]
+        assert abs((Q[j] * a).sum() - d["min_sum"][0, j]) < 1e-12
+
+
+def test_diagnostics_plain_ceiling_is_one_minus_total_variation():
+    rng = np.random.default_rng(3)
+    B, k, V = 20, 3, 50
+    Lt = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    Ld = (Lt[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    d = O.diagnostics(Lt, Ld, np.zeros((B, k)), 0.8, 0, 0.5, nthreads=4)
+    P = softmax(Lt[:, :k].astype(np.float64) / 0.8, axis=-1)
+    Q = softmax(Ld.astype(np.float64) / 0.8, axis=-1)
+    np.testing.assert_allclose(d["min_sum"], 1.0 - 0.5 * np.abs(P - Q).sum(-1), atol=1e-12)
+    # min(a, b) >= a b on [0, 1]: rejection sampling accepts at least as often as sampler-match
+    assert np.all(d["min_sum"] >= d["pq_sum"] - 1e-15)
+    assert np.all(d["min_sum"] <= 1.0 + 1e-12)
+
+
+def test_diagnostics_greedy_and_invalid_rows():
+    Lt = np.array([[[0.0, 2.0, 1.0], [1.0, 0.0, 0.0], [0.0, 0.0, 0.0]]], dtype=np.float32)
+    Ld = np.array([[[0.0, 3.0, 0.0], [0.0, 1.0, 0.0]]], dtype=np.float32)
+    d = O.diagnostics(Lt, Ld, np.array([[1, 0]]), 0.0, 0, 0.5)
+    # one-hot p and q: the argmaxes agree at step 0 (token 1), differ at step 1
+    assert list(d["min_sum"][0]) == [1.0, 0.0] and list(d["pq_sum"][0]) == [1.0, 0.0]
+    assert list(d["argmax_q"][0]) == [1.0, 0.0]
+    bad = Lt.copy()
+    bad[0, 1, 2] = np.nan
+    d = O.diagnostics(bad, Ld, np.array([[1, 0]]), 1.0, 1, 0.3, tau_sched=[0.0], min_cum=0.1)
+    assert np.isfinite(d["min_sum"][0, 0]) and np.isnan(d["min_sum"][0, 1])
+    # a drafted token out of range poisons the cumulative product behind it
+    d = O.diagnostics(Lt, Ld, np.array([[7, 0]]), 1.0, 1, 0.3, tau_sched=[0.0], min_cum=0.1)
+    assert np.isfinite(d["pq_sum"][0, 0]) and np.isnan(d["pq_sum"][0, 1])
+    d = O.diagnostics(Lt, Ld, np.array([[7, 0]]), 1.0, 1, 0.3)
+    assert np.all(np.isfinite(d["pq_sum"]))
