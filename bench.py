@@ -6,12 +6,16 @@ synthetic workload, inputs resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--temperature T] [--gate plain|gated|half]
-                  [--gate-schedule T0,T1,...] [--min-cum F]
+                  [--gate-schedule T0,T1,...] [--min-cum F] [--diagnostics]
 
 --temperature and --gate override the workload's temperature (0 = greedy
 decoding) and gate recipe; the logits and drafted tokens stay the same.
 --gate-schedule / --min-cum set the gate policy of the gated sequences
 (per-step thresholds, the last repeating; the cumulative prefix-product floor).
+--diagnostics times spec_verify_diagnostics (the closed-form acceptance of
+every draft position: a stream pass plus a second read of each (p_j, q_j)
+pair) instead of the verification call; it has no host-buffer entry point, so
+that line carries no e2e figure.
 
 --impl reference times the fp64 CPU oracle on the host cores (the baseline
 arm); under torchrun only rank 0 runs it.  Multi-GPU runs shard sequences
@@ -60,6 +64,8 @@ def parse():
                     help="per-step gate thresholds, comma-separated (the last repeats)")
     ap.add_argument("--min-cum", type=float, default=0.0,
                     help="cumulative floor on the drafted prefix's product of draft probabilities")
+    ap.add_argument("--diagnostics", action="store_true",
+                    help="time the closed-form acceptance diagnostics instead of verification")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--clock-window", type=float, default=1.0,
@@ -84,7 +90,7 @@ def make_workload(args, seed, device, B=None):
 
 def overridden(args) -> bool:
     return (args.temperature is not None or args.gate is not None or args.gate_schedule is not None
-            or args.min_cum > 0)
+            or args.min_cum > 0 or args.diagnostics)
 
 
 def gate_policy(args):
@@ -204,6 +210,25 @@ def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
     return reps * w.B * w.k / el, reps, el
 
 
+def cpu_diag_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
+    """Time the fp64 oracle's diagnostics on the workload's sequences for about `seconds`."""
+    from oracle import oracle as O
+    Lt = workloads.to_numpy_logits(w.Lt)
+    Ld = workloads.to_numpy_logits(w.Ld)
+    D = w.D.cpu().numpy()
+    gate = w.gate.cpu().numpy()
+    tau = w.tau.cpu().numpy().astype(np.float64)
+    pol = dict(tau_sched=sched, min_cum=cum)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=nthreads, **pol)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return reps * w.B * w.k / el, reps, el
+
+
 def run_reference(args, ws, rank):
     """The baseline arm: the fp64 CPU oracle on host cores."""
     if rank != 0:
@@ -220,8 +245,14 @@ def run_reference(args, ws, rank):
     cores = os.cpu_count() or 1
     sched, cum = gate_policy(args)
     pol = dict(tau_sched=sched, min_cum=cum)
+
+    def one():
+        if args.diagnostics:
+            O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=cores, **pol)
+        else:
+            O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
     t0 = time.perf_counter()
-    O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
+    one()
     t_step = time.perf_counter() - t0
     # a deliberately slow program: bound the whole run to a few minutes
     budget = 150.0
@@ -231,10 +262,10 @@ def run_reference(args, ws, rank):
         warm = min(warm, 3)
         steps = max(1, int(budget / t_step) - warm)
     for _ in range(warm):
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
+        one()
     t0 = time.perf_counter()
     for _ in range(steps):
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
+        one()
     el = time.perf_counter() - t0
     value = steps * sample_B * w.k / el
     sample = (f"{sample_B} of {cfg['B']} sequences of {args.workload} per step; "
@@ -247,7 +278,8 @@ def run_reference(args, ws, rank):
         "config": {"workload": args.workload, "B_sample": sample_B, "k": w.k, "V": w.V,
                    "logits_dtype": w.dtype, "T": w.T,
                    "gate": args.gate or workloads.CONFIGS[args.workload]["gate"],
-                   "gate_schedule": sched, "min_cum": cum},
+                   "gate_schedule": sched, "min_cum": cum,
+                   "call": "oracle_diagnostics" if args.diagnostics else "oracle_verify"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
@@ -293,11 +325,18 @@ def main():
     if sched is not None or cum > 0:
         ver.set_gate_policy(sched, cum)
     outs = [ver.outputs(B) for _ in range(nsets)]
+    douts = [{key: torch.empty(B, k, dtype=torch.float32, device=dev)
+              for key in ("min_sum", "pq_sum", "argmax_q")} for _ in range(nsets)]
     seq_offset = rank * B
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
         w = sets[i % nsets]
+        if args.diagnostics:
+            ver.diagnostics(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU,
+                            threshold=float(cfg["tau"]), gate_per_seq=w.gate,
+                            threshold_per_seq=w.tau, out=douts[i % nsets])
+            return
         ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]),
                 gate_per_seq=w.gate, threshold_per_seq=w.tau, seed=w.philox_seed,
                 seq_offset=seq_offset, out=outs[i % nsets])
@@ -361,7 +400,7 @@ def main():
 
     # e2e through the host-buffer entry point: pinned inputs, H2D + verify + D2H per step
     e2e = None
-    if rank == 0 or ws > 1:
+    if (rank == 0 or ws > 1) and not args.diagnostics:
         wh = sets[0]
         Lt_h = wh.Lt.cpu().pin_memory()
         Ld_h = wh.Ld.cpu().pin_memory()
@@ -391,7 +430,14 @@ def main():
                "d2h_bytes_per_step": d2h}
 
     cpu = None
-    if rank == 0:
+    if rank == 0 and args.diagnostics:
+        cores = os.cpu_count() or 1
+        small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
+        rate, reps, cel = cpu_diag_rate(small, args.cpu_seconds, cores, sched, cum)
+        cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
+               "sample": f"oracle_diagnostics on {small.B} sequences of {args.workload} x {reps} "
+                         f"repetitions ({cel:.1f} s)"}
+    elif rank == 0:
         cores = os.cpu_count() or 1
         small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
         rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores, sched, cum)
@@ -412,6 +458,7 @@ def main():
             "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
                        "logits_dtype": w0.dtype, "T": w0.T, "gate": args.gate or cfg["gate"],
                        "gate_schedule": sched, "min_cum": cum,
+                       "call": "spec_verify_diagnostics" if args.diagnostics else "spec_verify_run",
                        "threshold": cfg["tau"],
                        "l2": f"inputs larger than L2: {nsets} rotated copies of "
                              f"{per_set / 1e6:.1f} MB logits",
@@ -428,7 +475,9 @@ def main():
                                    "the K steps"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * sv.spec_verify_launches_per_run(),
+            # the diagnostics launch 4 kernels per call (2 at temperature 0)
+            "gpu_launches": args.steps * ((2 if w0.T == 0 else 4) if args.diagnostics
+                                          else sv.spec_verify_launches_per_run()),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -156,6 +156,37 @@ sv_status spec_verify_run_ex(spec_verify_t h,
                              int8_t* flags, uint64_t* counters, float* row_stats,
                              void* cuda_stream);
 
+/* Closed-form acceptance of every draft position (mlxcel PR #992, "The
+ * acceptance ceiling"): for a draft drawn from q_j,
+ *   min_sum [B, k]  = sum_x min(p_j(x), mu_j(x)): the acceptance probability of
+ *                     modified rejection sampling, i.e. the mean of accept_prob
+ *                     over D_j ~ q_j (plain mode: 1 - TV(p_j, q_j), the
+ *                     ceiling of every distribution-preserving rule);
+ *   pq_sum [B, k]   = sum_x p_j(x) q_j(x): the sampler-match rule's;
+ *   argmax_q [B, k] = q_j(argmax p_j): the argmax rule's (first largest p_j).
+ * Device float outputs, each optional (NULL skips it; all NULL: nothing runs).
+ * Inputs as spec_verify_run; mu_j follows each sequence's gate and the
+ * handle's gate policy, whose cumulative floor reads the drafted prefix
+ * draft_tokens[b, 0..j-1] (otherwise draft_tokens is not used).  Temperature 0
+ * gives the one-hot values (1 or 0).  A position whose rows p_j or q_j are
+ * invalid (a NaN or +inf logit, or every logit -inf) -- or, with a cumulative
+ * floor, one behind an invalid earlier draft row or an out-of-range drafted
+ * token -- gets NaN, as does every position of a gated sequence whose own
+ * threshold is outside (0, 1] with no schedule.  Cost: the stream pass over
+ * every row, then a second read of each pair (p_j, q_j), j < k.  Host errors
+ * and asynchrony as spec_verify_run; it shares the handle's workspace, so it
+ * must not overlap a run on the same handle. */
+sv_status spec_verify_diagnostics(spec_verify_t h,
+                                  const void* target_logits, sv_dtype tdt,
+                                  const void* draft_logits, sv_dtype ddt,
+                                  const int32_t* draft_tokens,
+                                  int B, float temperature,
+                                  sv_gate gate_mode, float threshold,
+                                  const uint8_t* gate_mode_per_seq,
+                                  const float* threshold_per_seq,
+                                  float* min_sum, float* pq_sum, float* argmax_q,
+                                  void* cuda_stream);
+
 /* spec_verify_run with HOST buffers for every input and output (same shapes;
  * gate_mode_per_seq / threshold_per_seq / flags / counters optional, host).
  * Copies the inputs to device staging buffers, verifies, copies the outputs

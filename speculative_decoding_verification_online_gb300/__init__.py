@@ -8,6 +8,6 @@ the build step, the ctypes binding and the sequence-sharding helper.
 from .spec_verify import (  # noqa: F401
     COUNTER_NAMES, SV_BF16, SV_F32, SV_FLAG_ACCEPT, SV_FLAG_INVALID, SV_FLAG_NULL, SV_FLAG_REJECT,
     SV_FLAG_UNREACHED, SV_GATED_MU, SV_PLAIN, SpecVerifier, SpecVerifyError, load,
-    spec_verify_free, spec_verify_init, spec_verify_launches_per_run, spec_verify_mark_next,
+    spec_verify_diagnostics, spec_verify_free, spec_verify_init, spec_verify_launches_per_run, spec_verify_mark_next,
     spec_verify_run, spec_verify_run_ex, spec_verify_run_host, spec_verify_run_noalloc,
     spec_verify_set_gate_policy, spec_verify_status_string, run_noalloc)

@@ -12,6 +12,7 @@
 
 #include "spec_verify.h"
 #include "verify_kernel.cuh"
+#include "diag_kernel.cuh"
 
 struct spec_verify_s {
   int device = 0;
@@ -24,6 +25,7 @@ struct spec_verify_s {
   float* xD = nullptr;
   sv::Cand* cand = nullptr;
   unsigned* cand_over = nullptr;
+  sv::DiagNorm* dnorm = nullptr;  // [max_B, k] (diagnostics)
   // one-shot timing marks around the next stream pass
   cudaEvent_t mark_before = nullptr, mark_after = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
@@ -52,6 +54,12 @@ constexpr int dyn_smem() {
 }
 
 // opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
+template <typename TT, typename TD>
+constexpr int pair_smem() {
+  return sv::PairStages<TT, TD>::kWarpsPerCta * sv::PairStages<TT, TD>::kDepth *
+         sv::PairStages<TT, TD>::kBytes;
+}
+
 template <typename TT, typename TD, int G>
 cudaError_t configure_one() {
   cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
@@ -69,6 +77,12 @@ cudaError_t configure(int* blocks_per_sm) {
   cudaError_t e = configure_one<TT, TD, sv::kModeSample>();
   if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>();
   if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>();
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeStats>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sv::pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair_smem<TT, TD>());
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
                                                        sv::stream_kernel<TT, TD, sv::kModeSample>,
@@ -76,9 +90,9 @@ cudaError_t configure(int* blocks_per_sm) {
                                                        dyn_smem<TT, TD>());
 }
 
+// the stream pass (variant G), with the handle's one-shot timing marks around it
 template <typename TT, typename TD, int G>
-sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
-                 cudaStream_t st) {
+sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
   const long long need = (static_cast<long long>(P.total_chunks) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
@@ -95,6 +109,14 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
     h->mark_before = h->mark_after = nullptr;
     if (e != cudaSuccess) return SV_ECUDA;
   }
+  return SV_OK;
+}
+
+template <typename TT, typename TD, int G>
+sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
+                 cudaStream_t st) {
+  const sv_status rs = launch_stream<TT, TD, G>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
   // the finishing pass: one CTA per sequence, allowed to launch while the
   // stream pass drains; it waits (griddepcontrol.wait) before reading its output
   cudaLaunchConfig_t cfg = {};
@@ -137,6 +159,53 @@ sv_status launch_mode(spec_verify_t h, const sv::Params& P, int bps, bool dense_
   if (tb && !db) return launch<uint16_t, float, G>(h, P, bps, dense_likely, st);
   if (!tb && db) return launch<float, uint16_t, G>(h, P, bps, dense_likely, st);
   return launch<float, float, G>(h, P, bps, dense_likely, st);
+}
+
+// PDL launch of a small per-(sequence, position) kernel: warp per pair
+template <typename K, typename... A>
+cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
+                             A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// the acceptance diagnostics: the stream pass, the per-position merge, and
+// (temperature > 0) the pair sweep and its reduction, each launch a
+// programmatic dependent of the one before
+template <typename TT, typename TD, bool kGreedy>
+sv_status launch_diag(spec_verify_t h, const sv::Params& P, int blocks_per_sm, float* min_sum,
+                      float* pq_sum, float* argmax_q, cudaStream_t st) {
+  const sv_status rs = launch_stream<TT, TD, kGreedy ? sv::kModeGreedy : sv::kModeStats>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
+  const unsigned npos = static_cast<unsigned>(P.B * P.k);
+  const unsigned small_grid = (npos + sv::kDiagWarps - 1) / sv::kDiagWarps;
+  if (launch_dependent(sv::diag_norm_kernel<kGreedy>, small_grid, sv::kDiagThreads, 0, st, P, h->dnorm,
+                       min_sum, pq_sum, argmax_q) != cudaSuccess)
+    return SV_ECUDA;
+  if (!kGreedy) {
+    const unsigned total = npos * static_cast<unsigned>(P.nchunk);
+    constexpr int kW = sv::PairStages<TT, TD>::kWarpsPerCta;
+    long long grid = h->num_sms;
+    const long long need = (static_cast<long long>(total) + kW - 1) / kW;
+    if (grid > need) grid = need;
+    if (launch_dependent(sv::pair_kernel<TT, TD>, static_cast<unsigned>(grid),
+                         sv::PairStages<TT, TD>::kThreadsPerCta, pair_smem<TT, TD>(), st, P,
+                         static_cast<const sv::DiagNorm*>(h->dnorm), total) != cudaSuccess)
+      return SV_ECUDA;
+    if (launch_dependent(sv::diag_reduce_kernel<TD>, small_grid, sv::kDiagThreads, 0, st, P,
+                         static_cast<const sv::DiagNorm*>(h->dnorm), min_sum, pq_sum, argmax_q) != cudaSuccess)
+      return SV_ECUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 struct DeviceGuard {
@@ -218,6 +287,7 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   const size_t n_cand = n_rowc * h->nchunk * sv::kTopM;
   const size_t o_cd = off;   off = align_up(off + n_cand * sizeof(sv::Cand), 256);
   const size_t o_co = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
+  const size_t o_dn = off;   off = align_up(off + n_rowc * sizeof(sv::DiagNorm), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
@@ -228,6 +298,7 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   h->xD = reinterpret_cast<float*>(base + o_xd);
   h->cand = reinterpret_cast<sv::Cand*>(base + o_cd);
   h->cand_over = reinterpret_cast<unsigned*>(base + o_co);
+  h->dnorm = reinterpret_cast<sv::DiagNorm*>(base + o_dn);
   // everything starts at zero except the candidate slots, which start empty
   // (all bits set: token id -1); the finishing pass restores both after use
   if (cudaMemset(h->ws, 0, off) != cudaSuccess ||
@@ -241,14 +312,18 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   return SV_OK;
 }
 
-sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtype tdt,
-                             const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens,
-                             int B, float temperature, sv_gate gate_mode, float threshold,
-                             const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
-                             uint64_t seed, uint64_t seq_offset, const float* u_accept,
-                             const float* u_residual, int32_t* accepted_len, int32_t* tokens,
-                             float* accept_prob, int8_t* flags, uint64_t* counters,
-                             float* row_stats, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Validate what every verifying call shares and fill the launch arguments
+// (outputs and draws left empty).  SV_OK with *empty = true: nothing to do.
+sv_status prepare_params(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                         const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens, int B,
+                         float temperature, sv_gate gate_mode, float threshold,
+                         const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                         sv::Params& P, bool* empty) {
+  *empty = false;
   if (!h) return SV_EINVAL;
   if (B < 0 || B > h->max_B) return SV_EINVAL;
   if (!valid_dtype(tdt) || !valid_dtype(ddt)) return SV_EINVAL;
@@ -258,14 +333,13 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   const bool default_tau_used =
       (gate_mode == SV_GATED_MU || gate_mode_per_seq) && !threshold_per_seq && h->n_sched == 0;
   if (default_tau_used && !(threshold > 0.f && threshold <= 1.f)) return SV_EINVAL;
-  if (B == 0) return SV_OK;
-  if (!target_logits || !draft_logits || !draft_tokens || !accepted_len || !tokens || !accept_prob)
-    return SV_EINVAL;
-  DeviceGuard g(h->device);
-  if (!g.ok) return SV_ECUDA;
-
+  if (B == 0) {
+    *empty = true;
+    return SV_OK;
+  }
+  if (!target_logits || !draft_logits || !draft_tokens) return SV_EINVAL;
   const int k = h->k, V = h->V;
-  sv::Params P{};
+  P = sv::Params{};
   P.Lt = target_logits;
   P.Ld = draft_logits;
   P.D = draft_tokens;
@@ -290,6 +364,39 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.min_cum = h->min_cum;
   for (int j = 0; j < k; ++j)
     P.tau_step[j] = h->n_sched > 0 ? h->sched[j < h->n_sched ? j : h->n_sched - 1] : 0.f;
+  P.part = h->part;
+  P.xD = h->xD;
+  P.cand = h->cand;
+  P.cand_over = h->cand_over;
+  const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
+  const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
+  P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);
+  P.vec_d = (row_d % 16 == 0) && (reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                             const void* draft_logits, sv_dtype ddt, const int32_t* draft_tokens,
+                             int B, float temperature, sv_gate gate_mode, float threshold,
+                             const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                             uint64_t seed, uint64_t seq_offset, const float* u_accept,
+                             const float* u_residual, int32_t* accepted_len, int32_t* tokens,
+                             float* accept_prob, int8_t* flags, uint64_t* counters,
+                             float* row_stats, void* cuda_stream) {
+  sv::Params P;
+  bool empty = false;
+  const sv_status ps = prepare_params(h, target_logits, tdt, draft_logits, ddt, draft_tokens, B,
+                                      temperature, gate_mode, threshold, gate_mode_per_seq,
+                                      threshold_per_seq, P, &empty);
+  if (ps != SV_OK || empty) return ps;
+  if (!accepted_len || !tokens || !accept_prob) return SV_EINVAL;
+  DeviceGuard g(h->device);
+  if (!g.ok) return SV_ECUDA;
+  const int k = h->k;
   P.seed = seed;
   P.seq_offset = seq_offset;
   P.u0 = u_accept;
@@ -300,14 +407,6 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   P.flags = flags;
   P.counters = reinterpret_cast<unsigned long long*>(counters);
   P.row_stats = row_stats;
-  P.part = h->part;
-  P.xD = h->xD;
-  P.cand = h->cand;
-  P.cand_over = h->cand_over;
-  const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
-  const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
-  P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);
-  P.vec_d = (row_d % 16 == 0) && (reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
 
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
@@ -324,6 +423,37 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   if (P.greedy) return launch_mode<sv::kModeGreedy>(h, P, bps, false, tb, db, st);
   if (P.has_sched || P.min_cum > 0.f) return launch_mode<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
   return launch_mode<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
+}
+
+sv_status spec_verify_diagnostics(spec_verify_t h, const void* target_logits, sv_dtype tdt,
+                                  const void* draft_logits, sv_dtype ddt,
+                                  const int32_t* draft_tokens, int B, float temperature,
+                                  sv_gate gate_mode, float threshold,
+                                  const uint8_t* gate_mode_per_seq, const float* threshold_per_seq,
+                                  float* min_sum, float* pq_sum, float* argmax_q, void* cuda_stream) {
+  sv::Params P;
+  bool empty = false;
+  const sv_status ps = prepare_params(h, target_logits, tdt, draft_logits, ddt, draft_tokens, B,
+                                      temperature, gate_mode, threshold, gate_mode_per_seq,
+                                      threshold_per_seq, P, &empty);
+  if (ps != SV_OK || empty) return ps;
+  if (!min_sum && !pq_sum && !argmax_q) return SV_OK;
+  if (!h->dnorm) return SV_EUNSUPPORTED;
+  DeviceGuard g(h->device);
+  if (!g.ok) return SV_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
+  const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
+  if (P.greedy) {
+    if (tb && db) return launch_diag<uint16_t, uint16_t, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+    if (tb && !db) return launch_diag<uint16_t, float, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+    if (!tb && db) return launch_diag<float, uint16_t, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+    return launch_diag<float, float, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  }
+  if (tb && db) return launch_diag<uint16_t, uint16_t, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  if (tb && !db) return launch_diag<uint16_t, float, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  if (!tb && db) return launch_diag<float, uint16_t, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  return launch_diag<float, float, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
 }
 
 sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,

@@ -64,7 +64,9 @@ constexpr float kGateSlack = 1.0f - 1.0f / 1024.0f;
 // with a gate policy (per-step thresholds and/or a cumulative floor), and
 // greedy decoding (temperature 0, which honours the policy too).  Each is its
 // own instantiation, so the plain sampling path carries no policy code.
-enum : int { kModeSample = 0, kModePolicy = 1, kModeGreedy = 2 };
+// kModeStats is the stream pass alone (chunk statistics and drafted-token
+// logits, no gate candidates), for the acceptance diagnostics.
+enum : int { kModeSample = 0, kModePolicy = 1, kModeGreedy = 2, kModeStats = 3 };
 
 struct Cand {  // a gate candidate: raw logit and token id (id -1: empty slot)
   float x;
@@ -517,7 +519,7 @@ __device__ __forceinline__ void process_chunk_greedy(const Params& P, const unsi
 }
 
 // one chunk, by one warp: statistics, drafted-token logit, gate candidates
-template <typename T, bool kPol>
+template <typename T, bool kPol, bool kCand>
 __device__ __forceinline__ void process_chunk(const Params& P, const unsigned char* stage, int b, int r,
                                               int ch, int d, int lane) {
   const int k = P.k;
@@ -546,7 +548,7 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   // > 1), and a chunk can hold one only if s <= 1 / (slack tau) (the chunk's
   // largest term contributes 1 to s): s < kTopM + 1 rules out almost every
   // chunk before the row's gate settings are even read
-  if (is_draft && s < static_cast<float>(kTopM + 1)) {
+  if (kCand && is_draft && s < static_cast<float>(kTopM + 1)) {
     const float tau = kPol ? step_floor(P, b, j) : seq_tau(P, b);
     if (seq_gated(P, b) && gate_fast_path(tau) && s > 0.f && isfinite(s)) {
       // a token's in-chunk probability exp2(fma(x, c, -mc)) / s reaches
@@ -594,6 +596,7 @@ template <typename TT, typename TD, int kMode>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
     stream_kernel(const __grid_constant__ Params P) {
   constexpr bool kPol = kMode == kModePolicy;
+  constexpr bool kCand = kMode != kModeStats;
   constexpr int S = Stages<TT, TD>::kDepth;
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
@@ -639,9 +642,9 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
       if (it.y <= k) process_chunk_greedy<TT>(P, stage, it.x, it.y, it.z, lane);
       else process_chunk_greedy<TD>(P, stage, it.x, it.y, it.z, lane);
     } else if (it.y <= k) {
-      process_chunk<TT, kPol>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TT, kPol, kCand>(P, stage, it.x, it.y, it.z, d, lane);
     } else {
-      process_chunk<TD, kPol>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TD, kPol, kCand>(P, stage, it.x, it.y, it.z, d, lane);
     }
     __syncwarp();
   }

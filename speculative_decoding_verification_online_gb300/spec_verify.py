@@ -64,6 +64,8 @@ def load() -> ctypes.CDLL:
     L.spec_verify_run_noalloc.restype = I
     L.spec_verify_set_gate_policy.argtypes = [P, P, I, F]
     L.spec_verify_set_gate_policy.restype = I
+    L.spec_verify_diagnostics.argtypes = [P, P, I, P, I, P, I, F, I, F, P, P, P, P, P, P]
+    L.spec_verify_diagnostics.restype = I
     _lib = L
     return L
 
@@ -115,6 +117,14 @@ def spec_verify_free(h) -> int:
 def spec_verify_set_gate_policy(h, schedule, n_schedule, min_cum) -> int:
     """Raw call: schedule is a ctypes float array (or None), min_cum a float."""
     return load().spec_verify_set_gate_policy(h, schedule, n_schedule, min_cum)
+
+
+def spec_verify_diagnostics(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode, threshold,
+                            gate_per_seq, threshold_per_seq, min_sum, pq_sum, argmax_q, stream) -> int:
+    """Raw call of the acceptance diagnostics; returns the status."""
+    return load().spec_verify_diagnostics(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode,
+                                          threshold, gate_per_seq, threshold_per_seq, min_sum,
+                                          pq_sum, argmax_q, stream)
 
 
 def spec_verify_launches_per_run() -> int:
@@ -246,6 +256,33 @@ class SpecVerifier:
         if rs is not None:
             o["row_stats"] = rs
         return o
+
+    def diagnostics(self, Lt, Ld, D, temperature, gate_mode=SV_PLAIN, threshold=0.5,
+                    gate_per_seq=None, threshold_per_seq=None, out=None, stream=None):
+        """Closed-form acceptance of every draft position: a dict of [B, k]
+        float device tensors min_sum (sum min(p, mu)), pq_sum (sum p q) and
+        argmax_q (q at the first largest p); NaN where the rows are invalid."""
+        B = Lt.shape[0]
+        k, V, dev = self.k, self.V, self.device
+        _check(Lt, "target_logits", (B, k + 1, V), device=dev)
+        _check(Ld, "draft_logits", (B, k, V), device=dev)
+        _check(D, "draft_tokens", (B, k), torch.int32, dev)
+        if gate_per_seq is not None:
+            _check(gate_per_seq, "gate_mode_per_seq", (B,), torch.uint8, dev)
+        if threshold_per_seq is not None:
+            _check(threshold_per_seq, "threshold_per_seq", (B,), torch.float32, dev)
+        if out is None:
+            out = {key: torch.empty(B, k, dtype=torch.float32, device=dev)
+                   for key in ("min_sum", "pq_sum", "argmax_q")}
+        st = torch.cuda.current_stream(dev).cuda_stream if stream is None else stream
+        rc = spec_verify_diagnostics(self.handle, Lt.data_ptr(), _dt(Lt), Ld.data_ptr(), _dt(Ld),
+                                     D.data_ptr(), B, float(temperature), int(gate_mode),
+                                     float(threshold), _ptr(gate_per_seq), _ptr(threshold_per_seq),
+                                     _ptr(out.get("min_sum")), _ptr(out.get("pq_sum")),
+                                     _ptr(out.get("argmax_q")), st)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_diagnostics")
+        return out
 
     def run_host(self, Lt, Ld, D, temperature, gate_mode=SV_PLAIN, threshold=0.5,
                  gate_per_seq=None, threshold_per_seq=None, seed=0, out=None, counters=None,

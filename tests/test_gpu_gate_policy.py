@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import workloads
-from tests.gpu_helpers import compare, oracle_for
+from tests.gpu_helpers import compare, oracle_for, peaked_workload as _peaked
 
 pytestmark = pytest.mark.gpu
 
@@ -25,27 +25,6 @@ def sv():
     B.build()
     pkg.load()
     return pkg
-
-
-def _peaked(B, k, V, dtype, seed, gate=1, tau=0.5, T=1.0, device="cuda"):
-    """Rows with one boosted token whose boost varies from row to row, so the
-    drafted tokens' q spans (0, 1) and gates pass and fail at every step."""
-    g = torch.Generator(device=device)
-    g.manual_seed(seed)
-    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    t = torch.randn(B, k + 1, V, generator=g, device=device)
-    peak = torch.randint(0, V, (B, k + 1), generator=g, device=device)
-    boost = 6.0 + 9.0 * torch.rand(B, k + 1, generator=g, device=device)
-    t.scatter_add_(2, peak.unsqueeze(-1), boost.unsqueeze(-1))
-    d = t[:, :k] + torch.randn(B, k, V, generator=g, device=device) * 0.5
-    Lt, Ld = t.to(dt), d.to(dt)
-    u = torch.rand(B, k, V, generator=g, device=device).clamp_(1e-30, 1 - 1e-7)
-    D = torch.argmax(Ld.float() / T - torch.log(-torch.log(u)), dim=2).to(torch.int32)
-    gate_t = torch.as_tensor(np.broadcast_to(np.asarray(gate, dtype=np.uint8), (B,)).copy(),
-                             device=device)
-    tau_t = torch.full((B,), float(tau), dtype=torch.float32, device=device)
-    return workloads.Workload(name="peaked", Lt=Lt, Ld=Ld, D=D, T=T, gate=gate_t, tau=tau_t,
-                              philox_seed=seed + 2, B=B, k=k, V=V, dtype=dtype)
 
 
 def _run(sv, ver, w, **kw):
