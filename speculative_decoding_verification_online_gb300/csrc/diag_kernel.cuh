@@ -323,6 +323,7 @@ __global__ void __launch_bounds__(kDiagThreads)
   const int g = static_cast<int>(blockIdx.x) * kDiagWarps + (threadIdx.x >> 5);
   const int k = P.k, V = P.V, nch = P.nchunk;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (g >= P.B * k) return;
   const DiagNorm nm = norm[g];
   if (nm.bad) {

@@ -90,6 +90,25 @@ cudaError_t configure(int* blocks_per_sm) {
                                                        dyn_smem<TT, TD>());
 }
 
+// a programmatic dependent launch: the kernel may become resident while the
+// previous kernel in the stream drains (it calls griddepcontrol.wait before it
+// reads what that kernel writes)
+template <typename K, typename... A>
+cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
+                             A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // the stream pass (variant G), with the handle's one-shot timing marks around it
 template <typename TT, typename TD, int G>
 sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
@@ -101,8 +120,11 @@ sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm,
   if (grid < 1) grid = 1;
   const bool marked = h->mark_before != nullptr;
   if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
-  sv::stream_kernel<TT, TD, G><<<static_cast<unsigned>(grid), sv::Stages<TT, TD>::kThreadsPerCta,
-                                 dyn_smem<TT, TD>(), st>>>(P);
+  // a programmatic dependent launch: resident early, it waits for the previous
+  // kernel in the stream before touching memory
+  if (launch_dependent(sv::stream_kernel<TT, TD, G>, static_cast<unsigned>(grid),
+                       sv::Stages<TT, TD>::kThreadsPerCta, dyn_smem<TT, TD>(), st, P) != cudaSuccess)
+    return SV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
   if (marked) {
     const cudaError_t e = cudaEventRecord(h->mark_after, st);
@@ -161,22 +183,6 @@ sv_status launch_mode(spec_verify_t h, const sv::Params& P, int bps, bool dense_
   return launch<float, float, G>(h, P, bps, dense_likely, st);
 }
 
-// PDL launch of a small per-(sequence, position) kernel: warp per pair
-template <typename K, typename... A>
-cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
-                             A... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
 
 // the acceptance diagnostics: the stream pass, the per-position merge, and
 // (temperature > 0) the pair sweep and its reduction, each launch a

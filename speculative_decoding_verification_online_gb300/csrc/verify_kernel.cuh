@@ -642,9 +642,15 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // step n - 1, so it has landed when the chunk has.
   if (threadIdx.x == 0) cta_next = 0u;
   __syncthreads();
-  // the finishing grid may launch at once: its CTAs take SMs as this grid's
-  // CTAs retire, run their input-only prologue, and wait (griddepcontrol.wait)
-  // for this grid to complete and its memory to be visible
+  // This grid is itself a programmatic dependent launch: its CTAs may be
+  // resident while the previous kernel in the stream (the producer of the
+  // logits, or the previous call's finishing pass, which reads the workspace)
+  // drains, and touch no global memory before that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Then the finishing grid may launch: its CTAs take SMs as this grid's CTAs
+  // retire, run their input-only prologue (the inputs are complete: see the
+  // wait above), and wait for this grid to complete and its memory to be
+  // visible.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lane == 0) put_item(P, Q, 0, next_chunk(P, &cta_next));
   __syncwarp();
@@ -1479,6 +1485,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_con
   const int cid = static_cast<int>(blockIdx.x) / csize;
   const int ncl = static_cast<int>(gridDim.x) / csize;
   FinishShared* lead = csize > 1 ? cluster.map_shared_rank(&sh, 0) : &sh;
+  // the next call's stream pass may launch (it waits for this grid to
+  // complete before it touches memory)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the first sequence's input-only work overlaps the end of the stream pass;
   // then wait for the stream pass (programmatic dependent launch) before
   // reading its output
