@@ -93,6 +93,19 @@ def overridden(args) -> bool:
             or args.min_cum > 0 or args.diagnostics)
 
 
+def gate_args(args, w, cfg, sv):
+    """The gate arguments of a call: the scalars when every sequence shares one
+    mode and threshold (what a caller with one configuration passes; the host
+    then knows whether dense residuals can occur), else the per-sequence arrays."""
+    recipe = args.gate or cfg["gate"]
+    if recipe == "gated":
+        return dict(gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]))
+    if recipe == "plain":
+        return dict(gate_mode=sv.SV_PLAIN, threshold=float(cfg["tau"]))
+    return dict(gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]), gate_per_seq=w.gate,
+                threshold_per_seq=w.tau)
+
+
 def gate_policy(args):
     sched = None
     if args.gate_schedule is not None:
@@ -108,17 +121,19 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profile_traffic():
+def profile_traffic(path=PROFILE, current_hash=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
-    if not os.path.exists(PROFILE):
+    the current kernel sources (else None).  The summary lists
+    `- kernel_hash: ...` and `- traffic_bytes_per_launch: ...` lines."""
+    if not os.path.exists(path):
         return None
     vals = {}
-    for line in open(PROFILE):
-        if ":" in line and line.strip().startswith(("kernel_hash", "traffic_bytes_per_launch")):
-            key, val = line.split(":", 1)
-            vals[key.strip(" -*`")] = val.strip(" `\n")
-    if vals.get("kernel_hash") != kernel_hash():
+    for line in open(path):
+        item = line.strip().lstrip("-* ")
+        if ":" in item and item.startswith(("kernel_hash", "traffic_bytes_per_launch")):
+            key, val = item.split(":", 1)
+            vals[key.strip(" `")] = val.strip(" `\n")
+    if vals.get("kernel_hash") != (current_hash or kernel_hash()):
         return None
     try:
         return int(vals["traffic_bytes_per_launch"])
@@ -330,16 +345,15 @@ def main():
     seq_offset = rank * B
     stream = torch.cuda.current_stream(dev)
 
+    gargs = [gate_args(args, w, cfg, sv) for w in sets]
+
     def step(i):
         w = sets[i % nsets]
         if args.diagnostics:
-            ver.diagnostics(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU,
-                            threshold=float(cfg["tau"]), gate_per_seq=w.gate,
-                            threshold_per_seq=w.tau, out=douts[i % nsets])
+            ver.diagnostics(w.Lt, w.Ld, w.D, w.T, out=douts[i % nsets], **gargs[i % nsets])
             return
-        ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]),
-                gate_per_seq=w.gate, threshold_per_seq=w.tau, seed=w.philox_seed,
-                seq_offset=seq_offset, out=outs[i % nsets])
+        ver.run(w.Lt, w.Ld, w.D, w.T, seed=w.philox_seed, seq_offset=seq_offset,
+                out=outs[i % nsets], **gargs[i % nsets])
 
     sampler = ClockSampler(local)
     for i in range(args.warmup):
@@ -412,10 +426,13 @@ def main():
                      accept_prob=torch.empty(B, k, dtype=torch.float32).pin_memory(),
                      flags=torch.empty(B, k, dtype=torch.int8).pin_memory())
 
+        ga = gate_args(args, wh, cfg, sv)
+        per_seq = "gate_per_seq" in ga
+        if per_seq:
+            ga = dict(ga, gate_per_seq=g_h, threshold_per_seq=tau_h)
+
         def hstep():
-            ver.run_host(Lt_h, Ld_h, D_h, wh.T, gate_mode=sv.SV_GATED_MU,
-                         threshold=float(cfg["tau"]), gate_per_seq=g_h, threshold_per_seq=tau_h,
-                         seed=wh.philox_seed, out=out_h)
+            ver.run_host(Lt_h, Ld_h, D_h, wh.T, seed=wh.philox_seed, out=out_h, **ga)
         for _ in range(3):
             hstep()
         n_e2e = max(1, args.e2e_steps)
@@ -424,7 +441,7 @@ def main():
             hstep()
         e2e_s = (time.perf_counter() - t0) / n_e2e
         h2d = (Lt_h.numel() * Lt_h.element_size() + Ld_h.numel() * Ld_h.element_size() +
-               D_h.numel() * 4 + g_h.numel() + tau_h.numel() * 4)
+               D_h.numel() * 4 + ((g_h.numel() + tau_h.numel() * 4) if per_seq else 0))
         d2h = sum(t.numel() * t.element_size() for t in out_h.values())
         e2e = {"value": ws * B * k / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
@@ -458,6 +475,7 @@ def main():
             "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
                        "logits_dtype": w0.dtype, "T": w0.T, "gate": args.gate or cfg["gate"],
                        "gate_schedule": sched, "min_cum": cum,
+                       "gate_args": "per-sequence arrays" if "gate_per_seq" in gargs[0] else "scalars",
                        "call": "spec_verify_diagnostics" if args.diagnostics else "spec_verify_run",
                        "threshold": cfg["tau"],
                        "l2": f"inputs larger than L2: {nsets} rotated copies of "

@@ -1,0 +1,40 @@
+"""Host logic of bench.py (no GPU): the ncu summary parser that feeds
+roofline.traffic, and the reference arm's JSON line."""
+import json
+import os
+import runpy
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    return runpy.run_path(os.path.join(ROOT, "bench.py"))
+
+
+def test_profile_traffic_reads_the_summary_only_for_the_current_sources(tmp_path):
+    b = _bench()
+    p = tmp_path / "summary.md"
+    p.write_text("# x\n\n- kernel_hash: `abc123`\n- traffic_bytes_per_launch: `184297984`\n")
+    assert b["profile_traffic"](str(p), current_hash="abc123") == 184297984
+    assert b["profile_traffic"](str(p), current_hash="other") is None
+    assert b["profile_traffic"](str(tmp_path / "missing.md"), current_hash="abc123") is None
+    # the committed summary names a 16-hex-digit hash and an integer byte count
+    text = open(os.path.join(ROOT, "profiles", "stream_kernel_b64_v128256_zipf_gated.md")).read()
+    assert "- kernel_hash: `" in text and "- traffic_bytes_per_launch: `" in text
+
+
+def test_reference_arm_prints_one_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0", "--workload", "tiny_v8_f32"],
+                         capture_output=True, text=True, check=True, cwd=ROOT, timeout=300)
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
