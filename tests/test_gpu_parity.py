@@ -100,6 +100,22 @@ def test_parity_k1_and_max_k(sv):
         ver.close()
 
 
+@pytest.mark.parametrize("V,dtype", [(4104, "bf16"), (4099, "bf16"), (2050, "f32"), (2047, "f32"), (7, "bf16")])
+def test_parity_partial_last_chunks_and_unaligned_rows(sv, V, dtype):
+    # the last chunk of a row: its whole 16-byte slots arrive by cp.async and
+    # the rest (a partial slot, the -inf padding) by plain loads; odd V also
+    # makes the rows unaligned, so every slot takes the plain path
+    B, k = 24, 3
+    w = _custom(B, k, V, dtype, 1.0, (np.arange(B) % 2), 0.3, seed=V + 11, scale=2.0, noise=0.5)
+    ver = _verifier(sv, w)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w)
+    compare(w, out, ref, what=f"partial V={V} {dtype}")
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[..., 1], ref["row_stats"][..., 1], rtol=1e-5, atol=1e-5)
+    ver.close()
+
+
 # ------------------------------------------------------ tiny config, 1e5 trials
 
 @pytest.mark.parametrize("gated", [0, 1])
