@@ -81,6 +81,15 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
                                          ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int]
         L.oracle_diagnostics.restype = ctypes.c_int
+        L.oracle_filtered_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                          ctypes.c_double, ctypes.c_double, P, P]
+        L.oracle_filtered_row.restype = ctypes.c_int
+        L.oracle_verify_filtered.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
+                                             ctypes.c_int, ctypes.c_double, P, P, P, ctypes.c_uint64,
+                                             ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P,
+                                             P, P, ctypes.c_int]
+        L.oracle_verify_filtered.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -128,9 +137,25 @@ def inverse_cdf(r: np.ndarray, u: float):
     return int(v), float(m[0])
 
 
+def filtered_row(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.0,
+                 min_p: float = 0.0):
+    """The filtered distribution of one row (temperature softmax, then top-k,
+    top-p, min-p): returns (p, margin)."""
+    p, _, _, ok = softmax_row(logits, T)
+    if not ok:
+        raise ValueError("invalid row")
+    x = np.ascontiguousarray(logits)
+    m = np.zeros(1, dtype=np.float64)
+    rc = lib().oracle_filtered_row(_ptr(x), _dtype_code(x), x.shape[-1], float(T), int(top_k),
+                                   float(top_p), float(min_p), _ptr(p), _ptr(m))
+    if rc != 0:
+        raise MemoryError("oracle_filtered_row")
+    return p, float(m[0])
+
+
 def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, seed: int = 0,
            seq_offset: int = 0, u0=None, u1=None, rule: int = RULE_MU, nthreads: int = 1,
-           tau_sched=None, min_cum: float = 0.0):
+           tau_sched=None, min_cum: float = 0.0, filters=None):
     """Run the oracle on a batch.
 
     Lt [B, k+1, V], Ld [B, k, V] (float32, or uint16 bf16 bits), D [B, k] int32.
@@ -138,7 +163,9 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
     ``u0`` [B, k] / ``u1`` [B] give explicit uniforms instead of Philox draws.
     ``tau_sched`` (a sequence of per-step thresholds, the last repeating) and
     ``min_cum`` (the cumulative floor, 0 = off) are the gate policy of gated
-    sequences (``oracle_verify_policy``).
+    sequences (``oracle_verify_policy``).  ``filters`` = ((top_k, top_p,
+    min_p) of the target rows, (top_k, top_p, min_p) of the draft rows) turns
+    on the sampler filters (``oracle_verify_filtered``).
     Returns a dict of numpy arrays: accepted_len, tokens, alpha, flags,
     row_stats [B, 2k+1, 2] (max, lse of L/T), margin (all used draws),
     margin_pick (the residual / bonus pick alone), degenerate.
@@ -168,13 +195,19 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
     )
     sched = None if tau_sched is None else np.ascontiguousarray(tau_sched, dtype=np.float64).ravel()
     n_sched = 0 if sched is None else int(sched.shape[0])
-    rc = lib().oracle_verify_policy(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B,
-                                    k, V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
-                                    float(min_cum), int(seed), int(seq_offset), _ptr(u0), _ptr(u1),
-                                    int(rule), _ptr(out["accepted_len"]), _ptr(out["tokens"]),
-                                    _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
-                                    _ptr(out["margin"]), _ptr(out["margin_pick"]),
-                                    _ptr(out["degenerate"]), int(nthreads))
+    fk = fp = fm = None
+    if filters is not None:
+        fk = np.array([int(filters[0][0]), int(filters[1][0])], dtype=np.int32)
+        fp = np.array([float(filters[0][1]), float(filters[1][1])], dtype=np.float64)
+        fm = np.array([float(filters[0][2]), float(filters[1][2])], dtype=np.float64)
+    rc = lib().oracle_verify_filtered(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D),
+                                      B, k, V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
+                                      float(min_cum), _ptr(fk), _ptr(fp), _ptr(fm), int(seed),
+                                      int(seq_offset), _ptr(u0), _ptr(u1), int(rule),
+                                      _ptr(out["accepted_len"]), _ptr(out["tokens"]),
+                                      _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
+                                      _ptr(out["margin"]), _ptr(out["margin_pick"]),
+                                      _ptr(out["degenerate"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out

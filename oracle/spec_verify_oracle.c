@@ -117,6 +117,103 @@ int oracle_softmax_row(const void* logits, int dt, int64_t V, double T,
   return 0;
 }
 
+/* ------------------------------------------------------------ filters */
+
+typedef struct {
+  double x;   /* logit */
+  int64_t v;  /* token */
+} ranked_t;
+
+/* decreasing logit, then increasing token */
+static int ranked_cmp(const void* a, const void* b) {
+  const ranked_t* ra = (const ranked_t*)a;
+  const ranked_t* rb = (const ranked_t*)b;
+  if (ra->x > rb->x) return -1;
+  if (ra->x < rb->x) return 1;
+  return ra->v < rb->v ? -1 : (ra->v > rb->v ? 1 : 0);
+}
+
+/* The sampler's filter chain after the temperature [M "What changed": the
+ * sampler's own chain -- temperature, top-k, top-p, min-p -- whose softmax is
+ * the effective distribution; a top_k of 1 is greedy].  p holds the row's
+ * temperature softmax on entry and the filtered, renormalised distribution on
+ * exit.  Readings: each filter keeps every token tied with its boundary
+ * token; top-p works on the top-k survivors renormalised, in decreasing
+ * probability, keeping the shortest prefix whose mass reaches top_p; min-p
+ * keeps p >= min_p * max p.  *margin: the smallest relative distance of a
+ * top-p or min-p decision to its boundary (top-k compares logits exactly). */
+int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top_k, double top_p,
+                        double min_p, double* p, double* margin) {
+  double marg = INFINITY;
+  const int use_k = top_k >= 1 && (int64_t)top_k < V;
+  const int use_p = top_p > 0.0 && top_p < 1.0;
+  const int use_m = min_p > 0.0;
+  if (margin) *margin = marg;
+  if (T == 0.0 || !(use_k || use_p || use_m)) return 0;  /* greedy rows are one-hot already */
+  ranked_t* rk = (ranked_t*)malloc((size_t)V * sizeof(ranked_t));
+  unsigned char* keep = (unsigned char*)malloc((size_t)V);
+  if (!rk || !keep) {
+    free(rk); free(keep);
+    return 1;
+  }
+  for (int64_t v = 0; v < V; ++v) {
+    rk[v].x = logit_at(logits, dt, v);
+    rk[v].v = v;
+    keep[v] = 1;
+  }
+  qsort(rk, (size_t)V, sizeof(ranked_t), ranked_cmp);
+  if (top_k == 1) {
+    /* greedy: one-hot at the first largest logit */
+    for (int64_t v = 0; v < V; ++v) p[v] = 0.0;
+    p[rk[0].v] = 1.0;
+    free(rk); free(keep);
+    return 0;
+  }
+  if (use_k) {
+    const double xk = rk[top_k - 1].x;
+    for (int64_t i = 0; i < V; ++i) keep[rk[i].v] = rk[i].x >= xk;
+  }
+  if (use_p) {
+    double Sk = 0.0;
+    for (int64_t i = 0; i < V; ++i)
+      if (keep[rk[i].v]) Sk += p[rk[i].v];
+    const double target = top_p * Sk;
+    double c = 0.0, before = 0.0;
+    int64_t m = -1;
+    for (int64_t i = 0; i < V; ++i) {
+      if (!keep[rk[i].v]) continue;
+      before = c;
+      c += p[rk[i].v];
+      if (c >= target) {
+        m = i;
+        break;
+      }
+    }
+    if (m >= 0) {
+      marg = fmin(marg, fmin(target - before, c - target) / Sk);
+      const double xm = rk[m].x;
+      for (int64_t i = 0; i < V; ++i)
+        if (rk[i].x < xm) keep[rk[i].v] = 0;
+    }
+  }
+  if (use_m) {
+    const double xmax = rk[0].x;
+    for (int64_t i = 0; i < V; ++i) {
+      if (!keep[rk[i].v]) continue;
+      const double ratio = exp((rk[i].x - xmax) / T);  /* p / max p */
+      marg = fmin(marg, fabs(ratio - min_p));
+      if (!(ratio >= min_p)) keep[rk[i].v] = 0;
+    }
+  }
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v)
+    if (keep[v]) S += p[v];
+  for (int64_t v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / S : 0.0;
+  free(rk); free(keep);
+  if (margin) *margin = marg;
+  return 0;
+}
+
 /* ------------------------------------------------------------ sampling */
 
 /* Inverse-CDF pick: the smallest v with prefix(v) > u * Z.  Reading: the
@@ -174,6 +271,8 @@ typedef struct {
   double* row_stats; double* margin; double* margin_pick; int32_t* degenerate;
   const double* tau_sched; int n_sched; /* per-step thresholds (NULL: tau[b] at every step) */
   double min_cum;                       /* cumulative floor (0: no cumulative gate) */
+  /* sampler filters of the target [0] and draft [1] rows (NULL: none) */
+  const int* top_k; const double* top_p; const double* min_p;
   /* oracle_diagnostics outputs (diagnose = 1 runs diagnose_one instead of verify_one) */
   int diagnose;
   double* diag_min; double* diag_pq; double* diag_argq;
@@ -257,12 +356,18 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   const int32_t* Db = J->D + (int64_t)b * k;
   const int esz_t = J->tdt == ORACLE_BF16 ? 2 : 4, esz_d = J->ddt == ORACLE_BF16 ? 2 : 4;
 
-  /* step 1: the row distributions p_0..p_k and q_0..q_{k-1} */
+  /* step 1: the row distributions p_0..p_k and q_0..q_{k-1} (row
+   * statistics of the unfiltered L/T), filtered when filters are set */
   int invalid = 0;
+  double fmarg = INFINITY;  /* filter decisions near their boundaries */
   for (int j = 0; j <= k; ++j) {
     const char* row = (const char*)J->Lt + ((int64_t)b * (k + 1) + j) * V * esz_t;
-    double mx, lse;
+    double mx, lse, fm = INFINITY;
     invalid |= oracle_softmax_row(row, J->tdt, V, J->T, S->P + (int64_t)j * V, &mx, &lse);
+    if (J->top_k && !invalid)
+      invalid |= oracle_filtered_row(row, J->tdt, V, J->T, J->top_k[0], J->top_p[0], J->min_p[0],
+                                     S->P + (int64_t)j * V, &fm);
+    fmarg = fmin(fmarg, fm);
     if (J->row_stats) {
       J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 0] = mx;
       J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 1] = lse;
@@ -270,8 +375,12 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   }
   for (int j = 0; j < k; ++j) {
     const char* row = (const char*)J->Ld + ((int64_t)b * k + j) * V * esz_d;
-    double mx, lse;
+    double mx, lse, fm = INFINITY;
     invalid |= oracle_softmax_row(row, J->ddt, V, J->T, S->Q + (int64_t)j * V, &mx, &lse);
+    if (J->top_k && !invalid)
+      invalid |= oracle_filtered_row(row, J->ddt, V, J->T, J->top_k[1], J->top_p[1], J->min_p[1],
+                                     S->Q + (int64_t)j * V, &fm);
+    fmarg = fmin(fmarg, fm);
     if (J->row_stats) {
       J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 0] = mx;
       J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 1] = lse;
@@ -280,7 +389,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
   for (int j = 0; j < k; ++j)
     if (Db[j] < 0 || (int64_t)Db[j] >= V) invalid = 1;
 
-  double marg = INFINITY;      /* accept tests and gates of tested positions */
+  double marg = fmarg;         /* accept tests, gates of tested positions, filters */
   double marg_pick = INFINITY; /* the residual / bonus pick */
   if (J->degenerate) J->degenerate[b] = 0;
   if (invalid) {
@@ -567,7 +676,26 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
                          int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                          double* row_stats, double* margin, double* margin_pick,
                          int32_t* degenerate, int nthreads) {
+  return oracle_verify_filtered(Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, tau_sched, n_sched, min_cum,
+                                NULL, NULL, NULL, seed, seq_offset, u0, u1, rule, accepted_len, tokens,
+                                alpha, flags, row_stats, margin, margin_pick, degenerate, nthreads);
+}
+
+int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                           int B, int k, int64_t V, double T,
+                           const uint8_t* gate, const double* tau,
+                           const double* tau_sched, int n_sched, double min_cum,
+                           const int* top_k, const double* top_p, const double* min_p,
+                           uint64_t seed, uint64_t seq_offset,
+                           const double* u0, const double* u1, int rule,
+                           int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                           double* row_stats, double* margin, double* margin_pick,
+                           int32_t* degenerate, int nthreads) {
   if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
+  if ((top_k != NULL) != (top_p != NULL) || (top_k != NULL) != (min_p != NULL)) return 1;
+  for (int i = 0; top_k && i < 2; ++i)
+    if (top_k[i] < 0 || !(top_p[i] > 0.0 && top_p[i] <= 1.0) || !(min_p[i] >= 0.0 && min_p[i] <= 1.0))
+      return 1;
   if (tau_sched && n_sched < 1) return 1;
   if (!(min_cum >= 0.0 && min_cum <= 1.0)) return 1;
   if (B == 0) return 0;
@@ -576,7 +704,7 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
   if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_MU_STEP_ONLY) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
              accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate,
-             tau_sched, n_sched, min_cum, 0, NULL, NULL, NULL};
+             tau_sched, n_sched, min_cum, top_k, top_p, min_p, 0, NULL, NULL, NULL};
   return run_jobs(&J, nthreads);
 }
 
@@ -594,7 +722,7 @@ int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const i
   if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, 0, 0, NULL, NULL, ORACLE_RULE_MU,
              NULL, NULL, NULL, NULL, NULL, margin, NULL, NULL,
-             tau_sched, n_sched, min_cum, 1, min_sum, pq_sum, argmax_q};
+             tau_sched, n_sched, min_cum, NULL, NULL, NULL, 1, min_sum, pq_sum, argmax_q};
   return run_jobs(&J, nthreads);
 }
 

@@ -144,6 +144,42 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
                          int32_t* degenerate, int nthreads);
 
 /*
+ * The sampler's filter chain on one row [M] "What changed" (temperature,
+ * top-k, top-p, min-p, then the softmax; top_k == 1 is greedy):
+ *   top_k >= 1: keep the tokens whose logit is at least the k-th largest
+ *     (ties at the boundary kept); 0 = off; 1 = one-hot at the first largest.
+ *   top_p in (0, 1): on the top-k survivors, renormalised, in decreasing
+ *     probability, keep the shortest prefix whose mass reaches top_p, plus
+ *     every token tied with its last one; 1 = off.
+ *   min_p in (0, 1]: keep p >= min_p * max p; 0 = off.
+ * p holds the row's temperature softmax (oracle_softmax_row) on entry and the
+ * renormalised filtered distribution on exit; T = 0 rows are left one-hot.
+ * *margin (may be NULL): the smallest distance of a top-p decision (in units
+ * of the top-k mass) or a min-p decision (in units of p / max p) to its
+ * boundary.  Returns 0, or 1 when memory runs out.
+ */
+int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top_k, double top_p,
+                        double min_p, double* p, double* margin);
+
+/*
+ * oracle_verify_policy with sampler filters: top_k[2], top_p[2], min_p[2]
+ * (index 0 the target rows, 1 the draft rows; all three NULL for none) turn
+ * every p_j and q_j into its filtered distribution (oracle_filtered_row)
+ * before the rule runs; row_stats stay those of the unfiltered L/T; margin
+ * also covers the filter decisions of every row of the sequence.
+ */
+int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                           int B, int k, int64_t V, double T,
+                           const uint8_t* gate, const double* tau,
+                           const double* tau_sched, int n_sched, double min_cum,
+                           const int* top_k, const double* top_p, const double* min_p,
+                           uint64_t seed, uint64_t seq_offset,
+                           const double* u0, const double* u1, int rule,
+                           int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
+                           double* row_stats, double* margin, double* margin_pick,
+                           int32_t* degenerate, int nthreads);
+
+/*
  * Closed-form acceptance of every draft position [M] "The acceptance ceiling":
  * for a draft drawn from q_j,
  *   min_sum[b, j]  = sum_x min(p_j(x), mu_j(x))  -- modified rejection sampling

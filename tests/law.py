@@ -28,9 +28,15 @@ from scipy.special import softmax
 from oracle import oracle as O
 
 
-def distributions(Lt: np.ndarray, Ld: np.ndarray, T: float):
-    P = softmax(Lt.astype(np.float64) / T, axis=-1)
-    Q = softmax(Ld.astype(np.float64) / T, axis=-1)
+def distributions(Lt: np.ndarray, Ld: np.ndarray, T: float, filters=None):
+    """Row distributions: scipy's softmax, or -- with sampler filters -- the
+    oracle's filtered rows (pinned on their own by the filter examples)."""
+    if filters is None:
+        P = softmax(Lt.astype(np.float64) / T, axis=-1)
+        Q = softmax(Ld.astype(np.float64) / T, axis=-1)
+        return P, Q
+    P = np.stack([O.filtered_row(r, T, *filters[0])[0] for r in Lt])
+    Q = np.stack([O.filtered_row(r, T, *filters[1])[0] for r in Ld])
     return P, Q
 
 
@@ -75,18 +81,18 @@ def _u1_edges(P, Q, gated, tau, grid, tau_sched=None, min_cum=0.0):
     return e
 
 
-def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32, tau_sched=None, min_cum=0.0):
+def exact_law(Lt, Ld, T, gated, tau, rule=O.RULE_MU, grid=32, tau_sched=None, min_cum=0.0, filters=None):
     """Law of (accepted_len, tokens) for one sequence, as a dict -> probability.
 
     Lt [k+1, V], Ld [k, V] float32 (one sequence); tau_sched / min_cum: the
     gate policy passed through to the oracle.
     """
-    pol = dict(tau_sched=tau_sched, min_cum=min_cum)
+    pol = dict(tau_sched=tau_sched, min_cum=min_cum, filters=filters)
     Lt = np.asarray(Lt, dtype=np.float32)
     Ld = np.asarray(Ld, dtype=np.float32)
     k1, V = Lt.shape
     k = k1 - 1
-    P, Q = distributions(Lt, Ld, T)
+    P, Q = distributions(Lt, Ld, T, filters)
     drafts = np.array(list(itertools.product(range(V), repeat=k)), dtype=np.int32)
     nD = drafts.shape[0]
     wD = np.prod(Q[np.arange(k)[None, :], drafts], axis=1)

@@ -703,3 +703,94 @@ def test_diagnostics_greedy_and_invalid_rows():
     assert np.isfinite(d["pq_sum"][0, 0]) and np.isnan(d["pq_sum"][0, 1])
     d = O.diagnostics(Lt, Ld, np.array([[7, 0]]), 1.0, 1, 0.3)
     assert np.all(np.isfinite(d["pq_sum"]))
+
+
+# ------------------------------------------------------------ sampler filters
+
+def test_filter_examples_worked_by_hand():
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    L = np.log(p).astype(np.float32)
+    rows = _golden_rows("filter_examples.txt")
+    assert len(rows) == 10
+    for r in rows:
+        top_k, top_p, min_p = int(r[0]), float(r[1]), float(r[2])
+        want = np.array([float(x) for x in r[3:]])
+        got, margin = O.filtered_row(L, 1.0, top_k, top_p, min_p)
+        np.testing.assert_allclose(got, want, atol=1e-6, err_msg=str(r[:3]))
+        assert margin > 1e-3  # no example sits on a boundary
+
+
+def test_filters_keep_ties_and_follow_the_chain_order():
+    # ties at the top-k boundary are kept
+    L = np.array([2.0, 1.0, 1.0, 0.0], dtype=np.float32)
+    got, _ = O.filtered_row(L, 1.0, 2, 1.0, 0.0)
+    e = np.exp([2.0, 1.0, 1.0])
+    np.testing.assert_allclose(got, np.append(e / e.sum(), 0.0), atol=1e-12)
+    # top-p sees the top-k survivors renormalised: p = (0.5, 0.3, 0.15, 0.05)
+    # with top_k = 2 gives (0.625, 0.375), so top_p = 0.6 keeps one token,
+    # while on the full row 0.6 would keep two
+    L = np.log(np.array([0.5, 0.3, 0.15, 0.05])).astype(np.float32)
+    assert np.count_nonzero(O.filtered_row(L, 1.0, 2, 0.6, 0.0)[0]) == 1
+    assert np.count_nonzero(O.filtered_row(L, 1.0, 0, 0.6, 0.0)[0]) == 2
+    # min_p = 1 keeps the largest only; filters off leave the softmax as is
+    assert np.count_nonzero(O.filtered_row(L, 1.0, 0, 1.0, 1.0)[0]) == 1
+    p0, _, _, _ = O.softmax_row(L, 1.3)
+    np.testing.assert_array_equal(O.filtered_row(L, 1.3, 0, 1.0, 0.0)[0], p0)
+
+
+def test_filtered_target_support_is_never_violated():
+    # [M "Where chi-square is blind"]: a top_k = 2 target against an
+    # unfiltered drafter must never emit (or accept) a token outside the
+    # target's two-token support
+    rng = np.random.default_rng(12)
+    n, k, V = 3000, 3, 6
+    Lt = (rng.standard_normal((k + 1, V)) * 1.5).astype(np.float32)
+    Ld = (rng.standard_normal((k, V)) * 1.5).astype(np.float32)
+    _, Q = distributions(Lt, Ld, 1.0)
+    D = np.stack([rng.choice(V, size=n, p=Q[j]) for j in range(k)], axis=1).astype(np.int32)
+    filt = ((2, 1.0, 0.0), (0, 1.0, 0.0))
+    out = O.verify(np.broadcast_to(Lt, (n, k + 1, V)), np.broadcast_to(Ld, (n, k, V)), D, 1.0, 0, 0.5,
+                   seed=3, nthreads=4, filters=filt)
+    support = [set(np.argsort(-Lt[j])[:2]) for j in range(k + 1)]
+    for b in range(n):
+        a = out["accepted_len"][b]
+        for j in range(a + 1):
+            assert out["tokens"][b, j] in support[j], (b, j)
+
+
+@pytest.mark.parametrize("filt", [((2, 1.0, 0.0), (0, 1.0, 0.0)), ((0, 0.7, 0.0), (3, 1.0, 0.0)),
+                                  ((3, 0.9, 0.1), (2, 0.8, 0.0)), ((0, 1.0, 0.3), (0, 1.0, 0.2))])
+@pytest.mark.parametrize("gated", [False, True])
+def test_exact_law_is_lossless_with_filtered_distributions(filt, gated):
+    # modified rejection sampling preserves whatever p it is given: the
+    # emitted marginals equal the filtered target rows, drafts drawn from the
+    # filtered draft rows
+    rng = np.random.default_rng(5 + int(gated) + 10 * filt[0][0])
+    Lt, Ld = _random_case(rng, 5, 2, scale=1.5)
+    law = exact_law(Lt, Ld, 1.0, gated, 0.3, filters=filt)
+    P, _ = distributions(Lt, Ld, 1.0, filt)
+    _check_emits_p(law, P)
+
+
+def test_top_k_one_is_greedy_and_filters_off_change_nothing():
+    rng = np.random.default_rng(8)
+    B, k, V = 200, 3, 12
+    Lt, Ld, D = _greedy_case(rng, B, k, V, ties=False)
+    for gated in (0, 1):
+        g = O.verify(Lt, Ld, D, 0.0, gated, 0.5, seed=4)
+        f = O.verify(Lt, Ld, D, 0.9, gated, 0.5, seed=4, filters=((1, 1.0, 0.0), (1, 1.0, 0.0)))
+        for key in ("accepted_len", "tokens", "flags", "alpha"):
+            assert np.array_equal(g[key], f[key]), key
+    a = O.verify(Lt, Ld, D, 0.9, 1, 0.5, seed=4)
+    b = O.verify(Lt, Ld, D, 0.9, 1, 0.5, seed=4, filters=((0, 1.0, 0.0), (0, 1.0, 0.0)))
+    for key in ("accepted_len", "tokens", "flags", "alpha", "margin"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_filter_margin_reports_top_p_and_min_p_boundaries():
+    L = np.log(np.array([0.5, 0.3, 0.15, 0.05])).astype(np.float32)
+    assert O.filtered_row(L, 1.0, 0, 0.8 + 1e-8, 0.0)[1] < 1e-6   # 0.5 + 0.3 reaches 0.8
+    assert O.filtered_row(L, 1.0, 0, 1.0, 0.3 + 1e-8)[1] < 1e-6   # 0.15 / 0.5 = 0.3
+    with pytest.raises(ValueError):
+        O.verify(L[None, None].repeat(2, 1), L[None, None], np.zeros((1, 1)), 1.0, 0, 0.5,
+                 filters=((0, 0.0, 0.0), (0, 1.0, 0.0)))
