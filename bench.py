@@ -7,11 +7,14 @@ synthetic workload, inputs resident in HBM.  Prints one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--temperature T] [--gate plain|gated|half]
                   [--gate-schedule T0,T1,...] [--min-cum F] [--diagnostics]
+                  [--target-filter K,P,M] [--draft-filter K,P,M]
 
 --temperature and --gate override the workload's temperature (0 = greedy
 decoding) and gate recipe; the logits and drafted tokens stay the same.
 --gate-schedule / --min-cum set the gate policy of the gated sequences
 (per-step thresholds, the last repeating; the cumulative prefix-product floor).
+--target-filter / --draft-filter set the sampler filters (top_k, top_p, min_p)
+of the target and draft rows.
 --diagnostics times spec_verify_diagnostics (the closed-form acceptance of
 every draft position: a stream pass plus a second read of each (p_j, q_j)
 pair) instead of the verification call; it has no host-buffer entry point, so
@@ -64,6 +67,8 @@ def parse():
                     help="per-step gate thresholds, comma-separated (the last repeats)")
     ap.add_argument("--min-cum", type=float, default=0.0,
                     help="cumulative floor on the drafted prefix's product of draft probabilities")
+    ap.add_argument("--target-filter", default=None, help="top_k,top_p,min_p of the target rows")
+    ap.add_argument("--draft-filter", default=None, help="top_k,top_p,min_p of the draft rows")
     ap.add_argument("--diagnostics", action="store_true",
                     help="time the closed-form acceptance diagnostics instead of verification")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -90,7 +95,18 @@ def make_workload(args, seed, device, B=None):
 
 def overridden(args) -> bool:
     return (args.temperature is not None or args.gate is not None or args.gate_schedule is not None
-            or args.min_cum > 0 or args.diagnostics)
+            or args.min_cum > 0 or args.diagnostics or filters_of(args) is not None)
+
+
+def filters_of(args):
+    """((top_k, top_p, min_p) target, (...) draft), or None when both are off."""
+    def parse_one(text):
+        if text is None:
+            return (0, 1.0, 0.0)
+        k, p, m = text.split(",")
+        return (int(k), float(p), float(m))
+    ft, fd = parse_one(args.target_filter), parse_one(args.draft_filter)
+    return None if ft == fd == (0, 1.0, 0.0) else (ft, fd)
 
 
 def gate_args(args, w, cfg, sv):
@@ -205,7 +221,7 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
+def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0, filters=None):
     """Time the fp64 oracle on the workload's sequences for about `seconds`."""
     from oracle import oracle as O
     Lt = workloads.to_numpy_logits(w.Lt)
@@ -214,10 +230,11 @@ def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
     gate = w.gate.cpu().numpy()
     tau = w.tau.cpu().numpy().astype(np.float64)
     pol = dict(tau_sched=sched, min_cum=cum)
-    O.verify(Lt[:1], Ld[:1], D[:1], w.T, gate[:1], tau[:1], seed=w.philox_seed, **pol)  # build + warm
+    O.verify(Lt[:1], Ld[:1], D[:1], w.T, gate[:1], tau[:1], seed=w.philox_seed,
+             **dict(pol, filters=filters))  # build + warm
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=nthreads, **pol)
+        O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=nthreads, filters=filters, **pol)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -225,7 +242,7 @@ def cpu_oracle_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
     return reps * w.B * w.k / el, reps, el
 
 
-def cpu_diag_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
+def cpu_diag_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0, filters=None):
     """Time the fp64 oracle's diagnostics on the workload's sequences for about `seconds`."""
     from oracle import oracle as O
     Lt = workloads.to_numpy_logits(w.Lt)
@@ -236,7 +253,7 @@ def cpu_diag_rate(w, seconds: float, nthreads: int, sched=None, cum=0.0):
     pol = dict(tau_sched=sched, min_cum=cum)
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=nthreads, **pol)
+        O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=nthreads, filters=filters, **pol)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -261,11 +278,13 @@ def run_reference(args, ws, rank):
     sched, cum = gate_policy(args)
     pol = dict(tau_sched=sched, min_cum=cum)
 
+    filt = filters_of(args)
+
     def one():
         if args.diagnostics:
-            O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=cores, **pol)
+            O.diagnostics(Lt, Ld, D, w.T, gate, tau, nthreads=cores, filters=filt, **pol)
         else:
-            O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, **pol)
+            O.verify(Lt, Ld, D, w.T, gate, tau, seed=w.philox_seed, nthreads=cores, filters=filt, **pol)
     t0 = time.perf_counter()
     one()
     t_step = time.perf_counter() - t0
@@ -293,7 +312,7 @@ def run_reference(args, ws, rank):
         "config": {"workload": args.workload, "B_sample": sample_B, "k": w.k, "V": w.V,
                    "logits_dtype": w.dtype, "T": w.T,
                    "gate": args.gate or workloads.CONFIGS[args.workload]["gate"],
-                   "gate_schedule": sched, "min_cum": cum,
+                   "gate_schedule": sched, "min_cum": cum, "filters": filt,
                    "call": "oracle_diagnostics" if args.diagnostics else "oracle_verify"},
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -339,6 +358,9 @@ def main():
     sched, cum = gate_policy(args)
     if sched is not None or cum > 0:
         ver.set_gate_policy(sched, cum)
+    filt = filters_of(args)
+    if filt is not None:
+        ver.set_filters(*filt)
     outs = [ver.outputs(B) for _ in range(nsets)]
     douts = [{key: torch.empty(B, k, dtype=torch.float32, device=dev)
               for key in ("min_sum", "pq_sum", "argmax_q")} for _ in range(nsets)]
@@ -450,14 +472,14 @@ def main():
     if rank == 0 and args.diagnostics:
         cores = os.cpu_count() or 1
         small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
-        rate, reps, cel = cpu_diag_rate(small, args.cpu_seconds, cores, sched, cum)
+        rate, reps, cel = cpu_diag_rate(small, args.cpu_seconds, cores, sched, cum, filters_of(args))
         cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
                "sample": f"oracle_diagnostics on {small.B} sequences of {args.workload} x {reps} "
                          f"repetitions ({cel:.1f} s)"}
     elif rank == 0:
         cores = os.cpu_count() or 1
         small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
-        rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores, sched, cum)
+        rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores, sched, cum, filters_of(args))
         cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
                "sample": f"{small.B} sequences of {args.workload} x {reps} repetitions "
                          f"({cel:.1f} s)"}
@@ -474,7 +496,7 @@ def main():
             "data": "synthetic",
             "config": {"workload": args.workload, "B_per_gpu": B, "k": k, "V": V,
                        "logits_dtype": w0.dtype, "T": w0.T, "gate": args.gate or cfg["gate"],
-                       "gate_schedule": sched, "min_cum": cum,
+                       "gate_schedule": sched, "min_cum": cum, "filters": filt,
                        "gate_args": "per-sequence arrays" if "gate_per_seq" in gargs[0] else "scalars",
                        "call": "spec_verify_diagnostics" if args.diagnostics else "spec_verify_run",
                        "threshold": cfg["tau"],
@@ -493,9 +515,11 @@ def main():
                                    "the K steps"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            # the diagnostics launch 4 kernels per call (2 at temperature 0)
-            "gpu_launches": args.steps * ((2 if w0.T == 0 else 4) if args.diagnostics
-                                          else sv.spec_verify_launches_per_run()),
+            # the diagnostics launch 4 kernels per call (2 at temperature 0);
+            # sampler filters add 3 in front (temperature > 0)
+            "gpu_launches": args.steps * (((2 if w0.T == 0 else 4) if args.diagnostics
+                                           else sv.spec_verify_launches_per_run())
+                                          + (3 if filt is not None and w0.T > 0 else 0)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -231,6 +231,34 @@ sv_status spec_verify_run_host(spec_verify_t h,
 sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, int n_schedule,
                                       float min_cum);
 
+/* Sampler filters of the target rows (p) and the draft rows (q) of every later
+ * call on this handle: mlxcel PR #992, "What changed" -- the effective
+ * distribution is the sampler's own chain: temperature, top-k, top-p, min-p,
+ * then the softmax of the survivors; top_k == 1 is greedy.
+ *   top_k >= 0: keep the tokens whose logit is at least the k-th largest (ties
+ *     at the boundary kept); 0 = off; 1 = only the first largest logit.
+ *   top_p in (0, 1]: on the top-k survivors renormalised, in decreasing
+ *     probability, keep the shortest prefix whose mass reaches top_p, plus the
+ *     tokens tied with its last one; 1 = off.
+ *   min_p in [0, 1]: keep p >= min_p * max p; 0 = off.
+ * With any filter on (and temperature > 0) a call first runs a statistics pass
+ * over the logits, finds each row's kept set, writes masked copies of the
+ * logits (-inf outside the kept set; a NaN is kept so the row stays invalid)
+ * into a buffer of the handle (max_B * (2k+1) * V * 4 bytes, allocated on the
+ * first filtered call) and then verifies the copies exactly as an unfiltered
+ * call would: 5 launches instead of 2 and about five reads of the logits.
+ * row_stats then describe the filtered rows.  spec_verify_diagnostics applies
+ * the same filters.  Decisions of top-p and min-p sit on fp32 arithmetic (the
+ * top-p masses are summed as integers, so they do not depend on the order of
+ * the additions).  Default: all off.  Returns SV_EINVAL (filters unchanged) for
+ * a NULL handle or a value outside its range. */
+sv_status spec_verify_set_filters(spec_verify_t h, int top_k_target, float top_p_target,
+                                  float min_p_target, int top_k_draft, float top_p_draft,
+                                  float min_p_draft);
+
+/* Kernel launches of a call with sampler filters on (temperature > 0). */
+int spec_verify_launches_per_filtered_run(void);
+
 /* Release the handle and its device memory (NULL is a no-op).  Synchronises
  * the handle's device first. */
 sv_status spec_verify_free(spec_verify_t h);

@@ -79,16 +79,17 @@ def lib() -> ctypes.CDLL:
         L.oracle_verify_policy.restype = ctypes.c_int
         L.oracle_diagnostics.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
                                          ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
-                                         ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int]
+                                         ctypes.c_int, ctypes.c_double, P, P, P, P, P, P, P,
+                                         ctypes.c_int]
         L.oracle_diagnostics.restype = ctypes.c_int
         L.oracle_filtered_row.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
-                                          ctypes.c_double, ctypes.c_double, P, P]
+                                          ctypes.c_double, ctypes.c_double, P, P, P]
         L.oracle_filtered_row.restype = ctypes.c_int
         L.oracle_verify_filtered.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int64, ctypes.c_double, P, P, P,
                                              ctypes.c_int, ctypes.c_double, P, P, P, ctypes.c_uint64,
                                              ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P,
-                                             P, P, ctypes.c_int]
+                                             P, P, P, ctypes.c_int]
         L.oracle_verify_filtered.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -147,7 +148,7 @@ def filtered_row(logits: np.ndarray, T: float, top_k: int = 0, top_p: float = 1.
     x = np.ascontiguousarray(logits)
     m = np.zeros(1, dtype=np.float64)
     rc = lib().oracle_filtered_row(_ptr(x), _dtype_code(x), x.shape[-1], float(T), int(top_k),
-                                   float(top_p), float(min_p), _ptr(p), _ptr(m))
+                                   float(top_p), float(min_p), _ptr(p), _ptr(m), None)
     if rc != 0:
         raise MemoryError("oracle_filtered_row")
     return p, float(m[0])
@@ -168,7 +169,8 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
     on the sampler filters (``oracle_verify_filtered``).
     Returns a dict of numpy arrays: accepted_len, tokens, alpha, flags,
     row_stats [B, 2k+1, 2] (max, lse of L/T), margin (all used draws),
-    margin_pick (the residual / bonus pick alone), degenerate.
+    margin_pick (the residual / bonus pick alone), margin_filter (the sampler
+    filters' decisions alone), degenerate.
     """
     Lt = np.ascontiguousarray(Lt)
     Ld = np.ascontiguousarray(Ld)
@@ -191,15 +193,12 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
         row_stats=np.zeros((B, 2 * k + 1, 2), dtype=np.float64),
         margin=np.zeros(B, dtype=np.float64),
         margin_pick=np.zeros(B, dtype=np.float64),
+        margin_filter=np.full(B, np.inf, dtype=np.float64),
         degenerate=np.zeros(B, dtype=np.int32),
     )
     sched = None if tau_sched is None else np.ascontiguousarray(tau_sched, dtype=np.float64).ravel()
     n_sched = 0 if sched is None else int(sched.shape[0])
-    fk = fp = fm = None
-    if filters is not None:
-        fk = np.array([int(filters[0][0]), int(filters[1][0])], dtype=np.int32)
-        fp = np.array([float(filters[0][1]), float(filters[1][1])], dtype=np.float64)
-        fm = np.array([float(filters[0][2]), float(filters[1][2])], dtype=np.float64)
+    fk, fp, fm = _filter_arrays(filters)
     rc = lib().oracle_verify_filtered(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D),
                                       B, k, V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
                                       float(min_cum), _ptr(fk), _ptr(fp), _ptr(fm), int(seed),
@@ -207,14 +206,22 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
                                       _ptr(out["accepted_len"]), _ptr(out["tokens"]),
                                       _ptr(out["alpha"]), _ptr(out["flags"]), _ptr(out["row_stats"]),
                                       _ptr(out["margin"]), _ptr(out["margin_pick"]),
-                                      _ptr(out["degenerate"]), int(nthreads))
+                                      _ptr(out["margin_filter"]), _ptr(out["degenerate"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out
 
 
+def _filter_arrays(filters):
+    if filters is None:
+        return None, None, None
+    return (np.array([int(filters[0][0]), int(filters[1][0])], dtype=np.int32),
+            np.array([float(filters[0][1]), float(filters[1][1])], dtype=np.float64),
+            np.array([float(filters[0][2]), float(filters[1][2])], dtype=np.float64))
+
+
 def diagnostics(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, tau_sched=None,
-                min_cum: float = 0.0, nthreads: int = 1):
+                min_cum: float = 0.0, nthreads: int = 1, filters=None):
     """Closed-form acceptance of every draft position (``oracle_diagnostics``).
 
     Returns a dict of numpy arrays: min_sum [B, k] (sum min(p, mu)), pq_sum
@@ -234,9 +241,11 @@ def diagnostics(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, t
     n_sched = 0 if sched is None else int(sched.shape[0])
     out = dict(min_sum=np.zeros((B, k)), pq_sum=np.zeros((B, k)), argmax_q=np.zeros((B, k)),
                margin=np.zeros(B))
+    fk, fp, fm = _filter_arrays(filters)
     rc = lib().oracle_diagnostics(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), B, k,
                                   V, float(T), _ptr(gate), _ptr(tau), _ptr(sched), n_sched,
-                                  float(min_cum), _ptr(out["min_sum"]), _ptr(out["pq_sum"]),
+                                  float(min_cum), _ptr(fk), _ptr(fp), _ptr(fm),
+                                  _ptr(out["min_sum"]), _ptr(out["pq_sum"]),
                                   _ptr(out["argmax_q"]), _ptr(out["margin"]), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_diagnostics rejected its arguments")

@@ -143,12 +143,13 @@ static int ranked_cmp(const void* a, const void* b) {
  * keeps p >= min_p * max p.  *margin: the smallest relative distance of a
  * top-p or min-p decision to its boundary (top-k compares logits exactly). */
 int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top_k, double top_p,
-                        double min_p, double* p, double* margin) {
+                        double min_p, double* p, double* margin, double* kept) {
   double marg = INFINITY;
   const int use_k = top_k >= 1 && (int64_t)top_k < V;
   const int use_p = top_p > 0.0 && top_p < 1.0;
   const int use_m = min_p > 0.0;
   if (margin) *margin = marg;
+  if (kept) *kept = 1.0;
   if (T == 0.0 || !(use_k || use_p || use_m)) return 0;  /* greedy rows are one-hot already */
   ranked_t* rk = (ranked_t*)malloc((size_t)V * sizeof(ranked_t));
   unsigned char* keep = (unsigned char*)malloc((size_t)V);
@@ -164,6 +165,7 @@ int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top
   qsort(rk, (size_t)V, sizeof(ranked_t), ranked_cmp);
   if (top_k == 1) {
     /* greedy: one-hot at the first largest logit */
+    if (kept) *kept = p[rk[0].v];
     for (int64_t v = 0; v < V; ++v) p[v] = 0.0;
     p[rk[0].v] = 1.0;
     free(rk); free(keep);
@@ -211,6 +213,7 @@ int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top
   for (int64_t v = 0; v < V; ++v) p[v] = keep[v] ? p[v] / S : 0.0;
   free(rk); free(keep);
   if (margin) *margin = marg;
+  if (kept) *kept = S;
   return 0;
 }
 
@@ -269,6 +272,7 @@ typedef struct {
   int rule;
   int32_t* accepted_len; int32_t* tokens; double* alpha; int8_t* flags;
   double* row_stats; double* margin; double* margin_pick; int32_t* degenerate;
+  double* margin_filter;  /* the part of margin that comes from the sampler filters */
   const double* tau_sched; int n_sched; /* per-step thresholds (NULL: tau[b] at every step) */
   double min_cum;                       /* cumulative floor (0: no cumulative gate) */
   /* sampler filters of the target [0] and draft [1] rows (NULL: none) */
@@ -364,10 +368,12 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     const char* row = (const char*)J->Lt + ((int64_t)b * (k + 1) + j) * V * esz_t;
     double mx, lse, fm = INFINITY;
     invalid |= oracle_softmax_row(row, J->tdt, V, J->T, S->P + (int64_t)j * V, &mx, &lse);
+    double kept = 1.0;
     if (J->top_k && !invalid)
       invalid |= oracle_filtered_row(row, J->tdt, V, J->T, J->top_k[0], J->top_p[0], J->min_p[0],
-                                     S->P + (int64_t)j * V, &fm);
+                                     S->P + (int64_t)j * V, &fm, &kept);
     fmarg = fmin(fmarg, fm);
+    lse += log(kept);  /* the statistics of the filtered row (its max is always kept) */
     if (J->row_stats) {
       J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 0] = mx;
       J->row_stats[((int64_t)b * (2 * k + 1) + j) * 2 + 1] = lse;
@@ -377,10 +383,12 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
     const char* row = (const char*)J->Ld + ((int64_t)b * k + j) * V * esz_d;
     double mx, lse, fm = INFINITY;
     invalid |= oracle_softmax_row(row, J->ddt, V, J->T, S->Q + (int64_t)j * V, &mx, &lse);
+    double kept = 1.0;
     if (J->top_k && !invalid)
       invalid |= oracle_filtered_row(row, J->ddt, V, J->T, J->top_k[1], J->top_p[1], J->min_p[1],
-                                     S->Q + (int64_t)j * V, &fm);
+                                     S->Q + (int64_t)j * V, &fm, &kept);
     fmarg = fmin(fmarg, fm);
+    lse += log(kept);
     if (J->row_stats) {
       J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 0] = mx;
       J->row_stats[((int64_t)b * (2 * k + 1) + k + 1 + j) * 2 + 1] = lse;
@@ -391,6 +399,7 @@ static void verify_one(const job_t* J, int b, scratch_t* S) {
 
   double marg = fmarg;         /* accept tests, gates of tested positions, filters */
   double marg_pick = INFINITY; /* the residual / bonus pick */
+  if (J->margin_filter) J->margin_filter[b] = fmarg;
   if (J->degenerate) J->degenerate[b] = 0;
   if (invalid) {
     J->accepted_len[b] = -1;
@@ -585,15 +594,27 @@ static void diagnose_one(const job_t* J, int b, scratch_t* S) {
   const int esz_t = J->tdt == ORACLE_BF16 ? 2 : 4, esz_d = J->ddt == ORACLE_BF16 ? 2 : 4;
   int bad_t[ORACLE_MAX_K], bad_d[ORACLE_MAX_K];
   double mx, lse;
+  double marg = INFINITY;
   for (int j = 0; j < k; ++j) {
     const char* rt = (const char*)J->Lt + ((int64_t)b * (k + 1) + j) * V * esz_t;
     const char* rd = (const char*)J->Ld + ((int64_t)b * k + j) * V * esz_d;
     bad_t[j] = oracle_softmax_row(rt, J->tdt, V, J->T, S->P + (int64_t)j * V, &mx, &lse);
     bad_d[j] = oracle_softmax_row(rd, J->ddt, V, J->T, S->Q + (int64_t)j * V, &mx, &lse);
+    if (J->top_k) {  /* the sampler filters, as in verify_one */
+      double fm = INFINITY;
+      if (!bad_t[j])
+        bad_t[j] = oracle_filtered_row(rt, J->tdt, V, J->T, J->top_k[0], J->top_p[0], J->min_p[0],
+                                       S->P + (int64_t)j * V, &fm, NULL);
+      marg = fmin(marg, fm);
+      fm = INFINITY;
+      if (!bad_d[j])
+        bad_d[j] = oracle_filtered_row(rd, J->ddt, V, J->T, J->top_k[1], J->top_p[1], J->min_p[1],
+                                       S->Q + (int64_t)j * V, &fm, NULL);
+      marg = fmin(marg, fm);
+    }
   }
   const int cum = gated && J->min_cum > 0.0;
   const int bad_tau = gated && !J->tau_sched && !(J->tau[b] > 0.0 && J->tau[b] <= 1.0);
-  double marg = INFINITY;
   double cprev = 1.0;   /* prod_{i<j} q_i(D_i) */
   int prefix_bad = 0;   /* an earlier draft row or drafted token the product needs is invalid */
   for (int j = 0; j < k; ++j) {
@@ -678,7 +699,7 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
                          int32_t* degenerate, int nthreads) {
   return oracle_verify_filtered(Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, tau_sched, n_sched, min_cum,
                                 NULL, NULL, NULL, seed, seq_offset, u0, u1, rule, accepted_len, tokens,
-                                alpha, flags, row_stats, margin, margin_pick, degenerate, nthreads);
+                                alpha, flags, row_stats, margin, margin_pick, NULL, degenerate, nthreads);
 }
 
 int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
@@ -690,7 +711,7 @@ int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, con
                            const double* u0, const double* u1, int rule,
                            int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                            double* row_stats, double* margin, double* margin_pick,
-                           int32_t* degenerate, int nthreads) {
+                           double* margin_filter, int32_t* degenerate, int nthreads) {
   if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
   if ((top_k != NULL) != (top_p != NULL) || (top_k != NULL) != (min_p != NULL)) return 1;
   for (int i = 0; top_k && i < 2; ++i)
@@ -704,7 +725,7 @@ int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, con
   if (rule < ORACLE_RULE_MU || rule > ORACLE_RULE_MU_STEP_ONLY) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, seed, seq_offset, u0, u1, rule,
              accepted_len, tokens, alpha, flags, row_stats, margin, margin_pick, degenerate,
-             tau_sched, n_sched, min_cum, top_k, top_p, min_p, 0, NULL, NULL, NULL};
+             margin_filter, tau_sched, n_sched, min_cum, top_k, top_p, min_p, 0, NULL, NULL, NULL};
   return run_jobs(&J, nthreads);
 }
 
@@ -712,6 +733,7 @@ int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const i
                        int B, int k, int64_t V, double T,
                        const uint8_t* gate, const double* tau,
                        const double* tau_sched, int n_sched, double min_cum,
+                       const int* top_k, const double* top_p, const double* min_p,
                        double* min_sum, double* pq_sum, double* argmax_q, double* margin,
                        int nthreads) {
   if (B < 0 || k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
@@ -721,8 +743,8 @@ int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const i
   if (!Lt || !Ld || !D || !gate || !tau) return 1;
   if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
   job_t J = {Lt, tdt, Ld, ddt, D, B, k, V, T, gate, tau, 0, 0, NULL, NULL, ORACLE_RULE_MU,
-             NULL, NULL, NULL, NULL, NULL, margin, NULL, NULL,
-             tau_sched, n_sched, min_cum, NULL, NULL, NULL, 1, min_sum, pq_sum, argmax_q};
+             NULL, NULL, NULL, NULL, NULL, margin, NULL, NULL, NULL,
+             tau_sched, n_sched, min_cum, top_k, top_p, min_p, 1, min_sum, pq_sum, argmax_q};
   return run_jobs(&J, nthreads);
 }
 

@@ -156,17 +156,20 @@ int oracle_verify_policy(const void* Lt, int tdt, const void* Ld, int ddt, const
  * renormalised filtered distribution on exit; T = 0 rows are left one-hot.
  * *margin (may be NULL): the smallest distance of a top-p decision (in units
  * of the top-k mass) or a min-p decision (in units of p / max p) to its
- * boundary.  Returns 0, or 1 when memory runs out.
+ * boundary.  *kept (may be NULL): the unfiltered probability mass of the
+ * survivors.  Returns 0, or 1 when memory runs out.
  */
 int oracle_filtered_row(const void* logits, int dt, int64_t V, double T, int top_k, double top_p,
-                        double min_p, double* p, double* margin);
+                        double min_p, double* p, double* margin, double* kept);
 
 /*
  * oracle_verify_policy with sampler filters: top_k[2], top_p[2], min_p[2]
  * (index 0 the target rows, 1 the draft rows; all three NULL for none) turn
  * every p_j and q_j into its filtered distribution (oracle_filtered_row)
- * before the rule runs; row_stats stay those of the unfiltered L/T; margin
- * also covers the filter decisions of every row of the sequence.
+ * before the rule runs; row_stats then describe the filtered rows (max and
+ * log-sum-exp of L/T over the survivors); margin also covers the filter
+ * decisions of every row of the sequence, and margin_filter[B] (may be NULL)
+ * reports that part alone.
  */
 int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
                            int B, int k, int64_t V, double T,
@@ -177,7 +180,7 @@ int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, con
                            const double* u0, const double* u1, int rule,
                            int32_t* accepted_len, int32_t* tokens, double* alpha, int8_t* flags,
                            double* row_stats, double* margin, double* margin_pick,
-                           int32_t* degenerate, int nthreads);
+                           double* margin_filter, int32_t* degenerate, int nthreads);
 
 /*
  * Closed-form acceptance of every draft position [M] "The acceptance ceiling":
@@ -194,12 +197,15 @@ int oracle_verify_filtered(const void* Lt, int tdt, const void* Ld, int ddt, con
  * rows p_j or q_j are invalid (NaN or +inf logit, all -inf), or -- with a
  * cumulative floor -- behind an invalid earlier draft row or drafted token,
  * gets NaN; so does every position of a gated sequence with a threshold
- * outside (0, 1] and no schedule.  Returns 1 on bad args.
+ * outside (0, 1] and no schedule.  top_k / top_p / min_p ([2] each, or NULL)
+ * apply the sampler filters of oracle_verify_filtered first; margin then also
+ * covers their decisions.  Returns 1 on bad args.
  */
 int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
                        int B, int k, int64_t V, double T,
                        const uint8_t* gate, const double* tau,
                        const double* tau_sched, int n_sched, double min_cum,
+                       const int* top_k, const double* top_p, const double* min_p,
                        double* min_sum, double* pq_sum, double* argmax_q, double* margin,
                        int nthreads);
 

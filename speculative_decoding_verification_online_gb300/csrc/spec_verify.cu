@@ -13,6 +13,7 @@
 #include "spec_verify.h"
 #include "verify_kernel.cuh"
 #include "diag_kernel.cuh"
+#include "filter_kernel.cuh"
 
 struct spec_verify_s {
   int device = 0;
@@ -35,6 +36,11 @@ struct spec_verify_s {
   int n_sched = 0;
   float sched[SV_MAX_K] = {};
   float min_cum = 0.f;
+  // sampler filters (spec_verify_set_filters) and their buffers, allocated on
+  // the first filtered call: masked copies of the logits, per-row thresholds
+  sv::Filter filt[2] = {{0, 1.f, 0.f}, {0, 1.f, 0.f}};
+  void* fbuf = nullptr;
+  size_t fbuf_bytes = 0;
 };
 
 namespace {
@@ -83,6 +89,9 @@ cudaError_t configure(int* blocks_per_sm) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sv::pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sv::select_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(sv::SelShared)));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
                                                        sv::stream_kernel<TT, TD, sv::kModeSample>,
@@ -214,6 +223,65 @@ sv_status launch_diag(spec_verify_t h, const sv::Params& P, int blocks_per_sm, f
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
+bool filter_on(const sv::Filter& f) { return f.top_k != 0 || f.top_p < 1.f || f.min_p > 0.f; }
+
+// the filter prefix of a call: statistics pass, per-row thresholds, masked
+// copies; on return P reads the masked copies
+template <typename TT, typename TD>
+sv_status launch_filters(spec_verify_t h, sv::Params& P, int blocks_per_sm, cudaStream_t st) {
+  const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
+  const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
+  const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
+  const size_t o_t = 0, o_d = align_up(bt, 256), o_key = align_up(o_d + bd, 256);
+  const size_t o_first = align_up(o_key + rows_all * sizeof(unsigned), 256);
+  const size_t need = align_up(o_first + rows_all * sizeof(int), 256);
+  if (!h->fbuf) {
+    if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
+      h->fbuf = nullptr;
+      return SV_ENOMEM;
+    }
+    h->fbuf_bytes = need;
+  }
+  char* base = static_cast<char*>(h->fbuf);
+  sv::FilterParams F;
+  F.f[0] = h->filt[0];
+  F.f[1] = h->filt[1];
+  F.key = reinterpret_cast<unsigned*>(base + o_key);
+  F.first = reinterpret_cast<int*>(base + o_first);
+  F.Lt_m = base + o_t;
+  F.Ld_m = base + o_d;
+  sv_status rs = launch_stream<TT, TD, sv::kModeStats>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
+  const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
+  if (launch_dependent(sv::select_kernel<TT, TD>, nrows, sv::kSelThreads, sizeof(sv::SelShared), st, P, F) !=
+      cudaSuccess)
+    return SV_ECUDA;
+  const long long groups = (static_cast<long long>(P.V) + 7) / 8;
+  const long long work = static_cast<long long>(P.B) * P.rows * groups;
+  long long grid = (work + 255) / 256;
+  if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
+  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), 256u, 0, st, P, F, groups) !=
+      cudaSuccess)
+    return SV_ECUDA;
+  P.Lt = F.Lt_m;
+  P.Ld = F.Ld_m;
+  P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
+  P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+template <int G>
+sv_status launch_mode_filtered(spec_verify_t h, sv::Params& P, int bps, bool dense_likely, bool tb, bool db,
+                               cudaStream_t st) {
+  sv_status rs;
+  if (tb && db) rs = launch_filters<uint16_t, uint16_t>(h, P, bps, st);
+  else if (tb && !db) rs = launch_filters<uint16_t, float>(h, P, bps, st);
+  else if (!tb && db) rs = launch_filters<float, uint16_t>(h, P, bps, st);
+  else rs = launch_filters<float, float>(h, P, bps, st);
+  if (rs != SV_OK) return rs;
+  return launch_mode<G>(h, P, bps, dense_likely, tb, db, st);
+}
+
 struct DeviceGuard {
   int prev = -1;
   bool ok = true;
@@ -246,6 +314,8 @@ const char* spec_verify_status_string(sv_status s) {
 }
 
 int spec_verify_launches_per_run(void) { return 2; }
+
+int spec_verify_launches_per_filtered_run(void) { return 5; }
 
 sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after) {
   if (!h || (ev_before == nullptr) != (ev_after == nullptr)) return SV_EINVAL;
@@ -426,6 +496,12 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
                         (P.has_sched || (!threshold_per_seq && fast_floor(threshold)));
   for (int j = 0; P.has_sched && j < k; ++j) all_fast_gated = all_fast_gated && fast_floor(P.tau_step[j]);
   const bool dense_likely = !all_fast_gated && !P.greedy;
+  // sampler filters (temperature > 0: a greedy call is one-hot already)
+  if (!P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]))) {
+    if (P.has_sched || P.min_cum > 0.f)
+      return launch_mode_filtered<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
+    return launch_mode_filtered<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
+  }
   if (P.greedy) return launch_mode<sv::kModeGreedy>(h, P, bps, false, tb, db, st);
   if (P.has_sched || P.min_cum > 0.f) return launch_mode<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
   return launch_mode<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
@@ -450,6 +526,14 @@ sv_status spec_verify_diagnostics(spec_verify_t h, const void* target_logits, sv
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
   const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
+  if (!P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]))) {
+    sv_status rs;
+    if (tb && db) rs = launch_filters<uint16_t, uint16_t>(h, P, bps, st);
+    else if (tb && !db) rs = launch_filters<uint16_t, float>(h, P, bps, st);
+    else if (!tb && db) rs = launch_filters<float, uint16_t>(h, P, bps, st);
+    else rs = launch_filters<float, float>(h, P, bps, st);
+    if (rs != SV_OK) return rs;
+  }
   if (P.greedy) {
     if (tb && db) return launch_diag<uint16_t, uint16_t, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
     if (tb && !db) return launch_diag<uint16_t, float, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
@@ -553,6 +637,17 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
   return SV_OK;
 }
 
+sv_status spec_verify_set_filters(spec_verify_t h, int top_k_t, float top_p_t, float min_p_t, int top_k_d,
+                                  float top_p_d, float min_p_d) {
+  if (!h) return SV_EINVAL;
+  const int kk[2] = {top_k_t, top_k_d};
+  const float pp[2] = {top_p_t, top_p_d}, mm[2] = {min_p_t, min_p_d};
+  for (int i = 0; i < 2; ++i)
+    if (kk[i] < 0 || !(pp[i] > 0.f && pp[i] <= 1.f) || !(mm[i] >= 0.f && mm[i] <= 1.f)) return SV_EINVAL;
+  for (int i = 0; i < 2; ++i) h->filt[i] = sv::Filter{kk[i], pp[i], mm[i]};
+  return SV_OK;
+}
+
 sv_status spec_verify_free(spec_verify_t h) {
   if (!h) return SV_OK;
   sv_status rc = SV_OK;
@@ -561,6 +656,7 @@ sv_status spec_verify_free(spec_verify_t h) {
     if (!g.ok || cudaDeviceSynchronize() != cudaSuccess) rc = SV_ECUDA;
     if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = SV_ECUDA;
     if (h->stage && cudaFree(h->stage) != cudaSuccess) rc = SV_ECUDA;
+    if (h->fbuf && cudaFree(h->fbuf) != cudaSuccess) rc = SV_ECUDA;
   }
   delete h;
   return rc;

@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     L.spec_verify_set_gate_policy.restype = I
     L.spec_verify_diagnostics.argtypes = [P, P, I, P, I, P, I, F, I, F, P, P, P, P, P, P]
     L.spec_verify_diagnostics.restype = I
+    L.spec_verify_set_filters.argtypes = [P, I, F, F, I, F, F]
+    L.spec_verify_set_filters.restype = I
+    L.spec_verify_launches_per_filtered_run.argtypes = []
+    L.spec_verify_launches_per_filtered_run.restype = I
     _lib = L
     return L
 
@@ -125,6 +129,15 @@ def spec_verify_diagnostics(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode, t
     return load().spec_verify_diagnostics(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode,
                                           threshold, gate_per_seq, threshold_per_seq, min_sum,
                                           pq_sum, argmax_q, stream)
+
+
+def spec_verify_set_filters(h, top_k_t, top_p_t, min_p_t, top_k_d, top_p_d, min_p_d) -> int:
+    """Raw call: sampler filters of the target and draft rows."""
+    return load().spec_verify_set_filters(h, top_k_t, top_p_t, min_p_t, top_k_d, top_p_d, min_p_d)
+
+
+def spec_verify_launches_per_filtered_run() -> int:
+    return load().spec_verify_launches_per_filtered_run()
 
 
 def spec_verify_launches_per_run() -> int:
@@ -198,6 +211,14 @@ class SpecVerifier:
         rc = spec_verify_mark_next(self.handle, ev_before.cuda_event, ev_after.cuda_event)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_mark_next")
+
+    def set_filters(self, target=(0, 1.0, 0.0), draft=(0, 1.0, 0.0)):
+        """Sampler filters (top_k, top_p, min_p) of the target rows and of the
+        draft rows for later calls; (0, 1.0, 0.0) is off."""
+        rc = spec_verify_set_filters(self.handle, int(target[0]), float(target[1]), float(target[2]),
+                                     int(draft[0]), float(draft[1]), float(draft[2]))
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_set_filters")
 
     def set_gate_policy(self, schedule=None, min_cum: float = 0.0):
         """Per-step thresholds (a sequence of floats in [0, 1], the last one

@@ -1,0 +1,160 @@
+"""GPU parity of the sampler filters (mlxcel PR #992, "What changed": top-k,
+top-p and min-p before the softmax of p and q; top_k = 1 greedy) against the
+oracle, through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import oracle as O
+from tests.gpu_helpers import compare, oracle_for, peaked_workload
+
+pytestmark = pytest.mark.gpu
+
+OFF = (0, 1.0, 0.0)
+FILTERS = {
+    "topk_target": ((50, 1.0, 0.0), OFF),
+    "topp_both": ((0, 0.9, 0.0), (0, 0.9, 0.0)),
+    "chain": ((40, 0.8, 0.05), (20, 0.95, 0.01)),
+    "greedy_target": ((1, 1.0, 0.0), OFF),
+    "minp_both": ((0, 1.0, 0.2), (0, 1.0, 0.2)),
+    "topk_draft": (OFF, (3, 1.0, 0.0)),
+}
+
+
+@pytest.fixture(scope="module")
+def sv():
+    import speculative_decoding_verification_online_gb300 as pkg
+    from speculative_decoding_verification_online_gb300 import build as B
+    B.build()
+    pkg.load()
+    return pkg
+
+
+def _run(sv, ver, w, **kw):
+    out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=0.5, gate_per_seq=w.gate,
+                  threshold_per_seq=w.tau, seed=w.philox_seed, **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def _filtered_drafts(w, fd):
+    """Drafted tokens drawn from the filtered q (a drafter that samples with its own filters)."""
+    if fd == OFF:
+        return w
+    Ld = workloads.to_numpy_logits(w.Ld)
+    rng = np.random.default_rng(w.philox_seed)
+    D = np.zeros((w.B, w.k), dtype=np.int32)
+    for b in range(w.B):
+        for j in range(w.k):
+            q, _ = O.filtered_row(Ld[b, j], w.T, *fd)
+            D[b, j] = rng.choice(w.V, p=q / q.sum())
+    w.D = torch.as_tensor(D, device=w.D.device)
+    return w
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 20000), ("f32", 4099)])
+@pytest.mark.parametrize("name", sorted(FILTERS))
+def test_filter_parity(sv, dtype, V, name):
+    ft, fd = FILTERS[name]
+    B, k = 40, 4
+    gate = (np.arange(B) % 2).astype(np.uint8)
+    seed = 300 + 7 * sorted(FILTERS).index(name) + (dtype == "f32")
+    w = _filtered_drafts(peaked_workload(B, k, V, dtype, seed=seed, gate=gate, tau=0.3, T=0.9), fd)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(ft, fd)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w, filters=(ft, fd))
+    st = compare(w, out, ref, what=f"filters {name} {dtype} V={V}")
+    ok = ref["margin"] >= 1e-6
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
+    assert st["compared"] >= B // 2
+    ver.close()
+
+
+def test_filtered_target_support_is_never_violated_on_the_gpu(sv):
+    # a top_k = 2 target against an unfiltered drafter: every emitted token is
+    # in the target row's two-token support (zero tolerance)
+    B, k, V = 256, 4, 3000
+    w = peaked_workload(B, k, V, "bf16", seed=41, gate=0, T=1.0)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters((2, 1.0, 0.0), OFF)
+    out = _run(sv, ver, w)
+    top2 = torch.topk(w.Lt.float(), 2, dim=2).indices.cpu().numpy()
+    al = out["accepted_len"].cpu().numpy()
+    tok = out["tokens"].cpu().numpy()
+    for b in range(B):
+        for j in range(al[b] + 1):
+            assert tok[b, j] in top2[b, j], (b, j)
+    ver.close()
+
+
+def test_top_k_one_on_both_sides_is_the_greedy_call(sv):
+    B, k, V = 32, 4, 5000
+    w = peaked_workload(B, k, V, "bf16", seed=9, gate=(np.arange(B) % 2), T=0.8)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters((1, 1.0, 0.0), (1, 1.0, 0.0))
+    f = _run(sv, ver, w)
+    ver.set_filters(OFF, OFF)
+    g = ver.run(w.Lt, w.Ld, w.D, 0.0, gate_mode=sv.SV_GATED_MU, threshold=0.5, gate_per_seq=w.gate,
+                threshold_per_seq=w.tau, seed=w.philox_seed)
+    torch.cuda.synchronize()
+    for key in ("accepted_len", "tokens", "flags"):
+        assert torch.equal(f[key], g[key]), key
+    ver.close()
+
+
+def test_filters_off_again_match_a_fresh_handle(sv):
+    B, k, V = 24, 3, 6000
+    w = peaked_workload(B, k, V, "f32", seed=13, gate=1, tau=0.4)
+    a = sv.SpecVerifier(B, k, V, device=0)
+    a.set_filters((10, 0.9, 0.1), (5, 1.0, 0.0))
+    _run(sv, a, w)
+    a.set_filters(OFF, OFF)
+    x = _run(sv, a, w)
+    b = sv.SpecVerifier(B, k, V, device=0)
+    y = _run(sv, b, w)
+    for key in ("accepted_len", "tokens", "accept_prob", "flags"):
+        assert torch.equal(x[key], y[key]), key
+    for bad in (((-1, 1.0, 0.0), OFF), ((0, 0.0, 0.0), OFF), ((0, 1.5, 0.0), OFF), (OFF, (0, 1.0, -0.1)),
+                (OFF, (0, 1.0, 1.5)), ((0, float("nan"), 0.0), OFF)):
+        with pytest.raises(sv.SpecVerifyError):
+            a.set_filters(*bad)
+    a.close()
+    b.close()
+
+
+def test_filter_full_size_128k(sv):
+    w = workloads.make("b64_v128256_zipf_gated", seed=1234, device="cuda")
+    ver = sv.SpecVerifier(w.B, w.k, w.V, device=0)
+    # top-p inside top-k (the usual serving setting): over a whole Zipf row
+    # top-p alone sits within 1e-6 of some tail token's boundary in every row
+    for filt in (((50, 0.9, 0.0), (40, 0.95, 0.0)), ((0, 1.0, 0.01), (64, 1.0, 0.0))):
+        ver.set_filters(*filt)
+        out = _run(sv, ver, w)
+        st = compare(w, out, oracle_for(w, nthreads=16, filters=filt), what=f"128k filtered {filt}")
+        assert st["compared"] >= w.B // 2
+    ver.close()
+
+
+def test_filtered_diagnostics(sv):
+    B, k, V = 24, 4, 8000
+    w = peaked_workload(B, k, V, "bf16", seed=17, gate=(np.arange(B) % 2), tau=0.3)
+    filt = ((30, 0.9, 0.0), (0, 1.0, 0.05))
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = ver.diagnostics(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=0.5,
+                          gate_per_seq=w.gate, threshold_per_seq=w.tau)
+    torch.cuda.synchronize()
+    ref = O.diagnostics(workloads.to_numpy_logits(w.Lt), workloads.to_numpy_logits(w.Ld), w.D.cpu().numpy(),
+                        w.T, w.gate.cpu().numpy(), w.tau.cpu().numpy().astype(np.float64), filters=filt,
+                        nthreads=16)
+    keep = ref["margin"] >= 1e-6
+    for key in ("min_sum", "pq_sum", "argmax_q"):
+        np.testing.assert_allclose(out[key].cpu().numpy()[keep], ref[key][keep], rtol=2e-5, atol=2e-6,
+                                   err_msg=key)
+    assert keep.sum() >= B // 2
+    ver.close()

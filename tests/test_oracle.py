@@ -794,3 +794,27 @@ def test_filter_margin_reports_top_p_and_min_p_boundaries():
     with pytest.raises(ValueError):
         O.verify(L[None, None].repeat(2, 1), L[None, None], np.zeros((1, 1)), 1.0, 0, 0.5,
                  filters=((0, 0.0, 0.0), (0, 1.0, 0.0)))
+
+
+def test_filtered_row_statistics_and_diagnostics():
+    # row_stats of a filtered row: max and log-sum-exp of L/T over the
+    # survivors (scipy's logsumexp); the diagnostics' sum min(p, q) is the
+    # mean acceptance probability over drafts drawn from the filtered q
+    rng = np.random.default_rng(21)
+    V, k = 7, 2
+    Lt, Ld = _random_case(rng, V, k, scale=1.5)
+    filt = ((3, 0.9, 0.0), (0, 0.8, 0.05))
+    out = O.verify(Lt[None], Ld[None], np.zeros((1, k), np.int32), 0.8, 0, 0.5, filters=filt)
+    for j in range(k + 1):
+        p, _ = O.filtered_row(Lt[j], 0.8, *filt[0])
+        kept = p > 0
+        assert abs(out["row_stats"][0, j, 1] - logsumexp(Lt[j][kept].astype(np.float64) / 0.8)) < 1e-12
+    P, Q = distributions(Lt, Ld, 0.8, filt)
+    prefix = np.array([int(np.argmax(Q[0])), 0])
+    d = O.diagnostics(Lt[None], Ld[None], prefix[None], 0.8, 0, 0.5, filters=filt)
+    for j in range(k):
+        D = np.broadcast_to(prefix, (V, k)).copy()
+        D[:, j] = np.arange(V)
+        a = O.verify(np.broadcast_to(Lt, (V, k + 1, V)), np.broadcast_to(Ld, (V, k, V)), D, 0.8, 0, 0.5,
+                     filters=filt)["alpha"][:, j]
+        assert abs((Q[j] * a).sum() - d["min_sum"][0, j]) < 1e-12
