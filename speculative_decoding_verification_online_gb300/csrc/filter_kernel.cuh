@@ -37,6 +37,7 @@ struct FilterParams {
 };
 
 constexpr int kSelThreads = 512;
+constexpr int kListCap = 4096;  // logits gathered for an in-shared-memory selection
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr float kMassScalef = 1099511627776.0f;  // 2^40: masses as integers
 
@@ -66,34 +67,61 @@ struct SelShared {
   unsigned long long wsum[kSelWarps];
   int wfirst[kSelWarps];
   unsigned long long Sk;           // mass of the top-k survivors
+  unsigned long long h0mass[256];  // the level-0 mass histogram (all keys), kept for top-p
+  unsigned lkey[kListCap];         // gathered logits' keys
+  unsigned long long lmass[kListCap];
+  int ln;
   unsigned kmax;                   // the row's largest key
   float Mc;
   int bad;
 };
 
 // one pass over the row: per-digit counts and fixed-point masses of the keys
-// that share `prefix` on the bits above `shift + 8`
+// that share `prefix` on the bits above `shift + 8`.  A thread reads eight
+// consecutive entries at a time and keeps a running (digit, count, mass) that
+// it adds to its warp's histogram only when the digit changes: neighbouring
+// logits mostly share their leading digits, so the shared-memory atomics stay
+// few.
 template <typename T>
-__device__ void sel_histogram(const T* row, int V, float c, float Mc, unsigned prefix, int shift,
+__device__ void sel_histogram(const T* row, int V, bool vec, float c, float Mc, unsigned prefix, int shift,
                               bool masses, SelShared& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   for (int i = tid; i < kSelWarps * 256; i += kSelThreads) {
     (&sh.cnt[0][0])[i] = 0u;
     (&sh.mass[0][0])[i] = 0ull;
   }
   __syncthreads();
   const unsigned hi_mask = shift + 8 >= 32 ? 0u : (0xffffffffu << (shift + 8));
-#pragma unroll 4
-  for (int v = tid; v < V; v += kSelThreads) {
-    const float x = row_at<T>(row, v);
-    const unsigned kx = key_of(x);
-    if ((kx & hi_mask) != (prefix & hi_mask)) continue;
-    const int d = static_cast<int>((kx >> shift) & 255u);
-    atomicAdd(&sh.cnt[warp][d], 1u);
-    if (masses) {
-      const float w = exp2f(fmaf(x, c, -Mc));
-      atomicAdd(&sh.mass[warp][d], __float2ull_rn(w * kMassScalef));  // exact power-of-two scaling
+  const unsigned want = prefix & hi_mask;
+  int cd = -1;
+  unsigned cc = 0u;
+  unsigned long long cm = 0ull;
+#pragma unroll 1
+  for (int v0 = tid * 8; v0 < V; v0 += kSelThreads * 8) {
+    float x[8];
+    load8<T>(row, v0, V, vec, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const unsigned kx = key_of(x[e]);
+      if (v0 + e >= V || (kx & hi_mask) != want) continue;
+      const int d = static_cast<int>((kx >> shift) & 255u);
+      const unsigned long long wq = masses ? __float2ull_rn(ex2_approx(fmaf(x[e], c, -Mc)) * kMassScalef) : 0ull;
+      if (d != cd) {
+        if (cd >= 0) {
+          atomicAdd(&sh.cnt[warp][cd], cc);
+          if (masses) atomicAdd(&sh.mass[warp][cd], cm);
+        }
+        cd = d;
+        cc = 0u;
+        cm = 0ull;
+      }
+      ++cc;
+      cm += wq;
     }
+  }
+  if (cd >= 0) {
+    atomicAdd(&sh.cnt[warp][cd], cc);
+    if (masses) atomicAdd(&sh.mass[warp][cd], cm);
   }
   __syncthreads();
   for (int d = tid; d < 256; d += kSelThreads) {
@@ -105,25 +133,85 @@ __device__ void sel_histogram(const T* row, int V, float c, float Mc, unsigned p
     sh.hcnt[d] = a;
     sh.hmass[d] = m;
   }
-  (void)lane;
   __syncthreads();
 }
 
-// thread 0: the largest digit d with (sum of the level histogram over digits
-// >= d) + carry >= target; records it and the sum strictly above it
+// warp 0: the largest digit d with (sum of the level histogram over digits
+// >= d) + carry >= target; records it and the sum strictly above it.  The
+// sums are integers, so comparing them with ceil(target) is exact; lane l
+// holds digits 255 - 8l - i, i = 0..7, and a scan over the lanes gives each
+// digit's sum from the top.
 __device__ __forceinline__ void sel_descend(const unsigned long long* h, unsigned long long carry,
                                             double target, SelShared& sh) {
-  if (threadIdx.x == 0) {
-    unsigned long long acc = carry;
-    int d = 255;
-    for (; d > 0; --d) {
-      if (static_cast<double>(acc + h[d]) >= target) break;
-      acc += h[d];
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const double tc = ceil(target);
+    const unsigned long long tu = tc <= 0.0 ? 0ull : (tc >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(tc));
+    unsigned long long v[8], lsum = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = h[255 - 8 * lane - i];
+      lsum += v[i];
     }
-    sh.digit = d;
-    sh.above = acc;
+    unsigned long long incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    unsigned long long acc = carry + (incl - lsum);  // sum of the digits above this lane's
+    int hit = -1;
+    unsigned long long above = 0ull;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (hit < 0 && acc + v[i] >= tu) {
+        hit = 255 - 8 * lane - i;
+        above = acc;
+      }
+      acc += v[i];
+    }
+    // the digit 0 takes whatever is left (the target is always reached by then)
+    if (lane == 31 && hit < 0) {
+      hit = 0;
+      above = acc - v[7];
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+    const int src = __ffs(m) - 1;
+    const int d = __shfl_sync(0xffffffffu, hit, src);
+    const unsigned long long ab = __shfl_sync(0xffffffffu, above, src);
+    if (lane == 0) {
+      sh.digit = d;
+      sh.above = ab;
+    }
   }
   __syncthreads();
+}
+
+// over a list in shared memory: the largest key K such that the weights
+// (counts when w is null) of the entries with key >= K, among those with key
+// >= floor, reach target -- the radix descent of sel_histogram, 8 bits a level
+__device__ unsigned list_descend(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
+                                 double target, SelShared& sh) {
+  const int tid = threadIdx.x;
+  unsigned prefix = 0u;
+  unsigned long long carry = 0ull;
+  for (int l = 0; l < 4; ++l) {
+    const int shift = 24 - 8 * l;
+    const unsigned hi_mask = shift + 8 >= 32 ? 0u : (0xffffffffu << (shift + 8));
+    for (int d = tid; d < 256; d += kSelThreads) sh.hcnt[d] = 0ull;
+    __syncthreads();
+    for (int i = tid; i < n; i += kSelThreads) {
+      const unsigned kx = keys[i];
+      if (kx < floor || (kx & hi_mask) != (prefix & hi_mask)) continue;
+      atomicAdd(&sh.hcnt[(kx >> shift) & 255u], w ? w[i] : 1ull);
+    }
+    __syncthreads();
+    sel_descend(sh.hcnt, carry, target, sh);
+    carry = sh.above;
+    prefix |= static_cast<unsigned>(sh.digit) << shift;
+    __syncthreads();
+  }
+  return prefix;
 }
 
 // the key K of each row (and the first index for top_k == 1)
@@ -150,19 +238,38 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     return;
   }
-  // the row's scaled maximum from the chunk statistics (one warp)
+  // the row's scaled maximum from the chunk statistics, and the first chunk
+  // holding it (one warp)
   if (warp == 0) {
     const float2* part = P.part + static_cast<int64_t>(g) * P.nchunk;
     float M = -INFINITY;
-    for (int ch = lane; ch < P.nchunk; ch += 32) M = fmaxf(M, ldcg_f2(part + ch).x);
-    M = warp_max(M);
+    int mch = P.nchunk;
+    for (int ch = lane; ch < P.nchunk; ch += 32) {
+      const float m = ldcg_f2(part + ch).x;
+      if (m > M) {
+        M = m;
+        mch = ch;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oM = __shfl_xor_sync(0xffffffffu, M, o);
+      const int och = __shfl_xor_sync(0xffffffffu, mch, o);
+      if (oM > M || (oM == M && och < mch)) {
+        M = oM;
+        mch = och;
+      }
+    }
     if (lane == 0) {
       sh.Mc = M;
+      sh.digit = mch;
       sh.bad = !(M > -INFINITY) || !isfinite(M);
     }
   }
   __syncthreads();
   const float Mc = sh.Mc, c = P.c;
+  const int mch = sh.digit;
+  __syncthreads();
   if (sh.bad) {  // an invalid row: the verification flags it; nothing to filter
     if (tid == 0) {
       F.key[g] = 0u;
@@ -172,6 +279,7 @@ __global__ void __launch_bounds__(kSelThreads)
   }
   auto run = [&](const auto* row) {
     using T = typename std::remove_const<typename std::remove_pointer<decltype(row)>::type>::type;
+    const bool vec = (draft ? P.vec_d : P.vec_t) != 0;
     if (f.top_k == 1) {
       // greedy: the first index holding the largest logit
       float best = -INFINITY;
@@ -213,14 +321,78 @@ __global__ void __launch_bounds__(kSelThreads)
       return;
     }
     const int levels = sizeof(T) == 2 ? 2 : 4;  // bf16 keys have 16 significant bits
-    // top-k: the k-th largest key, and (for top-p) the mass at or above it
     unsigned K = 0u;
-    if (use_k) {
+    // With top-k (k at most the number of chunks): the k-th largest chunk
+    // maximum is a lower bound of the k-th largest logit (the k chunk maxima
+    // are k distinct logits), and rounding is monotone, so every logit of the
+    // top-k set has fl(x c) at or above the k-th largest scaled chunk maximum.
+    // One pass gathers those logits; the selections then run on the list.
+    bool listed = false;
+    if (use_k && f.top_k <= P.nchunk) {
+      const float2* part = P.part + static_cast<int64_t>(g) * P.nchunk;
+      for (int ch = tid; ch < P.nchunk; ch += kSelThreads) sh.lkey[ch] = key_of(ldcg_f2(part + ch).x);
+      if (tid == 0) sh.ln = 0;
+      __syncthreads();
+      const float th = float_of_key(list_descend(sh.lkey, nullptr, P.nchunk, 0u,
+                                                  static_cast<double>(f.top_k), sh));
+      // warp-uniform trip count: the ballots below need every lane
+#pragma unroll 1
+      for (int wb = warp * 256; wb < V; wb += kSelWarps * 256) {
+        const int v0 = wb + lane * 8;
+        float x[8];
+        load8<T>(row, v0, V, vec, x);  // entries past V read as -inf
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool take = v0 + e < V && x[e] * c >= th;
+          const unsigned m = __ballot_sync(0xffffffffu, take);
+          if (m == 0u) continue;
+          int base = 0;
+          if (lane == __ffs(m) - 1) base = atomicAdd(&sh.ln, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+          const int pos = base + __popc(m & ((1u << lane) - 1u));
+          if (take && pos < kListCap) {
+            sh.lkey[pos] = key_of(x[e]);
+            sh.lmass[pos] = use_p ? __float2ull_rn(ex2_approx(fmaf(x[e], c, -Mc)) * kMassScalef) : 0ull;
+          }
+        }
+      }
+      __syncthreads();
+      const int n = sh.ln;
+      if (n <= kListCap) {
+        listed = true;
+        K = list_descend(sh.lkey, nullptr, n, 0u, static_cast<double>(f.top_k), sh);
+        if (use_p) {
+          // S_k: the mass of the top-k survivors; then top-p among them
+          unsigned long long part_sum = 0ull;
+          for (int i = tid; i < n; i += kSelThreads)
+            if (sh.lkey[i] >= K) part_sum += sh.lmass[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) part_sum += __shfl_xor_sync(0xffffffffu, part_sum, o);
+          if (lane == 0) sh.wsum[warp] = part_sum;
+          __syncthreads();
+          if (tid == 0) {
+            unsigned long long t = 0ull;
+            for (int w = 0; w < kSelWarps; ++w) t += sh.wsum[w];
+            sh.Sk = t;
+          }
+          __syncthreads();
+          const unsigned Kp = list_descend(sh.lkey, sh.lmass, n, K,
+                                           static_cast<double>(f.top_p) * static_cast<double>(sh.Sk), sh);
+          if (Kp > K) K = Kp;
+        }
+      }
+      __syncthreads();
+    }
+    // top-k by radix descent over the whole row: the k-th largest key, and
+    // (for top-p) the mass at or above it
+    if (use_k && !listed) {
       unsigned prefix = 0u;
       unsigned long long carry_c = 0ull, carry_m = 0ull;
       for (int l = 0; l < levels; ++l) {
         const int shift = 24 - 8 * l;
-        sel_histogram<T>(row, V, c, Mc, prefix, shift, use_p, sh);
+        sel_histogram<T>(row, V, vec, c, Mc, prefix, shift, use_p, sh);
+        if (l == 0 && use_p)
+          for (int d = tid; d < 256; d += kSelThreads) sh.h0mass[d] = sh.hmass[d];
         sel_descend(sh.hcnt, carry_c, static_cast<double>(f.top_k), sh);
         const int d = sh.digit;
         if (tid == 0) {
@@ -237,12 +409,18 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     // top-p on the top-k survivors: the largest key K' (>= K) whose mass at
     // or above reaches top_p * S_k
-    if (use_p) {
+    if (use_p && !listed) {
       unsigned prefix = 0u;
       unsigned long long carry = 0ull;
       for (int l = 0; l < levels; ++l) {
         const int shift = 24 - 8 * l;
-        sel_histogram<T>(row, V, c, Mc, prefix, shift, true, sh);
+        if (l == 0 && use_k) {
+          // the level-0 masses are the top-k pass's
+          for (int d = tid; d < 256; d += kSelThreads) sh.hmass[d] = sh.h0mass[d];
+          __syncthreads();
+        } else {
+          sel_histogram<T>(row, V, vec, c, Mc, prefix, shift, true, sh);
+        }
         if (l == 0 && !use_k && tid == 0) {  // no top-k: every token survives
           unsigned long long all = 0ull;
           for (int e = 0; e < 256; ++e) all += sh.hmass[e];
@@ -261,8 +439,10 @@ __global__ void __launch_bounds__(kSelThreads)
     // smallest one whose logit passes (bisection: the test is monotone in
     // the logit), but never above the row's largest key
     if (use_m) {
+      // the row's largest key lies in the chunk holding the largest scaled max
       unsigned km = 0u;
-      for (int v = tid; v < V; v += kSelThreads) km = max(km, key_of(row_at<T>(row, v)));
+      const int c0 = mch * kChunk;
+      for (int v = c0 + tid; v < min(V, c0 + kChunk); v += kSelThreads) km = max(km, key_of(row_at<T>(row, v)));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) km = max(km, __shfl_xor_sync(0xffffffffu, km, o));
       if (lane == 0) sh.wfirst[warp] = static_cast<int>(km);
@@ -295,44 +475,77 @@ __global__ void __launch_bounds__(kSelThreads)
 }
 
 // the masked copies: x where key(x) >= K of its row (or only at the kept index
-// for top_k == 1), -inf elsewhere; one thread per 8 entries
+// for top_k == 1), -inf elsewhere.  Each side (target rows, draft rows) is one
+// flat row-major array; a thread takes 16-byte vectors of it (plain entries
+// when the rows are not 16-byte aligned).
 template <typename T>
-__device__ __forceinline__ void mask8(const T* src, T* dst, int64_t o, int v0, int V, unsigned K, int first) {
+__device__ __forceinline__ bool mask_keep(float x, int v, unsigned K, int first) {
+  // a NaN stays, whatever its sign, so that the row is still rejected as invalid
+  return isnan(x) || (first >= 0 ? v == first : key_of(x) >= K);
+}
+
+template <typename T>
+__device__ void mask_side(const T* __restrict__ src, T* __restrict__ dst, int nrows, int V, bool vec,
+                          const FilterParams& F, int rows, int k, bool draft, long long t0, long long nt) {
+  constexpr int kVE = 16 / static_cast<int>(sizeof(T));
+  auto row_g = [&](int row) {  // the row's index b * rows + r in the per-row arrays
+    const int per = draft ? k : k + 1;
+    const int b = row / per, j = row - b * per;
+    return b * rows + (draft ? k + 1 + j : j);
+  };
+  if (vec) {
+    const int vpr = V / kVE;  // vectors per row
+    const long long nv = static_cast<long long>(nrows) * vpr;
+    for (long long i = t0; i < nv; i += nt) {
+      const int row = static_cast<int>(i / vpr);
+      const int v0 = static_cast<int>(i - static_cast<long long>(row) * vpr) * kVE;
+      const int g = row_g(row);
+      const unsigned K = __ldg(F.key + g);
+      const int first = __ldg(F.first + g);
+      const int64_t o = static_cast<int64_t>(row) * V + v0;
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(src + o));
+      if constexpr (sizeof(T) == 2) {
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const int v = v0 + e;
-    if (v >= V) break;
-    const float x = row_at<T>(src + o, v);
-    // a NaN stays, whatever its sign, so that the row is still rejected as invalid
-    const bool keep = isnan(x) || (first >= 0 ? v == first : key_of(x) >= K);
-    if constexpr (sizeof(T) == 2) {
-      dst[o + v] = keep ? src[o + v] : static_cast<uint16_t>(0xFF80u);
-    } else {
-      dst[o + v] = keep ? x : -INFINITY;
+        for (int q = 0; q < 4; ++q) {
+          uint32_t lo = w[q] & 0xffffu, hi = w[q] >> 16;
+          if (!mask_keep<T>(__uint_as_float(lo << 16), v0 + 2 * q, K, first)) lo = 0xFF80u;
+          if (!mask_keep<T>(__uint_as_float(hi << 16), v0 + 2 * q + 1, K, first)) hi = 0xFF80u;
+          w[q] = lo | (hi << 16);
+        }
+        u = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        float x[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (!mask_keep<T>(x[q], v0 + q, K, first)) x[q] = -INFINITY;
+        u = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+      }
+      *reinterpret_cast<uint4*>(dst + o) = u;
+    }
+  } else {
+    const long long ne = static_cast<long long>(nrows) * V;
+    for (long long i = t0; i < ne; i += nt) {
+      const int row = static_cast<int>(i / V);
+      const int v = static_cast<int>(i - static_cast<long long>(row) * V);
+      const int g = row_g(row);
+      const float x = row_at<T>(src + static_cast<int64_t>(row) * V, v);
+      const bool keep = mask_keep<T>(x, v, __ldg(F.key + g), __ldg(F.first + g));
+      if constexpr (sizeof(T) == 2) dst[i] = keep ? src[i] : static_cast<uint16_t>(0xFF80u);
+      else dst[i] = keep ? x : -INFINITY;
     }
   }
 }
 
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(256) mask_kernel(const __grid_constant__ Params P, FilterParams F,
-                                                   long long groups_per_row) {
+__global__ void __launch_bounds__(256) mask_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long total = static_cast<long long>(P.B) * P.rows * groups_per_row;
-  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < total; i += static_cast<long long>(gridDim.x) * 256ll) {
-    const int g = static_cast<int>(i / groups_per_row);
-    const int v0 = static_cast<int>(i - static_cast<long long>(g) * groups_per_row) * 8;
-    const int b = g / P.rows, r = g % P.rows;
-    const unsigned K = F.key[g];
-    const int first = F.first[g];
-    if (r <= P.k) {
-      const int64_t o = (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V;
-      mask8<TT>(static_cast<const TT*>(P.Lt), static_cast<TT*>(F.Lt_m), o, v0, P.V, K, first);
-    } else {
-      const int64_t o = (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V;
-      mask8<TD>(static_cast<const TD*>(P.Ld), static_cast<TD*>(F.Ld_m), o, v0, P.V, K, first);
-    }
-  }
+  const long long t0 = blockIdx.x * 256ll + threadIdx.x, nt = static_cast<long long>(gridDim.x) * 256ll;
+  mask_side<TT>(static_cast<const TT*>(P.Lt), static_cast<TT*>(F.Lt_m), P.B * (P.k + 1), P.V, P.vec_t != 0, F,
+                P.rows, P.k, false, t0, nt);
+  mask_side<TD>(static_cast<const TD*>(P.Ld), static_cast<TD*>(F.Ld_m), P.B * P.k, P.V, P.vec_d != 0, F,
+                P.rows, P.k, true, t0, nt);
 }
 
 }  // namespace sv

@@ -256,12 +256,11 @@ sv_status launch_filters(spec_verify_t h, sv::Params& P, int blocks_per_sm, cuda
   if (launch_dependent(sv::select_kernel<TT, TD>, nrows, sv::kSelThreads, sizeof(sv::SelShared), st, P, F) !=
       cudaSuccess)
     return SV_ECUDA;
-  const long long groups = (static_cast<long long>(P.V) + 7) / 8;
-  const long long work = static_cast<long long>(P.B) * P.rows * groups;
+  const long long work = static_cast<long long>(P.B) * P.rows * P.V / 8;
   long long grid = (work + 255) / 256;
   if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
-  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), 256u, 0, st, P, F, groups) !=
-      cudaSuccess)
+  if (grid < 1) grid = 1;
+  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), 256u, 0, st, P, F) != cudaSuccess)
     return SV_ECUDA;
   P.Lt = F.Lt_m;
   P.Ld = F.Ld_m;
