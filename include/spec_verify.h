@@ -245,7 +245,8 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
  * over the logits, finds each row's kept set, writes masked copies of the
  * logits (-inf outside the kept set; a NaN is kept so the row stays invalid)
  * into a buffer of the handle (max_B * (2k+1) * V * 4 bytes, allocated on the
- * first filtered call) and then verifies the copies exactly as an unfiltered
+ * first filtered call -- make that call outside any stream capture; SV_ENOMEM
+ * if it fails) and then verifies the copies exactly as an unfiltered
  * call would: 5 launches instead of 2 and about five reads of the logits.
  * row_stats then describe the filtered rows.  spec_verify_diagnostics applies
  * the same filters.  Decisions of top-p and min-p sit on fp32 arithmetic (the
