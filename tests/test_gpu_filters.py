@@ -158,3 +158,23 @@ def test_filtered_diagnostics(sv):
                                    err_msg=key)
     assert keep.sum() >= B // 2
     ver.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_filters_with_a_gate_policy(sv, dtype):
+    # the features compose: filtered p and q, a per-step schedule and a
+    # cumulative floor on the filtered q, gated and plain sequences mixed
+    B, k, V = 48, 5, 9000
+    filt = ((20, 0.9, 0.0), (0, 0.95, 0.02))
+    sched, cum = [0.3, 0.5], 0.1
+    w = _filtered_drafts(peaked_workload(B, k, V, dtype, seed=61 + (dtype == "f32"),
+                                         gate=(np.arange(B) % 3 != 2), tau=0.4), filt[1])
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    ver.set_gate_policy(sched, cum)
+    out = _run(sv, ver, w)
+    ref = oracle_for(w, tau_sched=sched, min_cum=cum, filters=filt)
+    st = compare(w, out, ref, what=f"filters + policy {dtype}", tau_sched=sched, min_cum=cum)
+    assert st["compared"] >= B // 2
+    assert int((ref["flags"] == 3).sum()) > 0  # the gate still bites on the filtered q
+    ver.close()
