@@ -54,14 +54,18 @@ __device__ __forceinline__ RowMerge merge_row(const Params& P, int b, int r, int
   const int nch = P.nchunk;
   const float2* part = P.part + (static_cast<int64_t>(b) * P.rows + r) * nch;
   RowMerge out{0.f, 0.f, -1, true};
+  // every lane runs the same trip count (a lane without a chunk adds
+  // nothing), so the warp reaches its shuffles converged
+  const int niter = (nch + 31) >> 5;
   if constexpr (kGreedy) {
     // (max, first index of the max) per chunk; a negative index marks a bad chunk
     float M = -INFINITY;
     int bc = nch;
     bool bad = false;
 #pragma unroll 1
-    for (int ch = lane; ch < nch; ch += 32) {
-      const float2 ms = ldcg_f2(part + ch);
+    for (int i = 0; i < niter; ++i) {
+      const int ch = lane + 32 * i;
+      const float2 ms = ch < nch ? ldcg_f2(part + ch) : make_float2(-INFINITY, 0.f);
       if (__float_as_int(ms.y) < 0) bad = true;
       if (ms.x > M) {
         M = ms.x;
@@ -82,12 +86,16 @@ __device__ __forceinline__ RowMerge merge_row(const Params& P, int b, int r, int
   } else {
     float M = -INFINITY;
 #pragma unroll 1
-    for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, ldcg_f2(part + ch).x);
+    for (int i = 0; i < niter; ++i) {
+      const int ch = lane + 32 * i;
+      M = fmaxf(M, ch < nch ? ldcg_f2(part + ch).x : -INFINITY);
+    }
     M = warp_max(M);
     dfloat S = df(0.f);
 #pragma unroll 1
-    for (int ch = lane; ch < nch; ch += 32) {
-      const float2 ms = ldcg_f2(part + ch);
+    for (int i = 0; i < niter; ++i) {
+      const int ch = lane + 32 * i;
+      const float2 ms = ch < nch ? ldcg_f2(part + ch) : make_float2(-INFINITY, 0.f);
       S = df_add(S, df(ms.x == -INFINITY ? ms.y * 0.f : ms.y * exp2f(ms.x - M)));
     }
 #pragma unroll
@@ -333,8 +341,12 @@ __global__ void __launch_bounds__(kDiagThreads)
   const float4* part = pair_partials(P) + static_cast<int64_t>(g) * nch;
   float amin = 0.f, apq = 0.f, best = -INFINITY;
   int bidx = 0x7fffffff;
+  // the same trip count on every lane: the shuffles below run converged
+  const int niter = (nch + 31) >> 5;
 #pragma unroll 1
-  for (int ch = lane; ch < nch; ch += 32) {
+  for (int i = 0; i < niter; ++i) {
+    const int ch = lane + 32 * i;
+    if (ch >= nch) continue;
     const float4 r = __ldcg(part + ch);
     amin += r.x;
     apq += r.y;

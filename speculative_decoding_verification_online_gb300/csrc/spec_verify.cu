@@ -20,6 +20,7 @@ struct spec_verify_s {
   int max_B = 0, k = 0, V = 0, nchunk = 0;
   int num_sms = 0;
   int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [target is bf16][draft is bf16]
+  int fin_spread_smem = 0;                     // see finish_spread_smem
   void* ws = nullptr;                          // one device allocation for the workspace
   size_t ws_bytes = 0;
   float2* part = nullptr;
@@ -50,6 +51,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 
 constexpr int kFinCluster = 4;  // CTAs sharing a sequence's dense residual
+constexpr int kFinWarm = 2;     // warming CTAs of a single-CTA finishing grid
 
 bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
@@ -66,23 +68,38 @@ constexpr int pair_smem() {
          sv::PairStages<TT, TD>::kBytes;
 }
 
+// Dynamic shared memory for a finishing CTA that is to have its SM to itself:
+// just over half of an SM's shared memory, or 0 where the device cannot give
+// that much to one CTA.  Two finishing CTAs on one SM slow each other's
+// dependent chains (measured: about 1 us per call on the 128K-vocabulary
+// batch), so a grid that fits one CTA per SM asks for this much.
+int finish_spread_smem(int device) {
+  int per_sm = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+    return 0;
+  const int want = per_sm / 2 + 1024;
+  return want <= optin && want > static_cast<int>(sizeof(sv::FinishShared)) ? want : 0;
+}
+
 template <typename TT, typename TD, int G>
-cudaError_t configure_one() {
+cudaError_t configure_one(int fin_spread_smem) {
   cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
+  const int fin = static_cast<int>(sizeof(sv::FinishShared));
   return cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(sv::FinishShared)));
+                              fin_spread_smem > fin ? fin_spread_smem : fin);
 }
 
 // every variant (sampling, sampling with a gate policy, greedy) of a dtype
 // pair: opt the kernels into their dynamic shared memory and ask how many
 // stream CTAs fit on an SM
 template <typename TT, typename TD>
-cudaError_t configure(int* blocks_per_sm) {
-  cudaError_t e = configure_one<TT, TD, sv::kModeSample>();
-  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>();
-  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>();
+cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
+  cudaError_t e = configure_one<TT, TD, sv::kModeSample>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>(fin_spread_smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeStats>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
@@ -165,9 +182,17 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
       }
   const int max_clusters = 2 * h->num_sms / csize;
   const int clusters = P.B < max_clusters ? P.B : max_clusters;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * csize));
+  // warming CTAs in front of single-CTA clusters, while every CTA still has
+  // an SM slot at once (two per SM)
+  sv::Params Pf = P;
+  Pf.fin_warm = csize == 1 && clusters + kFinWarm <= 2 * h->num_sms ? kFinWarm : 0;
+  const int grid = clusters * csize + Pf.fin_warm;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(sv::kFinThreads);
-  cfg.dynamicSmemBytes = sizeof(sv::FinishShared);
+  // a grid that fits one CTA per SM gets it (finish_spread_smem)
+  cfg.dynamicSmemBytes = h->fin_spread_smem > 0 && grid <= h->num_sms
+                             ? static_cast<size_t>(h->fin_spread_smem)
+                             : sizeof(sv::FinishShared);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -178,7 +203,7 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G>, P) != cudaSuccess) return SV_ECUDA;
+  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G>, Pf) != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -344,10 +369,11 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
     delete h;
     return SV_ECUDA;
   }
-  cudaError_t e = configure<float, float>(&h->blocks_per_sm[0][0]);
-  if (e == cudaSuccess) e = configure<float, uint16_t>(&h->blocks_per_sm[0][1]);
-  if (e == cudaSuccess) e = configure<uint16_t, float>(&h->blocks_per_sm[1][0]);
-  if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&h->blocks_per_sm[1][1]);
+  h->fin_spread_smem = finish_spread_smem(device);
+  cudaError_t e = configure<float, float>(&h->blocks_per_sm[0][0], h->fin_spread_smem);
+  if (e == cudaSuccess) e = configure<float, uint16_t>(&h->blocks_per_sm[0][1], h->fin_spread_smem);
+  if (e == cudaSuccess) e = configure<uint16_t, float>(&h->blocks_per_sm[1][0], h->fin_spread_smem);
+  if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&h->blocks_per_sm[1][1], h->fin_spread_smem);
   if (e != cudaSuccess) {
     delete h;
     return SV_ECUDA;
@@ -697,6 +723,7 @@ struct NoallocDevice {
   unsigned char* base = nullptr;  // device address of g_noalloc_scratch on this device
   int num_sms = 0;
   int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};
+  int fin_spread_smem = 0;
 };
 constexpr int kNaMaxDevices = 64;
 NoallocDevice g_na[kNaMaxDevices];
@@ -712,10 +739,11 @@ sv_status noalloc_setup(int dev, NoallocDevice** out) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SV_ECUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SV_ECUDA;
-    cudaError_t e = configure<float, float>(&d.blocks_per_sm[0][0]);
-    if (e == cudaSuccess) e = configure<float, uint16_t>(&d.blocks_per_sm[0][1]);
-    if (e == cudaSuccess) e = configure<uint16_t, float>(&d.blocks_per_sm[1][0]);
-    if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&d.blocks_per_sm[1][1]);
+    d.fin_spread_smem = finish_spread_smem(dev);
+    cudaError_t e = configure<float, float>(&d.blocks_per_sm[0][0], d.fin_spread_smem);
+    if (e == cudaSuccess) e = configure<float, uint16_t>(&d.blocks_per_sm[0][1], d.fin_spread_smem);
+    if (e == cudaSuccess) e = configure<uint16_t, float>(&d.blocks_per_sm[1][0], d.fin_spread_smem);
+    if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&d.blocks_per_sm[1][1], d.fin_spread_smem);
     if (e != cudaSuccess) return SV_ECUDA;
     unsigned char* base = static_cast<unsigned char*>(p);
     if (cudaMemset(base, 0xFF, kNaCandBytes) != cudaSuccess ||
@@ -767,6 +795,7 @@ extern "C" sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype
   h.V = V;
   h.nchunk = static_cast<int>(nchunk);
   h.num_sms = d->num_sms;
+  h.fin_spread_smem = d->fin_spread_smem;
   for (int a = 0; a < 2; ++a)
     for (int b = 0; b < 2; ++b) h.blocks_per_sm[a][b] = d->blocks_per_sm[a][b];
   h.cand = reinterpret_cast<sv::Cand*>(d->base);
