@@ -88,8 +88,12 @@ cudaError_t configure_one(int fin_spread_smem) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
   const int fin = static_cast<int>(sizeof(sv::FinishShared));
-  return cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              fin_spread_smem > fin ? fin_spread_smem : fin);
+  const int fin_max = fin_spread_smem > fin ? fin_spread_smem : fin;
+  e = cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fin_max);
+  if (e != cudaSuccess || G == sv::kModeGreedy) return e;
+  return cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G, G != sv::kModeGreedy>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, fin_max);
 }
 
 // every variant (sampling, sampling with a gate policy, greedy) of a dtype
@@ -203,7 +207,14 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = csize > 1 ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G>, Pf) != cudaSuccess) return SV_ECUDA;
+  // the finishing kernel with the dense pass (clusters) when dense residuals
+  // are likely; otherwise the one without it (greedy calls never need it)
+  cudaError_t e;
+  if (G != sv::kModeGreedy && dense_likely)
+    e = cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G, G != sv::kModeGreedy>, Pf);
+  else
+    e = cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G, false>, Pf);
+  if (e != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 

@@ -8,7 +8,7 @@ import torch
 from scipy.stats import chi2
 
 import workloads
-from tests.gpu_helpers import compare, oracle_for
+from tests.gpu_helpers import compare, oracle_for, peaked_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -77,6 +77,66 @@ def test_parity_gate_thresholds_fast_and_dense_paths(sv, tau):
     out = _run(sv, ver, w)
     ref = oracle_for(w)
     compare(w, out, ref, what=f"tau={tau}")
+    ver.close()
+
+
+def _run_scalar_gate(sv, ver, w, tau):
+    # uniform gate settings as scalars: with tau on the candidate fast path the
+    # finishing kernel without the dense pass runs
+    out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=tau, seed=w.philox_seed)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_parity_scalar_fast_gate(sv, dtype):
+    B, k, V = 40, 4, 30000
+    w = peaked_workload(B, k, V, dtype, seed=81 + (dtype == "f32"), gate=1, tau=0.5)
+    ver = _verifier(sv, w)
+    out = _run_scalar_gate(sv, ver, w, 0.5)
+    ref = oracle_for(w)
+    compare(w, out, ref, what=f"scalar fast gate {dtype}")
+    assert int((ref["flags"] == 3).sum()) > 0 and int((ref["flags"] == 1).sum()) > 0
+    ver.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_candidate_overflow_on_the_fast_path_takes_the_chunk_pass(sv, dtype):
+    # Every chunk of a draft row holds four equal spikes (in-chunk probability
+    # ~1/4 each, above slack * 0.21), so a row yields 4 * 80 = 320 gate
+    # candidates -- more than a sequence's candidate list holds.  The row's
+    # admitted set is then unknown, and the stop row (position 0: q(D) is
+    # ~1/320 < tau, a NULL) needs the dense residual, which the fast-path
+    # kernel computes one chunk per pass.
+    B, k, nch = 12, 2, 80
+    V = nch * 2048
+    g = torch.Generator(device="cuda")
+    g.manual_seed(97 + (dtype == "f32"))
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Lt = (torch.randn(B, k + 1, V, generator=g, device="cuda") * 2.0).to(dt)
+    Ld = torch.full((B, k, V), -30.0, device="cuda")
+    off = torch.randint(0, 2048 - 4, (B, k, nch), generator=g, device="cuda")
+    idx = (torch.arange(nch, device="cuda") * 2048).view(1, 1, nch) + off
+    for s_ in range(4):
+        Ld.scatter_(2, idx + s_, 4.0)
+    Ld = Ld.to(dt)
+    u = torch.rand(B, k, V, generator=g, device="cuda").clamp_(1e-30, 1 - 1e-7)
+    D = torch.argmax(Ld.float() - torch.log(-torch.log(u)), dim=2).to(torch.int32)
+    w = workloads.Workload(name="spikes", Lt=Lt, Ld=Ld, D=D, T=1.0,
+                           gate=torch.ones(B, dtype=torch.uint8, device="cuda"),
+                           tau=torch.full((B,), 0.21, device="cuda"), philox_seed=5, B=B, k=k, V=V,
+                           dtype=dtype)
+    ver = _verifier(sv, w)
+    cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
+    out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=0.21, seed=w.philox_seed,
+                  counters=cnt)
+    torch.cuda.synchronize()
+    ref = oracle_for(w)
+    compare(w, out, ref, what=f"candidate overflow {dtype}")
+    # every sequence stops at position 0 with a NULL and emits a residual token
+    assert (ref["flags"][:, 0] == 3).all()
+    assert (out["accepted_len"] == 0).all()
+    assert int(cnt[2]) == B  # NULL stops
     ver.close()
 
 
