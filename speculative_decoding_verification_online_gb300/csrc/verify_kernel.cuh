@@ -468,11 +468,12 @@ struct Stages {
 // CTA c owns chunks c, c + NC, c + 2 NC, ... (NC CTAs), so the grid sweeps
 // memory front to back and every SM gets the same share.  Inside a CTA the
 // warps take the CTA's chunks one at a time from a shared-memory counter.
-// Measured on this part: SMs given equal shares finish within about a
-// microsecond of each other, while warps on one SM drift apart by several, so
-// balancing is needed inside the SM only; no global atomics are involved (a
-// stream of global atomics issued alongside the logits traffic sees replies
-// delayed by tens of microseconds).
+// Measured on this part: warps on one SM drift apart by several
+// microseconds, so balancing inside the SM pays; SMs given equal shares end
+// up to a few microseconds apart, at random from call to call, but handing
+// out work across SMs takes global atomics, whose replies under the logits
+// stream come back too late (a stream of them as the work queue, or only for
+// the last part of the work, made the pass slower), so none are used.
 
 constexpr int kItemRing = 8;       // decoded chunks known to a warp (in flight or next)
 constexpr unsigned kNoWork = 0xffffffffu;
@@ -1386,12 +1387,12 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
       if (warp == 0) {
         const float invS = sh.rowInvS[rt];
         auto chunk_sums = [&](int use_mode) {
-    #pragma unroll 1
+#pragma unroll 1
           for (int ch = lane; ch < nch; ch += 32) {
             const float2 ms = part_at(rt, ch);
             float t = ms.x == -INFINITY ? 0.f : ms.y * exp2f(ms.x - ev.Mt) * invS;
             if (use_mode == 1) {
-    #pragma unroll 1
+#pragma unroll 1
               for (int a = 0; a < nadm; ++a)
                 if (sh.adm_i[jstar][a] / kChunk == ch) t -= fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]);
               t = fmaxf(t, 0.f);
@@ -1403,7 +1404,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
         // one pass gives every chunk's inclusive prefix (float-float) and the total
         auto scan_all = [&]() {
           dfloat carry = df(0.f);
-    #pragma unroll 1
+#pragma unroll 1
           for (int g0 = 0; g0 < nch; g0 += 32) {
             const int ch = g0 + lane;
             const float t = ch < nch ? sh.tile[ch] : 0.f;
@@ -1427,7 +1428,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
         const dfloat y = df_mul(Z, u1);
         dfloat before = df(0.f);
         int found = -1, last = -1;
-    #pragma unroll 1
+#pragma unroll 1
         for (int g0 = 0; g0 < nch; g0 += 32) {
           const int ch = g0 + lane;
           const bool in = ch < nch;
@@ -1438,7 +1439,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
             before = df_sub(sh.prefix[found], df(sh.tile[found]));
           }
         }
-    #pragma unroll
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
         if (found < 0) {  // rounding left y at or past the total: the last chunk with mass
           found = last < 0 ? 0 : last;
@@ -1473,7 +1474,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
     {
       int lastpos = -1;
       float t0 = 0.f, t1 = 0.f;
-  #pragma unroll
+#pragma unroll
       for (int e = 0; e < 8; ++e) {
         if (e & 1) t1 += r8[e]; else t0 += r8[e];
         if (r8[e] > 0.f) lastpos = c0 + e0 + e;
@@ -1483,14 +1484,14 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
       dfloat wexcl = shfl_up_df(wincl, 1);
       if (lane == 0) wexcl = df(0.f);
       int wl = lastpos;
-  #pragma unroll
+#pragma unroll
       for (int o = 16; o > 0; o >>= 1) wl = max(wl, __shfl_xor_sync(0xffffffffu, wl, o));
       if (lane == 31) sh.wtot[warp] = wincl;
       if (lane == 0) sh.wlast[warp] = wl;
       __syncthreads();
       // every thread forms its warp's base from the (at most 8) warp totals
       dfloat wbase = df(0.f);
-  #pragma unroll 1
+#pragma unroll 1
       for (int w = 0; w < warp; ++w) wbase = df_add(wbase, sh.wtot[w]);
       const dfloat lo = df_add(wbase, wexcl), hi = df_add(wbase, wincl);
       if (masses && tid == 0) {  // the chunk's residual mass: the warp totals in order
@@ -1504,7 +1505,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
         float run = 0.f, prev = 0.f;
         int pick = lastpos;  // rounding inside the thread: its last positive entry
         bool hit = false;
-  #pragma unroll
+#pragma unroll
         for (int e = 0; e < 8; ++e) {
           if (!hit) {
             prev = run;
