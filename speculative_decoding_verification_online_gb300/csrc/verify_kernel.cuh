@@ -1317,23 +1317,46 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
                         kPol && gated && P.min_cum > 0.f ? P.min_cum : -1.f, 0, nullptr, nullptr};
   const bool vt = P.vec_t != 0, vd = P.vec_d != 0;
   constexpr int kLaneGroups = kChunk / 8 / 32;
+  // bf16 row pairs: a lane's whole share of the chunk (eight 16-byte loads
+  // per row) in flight at once, kept raw until each group is evaluated; the
+  // ragged or unaligned chunk, and wider types, four groups at a time
+  constexpr bool kNarrow = sizeof(TT) == 2 && sizeof(TD) == 2;
 #pragma unroll 1
   for (int ch = rank * kFinWarps + warp; ch < nch; ch += csize * kFinWarps) {
     const int c0 = ch * kChunk;
     float acc = 0.f;
-#pragma unroll 1
-    for (int h = 0; h < kLaneGroups; h += 4) {
-      float xt[4][8], xd[4][8];
+    if (kNarrow && vt && vd && c0 + kChunk <= V) {
+      uint4 rt[kLaneGroups], rd[kLaneGroups];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
-        load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
+      for (int g = 0; g < kLaneGroups; ++g) {
+        rt[g] = __ldcg(reinterpret_cast<const uint4*>(trow + c0 + (g * 32 + lane) * 8));
+        rd[g] = __ldcg(reinterpret_cast<const uint4*>(drow + c0 + (g * 32 + lane) * 8));
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int g = 0; g < kLaneGroups; ++g) {
+        const float xt[8] = {bf16_lo(rt[g].x), bf16_hi(rt[g].x), bf16_lo(rt[g].y), bf16_hi(rt[g].y),
+                             bf16_lo(rt[g].z), bf16_hi(rt[g].z), bf16_lo(rt[g].w), bf16_hi(rt[g].w)};
+        const float xd[8] = {bf16_lo(rd[g].x), bf16_hi(rd[g].x), bf16_lo(rd[g].y), bf16_hi(rd[g].y),
+                             bf16_lo(rd[g].z), bf16_hi(rd[g].z), bf16_lo(rd[g].w), bf16_hi(rd[g].w)};
         float rr[8];
-        residual8<kPol>(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
+        residual8<kPol>(ev, xt, xd, c0 + (g * 32 + lane) * 8, V, rr);
         acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+      }
+    } else {
+#pragma unroll 1
+      for (int h = 0; h < kLaneGroups; h += 4) {
+        float xt[4][8], xd[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
+          load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float rr[8];
+          residual8<kPol>(ev, xt[u], xd[u], c0 + ((h + u) * 32 + lane) * 8, V, rr);
+          acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
+        }
       }
     }
     acc = warp_sum(acc);
