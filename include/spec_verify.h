@@ -193,7 +193,13 @@ sv_status spec_verify_diagnostics(spec_verify_t h,
  * back and synchronises the stream before returning; counters are overwritten,
  * not accumulated.  The staging buffers (sized for max_B) are allocated on the
  * first call and kept by the handle.  Pinned host memory makes the copies
- * asynchronous DMA; pageable memory works but is slower. */
+ * asynchronous DMA; pageable memory works but is slower.  Logits in
+ * page-locked host memory that the device can address are not copied when
+ * the call reads them about once -- no sampler filters, and no dense residual
+ * pass (temperature 0, or every row gated with scalar settings or the
+ * handle's schedule on the candidate fast path): the kernels then read them
+ * in place over the host link, and the caller must keep them unchanged until
+ * the call returns (it returns after the stream has synchronised). */
 sv_status spec_verify_run_host(spec_verify_t h,
                                const void* target_logits, sv_dtype tdt,
                                const void* draft_logits, sv_dtype ddt,

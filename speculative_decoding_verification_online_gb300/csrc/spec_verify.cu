@@ -428,6 +428,36 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
 
 namespace {
 
+// Whether a call may need the dense residual pass.  It does not when the call
+// is greedy, or when every row is gated on the candidate fast path: uniform
+// settings, or the handle's schedule, with every floor (the step's threshold
+// or the cumulative floor, whichever is higher) above the fast path's bound.
+// Per-sequence settings are device data: their presence counts as likely.
+bool dense_residuals_likely(spec_verify_t h, float temperature, sv_gate gate_mode, float threshold,
+                            const uint8_t* gate_mode_per_seq, const float* threshold_per_seq) {
+  if (temperature == 0.f) return false;
+  auto fast_floor = [&](float t) {
+    return std::max(t, h->min_cum) * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
+  };
+  const bool has_sched = h->n_sched > 0;
+  bool all_fast = gate_mode == SV_GATED_MU && !gate_mode_per_seq &&
+                  (has_sched || (!threshold_per_seq && fast_floor(threshold)));
+  for (int j = 0; has_sched && j < h->k; ++j)
+    all_fast = all_fast && fast_floor(h->sched[j < h->n_sched ? j : h->n_sched - 1]);
+  return !all_fast;
+}
+
+// The device address of page-locked host memory the device can read, or null
+// (device memory, pageable or unknown memory)
+const void* host_device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // Validate what every verifying call shares and fill the launch arguments
 // (outputs and draws left empty).  SV_OK with *empty = true: nothing to do.
 sv_status prepare_params(spec_verify_t h, const void* target_logits, sv_dtype tdt,
@@ -508,7 +538,6 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   if (!accepted_len || !tokens || !accept_prob) return SV_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return SV_ECUDA;
-  const int k = h->k;
   P.seed = seed;
   P.seq_offset = seq_offset;
   P.u0 = u_accept;
@@ -523,15 +552,8 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
   const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
-  // dense residuals are likely unless every row is gated on the candidate fast
-  // path (per-sequence settings are device data: their presence counts as likely)
-  auto fast_floor = [&](float t) {
-    return std::max(t, P.min_cum) * (1.0f - 1.0f / 1024.0f) * (sv::kTopM + 1) > 1.0f;
-  };
-  bool all_fast_gated = gate_mode == SV_GATED_MU && !gate_mode_per_seq &&
-                        (P.has_sched || (!threshold_per_seq && fast_floor(threshold)));
-  for (int j = 0; P.has_sched && j < k; ++j) all_fast_gated = all_fast_gated && fast_floor(P.tau_step[j]);
-  const bool dense_likely = !all_fast_gated && !P.greedy;
+  const bool dense_likely =
+      dense_residuals_likely(h, temperature, gate_mode, threshold, gate_mode_per_seq, threshold_per_seq);
   // sampler filters (temperature > 0: a greedy call is one-hot already)
   if (!P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]))) {
     if (P.has_sched || P.min_cum > 0.f)
@@ -633,9 +655,26 @@ sv_status spec_verify_run_host(spec_verify_t h, const void* target_logits, sv_dt
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const size_t bt = static_cast<size_t>(B) * (k + 1) * V * elem_size(tdt);
   const size_t bd = static_cast<size_t>(B) * k * V * elem_size(ddt);
+  // Logits in page-locked host memory that the device can address are read
+  // in place over the host link -- the kernels' own reads are the transfer --
+  // when the call reads them about once (no dense residual pass, no sampler
+  // filters); otherwise they are copied into the staging buffer first.  The
+  // link's bandwidth is the same either way; in place, the copy no longer
+  // precedes the verification as a separate step.
+  const bool in_place = !filter_on(h->filt[0]) && !filter_on(h->filt[1]) &&
+                        !dense_residuals_likely(h, temperature, gate_mode, threshold, gate_mode_per_seq,
+                                                threshold_per_seq);
+  const void* lt = in_place ? host_device_view(target_logits) : nullptr;
+  const void* ld = in_place ? host_device_view(draft_logits) : nullptr;
   bool ok = true;
-  ok = ok && cudaMemcpyAsync(s + o_t, target_logits, bt, cudaMemcpyHostToDevice, st) == cudaSuccess;
-  ok = ok && cudaMemcpyAsync(s + o_d, draft_logits, bd, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  if (!lt) {
+    ok = ok && cudaMemcpyAsync(s + o_t, target_logits, bt, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    lt = s + o_t;
+  }
+  if (!ld) {
+    ok = ok && cudaMemcpyAsync(s + o_d, draft_logits, bd, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    ld = s + o_d;
+  }
   ok = ok && cudaMemcpyAsync(s + o_D, draft_tokens, static_cast<size_t>(B) * k * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
   if (gate_mode_per_seq)
     ok = ok && cudaMemcpyAsync(s + o_g, gate_mode_per_seq, static_cast<size_t>(B), cudaMemcpyHostToDevice, st) == cudaSuccess;
@@ -644,7 +683,7 @@ sv_status spec_verify_run_host(spec_verify_t h, const void* target_logits, sv_dt
   if (counters) ok = ok && cudaMemsetAsync(s + o_cnt, 0, SV_NUM_COUNTERS * 8, st) == cudaSuccess;
   if (!ok) return SV_ECUDA;
   sv_status rc = spec_verify_run_ex(
-      h, s + o_t, tdt, s + o_d, ddt, reinterpret_cast<const int32_t*>(s + o_D), B, temperature,
+      h, lt, tdt, ld, ddt, reinterpret_cast<const int32_t*>(s + o_D), B, temperature,
       gate_mode, threshold, gate_mode_per_seq ? reinterpret_cast<const uint8_t*>(s + o_g) : nullptr,
       threshold_per_seq ? reinterpret_cast<const float*>(s + o_tau) : nullptr, seed, 0, nullptr,
       nullptr, reinterpret_cast<int32_t*>(s + o_al), reinterpret_cast<int32_t*>(s + o_tok),

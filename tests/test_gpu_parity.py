@@ -393,6 +393,22 @@ def test_host_buffer_entry_point_matches_device_path(sv):
     ver.close()
 
 
+@pytest.mark.parametrize("mode", ["gated_scalar", "greedy", "plain"])
+def test_host_buffer_entry_point_reads_pinned_logits_in_place(sv, mode):
+    # pinned logits are read in place by the fast-path and greedy calls, and
+    # staged by a call with dense residuals; every way matches the device path
+    w = peaked_workload(24, 4, 20000, "bf16", seed=57, gate=1, tau=0.5, T=0.0 if mode == "greedy" else 1.0)
+    ver = _verifier(sv, w)
+    gm = sv.SV_PLAIN if mode == "plain" else sv.SV_GATED_MU
+    dev = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=gm, threshold=0.5, seed=w.philox_seed)
+    torch.cuda.synchronize()
+    host = ver.run_host(w.Lt.cpu().pin_memory(), w.Ld.cpu().pin_memory(), w.D.cpu().pin_memory(),
+                        w.T, gate_mode=gm, threshold=0.5, seed=w.philox_seed)
+    for key in ("accepted_len", "tokens", "accept_prob", "flags"):
+        assert torch.equal(dev[key].cpu(), host[key]), key
+    ver.close()
+
+
 # ------------------------------------------------------ temperature 0 (greedy)
 
 def _greedy_custom(B, k, V, dtype, seed, gate):
