@@ -1629,9 +1629,9 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_con
     const int fmode = lead->fmode;
     if constexpr (kDense) {
       if (fmode == 2) dense_chunk_sums<TT, TD, kPol>(P, b, *lead, lead->tile, rank, csize);
+      if (csize > 1) cluster.sync();  // every chunk mass is in the leading CTA
+      else __syncthreads();
     }
-    if (csize > 1) cluster.sync();  // every chunk mass is in the leading CTA
-    else __syncthreads();
     if (rank == 0 && fmode >= 0) finish_back<TT, TD, kPol, kDense>(P, b, sh);
   }
 }
