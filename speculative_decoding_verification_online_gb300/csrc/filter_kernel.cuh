@@ -37,6 +37,12 @@ struct FilterParams {
 };
 
 constexpr int kSelThreads = 512;
+constexpr int kMaskThreads = 256;  // threads of a masking CTA
+// A selecting CTA sweeps its row with one 16-byte load per thread per step,
+// used at once (its registers are at the two-CTAs-per-SM cap), so each step
+// would wait a full DRAM round trip; every thread therefore also pulls its
+// entries kSelAhead steps ahead into L2 (no registers), and the loads hit L2.
+constexpr int kSelAhead = 4;
 constexpr int kListCap = 4096;  // logits gathered for an in-shared-memory selection
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr float kMassScalef = 1099511627776.0f;  // 2^40: masses as integers
@@ -96,8 +102,12 @@ __device__ void sel_histogram(const T* row, int V, bool vec, float c, float Mc, 
   int cd = -1;
   unsigned cc = 0u;
   unsigned long long cm = 0ull;
+#pragma unroll
+  for (int a = 0; a < kSelAhead; ++a)
+    if (tid * 8 + a * kSelThreads * 8 < V) prefetch_l2(row + tid * 8 + a * kSelThreads * 8);
 #pragma unroll 1
   for (int v0 = tid * 8; v0 < V; v0 += kSelThreads * 8) {
+    if (v0 + kSelAhead * kSelThreads * 8 < V) prefetch_l2(row + v0 + kSelAhead * kSelThreads * 8);
     float x[8];
     load8<T>(row, v0, V, vec, x);
 #pragma unroll
@@ -336,9 +346,15 @@ __global__ void __launch_bounds__(kSelThreads)
       const float th = float_of_key(list_descend(sh.lkey, nullptr, P.nchunk, 0u,
                                                   static_cast<double>(f.top_k), sh));
       // warp-uniform trip count: the ballots below need every lane
+#pragma unroll
+      for (int a = 0; a < kSelAhead; ++a) {
+        const int vp = warp * 256 + lane * 8 + a * kSelWarps * 256;
+        if (vp < V) prefetch_l2(row + vp);
+      }
 #pragma unroll 1
       for (int wb = warp * 256; wb < V; wb += kSelWarps * 256) {
         const int v0 = wb + lane * 8;
+        if (v0 + kSelAhead * kSelWarps * 256 < V) prefetch_l2(row + v0 + kSelAhead * kSelWarps * 256);
         float x[8];
         load8<T>(row, v0, V, vec, x);  // entries past V read as -inf
 #pragma unroll
@@ -484,68 +500,84 @@ __device__ __forceinline__ bool mask_keep(float x, int v, unsigned K, int first)
   return isnan(x) || (first >= 0 ? v == first : key_of(x) >= K);
 }
 
+// one 16-byte vector of row entries [v0, v0 + 16 / sizeof(T)), masked
 template <typename T>
-__device__ void mask_side(const T* __restrict__ src, T* __restrict__ dst, int nrows, int V, bool vec,
-                          const FilterParams& F, int rows, int k, bool draft, long long t0, long long nt) {
-  constexpr int kVE = 16 / static_cast<int>(sizeof(T));
-  auto row_g = [&](int row) {  // the row's index b * rows + r in the per-row arrays
-    const int per = draft ? k : k + 1;
-    const int b = row / per, j = row - b * per;
-    return b * rows + (draft ? k + 1 + j : j);
-  };
-  if (vec) {
-    const int vpr = V / kVE;  // vectors per row
-    const long long nv = static_cast<long long>(nrows) * vpr;
-    for (long long i = t0; i < nv; i += nt) {
-      const int row = static_cast<int>(i / vpr);
-      const int v0 = static_cast<int>(i - static_cast<long long>(row) * vpr) * kVE;
-      const int g = row_g(row);
-      const unsigned K = __ldg(F.key + g);
-      const int first = __ldg(F.first + g);
-      const int64_t o = static_cast<int64_t>(row) * V + v0;
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(src + o));
-      if constexpr (sizeof(T) == 2) {
-        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ uint4 mask_vec(uint4 u, int v0, unsigned K, int first) {
+  if constexpr (sizeof(T) == 2) {
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t lo = w[q] & 0xffffu, hi = w[q] >> 16;
-          if (!mask_keep<T>(__uint_as_float(lo << 16), v0 + 2 * q, K, first)) lo = 0xFF80u;
-          if (!mask_keep<T>(__uint_as_float(hi << 16), v0 + 2 * q + 1, K, first)) hi = 0xFF80u;
-          w[q] = lo | (hi << 16);
-        }
-        u = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        float x[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (!mask_keep<T>(x[q], v0 + q, K, first)) x[q] = -INFINITY;
-        u = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
-      }
-      *reinterpret_cast<uint4*>(dst + o) = u;
+    for (int q = 0; q < 4; ++q) {
+      uint32_t lo = w[q] & 0xffffu, hi = w[q] >> 16;
+      if (!mask_keep<T>(__uint_as_float(lo << 16), v0 + 2 * q, K, first)) lo = 0xFF80u;
+      if (!mask_keep<T>(__uint_as_float(hi << 16), v0 + 2 * q + 1, K, first)) hi = 0xFF80u;
+      w[q] = lo | (hi << 16);
     }
+    return make_uint4(w[0], w[1], w[2], w[3]);
   } else {
-    const long long ne = static_cast<long long>(nrows) * V;
-    for (long long i = t0; i < ne; i += nt) {
-      const int row = static_cast<int>(i / V);
-      const int v = static_cast<int>(i - static_cast<long long>(row) * V);
-      const int g = row_g(row);
-      const float x = row_at<T>(src + static_cast<int64_t>(row) * V, v);
-      const bool keep = mask_keep<T>(x, v, __ldg(F.key + g), __ldg(F.first + g));
-      if constexpr (sizeof(T) == 2) dst[i] = keep ? src[i] : static_cast<uint16_t>(0xFF80u);
-      else dst[i] = keep ? x : -INFINITY;
+    float x[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (!mask_keep<T>(x[q], v0 + q, K, first)) x[q] = -INFINITY;
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+  }
+}
+
+// One row (index g in the per-row arrays) by one CTA: the threshold read
+// once, then every thread with four independent 16-byte vectors in flight.
+template <typename T>
+__device__ void mask_row(const T* __restrict__ src, T* __restrict__ dst, int V, bool vec, unsigned K,
+                         int first) {
+  constexpr int kVE = 16 / static_cast<int>(sizeof(T));
+  constexpr int kT = kMaskThreads;
+  if (vec) {  // V is a multiple of kVE (the row is 16-byte aligned and sized)
+    const int vpr = V / kVE;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    int v = threadIdx.x;
+#pragma unroll 1
+    for (; v + 3 * kT < vpr; v += 4 * kT) {
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[q] = __ldg(s4 + v + q * kT);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d4[v + q * kT] = mask_vec<T>(u[q], (v + q * kT) * kVE, K, first);
+    }
+#pragma unroll 1
+    for (; v < vpr; v += kT) d4[v] = mask_vec<T>(__ldg(s4 + v), v * kVE, K, first);
+  } else {
+#pragma unroll 1
+    for (int v = threadIdx.x; v < V; v += kT) {
+      const float x = row_at<T>(src, v);
+      const bool keep = mask_keep<T>(x, v, K, first);
+      if constexpr (sizeof(T) == 2) dst[v] = keep ? src[v] : static_cast<uint16_t>(0xFF80u);
+      else dst[v] = keep ? x : -INFINITY;
     }
   }
 }
 
+// The masked copies of every target and draft row: CTA i takes rows i,
+// i + grid, ... of the target rows followed by the draft rows.
 template <typename TT, typename TD>
-__global__ void __launch_bounds__(256) mask_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
+__global__ void __launch_bounds__(kMaskThreads) mask_kernel(const __grid_constant__ Params P,
+                                                             const __grid_constant__ FilterParams F) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long t0 = blockIdx.x * 256ll + threadIdx.x, nt = static_cast<long long>(gridDim.x) * 256ll;
-  mask_side<TT>(static_cast<const TT*>(P.Lt), static_cast<TT*>(F.Lt_m), P.B * (P.k + 1), P.V, P.vec_t != 0, F,
-                P.rows, P.k, false, t0, nt);
-  mask_side<TD>(static_cast<const TD*>(P.Ld), static_cast<TD*>(F.Ld_m), P.B * P.k, P.V, P.vec_d != 0, F,
-                P.rows, P.k, true, t0, nt);
+  const int nt = P.B * (P.k + 1), nd = P.B * P.k;
+#pragma unroll 1
+  for (int row = blockIdx.x; row < nt + nd; row += gridDim.x) {
+    const bool draft = row >= nt;
+    const int rr = draft ? row - nt : row;
+    const int per = draft ? P.k : P.k + 1;
+    const int b = rr / per, j = rr - b * per;
+    const int g = b * P.rows + (draft ? P.k + 1 + j : j);  // index in the per-row arrays
+    const unsigned K = __ldg(F.key + g);
+    const int first = __ldg(F.first + g);
+    const int64_t o = static_cast<int64_t>(rr) * P.V;
+    if (draft)
+      mask_row<TD>(static_cast<const TD*>(P.Ld) + o, static_cast<TD*>(F.Ld_m) + o, P.V, P.vec_d != 0, K, first);
+    else
+      mask_row<TT>(static_cast<const TT*>(P.Lt) + o, static_cast<TT*>(F.Lt_m) + o, P.V, P.vec_t != 0, K, first);
+  }
 }
 
 }  // namespace sv

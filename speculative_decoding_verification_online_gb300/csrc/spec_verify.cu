@@ -292,11 +292,12 @@ sv_status launch_filters(spec_verify_t h, sv::Params& P, int blocks_per_sm, cuda
   if (launch_dependent(sv::select_kernel<TT, TD>, nrows, sv::kSelThreads, sizeof(sv::SelShared), st, P, F) !=
       cudaSuccess)
     return SV_ECUDA;
-  const long long work = static_cast<long long>(P.B) * P.rows * P.V / 8;
-  long long grid = (work + 255) / 256;
+  // one CTA per row at a time, at most eight per SM
+  long long grid = static_cast<long long>(P.B) * P.rows;
   if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
   if (grid < 1) grid = 1;
-  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), 256u, 0, st, P, F) != cudaSuccess)
+  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(sv::kMaskThreads),
+                       0, st, P, F) != cudaSuccess)
     return SV_ECUDA;
   P.Lt = F.Lt_m;
   P.Ld = F.Ld_m;
