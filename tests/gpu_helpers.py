@@ -50,11 +50,15 @@ def oracle_for(w: workloads.Workload, idx=None, nthreads=8, u0=None, u1=None, ta
 
 
 def gated_q_of_drafts(w: workloads.Workload, ref, idx=None):
-    """q_j(D_j) in fp64 from the oracle's row statistics (for excluding gate-boundary alphas)."""
+    """q_j(D_j) in fp64 from the oracle's row statistics (for excluding gate-boundary alphas);
+    at temperature 0, 1 where D_j is the first largest draft logit and 0 elsewhere."""
     sel = slice(None) if idx is None else torch.as_tensor(idx)
     Ld = w.Ld[sel].float().cpu().double()
     D = w.D[sel].cpu().long()
     k = w.k
+    if w.T == 0:
+        # greedy decoding: q is one-hot at the first largest draft logit
+        return (D.numpy() == np.argmax(Ld.numpy(), axis=2)).astype(np.float64)
     x = torch.gather(Ld, 2, D.unsqueeze(-1)).squeeze(-1) / w.T
     lse = torch.as_tensor(ref["row_stats"][:, k + 1:, 1])
     return torch.exp(x - lse).numpy()
