@@ -304,6 +304,69 @@ def test_zero_target_mass_never_accepted_or_emitted(sv):
         ver.close()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gate_equality_all_null_and_all_accepted(sv, dtype):
+    # every draft and target row holds two equal logits (tokens 5 and 2100, in
+    # different chunks of a ragged 4104-token row) and -inf elsewhere, so
+    # q(D) = p(D) = 1/2 exactly in fp32: at tau = 1/2 the gate admits D
+    # (equality passes), alpha = 1 and every sequence takes the bonus; at the
+    # next float above 1/2 every position-0 draft is an explicit NULL row and
+    # the residual (mu = 0 everywhere) samples p
+    B, k, V, hot = 64, 2, 4104, (5, 2100)
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Lt = torch.full((B, k + 1, V), float("-inf"), device="cuda")
+    Lt[:, :, list(hot)] = 0.0
+    Ld = Lt[:, :k].clone()
+    D = torch.tensor(hot, dtype=torch.int32, device="cuda")[torch.arange(B * k, device="cuda") % 2]
+    D = D.view(B, k).contiguous()
+    above = float(np.nextafter(np.float32(0.5), np.float32(1.0)))
+    for tau, want_len, want_flag in ((0.5, k, 1), (above, 0, 3)):
+        w = workloads.Workload(name="equality", Lt=Lt.to(dt), Ld=Ld.to(dt), D=D, T=1.0,
+                               gate=torch.ones(B, dtype=torch.uint8, device="cuda"),
+                               tau=torch.full((B,), tau, device="cuda"), philox_seed=17, B=B, k=k,
+                               V=V, dtype=dtype)
+        ver = _verifier(sv, w)
+        for scalar in (False, True):
+            if scalar:  # the same setting given as the scalar arguments
+                out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=tau,
+                              seed=w.philox_seed)
+                torch.cuda.synchronize()
+            else:
+                out = _run(sv, ver, w)
+            assert torch.all(out["accepted_len"] == want_len), (tau, scalar)
+            assert torch.all(out["flags"][:, 0] == want_flag), (tau, scalar)
+            emitted = out["tokens"][:, want_len]
+            assert torch.all((emitted == hot[0]) | (emitted == hot[1])), (tau, scalar)
+            if want_len == k:
+                assert torch.all(out["accept_prob"] == 1.0)
+                assert torch.equal(out["tokens"][:, :k], D)
+            else:
+                assert torch.all(out["accept_prob"][:, 0] == 0.0)
+                assert torch.all(out["tokens"][:, 1:] == -1)
+        ref = oracle_for(w)
+        assert np.all(ref["accepted_len"] == want_len)
+        assert np.array_equal(out["tokens"].cpu().numpy(), ref["tokens"])
+        ver.close()
+
+
+def test_plain_draft_with_zero_proposal_mass_is_accepted(sv):
+    # plain mode, q(D) = 0 (the drafted token's logit is -inf) and p(D) > 0:
+    # u0 * 0 <= p(D) always holds, so the draft is accepted with alpha = 1
+    B, k, V = 256, 1, 3000
+    w = _custom(B, k, V, "f32", 1.0, 0, 0.5, seed=23)
+    Ld = w.Ld.clone()
+    Ld.view(B * k, V)[torch.arange(B * k, device="cuda"), w.D.view(-1).long()] = float("-inf")
+    w = workloads.Workload(name="zero_q", Lt=w.Lt, Ld=Ld, D=w.D, T=1.0, gate=w.gate, tau=w.tau,
+                           philox_seed=w.philox_seed, B=B, k=k, V=V, dtype="f32")
+    ver = _verifier(sv, w)
+    out = _run(sv, ver, w)
+    assert torch.all(out["flags"][:, 0] == 1)
+    assert torch.all(out["accept_prob"][:, 0] == 1.0)
+    assert torch.all(out["accepted_len"] == k)
+    compare(w, out, oracle_for(w), what="zero proposal mass")
+    ver.close()
+
+
 def test_explicit_uniforms_probe_decisions(sv):
     # u0 at 0 accepts everything with p > 0; u0 just below 1 rejects every ratio < 1
     B, k, V = 32, 4, 5000
