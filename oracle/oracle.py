@@ -52,11 +52,19 @@ def build(force: bool = False) -> str:
     return LIBRARY
 
 
+# A test that checks whether the pins catch a planted mistake points this
+# variable at an oracle library built from a mutated copy of the source;
+# nothing else sets it.
+LIBRARY_OVERRIDE_ENV = "SPEC_VERIFY_ORACLE_LIBRARY"
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(LIBRARY)
+        override = os.environ.get(LIBRARY_OVERRIDE_ENV)
+        if not override:
+            build()
+        L = ctypes.CDLL(override or LIBRARY)
         P = ctypes.c_void_p
         L.oracle_philox4x32_10.argtypes = [P, P, P]
         L.oracle_philox4x32_10.restype = None

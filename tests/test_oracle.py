@@ -523,6 +523,24 @@ def test_gate_policy_floors_compose_by_logical_and():
     assert O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.2], min_cum=0.2)["accepted_len"][0] == 2
 
 
+def test_gate_policy_cumulative_product_uses_draft_probabilities():
+    # [R "schedule behavior"]: the prefix product is of the draft's own
+    # probabilities of its drafted tokens; the target rows play no part in the
+    # gate.  q_0(D_0) = q_1(D_1) = 1/2 while p_0(D_0) = 1/8: the floor 1/4 is
+    # met exactly by the draft product at step 1 (equality passes) and would
+    # be missed by the target's (1/16).  u0 = 0 accepts every admitted draft.
+    V = 8
+    Ld = np.full((1, 2, V), -np.inf, dtype=np.float32)
+    Ld[0, :, :2] = 0.0
+    Lt = np.zeros((1, 3, V), dtype=np.float32)
+    D = np.zeros((1, 2), dtype=np.int32)
+    out = O.verify(Lt, Ld, D, 1.0, 1, 0.5, tau_sched=[0.0], min_cum=0.25, u0=np.zeros((1, 2)),
+                   u1=np.full(1, 0.5))
+    assert out["accepted_len"][0] == 2
+    assert list(out["flags"][0]) == [O.FLAG_ACCEPT, O.FLAG_ACCEPT]
+    np.testing.assert_allclose(out["alpha"][0], [0.25, 0.25], rtol=0, atol=1e-15)
+
+
 def test_gate_policy_special_cases_reduce_to_the_plain_and_flat_rules():
     rng = np.random.default_rng(77)
     B, k, V = 300, 4, 40
@@ -736,6 +754,31 @@ def test_filters_keep_ties_and_follow_the_chain_order():
     assert np.count_nonzero(O.filtered_row(L, 1.0, 0, 1.0, 1.0)[0]) == 1
     p0, _, _, _ = O.softmax_row(L, 1.3)
     np.testing.assert_array_equal(O.filtered_row(L, 1.3, 0, 1.0, 0.0)[0], p0)
+
+
+def test_top_p_keeps_the_prefix_whose_mass_reaches_top_p_exactly():
+    # [M] "What changed", as read here: top-p keeps the shortest prefix, in decreasing
+    # probability, whose mass reaches top_p.  With top_p chosen so that
+    # top_p * (total mass) equals the first token's probability exactly in
+    # double, the first token alone reaches it; the next top_p up needs two.
+    L = np.array([1.5, 0.25, -0.5, -2.0], dtype=np.float32)
+    p, _, _, _ = O.softmax_row(L, 1.0)
+    total = 0.0
+    for v in np.argsort(-L, kind="stable"):  # decreasing logit, the filter's order
+        total += p[v]
+    tp = p[0] / total
+    for _ in range(8):  # a few ulps either way until the product is exact
+        if tp * total == p[0]:
+            break
+        tp = np.nextafter(tp, 1.0 if tp * total < p[0] else 0.0)
+    assert tp * total == p[0]
+    got, margin = O.filtered_row(L, 1.0, 0, tp, 0.0)
+    assert np.count_nonzero(got) == 1 and got[0] == 1.0
+    assert margin == 0.0  # the decision sits on its boundary
+    up = np.nextafter(tp, 1.0)
+    while up * total <= p[0]:
+        up = np.nextafter(up, 1.0)
+    assert np.count_nonzero(O.filtered_row(L, 1.0, 0, up, 0.0)[0]) == 2
 
 
 def test_filtered_target_support_is_never_violated():
