@@ -480,7 +480,10 @@ def main():
         cores = os.cpu_count() or 1
         small = make_workload(args, args.seed, "cpu", B=min(B, 16 if V > 100000 else B))
         rate, reps, cel = cpu_oracle_rate(small, args.cpu_seconds, cores, sched, cum, filters_of(args))
+        # the same oracle on one thread, on a quarter of the time
+        rate1, _, _ = cpu_oracle_rate(small, max(args.cpu_seconds / 4, 0.1), 1, sched, cum, filters_of(args))
         cpu = {"value": rate, "unit": "positions/s", "cores": cores, "kind": "oracle",
+               "single_thread_value": rate1,
                "sample": f"{small.B} sequences of {args.workload} x {reps} repetitions "
                          f"({cel:.1f} s)"}
 

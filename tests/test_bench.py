@@ -38,3 +38,15 @@ def test_reference_arm_prints_one_json_line():
         assert key in d, key
     assert d["impl"] == "reference" and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["value"] > 0
+
+
+def test_cpu_oracle_rate_on_one_thread_and_a_pool():
+    # the CPU-baseline leg: the oracle timed on the workload's sequences, with
+    # the pool of host cores and on a single thread
+    import workloads
+    b = _bench()
+    w = workloads.make("b16_v32000_bf16", seed=1, device="cpu", B=2)
+    for threads in (1, 2):
+        rate, reps, el = b["cpu_oracle_rate"](w, 0.05, threads)
+        assert rate > 0 and reps >= 1 and el >= 0.05
+        assert abs(rate - reps * w.B * w.k / el) < 1e-9 * rate
