@@ -112,9 +112,10 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
  *     draft argmax), alpha is 1 or 0, the stop row emits its target argmax,
  *     no uniform is drawn, and row_stats holds (max L, max L).  A positive
  *     temperature is applied as the fp32 factor log2(e) / T; a temperature so
- *     small that a row's scaled logits overflow fp32 (|L| log2(e) / T above
- *     3.4e38: T below about 1e-37 for logits of size 30) makes the row's
- *     normaliser non-finite, and the sequence fails closed as invalid input.
+ *     small that a row's largest logit, scaled, overflows fp32
+ *     (|max L| log2(e) / T above 3.4e38: T below about 1e-37 when that logit
+ *     has size 30) makes the row's normaliser non-finite, and the sequence
+ *     fails closed as invalid input.
  *   gate_mode / threshold: the default mode and threshold of every sequence;
  *     threshold must lie in (0, 1] when gate_mode is SV_GATED_MU.
  *   gate_mode_per_seq [B] uint8 (0 plain, 1 gated) and threshold_per_seq [B]
