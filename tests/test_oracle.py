@@ -334,6 +334,27 @@ def test_null_row_ends_the_chain_and_samples_the_residual():
     assert out["alpha"][0, 0] == 0.0 and out["alpha"][0, 1] > 0.5
 
 
+def test_residual_without_mass_samples_p_and_is_reported():
+    # [M] names a fallback for a degenerate residual without defining it; the
+    # reading: when (p - mu)+ has no mass (mu = p), sample p with the same u1
+    # and report the sequence as degenerate.  Here p = q = mu = (1, 0) at
+    # threshold 1/2 and the offered token 1 has q = 0: a NULL row whose
+    # residual is empty, so token 0 (all of p) is emitted.
+    Lt = np.array([[[0.0, -np.inf], [0.0, -np.inf]]], dtype=np.float32)
+    Ld = np.array([[[0.0, -np.inf]]], dtype=np.float32)
+    out = O.verify(Lt, Ld, np.array([[1]], dtype=np.int32), 1.0, 1, 0.5)
+    assert out["accepted_len"][0] == 0 and out["flags"][0, 0] == O.FLAG_NULL
+    assert list(out["tokens"][0]) == [0, -1]
+    assert out["degenerate"][0] == 1
+    # an ordinary stop row is not degenerate
+    p = np.array([0.5, 0.5])
+    q = np.array([0.875, 0.125])
+    Lt = np.log(np.stack([p, p])).astype(np.float32)[None]
+    Ld = np.log(q).astype(np.float32)[None, None]
+    out = O.verify(Lt, Ld, np.array([[1]], dtype=np.int32), 1.0, 1, 0.5)
+    assert out["accepted_len"][0] == 0 and out["degenerate"][0] == 0
+
+
 def test_invalid_sequences_fail_closed():
     rng = np.random.default_rng(1)
     Lt, Ld = _random_case(rng, 5, 2)
@@ -703,6 +724,21 @@ def test_diagnostics_plain_ceiling_is_one_minus_total_variation():
     # min(a, b) >= a b on [0, 1]: rejection sampling accepts at least as often as sampler-match
     assert np.all(d["min_sum"] >= d["pq_sum"] - 1e-15)
     assert np.all(d["min_sum"] <= 1.0 + 1e-12)
+
+
+def test_diagnostics_argmax_rule_takes_the_first_largest_target_probability():
+    # [M] "The acceptance ceiling": the argmax rule accepts with q(argmax p);
+    # among equal largest p the first token is its argmax (the greedy tie rule)
+    with np.errstate(divide="ignore"):
+        Lt = np.log(np.array([[0.4, 0.4, 0.2], [0.4, 0.4, 0.2]]))[None].astype(np.float32)
+        Ld = np.log(np.array([[0.1, 0.6, 0.3]]))[None].astype(np.float32)
+    d = O.diagnostics(Lt, Ld, np.zeros((1, 1), dtype=np.int32), 1.0, 0, 0.5)
+    assert abs(d["argmax_q"][0, 0] - 0.1) < 1e-7
+    # the argmax control rule accepts only the first largest token
+    out = O.verify(Lt, Ld, np.array([[1]], dtype=np.int32), 1.0, 0, 0.5, rule=O.RULE_ARGMAX)
+    assert out["accepted_len"][0] == 0 and out["tokens"][0, 0] == 0
+    out = O.verify(Lt, Ld, np.array([[0]], dtype=np.int32), 1.0, 0, 0.5, rule=O.RULE_ARGMAX)
+    assert out["accepted_len"][0] == 1 and list(out["tokens"][0]) == [0, 0]
 
 
 def test_diagnostics_greedy_and_invalid_rows():

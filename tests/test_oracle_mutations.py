@@ -67,6 +67,28 @@ MUTATIONS = {
     "diagnostics_sum_max": [("smin += fmin(pj[v], S->mu[v]);", "smin += fmax(pj[v], S->mu[v]);")],
     # top-p keeping the prefix that passes top_p strictly
     "top_p_strict": [("if (c >= target) {", "if (c > target) {")],
+    # greedy rows one-hot at the last of equal largest logits
+    "greedy_last_max": [("      if (x > m) {\n        m = x;\n        best = v;",
+                         "      if (x >= m) {\n        m = x;\n        best = v;")],
+    # the argmax rule and diagnostics taking the last largest p
+    "argmax_last": [("if (p[v] > p[best]) best = v;", "if (p[v] >= p[best]) best = v;")],
+    # the argmax rule's acceptance read from p instead of q
+    "diagnostics_argmax_reads_p": [("J->diag_argq[o] = qj[argmax_first(pj, V)];",
+                                    "J->diag_argq[o] = pj[argmax_first(pj, V)];")],
+    # sampler-match's acceptance summed against mu instead of q
+    "diagnostics_pq_uses_mu": [("spq += pj[v] * qj[v];", "spq += pj[v] * S->mu[v];")],
+    # top-k dropping the tokens tied with its boundary token
+    "top_k_drops_ties": [("keep[rk[i].v] = rk[i].x >= xk;", "keep[rk[i].v] = i < top_k;")],
+    # min-p with a strict comparison
+    "min_p_strict": [("if (!(ratio >= min_p)) keep[rk[i].v] = 0;", "if (!(ratio > min_p)) keep[rk[i].v] = 0;")],
+    # a residual with no mass not reported as degenerate
+    "degenerate_unreported": [("if (J->degenerate) J->degenerate[b] = 1;", "if (J->degenerate) J->degenerate[b] = 0;")],
+    # the accept uniforms keyed on the local sequence index, without the offset
+    "sequence_offset_ignored": [("return oracle_uniform(J->seed, J->seq_offset + (uint64_t)b, (uint32_t)j, 0u);",
+                                 "return oracle_uniform(J->seed, (uint64_t)b, (uint32_t)j, 0u);")],
+    # position and draw swapped in the Philox counter
+    "counter_words_swapped": [("uint32_t ctr[4] = {(uint32_t)seq, pos, draw, (uint32_t)(seq >> 32)};",
+                               "uint32_t ctr[4] = {(uint32_t)seq, draw, pos, (uint32_t)(seq >> 32)};")],
 }
 
 
