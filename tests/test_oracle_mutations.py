@@ -14,6 +14,7 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -118,18 +119,28 @@ def _pins(lib):
 
 
 @pytest.fixture(scope="module")
-def gcc():
+def results(tmp_path_factory):
+    """Build every copy and run the pins against it, several at a time."""
     if shutil.which("gcc") is None:
         pytest.skip("gcc not found")
+    base = tmp_path_factory.mktemp("mutants")
+    names = ["unmutated"] + sorted(MUTATIONS)
+
+    def one(name):
+        return _pins(_build(base, name, MUTATIONS.get(name, [])))
+
+    with ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+        futures = {name: ex.submit(one, name) for name in names}
+        return {name: f.result() for name, f in futures.items()}
 
 
-def test_unmutated_copy_passes_every_pin(gcc, tmp_path):
-    r = _pins(_build(tmp_path, "unmutated", []))
+def test_unmutated_copy_passes_every_pin(results):
+    r = results["unmutated"]
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_planted_mistake_fails_a_pin(gcc, tmp_path, name):
-    r = _pins(_build(tmp_path, name, MUTATIONS[name]))
+def test_planted_mistake_fails_a_pin(results, name):
+    r = results[name]
     # 1 = a test failed (not a collection error, a crash or a timeout)
     assert r.returncode == 1, f"{name}: pins returned {r.returncode}\n" + r.stdout[-3000:] + r.stderr[-2000:]
