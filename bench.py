@@ -73,6 +73,8 @@ def parse():
                     help="time the closed-form acceptance diagnostics instead of verification")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--single-replays", type=int, default=60,
+                    help="cold single-call replays (L2 flushed before each) for the latency median")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of load (timed region plus untimed steps) seen by the clock sampler")
     return ap.parse_args()
@@ -381,6 +383,25 @@ def main():
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
+
+    # The K timed steps as CUDA graph replays: the same launches (programmatic
+    # dependent launches become programmatic edges of the graph), without the
+    # Python marshalling of each call in front of the device.  Graphs of at
+    # most 500 steps, replayed once each untimed first (upload).
+    graphs = []
+    first = 0
+    while first < args.steps:
+        n = min(500, args.steps - first)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(first, first + n):
+                step(i)
+        graphs.append(g)
+        first += n
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
     if ws > 1:
@@ -390,21 +411,61 @@ def main():
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    for g in graphs:
+        g.replay()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall
     if ws > 1:
         dist.barrier()
+    # the same K steps launched call by call from Python: device time, and the
+    # host's enqueue time per call (the loop returns before the device is done
+    # as long as the host keeps ahead of it)
+    ed0, ed1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ed0.record(stream)
+    t_host = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    t_host = time.perf_counter() - t_host
+    ed1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_direct = ed0.elapsed_time(ed1)
     # keep the GPU busy (untimed) until the sampler has seen ~1 s under load
     t_extra = time.perf_counter()
     while t_wall + (time.perf_counter() - t_extra) < args.clock_window:
-        for i in range(1000):
-            step(i)
+        for g in graphs:
+            g.replay()
         torch.cuda.synchronize(dev)
     sampler.stop()
     ms = ev0.elapsed_time(ev1)
+
+    # one call at a time, cold: a graph of one step per input copy, the L2
+    # flushed (a 2 x L2 buffer written) before each replay, the median of the
+    # replays' event-timed durations
+    single = None
+    if not args.diagnostics and args.single_replays > 0:
+        one_graphs = []
+        for s_ in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(s_)
+            one_graphs.append(g)
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        durs = []
+        for r in range(args.single_replays + 3):
+            flush.fill_(float(r))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            one_graphs[r % nsets].replay()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if r >= 3:
+                durs.append(e0.elapsed_time(e1))
+        del flush
+        single = {"median_us": 1e3 * statistics.median(durs), "min_us": 1e3 * min(durs),
+                  "replays": len(durs),
+                  "protocol": "CUDA graph of one call, L2 flushed (2 x L2 written) before each "
+                              "replay, CUDA events, median"}
 
     # the dominant kernel alone: the same K steps again, with CUDA events that
     # the library records around each stream-pass launch
@@ -506,6 +567,11 @@ def main():
                        "l2": f"inputs larger than L2: {nsets} rotated copies of "
                              f"{per_set / 1e6:.1f} MB logits",
                        "parallelism": f"replicas x{ws} (sequence shards)"},
+            "timing": {"steps": "CUDA graph replays of the K calls (graphs of <= 500 calls), "
+                                 "CUDA events around them",
+                       "ms_per_step_direct": ms_direct / args.steps,
+                       "host_enqueue_us_per_call": 1e6 * t_host / args.steps,
+                       "single_call": single},
             "logits_gbs": step_gbs,
             "logits_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
             "logits_frac_of_measured": step_gbs / peak,

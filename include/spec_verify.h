@@ -315,7 +315,14 @@ sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after
  * with their empty marker (a synchronous memset).  Make that first call
  * outside any stream capture.  What must hold before every call: every
  * candidate slot empty (all bits set) and every row-overflow flag zero; set-up
- * establishes it and every call that completes restores it.
+ * establishes it and every call that completes restores it.  A call that
+ * returns SV_ECUDA may have launched its first kernel and not its second, so
+ * it marks the device's set-up as undone: the next call on that device does
+ * the set-up again (after a cudaDeviceSynchronize, so outside any capture).
+ * A device reset (cudaDeviceReset) reloads the library's device code and so
+ * refills the buffer with zeros, which the library cannot detect: after a
+ * reset, reload the library (or restart the process) before calling this
+ * entry point again.
  *
  * Concurrency: all calls on a device share the one buffer, so they must not
  * overlap -- issue them on one stream or otherwise order them.  Two calls in

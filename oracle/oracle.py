@@ -99,6 +99,11 @@ def lib() -> ctypes.CDLL:
                                              ctypes.c_uint64, P, P, ctypes.c_int, P, P, P, P, P, P,
                                              P, P, P, ctypes.c_int]
         L.oracle_verify_filtered.restype = ctypes.c_int
+        L.oracle_pick_interval.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
+                                           ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+                                           ctypes.c_double, P, ctypes.c_int, ctypes.c_double, P, P, P,
+                                           ctypes.c_int, ctypes.c_int64, P, P, P, P]
+        L.oracle_pick_interval.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -218,6 +223,37 @@ def verify(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gate, tau, s
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out
+
+
+def pick_interval(Lt: np.ndarray, Ld: np.ndarray, D: np.ndarray, T: float, gated: int, tau: float,
+                  j: int, v: int, tau_sched=None, min_cum: float = 0.0, filters=None):
+    """Where token v lies in the distribution the stop row of ONE sequence
+    samples from when its chain stops at position j (``oracle_pick_interval``).
+
+    Lt [k+1, V], Ld [k, V] (float32, or uint16 bf16 bits), D [k].  Returns
+    (weight, lo, hi, gate_margin): r(v) / Z and the interval [C(v-1) / Z,
+    C(v) / Z) of the stop row's weights r, and the closest q_j(x) of a gated
+    stop row to a gate boundary (inf otherwise)."""
+    Lt = np.ascontiguousarray(Lt)
+    Ld = np.ascontiguousarray(Ld)
+    k1, V = Lt.shape
+    k = k1 - 1
+    if Ld.shape != (k, V):
+        raise ValueError(f"draft logits shape {Ld.shape} != {(k, V)}")
+    D = np.ascontiguousarray(D, dtype=np.int32).reshape(k)
+    sched = None if tau_sched is None else np.ascontiguousarray(tau_sched, dtype=np.float64).ravel()
+    n_sched = 0 if sched is None else int(sched.shape[0])
+    fk, fp, fm = _filter_arrays(filters)
+    out = np.zeros(4, dtype=np.float64)
+    P = ctypes.c_void_p
+    ptrs = [P(out.ctypes.data + 8 * i) for i in range(4)]
+    rc = lib().oracle_pick_interval(_ptr(Lt), _dtype_code(Lt), _ptr(Ld), _dtype_code(Ld), _ptr(D), k, V,
+                                    float(T), int(gated), float(tau), _ptr(sched), n_sched,
+                                    float(min_cum), _ptr(fk), _ptr(fp), _ptr(fm), int(j), int(v),
+                                    *ptrs)
+    if rc != 0:
+        raise ValueError("oracle_pick_interval rejected its arguments (or the row is invalid)")
+    return float(out[0]), float(out[1]), float(out[2]), float(out[3])
 
 
 def _filter_arrays(filters):

@@ -644,6 +644,96 @@ static void diagnose_one(const job_t* J, int b, scratch_t* S) {
   if (J->margin) J->margin[b] = marg;
 }
 
+/* ------------------------------------------- pick intervals (test aid) */
+
+/* Where token v lies in the distribution that a stop row samples from, so
+ * that a result computed in lower precision near a decision boundary can be
+ * judged: the chain of one sequence stops at position j, and the stop row
+ * samples, as in step 5 of verify_one, p_k (j = k, the ordinary bonus sample
+ * [S "Approach"]) or the positive part of p_j - mu_j, mu_j the retained
+ * measure of the gate at step j behind the drafted prefix D_0..D_{j-1} (plain
+ * mode mu_j = q_j [M "What changed"]), or p_j when that part has no mass.
+ * The weights are written out here once more, separately from verify_one, so
+ * that the two can be checked against each other. */
+int oracle_pick_interval(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                         int k, int64_t V, double T, int gated, double tau,
+                         const double* tau_sched, int n_sched, double min_cum,
+                         const int* top_k, const double* top_p, const double* min_p,
+                         int j, int64_t v, double* weight, double* lo, double* hi,
+                         double* gate_marg) {
+  if (k < 1 || k > ORACLE_MAX_K || V < 1 || !(T >= 0.0) || isinf(T)) return 1;
+  if (j < 0 || j > k || v < 0 || v >= V || !Lt || !Ld || !D || !weight || !lo || !hi) return 1;
+  if ((tdt != ORACLE_F32 && tdt != ORACLE_BF16) || (ddt != ORACLE_F32 && ddt != ORACLE_BF16)) return 1;
+  if ((top_k != NULL) != (top_p != NULL) || (top_k != NULL) != (min_p != NULL)) return 1;
+  if (tau_sched && n_sched < 1) return 1;
+  const uint8_t g = gated ? 1 : 0;
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.k = k;
+  J.V = V;
+  J.T = T;
+  J.gate = &g;
+  J.tau = &tau;
+  J.rule = ORACLE_RULE_MU;
+  J.tau_sched = tau_sched;
+  J.n_sched = n_sched;
+  J.min_cum = min_cum;
+  const int esz_t = tdt == ORACLE_BF16 ? 2 : 4, esz_d = ddt == ORACLE_BF16 ? 2 : 4;
+  double* pj = (double*)malloc((size_t)V * sizeof(double));
+  double* qi = (double*)malloc((size_t)V * sizeof(double));
+  double* mu = (double*)malloc((size_t)V * sizeof(double));
+  int bad = !pj || !qi || !mu;
+  double mx, lse;
+  /* the stop row's target distribution (filtered like the rows of verify_one) */
+  if (!bad) {
+    const char* row = (const char*)Lt + (int64_t)j * V * esz_t;
+    bad = oracle_softmax_row(row, tdt, V, T, pj, &mx, &lse);
+    if (!bad && top_k) bad = oracle_filtered_row(row, tdt, V, T, top_k[0], top_p[0], min_p[0], pj, NULL, NULL);
+  }
+  /* the draft rows up to the stop row: the prefix product of the drafted
+   * tokens' draft probabilities, and mu_j from q_j */
+  double cprev = 1.0;
+  for (int i = 0; !bad && i < k && i <= j; ++i) {
+    const char* row = (const char*)Ld + (int64_t)i * V * esz_d;
+    bad = oracle_softmax_row(row, ddt, V, T, qi, &mx, &lse);
+    if (!bad && top_k) bad = oracle_filtered_row(row, ddt, V, T, top_k[1], top_p[1], min_p[1], qi, NULL, NULL);
+    if (bad) break;
+    if (i < j) {
+      if (D[i] < 0 || (int64_t)D[i] >= V) bad = 1;
+      else cprev *= qi[D[i]];
+    }
+  }
+  double gm = INFINITY;
+  if (!bad) {
+    if (j < k) {
+      const double tau_j = step_threshold(&J, 0, j);
+      retained_measure(&J, gated, tau_j, cprev, qi, mu);
+      if (gated)
+        for (int64_t x = 0; x < V; ++x) gm = fmin(gm, gate_margin(&J, tau_j, cprev, qi[x]));
+      double mass = 0.0;
+      for (int64_t x = 0; x < V; ++x) mass += fmax(pj[x] - mu[x], 0.0);
+      if (mass > 0.0)
+        for (int64_t x = 0; x < V; ++x) mu[x] = fmax(pj[x] - mu[x], 0.0);
+      else
+        memcpy(mu, pj, (size_t)V * sizeof(double));  /* no residual mass: p itself */
+    } else {
+      memcpy(mu, pj, (size_t)V * sizeof(double));
+    }
+    /* mu now holds the stop row's weights; prefix sums in token order */
+    double Z = 0.0, below = 0.0;
+    for (int64_t x = 0; x < V; ++x) {
+      if (x == v) below = Z;
+      Z += mu[x];
+    }
+    *weight = mu[v] / Z;
+    *lo = below / Z;
+    *hi = (below + mu[v]) / Z;
+  }
+  if (gate_marg) *gate_marg = gm;
+  free(pj); free(qi); free(mu);
+  return bad ? 1 : 0;
+}
+
 /* ------------------------------------------------------------- batch */
 
 typedef struct {

@@ -209,6 +209,27 @@ int oracle_diagnostics(const void* Lt, int tdt, const void* Ld, int ddt, const i
                        double* min_sum, double* pq_sum, double* argmax_q, double* margin,
                        int nthreads);
 
+/*
+ * The interval of token v in the distribution that the stop row of one
+ * sequence samples from when its chain stops at position j (j = k: the bonus
+ * row p_k; else the residual (p_j - mu_j)+ with mu_j the retained measure of
+ * the gate at step j behind the drafted prefix, or p_j when the residual has
+ * no mass) -- for judging picks made in lower precision near a boundary.
+ * Lt [k+1, V], Ld [k, V] and D [k] are that sequence's rows and drafted
+ * tokens; gated / tau its gate; tau_sched, n_sched, min_cum and the filters
+ * as in oracle_verify_filtered.  With r those weights, Z = sum r and C the
+ * inclusive prefix sums in token order: *weight = r(v) / Z, *lo = C(v-1) / Z,
+ * *hi = C(v) / Z; *gate_marg (may be NULL) = the closest q_j(x) of a gated
+ * stop row to a gate boundary (INFINITY otherwise).  Returns 0, or 1 on bad
+ * arguments or an invalid row.
+ */
+int oracle_pick_interval(const void* Lt, int tdt, const void* Ld, int ddt, const int32_t* D,
+                         int k, int64_t V, double T, int gated, double tau,
+                         const double* tau_sched, int n_sched, double min_cum,
+                         const int* top_k, const double* top_p, const double* min_p,
+                         int j, int64_t v, double* weight, double* lo, double* hi,
+                         double* gate_marg);
+
 #ifdef __cplusplus
 }
 #endif

@@ -797,7 +797,10 @@ sv_status noalloc_setup(int dev, NoallocDevice** out) {
     if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&d.blocks_per_sm[1][1], d.fin_spread_smem);
     if (e != cudaSuccess) return SV_ECUDA;
     unsigned char* base = static_cast<unsigned char*>(p);
-    if (cudaMemset(base, 0xFF, kNaCandBytes) != cudaSuccess ||
+    // a set-up redone after a failed call: that call's kernels (if any ran)
+    // are finished before the slots and flags are reset
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemset(base, 0xFF, kNaCandBytes) != cudaSuccess ||
         cudaMemset(base + kNaCandBytes, 0, kNaOverBytes) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return SV_ECUDA;
@@ -853,8 +856,15 @@ extern "C" sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype
   h.cand_over = reinterpret_cast<unsigned*>(d->base + kNaCandBytes);
   h.part = reinterpret_cast<float2*>(d->base + kNaCandBytes + kNaOverBytes);
   h.xD = reinterpret_cast<float*>(d->base + kNaCandBytes + kNaOverBytes + part_bytes);
-  return spec_verify_run_ex(&h, target_logits, tdt, draft_logits, ddt, draft_tokens, B, temperature,
-                            gate_mode, threshold, gate_mode_per_seq, threshold_per_seq, seed, 0,
-                            nullptr, nullptr, accepted_len, tokens, accept_prob, flags, counters,
-                            nullptr, cuda_stream);
+  const sv_status rc = spec_verify_run_ex(&h, target_logits, tdt, draft_logits, ddt, draft_tokens, B,
+                                          temperature, gate_mode, threshold, gate_mode_per_seq,
+                                          threshold_per_seq, seed, 0, nullptr, nullptr, accepted_len,
+                                          tokens, accept_prob, flags, counters, nullptr, cuda_stream);
+  if (rc == SV_ECUDA) {
+    // a launch failed, possibly after the stream pass had written candidate
+    // slots that no finishing pass will empty: the next call sets up again
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    d->ready = false;
+  }
+  return rc;
 }

@@ -10,7 +10,12 @@ Comparison rules:
     number under 1e-5 of those draws (plus a small allowance for small
     samples); the residual / bonus pick over V tokens has V interval edges,
     so at large V many picks sit within 1e-6 of an edge whatever the
-    arithmetic -- those are reported, and mismatches among them bounded;
+    arithmetic -- those are counted and reported apart;
+  * every mismatch inside a band must be a result that is still correct to
+    within the band: a flipped decision only where that decision's draw lies
+    within 1e-6 of its boundary, and an emitted token only where it is a
+    valid pick of the oracle's own stop-row distribution, u1 within 1e-6 of
+    its interval (see _judge_boundary_mismatch);
   * acceptance probabilities agree within 1e-5 relative (fp32 against fp64),
     except on positions whose gated q(D) lies within 1e-6 of the threshold
     (there the NULL decision itself is a boundary case).
@@ -84,12 +89,80 @@ def gate_near_boundary(w: workloads.Workload, ref, idx=None, tau_sched=None, min
     return gate[:, None] & near
 
 
+def _judge_boundary_mismatch(w, i, b, g_len, g_tok, g_flags, ref, gate_near, u0, u1,
+                             tau_sched, min_cum, filters):
+    """Why a GPU result inside a boundary band differs from the oracle's, or
+    None when nothing explains it.  Sequence b (row i of the compared arrays):
+      * a flipped decision (a different stop position, or REJECT against NULL
+        at the same one) is explained only by that position's draw lying within
+        1e-6 of its boundary: |u0 - p/mu| where p/mu < 1, or a gate decision
+        within 1e-6 of its threshold;
+      * the token the GPU emits at its own stop position j must be a valid
+        pick of the oracle's stop-row distribution at j (the residual, or p for
+        the bonus row): weight > 0 and u1 within 1e-6 of the token's interval
+        [C(v-1)/Z, C(v)/Z) in fp64 -- unless a token of that row sits within
+        1e-6 of the gate (then the retained measure itself is a boundary case)
+        or a sampler filter decision of the sequence does (the kept set is)."""
+    gl, ol = int(g_len[i]), int(ref["accepted_len"][i])
+    if gl < 0 or ol < 0:
+        return None  # validity never depends on a draw
+    D = w.D[b].cpu().numpy()
+    if not np.array_equal(g_tok[i, :gl], D[:gl]):
+        return None
+    seed = w.philox_seed
+    kind = "pick"
+    # every decision the GPU took on its way to its stop position j: accepted
+    # before j, not accepted at j (when j < k).  The oracle decides position
+    # i by alpha_i = min(1, p/mu) (0 for NULL or p = 0): accept iff alpha_i > 0
+    # and u0 <= alpha_i.  A disagreement is a boundary case only if u0 lies
+    # within 1e-6 of alpha_i < 1, or the gate decision lies within 1e-6.
+    for j in range(min(gl + 1, w.k)):
+        a = float(ref["alpha"][i, j])
+        uj = float(u0[b, j]) if u0 is not None else O.uniform(seed, b, j, 0)
+        if (a > 0.0 and uj <= a) != (j < gl):
+            if not (gate_near[i, j] or (0.0 < a < 1.0 and abs(uj - a) < BOUNDARY)):
+                return None
+            kind = "decision"
+    # REJECT against NULL at the same stop position: the gate decision flipped
+    if g_flags is not None and gl == ol and gl < w.k and g_flags[i, gl] != ref["flags"][i, gl]:
+        if not gate_near[i, gl]:
+            return None
+        kind = "decision"
+    filt_near = ref.get("margin_filter", np.full(len(g_len), np.inf))[i] < BOUNDARY
+    gate_b = int(w.gate[b].item())
+    tau_b = float(w.tau[b].item())
+    Lt = workloads.to_numpy_logits(w.Lt[b:b + 1])[0]
+    Ld = workloads.to_numpy_logits(w.Ld[b:b + 1])[0]
+    v = int(g_tok[i, gl])
+    if not 0 <= v < w.V:
+        return None
+    wt, lo, hi, gm = O.pick_interval(Lt, Ld, D, w.T, gate_b, tau_b, gl, v, tau_sched=tau_sched,
+                                     min_cum=min_cum, filters=filters)
+    uj = float(u1[b]) if u1 is not None else O.uniform(seed, b, gl, 1)
+    if wt > 0.0 and (w.T == 0.0 or lo - BOUNDARY <= uj < hi + BOUNDARY):
+        return kind
+    if gm < BOUNDARY:
+        return "gate_row"
+    if filt_near:
+        return "filter"
+    return None
+
+
 def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what="", tau_sched=None,
-            min_cum=0.0):
-    """Assert parity; returns a dict of counts (compared, boundary, boundary_decision,
-    boundary_pick, boundary_mismatch, draws).  tau_sched / min_cum: the gate
-    policy both sides ran with."""
+            min_cum=0.0, filters=None, u0=None, u1=None):
+    """Assert parity; returns a dict of counts.  tau_sched / min_cum: the gate
+    policy both sides ran with; filters: their sampler filters; u0 [B, k] /
+    u1 [B]: explicit uniforms both sides were given (else the Philox draws,
+    keyed on the sequence's index in w).
+
+    Every sequence outside the boundary bands must match bit for bit.  Every
+    mismatch inside them must be explained (see _judge_boundary_mismatch).
+    Counts: compared, boundary (sequences with a draw within 1e-6 of a
+    boundary), boundary_decision / boundary_pick / boundary_filter (by the
+    kind of the closest draw), boundary_mismatch and its kinds, draws (accept
+    draws of the tested positions plus one pick per valid sequence)."""
     sel = slice(None) if idx is None else np.asarray(idx)
+    gidx = np.arange(w.B)[sel]
     g_len = got["accepted_len"].cpu().numpy()[sel]
     g_tok = got["tokens"].cpu().numpy()[sel]
     g_alpha = got["accept_prob"].cpu().numpy()[sel].astype(np.float64)
@@ -105,11 +178,20 @@ def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what="", tau_
         f"gpu len {g_len[bad[:3]]} tok {g_tok[bad[:3]]} | oracle len {ref['accepted_len'][bad[:3]]} "
         f"tok {ref['tokens'][bad[:3]]} margin {margin[bad[:3]]}")
     gate = w.gate.cpu().numpy()[sel].astype(bool)
-    keep = np.ones_like(g_alpha, dtype=bool)
-    if gate.any():
-        keep &= ~gate_near_boundary(w, ref, idx, tau_sched, min_cum)
+    near = gate_near_boundary(w, ref, idx, tau_sched, min_cum) if gate.any() else \
+        np.zeros_like(g_alpha, dtype=bool)
+    keep = ~near
     np.testing.assert_allclose(g_alpha[keep], ref["alpha"][keep], rtol=ALPHA_RTOL, atol=ALPHA_ATOL,
                                err_msg=what)
+    kinds = {"decision": 0, "pick": 0, "gate_row": 0, "filter": 0}
+    unexplained = []
+    for i in np.nonzero(~ok & mism)[0]:
+        kind = _judge_boundary_mismatch(w, i, int(gidx[i]), g_len, g_tok, g_flags, ref, near, u0, u1,
+                                        tau_sched, min_cum, filters)
+        if kind is None:
+            unexplained.append(int(gidx[i]))
+        else:
+            kinds[kind] += 1
     valid = ref["accepted_len"] >= 0
     tested = np.where(valid, np.minimum(ref["accepted_len"] + 1, w.k), 0)
     pick_bnd = ref["margin_pick"] < BOUNDARY
@@ -122,10 +204,13 @@ def compare(w: workloads.Workload, got: dict, ref: dict, idx=None, what="", tau_
                  boundary_decision=int(dec_bnd.sum()), boundary_pick=int(pick_bnd.sum()),
                  boundary_filter=int(filt_bnd.sum()),
                  boundary_mismatch=int((~ok & mism).sum()),
+                 mismatch_decision=kinds["decision"], mismatch_pick=kinds["pick"],
+                 mismatch_gate_row=kinds["gate_row"], mismatch_filter=kinds["filter"],
                  draws=int((tested + valid).sum()))
     print(f"[parity] {what}: {stats}")
+    assert not unexplained, (f"{what}: boundary-band mismatches the oracle does not explain, "
+                             f"sequences {unexplained[:8]}", stats)
     assert stats["boundary_decision"] <= 1e-5 * stats["draws"] + 2, (what, stats)
-    assert stats["boundary_mismatch"] <= 0.1 * max(stats["boundary"], 1) + 1, (what, stats)
     return stats
 
 

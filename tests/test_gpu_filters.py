@@ -67,7 +67,7 @@ def test_filter_parity(sv, dtype, V, name):
     ver.set_filters(ft, fd)
     out = _run(sv, ver, w, row_stats=True)
     ref = oracle_for(w, filters=(ft, fd))
-    st = compare(w, out, ref, what=f"filters {name} {dtype} V={V}")
+    st = compare(w, out, ref, what=f"filters {name} {dtype} V={V}", filters=(ft, fd))
     ok = ref["margin"] >= 1e-6
     rs = out["row_stats"].cpu().numpy().astype(np.float64)
     np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
@@ -135,7 +135,8 @@ def test_filter_full_size_128k(sv):
     for filt in (((50, 0.9, 0.0), (40, 0.95, 0.0)), ((0, 1.0, 0.01), (64, 1.0, 0.0))):
         ver.set_filters(*filt)
         out = _run(sv, ver, w)
-        st = compare(w, out, oracle_for(w, nthreads=16, filters=filt), what=f"128k filtered {filt}")
+        st = compare(w, out, oracle_for(w, nthreads=16, filters=filt), what=f"128k filtered {filt}",
+                     filters=filt)
         assert st["compared"] >= w.B // 2
     ver.close()
 
@@ -174,7 +175,8 @@ def test_filters_with_a_gate_policy(sv, dtype):
     ver.set_gate_policy(sched, cum)
     out = _run(sv, ver, w)
     ref = oracle_for(w, tau_sched=sched, min_cum=cum, filters=filt)
-    st = compare(w, out, ref, what=f"filters + policy {dtype}", tau_sched=sched, min_cum=cum)
+    st = compare(w, out, ref, what=f"filters + policy {dtype}", tau_sched=sched, min_cum=cum,
+                     filters=filt)
     assert st["compared"] >= B // 2
     assert int((ref["flags"] == 3).sum()) > 0  # the gate still bites on the filtered q
     ver.close()

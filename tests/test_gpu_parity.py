@@ -258,6 +258,49 @@ def test_full_size_configs(sv, name, B, sample):
     torch.cuda.empty_cache()
 
 
+# The call the benchmark times: uniform gate settings given as the scalar
+# arguments, so the host knows every row is on the candidate fast path and the
+# finishing kernel without the dense pass runs -- at full size, every sequence
+# of the 128K-vocabulary batch, and sampled sequences of the 262144-token one.
+SCALAR_FULL = [
+    ("b64_v128256_zipf_gated", None),
+    ("b1024_v262144_zipf_stress", 48),
+]
+
+
+@pytest.mark.parametrize("name,sample", SCALAR_FULL)
+def test_full_size_benchmarked_call_scalar_gate(sv, name, sample):
+    w = workloads.make(name, seed=1234, device="cuda")
+    cfg = workloads.CONFIGS[name]
+    assert cfg["gate"] == "gated"
+    ver = _verifier(sv, w)
+    cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
+    out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]),
+                  seed=w.philox_seed, counters=cnt)
+    torch.cuda.synchronize()
+    if sample is None:
+        ref = oracle_for(w, nthreads=16)
+        idx = None
+    else:
+        rng = np.random.default_rng(11)
+        idx = np.sort(rng.choice(w.B, size=sample, replace=False))
+        ref = oracle_for(w, idx=idx)
+    st = compare(w, out, ref, idx=idx, what=f"{name} scalar gate (benchmarked call)")
+    assert st["compared"] >= (w.B if idx is None else len(idx)) // 2
+    al = out["accepted_len"].cpu().numpy()
+    c = cnt.cpu().numpy()
+    assert np.all((al >= 0) & (al <= w.k)) and c[1] == al.sum() and c[6] == 0
+    # the same call repeated gives the same outputs (the workspace is restored)
+    again = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=float(cfg["tau"]),
+                    seed=w.philox_seed)
+    torch.cuda.synchronize()
+    for key in ("accepted_len", "tokens", "accept_prob", "flags"):
+        assert torch.equal(out[key], again[key]), key
+    ver.close()
+    del w
+    torch.cuda.empty_cache()
+
+
 # -------------------------------------------------------------- edge cases
 
 def test_invalid_inputs_fail_closed_without_trapping(sv):
@@ -376,8 +419,9 @@ def test_explicit_uniforms_probe_decisions(sv):
         u0 = torch.full((B, k), u0v, device="cuda")
         u1 = torch.full((B,), u1v, device="cuda")
         out = _run(sv, ver, w, u_accept=u0, u_residual=u1)
-        ref = oracle_for(w, u0=u0.double().cpu().numpy(), u1=u1.double().cpu().numpy())
-        compare(w, out, ref, what=f"u0={u0v} u1={u1v}")
+        u0n, u1n = u0.double().cpu().numpy(), u1.double().cpu().numpy()
+        ref = oracle_for(w, u0=u0n, u1=u1n)
+        compare(w, out, ref, what=f"u0={u0v} u1={u1v}", u0=u0n, u1=u1n)
     ver.close()
 
 

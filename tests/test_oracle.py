@@ -897,3 +897,93 @@ def test_filtered_row_statistics_and_diagnostics():
         a = O.verify(np.broadcast_to(Lt, (V, k + 1, V)), np.broadcast_to(Ld, (V, k, V)), D, 0.8, 0, 0.5,
                      filters=filt)["alpha"][:, j]
         assert abs((Q[j] * a).sum() - d["min_sum"][0, j]) < 1e-12
+
+
+# ------------------------------------------- pick intervals (judging near-boundary picks)
+
+def test_pick_interval_of_the_worked_example():
+    # Strata PR #3416, "Problem and result": p = (1/2, 1/2), q = (7/8, 1/8),
+    # threshold 1/2.  Stopping at position 0 the residual (p - mu)+ with
+    # mu = (7/8, 0) is (0, 1/2): token 1 takes all of [0, 1), token 0 nothing;
+    # the bonus row is p itself.
+    Lt, Ld = _worked_example_rows()
+    w0, lo0, hi0, _ = O.pick_interval(Lt, Ld, np.array([0]), 1.0, 1, 0.5, 0, 0)
+    w1, lo1, hi1, gm = O.pick_interval(Lt, Ld, np.array([0]), 1.0, 1, 0.5, 0, 1)
+    assert (w0, w1) == (0.0, 1.0) and (lo1, hi1) == (0.0, 1.0) and lo0 == hi0 == 0.0
+    assert abs(gm - 0.375) < 1e-9  # the closer of q = 7/8 and 1/8 to the threshold 1/2
+    wb, lob, hib, gmb = O.pick_interval(Lt, Ld, np.array([0]), 1.0, 1, 0.5, 1, 1)
+    assert abs(wb - 0.5) < 1e-12 and abs(lob - 0.5) < 1e-12 and hib == 1.0 and gmb == np.inf
+
+
+def _worked_example_rows():
+    p = np.array([0.5, 0.5])
+    q = np.array([0.875, 0.125])
+    return np.log(np.stack([p, p])).astype(np.float32), np.log(q)[None].astype(np.float32)
+
+
+PICK_CASES = [
+    # (V, k, T, gate, tau, sched, cum, filters)
+    (40, 3, 1.0, 0, 0.5, None, 0.0, None),
+    (40, 3, 0.7, 1, 0.3, None, 0.0, None),
+    (9, 2, 1.3, 1, 0.2, None, 0.0, None),
+    (60, 4, 1.0, 1, 0.5, [0.25, 0.1], 0.02, None),
+    (50, 2, 0.8, 0, 0.5, None, 0.0, ((5, 0.9, 0.0), (0, 0.95, 0.05))),
+    (30, 3, 0.0, 1, 0.5, None, 0.0, None),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PICK_CASES)))
+def test_pick_interval_holds_the_oracles_own_pick(case):
+    # A separately written restatement of the stop row's weights: for every
+    # sequence the emitted token's interval has weight and holds u1 (the same
+    # u1 the oracle drew), at the oracle's own stop position.
+    V, k, T, gate, tau, sched, cum, filt = PICK_CASES[case]
+    rng = np.random.default_rng(100 + case)
+    B = 60
+    Lt = (rng.normal(size=(B, k + 1, V)) * 2.0).astype(np.float32)
+    Ld = (Lt[:, :k] + rng.normal(size=(B, k, V))).astype(np.float32)
+    if T == 0.0:
+        Lt = np.round(Lt).astype(np.float32)
+        Ld = np.round(Ld).astype(np.float32)
+    D = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    # drafts often at a row's largest draft logit, so that gates pass and chains run on
+    D = np.where(rng.random((B, k)) < 0.6, np.argmax(Ld, axis=2), D).astype(np.int32)
+    out = O.verify(Lt, Ld, D, T, gate, tau, seed=77, tau_sched=sched, min_cum=cum, filters=filt)
+    for b in range(B):
+        j = int(out["accepted_len"][b])
+        v = int(out["tokens"][b, j])
+        u1 = O.uniform(77, b, j, 1)
+        w, lo, hi, _ = O.pick_interval(Lt[b], Ld[b], D[b], T, gate, tau, j, v, tau_sched=sched,
+                                       min_cum=cum, filters=filt)
+        assert w > 0.0, (b, j, v)
+        if T > 0.0:
+            assert lo - 1e-12 <= u1 < hi + 1e-12, (b, j, v, u1, lo, hi)
+
+
+@pytest.mark.parametrize("gate,j", [(0, 0), (1, 1), (1, 3)])
+def test_pick_intervals_tile_the_unit_interval(gate, j):
+    rng = np.random.default_rng(5 + j)
+    V, k = 25, 3
+    Lt = (rng.normal(size=(k + 1, V)) * 2.0).astype(np.float32)
+    Ld = (Lt[:k] + rng.normal(size=(k, V))).astype(np.float32)
+    D = np.argmax(Ld, axis=1).astype(np.int32)
+    iv = [O.pick_interval(Lt, Ld, D, 1.0, gate, 0.2, j, v) for v in range(V)]
+    w = np.array([x[0] for x in iv])
+    lo = np.array([x[1] for x in iv])
+    hi = np.array([x[2] for x in iv])
+    assert abs(w.sum() - 1.0) < 1e-12 and lo[0] == 0.0 and abs(hi[-1] - 1.0) < 1e-12
+    np.testing.assert_allclose(lo[1:], hi[:-1], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(hi - lo, w, rtol=0, atol=1e-15)
+    if j == k:  # the bonus row: the weights are p_k itself
+        np.testing.assert_allclose(w, softmax(Lt[k].astype(np.float64)), rtol=1e-12, atol=1e-15)
+
+
+def test_pick_interval_rejects_bad_arguments():
+    Lt, Ld = _worked_example_rows()
+    for j, v in ((-1, 0), (2, 0), (0, 2), (0, -1)):
+        with pytest.raises(ValueError):
+            O.pick_interval(Lt, Ld, np.array([0]), 1.0, 1, 0.5, j, v)
+    bad = Lt.copy()
+    bad[0, 0] = np.nan
+    with pytest.raises(ValueError):
+        O.pick_interval(bad, Ld, np.array([0]), 1.0, 1, 0.5, 0, 1)

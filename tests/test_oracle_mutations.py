@@ -87,6 +87,11 @@ MUTATIONS = {
     # the accept uniforms keyed on the local sequence index, without the offset
     "sequence_offset_ignored": [("return oracle_uniform(J->seed, J->seq_offset + (uint64_t)b, (uint32_t)j, 0u);",
                                  "return oracle_uniform(J->seed, (uint64_t)b, (uint32_t)j, 0u);")],
+    # the pick interval's upper end without the token's own weight
+    "pick_interval_without_own_weight": [("*hi = (below + mu[v]) / Z;", "*hi = below / Z;")],
+    # the pick interval's gated residual built from q instead of mu
+    "pick_interval_residual_from_q": [("retained_measure(&J, gated, tau_j, cprev, qi, mu);",
+                                       "memcpy(mu, qi, (size_t)V * sizeof(double));")],
     # position and draw swapped in the Philox counter
     "counter_words_swapped": [("uint32_t ctr[4] = {(uint32_t)seq, pos, draw, (uint32_t)(seq >> 32)};",
                                "uint32_t ctr[4] = {(uint32_t)seq, draw, pos, (uint32_t)(seq >> 32)};")],
