@@ -525,11 +525,7 @@ sv_status prepare_params(spec_verify_t h, const void* target_logits, sv_dtype td
   P.xD = h->xD;
   P.cand = h->cand;
   P.cand_over = h->cand_over;
-  P.units_per_row = static_cast<unsigned>((h->nchunk + sv::kUnitChunks - 1) / sv::kUnitChunks);
-  P.div_units = sv::make_fastdiv(P.units_per_row);
-  const long long units = static_cast<long long>(B) * P.rows * P.units_per_row;
-  if (units >= (1ll << 31)) return SV_EUNSUPPORTED;
-  P.total_units = static_cast<unsigned>(units);
+  P.total_units = static_cast<unsigned>((total + sv::kUnitChunks - 1) / sv::kUnitChunks);
   P.err = h->err + (h->calls & 1u);
   P.err_next = h->err + ((h->calls + 1u) & 1u);
   P.wait_limit = h->wait_limit;

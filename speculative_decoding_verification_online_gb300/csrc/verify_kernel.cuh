@@ -129,12 +129,10 @@ struct Params {
   // finishing grid: CTAs [0, fin_warm) run the finishing code once, writing
   // nothing, while the stream pass drains (see finish_kernel)
   int fin_warm;
-  // work units of the dynamic stream pass (see stream_kernel): kUnitChunks
-  // chunks of one row each, units_per_row per row, unit u of row g = u / units_per_row
+  // work units of the dynamic stream pass (see stream_kernel): unit u is the
+  // chunks [kUnitChunks u, kUnitChunks (u + 1)) of the sequence-major order
   int dyn;                 // the stream pass ran with dynamic units (the finisher checks err)
-  unsigned units_per_row;
-  FastDiv div_units;       // by units_per_row
-  unsigned total_units;    // B * rows * units_per_row
+  unsigned total_units;    // ceil(total_chunks / kUnitChunks)
   // workspace words of alternate calls: err (this call's) is set when the
   // stream pass gave up a wait; the stream pass clears err_next, the next
   // call's, which no kernel still running can be reading
@@ -493,8 +491,8 @@ struct Stages {
 
 constexpr int kItemRing = 8;       // decoded chunks known to a warp (in flight or next)
 constexpr unsigned kNoWork = 0xffffffffu;
-constexpr int kUnitChunks = 16;    // chunks of one row per work unit of the dynamic stream pass
-constexpr int kClcRing = 8;        // unit requests a CTA keeps track of (slots s % kClcRing)
+constexpr int kUnitChunks = 16;    // consecutive chunks per work unit of the dynamic stream pass
+constexpr int kClcRing = 8;        // unit requests a CTA keeps track of (a ring of answers)
 constexpr unsigned kDefaultWaitLimit = 1u << 24;
 
 struct WarpQueue {
@@ -528,8 +526,7 @@ __device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot
 // ---- dynamic work units (cluster launch control)
 //
 // The verifying stream pass is launched with one CTA per work unit: kUnitChunks
-// consecutive chunks of one row, units in the sequence-major order of the
-// chunks.  As many CTAs as fit start (one per SM); each processes its own unit
+// consecutive chunks in the sequence-major order of the chunks.  As many CTAs as fit start (one per SM); each processes its own unit
 // and then takes further units from CTAs that have not started yet, by
 // cancelling them (clusterlaunchcontrol.try_cancel): the hardware answers each
 // request with the index of the cancelled CTA, whose unit the requester then
@@ -541,14 +538,17 @@ __device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot
 // counter n: slot s = n / kUnitChunks is the CTA's s-th unit (slot 0 its own),
 // and the claimer of a slot's first chunk requests the next slot's unit.  One
 // request is in flight at a time, issued only after the previous one
-// succeeded.  Request s uses ring entry s % kClcRing (a 16-byte answer and an
-// mbarrier whose phase s / kClcRing completes with it); every claimer of slot
-// s reads the answer right after its claim, and the claims of slot s +
-// kClcRing come at least 16 (kClcRing - 1) claims later, so an entry is never
-// overwritten before its readers are done with it.
+// succeeded.  The unit of slot s >= 1 comes from request t = s - 1 (requests
+// are numbered from 0: slot 0 needs none), which uses ring entry t % kClcRing
+// -- a 16-byte answer and an mbarrier whose phase t / kClcRing completes with
+// it, so the wait is on parity (t / kClcRing) & 1.  Every claimer of slot s
+// reads the answer right after its claim, and the claims of the slot that
+// reuses the entry come at least kUnitChunks (kClcRing - 1) claims later, so
+// an entry is never overwritten before its readers are done with it.
 //
-// Every wait is bounded (P.wait_limit iterations).  A wait that gives up sets
-// the call's error word and stops the CTA taking work; a unit may then be
+// Every wait is bounded (P.wait_limit iterations, and it ends early once any
+// CTA has given up).  A wait that gives up sets the call's error word and
+// stops the CTA taking work; a unit may then be
 // lost, so the finishing pass fails every sequence of the call closed
 // (accepted_len = -1).  Calls alternate between two error words, and every
 // stream CTA clears the next call's word once the previous kernel (the
@@ -575,10 +575,15 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
   return done != 0;
 }
 
-// bounded wait for the phase of the given parity to complete
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity, unsigned limit) {
-  for (unsigned it = 0; it < limit; ++it)
+// bounded wait for the phase of the given parity to complete; it also ends
+// (false) once *err is set, checked every 1024 tries, so that one CTA giving
+// up ends every other CTA's waits quickly
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity, unsigned limit,
+                                                  const unsigned* err) {
+  for (unsigned it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 1023u) == 1023u && err && *reinterpret_cast<const volatile unsigned*>(err) != 0u) return false;
+  }
   return false;
 }
 
@@ -597,10 +602,14 @@ __device__ __forceinline__ void clc_give_up(const Params& P, ClcState& C) {
   atomicOr(P.err, 1u);
 }
 
+// ring entry and phase parity of the request for slot s >= 1
+__device__ __forceinline__ int clc_entry(int s) { return (s - 1) % kClcRing; }
+__device__ __forceinline__ unsigned clc_parity(int s) { return static_cast<unsigned>(((s - 1) / kClcRing) & 1); }
+
 // lane 0: request the unit of slot s (slot s - 1 is known to have one)
 __device__ __forceinline__ void clc_request(ClcState& C, int s) {
   if (C.abort) return;
-  const int e = s % kClcRing;
+  const int e = clc_entry(s);
   const unsigned bar = smem_u32(&C.bar[e]);
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;" ::"r"(bar) : "memory");
   asm volatile(
@@ -619,17 +628,18 @@ __device__ __forceinline__ int clc_slot_unit(const Params& P, ClcState& C, int s
   for (unsigned it = 0;; ++it) {
     if (C.abort || s >= C.failed) return -1;
     if (C.issued >= s) break;
-    if (it >= limit) {
+    if (it >= limit ||
+        ((it & 1023u) == 1023u && *reinterpret_cast<const volatile unsigned*>(P.err) != 0u)) {
       clc_give_up(P, C);
       return -1;
     }
     __nanosleep(32);
   }
-  const int e = s % kClcRing;
+  const int e = clc_entry(s);
   const bool stall = P.test_stall && s == 1;
   const unsigned bar = smem_u32(stall ? &C.stall_bar : &C.bar[e]);
-  const unsigned parity = stall ? 0u : static_cast<unsigned>((s / kClcRing) & 1);
-  if (!mbar_wait_bounded(bar, parity, limit)) {
+  const unsigned parity = stall ? 0u : clc_parity(s);
+  if (!mbar_wait_bounded(bar, parity, limit, P.err)) {
     clc_give_up(P, C);
     return -1;
   }
@@ -659,10 +669,9 @@ __device__ __forceinline__ unsigned next_chunk_dyn(const Params& P, unsigned* ct
     const int unit = s == 0 ? static_cast<int>(blockIdx.x) : clc_slot_unit(P, C, s);
     if (unit < 0) return kNoWork;
     if (c == 0) clc_request(C, s + 1);  // this slot has a unit: ask for the next one
-    const unsigned g = fastdiv(static_cast<unsigned>(unit), P.div_units);
-    const unsigned ch = (static_cast<unsigned>(unit) - g * P.units_per_row) * kUnitChunks + c;
-    if (ch < static_cast<unsigned>(P.nchunk)) return g * static_cast<unsigned>(P.nchunk) + ch;
-    // the row's last unit is shorter: claim again
+    const unsigned x = static_cast<unsigned>(unit) * kUnitChunks + c;
+    if (x < P.total_chunks) return x;
+    // past the end of the last (shorter) unit: claim again
   }
 }
 
@@ -672,8 +681,7 @@ __device__ __forceinline__ unsigned next_chunk_dyn(const Params& P, unsigned* ct
 __device__ __forceinline__ void clc_drain(const Params& P, ClcState& C) {
   const int s = C.issued;
   if (s < 1) return;
-  if (!mbar_wait_bounded(smem_u32(&C.bar[s % kClcRing]), static_cast<unsigned>((s / kClcRing) & 1),
-                         kDefaultWaitLimit))
+  if (!mbar_wait_bounded(smem_u32(&C.bar[clc_entry(s)]), clc_parity(s), kDefaultWaitLimit, nullptr))
     clc_give_up(P, C);
 }
 
