@@ -42,10 +42,7 @@
  * sees -- a draft token outside [0, V), a row with a NaN or +inf logit or with
  * every logit -inf, a per-sequence threshold outside (0, 1] -- never trap: that
  * sequence gets accepted_len = -1, tokens = -1, flags = SV_FLAG_INVALID,
- * accept_prob = 0, and counters[SV_CNT_INVALID] is incremented.  Every wait
- * inside the kernels is bounded: should one give up (the stream pass's
- * requests for work units, see spec_verify_set_test_hooks), every sequence of
- * that call fails closed the same way; no kernel hangs or traps.
+ * accept_prob = 0, and counters[SV_CNT_INVALID] is incremented.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -245,21 +242,6 @@ sv_status spec_verify_run_host(spec_verify_t h,
 sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, int n_schedule,
                                       float min_cum);
 
-/* Test hook of the bounded waits (not for normal use).  The verifying stream
- * pass hands out its work in units that its CTAs request from the hardware
- * (cluster launch control: a running CTA cancels a CTA that has not started
- * and processes that CTA's unit); each wait for an answer, or for the request
- * to be issued, gives up after wait_limit iterations (0 = the default,
- * 2^24, far beyond any answer's latency).  A wait that gives up may lose a
- * unit of work, so every sequence of that call then fails closed
- * (accepted_len = -1, flags SV_FLAG_INVALID, counters[SV_CNT_INVALID] + 1 per
- * sequence); the next call is unaffected.  stall_first_request != 0 makes each
- * CTA's first wait for an answer wait on a barrier that nothing completes, so
- * that a test can watch the limit run out (with a small wait_limit) without
- * anything faulting or hanging.  Applies to later calls on the handle.
- * Returns SV_EINVAL for a NULL handle. */
-sv_status spec_verify_set_test_hooks(spec_verify_t h, unsigned wait_limit, int stall_first_request);
-
 /* Sampler filters of the target rows (p) and the draft rows (q) of every later
  * call on this handle: mlxcel PR #992, "What changed" -- the effective
  * distribution is the sampler's own chain: temperature, top-k, top-p, min-p,
@@ -324,7 +306,7 @@ sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after
  *   B * k * ceil(V / 2048) * 4 <= SV_NOALLOC_MAX_CAND_SLOTS
  *   B * k                      <= SV_NOALLOC_MAX_ROWS
  *   B * (2k+1) * ceil(V / 2048) * 8 + B * (2k+1) * 4 (each rounded up to 256)
- *                              <= SV_NOALLOC_STATS_BYTES - 256
+ *                              <= SV_NOALLOC_STATS_BYTES
  * (B = 64, k = 5, V = 128256 uses 80,640 slots and 0.36 MiB of statistics;
  * B = 256, k = 8, V = 151936 does not fit.)
  *

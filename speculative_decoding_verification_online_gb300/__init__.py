@@ -11,6 +11,6 @@ from .spec_verify import (  # noqa: F401
     SV_FLAG_UNREACHED, SV_GATED_MU, SV_PLAIN, SpecVerifier, SpecVerifyError, load,
     spec_verify_diagnostics, spec_verify_free, spec_verify_init, spec_verify_launches_per_run, spec_verify_mark_next,
     spec_verify_run, spec_verify_run_ex, spec_verify_run_host, spec_verify_run_noalloc,
-    spec_verify_set_filters, spec_verify_set_gate_policy, spec_verify_set_test_hooks, spec_verify_status_string, run_noalloc,
+    spec_verify_set_filters, spec_verify_set_gate_policy, spec_verify_status_string, run_noalloc,
     spec_verify_launches_per_filtered_run)
 from .metrics import acceptance_summary, rule_id, summary_line  # noqa: F401,E402

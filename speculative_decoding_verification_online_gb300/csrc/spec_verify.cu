@@ -28,11 +28,6 @@ struct spec_verify_s {
   sv::Cand* cand = nullptr;
   unsigned* cand_over = nullptr;
   sv::DiagNorm* dnorm = nullptr;  // [max_B, k] (diagnostics)
-  unsigned* err = nullptr;        // [2]: error words of alternate calls (see stream_kernel)
-  unsigned calls = 0;             // calls made, for the alternation
-  // bounded waits of the dynamic stream pass (spec_verify_set_test_hooks)
-  unsigned wait_limit = sv::kDefaultWaitLimit;
-  int test_stall = 0;
   // one-shot timing marks around the next stream pass
   cudaEvent_t mark_before = nullptr, mark_after = nullptr;
   // staging for spec_verify_run_host (allocated on first use)
@@ -89,7 +84,7 @@ int finish_spread_smem(int device) {
 
 template <typename TT, typename TD, int G>
 cudaError_t configure_one(int fin_spread_smem) {
-  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G, true>,
+  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
   const int fin = static_cast<int>(sizeof(sv::FinishShared));
@@ -110,10 +105,7 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
   if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>(fin_spread_smem);
   if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>(fin_spread_smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeStats, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeGreedy, false>,
+    e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeStats>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sv::pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -123,7 +115,7 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
                              static_cast<int>(sizeof(sv::SelShared)));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                       sv::stream_kernel<TT, TD, sv::kModeStats, false>,
+                                                       sv::stream_kernel<TT, TD, sv::kModeSample>,
                                                        sv::Stages<TT, TD>::kThreadsPerCta,
                                                        dyn_smem<TT, TD>());
 }
@@ -147,22 +139,20 @@ cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// the stream pass (variant G; kDyn: one CTA per work unit, see stream_kernel),
-// with the handle's one-shot timing marks around it
-template <typename TT, typename TD, int G, bool kDyn>
+// the stream pass (variant G), with the handle's one-shot timing marks around it
+template <typename TT, typename TD, int G>
 sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
   const long long need = (static_cast<long long>(P.total_chunks) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
                          sv::Stages<TT, TD>::kWarpsPerCta;
   if (grid > need) grid = need;
-  if (kDyn) grid = P.total_units;
   if (grid < 1) grid = 1;
   const bool marked = h->mark_before != nullptr;
   if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
   // a programmatic dependent launch: resident early, it waits for the previous
   // kernel in the stream before touching memory
-  if (launch_dependent(sv::stream_kernel<TT, TD, G, kDyn>, static_cast<unsigned>(grid),
+  if (launch_dependent(sv::stream_kernel<TT, TD, G>, static_cast<unsigned>(grid),
                        sv::Stages<TT, TD>::kThreadsPerCta, dyn_smem<TT, TD>(), st, P) != cudaSuccess)
     return SV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
@@ -177,7 +167,7 @@ sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm,
 template <typename TT, typename TD, int G>
 sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
                  cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, G, true>(h, P, blocks_per_sm, st);
+  const sv_status rs = launch_stream<TT, TD, G>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   // the finishing pass: one CTA per sequence, allowed to launch while the
   // stream pass drains; it waits (griddepcontrol.wait) before reading its output
@@ -199,7 +189,6 @@ sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool d
   // warming CTAs in front of single-CTA clusters, while every CTA still has
   // an SM slot at once (two per SM)
   sv::Params Pf = P;
-  Pf.dyn = 1;
   Pf.fin_warm = csize == 1 && clusters + kFinWarm <= 2 * h->num_sms ? kFinWarm : 0;
   const int grid = clusters * csize + Pf.fin_warm;
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -246,8 +235,7 @@ sv_status launch_mode(spec_verify_t h, const sv::Params& P, int bps, bool dense_
 template <typename TT, typename TD, bool kGreedy>
 sv_status launch_diag(spec_verify_t h, const sv::Params& P, int blocks_per_sm, float* min_sum,
                       float* pq_sum, float* argmax_q, cudaStream_t st) {
-  const sv_status rs =
-      launch_stream<TT, TD, kGreedy ? sv::kModeGreedy : sv::kModeStats, false>(h, P, blocks_per_sm, st);
+  const sv_status rs = launch_stream<TT, TD, kGreedy ? sv::kModeGreedy : sv::kModeStats>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned npos = static_cast<unsigned>(P.B * P.k);
   const unsigned small_grid = (npos + sv::kDiagWarps - 1) / sv::kDiagWarps;
@@ -298,7 +286,7 @@ sv_status launch_filters(spec_verify_t h, sv::Params& P, int blocks_per_sm, cuda
   F.first = reinterpret_cast<int*>(base + o_first);
   F.Lt_m = base + o_t;
   F.Ld_m = base + o_d;
-  sv_status rs = launch_stream<TT, TD, sv::kModeStats, false>(h, P, blocks_per_sm, st);
+  sv_status rs = launch_stream<TT, TD, sv::kModeStats>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
   if (launch_dependent(sv::select_kernel<TT, TD>, nrows, sv::kSelThreads, sizeof(sv::SelShared), st, P, F) !=
@@ -413,7 +401,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   const size_t o_cd = off;   off = align_up(off + n_cand * sizeof(sv::Cand), 256);
   const size_t o_co = off;   off = align_up(off + n_rowc * sizeof(unsigned), 256);
   const size_t o_dn = off;   off = align_up(off + n_rowc * sizeof(sv::DiagNorm), 256);
-  const size_t o_err = off;  off = align_up(off + 2 * sizeof(unsigned), 256);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     delete h;
     return SV_ENOMEM;
@@ -425,7 +412,6 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
   h->cand = reinterpret_cast<sv::Cand*>(base + o_cd);
   h->cand_over = reinterpret_cast<unsigned*>(base + o_co);
   h->dnorm = reinterpret_cast<sv::DiagNorm*>(base + o_dn);
-  h->err = reinterpret_cast<unsigned*>(base + o_err);
   // everything starts at zero except the candidate slots, which start empty
   // (all bits set: token id -1); the finishing pass restores both after use
   if (cudaMemset(h->ws, 0, off) != cudaSuccess ||
@@ -525,11 +511,6 @@ sv_status prepare_params(spec_verify_t h, const void* target_logits, sv_dtype td
   P.xD = h->xD;
   P.cand = h->cand;
   P.cand_over = h->cand_over;
-  P.total_units = static_cast<unsigned>((total + sv::kUnitChunks - 1) / sv::kUnitChunks);
-  P.err = h->err + (h->calls & 1u);
-  P.err_next = h->err + ((h->calls + 1u) & 1u);
-  P.wait_limit = h->wait_limit;
-  P.test_stall = h->test_stall;
   const size_t row_t = static_cast<size_t>(V) * elem_size(tdt);
   const size_t row_d = static_cast<size_t>(V) * elem_size(ddt);
   P.vec_t = (row_t % 16 == 0) && (reinterpret_cast<uintptr_t>(target_logits) % 16 == 0);
@@ -558,7 +539,6 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   if (!accepted_len || !tokens || !accept_prob) return SV_EINVAL;
   DeviceGuard g(h->device);
   if (!g.ok) return SV_ECUDA;
-  ++h->calls;  // the next call uses the other error word
   P.seed = seed;
   P.seq_offset = seq_offset;
   P.u0 = u_accept;
@@ -733,13 +713,6 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
   return SV_OK;
 }
 
-sv_status spec_verify_set_test_hooks(spec_verify_t h, unsigned wait_limit, int stall_first_request) {
-  if (!h) return SV_EINVAL;
-  h->wait_limit = wait_limit == 0 ? sv::kDefaultWaitLimit : wait_limit;
-  h->test_stall = stall_first_request ? 1 : 0;
-  return SV_OK;
-}
-
 sv_status spec_verify_set_filters(spec_verify_t h, int top_k_t, float top_p_t, float min_p_t, int top_k_d,
                                   float top_p_d, float min_p_d) {
   if (!h) return SV_EINVAL;
@@ -781,8 +754,7 @@ sv_status spec_verify_free(spec_verify_t h) {
 // from one call to the next whatever the shapes):
 //   [0, 4 MiB)                  candidate slots, all bits set when empty
 //   [4 MiB, 4 MiB + 64 KiB)     row-overflow flags, zero when clear
-//   [4 MiB + 64 KiB, 8 MiB - 256) chunk statistics, then drafted-token logits
-//   [8 MiB - 256, 8 MiB)        the stream pass's two error words, zero when clear
+//   [4 MiB + 64 KiB, 8 MiB)     chunk statistics, then drafted-token logits
 // The finishing pass empties every slot and clears every flag it reads, so a
 // completed call leaves the buffer as set-up left it.  Calls on one device
 // share the buffer and must not overlap.
@@ -797,11 +769,8 @@ static_assert(kNaCandBytes + kNaOverBytes + SV_NOALLOC_STATS_BYTES == SV_NOALLOC
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
 
-constexpr size_t kNaErrOffset = SV_NOALLOC_SCRATCH_BYTES - 256;
-
 struct NoallocDevice {
   bool ready = false;
-  unsigned calls = 0;             // calls made on this device, for the error-word alternation
   unsigned char* base = nullptr;  // device address of g_noalloc_scratch on this device
   int num_sms = 0;
   int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};
@@ -833,7 +802,6 @@ sv_status noalloc_setup(int dev, NoallocDevice** out) {
     if (cudaDeviceSynchronize() != cudaSuccess ||
         cudaMemset(base, 0xFF, kNaCandBytes) != cudaSuccess ||
         cudaMemset(base + kNaCandBytes, 0, kNaOverBytes) != cudaSuccess ||
-        cudaMemset(base + kNaErrOffset, 0, 256) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess)
       return SV_ECUDA;
     d.base = base;
@@ -863,7 +831,7 @@ extern "C" sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype
   const size_t part_bytes = align_up(static_cast<size_t>(B) * rows * nchunk * sizeof(float2), 256);
   const size_t xd_bytes = align_up(static_cast<size_t>(B) * rows * sizeof(float), 256);
   if (slots > SV_NOALLOC_MAX_CAND_SLOTS || static_cast<size_t>(B) * k > SV_NOALLOC_MAX_ROWS ||
-      part_bytes + xd_bytes > SV_NOALLOC_STATS_BYTES - 256)
+      part_bytes + xd_bytes > SV_NOALLOC_STATS_BYTES)
     return SV_EUNSUPPORTED;
   if (B == 0) return SV_OK;
   int dev = -1;
@@ -888,11 +856,6 @@ extern "C" sv_status spec_verify_run_noalloc(const void* target_logits, sv_dtype
   h.cand_over = reinterpret_cast<unsigned*>(d->base + kNaCandBytes);
   h.part = reinterpret_cast<float2*>(d->base + kNaCandBytes + kNaOverBytes);
   h.xD = reinterpret_cast<float*>(d->base + kNaCandBytes + kNaOverBytes + part_bytes);
-  h.err = reinterpret_cast<unsigned*>(d->base + kNaErrOffset);
-  {
-    std::lock_guard<std::mutex> lock(g_na_mutex);
-    h.calls = d->calls++;
-  }
   const sv_status rc = spec_verify_run_ex(&h, target_logits, tdt, draft_logits, ddt, draft_tokens, B,
                                           temperature, gate_mode, threshold, gate_mode_per_seq,
                                           threshold_per_seq, seed, 0, nullptr, nullptr, accepted_len,

@@ -129,17 +129,6 @@ struct Params {
   // finishing grid: CTAs [0, fin_warm) run the finishing code once, writing
   // nothing, while the stream pass drains (see finish_kernel)
   int fin_warm;
-  // work units of the dynamic stream pass (see stream_kernel): unit u is the
-  // chunks [kUnitChunks u, kUnitChunks (u + 1)) of the sequence-major order
-  int dyn;                 // the stream pass ran with dynamic units (the finisher checks err)
-  unsigned total_units;    // ceil(total_chunks / kUnitChunks)
-  // workspace words of alternate calls: err (this call's) is set when the
-  // stream pass gave up a wait; the stream pass clears err_next, the next
-  // call's, which no kernel still running can be reading
-  unsigned* err;
-  unsigned* err_next;
-  unsigned wait_limit;     // iterations of a bounded wait before it gives up
-  int test_stall;          // test hook: the first unit request waits on a barrier nobody arms
 };
 
 // ---------------------------------------------------------------- helpers
@@ -491,9 +480,6 @@ struct Stages {
 
 constexpr int kItemRing = 8;       // decoded chunks known to a warp (in flight or next)
 constexpr unsigned kNoWork = 0xffffffffu;
-constexpr int kUnitChunks = 16;    // consecutive chunks per work unit of the dynamic stream pass
-constexpr int kClcRing = 8;        // unit requests a CTA keeps track of (a ring of answers)
-constexpr unsigned kDefaultWaitLimit = 1u << 24;
 
 struct WarpQueue {
   int4 item[kItemRing];  // (b, r, ch, 1) of a chunk to stream; w = 0: no more work
@@ -521,168 +507,6 @@ __device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot
   Q.item[slot] = make_int4(static_cast<int>(b), r, ch, 1);
   const int j = r <= P.k ? r : r - P.k - 1;
   if (j < P.k) cp_async4(&Q.d[slot], P.D + static_cast<int64_t>(b) * P.k + j);
-}
-
-// ---- dynamic work units (cluster launch control)
-//
-// The verifying stream pass is launched with one CTA per work unit: kUnitChunks
-// consecutive chunks in the sequence-major order of the chunks.  As many CTAs as fit start (one per SM); each processes its own unit
-// and then takes further units from CTAs that have not started yet, by
-// cancelling them (clusterlaunchcontrol.try_cancel): the hardware answers each
-// request with the index of the cancelled CTA, whose unit the requester then
-// processes, or with a failure once every CTA of the grid has started or been
-// cancelled.  Faster SMs so take more units and the SMs finish close
-// together; no global atomics are involved.
-//
-// Inside a CTA the warps still take chunks one at a time from a shared-memory
-// counter n: slot s = n / kUnitChunks is the CTA's s-th unit (slot 0 its own),
-// and the claimer of a slot's first chunk requests the next slot's unit.  One
-// request is in flight at a time, issued only after the previous one
-// succeeded.  The unit of slot s >= 1 comes from request t = s - 1 (requests
-// are numbered from 0: slot 0 needs none), which uses ring entry t % kClcRing
-// -- a 16-byte answer and an mbarrier whose phase t / kClcRing completes with
-// it, so the wait is on parity (t / kClcRing) & 1.  Every claimer of slot s
-// reads the answer right after its claim, and the claims of the slot that
-// reuses the entry come at least kUnitChunks (kClcRing - 1) claims later, so
-// an entry is never overwritten before its readers are done with it.
-//
-// Every wait is bounded (P.wait_limit iterations, and it ends early once any
-// CTA has given up).  A wait that gives up sets the call's error word and
-// stops the CTA taking work; a unit may then be
-// lost, so the finishing pass fails every sequence of the call closed
-// (accepted_len = -1).  Calls alternate between two error words, and every
-// stream CTA clears the next call's word once the previous kernel (the
-// previous call's finishing pass, the last reader of that word) is complete.
-
-struct ClcState {
-  uint4 resp[kClcRing];
-  unsigned long long bar[kClcRing];
-  unsigned long long stall_bar;  // test hook: initialised, never armed
-  volatile int issued;           // highest slot whose unit request is out
-  volatile int failed;           // first slot whose request found no CTA to take
-  volatile int abort;            // a wait gave up
-};
-
-__device__ __forceinline__ unsigned smem_u32(const void* p) {
-  return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
-  unsigned done;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-  return done != 0;
-}
-
-// bounded wait for the phase of the given parity to complete; it also ends
-// (false) once *err is set, checked every 1024 tries, so that one CTA giving
-// up ends every other CTA's waits quickly
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity, unsigned limit,
-                                                  const unsigned* err) {
-  for (unsigned it = 0; it < limit; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 1023u && err && *reinterpret_cast<const volatile unsigned*>(err) != 0u) return false;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void clc_init(ClcState& C) {
-  for (int e = 0; e < kClcRing; ++e)
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&C.bar[e])));
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&C.stall_bar)));
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  C.issued = 0;
-  C.failed = 0x7fffffff;
-  C.abort = 0;
-}
-
-__device__ __forceinline__ void clc_give_up(const Params& P, ClcState& C) {
-  C.abort = 1;
-  atomicOr(P.err, 1u);
-}
-
-// ring entry and phase parity of the request for slot s >= 1
-__device__ __forceinline__ int clc_entry(int s) { return (s - 1) % kClcRing; }
-__device__ __forceinline__ unsigned clc_parity(int s) { return static_cast<unsigned>(((s - 1) / kClcRing) & 1); }
-
-// lane 0: request the unit of slot s (slot s - 1 is known to have one)
-__device__ __forceinline__ void clc_request(ClcState& C, int s) {
-  if (C.abort) return;
-  const int e = clc_entry(s);
-  const unsigned bar = smem_u32(&C.bar[e]);
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], 16;" ::"r"(bar) : "memory");
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-          smem_u32(&C.resp[e])),
-      "r"(bar)
-      : "memory");
-  __threadfence_block();
-  C.issued = s;
-}
-
-// lane 0: the unit of slot s >= 1, or -1 when there is none (no CTA was left
-// to take, or a wait gave up)
-__device__ __forceinline__ int clc_slot_unit(const Params& P, ClcState& C, int s) {
-  const unsigned limit = P.wait_limit;
-  for (unsigned it = 0;; ++it) {
-    if (C.abort || s >= C.failed) return -1;
-    if (C.issued >= s) break;
-    if (it >= limit ||
-        ((it & 1023u) == 1023u && *reinterpret_cast<const volatile unsigned*>(P.err) != 0u)) {
-      clc_give_up(P, C);
-      return -1;
-    }
-    __nanosleep(32);
-  }
-  const int e = clc_entry(s);
-  const bool stall = P.test_stall && s == 1;
-  const unsigned bar = smem_u32(stall ? &C.stall_bar : &C.bar[e]);
-  const unsigned parity = stall ? 0u : clc_parity(s);
-  if (!mbar_wait_bounded(bar, parity, limit, P.err)) {
-    clc_give_up(P, C);
-    return -1;
-  }
-  unsigned ok, x;
-  asm volatile(
-      "{ .reg .b128 r; .reg .pred p;\n"
-      "  ld.shared.b128 r, [%2];\n"
-      "  clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n"
-      "  selp.u32 %0, 1, 0, p;\n"
-      "  clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r; }"
-      : "=r"(ok), "=r"(x)
-      : "r"(smem_u32(&C.resp[e]))
-      : "memory");
-  if (!ok) {
-    atomicMin(const_cast<int*>(&C.failed), s);
-    return -1;
-  }
-  return static_cast<int>(x);
-}
-
-// lane 0: the warp's next chunk index in the dynamic stream pass, or kNoWork
-__device__ __forceinline__ unsigned next_chunk_dyn(const Params& P, unsigned* cta_next, ClcState& C) {
-  for (;;) {
-    const unsigned n = atomicAdd(cta_next, 1u);
-    const int s = static_cast<int>(n / kUnitChunks);
-    const unsigned c = n % kUnitChunks;
-    const int unit = s == 0 ? static_cast<int>(blockIdx.x) : clc_slot_unit(P, C, s);
-    if (unit < 0) return kNoWork;
-    if (c == 0) clc_request(C, s + 1);  // this slot has a unit: ask for the next one
-    const unsigned x = static_cast<unsigned>(unit) * kUnitChunks + c;
-    if (x < P.total_chunks) return x;
-    // past the end of the last (shorter) unit: claim again
-  }
-}
-
-// thread 0, after every warp is done claiming: a request still in flight
-// writes shared memory, so the CTA waits for its answer before it exits (with
-// the default bound: an answer always comes, whatever the call's own limit)
-__device__ __forceinline__ void clc_drain(const Params& P, ClcState& C) {
-  const int s = C.issued;
-  if (s < 1) return;
-  if (!mbar_wait_bounded(smem_u32(&C.bar[clc_entry(s)]), clc_parity(s), kDefaultWaitLimit, nullptr))
-    clc_give_up(P, C);
 }
 
 template <typename TT, typename TD>
@@ -804,9 +628,7 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   }
 }
 
-// kDyn: work in dynamic units (the verifying call); otherwise one CTA per SM
-// sweeps its static share (the statistics pass of the diagnostics and filters)
-template <typename TT, typename TD, int kMode, bool kDyn>
+template <typename TT, typename TD, int kMode>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
     stream_kernel(const __grid_constant__ Params P) {
   constexpr bool kPol = kMode == kModePolicy;
@@ -816,7 +638,6 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   extern __shared__ __align__(128) unsigned char stages[];
   __shared__ WarpQueue queues[Stages<TT, TD>::kWarpsPerCta];
   __shared__ unsigned cta_next;
-  __shared__ ClcState clc;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* ring = stages + warp * S * kStage;
   WarpQueue& Q = queues[warp];
@@ -826,10 +647,7 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // slot n % S at step n (S - 1 steps ahead of its use) and consumed at loop
   // iteration n; the copy of its drafted token rides in the commit group of
   // step n - 1, so it has landed when the chunk has.
-  if (threadIdx.x == 0) {
-    cta_next = 0u;
-    if constexpr (kDyn) clc_init(clc);
-  }
+  if (threadIdx.x == 0) cta_next = 0u;
   __syncthreads();
   // This grid is itself a programmatic dependent launch: its CTAs may be
   // resident while the previous kernel in the stream (the producer of the
@@ -841,20 +659,13 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // wait above), and wait for this grid to complete and its memory to be
   // visible.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if constexpr (kDyn) {
-    if (threadIdx.x == 0) *P.err_next = 0u;
-  }
-  auto claim = [&]() -> unsigned {
-    if constexpr (kDyn) return next_chunk_dyn(P, &cta_next, clc);
-    else return next_chunk(P, &cta_next);
-  };
-  if (lane == 0) put_item(P, Q, 0, claim());
+  if (lane == 0) put_item(P, Q, 0, next_chunk(P, &cta_next));
   __syncwarp();
   int issued = 0;
   auto issue_next = [&]() {
     const int4 it = Q.item[issued % kItemRing];
     if (it.w > 0) issue_chunk<TT, TD>(P, it.x, it.y, it.z, ring + (issued % S) * kStage, lane);
-    if (lane == 0) put_item(P, Q, (issued + 1) % kItemRing, it.w > 0 ? claim() : kNoWork);
+    if (lane == 0) put_item(P, Q, (issued + 1) % kItemRing, it.w > 0 ? next_chunk(P, &cta_next) : kNoWork);
     ++issued;
     cp_async_commit();
     __syncwarp();
@@ -880,10 +691,6 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     __syncwarp();
   }
   cp_async_wait<0>();
-  if constexpr (kDyn) {
-    __syncthreads();
-    if (threadIdx.x == 0) clc_drain(P, clc);
-  }
 }
 
 // ------------------------------------------------------------ finishing
@@ -990,7 +797,6 @@ struct FinishShared {
   dfloat Z;
   dfloat y;
   int fmode;  // the stop row's sampling mode (-1: the sequence is done)
-  int stream_err;  // the dynamic stream pass gave up a wait: every sequence fails closed
   int dry;    // a warming run: global memory is read, never written
   int targ[kMaxRows];  // greedy calls: each row's first largest logit
 };
@@ -1103,7 +909,7 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
     if constexpr (kMode == kModeSample)
       sh.fast_rows = (gated && gate_fast_path(tau)) ? (k >= 32 ? 0xffffffffu : (1u << k) - 1u) : 0u;
     // the sequence's own threshold is checked where it is used (no schedule)
-    sh.bad = ((gated && !P.has_sched && !(tau > 0.f && tau <= 1.f)) || sh.stream_err) ? 1 : 0;
+    sh.bad = (gated && !P.has_sched && !(tau > 0.f && tau <= 1.f)) ? 1 : 0;
     sh.ncand = 0;
     sh.overflow_rows = 0u;
     sh.boundary = 0;
@@ -1808,17 +1614,8 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_con
   // the first sequence's input-only work overlaps the end of the stream pass;
   // then wait for the stream pass (programmatic dependent launch) before
   // reading its output
-  if (threadIdx.x == 0) sh.stream_err = 0;
-  __syncthreads();
   if (rank == 0 && first < P.B) finish_prologue<kMode>(P, first, sh, warm);
-  if (!warm) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // a stream pass that gave up a wait may have lost a unit of work
-    if (P.dyn && threadIdx.x == 0 && *reinterpret_cast<volatile unsigned*>(P.err) != 0u) {
-      sh.stream_err = 1;
-      sh.bad = 1;
-    }
-  }
+  if (!warm) asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll 1
   for (int b = first; b < stop; b += stride) {
     if (rank == 0) {

@@ -68,8 +68,6 @@ def load() -> ctypes.CDLL:
     L.spec_verify_diagnostics.restype = I
     L.spec_verify_set_filters.argtypes = [P, I, F, F, I, F, F]
     L.spec_verify_set_filters.restype = I
-    L.spec_verify_set_test_hooks.argtypes = [P, ctypes.c_uint, I]
-    L.spec_verify_set_test_hooks.restype = I
     L.spec_verify_launches_per_filtered_run.argtypes = []
     L.spec_verify_launches_per_filtered_run.restype = I
     _lib = L
@@ -136,11 +134,6 @@ def spec_verify_diagnostics(h, Lt, tdt, Ld, ddt, D, B, temperature, gate_mode, t
 def spec_verify_set_filters(h, top_k_t, top_p_t, min_p_t, top_k_d, top_p_d, min_p_d) -> int:
     """Raw call: sampler filters of the target and draft rows."""
     return load().spec_verify_set_filters(h, top_k_t, top_p_t, min_p_t, top_k_d, top_p_d, min_p_d)
-
-
-def spec_verify_set_test_hooks(h, wait_limit, stall_first_request) -> int:
-    """Raw call: the bounded waits' iteration limit (0 = default) and the stall hook."""
-    return load().spec_verify_set_test_hooks(h, wait_limit, stall_first_request)
 
 
 def spec_verify_launches_per_filtered_run() -> int:
@@ -218,14 +211,6 @@ class SpecVerifier:
         rc = spec_verify_mark_next(self.handle, ev_before.cuda_event, ev_after.cuda_event)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify_mark_next")
-
-    def set_test_hooks(self, wait_limit: int = 0, stall_first_request: bool = False):
-        """Test hook: the iteration limit of the stream pass's bounded waits
-        (0 = the default) and whether each CTA's first wait for a work unit
-        waits on a barrier nothing completes (so the limit runs out)."""
-        rc = spec_verify_set_test_hooks(self.handle, int(wait_limit), 1 if stall_first_request else 0)
-        if rc != SV_OK:
-            raise SpecVerifyError(rc, "spec_verify_set_test_hooks")
 
     def set_filters(self, target=(0, 1.0, 0.0), draft=(0, 1.0, 0.0)):
         """Sampler filters (top_k, top_p, min_p) of the target rows and of the
