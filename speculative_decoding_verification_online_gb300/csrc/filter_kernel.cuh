@@ -200,7 +200,7 @@ __device__ __forceinline__ void sel_descend(const unsigned long long* h, unsigne
 // over a list in shared memory: the largest key K such that the weights
 // (counts when w is null) of the entries with key >= K, among those with key
 // >= floor, reach target -- the radix descent of sel_histogram, 8 bits a level
-__device__ unsigned list_descend(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
+static __device__ unsigned list_descend(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
                                  double target, SelShared& sh) {
   const int tid = threadIdx.x;
   unsigned prefix = 0u;

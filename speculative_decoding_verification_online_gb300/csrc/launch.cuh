@@ -1,0 +1,272 @@
+// Launch sequences of the library's calls, as templates over the (target,
+// draft) logits types.  Included only by the pair_*.cu translation units, each
+// of which instantiates them for one pair (see handle.h).
+#pragma once
+
+#include "handle.h"
+
+namespace sv {
+namespace {
+
+constexpr int kFinCluster = 4;  // CTAs sharing a sequence's dense residual
+constexpr int kFinWarm = 2;     // warming CTAs of a single-CTA finishing grid
+
+// every warp of a stream CTA owns a ring of kDepth chunk stages
+template <typename TT, typename TD>
+constexpr int dyn_smem() {
+  return Stages<TT, TD>::kWarpsPerCta * Stages<TT, TD>::kDepth * Stages<TT, TD>::kBytes;
+}
+
+// opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
+template <typename TT, typename TD>
+constexpr int pair_smem() {
+  return PairStages<TT, TD>::kWarpsPerCta * PairStages<TT, TD>::kDepth *
+         PairStages<TT, TD>::kBytes;
+}
+
+template <typename TT, typename TD, int G>
+cudaError_t configure_one(int fin_spread_smem) {
+  cudaError_t e = cudaFuncSetAttribute(stream_kernel<TT, TD, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e != cudaSuccess) return e;
+  const int fin = static_cast<int>(sizeof(FinishShared));
+  const int fin_max = fin_spread_smem > fin ? fin_spread_smem : fin;
+  e = cudaFuncSetAttribute(finish_kernel<TT, TD, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fin_max);
+  if (e != cudaSuccess || G == kModeGreedy) return e;
+  return cudaFuncSetAttribute(finish_kernel<TT, TD, G, G != kModeGreedy>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, fin_max);
+}
+
+// every variant (sampling, sampling with a gate policy, greedy) of a dtype
+// pair: opt the kernels into their dynamic shared memory and ask how many
+// stream CTAs fit on an SM
+template <typename TT, typename TD>
+cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
+  cudaError_t e = configure_one<TT, TD, kModeSample>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModePolicy>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModeGreedy>(fin_spread_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeStats>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(select_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SelShared)));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
+                                                       stream_kernel<TT, TD, kModeSample>,
+                                                       Stages<TT, TD>::kThreadsPerCta,
+                                                       dyn_smem<TT, TD>());
+}
+
+// a programmatic dependent launch: the kernel may become resident while the
+// previous kernel in the stream drains (it calls griddepcontrol.wait before it
+// reads what that kernel writes)
+template <typename K, typename... A>
+cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
+                             A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// the stream pass (variant G), with the handle's one-shot timing marks around it
+template <typename TT, typename TD, int G>
+sv_status launch_stream(spec_verify_t h, const Params& P, int blocks_per_sm, cudaStream_t st) {
+  long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
+  // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
+  const long long need = (static_cast<long long>(P.total_chunks) + Stages<TT, TD>::kWarpsPerCta - 1) /
+                         Stages<TT, TD>::kWarpsPerCta;
+  if (grid > need) grid = need;
+  if (grid < 1) grid = 1;
+  const bool marked = h->mark_before != nullptr;
+  if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
+  // a programmatic dependent launch: resident early, it waits for the previous
+  // kernel in the stream before touching memory
+  if (launch_dependent(stream_kernel<TT, TD, G>, static_cast<unsigned>(grid),
+                       Stages<TT, TD>::kThreadsPerCta, dyn_smem<TT, TD>(), st, P) != cudaSuccess)
+    return SV_ECUDA;
+  if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
+  if (marked) {
+    const cudaError_t e = cudaEventRecord(h->mark_after, st);
+    h->mark_before = h->mark_after = nullptr;
+    if (e != cudaSuccess) return SV_ECUDA;
+  }
+  return SV_OK;
+}
+
+template <typename TT, typename TD, int G>
+sv_status launch(spec_verify_t h, const Params& P, int blocks_per_sm, bool dense_likely,
+                 cudaStream_t st) {
+  const sv_status rs = launch_stream<TT, TD, G>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
+  // the finishing pass: one CTA per sequence, allowed to launch while the
+  // stream pass drains; it waits (griddepcontrol.wait) before reading its output
+  cudaLaunchConfig_t cfg = {};
+  // a cluster of CTAs per sequence at a time (two CTAs per SM at most; larger
+  // batches loop).  When dense residuals are likely (plain rows, or gated rows
+  // off the candidate fast path) and the whole batch fits at once, clusters of
+  // up to kFinCluster CTAs share the re-read of the stop row pair; otherwise
+  // one CTA per sequence (more sequences in flight beats wider sequences)
+  int csize = 1;
+  if (dense_likely)
+    for (int c = kFinCluster; c > 1; c /= 2)
+      if (static_cast<long long>(P.B) * c <= 2ll * h->num_sms) {
+        csize = c;
+        break;
+      }
+  const int max_clusters = 2 * h->num_sms / csize;
+  const int clusters = P.B < max_clusters ? P.B : max_clusters;
+  // warming CTAs in front of single-CTA clusters, while every CTA still has
+  // an SM slot at once (two per SM)
+  Params Pf = P;
+  Pf.fin_warm = csize == 1 && clusters + kFinWarm <= 2 * h->num_sms ? kFinWarm : 0;
+  const int grid = clusters * csize + Pf.fin_warm;
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kFinThreads);
+  // a grid that fits one CTA per SM gets it (finish_spread_smem)
+  cfg.dynamicSmemBytes = h->fin_spread_smem > 0 && grid <= h->num_sms
+                             ? static_cast<size_t>(h->fin_spread_smem)
+                             : sizeof(FinishShared);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = csize > 1 ? 2 : 1;
+  // the finishing kernel with the dense pass (clusters) when dense residuals
+  // are likely; otherwise the one without it (greedy calls never need it)
+  cudaError_t e;
+  if (G != kModeGreedy && dense_likely)
+    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, G != kModeGreedy>, Pf);
+  else
+    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, false>, Pf);
+  if (e != cudaSuccess) return SV_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+// the acceptance diagnostics: the stream pass, the per-position merge, and
+// (temperature > 0) the pair sweep and its reduction, each launch a
+// programmatic dependent of the one before
+template <typename TT, typename TD, bool kGreedy>
+sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float* min_sum,
+                      float* pq_sum, float* argmax_q, cudaStream_t st) {
+  const sv_status rs = launch_stream<TT, TD, kGreedy ? kModeGreedy : kModeStats>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
+  const unsigned npos = static_cast<unsigned>(P.B * P.k);
+  const unsigned small_grid = (npos + kDiagWarps - 1) / kDiagWarps;
+  if (launch_dependent(diag_norm_kernel<kGreedy>, small_grid, kDiagThreads, 0, st, P, h->dnorm,
+                       min_sum, pq_sum, argmax_q) != cudaSuccess)
+    return SV_ECUDA;
+  if (!kGreedy) {
+    const unsigned total = npos * static_cast<unsigned>(P.nchunk);
+    constexpr int kW = PairStages<TT, TD>::kWarpsPerCta;
+    long long grid = h->num_sms;
+    const long long need = (static_cast<long long>(total) + kW - 1) / kW;
+    if (grid > need) grid = need;
+    if (launch_dependent(pair_kernel<TT, TD>, static_cast<unsigned>(grid),
+                         PairStages<TT, TD>::kThreadsPerCta, pair_smem<TT, TD>(), st, P,
+                         static_cast<const DiagNorm*>(h->dnorm), total) != cudaSuccess)
+      return SV_ECUDA;
+    if (launch_dependent(diag_reduce_kernel<TD>, small_grid, kDiagThreads, 0, st, P,
+                         static_cast<const DiagNorm*>(h->dnorm), min_sum, pq_sum, argmax_q) != cudaSuccess)
+      return SV_ECUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+// the filter prefix of a call: statistics pass, per-row thresholds, masked
+// copies; on return P reads the masked copies
+template <typename TT, typename TD>
+sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, cudaStream_t st) {
+  const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
+  const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
+  const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
+  const size_t o_t = 0, o_d = align_up(bt, 256), o_key = align_up(o_d + bd, 256);
+  const size_t o_first = align_up(o_key + rows_all * sizeof(unsigned), 256);
+  const size_t need = align_up(o_first + rows_all * sizeof(int), 256);
+  if (!h->fbuf) {
+    if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
+      h->fbuf = nullptr;
+      return SV_ENOMEM;
+    }
+    h->fbuf_bytes = need;
+  }
+  char* base = static_cast<char*>(h->fbuf);
+  FilterParams F;
+  F.f[0] = h->filt[0];
+  F.f[1] = h->filt[1];
+  F.key = reinterpret_cast<unsigned*>(base + o_key);
+  F.first = reinterpret_cast<int*>(base + o_first);
+  F.Lt_m = base + o_t;
+  F.Ld_m = base + o_d;
+  sv_status rs = launch_stream<TT, TD, kModeStats>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
+  const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
+  if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
+      cudaSuccess)
+    return SV_ECUDA;
+  // one CTA per row at a time, at most eight per SM
+  long long grid = static_cast<long long>(P.B) * P.rows;
+  if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
+  if (grid < 1) grid = 1;
+  if (launch_dependent(mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(kMaskThreads),
+                       0, st, P, F) != cudaSuccess)
+    return SV_ECUDA;
+  P.Lt = F.Lt_m;
+  P.Ld = F.Ld_m;
+  P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
+  P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
+
+// one verifying call: the sampler filters' prefix when asked for, then the
+// stream pass and the finishing pass of the variant
+template <typename TT, typename TD>
+sv_status verify_pair(spec_verify_t h, Params& P, int mode, int bps, bool dense_likely, bool filtered,
+                      cudaStream_t st) {
+  if (filtered) {
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
+    if (rs != SV_OK) return rs;
+  }
+  if (mode == kModeGreedy) return launch<TT, TD, kModeGreedy>(h, P, bps, false, st);
+  if (mode == kModePolicy) return launch<TT, TD, kModePolicy>(h, P, bps, dense_likely, st);
+  return launch<TT, TD, kModeSample>(h, P, bps, dense_likely, st);
+}
+
+// the acceptance diagnostics, after the sampler filters' prefix when asked for
+template <typename TT, typename TD>
+sv_status diag_pair(spec_verify_t h, Params& P, int bps, bool filtered, float* min_sum, float* pq_sum,
+                    float* argmax_q, cudaStream_t st) {
+  if (filtered) {
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
+    if (rs != SV_OK) return rs;
+  }
+  if (P.greedy) return launch_diag<TT, TD, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  return launch_diag<TT, TD, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+}
+
+}  // namespace
+
+template <typename TT, typename TD>
+constexpr PairOps make_ops() {
+  return PairOps{&configure<TT, TD>, &verify_pair<TT, TD>, &diag_pair<TT, TD>};
+}
+
+}  // namespace sv

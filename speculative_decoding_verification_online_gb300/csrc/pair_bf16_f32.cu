@@ -1,0 +1,7 @@
+// The kernels and launch sequences for bf16 target logits and f32 draft logits
+// (bf16 logits are held as their uint16_t bit patterns).
+#include "launch.cuh"
+
+namespace sv {
+const PairOps ops_bf16_f32 = make_ops<uint16_t, float>();
+}  // namespace sv

@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/spec_verify.h: handle and
-// workspace management, argument validation, and the two launches of a call
-// (the stream pass, then the finishing pass as a programmatic dependent launch).
+// workspace management and argument validation.  The launches of each call
+// (the stream pass, then the finishing pass as a programmatic dependent
+// launch) are in launch.cuh, instantiated per pair of logits types in the
+// pair_*.cu translation units.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -10,312 +12,25 @@
 #include <mutex>
 #include <new>
 
-#include "spec_verify.h"
-#include "verify_kernel.cuh"
-#include "diag_kernel.cuh"
-#include "filter_kernel.cuh"
+#include "handle.h"
 
-struct spec_verify_s {
-  int device = 0;
-  int max_B = 0, k = 0, V = 0, nchunk = 0;
-  int num_sms = 0;
-  int blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [target is bf16][draft is bf16]
-  int fin_spread_smem = 0;                     // see finish_spread_smem
-  void* ws = nullptr;                          // one device allocation for the workspace
-  size_t ws_bytes = 0;
-  float2* part = nullptr;
-  float* xD = nullptr;
-  sv::Cand* cand = nullptr;
-  unsigned* cand_over = nullptr;
-  sv::DiagNorm* dnorm = nullptr;  // [max_B, k] (diagnostics)
-  // one-shot timing marks around the next stream pass
-  cudaEvent_t mark_before = nullptr, mark_after = nullptr;
-  // staging for spec_verify_run_host (allocated on first use)
-  void* stage = nullptr;
-  size_t stage_bytes = 0;
-  // gate policy (spec_verify_set_gate_policy): schedule entries, cumulative floor
-  int n_sched = 0;
-  float sched[SV_MAX_K] = {};
-  float min_cum = 0.f;
-  // sampler filters (spec_verify_set_filters) and their buffers, allocated on
-  // the first filtered call: masked copies of the logits, per-row thresholds
-  sv::Filter filt[2] = {{0, 1.f, 0.f}, {0, 1.f, 0.f}};
-  void* fbuf = nullptr;
-  size_t fbuf_bytes = 0;
-};
 
 namespace {
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+using sv::align_up;
+using sv::filter_on;
 
 size_t elem_size(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 
-constexpr int kFinCluster = 4;  // CTAs sharing a sequence's dense residual
-constexpr int kFinWarm = 2;     // warming CTAs of a single-CTA finishing grid
-
 bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16; }
 
-// every warp of a stream CTA owns a ring of kDepth chunk stages
-template <typename TT, typename TD>
-constexpr int dyn_smem() {
-  return sv::Stages<TT, TD>::kWarpsPerCta * sv::Stages<TT, TD>::kDepth * sv::Stages<TT, TD>::kBytes;
-}
-
-// opt the kernel into its dynamic shared memory and ask how many CTAs fit on an SM
-template <typename TT, typename TD>
-constexpr int pair_smem() {
-  return sv::PairStages<TT, TD>::kWarpsPerCta * sv::PairStages<TT, TD>::kDepth *
-         sv::PairStages<TT, TD>::kBytes;
-}
-
-// Dynamic shared memory for a finishing CTA that is to have its SM to itself:
-// just over half of an SM's shared memory, or 0 where the device cannot give
-// that much to one CTA.  Two finishing CTAs on one SM slow each other's
-// dependent chains (measured: about 1 us per call on the 128K-vocabulary
-// batch), so a grid that fits one CTA per SM asks for this much.
-int finish_spread_smem(int device) {
-  int per_sm = 0, optin = 0;
-  if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
-    return 0;
-  const int want = per_sm / 2 + 1024;
-  return want <= optin && want > static_cast<int>(sizeof(sv::FinishShared)) ? want : 0;
-}
-
-template <typename TT, typename TD, int G>
-cudaError_t configure_one(int fin_spread_smem) {
-  cudaError_t e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
-  if (e != cudaSuccess) return e;
-  const int fin = static_cast<int>(sizeof(sv::FinishShared));
-  const int fin_max = fin_spread_smem > fin ? fin_spread_smem : fin;
-  e = cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           fin_max);
-  if (e != cudaSuccess || G == sv::kModeGreedy) return e;
-  return cudaFuncSetAttribute(sv::finish_kernel<TT, TD, G, G != sv::kModeGreedy>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, fin_max);
-}
-
-// every variant (sampling, sampling with a gate policy, greedy) of a dtype
-// pair: opt the kernels into their dynamic shared memory and ask how many
-// stream CTAs fit on an SM
-template <typename TT, typename TD>
-cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
-  cudaError_t e = configure_one<TT, TD, sv::kModeSample>(fin_spread_smem);
-  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModePolicy>(fin_spread_smem);
-  if (e == cudaSuccess) e = configure_one<TT, TD, sv::kModeGreedy>(fin_spread_smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sv::stream_kernel<TT, TD, sv::kModeStats>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sv::pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             pair_smem<TT, TD>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(sv::select_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(sv::SelShared)));
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                       sv::stream_kernel<TT, TD, sv::kModeSample>,
-                                                       sv::Stages<TT, TD>::kThreadsPerCta,
-                                                       dyn_smem<TT, TD>());
-}
-
-// a programmatic dependent launch: the kernel may become resident while the
-// previous kernel in the stream drains (it calls griddepcontrol.wait before it
-// reads what that kernel writes)
-template <typename K, typename... A>
-cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t smem, cudaStream_t st,
-                             A... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-// the stream pass (variant G), with the handle's one-shot timing marks around it
-template <typename TT, typename TD, int G>
-sv_status launch_stream(spec_verify_t h, const sv::Params& P, int blocks_per_sm, cudaStream_t st) {
-  long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
-  // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
-  const long long need = (static_cast<long long>(P.total_chunks) + sv::Stages<TT, TD>::kWarpsPerCta - 1) /
-                         sv::Stages<TT, TD>::kWarpsPerCta;
-  if (grid > need) grid = need;
-  if (grid < 1) grid = 1;
-  const bool marked = h->mark_before != nullptr;
-  if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
-  // a programmatic dependent launch: resident early, it waits for the previous
-  // kernel in the stream before touching memory
-  if (launch_dependent(sv::stream_kernel<TT, TD, G>, static_cast<unsigned>(grid),
-                       sv::Stages<TT, TD>::kThreadsPerCta, dyn_smem<TT, TD>(), st, P) != cudaSuccess)
-    return SV_ECUDA;
-  if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
-  if (marked) {
-    const cudaError_t e = cudaEventRecord(h->mark_after, st);
-    h->mark_before = h->mark_after = nullptr;
-    if (e != cudaSuccess) return SV_ECUDA;
-  }
-  return SV_OK;
-}
-
-template <typename TT, typename TD, int G>
-sv_status launch(spec_verify_t h, const sv::Params& P, int blocks_per_sm, bool dense_likely,
-                 cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, G>(h, P, blocks_per_sm, st);
-  if (rs != SV_OK) return rs;
-  // the finishing pass: one CTA per sequence, allowed to launch while the
-  // stream pass drains; it waits (griddepcontrol.wait) before reading its output
-  cudaLaunchConfig_t cfg = {};
-  // a cluster of CTAs per sequence at a time (two CTAs per SM at most; larger
-  // batches loop).  When dense residuals are likely (plain rows, or gated rows
-  // off the candidate fast path) and the whole batch fits at once, clusters of
-  // up to kFinCluster CTAs share the re-read of the stop row pair; otherwise
-  // one CTA per sequence (more sequences in flight beats wider sequences)
-  int csize = 1;
-  if (dense_likely)
-    for (int c = kFinCluster; c > 1; c /= 2)
-      if (static_cast<long long>(P.B) * c <= 2ll * h->num_sms) {
-        csize = c;
-        break;
-      }
-  const int max_clusters = 2 * h->num_sms / csize;
-  const int clusters = P.B < max_clusters ? P.B : max_clusters;
-  // warming CTAs in front of single-CTA clusters, while every CTA still has
-  // an SM slot at once (two per SM)
-  sv::Params Pf = P;
-  Pf.fin_warm = csize == 1 && clusters + kFinWarm <= 2 * h->num_sms ? kFinWarm : 0;
-  const int grid = clusters * csize + Pf.fin_warm;
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(sv::kFinThreads);
-  // a grid that fits one CTA per SM gets it (finish_spread_smem)
-  cfg.dynamicSmemBytes = h->fin_spread_smem > 0 && grid <= h->num_sms
-                             ? static_cast<size_t>(h->fin_spread_smem)
-                             : sizeof(sv::FinishShared);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = static_cast<unsigned>(csize);
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = csize > 1 ? 2 : 1;
-  // the finishing kernel with the dense pass (clusters) when dense residuals
-  // are likely; otherwise the one without it (greedy calls never need it)
-  cudaError_t e;
-  if (G != sv::kModeGreedy && dense_likely)
-    e = cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G, G != sv::kModeGreedy>, Pf);
-  else
-    e = cudaLaunchKernelEx(&cfg, sv::finish_kernel<TT, TD, G, false>, Pf);
-  if (e != cudaSuccess) return SV_ECUDA;
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
-}
-
-// the kernel variant G for the call's logits types (tb / db: bf16)
-template <int G>
-sv_status launch_mode(spec_verify_t h, const sv::Params& P, int bps, bool dense_likely, bool tb, bool db,
-                      cudaStream_t st) {
-  if (tb && db) return launch<uint16_t, uint16_t, G>(h, P, bps, dense_likely, st);
-  if (tb && !db) return launch<uint16_t, float, G>(h, P, bps, dense_likely, st);
-  if (!tb && db) return launch<float, uint16_t, G>(h, P, bps, dense_likely, st);
-  return launch<float, float, G>(h, P, bps, dense_likely, st);
-}
-
-
-// the acceptance diagnostics: the stream pass, the per-position merge, and
-// (temperature > 0) the pair sweep and its reduction, each launch a
-// programmatic dependent of the one before
-template <typename TT, typename TD, bool kGreedy>
-sv_status launch_diag(spec_verify_t h, const sv::Params& P, int blocks_per_sm, float* min_sum,
-                      float* pq_sum, float* argmax_q, cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, kGreedy ? sv::kModeGreedy : sv::kModeStats>(h, P, blocks_per_sm, st);
-  if (rs != SV_OK) return rs;
-  const unsigned npos = static_cast<unsigned>(P.B * P.k);
-  const unsigned small_grid = (npos + sv::kDiagWarps - 1) / sv::kDiagWarps;
-  if (launch_dependent(sv::diag_norm_kernel<kGreedy>, small_grid, sv::kDiagThreads, 0, st, P, h->dnorm,
-                       min_sum, pq_sum, argmax_q) != cudaSuccess)
-    return SV_ECUDA;
-  if (!kGreedy) {
-    const unsigned total = npos * static_cast<unsigned>(P.nchunk);
-    constexpr int kW = sv::PairStages<TT, TD>::kWarpsPerCta;
-    long long grid = h->num_sms;
-    const long long need = (static_cast<long long>(total) + kW - 1) / kW;
-    if (grid > need) grid = need;
-    if (launch_dependent(sv::pair_kernel<TT, TD>, static_cast<unsigned>(grid),
-                         sv::PairStages<TT, TD>::kThreadsPerCta, pair_smem<TT, TD>(), st, P,
-                         static_cast<const sv::DiagNorm*>(h->dnorm), total) != cudaSuccess)
-      return SV_ECUDA;
-    if (launch_dependent(sv::diag_reduce_kernel<TD>, small_grid, sv::kDiagThreads, 0, st, P,
-                         static_cast<const sv::DiagNorm*>(h->dnorm), min_sum, pq_sum, argmax_q) != cudaSuccess)
-      return SV_ECUDA;
-  }
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
-}
-
-bool filter_on(const sv::Filter& f) { return f.top_k != 0 || f.top_p < 1.f || f.min_p > 0.f; }
-
-// the filter prefix of a call: statistics pass, per-row thresholds, masked
-// copies; on return P reads the masked copies
-template <typename TT, typename TD>
-sv_status launch_filters(spec_verify_t h, sv::Params& P, int blocks_per_sm, cudaStream_t st) {
-  const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
-  const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
-  const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
-  const size_t o_t = 0, o_d = align_up(bt, 256), o_key = align_up(o_d + bd, 256);
-  const size_t o_first = align_up(o_key + rows_all * sizeof(unsigned), 256);
-  const size_t need = align_up(o_first + rows_all * sizeof(int), 256);
-  if (!h->fbuf) {
-    if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
-      h->fbuf = nullptr;
-      return SV_ENOMEM;
-    }
-    h->fbuf_bytes = need;
-  }
-  char* base = static_cast<char*>(h->fbuf);
-  sv::FilterParams F;
-  F.f[0] = h->filt[0];
-  F.f[1] = h->filt[1];
-  F.key = reinterpret_cast<unsigned*>(base + o_key);
-  F.first = reinterpret_cast<int*>(base + o_first);
-  F.Lt_m = base + o_t;
-  F.Ld_m = base + o_d;
-  sv_status rs = launch_stream<TT, TD, sv::kModeStats>(h, P, blocks_per_sm, st);
-  if (rs != SV_OK) return rs;
-  const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
-  if (launch_dependent(sv::select_kernel<TT, TD>, nrows, sv::kSelThreads, sizeof(sv::SelShared), st, P, F) !=
-      cudaSuccess)
-    return SV_ECUDA;
-  // one CTA per row at a time, at most eight per SM
-  long long grid = static_cast<long long>(P.B) * P.rows;
-  if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
-  if (grid < 1) grid = 1;
-  if (launch_dependent(sv::mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(sv::kMaskThreads),
-                       0, st, P, F) != cudaSuccess)
-    return SV_ECUDA;
-  P.Lt = F.Lt_m;
-  P.Ld = F.Ld_m;
-  P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
-  P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
-}
-
-template <int G>
-sv_status launch_mode_filtered(spec_verify_t h, sv::Params& P, int bps, bool dense_likely, bool tb, bool db,
-                               cudaStream_t st) {
-  sv_status rs;
-  if (tb && db) rs = launch_filters<uint16_t, uint16_t>(h, P, bps, st);
-  else if (tb && !db) rs = launch_filters<uint16_t, float>(h, P, bps, st);
-  else if (!tb && db) rs = launch_filters<float, uint16_t>(h, P, bps, st);
-  else rs = launch_filters<float, float>(h, P, bps, st);
-  if (rs != SV_OK) return rs;
-  return launch_mode<G>(h, P, bps, dense_likely, tb, db, st);
+// every pair of logits types: kernel attributes, stream CTAs per SM
+cudaError_t configure_all(int (*blocks_per_sm)[2], int fin_spread_smem) {
+  cudaError_t e = sv::ops_f32_f32.configure(&blocks_per_sm[0][0], fin_spread_smem);
+  if (e == cudaSuccess) e = sv::ops_f32_bf16.configure(&blocks_per_sm[0][1], fin_spread_smem);
+  if (e == cudaSuccess) e = sv::ops_bf16_f32.configure(&blocks_per_sm[1][0], fin_spread_smem);
+  if (e == cudaSuccess) e = sv::ops_bf16_bf16.configure(&blocks_per_sm[1][1], fin_spread_smem);
+  return e;
 }
 
 struct DeviceGuard {
@@ -381,11 +96,8 @@ sv_status spec_verify_init(spec_verify_t* out, int max_B, int k, int V, int devi
     delete h;
     return SV_ECUDA;
   }
-  h->fin_spread_smem = finish_spread_smem(device);
-  cudaError_t e = configure<float, float>(&h->blocks_per_sm[0][0], h->fin_spread_smem);
-  if (e == cudaSuccess) e = configure<float, uint16_t>(&h->blocks_per_sm[0][1], h->fin_spread_smem);
-  if (e == cudaSuccess) e = configure<uint16_t, float>(&h->blocks_per_sm[1][0], h->fin_spread_smem);
-  if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&h->blocks_per_sm[1][1], h->fin_spread_smem);
+  h->fin_spread_smem = sv::finish_spread_smem(device);
+  const cudaError_t e = configure_all(h->blocks_per_sm, h->fin_spread_smem);
   if (e != cudaSuccess) {
     delete h;
     return SV_ECUDA;
@@ -556,14 +268,10 @@ sv_status spec_verify_run_ex(spec_verify_t h, const void* target_logits, sv_dtyp
   const bool dense_likely =
       dense_residuals_likely(h, temperature, gate_mode, threshold, gate_mode_per_seq, threshold_per_seq);
   // sampler filters (temperature > 0: a greedy call is one-hot already)
-  if (!P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]))) {
-    if (P.has_sched || P.min_cum > 0.f)
-      return launch_mode_filtered<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
-    return launch_mode_filtered<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
-  }
-  if (P.greedy) return launch_mode<sv::kModeGreedy>(h, P, bps, false, tb, db, st);
-  if (P.has_sched || P.min_cum > 0.f) return launch_mode<sv::kModePolicy>(h, P, bps, dense_likely, tb, db, st);
-  return launch_mode<sv::kModeSample>(h, P, bps, dense_likely, tb, db, st);
+  const bool filtered = !P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]));
+  const int mode = P.greedy ? sv::kModeGreedy
+                            : (P.has_sched || P.min_cum > 0.f ? sv::kModePolicy : sv::kModeSample);
+  return sv::pair_ops(tb, db).verify(h, P, mode, bps, dense_likely, filtered, st);
 }
 
 sv_status spec_verify_diagnostics(spec_verify_t h, const void* target_logits, sv_dtype tdt,
@@ -585,24 +293,8 @@ sv_status spec_verify_diagnostics(spec_verify_t h, const void* target_logits, sv
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const int tb = tdt == SV_BF16, db = ddt == SV_BF16;
   const int bps = h->blocks_per_sm[tb][db] > 0 ? h->blocks_per_sm[tb][db] : 1;
-  if (!P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]))) {
-    sv_status rs;
-    if (tb && db) rs = launch_filters<uint16_t, uint16_t>(h, P, bps, st);
-    else if (tb && !db) rs = launch_filters<uint16_t, float>(h, P, bps, st);
-    else if (!tb && db) rs = launch_filters<float, uint16_t>(h, P, bps, st);
-    else rs = launch_filters<float, float>(h, P, bps, st);
-    if (rs != SV_OK) return rs;
-  }
-  if (P.greedy) {
-    if (tb && db) return launch_diag<uint16_t, uint16_t, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-    if (tb && !db) return launch_diag<uint16_t, float, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-    if (!tb && db) return launch_diag<float, uint16_t, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-    return launch_diag<float, float, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-  }
-  if (tb && db) return launch_diag<uint16_t, uint16_t, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-  if (tb && !db) return launch_diag<uint16_t, float, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-  if (!tb && db) return launch_diag<float, uint16_t, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-  return launch_diag<float, float, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  const bool filtered = !P.greedy && (filter_on(h->filt[0]) || filter_on(h->filt[1]));
+  return sv::pair_ops(tb, db).diagnostics(h, P, bps, filtered, min_sum, pq_sum, argmax_q, st);
 }
 
 sv_status spec_verify_run(spec_verify_t h, const void* target_logits, sv_dtype tdt,
@@ -790,12 +482,8 @@ sv_status noalloc_setup(int dev, NoallocDevice** out) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SV_ECUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return SV_ECUDA;
-    d.fin_spread_smem = finish_spread_smem(dev);
-    cudaError_t e = configure<float, float>(&d.blocks_per_sm[0][0], d.fin_spread_smem);
-    if (e == cudaSuccess) e = configure<float, uint16_t>(&d.blocks_per_sm[0][1], d.fin_spread_smem);
-    if (e == cudaSuccess) e = configure<uint16_t, float>(&d.blocks_per_sm[1][0], d.fin_spread_smem);
-    if (e == cudaSuccess) e = configure<uint16_t, uint16_t>(&d.blocks_per_sm[1][1], d.fin_spread_smem);
-    if (e != cudaSuccess) return SV_ECUDA;
+    d.fin_spread_smem = sv::finish_spread_smem(dev);
+    if (configure_all(d.blocks_per_sm, d.fin_spread_smem) != cudaSuccess) return SV_ECUDA;
     unsigned char* base = static_cast<unsigned char*>(p);
     // a set-up redone after a failed call: that call's kernels (if any ran)
     // are finished before the slots and flags are reset

@@ -1,7 +1,7 @@
 """The host side of the C ABI under AddressSanitizer and UndefinedBehaviorSanitizer.
 
-``csrc/spec_verify.cu`` is compiled with both sanitizers on its host code (the
-device code as PTX only: no kernel runs here) and linked with
+Every translation unit of ``csrc/`` is compiled with both sanitizers on its
+host code (the device code as PTX only: no kernel runs here) and linked with
 ``abi_sanitize_driver.c``, which calls every entry point on the paths a host
 without a usable GPU reaches: status strings, launch counts, argument
 validation, a NULL handle, sizes beyond the limits, the allocation-free entry
@@ -37,15 +37,22 @@ def test_host_abi_is_clean_under_address_and_undefined_behaviour_sanitizers(tmp_
     libdir = os.path.join(cuda, "lib64")
     if not os.path.exists(os.path.join(libdir, "libcudart.so")):
         pytest.skip("no shared CUDA runtime under " + libdir)
-    lib_o, drv_o, exe = (str(tmp_path / n) for n in ("spec_verify.o", "driver.o", "abi_sanitized"))
+    drv_o, exe = str(tmp_path / "driver.o"), str(tmp_path / "abi_sanitized")
     xc = [a for f in SANITIZE for a in ("-Xcompiler", f)]
+    # every translation unit of the library (in parallel), then the driver
+    units = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    objs = [str(tmp_path / (u[:-3] + ".o")) for u in units]
+    procs = [subprocess.Popen([os.path.join(cuda, "bin", "nvcc"), "-gencode", "arch=compute_103a,code=compute_103a",
+                               "-O1", "-g", "-std=c++17", *xc, "-I", INCLUDE, "-I", CSRC, "-c",
+                               os.path.join(CSRC, u), "-o", o], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                              text=True) for u, o in zip(units, objs)]
+    for u, pr in zip(units, procs):
+        out, err = pr.communicate()
+        assert pr.returncode == 0, u + "\n" + err
     steps = [
-        [os.path.join(cuda, "bin", "nvcc"), "-gencode", "arch=compute_103a,code=compute_103a", "-O1", "-g",
-         "-std=c++17", *xc, "-I", INCLUDE, "-I", CSRC, "-c", os.path.join(CSRC, "spec_verify.cu"),
-         "-o", lib_o],
         ["gcc", "-std=c11", "-O1", "-g", *SANITIZE, "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, "-c",
          os.path.join(HERE, "abi_sanitize_driver.c"), "-o", drv_o],
-        ["g++", *SANITIZE, drv_o, lib_o, "-L", libdir, "-lcudart", "-Wl,-rpath," + libdir, "-o", exe],
+        ["g++", *SANITIZE, drv_o, *objs, "-L", libdir, "-lcudart", "-Wl,-rpath," + libdir, "-o", exe],
     ]
     for cmd in steps:
         r = subprocess.run(cmd, capture_output=True, text=True)
