@@ -585,10 +585,12 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             # the diagnostics launch 4 kernels per call (2 at temperature 0);
-            # sampler filters add 3 in front (temperature > 0)
+            # sampler filters add 2 in front of a verifying call (statistics,
+            # selection) and 3 in front of the diagnostics (and masked copies)
             "gpu_launches": args.steps * (((2 if w0.T == 0 else 4) if args.diagnostics
                                            else sv.spec_verify_launches_per_run())
-                                          + (3 if filt is not None and w0.T > 0 else 0)),
+                                          + ((3 if args.diagnostics else 2)
+                                             if filt is not None and w0.T > 0 else 0)),
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

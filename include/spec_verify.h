@@ -252,15 +252,17 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
  *     probability, keep the shortest prefix whose mass reaches top_p, plus the
  *     tokens tied with its last one; 1 = off.
  *   min_p in [0, 1]: keep p >= min_p * max p; 0 = off.
- * With any filter on (and temperature > 0) a call first runs a statistics pass
- * over the logits, finds each row's kept set, writes masked copies of the
- * logits (-inf outside the kept set; a NaN is kept so the row stays invalid)
- * into a buffer of the handle (max_B * (2k+1) * V * 4 bytes, allocated on the
- * first filtered call -- make that call outside any stream capture; SV_ENOMEM
- * if it fails) and then verifies the copies exactly as an unfiltered
- * call would: 5 launches instead of 2 and about five reads of the logits.
- * row_stats then describe the filtered rows.  spec_verify_diagnostics applies
- * the same filters.  Decisions of top-p and min-p sit on fp32 arithmetic (the
+ * With any filter on (and temperature > 0) a verifying call first runs a
+ * statistics pass over the logits and finds each row's kept set (a logit
+ * threshold, or the kept index of a top_k = 1 row) into a buffer of the
+ * handle (max_B * (2k+1) * 12 bytes, allocated on the first filtered call --
+ * make that call outside any stream capture; SV_ENOMEM if it fails); its
+ * verifying kernels then read every logit outside a row's kept set as -inf
+ * (a NaN is kept, so the row stays invalid): 4 launches instead of 2 and
+ * about three reads of the logits.  row_stats then describe the filtered
+ * rows.  spec_verify_diagnostics applies the same filters through masked
+ * copies of the logits, in a second buffer of the handle (max_B * (2k+1) * V
+ * * 4 bytes, allocated on the first filtered diagnostics call).  Decisions of top-p and min-p sit on fp32 arithmetic (the
  * top-p masses are summed as integers, so they do not depend on the order of
  * the additions).  Default: all off.  Returns SV_EINVAL (filters unchanged) for
  * a NULL handle or a value outside its range. */
@@ -268,7 +270,7 @@ sv_status spec_verify_set_filters(spec_verify_t h, int top_k_target, float top_p
                                   float min_p_target, int top_k_draft, float top_p_draft,
                                   float min_p_draft);
 
-/* Kernel launches of a call with sampler filters on (temperature > 0). */
+/* Kernel launches of a verifying call with sampler filters on (temperature > 0). */
 int spec_verify_launches_per_filtered_run(void);
 
 /* Release the handle and its device memory (NULL is a no-op).  Synchronises

@@ -1,9 +1,10 @@
 // filter_kernel.cuh -- the sampler's filter chain before the softmax (mlxcel
 // PR #992, "What changed": temperature, top-k, top-p, min-p, then the softmax
-// of the survivors; top_k == 1 is greedy), applied to every row of a call as
-// a masked copy of the logits (-inf outside the kept set).  The verification
-// kernels then run unchanged on the copies: the temperature softmax of a
-// masked row is exactly the filtered distribution.
+// of the survivors; top_k == 1 is greedy).  Each row's kept set is found here;
+// the verifying kernels then read every logit outside it as -inf, applying
+// the row's threshold as they load (the temperature softmax of a row masked
+// that way is exactly the filtered distribution).  The diagnostics read rows
+// as they are, so for them mask_kernel writes masked copies instead.
 //
 // Each filter keeps the tokens at or above a logit threshold (ties kept), so a
 // row's kept set is {x : key(x) >= K} for one key K in an order-preserving
@@ -12,8 +13,7 @@
 // keys, 8 bits a level, with per-warp histograms of counts (top-k) and of
 // fixed-point masses 2^40 exp2(x c - Mc) (top-p: integer sums, so the
 // decisions do not depend on the order of the additions); min-p is a
-// threshold on x itself, found by bisection over the keys.  mask_kernel then
-// writes the masked copy.
+// threshold on x itself, found by bisection over the keys.
 #pragma once
 
 #include <type_traits>
@@ -32,7 +32,8 @@ struct FilterParams {
   Filter f[2];          // [0] target rows, [1] draft rows
   unsigned* key;        // [B * rows] threshold key of each row (kept: key >= K)
   int* first;           // [B * rows] top_k == 1: the index kept, else -1
-  void* Lt_m;           // masked copies, same layouts and types as the inputs
+  float* thr;           // [B * rows] the same threshold as a logit: kept x >= thr (-inf: all)
+  void* Lt_m;           // masked copies, same layouts and types as the inputs (null: none)
   void* Ld_m;
 };
 
@@ -56,6 +57,10 @@ __device__ __forceinline__ unsigned key_of(float x) {
 __device__ __forceinline__ float float_of_key(unsigned k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
+// a row's threshold key as a logit threshold: key(x) >= K iff x >= float_of_key(K)
+// for every non-NaN x but -0 against +0 (which compare equal as logits, as in
+// the filters' own tie rule); K = 0 keeps every logit
+__device__ __forceinline__ float thr_of_key(unsigned K) { return K == 0u ? -INFINITY : float_of_key(K); }
 
 template <typename T> __device__ __forceinline__ float row_at(const T* row, int v);
 template <> __device__ __forceinline__ float row_at<uint16_t>(const uint16_t* row, int v) {
@@ -245,6 +250,7 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid == 0) {
       F.key[g] = 0u;
       F.first[g] = -1;
+      F.thr[g] = -INFINITY;
     }
     return;
   }
@@ -284,6 +290,7 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid == 0) {
       F.key[g] = 0u;
       F.first[g] = -1;
+      F.thr[g] = -INFINITY;
     }
     return;
   }
@@ -327,6 +334,7 @@ __global__ void __launch_bounds__(kSelThreads)
         }
         F.key[g] = key_of(tb);
         F.first[g] = ti;
+        F.thr[g] = tb;
       }
       return;
     }
@@ -484,6 +492,7 @@ __global__ void __launch_bounds__(kSelThreads)
     if (tid == 0) {
       F.key[g] = K;
       F.first[g] = -1;
+      F.thr[g] = thr_of_key(K);
     }
   };
   if (!draft) run(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * V);

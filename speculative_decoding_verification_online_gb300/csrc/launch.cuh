@@ -24,17 +24,17 @@ constexpr int pair_smem() {
          PairStages<TT, TD>::kBytes;
 }
 
-template <typename TT, typename TD, int G>
+template <typename TT, typename TD, int G, bool kFilt>
 cudaError_t configure_one(int fin_spread_smem) {
-  cudaError_t e = cudaFuncSetAttribute(stream_kernel<TT, TD, G>,
+  cudaError_t e = cudaFuncSetAttribute(stream_kernel<TT, TD, G, kFilt>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e != cudaSuccess) return e;
   const int fin = static_cast<int>(sizeof(FinishShared));
   const int fin_max = fin_spread_smem > fin ? fin_spread_smem : fin;
-  e = cudaFuncSetAttribute(finish_kernel<TT, TD, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(finish_kernel<TT, TD, G, false, kFilt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            fin_max);
   if (e != cudaSuccess || G == kModeGreedy) return e;
-  return cudaFuncSetAttribute(finish_kernel<TT, TD, G, G != kModeGreedy>,
+  return cudaFuncSetAttribute(finish_kernel<TT, TD, G, G != kModeGreedy, kFilt>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, fin_max);
 }
 
@@ -43,11 +43,13 @@ cudaError_t configure_one(int fin_spread_smem) {
 // stream CTAs fit on an SM
 template <typename TT, typename TD>
 cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
-  cudaError_t e = configure_one<TT, TD, kModeSample>(fin_spread_smem);
-  if (e == cudaSuccess) e = configure_one<TT, TD, kModePolicy>(fin_spread_smem);
-  if (e == cudaSuccess) e = configure_one<TT, TD, kModeGreedy>(fin_spread_smem);
+  cudaError_t e = configure_one<TT, TD, kModeSample, false>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModePolicy, false>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModeGreedy, false>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModeSample, true>(fin_spread_smem);
+  if (e == cudaSuccess) e = configure_one<TT, TD, kModePolicy, true>(fin_spread_smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeStats>,
+    e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeStats, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -57,7 +59,7 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
                              static_cast<int>(sizeof(SelShared)));
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
-                                                       stream_kernel<TT, TD, kModeSample>,
+                                                       stream_kernel<TT, TD, kModeSample, false>,
                                                        Stages<TT, TD>::kThreadsPerCta,
                                                        dyn_smem<TT, TD>());
 }
@@ -81,8 +83,9 @@ cudaError_t launch_dependent(K kernel, unsigned grid, unsigned threads, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// the stream pass (variant G), with the handle's one-shot timing marks around it
-template <typename TT, typename TD, int G>
+// the stream pass (variant G; kFilt: the sampler filters applied as chunks
+// load), with the handle's one-shot timing marks around it
+template <typename TT, typename TD, int G, bool kFilt>
 sv_status launch_stream(spec_verify_t h, const Params& P, int blocks_per_sm, cudaStream_t st) {
   long long grid = static_cast<long long>(h->num_sms) * blocks_per_sm;
   // a warp takes whole chunks, so more than total_chunks / warps-per-CTA CTAs idle
@@ -94,7 +97,7 @@ sv_status launch_stream(spec_verify_t h, const Params& P, int blocks_per_sm, cud
   if (marked && cudaEventRecord(h->mark_before, st) != cudaSuccess) return SV_ECUDA;
   // a programmatic dependent launch: resident early, it waits for the previous
   // kernel in the stream before touching memory
-  if (launch_dependent(stream_kernel<TT, TD, G>, static_cast<unsigned>(grid),
+  if (launch_dependent(stream_kernel<TT, TD, G, kFilt>, static_cast<unsigned>(grid),
                        Stages<TT, TD>::kThreadsPerCta, dyn_smem<TT, TD>(), st, P) != cudaSuccess)
     return SV_ECUDA;
   if (cudaGetLastError() != cudaSuccess) return SV_ECUDA;
@@ -106,10 +109,10 @@ sv_status launch_stream(spec_verify_t h, const Params& P, int blocks_per_sm, cud
   return SV_OK;
 }
 
-template <typename TT, typename TD, int G>
+template <typename TT, typename TD, int G, bool kFilt>
 sv_status launch(spec_verify_t h, const Params& P, int blocks_per_sm, bool dense_likely,
                  cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, G>(h, P, blocks_per_sm, st);
+  const sv_status rs = launch_stream<TT, TD, G, kFilt>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   // the finishing pass: one CTA per sequence, allowed to launch while the
   // stream pass drains; it waits (griddepcontrol.wait) before reading its output
@@ -153,9 +156,9 @@ sv_status launch(spec_verify_t h, const Params& P, int blocks_per_sm, bool dense
   // are likely; otherwise the one without it (greedy calls never need it)
   cudaError_t e;
   if (G != kModeGreedy && dense_likely)
-    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, G != kModeGreedy>, Pf);
+    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, G != kModeGreedy, kFilt>, Pf);
   else
-    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, false>, Pf);
+    e = cudaLaunchKernelEx(&cfg, finish_kernel<TT, TD, G, false, kFilt>, Pf);
   if (e != cudaSuccess) return SV_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
@@ -166,7 +169,7 @@ sv_status launch(spec_verify_t h, const Params& P, int blocks_per_sm, bool dense
 template <typename TT, typename TD, bool kGreedy>
 sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float* min_sum,
                       float* pq_sum, float* argmax_q, cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, kGreedy ? kModeGreedy : kModeStats>(h, P, blocks_per_sm, st);
+  const sv_status rs = launch_stream<TT, TD, kGreedy ? kModeGreedy : kModeStats, false>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned npos = static_cast<unsigned>(P.B * P.k);
   const unsigned small_grid = (npos + kDiagWarps - 1) / kDiagWarps;
@@ -190,16 +193,18 @@ sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
-// the filter prefix of a call: statistics pass, per-row thresholds, masked
-// copies; on return P reads the masked copies
+// The filter prefix of a call: the statistics pass of the raw rows, then each
+// row's kept set (select_kernel: threshold and, for top_k = 1, the kept
+// index).  A verifying call then applies them on the fly (P.fthr, P.ffirst:
+// its stream and finishing kernels mask every logit they load).  With
+// `copies` (the diagnostics, whose kernels read rows as they are) mask_kernel
+// also writes masked copies of the logits and P reads those instead.
 template <typename TT, typename TD>
-sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, cudaStream_t st) {
+sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool copies, cudaStream_t st) {
   const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
-  const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
-  const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
-  const size_t o_t = 0, o_d = align_up(bt, 256), o_key = align_up(o_d + bd, 256);
-  const size_t o_first = align_up(o_key + rows_all * sizeof(unsigned), 256);
-  const size_t need = align_up(o_first + rows_all * sizeof(int), 256);
+  const size_t o_key = 0, o_first = align_up(rows_all * sizeof(unsigned), 256);
+  const size_t o_thr = align_up(o_first + rows_all * sizeof(int), 256);
+  const size_t need = align_up(o_thr + rows_all * sizeof(float), 256);
   if (!h->fbuf) {
     if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
       h->fbuf = nullptr;
@@ -207,31 +212,49 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, cudaStre
     }
     h->fbuf_bytes = need;
   }
+  if (copies && !h->fcopy) {
+    // masked copies sized for max_B and fp32 (the larger element type)
+    const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
+    const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
+    if (cudaMalloc(&h->fcopy, align_up(bt, 256) + bd) != cudaSuccess) {
+      h->fcopy = nullptr;
+      return SV_ENOMEM;
+    }
+    h->fcopy_bytes = align_up(bt, 256) + bd;
+  }
   char* base = static_cast<char*>(h->fbuf);
   FilterParams F;
   F.f[0] = h->filt[0];
   F.f[1] = h->filt[1];
   F.key = reinterpret_cast<unsigned*>(base + o_key);
   F.first = reinterpret_cast<int*>(base + o_first);
-  F.Lt_m = base + o_t;
-  F.Ld_m = base + o_d;
-  sv_status rs = launch_stream<TT, TD, kModeStats>(h, P, blocks_per_sm, st);
+  F.thr = reinterpret_cast<float*>(base + o_thr);
+  F.Lt_m = copies ? h->fcopy : nullptr;
+  F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
+                        align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
+                  : nullptr;
+  sv_status rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
   if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
       cudaSuccess)
     return SV_ECUDA;
-  // one CTA per row at a time, at most eight per SM
-  long long grid = static_cast<long long>(P.B) * P.rows;
-  if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
-  if (grid < 1) grid = 1;
-  if (launch_dependent(mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(kMaskThreads),
-                       0, st, P, F) != cudaSuccess)
-    return SV_ECUDA;
-  P.Lt = F.Lt_m;
-  P.Ld = F.Ld_m;
-  P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
-  P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
+  if (copies) {
+    // one CTA per row at a time, at most eight per SM
+    long long grid = static_cast<long long>(P.B) * P.rows;
+    if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
+    if (grid < 1) grid = 1;
+    if (launch_dependent(mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(kMaskThreads),
+                         0, st, P, F) != cudaSuccess)
+      return SV_ECUDA;
+    P.Lt = F.Lt_m;
+    P.Ld = F.Ld_m;
+    P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
+    P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
+  } else {
+    P.fthr = F.thr;
+    P.ffirst = F.first;
+  }
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -241,13 +264,15 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, cudaStre
 template <typename TT, typename TD>
 sv_status verify_pair(spec_verify_t h, Params& P, int mode, int bps, bool dense_likely, bool filtered,
                       cudaStream_t st) {
+  if (mode == kModeGreedy) return launch<TT, TD, kModeGreedy, false>(h, P, bps, false, st);
   if (filtered) {
-    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, false, st);
     if (rs != SV_OK) return rs;
+    if (mode == kModePolicy) return launch<TT, TD, kModePolicy, true>(h, P, bps, dense_likely, st);
+    return launch<TT, TD, kModeSample, true>(h, P, bps, dense_likely, st);
   }
-  if (mode == kModeGreedy) return launch<TT, TD, kModeGreedy>(h, P, bps, false, st);
-  if (mode == kModePolicy) return launch<TT, TD, kModePolicy>(h, P, bps, dense_likely, st);
-  return launch<TT, TD, kModeSample>(h, P, bps, dense_likely, st);
+  if (mode == kModePolicy) return launch<TT, TD, kModePolicy, false>(h, P, bps, dense_likely, st);
+  return launch<TT, TD, kModeSample, false>(h, P, bps, dense_likely, st);
 }
 
 // the acceptance diagnostics, after the sampler filters' prefix when asked for
@@ -255,7 +280,7 @@ template <typename TT, typename TD>
 sv_status diag_pair(spec_verify_t h, Params& P, int bps, bool filtered, float* min_sum, float* pq_sum,
                     float* argmax_q, cudaStream_t st) {
   if (filtered) {
-    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, true, st);
     if (rs != SV_OK) return rs;
   }
   if (P.greedy) return launch_diag<TT, TD, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);

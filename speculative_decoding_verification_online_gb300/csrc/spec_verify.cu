@@ -66,7 +66,7 @@ const char* spec_verify_status_string(sv_status s) {
 
 int spec_verify_launches_per_run(void) { return 2; }
 
-int spec_verify_launches_per_filtered_run(void) { return 5; }
+int spec_verify_launches_per_filtered_run(void) { return 4; }
 
 sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after) {
   if (!h || (ev_before == nullptr) != (ev_after == nullptr)) return SV_EINVAL;
@@ -425,6 +425,7 @@ sv_status spec_verify_free(spec_verify_t h) {
     if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = SV_ECUDA;
     if (h->stage && cudaFree(h->stage) != cudaSuccess) rc = SV_ECUDA;
     if (h->fbuf && cudaFree(h->fbuf) != cudaSuccess) rc = SV_ECUDA;
+    if (h->fcopy && cudaFree(h->fcopy) != cudaSuccess) rc = SV_ECUDA;
   }
   delete h;
   return rc;

@@ -40,6 +40,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -129,6 +130,12 @@ struct Params {
   // finishing grid: CTAs [0, fin_warm) run the finishing code once, writing
   // nothing, while the stream pass drains (see finish_kernel)
   int fin_warm;
+  // sampler filters, per row g = b * rows + r (null: the call has none): the
+  // row keeps its logits x >= fthr[g] (-inf keeps every one), or -- when
+  // ffirst[g] >= 0, a top_k = 1 row -- only the entry at index ffirst[g]; the
+  // others read as -inf
+  const float* fthr;
+  const int* ffirst;
 };
 
 // ---------------------------------------------------------------- helpers
@@ -277,6 +284,29 @@ __device__ __forceinline__ bool gate_admits(float q, float tau, float cprev, boo
   return q >= tau && (!cum || cprev * q >= min_cum);
 }
 
+// ---- sampler filters applied on the fly (see Params::fthr)
+
+// one logit x at index v of a row with filter (thr, first)
+__device__ __forceinline__ float filt1(float x, int v, float thr, int first) {
+  if (first >= 0) return v == first ? x : -INFINITY;
+  return x < thr ? -INFINITY : x;  // ordered: a NaN stays (the row is then invalid)
+}
+// eight consecutive logits [v0, v0 + 8)
+__device__ __forceinline__ void filt8(float (&x)[8], int v0, float thr, int first) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x[e] = filt1(x[e], v0 + e, thr, first);
+}
+// the smallest bf16 value >= thr, as bf16 bits in both halves of a word: for
+// bf16 logits x, x >= thr iff x >= that value
+__device__ __forceinline__ uint32_t bf16_ceil_pair(float thr) {
+  const uint32_t u = __float_as_uint(thr);
+  uint32_t h = u >> 16;
+  // dropped low bits: truncation lowered a positive value (round its
+  // magnitude up) and raised a negative one (already above thr)
+  if ((u & 0xffffu) != 0u && !(u & 0x80000000u)) h += 1u;
+  return h | (h << 16);
+}
+
 // ------------------------------------------------------- chunk registers
 //
 // A warp holds one chunk: lane l owns NV 16-byte slots, slot i being vector
@@ -364,6 +394,27 @@ template <> struct Lane<uint16_t> {
     }
     return (a0 + a1) + (a2 + a3);
   }
+  // sampler filter: entries below the threshold (both halves of thr2 hold its
+  // bf16 ceiling) become -inf; the ordered compare keeps a NaN
+  __device__ __forceinline__ void mask(uint32_t thr2) {
+#pragma unroll
+    for (int q = 0; q < 4 * kNV; ++q) {
+      uint32_t m;
+      asm("set.lt.u32.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w[q]), "r"(thr2));
+      w[q] = (w[q] & ~m) | (0xFF80FF80u & m);
+    }
+  }
+  // a top_k = 1 row: every entry but chunk offset o_keep becomes -inf
+  __device__ __forceinline__ void keep_only(int o_keep, int lane) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int o = (32 * i + lane) * kVE + 2 * q;
+        const uint32_t lo = o == o_keep ? 0x0000ffffu : 0u, hi = o + 1 == o_keep ? 0xffff0000u : 0u;
+        w[4 * i + q] = (w[4 * i + q] & (lo | hi)) | (0xFF80FF80u & ~(lo | hi));
+      }
+  }
   // entries x of slot i with fma(x, c, nmc) >= lts, as a bit mask
   __device__ __forceinline__ unsigned slot_hits(int i, float c, float nmc, float lts) const {
     unsigned m = 0;
@@ -444,6 +495,18 @@ template <> struct Lane<float> {
     for (int e = 0; e < 4; ++e) m |= (fmaf(x[4 * i + e], c, nmc) >= lts ? 1u : 0u) << e;
     return m;
   }
+  // sampler filter: entries below the threshold become -inf (a NaN stays)
+  __device__ __forceinline__ void mask(float thr) {
+#pragma unroll
+    for (int e = 0; e < 4 * kNV; ++e) x[e] = x[e] < thr ? -INFINITY : x[e];
+  }
+  __device__ __forceinline__ void keep_only(int o_keep, int lane) {
+#pragma unroll
+    for (int i = 0; i < kNV; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((32 * i + lane) * kVE + e != o_keep) x[4 * i + e] = -INFINITY;
+  }
 };
 
 // ------------------------------------------------------- stream kernel
@@ -485,6 +548,11 @@ struct WarpQueue {
   int4 item[kItemRing];  // (b, r, ch, 1) of a chunk to stream; w = 0: no more work
   int d[kItemRing];      // the drafted token of the chunk's row (rows j < k), copied asynchronously
 };
+// a filtered call's queue also holds each chunk's row filter (threshold, kept index)
+struct WarpQueueFilt : WarpQueue {
+  float fthr[kItemRing];
+  int ffirst[kItemRing];
+};
 
 // lane 0: the warp's next chunk index, or kNoWork
 __device__ __forceinline__ unsigned next_chunk(const Params& P, unsigned* cta_next) {
@@ -494,8 +562,9 @@ __device__ __forceinline__ unsigned next_chunk(const Params& P, unsigned* cta_ne
 }
 
 // lane 0: decode chunk index x into item slot `slot` and start the copy of
-// its drafted token
-__device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot, unsigned x) {
+// its drafted token (and, kFilt, of its row's filter)
+template <bool kFilt, typename Queue>
+__device__ __forceinline__ void put_item(const Params& P, Queue& Q, int slot, unsigned x) {
   if (x == kNoWork) {
     Q.item[slot] = make_int4(0, 0, 0, 0);
     return;
@@ -507,6 +576,10 @@ __device__ __forceinline__ void put_item(const Params& P, WarpQueue& Q, int slot
   Q.item[slot] = make_int4(static_cast<int>(b), r, ch, 1);
   const int j = r <= P.k ? r : r - P.k - 1;
   if (j < P.k) cp_async4(&Q.d[slot], P.D + static_cast<int64_t>(b) * P.k + j);
+  if constexpr (kFilt) {
+    cp_async4(&Q.fthr[slot], P.fthr + rg);
+    cp_async4(&Q.ffirst[slot], P.ffirst + rg);
+  }
 }
 
 template <typename TT, typename TD>
@@ -555,9 +628,11 @@ __device__ __forceinline__ void process_chunk_greedy(const Params& P, const unsi
 }
 
 // one chunk, by one warp: statistics, drafted-token logit, gate candidates
-template <typename T, bool kPol, bool kCand>
+// (kFilt: of the row as its sampler filter leaves it, threshold fthr or kept
+// index ffirst)
+template <typename T, bool kPol, bool kCand, bool kFilt>
 __device__ __forceinline__ void process_chunk(const Params& P, const unsigned char* stage, int b, int r,
-                                              int ch, int d, int lane) {
+                                              int ch, int d, int lane, float fthr, int ffirst) {
   const int k = P.k;
   const int c0 = ch * kChunk;
   const bool is_draft = r > k;
@@ -565,6 +640,11 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
 
   Lane<T> regs;
   regs.load(stage, lane);
+  if constexpr (kFilt) {
+    if (ffirst >= 0) regs.keep_only(ffirst - c0, lane);
+    else if constexpr (sizeof(T) == 2) regs.mask(bf16_ceil_pair(fthr));
+    else regs.mask(fthr);
+  }
   // each lane sums against its own reference fl(m_l c); the warp then merges
   const float mine = regs.max();
   const float mct = mine == -INFINITY ? -INFINITY : mine * P.c;
@@ -577,7 +657,11 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   // the logit at the drafted token, written by the lane whose slot holds it
   if (j < k && d >= c0 && d < c0 + kChunk && d < P.V) {
     const int sv = (d - c0) / Lane<T>::kVE;
-    if ((sv & 31) == lane) P.xD[static_cast<int64_t>(b) * P.rows + r] = stage_logit<T>(stage, d - c0);
+    if ((sv & 31) == lane) {
+      float x = stage_logit<T>(stage, d - c0);
+      if constexpr (kFilt) x = filt1(x, d, fthr, ffirst);
+      P.xD[static_cast<int64_t>(b) * P.rows + r] = x;
+    }
   }
 
   // gated draft rows keep candidates only on the fast path (slack tau (kTopM + 1)
@@ -628,7 +712,8 @@ __device__ __forceinline__ void process_chunk(const Params& P, const unsigned ch
   }
 }
 
-template <typename TT, typename TD, int kMode>
+// kFilt: the call's sampler filters are applied to every chunk as it is loaded
+template <typename TT, typename TD, int kMode, bool kFilt>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
     stream_kernel(const __grid_constant__ Params P) {
   constexpr bool kPol = kMode == kModePolicy;
@@ -636,11 +721,12 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   constexpr int S = Stages<TT, TD>::kDepth;
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
-  __shared__ WarpQueue queues[Stages<TT, TD>::kWarpsPerCta];
+  using Queue = typename std::conditional<kFilt, WarpQueueFilt, WarpQueue>::type;
+  __shared__ Queue queues[Stages<TT, TD>::kWarpsPerCta];
   __shared__ unsigned cta_next;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* ring = stages + warp * S * kStage;
-  WarpQueue& Q = queues[warp];
+  Queue& Q = queues[warp];
   const int k = P.k;
 
   // item n (the warp's n-th chunk) is decoded at step n - 1, issued into ring
@@ -659,13 +745,13 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // wait above), and wait for this grid to complete and its memory to be
   // visible.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (lane == 0) put_item(P, Q, 0, next_chunk(P, &cta_next));
+  if (lane == 0) put_item<kFilt>(P, Q, 0, next_chunk(P, &cta_next));
   __syncwarp();
   int issued = 0;
   auto issue_next = [&]() {
     const int4 it = Q.item[issued % kItemRing];
     if (it.w > 0) issue_chunk<TT, TD>(P, it.x, it.y, it.z, ring + (issued % S) * kStage, lane);
-    if (lane == 0) put_item(P, Q, (issued + 1) % kItemRing, it.w > 0 ? next_chunk(P, &cta_next) : kNoWork);
+    if (lane == 0) put_item<kFilt>(P, Q, (issued + 1) % kItemRing, it.w > 0 ? next_chunk(P, &cta_next) : kNoWork);
     ++issued;
     cp_async_commit();
     __syncwarp();
@@ -679,14 +765,20 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     cp_async_wait<S - 1>();
     __syncwarp();
     const int d = Q.d[n % kItemRing];  // landed with the commit group of step n - 1
+    float fthr = 0.f;  // likewise
+    int ffirst = -1;
+    if constexpr (kFilt) {
+      fthr = Q.fthr[n % kItemRing];
+      ffirst = Q.ffirst[n % kItemRing];
+    }
     const unsigned char* stage = ring + (n % S) * kStage;
     if constexpr (kMode == kModeGreedy) {
       if (it.y <= k) process_chunk_greedy<TT>(P, stage, it.x, it.y, it.z, lane);
       else process_chunk_greedy<TD>(P, stage, it.x, it.y, it.z, lane);
     } else if (it.y <= k) {
-      process_chunk<TT, kPol, kCand>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TT, kPol, kCand, kFilt>(P, stage, it.x, it.y, it.z, d, lane, fthr, ffirst);
     } else {
-      process_chunk<TD, kPol, kCand>(P, stage, it.x, it.y, it.z, d, lane);
+      process_chunk<TD, kPol, kCand, kFilt>(P, stage, it.x, it.y, it.z, d, lane, fthr, ffirst);
     }
     __syncwarp();
   }
@@ -799,6 +891,8 @@ struct FinishShared {
   int fmode;  // the stop row's sampling mode (-1: the sequence is done)
   int dry;    // a warming run: global memory is read, never written
   int targ[kMaxRows];  // greedy calls: each row's first largest logit
+  float fthr[kMaxRows];  // filtered calls: each row's sampler-filter threshold and kept index
+  int ffirst[kMaxRows];
 };
 
 // residual weights of eight consecutive entries [v0, v0 + 8): max(0, p - mu)
@@ -885,6 +979,12 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
       if (draw == 1) sh.u1[tid] = u;
     }
   }
+  if (P.fthr && tid < P.rows) {
+    // the rows' sampler filters, chosen before the stream pass started (so
+    // complete when this grid launched)
+    sh.fthr[tid] = P.fthr[static_cast<int64_t>(b) * P.rows + tid];
+    sh.ffirst[tid] = P.ffirst[static_cast<int64_t>(b) * P.rows + tid];
+  }
   if (tid < k) {
     sh.Dv[tid] = __ldg(P.D + static_cast<int64_t>(b) * k + tid);
     sh.nadm[tid] = 0;
@@ -918,7 +1018,7 @@ __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishSh
   }
 }
 
-template <typename TT, typename TD, bool kPol>
+template <typename TT, typename TD, bool kPol, bool kFilt>
 __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
@@ -1003,6 +1103,7 @@ __device__ void finish_front(const Params& P, int b, FinishShared& sh) {
     cv = sh.cand_v[tid];
     cx = sh.cand_x[tid];
     cxt = logit_at<TT>(Lt + (static_cast<int64_t>(b) * (k + 1) + cj) * V, cv);
+    if constexpr (kFilt) cxt = filt1(cxt, cv, sh.fthr[cj], sh.ffirst[cj]);
   }
   {
     // the loops run the same trip count on every lane (a lane without an
@@ -1304,7 +1405,7 @@ __device__ void finish_greedy(const Params& P, int b, FinishShared& sh) {
 // every 8 n) and write the masses into the leading CTA's shared memory.  Lanes
 // take 8-entry groups lane, lane + 32, ... (16-byte coalesced loads), four
 // groups of both rows issued before use.
-template <typename TT, typename TD, bool kPol>
+template <typename TT, typename TD, bool kPol, bool kFilt>
 __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lead, float* lead_tile,
                                  int rank, int csize) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1337,10 +1438,14 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
       }
 #pragma unroll
       for (int g = 0; g < kLaneGroups; ++g) {
-        const float xt[8] = {bf16_lo(rt[g].x), bf16_hi(rt[g].x), bf16_lo(rt[g].y), bf16_hi(rt[g].y),
-                             bf16_lo(rt[g].z), bf16_hi(rt[g].z), bf16_lo(rt[g].w), bf16_hi(rt[g].w)};
-        const float xd[8] = {bf16_lo(rd[g].x), bf16_hi(rd[g].x), bf16_lo(rd[g].y), bf16_hi(rd[g].y),
-                             bf16_lo(rd[g].z), bf16_hi(rd[g].z), bf16_lo(rd[g].w), bf16_hi(rd[g].w)};
+        float xt[8] = {bf16_lo(rt[g].x), bf16_hi(rt[g].x), bf16_lo(rt[g].y), bf16_hi(rt[g].y),
+                       bf16_lo(rt[g].z), bf16_hi(rt[g].z), bf16_lo(rt[g].w), bf16_hi(rt[g].w)};
+        float xd[8] = {bf16_lo(rd[g].x), bf16_hi(rd[g].x), bf16_lo(rd[g].y), bf16_hi(rd[g].y),
+                       bf16_lo(rd[g].z), bf16_hi(rd[g].z), bf16_lo(rd[g].w), bf16_hi(rd[g].w)};
+        if constexpr (kFilt) {  // (rt, rd here are the raw vectors: the rows are jstar, k + 1 + jstar)
+          filt8(xt, c0 + (g * 32 + lane) * 8, lead.fthr[jstar], lead.ffirst[jstar]);
+          filt8(xd, c0 + (g * 32 + lane) * 8, lead.fthr[k + 1 + jstar], lead.ffirst[k + 1 + jstar]);
+        }
         float rr[8];
         residual8<kPol>(ev, xt, xd, c0 + (g * 32 + lane) * 8, V, rr);
         acc += ((rr[0] + rr[1]) + (rr[2] + rr[3])) + ((rr[4] + rr[5]) + (rr[6] + rr[7]));
@@ -1353,6 +1458,13 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
         for (int u = 0; u < 4; ++u) {
           load8<TT>(trow, c0 + ((h + u) * 32 + lane) * 8, V, vt, xt[u]);
           load8<TD>(drow, c0 + ((h + u) * 32 + lane) * 8, V, vd, xd[u]);
+        }
+        if constexpr (kFilt) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            filt8(xt[u], c0 + ((h + u) * 32 + lane) * 8, lead.fthr[rt], lead.ffirst[rt]);
+            filt8(xd[u], c0 + ((h + u) * 32 + lane) * 8, lead.fthr[rd], lead.ffirst[rd]);
+          }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -1367,7 +1479,7 @@ __device__ void dense_chunk_sums(const Params& P, int b, const FinishShared& lea
   }
 }
 
-template <typename TT, typename TD, bool kPol, bool kDense>
+template <typename TT, typename TD, bool kPol, bool kDense, bool kFilt>
 __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = P.k, R = P.rows, nch = P.nchunk, V = P.V;
@@ -1495,6 +1607,10 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
       float xt[8], xd[8];
       load8<TT>(trow, c0 + e0, V, vt, xt);
       if (ev.mode == 2) load8<TD>(drow, c0 + e0, V, vd, xd);
+      if constexpr (kFilt) {
+        filt8(xt, c0 + e0, sh.fthr[rt], sh.ffirst[rt]);
+        if (ev.mode == 2) filt8(xd, c0 + e0, sh.fthr[rd], sh.ffirst[rd]);
+      }
       residual8<kPol>(ev, xt, xd, c0 + e0, V, r8);
     }
     {
@@ -1583,7 +1699,7 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
 // The finishing grid runs in clusters of one or more CTAs (a cluster per
 // sequence at a time).  The leading CTA does all the work of a sequence except
 // the dense residual's chunk masses, which every CTA of the cluster shares.
-template <typename TT, typename TD, int kMode, bool kDense>
+template <typename TT, typename TD, int kMode, bool kDense, bool kFilt>
 __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_constant__ Params P) {
   constexpr bool kPol = kMode == kModePolicy;
   extern __shared__ __align__(16) unsigned char fin_smem[];
@@ -1625,17 +1741,17 @@ __global__ void __launch_bounds__(kFinThreads, 2) finish_kernel(const __grid_con
       }
       __syncthreads();
       if constexpr (kMode == kModeGreedy) finish_greedy<TT, TD>(P, b, sh);
-      else finish_front<TT, TD, kPol>(P, b, sh);
+      else finish_front<TT, TD, kPol, kFilt>(P, b, sh);
       __syncthreads();
     }
     if (csize > 1) cluster.sync();  // the leading CTA's decision, visible to the cluster
     const int fmode = lead->fmode;
     if constexpr (kDense) {
-      if (fmode == 2) dense_chunk_sums<TT, TD, kPol>(P, b, *lead, lead->tile, rank, csize);
+      if (fmode == 2) dense_chunk_sums<TT, TD, kPol, kFilt>(P, b, *lead, lead->tile, rank, csize);
       if (csize > 1) cluster.sync();  // every chunk mass is in the leading CTA
       else __syncthreads();
     }
-    if (rank == 0 && fmode >= 0) finish_back<TT, TD, kPol, kDense>(P, b, sh);
+    if (rank == 0 && fmode >= 0) finish_back<TT, TD, kPol, kDense, kFilt>(P, b, sh);
   }
 }
 
