@@ -50,14 +50,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((subprocess.Popen(cmd), obj, cmd))
-    failed = [cmd for p, _, cmd in procs if p.wait() != 0]
-    if failed:
-        raise subprocess.CalledProcessError(1, failed[0])
-    tmp = LIBRARY + f".tmp{os.getpid()}"
-    subprocess.run([nvcc(), *ARCH, "-shared", *[o for _, o, _ in procs], "-o", tmp], check=True)
-    os.replace(tmp, LIBRARY)
-    for _, obj, _ in procs:
-        os.remove(obj)
+    try:
+        failed = [cmd for p, _, cmd in procs if p.wait() != 0]
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIBRARY + f".tmp{os.getpid()}"
+        subprocess.run([nvcc(), *ARCH, "-shared", *[o for _, o, _ in procs], "-o", tmp], check=True)
+        os.replace(tmp, LIBRARY)
+    finally:
+        for _, obj, _ in procs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIBRARY
 
 

@@ -229,6 +229,63 @@ static __device__ unsigned list_descend(const unsigned* keys, const unsigned lon
   return prefix;
 }
 
+constexpr int kRankCap = 512;  // lists this short are selected by ranks (one entry per thread)
+
+// the same selection as list_descend for a short list (n <= kRankCap): each
+// thread takes one entry and sums the weights of the entries at or above it
+// (a sweep of the list, read by every thread at once), and the answer is the
+// largest key whose sum reaches the target -- one pass instead of four radix
+// levels with their barriers.  When no key reaches it (the radix descent then
+// ends at its lowest prefix), the smallest key at or above floor.
+static __device__ unsigned rank_select(const unsigned* keys, const unsigned long long* w, int n,
+                                       unsigned floor, double target, SelShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const double tc = ceil(target);
+  const unsigned long long tu = tc <= 0.0 ? 0ull : (tc >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(tc));
+  unsigned best = 0u, lowest = 0xffffffffu;
+  bool hit = false;
+  if (tid < n) {
+    const unsigned ki = keys[tid];
+    if (ki >= floor) {
+      unsigned long long acc = 0ull;
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const unsigned kj = keys[j];
+        if (kj >= ki) acc += w ? w[j] : 1ull;
+      }
+      hit = acc >= tu;
+      best = hit ? ki : 0u;
+      lowest = ki;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+    lowest = min(lowest, __shfl_xor_sync(0xffffffffu, lowest, o));
+  }
+  const unsigned any = __ballot_sync(0xffffffffu, hit);
+  if (lane == 0) {
+    sh.wfirst[warp] = static_cast<int>(best);
+    sh.wsum[warp] = (static_cast<unsigned long long>(any != 0u) << 32) | lowest;
+  }
+  __syncthreads();
+  unsigned K = 0u, low = 0xffffffffu;
+  bool found = false;
+  for (int q = 0; q < kSelWarps; ++q) {
+    K = max(K, static_cast<unsigned>(sh.wfirst[q]));
+    low = min(low, static_cast<unsigned>(sh.wsum[q] & 0xffffffffull));
+    found |= (sh.wsum[q] >> 32) != 0ull;
+  }
+  __syncthreads();
+  return found ? K : (low == 0xffffffffu ? floor : low);
+}
+
+static __device__ unsigned list_select(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
+                                       double target, SelShared& sh) {
+  if (n <= kRankCap) return rank_select(keys, w, n, floor, target, sh);
+  return list_descend(keys, w, n, floor, target, sh);
+}
+
 // the key K of each row (and the first index for top_k == 1)
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(kSelThreads)
@@ -351,32 +408,41 @@ __global__ void __launch_bounds__(kSelThreads)
       for (int ch = tid; ch < P.nchunk; ch += kSelThreads) sh.lkey[ch] = key_of(ldcg_f2(part + ch).x);
       if (tid == 0) sh.ln = 0;
       __syncthreads();
-      const float th = float_of_key(list_descend(sh.lkey, nullptr, P.nchunk, 0u,
-                                                  static_cast<double>(f.top_k), sh));
+      const float th = float_of_key(list_select(sh.lkey, nullptr, P.nchunk, 0u,
+                                                 static_cast<double>(f.top_k), sh));
       // warp-uniform trip count: the ballots below need every lane
 #pragma unroll
       for (int a = 0; a < kSelAhead; ++a) {
         const int vp = warp * 256 + lane * 8 + a * kSelWarps * 256;
         if (vp < V) prefetch_l2(row + vp);
       }
+      // two 256-entry blocks per warp and iteration, both loads issued before
+      // either is used
 #pragma unroll 1
-      for (int wb = warp * 256; wb < V; wb += kSelWarps * 256) {
-        const int v0 = wb + lane * 8;
-        if (v0 + kSelAhead * kSelWarps * 256 < V) prefetch_l2(row + v0 + kSelAhead * kSelWarps * 256);
-        float x[8];
-        load8<T>(row, v0, V, vec, x);  // entries past V read as -inf
+      for (int wb = warp * 256; wb < V; wb += 2 * kSelWarps * 256) {
+        float x[2][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const bool take = v0 + e < V && x[e] * c >= th;
-          const unsigned m = __ballot_sync(0xffffffffu, take);
-          if (m == 0u) continue;
-          int base = 0;
-          if (lane == __ffs(m) - 1) base = atomicAdd(&sh.ln, __popc(m));
-          base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-          const int pos = base + __popc(m & ((1u << lane) - 1u));
-          if (take && pos < kListCap) {
-            sh.lkey[pos] = key_of(x[e]);
-            sh.lmass[pos] = use_p ? __float2ull_rn(ex2_approx(fmaf(x[e], c, -Mc)) * kMassScalef) : 0ull;
+        for (int u = 0; u < 2; ++u) {
+          const int v0 = wb + u * kSelWarps * 256 + lane * 8;
+          if (v0 + kSelAhead * kSelWarps * 256 < V) prefetch_l2(row + v0 + kSelAhead * kSelWarps * 256);
+          load8<T>(row, v0, V, vec, x[u]);  // entries past V read as -inf
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int v0 = wb + u * kSelWarps * 256 + lane * 8;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool take = v0 + e < V && x[u][e] * c >= th;
+            const unsigned m = __ballot_sync(0xffffffffu, take);
+            if (m == 0u) continue;
+            int base = 0;
+            if (lane == __ffs(m) - 1) base = atomicAdd(&sh.ln, __popc(m));
+            base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
+            if (take && pos < kListCap) {
+              sh.lkey[pos] = key_of(x[u][e]);
+              sh.lmass[pos] = use_p ? __float2ull_rn(ex2_approx(fmaf(x[u][e], c, -Mc)) * kMassScalef) : 0ull;
+            }
           }
         }
       }
@@ -384,7 +450,7 @@ __global__ void __launch_bounds__(kSelThreads)
       const int n = sh.ln;
       if (n <= kListCap) {
         listed = true;
-        K = list_descend(sh.lkey, nullptr, n, 0u, static_cast<double>(f.top_k), sh);
+        K = list_select(sh.lkey, nullptr, n, 0u, static_cast<double>(f.top_k), sh);
         if (use_p) {
           // S_k: the mass of the top-k survivors; then top-p among them
           unsigned long long part_sum = 0ull;
@@ -400,8 +466,8 @@ __global__ void __launch_bounds__(kSelThreads)
             sh.Sk = t;
           }
           __syncthreads();
-          const unsigned Kp = list_descend(sh.lkey, sh.lmass, n, K,
-                                           static_cast<double>(f.top_p) * static_cast<double>(sh.Sk), sh);
+          const unsigned Kp = list_select(sh.lkey, sh.lmass, n, K,
+                                          static_cast<double>(f.top_p) * static_cast<double>(sh.Sk), sh);
           if (Kp > K) K = Kp;
         }
       }
