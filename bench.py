@@ -111,6 +111,16 @@ def filters_of(args):
     return None if ft == fd == (0, 1.0, 0.0) else (ft, fd)
 
 
+def filter_launches(filt, V, diagnostics):
+    """Launches the sampler filters add in front of a call: the statistics pass
+    and the selection, plus the bound and gathering passes when a side has
+    2 <= top_k <= the number of 2048-entry chunks (at most 512 chunks), plus
+    the masked copies of the diagnostics."""
+    nchunk = (V + 2047) // 2048
+    gathers = any(2 <= f[0] <= nchunk and nchunk <= 512 for f in filt)
+    return 2 + (2 if gathers else 0) + (1 if diagnostics else 0)
+
+
 def gate_args(args, w, cfg, sv):
     """The gate arguments of a call: the scalars when every sequence shares one
     mode and threshold (what a caller with one configuration passes; the host
@@ -585,11 +595,12 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             # the diagnostics launch 4 kernels per call (2 at temperature 0);
-            # sampler filters add 2 in front of a verifying call (statistics,
-            # selection) and 3 in front of the diagnostics (and masked copies)
+            # sampler filters add in front: statistics and selection (2), with
+            # the bound and gathering passes when a side's top-k set is
+            # gathered (+2), and masked copies for the diagnostics (+1)
             "gpu_launches": args.steps * (((2 if w0.T == 0 else 4) if args.diagnostics
                                            else sv.spec_verify_launches_per_run())
-                                          + ((3 if args.diagnostics else 2)
+                                          + (filter_launches(filt, w0.V, args.diagnostics)
                                              if filt is not None and w0.T > 0 else 0)),
             "clocks": clocks,
         }

@@ -35,7 +35,21 @@ struct FilterParams {
   float* thr;           // [B * rows] the same threshold as a logit: kept x >= thr (-inf: all)
   void* Lt_m;           // masked copies, same layouts and types as the inputs (null: none)
   void* Ld_m;
+  // top-k rows: the gathering pass before the selection (null: none) --
+  // gbound [B * rows] each row's lower bound of fl(x c) over its top-k set
+  // (+inf: not gathered), glist / gcount what the pass kept per chunk
+  float* gbound;
+  const float* glist;
+  const unsigned* gcount;
 };
+
+// rows whose top-k set the gathering pass collects: top_k >= 2 within the
+// number of chunks (see select_kernel), and a bound found among at most
+// kBoundCap chunk maxima
+constexpr int kBoundCap = 512;
+__host__ __device__ inline bool gathers_row(const Filter& f, int nchunk) {
+  return f.top_k >= 2 && f.top_k <= nchunk && nchunk <= kBoundCap;
+}
 
 constexpr int kSelThreads = 512;
 constexpr int kMaskThreads = 256;  // threads of a masking CTA
@@ -286,6 +300,50 @@ static __device__ unsigned list_select(const unsigned* keys, const unsigned long
   return list_descend(keys, w, n, floor, target, sh);
 }
 
+// Each row's lower bound of its top-k set for the gathering pass: the k-th
+// largest scaled chunk maximum (k distinct logits reach it, so the k-th
+// largest logit does too, and rounding is monotone), +inf for a row that is
+// not gathered.  One warp per row; the row's chunk maxima are staged in the
+// warp's shared memory and every lane ranks its own against all of them.
+constexpr int kBoundWarps = 8;
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(32 * kBoundWarps)
+    bound_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
+  __shared__ unsigned keys[kBoundWarps][kBoundCap];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = static_cast<int>(blockIdx.x) * kBoundWarps + warp;  // b * rows + r
+  if (g >= P.B * P.rows) return;
+  const Filter f = F.f[g % P.rows > P.k ? 1 : 0];
+  const int n = P.nchunk;
+  if (!gathers_row(f, n)) {
+    if (lane == 0) F.gbound[g] = INFINITY;
+    return;
+  }
+  const float2* part = P.part + static_cast<int64_t>(g) * n;
+  for (int ch = lane; ch < n; ch += 32) keys[warp][ch] = key_of(ldcg_f2(part + ch).x);
+  __syncwarp();
+  // the k-th largest key (counted with its repeats): the key with fewer than k
+  // keys above it and at least k at or above
+  unsigned K = 0u;
+  for (int i = lane; i < n; i += 32) {
+    const unsigned ki = keys[warp][i];
+    int gt = 0, ge = 0;
+    for (int j = 0; j < n; ++j) {
+      const unsigned kj = keys[warp][j];
+      gt += kj > ki;
+      ge += kj >= ki;
+    }
+    if (gt < f.top_k && f.top_k <= ge) K = ki;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) K = max(K, __shfl_xor_sync(0xffffffffu, K, o));
+  // a NaN chunk maximum (an invalid row) ranks as a key like any other; such
+  // a row is rejected by the verification whatever is gathered
+  if (lane == 0) F.gbound[g] = float_of_key(K);
+}
+
 // the key K of each row (and the first index for top_k == 1)
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(kSelThreads)
@@ -403,7 +461,38 @@ __global__ void __launch_bounds__(kSelThreads)
     // top-k set has fl(x c) at or above the k-th largest scaled chunk maximum.
     // One pass gathers those logits; the selections then run on the list.
     bool listed = false;
-    if (use_k && f.top_k <= P.nchunk) {
+    // the gathering pass's lists, when it ran and no chunk of the row overflowed
+    bool gathered = false;
+    if (use_k && F.gcount && gathers_row(f, P.nchunk)) {
+      if (tid == 0) {
+        sh.ln = 0;
+        sh.bad = 0;
+      }
+      __syncthreads();
+      const unsigned* cnt = F.gcount + static_cast<int64_t>(g) * P.nchunk;
+      const float* lst = F.glist + static_cast<int64_t>(g) * P.nchunk * kGatherCap;
+      for (int ch = tid; ch < P.nchunk; ch += kSelThreads) {
+        const unsigned m = __ldcg(cnt + ch);
+        if (m > static_cast<unsigned>(kGatherCap)) {
+          sh.bad = 1;  // (shared flag reused: the row reads itself below)
+          continue;
+        }
+        const int base = m ? atomicAdd(&sh.ln, static_cast<int>(m)) : 0;
+        for (unsigned i = 0; i < m; ++i) {
+          const float x = __ldcg(lst + ch * kGatherCap + i);
+          if (base + static_cast<int>(i) < kListCap) {
+            sh.lkey[base + i] = key_of(x);
+            sh.lmass[base + i] = use_p ? __float2ull_rn(ex2_approx(fmaf(x, c, -Mc)) * kMassScalef) : 0ull;
+          }
+        }
+      }
+      __syncthreads();
+      gathered = !sh.bad;
+      __syncthreads();
+      if (tid == 0) sh.bad = 0;
+      __syncthreads();
+    }
+    if (use_k && f.top_k <= P.nchunk && !gathered) {
       const float2* part = P.part + static_cast<int64_t>(g) * P.nchunk;
       for (int ch = tid; ch < P.nchunk; ch += kSelThreads) sh.lkey[ch] = key_of(ldcg_f2(part + ch).x);
       if (tid == 0) sh.ln = 0;
@@ -447,6 +536,8 @@ __global__ void __launch_bounds__(kSelThreads)
         }
       }
       __syncthreads();
+    }
+    if (use_k && f.top_k <= P.nchunk) {
       const int n = sh.ln;
       if (n <= kListCap) {
         listed = true;

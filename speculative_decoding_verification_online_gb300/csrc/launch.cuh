@@ -52,6 +52,9 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
     e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeStats, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeGather, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair_smem<TT, TD>());
   if (e == cudaSuccess)
@@ -202,9 +205,13 @@ sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float
 template <typename TT, typename TD>
 sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool copies, cudaStream_t st) {
   const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
+  const size_t chunks_all = rows_all * h->nchunk;
   const size_t o_key = 0, o_first = align_up(rows_all * sizeof(unsigned), 256);
   const size_t o_thr = align_up(o_first + rows_all * sizeof(int), 256);
-  const size_t need = align_up(o_thr + rows_all * sizeof(float), 256);
+  const size_t o_gb = align_up(o_thr + rows_all * sizeof(float), 256);
+  const size_t o_gc = align_up(o_gb + rows_all * sizeof(float), 256);
+  const size_t o_gl = align_up(o_gc + chunks_all * sizeof(unsigned), 256);
+  const size_t need = align_up(o_gl + chunks_all * kGatherCap * sizeof(float), 256);
   if (!h->fbuf) {
     if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
       h->fbuf = nullptr;
@@ -229,6 +236,9 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   F.key = reinterpret_cast<unsigned*>(base + o_key);
   F.first = reinterpret_cast<int*>(base + o_first);
   F.thr = reinterpret_cast<float*>(base + o_thr);
+  F.gbound = reinterpret_cast<float*>(base + o_gb);
+  F.gcount = nullptr;
+  F.glist = nullptr;
   F.Lt_m = copies ? h->fcopy : nullptr;
   F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
                         align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
@@ -236,6 +246,22 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   sv_status rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
+  if (gathers_row(F.f[0], P.nchunk) || gathers_row(F.f[1], P.nchunk)) {
+    // top-k rows: each row's lower bound from its chunk maxima, then the
+    // gathering pass keeps every logit at or above it, chunk by chunk
+    if (launch_dependent(bound_kernel<TT, TD>, (nrows + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, st,
+                         P, F) != cudaSuccess)
+      return SV_ECUDA;
+    Params Pg = P;
+    Pg.fthr = F.gbound;  // the gathering pass takes each row's bound in the threshold slot
+    Pg.ffirst = F.first;
+    Pg.gcount = reinterpret_cast<unsigned*>(base + o_gc);
+    Pg.glist = reinterpret_cast<float*>(base + o_gl);
+    rs = launch_stream<TT, TD, kModeGather, true>(h, Pg, blocks_per_sm, st);
+    if (rs != SV_OK) return rs;
+    F.gcount = Pg.gcount;
+    F.glist = Pg.glist;
+  }
   if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
       cudaSuccess)
     return SV_ECUDA;

@@ -66,8 +66,14 @@ constexpr float kGateSlack = 1.0f - 1.0f / 1024.0f;
 // greedy decoding (temperature 0, which honours the policy too).  Each is its
 // own instantiation, so the plain sampling path carries no policy code.
 // kModeStats is the stream pass alone (chunk statistics and drafted-token
-// logits, no gate candidates), for the acceptance diagnostics.
-enum : int { kModeSample = 0, kModePolicy = 1, kModeGreedy = 2, kModeStats = 3 };
+// logits, no gate candidates), for the acceptance diagnostics and the sampler
+// filters.  kModeGather is the sampler filters' gathering pass: every chunk
+// keeps the logits at or above its row's lower bound (see process_chunk_gather).
+enum : int { kModeSample = 0, kModePolicy = 1, kModeGreedy = 2, kModeStats = 3, kModeGather = 4 };
+
+// gathered logits kept per chunk by the gathering pass (more: the row's
+// selection reads the whole row itself)
+constexpr int kGatherCap = 32;
 
 struct Cand {  // a gate candidate: raw logit and token id (id -1: empty slot)
   float x;
@@ -121,6 +127,11 @@ struct Params {
   int8_t* flags;
   unsigned long long* counters;
   float* row_stats;
+  // the sampler filters' gathering pass (kModeGather): per chunk up to
+  // kGatherCap logits x with fl(x c) >= the row's bound (passed in fthr), and
+  // how many there were
+  float* glist;        // [B * rows * nchunk, kGatherCap]
+  unsigned* gcount;    // [B * rows * nchunk]
   // workspace
   float2* part;        // [B, rows, nchunk] (mc, s) per chunk
   float* xD;           // [B, rows] raw logit at the drafted token (rows j < k and draft rows)
@@ -627,6 +638,45 @@ __device__ __forceinline__ void process_chunk_greedy(const Params& P, const unsi
         make_float2(m, __int_as_float(bad ? -1 : ch * kChunk + first));
 }
 
+// one chunk of the sampler filters' gathering pass, by one warp: the logits x
+// with fl(x c) >= th (the row's lower bound of its top-k set; +inf: a row
+// that gathers nothing), up to kGatherCap of them in index order of the
+// lanes' slots, and their count
+template <typename T>
+__device__ __forceinline__ void process_chunk_gather(const Params& P, const unsigned char* stage, int b, int r,
+                                                     int ch, int lane, float th) {
+  const int64_t x = (static_cast<int64_t>(b) * P.rows + r) * P.nchunk + ch;
+  if (th == INFINITY) {
+    if (lane == 0) P.gcount[x] = 0u;
+    return;
+  }
+  Lane<T> regs;
+  regs.load(stage, lane);
+  unsigned hits[Lane<T>::kNV];
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < Lane<T>::kNV; ++i) {
+    hits[i] = regs.slot_hits(i, P.c, 0.f, th);  // fma(x, c, 0) is fl(x c)
+    mine += __popc(hits[i]);
+  }
+  int total;
+  int slot = warp_excl_scan_int(mine, lane, total);
+  float* out = P.glist + x * kGatherCap;
+  if (mine > 0) {
+#pragma unroll
+    for (int i = 0; i < Lane<T>::kNV; ++i) {
+      unsigned m = hits[i];
+      while (m) {
+        const int e = __ffs(m) - 1;
+        m &= m - 1;
+        if (slot < kGatherCap) out[slot] = stage_logit<T>(stage, (32 * i + lane) * Lane<T>::kVE + e);
+        ++slot;
+      }
+    }
+  }
+  if (lane == 0) P.gcount[x] = static_cast<unsigned>(total);
+}
+
 // one chunk, by one warp: statistics, drafted-token logit, gate candidates
 // (kFilt: of the row as its sampler filter leaves it, threshold fthr or kept
 // index ffirst)
@@ -717,7 +767,7 @@ template <typename TT, typename TD, int kMode, bool kFilt>
 __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>::kMinBlocks)
     stream_kernel(const __grid_constant__ Params P) {
   constexpr bool kPol = kMode == kModePolicy;
-  constexpr bool kCand = kMode != kModeStats;
+  constexpr bool kCand = kMode != kModeStats && kMode != kModeGather;
   constexpr int S = Stages<TT, TD>::kDepth;
   constexpr int kStage = Stages<TT, TD>::kBytes;
   extern __shared__ __align__(128) unsigned char stages[];
@@ -775,6 +825,10 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
     if constexpr (kMode == kModeGreedy) {
       if (it.y <= k) process_chunk_greedy<TT>(P, stage, it.x, it.y, it.z, lane);
       else process_chunk_greedy<TD>(P, stage, it.x, it.y, it.z, lane);
+    } else if constexpr (kMode == kModeGather) {
+      // (the row's bound rides in the filter-threshold slot of the queue)
+      if (it.y <= k) process_chunk_gather<TT>(P, stage, it.x, it.y, it.z, lane, fthr);
+      else process_chunk_gather<TD>(P, stage, it.x, it.y, it.z, lane, fthr);
     } else if (it.y <= k) {
       process_chunk<TT, kPol, kCand, kFilt>(P, stage, it.x, it.y, it.z, d, lane, fthr, ffirst);
     } else {
