@@ -113,12 +113,12 @@ def filters_of(args):
 
 def filter_launches(filt, V, diagnostics):
     """Launches the sampler filters add in front of a call: the statistics pass
-    and the selection, plus the bound and gathering passes when a side has
-    2 <= top_k <= the number of 2048-entry chunks (at most 512 chunks), plus
-    the masked copies of the diagnostics."""
+    and the selection, plus the bound, gathering and warp-selection passes when
+    a side has 2 <= top_k <= the number of 2048-entry chunks (at most 512
+    chunks), plus the masked copies of the diagnostics."""
     nchunk = (V + 2047) // 2048
     gathers = any(2 <= f[0] <= nchunk and nchunk <= 512 for f in filt)
-    return 2 + (2 if gathers else 0) + (1 if diagnostics else 0)
+    return 2 + (3 if gathers else 0) + (1 if diagnostics else 0)
 
 
 def gate_args(args, w, cfg, sv):
@@ -596,8 +596,8 @@ def main():
             "e2e": e2e,
             # the diagnostics launch 4 kernels per call (2 at temperature 0);
             # sampler filters add in front: statistics and selection (2), with
-            # the bound and gathering passes when a side's top-k set is
-            # gathered (+2), and masked copies for the diagnostics (+1)
+            # the bound, gathering and warp-selection passes when a side's
+            # top-k set is gathered (+3), and masked copies for the diagnostics (+1)
             "gpu_launches": args.steps * (((2 if w0.T == 0 else 4) if args.diagnostics
                                            else sv.spec_verify_launches_per_run())
                                           + (filter_launches(filt, w0.V, args.diagnostics)

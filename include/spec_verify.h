@@ -260,7 +260,7 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
  * SV_ENOMEM if it fails); for a top-k filter (2 <= top_k <= ceil(V / 2048)
  * <= 512) a gathering pass first collects each row's candidates chunk by
  * chunk.  Its verifying kernels then read every logit outside a row's kept
- * set as -inf (a NaN is kept, so the row stays invalid): 4 to 6 launches
+ * set as -inf (a NaN is kept, so the row stays invalid): 4 to 7 launches
  * instead of 2 and three or four reads of the logits.  row_stats then describe the filtered
  * rows.  spec_verify_diagnostics applies the same filters through masked
  * copies of the logits, in a second buffer of the handle (max_B * (2k+1) * V
@@ -273,7 +273,7 @@ sv_status spec_verify_set_filters(spec_verify_t h, int top_k_target, float top_p
                                   float min_p_draft);
 
 /* Kernel launches of a verifying call with sampler filters on (temperature > 0),
- * at most: 6 with a gathered top-k filter, 4 otherwise. */
+ * at most: 7 with a gathered top-k filter, 4 otherwise. */
 int spec_verify_launches_per_filtered_run(void);
 
 /* Release the handle and its device memory (NULL is a no-op).  Synchronises

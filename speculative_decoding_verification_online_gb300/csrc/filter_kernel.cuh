@@ -41,6 +41,7 @@ struct FilterParams {
   float* gbound;
   const float* glist;
   const unsigned* gcount;
+  int* done;            // [B * rows] the row was selected by warp_select_kernel (null: none was)
 };
 
 // rows whose top-k set the gathering pass collects: top_k >= 2 within the
@@ -344,6 +345,139 @@ __global__ void __launch_bounds__(32 * kBoundWarps)
   if (lane == 0) F.gbound[g] = float_of_key(K);
 }
 
+// rank_select for one warp: lane l takes entries l, l + 32, ...
+static __device__ unsigned warp_rank_select(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
+                                     double target) {
+  const int lane = threadIdx.x & 31;
+  const double tc = ceil(target);
+  const unsigned long long tu = tc <= 0.0 ? 0ull : (tc >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(tc));
+  unsigned best = 0u, lowest = 0xffffffffu;
+  bool hit = false;
+  for (int i = lane; i < n; i += 32) {
+    const unsigned ki = keys[i];
+    if (ki < floor) continue;
+    unsigned long long acc = 0ull;
+    for (int j = 0; j < n; ++j)
+      if (keys[j] >= ki) acc += w ? w[j] : 1ull;
+    if (acc >= tu) {
+      hit = true;
+      best = max(best, ki);
+    }
+    lowest = min(lowest, ki);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+    lowest = min(lowest, __shfl_xor_sync(0xffffffffu, lowest, o));
+  }
+  if (__any_sync(0xffffffffu, hit)) return best;
+  return lowest == 0xffffffffu ? floor : lowest;
+}
+
+// Rows whose top-k set the gathering pass collected in full (no chunk over
+// its cap, at most kRankCap logits in all): the whole selection by one warp on
+// the row's list in shared memory -- top-k by ranks, top-p among the top-k
+// survivors, min-p by bisection -- the decisions of select_kernel's list path.
+// Writes each such row's key, threshold and kept index and done[g] = 1; every
+// other row gets done[g] = 0 and is selected by select_kernel.
+constexpr int kWSelWarps = 4;
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(32 * kWSelWarps)
+    warp_select_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
+  __shared__ unsigned wkey[kWSelWarps][kRankCap];
+  __shared__ unsigned long long wmass[kWSelWarps][kRankCap];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = static_cast<int>(blockIdx.x) * kWSelWarps + warp;  // b * rows + r
+  if (g >= P.B * P.rows) return;
+  const Filter f = F.f[g % P.rows > P.k ? 1 : 0];
+  const int nch = P.nchunk;
+  const bool use_p = f.top_p < 1.f, use_m = f.min_p > 0.f;
+  if (!(f.top_k < P.V && gathers_row(f, nch))) {
+    if (lane == 0) F.done[g] = 0;
+    return;
+  }
+  // the row's scaled maximum (invalid rows: nothing to filter)
+  const float2* part = P.part + static_cast<int64_t>(g) * nch;
+  float M = -INFINITY;
+  for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, ldcg_f2(part + ch).x);
+  M = warp_max(M);
+  if (!(M > -INFINITY) || !isfinite(M)) {
+    if (lane == 0) {
+      F.key[g] = 0u;
+      F.first[g] = -1;
+      F.thr[g] = -INFINITY;
+      F.done[g] = 1;
+    }
+    return;
+  }
+  const float c = P.c, Mc = M;
+  // the lanes' chunks (lane l: chunks l, l + 32, ...), their counts and the list offsets
+  const unsigned* cnt = F.gcount + static_cast<int64_t>(g) * nch;
+  unsigned mine = 0u;
+  bool over = false;
+  for (int ch = lane; ch < nch; ch += 32) {
+    const unsigned m = __ldcg(cnt + ch);
+    over |= m > static_cast<unsigned>(kGatherCap);
+    mine += m;
+  }
+  int total;
+  const int base = warp_excl_scan_int(over ? 0 : static_cast<int>(mine), lane, total);
+  if (__any_sync(0xffffffffu, over) || total > kRankCap) {
+    if (lane == 0) F.done[g] = 0;
+    return;
+  }
+  const float* lst = F.glist + static_cast<int64_t>(g) * nch * kGatherCap;
+  int pos = base;
+  for (int ch = lane; ch < nch; ch += 32) {
+    const unsigned m = __ldcg(cnt + ch);
+    for (unsigned i = 0; i < m; ++i, ++pos) {
+      const float x = __ldcg(lst + ch * kGatherCap + i);
+      wkey[warp][pos] = key_of(x);
+      wmass[warp][pos] = use_p ? __float2ull_rn(ex2_approx(fmaf(x, c, -Mc)) * kMassScalef) : 0ull;
+    }
+  }
+  __syncwarp();
+  const int n = total;
+  const unsigned* keys = wkey[warp];
+  unsigned K = warp_rank_select(keys, nullptr, n, 0u, static_cast<double>(f.top_k));
+  if (use_p) {
+    // S_k: the mass of the top-k survivors; then top-p among them
+    unsigned long long sk = 0ull;
+    for (int i = lane; i < n; i += 32)
+      if (keys[i] >= K) sk += wmass[warp][i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, o);
+    const unsigned Kp = warp_rank_select(keys, wmass[warp], n, K, static_cast<double>(f.top_p) * static_cast<double>(sk));
+    if (Kp > K) K = Kp;
+  }
+  if (use_m) {
+    // the row's largest key is in the list (its chunk's maximum reaches the bound)
+    unsigned kmax = 0u;
+    for (int i = lane; i < n; i += 32) kmax = max(kmax, keys[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    if (lane == 0) {
+      const float lmp = log2f(f.min_p);
+      unsigned lo = 0u, hi = key_of(INFINITY);
+      while (hi - lo > 1u) {
+        const unsigned mid = lo + (hi - lo) / 2u;
+        const float xm = float_of_key(mid);
+        if (!isnan(xm) && fmaf(xm, c, -Mc) >= lmp) hi = mid;
+        else lo = mid;
+      }
+      K = max(K, min(hi, kmax));
+    }
+  }
+  if (lane == 0) {
+    F.key[g] = K;
+    F.first[g] = -1;
+    F.thr[g] = thr_of_key(K);
+    F.done[g] = 1;
+  }
+}
+
 // the key K of each row (and the first index for top_k == 1)
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(kSelThreads)
@@ -357,6 +491,7 @@ __global__ void __launch_bounds__(kSelThreads)
   const Filter f = F.f[draft ? 1 : 0];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (F.done && __ldcg(F.done + g)) return;  // selected by warp_select_kernel
   const int V = P.V;
   const bool use_k = f.top_k >= 2 && f.top_k < V;
   const bool use_p = f.top_p < 1.f;

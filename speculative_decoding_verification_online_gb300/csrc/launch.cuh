@@ -211,7 +211,8 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   const size_t o_gb = align_up(o_thr + rows_all * sizeof(float), 256);
   const size_t o_gc = align_up(o_gb + rows_all * sizeof(float), 256);
   const size_t o_gl = align_up(o_gc + chunks_all * sizeof(unsigned), 256);
-  const size_t need = align_up(o_gl + chunks_all * kGatherCap * sizeof(float), 256);
+  const size_t o_done = align_up(o_gl + chunks_all * kGatherCap * sizeof(float), 256);
+  const size_t need = align_up(o_done + rows_all * sizeof(int), 256);
   if (!h->fbuf) {
     if (cudaMalloc(&h->fbuf, need) != cudaSuccess) {
       h->fbuf = nullptr;
@@ -239,6 +240,7 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   F.gbound = reinterpret_cast<float*>(base + o_gb);
   F.gcount = nullptr;
   F.glist = nullptr;
+  F.done = nullptr;
   F.Lt_m = copies ? h->fcopy : nullptr;
   F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
                         align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
@@ -261,6 +263,11 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
     if (rs != SV_OK) return rs;
     F.gcount = Pg.gcount;
     F.glist = Pg.glist;
+    // gathered rows whose lists are short: selected by a warp each
+    F.done = reinterpret_cast<int*>(base + o_done);
+    if (launch_dependent(warp_select_kernel<TT, TD>, (nrows + kWSelWarps - 1) / kWSelWarps, 32 * kWSelWarps, 0,
+                         st, P, F) != cudaSuccess)
+      return SV_ECUDA;
   }
   if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
       cudaSuccess)

@@ -66,7 +66,7 @@ const char* spec_verify_status_string(sv_status s) {
 
 int spec_verify_launches_per_run(void) { return 2; }
 
-int spec_verify_launches_per_filtered_run(void) { return 6; }
+int spec_verify_launches_per_filtered_run(void) { return 7; }
 
 sv_status spec_verify_mark_next(spec_verify_t h, void* ev_before, void* ev_after) {
   if (!h || (ev_before == nullptr) != (ev_after == nullptr)) return SV_EINVAL;
