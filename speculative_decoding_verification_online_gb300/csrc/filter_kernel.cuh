@@ -345,33 +345,35 @@ __global__ void __launch_bounds__(32 * kBoundWarps)
   if (lane == 0) F.gbound[g] = float_of_key(K);
 }
 
-// rank_select for one warp: lane l takes entries l, l + 32, ...
-static __device__ unsigned warp_rank_select(const unsigned* keys, const unsigned long long* w, int n, unsigned floor,
-                                     double target) {
+// Descending bitonic sort of n <= N keys with their masses in shared memory,
+// by one warp (N a power of two, 32 <= N <= kRankCap); entries [n, N) are
+// filled with key 0 (below every logit's key) and mass 0 first.
+static __device__ void warp_sort_desc(unsigned* key, unsigned long long* mass, int n, int N) {
   const int lane = threadIdx.x & 31;
-  const double tc = ceil(target);
-  const unsigned long long tu = tc <= 0.0 ? 0ull : (tc >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(tc));
-  unsigned best = 0u, lowest = 0xffffffffu;
-  bool hit = false;
-  for (int i = lane; i < n; i += 32) {
-    const unsigned ki = keys[i];
-    if (ki < floor) continue;
-    unsigned long long acc = 0ull;
-    for (int j = 0; j < n; ++j)
-      if (keys[j] >= ki) acc += w ? w[j] : 1ull;
-    if (acc >= tu) {
-      hit = true;
-      best = max(best, ki);
+  for (int i = n + lane; i < N; i += 32) {
+    key[i] = 0u;
+    mass[i] = 0ull;
+  }
+  __syncwarp();
+  for (int k = 2; k <= N; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < N; i += 32) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned a = key[i], b = key[l];
+          // blocks with (i & k) == 0 run descending, the others ascending;
+          // the last merge (k = N) is descending throughout
+          if ((i & k) == 0 ? a < b : a > b) {
+            key[i] = b;
+            key[l] = a;
+            const unsigned long long t = mass[i];
+            mass[i] = mass[l];
+            mass[l] = t;
+          }
+        }
+      }
+      __syncwarp();
     }
-    lowest = min(lowest, ki);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
-    lowest = min(lowest, __shfl_xor_sync(0xffffffffu, lowest, o));
-  }
-  if (__any_sync(0xffffffffu, hit)) return best;
-  return lowest == 0xffffffffu ? floor : lowest;
 }
 
 // Rows whose top-k set the gathering pass collected in full (no chunk over
@@ -439,36 +441,61 @@ __global__ void __launch_bounds__(32 * kWSelWarps)
     }
   }
   __syncwarp();
+  // sorted by decreasing key: the k-th largest key (with its repeats) is the
+  // k-th entry; a key's weight at or above it is the prefix sum up to the
+  // last entry of its ties
   const int n = total;
-  const unsigned* keys = wkey[warp];
-  unsigned K = warp_rank_select(keys, nullptr, n, 0u, static_cast<double>(f.top_k));
+  int N = 32;
+  while (N < n) N <<= 1;
+  unsigned* keys = wkey[warp];
+  unsigned long long* mass = wmass[warp];
+  warp_sort_desc(keys, mass, n, N);
+  unsigned K = keys[f.top_k - 1];  // n >= top_k: each of the top_k chunks above the bound gave its maximum
   if (use_p) {
-    // S_k: the mass of the top-k survivors; then top-p among them
-    unsigned long long sk = 0ull;
-    for (int i = lane; i < n; i += 32)
-      if (keys[i] >= K) sk += wmass[warp][i];
+    // inclusive prefix sums of the masses in sorted order: each lane a run of N / 32
+    const int per = N / 32, i0 = lane * per;
+    unsigned long long run = 0ull;
+    for (int i = i0; i < i0 + per; ++i) run += mass[i];
+    unsigned long long incl = run;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    const unsigned Kp = warp_rank_select(keys, wmass[warp], n, K, static_cast<double>(f.top_p) * static_cast<double>(sk));
-    if (Kp > K) K = Kp;
-  }
-  if (use_m) {
-    // the row's largest key is in the list (its chunk's maximum reaches the bound)
-    unsigned kmax = 0u;
-    for (int i = lane; i < n; i += 32) kmax = max(kmax, keys[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    if (lane == 0) {
-      const float lmp = log2f(f.min_p);
-      unsigned lo = 0u, hi = key_of(INFINITY);
-      while (hi - lo > 1u) {
-        const unsigned mid = lo + (hi - lo) / 2u;
-        const float xm = float_of_key(mid);
-        if (!isnan(xm) && fmaf(xm, c, -Mc) >= lmp) hi = mid;
-        else lo = mid;
-      }
-      K = max(K, min(hi, kmax));
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    unsigned long long acc = incl - run;
+    for (int i = i0; i < i0 + per; ++i) {
+      acc += mass[i];
+      mass[i] = acc;
+    }
+    __syncwarp();
+    // S_k: the prefix up to the last entry at or above K; then the largest key
+    // (the first tie group) whose prefix reaches ceil(top_p S_k)
+    int last = 0;
+    for (int i = lane; i < N; i += 32)
+      if (keys[i] >= K && (i + 1 == N || keys[i + 1] < K)) last = i;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    const double tc = ceil(static_cast<double>(f.top_p) * static_cast<double>(mass[last]));
+    const unsigned long long tu = tc <= 0.0 ? 0ull : static_cast<unsigned long long>(tc);
+    int first_hit = N;
+    for (int i = lane; i <= last; i += 32)
+      if ((i + 1 == N || keys[i + 1] != keys[i]) && mass[i] >= tu) first_hit = min(first_hit, i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first_hit = min(first_hit, __shfl_xor_sync(0xffffffffu, first_hit, o));
+    if (first_hit < N && keys[first_hit] > K) K = keys[first_hit];
+  }
+  if (use_m && lane == 0) {
+    // min-p: the smallest key whose logit passes, but never above the row's largest key
+    const unsigned kmax = keys[0];
+    const float lmp = log2f(f.min_p);
+    unsigned lo = 0u, hi = key_of(INFINITY);
+    while (hi - lo > 1u) {
+      const unsigned mid = lo + (hi - lo) / 2u;
+      const float xm = float_of_key(mid);
+      if (!isnan(xm) && fmaf(xm, c, -Mc) >= lmp) hi = mid;
+      else lo = mid;
+    }
+    K = max(K, min(hi, kmax));
   }
   if (lane == 0) {
     F.key[g] = K;
