@@ -41,7 +41,7 @@ struct FilterParams {
   float* gbound;
   const float* glist;
   const unsigned* gcount;
-  int* done;            // [B * rows] the row was selected by warp_select_kernel (null: none was)
+  int* done;            // [B * rows] the row was selected by list_select_kernel (null: none was)
 };
 
 // rows whose top-k set the gathering pass collects: top_k >= 2 within the
@@ -345,24 +345,117 @@ __global__ void __launch_bounds__(32 * kBoundWarps)
   if (lane == 0) F.gbound[g] = float_of_key(K);
 }
 
-// Descending bitonic sort of n <= N keys with their masses in shared memory,
-// by one warp (N a power of two, 32 <= N <= kRankCap); entries [n, N) are
-// filled with key 0 (below every logit's key) and mass 0 first.
-static __device__ void warp_sort_desc(unsigned* key, unsigned long long* mass, int n, int N) {
-  const int lane = threadIdx.x & 31;
-  for (int i = n + lane; i < N; i += 32) {
+// Rows whose top-k set the gathering pass collected in full (no chunk over
+// its cap, at most kRankCap logits in all): the whole selection by a small CTA
+// per row on the row's list in shared memory -- a bitonic sort by decreasing
+// key, then top-k by position (the k-th largest key with its repeats), top-p
+// by a prefix sum over the top-k survivors' masses, min-p by bisection: the
+// decisions of select_kernel's list path.  Writes each such row's key,
+// threshold and kept index and done[g] = 1; every other row gets done[g] = 0
+// and is selected by select_kernel.
+constexpr int kLSelThreads = 256;
+constexpr int kLSelWarps = kLSelThreads / 32;
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(kLSelThreads)
+    list_select_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
+  __shared__ unsigned key[kRankCap];
+  __shared__ unsigned long long mass[kRankCap];
+  __shared__ unsigned long long wred[kLSelWarps];
+  __shared__ float wmax[kLSelWarps];
+  __shared__ int wint[kLSelWarps];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = static_cast<int>(blockIdx.x);  // b * rows + r
+  const Filter f = F.f[g % P.rows > P.k ? 1 : 0];
+  const int nch = P.nchunk;
+  const bool use_p = f.top_p < 1.f, use_m = f.min_p > 0.f;
+  if (!(f.top_k < P.V && gathers_row(f, nch))) {
+    if (tid == 0) F.done[g] = 0;
+    return;
+  }
+  // the row's scaled maximum; the counts of chunks tid and tid + kLSelThreads
+  // (nch <= kBoundCap = 2 kLSelThreads) and their list offsets (block scans
+  // in chunk order)
+  const float2* part = P.part + static_cast<int64_t>(g) * nch;
+  const unsigned* cnt = F.gcount + static_cast<int64_t>(g) * nch;
+  float M = -INFINITY;
+  unsigned m0 = 0u, m1 = 0u;
+  if (tid < nch) {
+    M = ldcg_f2(part + tid).x;
+    m0 = __ldcg(cnt + tid);
+  }
+  if (tid + kLSelThreads < nch) {
+    M = fmaxf(M, ldcg_f2(part + tid + kLSelThreads).x);
+    m1 = __ldcg(cnt + tid + kLSelThreads);
+  }
+  const int over = (m0 > static_cast<unsigned>(kGatherCap)) || (m1 > static_cast<unsigned>(kGatherCap));
+  if (over) m0 = m1 = 0u;
+  M = warp_max(M);
+  if (lane == 0) wmax[warp] = M;
+  int tot0, tot1;
+  const int w0 = warp_excl_scan_int(static_cast<int>(m0), lane, tot0);
+  const int w1 = warp_excl_scan_int(static_cast<int>(m1), lane, tot1);
+  if (lane == 0) {
+    wint[warp] = tot0;
+    wred[warp] = static_cast<unsigned long long>(tot1);
+  }
+  const int anyover = __syncthreads_or(over);
+  int base0 = 0, all0 = 0, base1 = 0, all1 = 0;
+  M = -INFINITY;
+  for (int w = 0; w < kLSelWarps; ++w) {
+    if (w < warp) {
+      base0 += wint[w];
+      base1 += static_cast<int>(wred[w]);
+    }
+    all0 += wint[w];
+    all1 += static_cast<int>(wred[w]);
+    M = fmaxf(M, wmax[w]);
+  }
+  const int n = all0 + all1;
+  base1 += all0;
+  __syncthreads();
+  if (!(M > -INFINITY) || !isfinite(M)) {  // an invalid row: nothing to filter
+    if (tid == 0) {
+      F.key[g] = 0u;
+      F.first[g] = -1;
+      F.thr[g] = -INFINITY;
+      F.done[g] = 1;
+    }
+    return;
+  }
+  if (anyover || n > kRankCap) {
+    if (tid == 0) F.done[g] = 0;
+    return;
+  }
+  const float c = P.c, Mc = M;
+  // the list: every thread copies its chunks' entries to their offsets
+  const float* lst = F.glist + static_cast<int64_t>(g) * nch * kGatherCap;
+  auto copy_chunk = [&](int ch, unsigned m, int o) {
+#pragma unroll 4
+    for (unsigned i = 0; i < m; ++i) {
+      const float x = __ldcg(lst + ch * kGatherCap + i);
+      key[o + i] = key_of(x);
+      mass[o + i] = use_p ? __float2ull_rn(ex2_approx(fmaf(x, c, -Mc)) * kMassScalef) : 0ull;
+    }
+  };
+  copy_chunk(tid, m0, base0 + w0);
+  copy_chunk(tid + kLSelThreads, m1, base1 + w1);
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int i = n + tid; i < N; i += kLSelThreads) {  // padding below every logit's key
     key[i] = 0u;
     mass[i] = 0ull;
   }
-  __syncwarp();
+  __syncthreads();
+  // bitonic sort by decreasing key (blocks with (i & k) == 0 run descending;
+  // the last merge, k = N, is descending throughout)
   for (int k = 2; k <= N; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lane; i < N; i += 32) {
+      for (int i = tid; i < N; i += kLSelThreads) {
         const int l = i ^ j;
         if (l > i) {
           const unsigned a = key[i], b = key[l];
-          // blocks with (i & k) == 0 run descending, the others ascending;
-          // the last merge (k = N) is descending throughout
           if ((i & k) == 0 ? a < b : a > b) {
             key[i] = b;
             key[l] = a;
@@ -372,132 +465,65 @@ static __device__ void warp_sort_desc(unsigned* key, unsigned long long* mass, i
           }
         }
       }
-      __syncwarp();
+      __syncthreads();
     }
-}
-
-// Rows whose top-k set the gathering pass collected in full (no chunk over
-// its cap, at most kRankCap logits in all): the whole selection by one warp on
-// the row's list in shared memory -- top-k by ranks, top-p among the top-k
-// survivors, min-p by bisection -- the decisions of select_kernel's list path.
-// Writes each such row's key, threshold and kept index and done[g] = 1; every
-// other row gets done[g] = 0 and is selected by select_kernel.
-constexpr int kWSelWarps = 4;
-template <typename TT, typename TD>
-__global__ void __launch_bounds__(32 * kWSelWarps)
-    warp_select_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
-  __shared__ unsigned wkey[kWSelWarps][kRankCap];
-  __shared__ unsigned long long wmass[kWSelWarps][kRankCap];
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = static_cast<int>(blockIdx.x) * kWSelWarps + warp;  // b * rows + r
-  if (g >= P.B * P.rows) return;
-  const Filter f = F.f[g % P.rows > P.k ? 1 : 0];
-  const int nch = P.nchunk;
-  const bool use_p = f.top_p < 1.f, use_m = f.min_p > 0.f;
-  if (!(f.top_k < P.V && gathers_row(f, nch))) {
-    if (lane == 0) F.done[g] = 0;
-    return;
-  }
-  // the row's scaled maximum (invalid rows: nothing to filter)
-  const float2* part = P.part + static_cast<int64_t>(g) * nch;
-  float M = -INFINITY;
-  for (int ch = lane; ch < nch; ch += 32) M = fmaxf(M, ldcg_f2(part + ch).x);
-  M = warp_max(M);
-  if (!(M > -INFINITY) || !isfinite(M)) {
-    if (lane == 0) {
-      F.key[g] = 0u;
-      F.first[g] = -1;
-      F.thr[g] = -INFINITY;
-      F.done[g] = 1;
-    }
-    return;
-  }
-  const float c = P.c, Mc = M;
-  // the lanes' chunks (lane l: chunks l, l + 32, ...), their counts and the list offsets
-  const unsigned* cnt = F.gcount + static_cast<int64_t>(g) * nch;
-  unsigned mine = 0u;
-  bool over = false;
-  for (int ch = lane; ch < nch; ch += 32) {
-    const unsigned m = __ldcg(cnt + ch);
-    over |= m > static_cast<unsigned>(kGatherCap);
-    mine += m;
-  }
-  int total;
-  const int base = warp_excl_scan_int(over ? 0 : static_cast<int>(mine), lane, total);
-  if (__any_sync(0xffffffffu, over) || total > kRankCap) {
-    if (lane == 0) F.done[g] = 0;
-    return;
-  }
-  const float* lst = F.glist + static_cast<int64_t>(g) * nch * kGatherCap;
-  int pos = base;
-  for (int ch = lane; ch < nch; ch += 32) {
-    const unsigned m = __ldcg(cnt + ch);
-    for (unsigned i = 0; i < m; ++i, ++pos) {
-      const float x = __ldcg(lst + ch * kGatherCap + i);
-      wkey[warp][pos] = key_of(x);
-      wmass[warp][pos] = use_p ? __float2ull_rn(ex2_approx(fmaf(x, c, -Mc)) * kMassScalef) : 0ull;
-    }
-  }
-  __syncwarp();
-  // sorted by decreasing key: the k-th largest key (with its repeats) is the
-  // k-th entry; a key's weight at or above it is the prefix sum up to the
-  // last entry of its ties
-  const int n = total;
-  int N = 32;
-  while (N < n) N <<= 1;
-  unsigned* keys = wkey[warp];
-  unsigned long long* mass = wmass[warp];
-  warp_sort_desc(keys, mass, n, N);
-  unsigned K = keys[f.top_k - 1];  // n >= top_k: each of the top_k chunks above the bound gave its maximum
+  // n >= top_k: each of the top_k chunks at or above the bound gave its maximum
+  unsigned K = key[f.top_k - 1];
   if (use_p) {
-    // inclusive prefix sums of the masses in sorted order: each lane a run of N / 32
-    const int per = N / 32, i0 = lane * per;
-    unsigned long long run = 0ull;
-    for (int i = i0; i < i0 + per; ++i) run += mass[i];
+    // inclusive prefix sums of the masses in sorted order (thread t: entries
+    // 2t and 2t + 1; N <= 2 kLSelThreads)
+    const int i0 = 2 * tid;
+    const unsigned long long a0 = i0 < N ? mass[i0] : 0ull, a1 = i0 + 1 < N ? mass[i0 + 1] : 0ull;
+    const unsigned long long run = a0 + a1;
     unsigned long long incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    unsigned long long acc = incl - run;
-    for (int i = i0; i < i0 + per; ++i) {
-      acc += mass[i];
-      mass[i] = acc;
-    }
-    __syncwarp();
+    __syncthreads();
+    if (lane == 31) wred[warp] = incl;
+    __syncthreads();
+    unsigned long long before = incl - run;
+    for (int w = 0; w < warp; ++w) before += wred[w];
+    if (i0 < N) mass[i0] = before + a0;
+    if (i0 + 1 < N) mass[i0 + 1] = before + a0 + a1;
+    __syncthreads();
     // S_k: the prefix up to the last entry at or above K; then the largest key
     // (the first tie group) whose prefix reaches ceil(top_p S_k)
     int last = 0;
-    for (int i = lane; i < N; i += 32)
-      if (keys[i] >= K && (i + 1 == N || keys[i + 1] < K)) last = i;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    for (int i = tid; i < N; i += kLSelThreads)
+      if (key[i] >= K && (i + 1 == N || key[i + 1] < K)) last = i;
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0) wint[warp] = last;
+    __syncthreads();
+    for (int w = 0; w < kLSelWarps; ++w) last = max(last, wint[w]);
     const double tc = ceil(static_cast<double>(f.top_p) * static_cast<double>(mass[last]));
     const unsigned long long tu = tc <= 0.0 ? 0ull : static_cast<unsigned long long>(tc);
-    int first_hit = N;
-    for (int i = lane; i <= last; i += 32)
-      if ((i + 1 == N || keys[i + 1] != keys[i]) && mass[i] >= tu) first_hit = min(first_hit, i);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) first_hit = min(first_hit, __shfl_xor_sync(0xffffffffu, first_hit, o));
-    if (first_hit < N && keys[first_hit] > K) K = keys[first_hit];
+    int hit = N;
+    for (int i = tid; i <= last; i += kLSelThreads)
+      if ((i + 1 == N || key[i + 1] != key[i]) && mass[i] >= tu) hit = min(hit, i);
+    hit = __reduce_min_sync(0xffffffffu, hit);
+    __syncthreads();
+    if (lane == 0) wint[warp] = hit;
+    __syncthreads();
+    for (int w = 0; w < kLSelWarps; ++w) hit = min(hit, wint[w]);
+    if (hit < N && key[hit] > K) K = key[hit];
   }
-  if (use_m && lane == 0) {
-    // min-p: the smallest key whose logit passes, but never above the row's largest key
-    const unsigned kmax = keys[0];
-    const float lmp = log2f(f.min_p);
-    unsigned lo = 0u, hi = key_of(INFINITY);
-    while (hi - lo > 1u) {
-      const unsigned mid = lo + (hi - lo) / 2u;
-      const float xm = float_of_key(mid);
-      if (!isnan(xm) && fmaf(xm, c, -Mc) >= lmp) hi = mid;
-      else lo = mid;
+  if (tid == 0) {
+    if (use_m) {
+      // min-p: the smallest key whose logit passes, never above the row's largest
+      const unsigned kmax = key[0];
+      const float lmp = log2f(f.min_p);
+      unsigned lo = 0u, hi = key_of(INFINITY);
+      while (hi - lo > 1u) {
+        const unsigned mid = lo + (hi - lo) / 2u;
+        const float xm = float_of_key(mid);
+        if (!isnan(xm) && fmaf(xm, c, -Mc) >= lmp) hi = mid;
+        else lo = mid;
+      }
+      K = max(K, min(hi, kmax));
     }
-    K = max(K, min(hi, kmax));
-  }
-  if (lane == 0) {
     F.key[g] = K;
     F.first[g] = -1;
     F.thr[g] = thr_of_key(K);
@@ -518,7 +544,7 @@ __global__ void __launch_bounds__(kSelThreads)
   const Filter f = F.f[draft ? 1 : 0];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (F.done && __ldcg(F.done + g)) return;  // selected by warp_select_kernel
+  if (F.done && __ldcg(F.done + g)) return;  // selected by list_select_kernel
   const int V = P.V;
   const bool use_k = f.top_k >= 2 && f.top_k < V;
   const bool use_p = f.top_p < 1.f;

@@ -263,10 +263,9 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
     if (rs != SV_OK) return rs;
     F.gcount = Pg.gcount;
     F.glist = Pg.glist;
-    // gathered rows whose lists are short: selected by a warp each
+    // gathered rows whose lists are short: selected by a small CTA each
     F.done = reinterpret_cast<int*>(base + o_done);
-    if (launch_dependent(warp_select_kernel<TT, TD>, (nrows + kWSelWarps - 1) / kWSelWarps, 32 * kWSelWarps, 0,
-                         st, P, F) != cudaSuccess)
+    if (launch_dependent(list_select_kernel<TT, TD>, nrows, kLSelThreads, 0, st, P, F) != cudaSuccess)
       return SV_ECUDA;
   }
   if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
