@@ -141,11 +141,20 @@ def gate_policy(args):
     return sched, float(args.min_cum)
 
 
+# the sources the verifying call's stream and finishing kernels are built
+# from: their code, launch configuration and arguments (the filter and
+# diagnostics kernels live in files of their own)
+STREAM_SOURCES = ("csrc/verify_kernel.cuh", "csrc/philox.cuh", "csrc/launch.cuh", "csrc/handle.h",
+                  "csrc/spec_verify.cu", "csrc/pair_bf16_bf16.cu")
+
+
 def kernel_hash() -> str:
+    """Hash of the files the stream kernel's profile depends on."""
     h = hashlib.sha256()
-    pkg = os.path.join(ROOT, "speculative_decoding_verification_online_gb300", "csrc")
-    for f in sorted(glob.glob(os.path.join(pkg, "*"))):
-        h.update(open(f, "rb").read())
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_online_gb300")
+    for f in sorted(STREAM_SOURCES):
+        h.update(open(os.path.join(pkg, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "spec_verify.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
