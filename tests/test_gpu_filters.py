@@ -180,3 +180,61 @@ def test_filters_with_a_gate_policy(sv, dtype):
     assert st["compared"] >= B // 2
     assert int((ref["flags"] == 3).sum()) > 0  # the gate still bites on the filtered q
     ver.close()
+
+
+# Rows whose top-k set the gathering pass collects (2 <= top_k <= the number
+# of 2048-entry chunks).  Both sides gathered: no statistics pass runs; one
+# side: the statistics pass runs and the other side selects from it.
+GATHERED = {
+    "both_topk": ((8, 1.0, 0.0), (12, 1.0, 0.0)),
+    "both_topk_topp_minp": ((16, 0.9, 0.02), (5, 0.85, 0.0)),
+    "target_only": ((8, 1.0, 0.0), (0, 0.9, 0.0)),
+}
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 40000), ("f32", 30001)])
+@pytest.mark.parametrize("name", sorted(GATHERED))
+def test_gathered_filter_parity(sv, dtype, V, name):
+    filt = GATHERED[name]
+    B, k = 32, 3
+    gate = (np.arange(B) % 2).astype(np.uint8)
+    seed = 500 + 5 * sorted(GATHERED).index(name) + (dtype == "f32")
+    w = _filtered_drafts(peaked_workload(B, k, V, dtype, seed=seed, gate=gate, tau=0.3, T=0.9), filt[1])
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w, filters=filt)
+    st = compare(w, out, ref, what=f"gathered {name} {dtype} V={V}", filters=filt)
+    ok = ref["margin"] >= 1e-6
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
+    assert st["compared"] >= B // 2
+    ver.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gathered_lists_that_overflow_fall_back(sv, dtype):
+    # integer logits: a chunk holds hundreds of logits tied at the top value,
+    # more than its 32 gathering slots, so every row is selected by the
+    # fallback (which, with no statistics pass, reads the row itself); the
+    # kept sets (every tie of the k-th largest) stay exact
+    B, k, V = 16, 2, 16384
+    g = torch.Generator(device="cuda")
+    g.manual_seed(71 + (dtype == "f32"))
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Lt = torch.randint(-3, 4, (B, k + 1, V), generator=g, device="cuda").float()
+    Ld = (Lt[:, :k] + torch.randint(-1, 2, (B, k, V), generator=g, device="cuda").float())
+    u = torch.rand(B, k, V, generator=g, device="cuda").clamp_(1e-30, 1 - 1e-7)
+    D = torch.argmax(Ld - torch.log(-torch.log(u)), dim=2).to(torch.int32)
+    w = workloads.Workload(name="ties", Lt=Lt.to(dt), Ld=Ld.to(dt), D=D, T=1.0,
+                           gate=torch.zeros(B, dtype=torch.uint8, device="cuda"),
+                           tau=torch.full((B,), 0.5, device="cuda"), philox_seed=9, B=B, k=k, V=V,
+                           dtype=dtype)
+    filt = ((4, 1.0, 0.0), (4, 0.9, 0.0))
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = _run(sv, ver, w)
+    ref = oracle_for(w, filters=filt)
+    st = compare(w, out, ref, what=f"gathered overflow {dtype}", filters=filt)
+    assert st["compared"] + st["boundary"] == B
+    ver.close()
