@@ -113,15 +113,12 @@ def filters_of(args):
 
 def filter_launches(filt, V, diagnostics):
     """Launches the sampler filters add in front of a call: the statistics pass
-    and the selection, plus the bound, gathering and list-selection passes when
+    and the selection, plus the bound, gathering and warp-selection passes when
     a side has 2 <= top_k <= the number of 2048-entry chunks (at most 512
-    chunks), plus the masked copies of the diagnostics; a verifying call whose
-    both sides gather runs no statistics pass (4 launches)."""
+    chunks), plus the masked copies of the diagnostics."""
     nchunk = (V + 2047) // 2048
-    gather = [2 <= f[0] <= nchunk and nchunk <= 512 for f in filt]
-    if all(gather) and not diagnostics:
-        return 4  # no statistics pass: subset bound, gathering, list and leftover selection
-    return 2 + (3 if any(gather) else 0) + (1 if diagnostics else 0)
+    gathers = any(2 <= f[0] <= nchunk and nchunk <= 512 for f in filt)
+    return 2 + (3 if gathers else 0) + (1 if diagnostics else 0)
 
 
 def gate_args(args, w, cfg, sv):

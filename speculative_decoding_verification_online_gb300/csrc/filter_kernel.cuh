@@ -42,7 +42,6 @@ struct FilterParams {
   const float* glist;
   const unsigned* gcount;
   int* done;            // [B * rows] the row was selected by list_select_kernel (null: none was)
-  int have_part;        // a statistics pass ran: P.part holds this call's chunk statistics
 };
 
 // rows whose top-k set the gathering pass collects: top_k >= 2 within the
@@ -346,104 +345,6 @@ __global__ void __launch_bounds__(32 * kBoundWarps)
   if (lane == 0) F.gbound[g] = float_of_key(K);
 }
 
-// Each row's lower bound of its top-k set when no statistics pass runs (both
-// sides gather): the k-th largest logit among the row's first kSubsetChunks
-// chunks -- any k distinct logits of a row bound its k-th largest from below
-// -- scaled like the chunk maxima, fl(x c).  A CTA per row: a radix descent
-// on the keys, 8 bits a level (bf16 keys carry 16 significant bits: two
-// levels; a negative bf16 bound then reads a hair lower, still a bound),
-// re-reading the subset (from L2) at each level.
-constexpr int kSubsetChunks = 16;
-constexpr int kSubThreads = 256;
-template <typename TT, typename TD>
-__global__ void __launch_bounds__(kSubThreads)
-    subset_bound_kernel(const __grid_constant__ Params P, const __grid_constant__ FilterParams F) {
-  __shared__ unsigned hist[256];
-  __shared__ unsigned sdigit, sabove;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int g = static_cast<int>(blockIdx.x);  // b * rows + r
-  const int b = g / P.rows, r = g % P.rows;
-  const bool draft = r > P.k;
-  const Filter f = F.f[draft ? 1 : 0];
-  if (!gathers_row(f, P.nchunk)) {
-    if (tid == 0) F.gbound[g] = INFINITY;
-    return;
-  }
-  const int n = min(P.V, kSubsetChunks * kChunk);
-  const unsigned k = static_cast<unsigned>(f.top_k);
-  auto run = [&](const auto* row, bool vec, int levels) {
-    using T = typename std::remove_const<typename std::remove_pointer<decltype(row)>::type>::type;
-    unsigned prefix = 0u, carry = 0u;
-    for (int l = 0; l < levels; ++l) {
-      const int shift = 24 - 8 * l;
-      const unsigned hi_mask = shift + 8 >= 32 ? 0u : (0xffffffffu << (shift + 8));
-      for (int d = tid; d < 256; d += kSubThreads) hist[d] = 0u;
-      __syncthreads();
-      for (int v0 = tid * 8; v0 < n; v0 += kSubThreads * 8) {
-        float x[8];
-        load8<T>(row, v0, n, vec, x);  // entries past the subset read as -inf and are skipped
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const unsigned kx = key_of(x[e]);
-          if (v0 + e < n && (kx & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(kx >> shift) & 255u], 1u);
-        }
-      }
-      __syncthreads();
-      if (tid < 32) {
-        // the largest digit d with carry + (count of digits >= d) >= k: lane
-        // l holds digits 255 - 8l - i, i = 0..7
-        unsigned h[8], lsum = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          h[i] = hist[255 - 8 * lane - i];
-          lsum += h[i];
-        }
-        unsigned incl = lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        unsigned acc = carry + (incl - lsum);
-        int hit = -1;
-        unsigned above = 0u;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (hit < 0 && acc + h[i] >= k) {
-            hit = 255 - 8 * lane - i;
-            above = acc;
-          }
-          acc += h[i];
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
-        const int src = m ? __ffs(m) - 1 : 31;
-        const int d = __shfl_sync(0xffffffffu, hit < 0 ? 0 : hit, src);
-        const unsigned ab = __shfl_sync(0xffffffffu, above, src);
-        if (lane == 0) {
-          sdigit = static_cast<unsigned>(d);
-          sabove = ab;
-        }
-      }
-      __syncthreads();
-      prefix |= sdigit << shift;
-      carry = sabove;
-      __syncthreads();
-    }
-    if (tid == 0) {
-      const float xk = float_of_key(prefix);
-      F.gbound[g] = xk * P.c;  // monotone: every x >= xk has fl(x c) >= fl(xk c)
-    }
-  };
-  if (!draft)
-    run(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V, P.vec_t != 0,
-        sizeof(TT) == 2 ? 2 : 4);
-  else
-    run(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V, P.vec_d != 0,
-        sizeof(TD) == 2 ? 2 : 4);
-}
-
 // Rows whose top-k set the gathering pass collected in full (no chunk over
 // its cap, at most kRankCap logits in all): the whole selection by a small CTA
 // per row on the row's list in shared memory -- a bitonic sort by decreasing
@@ -478,23 +379,15 @@ __global__ void __launch_bounds__(kLSelThreads)
   // in chunk order)
   const float2* part = P.part + static_cast<int64_t>(g) * nch;
   const unsigned* cnt = F.gcount + static_cast<int64_t>(g) * nch;
-  const float* lst = F.glist + static_cast<int64_t>(g) * nch * kGatherCap;
   float M = -INFINITY;
   unsigned m0 = 0u, m1 = 0u;
   if (tid < nch) {
+    M = ldcg_f2(part + tid).x;
     m0 = __ldcg(cnt + tid);
-    M = F.have_part ? ldcg_f2(part + tid).x : -INFINITY;
   }
   if (tid + kLSelThreads < nch) {
+    M = fmaxf(M, ldcg_f2(part + tid + kLSelThreads).x);
     m1 = __ldcg(cnt + tid + kLSelThreads);
-    M = fmaxf(M, F.have_part ? ldcg_f2(part + tid + kLSelThreads).x : -INFINITY);
-  }
-  if (!F.have_part) {
-    // no statistics pass: the row's maximum is in its list (it reaches the bound)
-    for (unsigned i = 0; i < min(m0, static_cast<unsigned>(kGatherCap)); ++i)
-      M = fmaxf(M, __ldcg(lst + tid * kGatherCap + i) * P.c);
-    for (unsigned i = 0; i < min(m1, static_cast<unsigned>(kGatherCap)); ++i)
-      M = fmaxf(M, __ldcg(lst + (tid + kLSelThreads) * kGatherCap + i) * P.c);
   }
   const int over = (m0 > static_cast<unsigned>(kGatherCap)) || (m1 > static_cast<unsigned>(kGatherCap));
   if (over) m0 = m1 = 0u;
@@ -537,6 +430,7 @@ __global__ void __launch_bounds__(kLSelThreads)
   }
   const float c = P.c, Mc = M;
   // the list: every thread copies its chunks' entries to their offsets
+  const float* lst = F.glist + static_cast<int64_t>(g) * nch * kGatherCap;
   auto copy_chunk = [&](int ch, unsigned m, int o) {
 #pragma unroll 4
     for (unsigned i = 0; i < m; ++i) {
@@ -664,48 +558,8 @@ __global__ void __launch_bounds__(kSelThreads)
     return;
   }
   // the row's scaled maximum from the chunk statistics, and the first chunk
-  // holding it (one warp); without a statistics pass, from the row itself
-  if (!F.have_part) {
-    float M = -INFINITY;
-    int mi = 0x7fffffff;
-    for (int v = tid; v < P.V; v += kSelThreads) {
-      const float x = draft ? row_at<TD>(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V, v)
-                            : row_at<TT>(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * P.V, v);
-      if (x > M) {  // (a NaN never compares greater; the verification rejects such a row)
-        M = x;
-        mi = v;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oM = __shfl_xor_sync(0xffffffffu, M, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
-      if (oM > M || (oM == M && oi < mi)) {
-        M = oM;
-        mi = oi;
-      }
-    }
-    if (lane == 0) {
-      sh.wsum[warp] = static_cast<unsigned long long>(__float_as_uint(M));
-      sh.wfirst[warp] = mi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float tM = -INFINITY;
-      int ti = 0x7fffffff;
-      for (int w = 0; w < kSelWarps; ++w) {
-        const float wM = __uint_as_float(static_cast<unsigned>(sh.wsum[w]));
-        if (wM > tM || (wM == tM && sh.wfirst[w] < ti)) {
-          tM = wM;
-          ti = sh.wfirst[w];
-        }
-      }
-      const float Ms = tM == -INFINITY ? -INFINITY : tM * P.c;  // the chunk statistics' fl(m c)
-      sh.Mc = Ms;
-      sh.digit = ti == 0x7fffffff ? 0 : ti / kChunk;
-      sh.bad = !(Ms > -INFINITY) || !isfinite(Ms);
-    }
-  } else if (warp == 0) {
+  // holding it (one warp)
+  if (warp == 0) {
     const float2* part = P.part + static_cast<int64_t>(g) * P.nchunk;
     float M = -INFINITY;
     int mch = P.nchunk;
@@ -826,7 +680,7 @@ __global__ void __launch_bounds__(kSelThreads)
       if (tid == 0) sh.bad = 0;
       __syncthreads();
     }
-    if (use_k && f.top_k <= P.nchunk && !gathered && F.have_part) {
+    if (use_k && f.top_k <= P.nchunk && !gathered) {
       const float2* part = P.part + static_cast<int64_t>(g) * P.nchunk;
       for (int ch = tid; ch < P.nchunk; ch += kSelThreads) sh.lkey[ch] = key_of(ldcg_f2(part + ch).x);
       if (tid == 0) sh.ln = 0;
@@ -871,7 +725,7 @@ __global__ void __launch_bounds__(kSelThreads)
       }
       __syncthreads();
     }
-    if (use_k && f.top_k <= P.nchunk && (gathered || F.have_part)) {
+    if (use_k && f.top_k <= P.nchunk) {
       const int n = sh.ln;
       if (n <= kListCap) {
         listed = true;

@@ -245,29 +245,15 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
                         align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
                   : nullptr;
+  sv_status rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
+  if (rs != SV_OK) return rs;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
-  const bool gather_t = gathers_row(F.f[0], P.nchunk), gather_d = gathers_row(F.f[1], P.nchunk);
-  // A verifying call whose every row gathers its top-k set needs no statistics
-  // pass: each row's bound comes from a subset of the row, and the selection
-  // takes the row maximum from its list (rows whose list overflows read the
-  // row themselves).  Otherwise the statistics pass runs first.
-  const bool nostats = !copies && gather_t && gather_d;
-  F.have_part = nostats ? 0 : 1;
-  sv_status rs = SV_OK;
-  if (!nostats) {
-    rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
-    if (rs != SV_OK) return rs;
-  }
-  if (gather_t || gather_d) {
-    // top-k rows: each row's lower bound, then the gathering pass keeps every
-    // logit at or above it, chunk by chunk
-    if (nostats) {
-      if (launch_dependent(subset_bound_kernel<TT, TD>, nrows, kSubThreads, 0, st, P, F) != cudaSuccess)
-        return SV_ECUDA;
-    } else if (launch_dependent(bound_kernel<TT, TD>, (nrows + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps,
-                                0, st, P, F) != cudaSuccess) {
+  if (gathers_row(F.f[0], P.nchunk) || gathers_row(F.f[1], P.nchunk)) {
+    // top-k rows: each row's lower bound from its chunk maxima, then the
+    // gathering pass keeps every logit at or above it, chunk by chunk
+    if (launch_dependent(bound_kernel<TT, TD>, (nrows + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, st,
+                         P, F) != cudaSuccess)
       return SV_ECUDA;
-    }
     Params Pg = P;
     Pg.fthr = F.gbound;  // the gathering pass takes each row's bound in the threshold slot
     Pg.ffirst = F.first;
