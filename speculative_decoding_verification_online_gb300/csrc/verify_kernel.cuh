@@ -263,9 +263,19 @@ __device__ __forceinline__ void load8<float>(const float* row, int v0, int V, bo
 
 // probability of a token with raw logit x in a row with scaled max Mc and
 // 1/sum invS: exp2(fma(x, c, -Mc)) * invS.  Every decision uses this formula.
+// The product is rounded on its own (__fmul_rn is never fused into a later
+// add): p - q of two equal rows is then exactly 0, where a fused
+// fma(e, invS, -q) would leave q's rounding error as residual mass.
 __device__ __forceinline__ float prob_of(float x, float Mc, float c, float invS) {
-  return exp2f(fmaf(x, c, -Mc)) * invS;
+  return __fmul_rn(exp2f(fmaf(x, c, -Mc)), invS);
 }
+
+// A gated stop row's residual per chunk is the chunk's mass (from its
+// statistics, relative rounding error below 5e-6: a 64-term sum per lane,
+// five merge levels, three more roundings) minus its admitted tokens'
+// min(p, q).  A remainder within kResidualTol of the chunk's mass is that
+// rounding, not mass: the chunk counts as empty.
+constexpr float kResidualTol = 1e-5f;
 
 __device__ __forceinline__ bool gate_fast_path(float tau) {
   return tau * kGateSlack * static_cast<float>(kTopM + 1) > 1.0f;
@@ -1582,12 +1592,13 @@ __device__ void finish_back(const Params& P, int b, FinishShared& sh) {
 #pragma unroll 1
           for (int ch = lane; ch < nch; ch += 32) {
             const float2 ms = part_at(rt, ch);
-            float t = ms.x == -INFINITY ? 0.f : ms.y * exp2f(ms.x - ev.Mt) * invS;
+            const float m = ms.x == -INFINITY ? 0.f : __fmul_rn(ms.y * exp2f(ms.x - ev.Mt), invS);
+            float t = m;
             if (use_mode == 1) {
 #pragma unroll 1
               for (int a = 0; a < nadm; ++a)
                 if (sh.adm_i[jstar][a] / kChunk == ch) t -= fminf(sh.adm_p[jstar][a], sh.adm_q[jstar][a]);
-              t = fmaxf(t, 0.f);
+              t = t > kResidualTol * m ? t : 0.f;
             }
             sh.tile[ch] = t;
           }

@@ -20,6 +20,8 @@ SV_OK, SV_EINVAL, SV_ENOMEM, SV_ECUDA, SV_EUNSUPPORTED = 0, 1, 2, 3, 4
 SV_F32, SV_BF16 = 0, 1
 SV_PLAIN, SV_GATED_MU = 0, 1
 SV_FLAG_UNREACHED, SV_FLAG_ACCEPT, SV_FLAG_REJECT, SV_FLAG_NULL, SV_FLAG_INVALID = 0, 1, 2, 3, 4
+(SV_CNT_TESTED, SV_CNT_ACCEPTED, SV_CNT_NULL, SV_CNT_REJECTED, SV_CNT_BONUS, SV_CNT_BOUNDARY, SV_CNT_INVALID,
+ SV_CNT_DEGENERATE) = range(8)
 COUNTER_NAMES = ("tested", "accepted", "null", "rejected", "bonus", "boundary", "invalid",
                  "degenerate")
 SV_MAX_K = 32

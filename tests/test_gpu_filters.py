@@ -238,3 +238,140 @@ def test_gathered_lists_that_overflow_fall_back(sv, dtype):
     st = compare(w, out, ref, what=f"gathered overflow {dtype}", filters=filt)
     assert st["compared"] + st["boundary"] == B
     ver.close()
+
+
+# bf16 rows take the histogram selection (one read of each row, a counter per
+# bf16 value of magnitude in [2^-15, 2^9)); these rows exercise its side
+# paths: logits >= 2^9, logits below -2^9 that still weigh under top-p, tiny
+# values |x| < 2^-15 (listed with their masses, or too many to list), a
+# threshold among the tiny values, masked vocabulary (-inf), and ties at zero
+# with both signs.  V = 4100 rows are not 16-byte multiples (the scalar loop).
+EDGE_KINDS = {
+    "above_2^9": (1.0, 4096, ((100, 0.9, 0.0), (0, 0.8, 0.05))),
+    "below_-2^9_hot": (100.0, 4100, ((100, 0.9, 0.0), (0, 0.8, 0.0))),
+    "below_-2^9_topk": (100.0, 4096, ((100, 1.0, 0.0), (7, 1.0, 0.0))),
+    "tiny_overflow": (1.0, 4096, ((0, 0.9, 0.0), (50, 1.0, 0.0))),
+    "tiny_listed": (1.0, 4100, ((0, 0.9, 0.0), (100, 0.95, 0.02))),
+    "tiny_threshold": (1.0, 4096, ((0, 0.05, 0.0), (0, 0.05, 0.0))),
+    "masked_vocab": (1.0, 4096, ((600, 0.9, 0.0), (20, 1.0, 0.1))),
+    # values -2..2, about 820 of each: top_k = 2000 and top_p = 0.9 both end at zero
+    "signed_zero_ties": (1.0, 4100, ((2000, 1.0, 0.0), (0, 0.9, 0.0))),
+}
+
+
+def _edge_workload(kind, B, k, V, T, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    R = B * (2 * k + 1)
+    x = torch.randn(R, V, generator=g, device="cuda")
+    if kind == "above_2^9":
+        x[:, : V // 16] += 600.0
+    elif kind.startswith("below_-2^9"):
+        x = x * 150.0 - 300.0  # max near 300; about 8 % below -512, weighing 2^-12 of the max at T = 100
+    elif kind == "tiny_overflow":
+        x = x * 1e-5
+    elif kind == "tiny_listed":
+        x[:, :20] = (torch.rand(R, 20, generator=g, device="cuda") - 0.5) * 4e-5
+    elif kind == "tiny_threshold":
+        # mass from the top: two tokens at 2 (14.8), forty tiny ones (40.0),
+        # the rest at -1 (735.8): top-p 0.05 ends among the tiny values
+        x.fill_(-1.0)
+        x[:, 0:2] = 2.0
+        x[:, 2:42] = 1e-6 * torch.arange(1, 41, device="cuda", dtype=torch.float32)
+        x[:, 2042:] = float("-inf")
+        x = x[:, torch.randperm(V, generator=g, device="cuda")]
+    elif kind == "masked_vocab":
+        x[torch.rand(R, V, generator=g, device="cuda") < 0.9] = float("-inf")
+    elif kind == "signed_zero_ties":
+        x = torch.randint(-2, 3, (R, V), generator=g, device="cuda").float()
+        neg = torch.rand(R, V, generator=g, device="cuda") < 0.5
+        x = torch.where((x == 0) & neg, torch.full_like(x, -0.0), x)
+    Lt = x[: B * (k + 1)].reshape(B, k + 1, V).to(torch.bfloat16)
+    Ld = x[B * (k + 1):].reshape(B, k, V).to(torch.bfloat16)
+    u = torch.rand(B, k, V, generator=g, device="cuda").clamp_(1e-30, 1 - 1e-7)
+    D = torch.argmax(Ld.float() / T - torch.log(-torch.log(u)), dim=2).to(torch.int32)
+    gate = torch.as_tensor((np.arange(B) % 2).astype(np.uint8), device="cuda")
+    return workloads.Workload(name=kind, Lt=Lt, Ld=Ld, D=D, T=T, gate=gate,
+                              tau=torch.full((B,), 0.3, device="cuda"), philox_seed=seed + 1, B=B, k=k, V=V,
+                              dtype="bf16")
+
+
+@pytest.mark.parametrize("kind", sorted(EDGE_KINDS))
+def test_histogram_selection_edge_rows(sv, kind):
+    T, V, filt = EDGE_KINDS[kind]
+    B, k = 12, 2
+    w = _edge_workload(kind, B, k, V, T, seed=700 + sorted(EDGE_KINDS).index(kind))
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w, filters=filt)
+    st = compare(w, out, ref, what=f"histogram edge rows {kind}", filters=filt)
+    # the filtered rows' statistics pin every row's kept set
+    ok = ref["margin"] >= 1e-6
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[ok][..., 0], ref["row_stats"][ok][..., 0], rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
+    assert ok.sum() >= B // 2
+    assert st["compared"] >= B // 2
+    ver.close()
+
+
+def _same_rows_workload(B, k, V, dtype, x, gate, tau, seed):
+    """Draft rows equal to the target rows (p = q at every position) and each
+    drafted token the smallest draft logit, outside any filtered set: every
+    position is rejected (p(D) = 0) or NULL (q(D) = 0 < tau)."""
+    dt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    Lt = x.to(dt)
+    Ld = x[:, :k].contiguous().to(dt)
+    D = torch.argmin(Ld.float(), dim=2).to(torch.int32)
+    return workloads.Workload(name="same_rows", Lt=Lt, Ld=Ld, D=D, T=1.0,
+                              gate=torch.as_tensor(np.broadcast_to(np.asarray(gate, dtype=np.uint8), (B,)).copy(),
+                                                   device="cuda"),
+                              tau=torch.full((B,), tau, device="cuda"), philox_seed=seed, B=B, k=k, V=V, dtype=dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("filt", [((5, 1.0, 0.0), (5, 1.0, 0.0)), ((0, 0.5, 0.0), (0, 0.5, 0.0))])
+def test_degenerate_residuals_fall_back_to_p(sv, dtype, filt):
+    # p = q on the kept sets and D outside them: a plain stop row's residual
+    # (p - q)+ is exactly empty, so the token is drawn from p (the reading of
+    # the oracle); the GPU must find it empty too, not sample rounding noise
+    B, k, V = 16, 2, 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x = torch.randn(B, k + 1, V, generator=g, device="cuda") * 2
+    w = _same_rows_workload(B, k, V, dtype, x, np.arange(B) % 2, 0.3, seed=11)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
+    out = _run(sv, ver, w, counters=cnt)
+    ref = oracle_for(w, filters=filt)
+    compare(w, out, ref, what=f"degenerate {dtype} {filt}", filters=filt)
+    assert int(cnt[sv.SV_CNT_DEGENERATE]) == int(ref["degenerate"].sum()) >= B // 2
+    ver.close()
+
+
+def test_degenerate_gated_residual_on_the_candidate_path(sv):
+    # two tied top tokens kept by top_k = 2 on both sides, q = 0.5 >= tau:
+    # both admitted, so mu = q = p and the residual of a NULL stop row is
+    # empty; the gated fast path computes it from chunk statistics minus the
+    # admitted overlap, which leaves only rounding -- still empty, drawn from p
+    B, k, V = 16, 2, 6000
+    g = torch.Generator(device="cuda")
+    g.manual_seed(6)
+    x = torch.randn(B, k + 1, V, generator=g, device="cuda") - 10.0
+    top = torch.stack([torch.randperm(V, generator=g, device="cuda")[:2] for _ in range(B * (k + 1))])
+    x.view(-1, V).scatter_(1, top, 5.0)
+    w = _same_rows_workload(B, k, V, "bf16", x, 1, 0.3, seed=13)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    filt = ((2, 1.0, 0.0), (2, 1.0, 0.0))
+    ver.set_filters(*filt)
+    cnt = torch.zeros(8, dtype=torch.int64, device="cuda")
+    out = ver.run(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=0.3, seed=w.philox_seed,
+                  counters=cnt)
+    torch.cuda.synchronize()
+    ref = oracle_for(w, filters=filt)
+    compare(w, out, ref, what="degenerate gated", filters=filt)
+    assert int(cnt[sv.SV_CNT_DEGENERATE]) == int(ref["degenerate"].sum()) == B
+    assert (out["tokens"][:, 0] >= 0).all()
+    ver.close()
