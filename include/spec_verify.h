@@ -252,16 +252,18 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
  *     probability, keep the shortest prefix whose mass reaches top_p, plus the
  *     tokens tied with its last one; 1 = off.
  *   min_p in [0, 1]: keep p >= min_p * max p; 0 = off.
- * With any filter on (and temperature > 0) a verifying call first runs a
- * statistics pass over the logits and finds each row's kept set (a logit
- * threshold, or the kept index of a top_k = 1 row) into a buffer of the
- * handle (max_B * (2k+1) * (16 + ceil(V / 2048) * 132) bytes, allocated on
- * the first filtered call -- make that call outside any stream capture;
- * SV_ENOMEM if it fails); for a top-k filter (2 <= top_k <= ceil(V / 2048)
- * <= 512) a gathering pass first collects each row's candidates chunk by
- * chunk.  Its verifying kernels then read every logit outside a row's kept
- * set as -inf (a NaN is kept, so the row stays invalid): 4 to 7 launches
- * instead of 2 and three or four reads of the logits.  row_stats then describe the filtered
+ * With any filter on (and temperature > 0) a verifying call first finds each
+ * row's kept set (a logit threshold, or the kept index of a top_k = 1 row)
+ * into a buffer of the handle (max_B * (2k+1) * (16 + ceil(V / 2048) * 132)
+ * bytes, allocated on the first filtered call -- make that call outside any
+ * stream capture; SV_ENOMEM if it fails).  When every filtered side holds
+ * bf16 logits and none has top_k = 1, one read of each row decides it (a
+ * histogram over the bf16 values); otherwise a statistics pass over the
+ * logits runs first, and for a top-k filter (2 <= top_k <= ceil(V / 2048)
+ * <= 512) a gathering pass collects each row's candidates chunk by chunk.
+ * Its verifying kernels then read every logit outside a row's kept set as
+ * -inf (a NaN is kept, so the row stays invalid): 3 to 7 launches instead of
+ * 2 and two to four reads of the logits.  row_stats then describe the filtered
  * rows.  spec_verify_diagnostics applies the same filters through masked
  * copies of the logits, in a second buffer of the handle (max_B * (2k+1) * V
  * * 4 bytes, allocated on the first filtered diagnostics call).  Decisions of top-p and min-p sit on fp32 arithmetic (the
@@ -273,7 +275,8 @@ sv_status spec_verify_set_filters(spec_verify_t h, int top_k_target, float top_p
                                   float min_p_draft);
 
 /* Kernel launches of a verifying call with sampler filters on (temperature > 0),
- * at most: 7 with a gathered top-k filter, 4 otherwise. */
+ * at most: 7 with a gathered top-k filter, 4 otherwise; 3 when every filtered
+ * side holds bf16 logits and none has top_k = 1. */
 int spec_verify_launches_per_filtered_run(void);
 
 /* Release the handle and its device memory (NULL is a no-op).  Synchronises

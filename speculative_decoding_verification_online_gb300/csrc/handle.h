@@ -12,6 +12,7 @@
 #include "verify_kernel.cuh"
 #include "diag_kernel.cuh"
 #include "filter_kernel.cuh"
+#include "hist_kernel.cuh"
 
 struct spec_verify_s {
   int device = 0;

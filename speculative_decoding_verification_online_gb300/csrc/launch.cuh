@@ -60,6 +60,9 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(select_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(SelShared)));
+  // several histogram CTAs per SM need the largest shared-memory split
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(hist_kernel<TT, TD>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm,
                                                        stream_kernel<TT, TD, kModeSample, false>,
@@ -196,12 +199,48 @@ sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
-// The filter prefix of a call: the statistics pass of the raw rows, then each
-// row's kept set (select_kernel: threshold and, for top_k = 1, the kept
-// index).  A verifying call then applies them on the fly (P.fthr, P.ffirst:
-// its stream and finishing kernels mask every logit they load).  With
-// `copies` (the diagnostics, whose kernels read rows as they are) mask_kernel
-// also writes masked copies of the logits and P reads those instead.
+// The selection after the statistics pass: top-k rows' bounds, the gathering
+// pass and the short lists' selection when a side gathers, then select_kernel
+// (every row not selected before).  gc, gl, done: the gathering buffers.
+template <typename TT, typename TD>
+sv_status launch_selection(spec_verify_t h, const Params& P, FilterParams& F, int blocks_per_sm, char* gc,
+                           char* gl, char* done, cudaStream_t st) {
+  const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
+  if (gathers_row(F.f[0], P.nchunk) || gathers_row(F.f[1], P.nchunk)) {
+    // top-k rows: each row's lower bound from its chunk maxima, then the
+    // gathering pass keeps every logit at or above it, chunk by chunk
+    if (launch_dependent(bound_kernel<TT, TD>, (nrows + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, st,
+                         P, F) != cudaSuccess)
+      return SV_ECUDA;
+    Params Pg = P;
+    Pg.fthr = F.gbound;  // the gathering pass takes each row's bound in the threshold slot
+    Pg.ffirst = F.first;
+    Pg.gcount = reinterpret_cast<unsigned*>(gc);
+    Pg.glist = reinterpret_cast<float*>(gl);
+    const sv_status rs = launch_stream<TT, TD, kModeGather, true>(h, Pg, blocks_per_sm, st);
+    if (rs != SV_OK) return rs;
+    F.gcount = Pg.gcount;
+    F.glist = Pg.glist;
+    // gathered rows whose lists are short: selected by a small CTA each
+    F.done = reinterpret_cast<int*>(done);
+    if (launch_dependent(list_select_kernel<TT, TD>, nrows, kLSelThreads, 0, st, P, F) != cudaSuccess)
+      return SV_ECUDA;
+  }
+  if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
+      cudaSuccess)
+    return SV_ECUDA;
+  return SV_OK;
+}
+
+// The filter prefix of a call: each row's kept set (a threshold and, for
+// top_k = 1, the kept index).  When every filtered side holds bf16 logits and
+// none is top_k = 1, hist_kernel finds it from one read of each row;
+// otherwise the statistics pass of the raw rows, then (top-k rows) the
+// gathering passes, then select_kernel.  A verifying call then applies them
+// on the fly (P.fthr, P.ffirst: its stream and finishing kernels mask every
+// logit they load).  With `copies` (the diagnostics, whose kernels read rows
+// as they are) mask_kernel also writes masked copies of the logits and P
+// reads those instead.
 template <typename TT, typename TD>
 sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool copies, cudaStream_t st) {
   const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
@@ -245,32 +284,15 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
                         align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
                   : nullptr;
-  sv_status rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
-  if (rs != SV_OK) return rs;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
-  if (gathers_row(F.f[0], P.nchunk) || gathers_row(F.f[1], P.nchunk)) {
-    // top-k rows: each row's lower bound from its chunk maxima, then the
-    // gathering pass keeps every logit at or above it, chunk by chunk
-    if (launch_dependent(bound_kernel<TT, TD>, (nrows + kBoundWarps - 1) / kBoundWarps, 32 * kBoundWarps, 0, st,
-                         P, F) != cudaSuccess)
-      return SV_ECUDA;
-    Params Pg = P;
-    Pg.fthr = F.gbound;  // the gathering pass takes each row's bound in the threshold slot
-    Pg.ffirst = F.first;
-    Pg.gcount = reinterpret_cast<unsigned*>(base + o_gc);
-    Pg.glist = reinterpret_cast<float*>(base + o_gl);
-    rs = launch_stream<TT, TD, kModeGather, true>(h, Pg, blocks_per_sm, st);
+  if (hist_selects(F.f[0], sizeof(TT) == 2) && hist_selects(F.f[1], sizeof(TD) == 2)) {
+    if (launch_dependent(hist_kernel<TT, TD>, nrows, kHThreads, 0, st, P, F) != cudaSuccess) return SV_ECUDA;
+  } else {
+    sv_status rs = launch_stream<TT, TD, kModeStats, false>(h, P, blocks_per_sm, st);
     if (rs != SV_OK) return rs;
-    F.gcount = Pg.gcount;
-    F.glist = Pg.glist;
-    // gathered rows whose lists are short: selected by a small CTA each
-    F.done = reinterpret_cast<int*>(base + o_done);
-    if (launch_dependent(list_select_kernel<TT, TD>, nrows, kLSelThreads, 0, st, P, F) != cudaSuccess)
-      return SV_ECUDA;
+    rs = launch_selection<TT, TD>(h, P, F, blocks_per_sm, base + o_gc, base + o_gl, base + o_done, st);
+    if (rs != SV_OK) return rs;
   }
-  if (launch_dependent(select_kernel<TT, TD>, nrows, kSelThreads, sizeof(SelShared), st, P, F) !=
-      cudaSuccess)
-    return SV_ECUDA;
   if (copies) {
     // one CTA per row at a time, at most eight per SM
     long long grid = static_cast<long long>(P.B) * P.rows;
