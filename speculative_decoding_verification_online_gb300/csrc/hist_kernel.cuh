@@ -38,9 +38,14 @@ constexpr int kHBins = 2 * kHSide + 3;
 // The scans take them by rank, in decreasing order of value: positive values,
 // the tiny positive ones, zero, the tiny negative ones, negative values.
 constexpr int kRPosTiny = kHSide, kRZero = kHSide + 1, kRNegTiny = kHSide + 2, kRNeg0 = kHSide + 3;
-constexpr int kHNBlk = (kHBins + 31) / 32;                      // blocks of 32 ranks
-constexpr int kHBlkPerWarp = (kHNBlk + kHWarps - 1) / kHWarps;  // a warp's share of the blocks
-static_assert(kHBlkPerWarp <= 32, "a lane per block");
+// The scans sum blocks of 128 counters, contiguous in memory and in rank:
+// rank blocks [0, kHPB) are the positive counters from the top (each block
+// in decreasing order of its counters), block kHPB the three side counters,
+// blocks (kHPB, kHNBlk) the negative counters (increasing order).
+constexpr int kHBlk = 128;
+constexpr int kHPB = kHSide / kHBlk;       // 24 blocks per sign
+constexpr int kHNBlk = 2 * kHPB + 1;       // 49 rank blocks
+static_assert(kHSide % kHBlk == 0 && kHNBlk <= 64, "two blocks per lane in a crossing");
 constexpr int kTinyCap = 64;              // tiny values listed per sign
 constexpr unsigned kKeyNegInf = 0x007fu;  // 16-bit key of -inf
 constexpr unsigned kKeyPosInf = 0xff80u;  // and of +inf
@@ -52,7 +57,7 @@ __host__ __device__ inline bool hist_selects(const Filter& f, bool bf16) {
   return !on || (bf16 && f.top_k != 1);
 }
 
-struct HistShared {
+struct alignas(16) HistShared {  // (16-byte loads of the counters)
   union {
     unsigned cnt[kHBins];
     struct {  // the radix fallback's level histograms, one per warp
@@ -68,7 +73,6 @@ struct HistShared {
   unsigned bcnt[kHNBlk];    // per block of 32 ranks: counts and masses
   unsigned long long bmass[kHNBlk];
   unsigned long long wsum[kHWarps];  // per warp: its blocks' mass
-  unsigned long long wtc[kHWarps], wtm[kHWarps];
   unsigned wmax[kHWarps];
   int hit;
   unsigned long long hit_incl;
@@ -209,13 +213,6 @@ __device__ __forceinline__ void hist_sweep(const uint4* r4, int nv, unsigned& mx
 }
 
 // ---- the crossings over the ranks (the largest values first)
-//
-// The warps sum blocks of 32 consecutive ranks, a lane per rank and a mass
-// only where the rank holds logits (a row's occupied ranks are often a few
-// hundred consecutive ones, which this spreads over all lanes).  A crossing
-// then takes the warp totals of those block sums, the warp whose share holds
-// the target, that warp's blocks, and the block's ranks: a few short warp
-// scans, no serial walk.
 
 // rank r's count, and the fixed-point mass of all its logits (a tiny class:
 // summed over its list, 0 when the list overflowed -- the caller then falls
@@ -259,20 +256,64 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return v;
 }
 
-// the block sums of counts and (masses) of masses; returns the total mass
+// lane l's four ranks of rank block q, in rank order: their first rank, and
+// their counts (side block: lanes 0..2 one rank each)
+__device__ __forceinline__ int lane_ranks(int q, int lane, const HistShared& sh, unsigned (&n)[4]) {
+  if (q < kHPB) {  // positive counters, decreasing
+    const int top = 2 * kHSide - 1 - q * kHBlk - 4 * lane;  // counter of the lane's first rank
+    const uint4 u = *reinterpret_cast<const uint4*>(&sh.cnt[top - 3]);
+    n[0] = u.w;
+    n[1] = u.z;
+    n[2] = u.y;
+    n[3] = u.x;
+    return q * kHBlk + 4 * lane;
+  }
+  if (q > kHPB) {  // negative counters, increasing
+    const int lo = (q - kHPB - 1) * kHBlk + 4 * lane;
+    const uint4 u = *reinterpret_cast<const uint4*>(&sh.cnt[lo]);
+    n[0] = u.x;
+    n[1] = u.y;
+    n[2] = u.z;
+    n[3] = u.w;
+    return kRNeg0 + lo;
+  }
+  n[0] = lane < 3 ? rank_count(kHSide + lane, sh) : 0u;  // the side counters
+  n[1] = n[2] = n[3] = 0u;
+  return kHSide + min(lane, 2);
+}
+
+// the four ranks' masses from their counts (0 where the count is)
+__device__ __forceinline__ void lane_masses(int q, int r0, const unsigned (&n)[4], float c, float Mc,
+                                            const HistShared& sh, unsigned long long (&m)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = 0ull;
+  if (q == kHPB) {
+    m[0] = rank_mass(r0, n[0], c, Mc, sh);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (n[i]) m[i] = static_cast<unsigned long long>(n[i]) * mass_of(__uint_as_float(rank_bits(r0 + i) << 16), c, Mc);
+}
+
+// the rank blocks' sums of counts and (masses) of masses; returns the total mass
 static __device__ unsigned long long hist_block_sums(bool masses, float c, float Mc, HistShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long wtot = 0ull;
 #pragma unroll 1
-  for (int blk = warp; blk < kHNBlk; blk += kHWarps) {
-    const int r = blk * 32 + lane;
-    const unsigned n = r < kHBins ? rank_count(r, sh) : 0u;
-    const unsigned cs = __reduce_add_sync(0xffffffffu, n);
+  for (int q = warp; q < kHNBlk; q += kHWarps) {
+    unsigned n[4];
+    const int r0 = lane_ranks(q, lane, sh, n);
+    const unsigned cs = __reduce_add_sync(0xffffffffu, (n[0] + n[1]) + (n[2] + n[3]));
     unsigned long long ms = 0ull;
-    if (masses && cs) ms = warp_sum_exact(rank_mass(r, n, c, Mc, sh));
+    if (masses && cs) {
+      unsigned long long m[4];
+      lane_masses(q, r0, n, c, Mc, sh, m);
+      ms = warp_sum_exact((m[0] + m[1]) + (m[2] + m[3]));
+    }
     if (lane == 0) {
-      sh.bcnt[blk] = cs;
-      sh.bmass[blk] = ms;
+      sh.bcnt[q] = cs;
+      sh.bmass[q] = ms;
     }
     wtot += ms;
   }
@@ -286,56 +327,64 @@ static __device__ unsigned long long hist_block_sums(bool masses, float c, float
 
 // the first rank at which the running counts (by_mass false) or masses reach
 // target, and the running mass through it (masses: the block sums hold them);
-// rank -1 when the target is not reached
+// rank -1 when the target is not reached.  Warp 0: the rank blocks two per
+// lane, then the block's lanes, then the lane's four ranks.
 static __device__ void hist_cross(bool by_mass, bool masses, unsigned long long target, float c, float Mc,
                                   HistShared& sh, int* rank, unsigned long long* mass_incl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = warp * kHBlkPerWarp + lane;
-  const bool in = lane < kHBlkPerWarp && b < kHNBlk;
-  const unsigned long long vc = in ? sh.bcnt[b] : 0ull;
-  const unsigned long long vm = in && masses ? sh.bmass[b] : 0ull;
-  const unsigned long long wc = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(vc));
-  const unsigned long long wm = masses ? warp_sum_exact(vm) : 0ull;
-  if (lane == 0) {
-    sh.wtc[warp] = wc;
-    sh.wtm[warp] = wm;
-  }
-  if (threadIdx.x == 0) sh.hit = -1;
-  __syncthreads();
-  // the warp whose share of the blocks holds the crossing (every thread
-  // finds the same one)
-  unsigned long long cc = 0ull, cm = 0ull;
-  int wstar = -1;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int q0 = 2 * lane, q1 = q0 + 1;
+    const unsigned long long c0 = q0 < kHNBlk ? sh.bcnt[q0] : 0ull, c1 = q1 < kHNBlk ? sh.bcnt[q1] : 0ull;
+    const unsigned long long m0 = masses && q0 < kHNBlk ? sh.bmass[q0] : 0ull;
+    const unsigned long long m1 = masses && q1 < kHNBlk ? sh.bmass[q1] : 0ull;
+    const unsigned long long ic = warp_incl_scan_u64(c0 + c1, lane);
+    const unsigned long long im = masses ? warp_incl_scan_u64(m0 + m1, lane) : 0ull;
+    const unsigned hit = __ballot_sync(0xffffffffu, (by_mass ? im : ic) >= target);
+    int res = -1;
+    unsigned long long resm = 0ull;
+    if (hit) {
+      const int f = __ffs(hit) - 1;
+      // the sums before lane f's blocks, and which of its two blocks
+      unsigned long long bc = __shfl_sync(0xffffffffu, ic - (c0 + c1), f);
+      unsigned long long bm = __shfl_sync(0xffffffffu, im - (m0 + m1), f);
+      const unsigned long long fc0 = __shfl_sync(0xffffffffu, c0, f), fm0 = __shfl_sync(0xffffffffu, m0, f);
+      int q = 2 * f;
+      if ((by_mass ? bm + fm0 : bc + fc0) < target) {
+        bc += fc0;
+        bm += fm0;
+        ++q;
+      }
+      // the block's lanes
+      unsigned n[4];
+      const int r0 = lane_ranks(q, lane, sh, n);
+      unsigned long long m[4] = {0ull, 0ull, 0ull, 0ull};
+      if (masses) lane_masses(q, r0, n, c, Mc, sh, m);
+      const unsigned long long lc = (n[0] + n[1]) + (n[2] + n[3]);
+      const unsigned long long lm = (m[0] + m[1]) + (m[2] + m[3]);
+      const unsigned long long jc = warp_incl_scan_u64(lc, lane) + bc;
+      const unsigned long long jm = masses ? warp_incl_scan_u64(lm, lane) + bm : 0ull;
+      const unsigned hit2 = __ballot_sync(0xffffffffu, (by_mass ? jm : jc) >= target);
+      if (hit2) {
+        const int f2 = __ffs(hit2) - 1;
+        // the lane's ranks in order
+        int rr = -1;
+        unsigned long long ac = jc - lc, am = jm - lm, at = 0ull;
 #pragma unroll
-  for (int w = 0; w < kHWarps; ++w) {
-    if (wstar >= 0) break;
-    const unsigned long long nc = cc + sh.wtc[w], nm = cm + sh.wtm[w];
-    if ((by_mass ? nm : nc) >= target) {
-      wstar = w;
-    } else {
-      cc = nc;
-      cm = nm;
+        for (int i = 0; i < 4; ++i) {
+          ac += n[i];
+          am += m[i];
+          if (rr < 0 && (by_mass ? am : ac) >= target) {
+            rr = r0 + i;
+            at = am;
+          }
+        }
+        res = __shfl_sync(0xffffffffu, rr, f2);
+        resm = __shfl_sync(0xffffffffu, at, f2);
+      }
     }
-  }
-  if (warp == wstar) {
-    // its blocks (lanes past its share hold 0, so the first hit is a block)
-    const unsigned long long ic = warp_incl_scan_u64(vc, lane) + cc;
-    const unsigned long long im = masses ? warp_incl_scan_u64(vm, lane) + cm : 0ull;
-    const int f = __ffs(__ballot_sync(0xffffffffu, (by_mass ? im : ic) >= target)) - 1;
-    const int blk = warp * kHBlkPerWarp + f;
-    const unsigned long long bc = __shfl_sync(0xffffffffu, ic - vc, f);
-    const unsigned long long bm = __shfl_sync(0xffffffffu, im - vm, f);
-    // the block's ranks
-    const int r = blk * 32 + lane;
-    const unsigned n = r < kHBins ? rank_count(r, sh) : 0u;
-    const unsigned long long rm = masses ? rank_mass(r, n, c, Mc, sh) : 0ull;
-    const unsigned long long rc = warp_incl_scan_u64(n, lane) + bc;
-    const unsigned long long rmi = masses ? warp_incl_scan_u64(rm, lane) + bm : 0ull;
-    const int f2 = __ffs(__ballot_sync(0xffffffffu, (by_mass ? rmi : rc) >= target)) - 1;
-    const unsigned long long at = __shfl_sync(0xffffffffu, rmi, f2);
     if (lane == 0) {
-      sh.hit = blk * 32 + f2;
-      sh.hit_incl = at;
+      sh.hit = res;
+      sh.hit_incl = resm;
     }
   }
   __syncthreads();
