@@ -111,20 +111,20 @@ def filters_of(args):
     return None if ft == fd == (0, 1.0, 0.0) else (ft, fd)
 
 
-def filter_launches(filt, V, diagnostics, dtypes):
-    """Launches the sampler filters add in front of a call.  When every
-    filtered side holds bf16 logits and none is top_k = 1: the histogram
-    selection (1).  Otherwise the statistics pass and the selection (2), plus
-    the bound, gathering and list-selection passes when a side has
-    2 <= top_k <= the number of 2048-entry chunks (at most 512 chunks).  The
-    diagnostics add the masked copies (1)."""
+def filter_launches(filt, V, dtypes):
+    """Launches the sampler filters add in front of a verifying or diagnostics
+    call.  When every filtered side holds bf16 logits and none is top_k = 1:
+    the histogram selection (1).  Otherwise the statistics pass and the
+    selection (2), plus the bound, gathering and list-selection passes when a
+    side has 2 <= top_k <= the number of 2048-entry chunks (at most 512
+    chunks)."""
     def on(f):
         return f[0] != 0 or f[1] < 1.0 or f[2] > 0.0
     if all(not on(f) or (dt == "bf16" and f[0] != 1) for f, dt in zip(filt, dtypes)):
-        return 1 + (1 if diagnostics else 0)
+        return 1
     nchunk = (V + 2047) // 2048
     gathers = any(2 <= f[0] <= nchunk and nchunk <= 512 for f in filt)
-    return 2 + (3 if gathers else 0) + (1 if diagnostics else 0)
+    return 2 + (3 if gathers else 0)
 
 
 def gate_args(args, w, cfg, sv):
@@ -613,7 +613,7 @@ def main():
             # sampler filters add the launches of filter_launches in front
             "gpu_launches": args.steps * (((2 if w0.T == 0 else 4) if args.diagnostics
                                            else sv.spec_verify_launches_per_run())
-                                          + (filter_launches(filt, w0.V, args.diagnostics, (w0.dtype, w0.dtype))
+                                          + (filter_launches(filt, w0.V, (w0.dtype, w0.dtype))
                                              if filt is not None and w0.T > 0 else 0)),
             "clocks": clocks,
         }

@@ -264,11 +264,11 @@ sv_status spec_verify_set_gate_policy(spec_verify_t h, const float* schedule, in
  * Its verifying kernels then read every logit outside a row's kept set as
  * -inf (a NaN is kept, so the row stays invalid): 3 to 7 launches instead of
  * 2 and two to four reads of the logits.  row_stats then describe the filtered
- * rows.  spec_verify_diagnostics applies the same filters through masked
- * copies of the logits, in a second buffer of the handle (max_B * (2k+1) * V
- * * 4 bytes, allocated on the first filtered diagnostics call).  Decisions of top-p and min-p sit on fp32 arithmetic (the
- * top-p masses are summed as integers, so they do not depend on the order of
- * the additions).  Default: all off.  Returns SV_EINVAL (filters unchanged) for
+ * rows.  spec_verify_diagnostics applies the same filters the same way (its
+ * kernels read every logit outside a row's kept set as -inf; the launches of
+ * the kept sets come in front of its own).  Decisions of top-p and min-p sit
+ * on fp32 arithmetic (the top-p masses are summed as integers, so they do not
+ * depend on the order of the additions).  Default: all off.  Returns SV_EINVAL (filters unchanged) for
  * a NULL handle or a value outside its range. */
 sv_status spec_verify_set_filters(spec_verify_t h, int top_k_target, float top_p_target,
                                   float min_p_target, int top_k_draft, float top_p_draft,

@@ -8,8 +8,10 @@
 // behavior"); the cumulative floor uses the drafted prefix D_0..D_{j-1}.
 //
 // min(p, mu) needs both rows' normalisers before any term can be formed, so
-// the diagnostics read the rows twice.  Launches, each a programmatic
-// dependent of the one before:
+// the diagnostics read the rows twice.  With sampler filters every row's kept
+// set comes first (as for a verifying call) and launches 1, 3 and 4 read every
+// logit outside it as -inf.  Launches, each a programmatic dependent of the
+// one before:
 //   1. stream_kernel<kModeStats> (or <kModeGreedy> at temperature 0): chunk
 //      statistics and drafted-token logits of every row;
 //   2. diag_norm_kernel: one warp per (sequence, position) merges the two rows'
@@ -186,6 +188,8 @@ struct PairStages {
 struct PairQueue {
   int4 item[kItemRing];      // (b, j, ch, 1); w = 0: no more work
   DiagNorm nrm[kItemRing];   // the item's DiagNorm, copied asynchronously
+  float fthr[kItemRing][2];  // (filtered calls) the target and draft rows'
+  int ffirst[kItemRing][2];  // thresholds and kept indices, likewise
 };
 
 // partial record of chunk pair (b, j, ch): (sum min(p, mu), sum p q, largest
@@ -206,7 +210,8 @@ __device__ __forceinline__ void stage8(const unsigned char* stage, int o, float 
   }
 }
 
-template <typename TT, typename TD>
+// kFilt: the call's sampler filters applied to both rows as they are read
+template <typename TT, typename TD, bool kFilt>
 __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
     pair_kernel(const __grid_constant__ Params P, const DiagNorm* __restrict__ norm, unsigned total) {
   constexpr int S = PairStages<TT, TD>::kDepth;
@@ -242,10 +247,18 @@ __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
     }
     const unsigned rg = fastdiv(x, P.div_nchunk);  // b k + j
     const int ch = static_cast<int>(x - rg * static_cast<unsigned>(nch));
-    Q.item[slot] = make_int4(static_cast<int>(rg / static_cast<unsigned>(k)), static_cast<int>(rg % k), ch, 1);
+    const int b = static_cast<int>(rg / static_cast<unsigned>(k)), j = static_cast<int>(rg % k);
+    Q.item[slot] = make_int4(b, j, ch, 1);
     cp_async16(&Q.nrm[slot], norm + rg);
     cp_async16(reinterpret_cast<unsigned char*>(&Q.nrm[slot]) + 16,
                reinterpret_cast<const unsigned char*>(norm + rg) + 16);
+    if constexpr (kFilt) {
+      const int64_t gt = static_cast<int64_t>(b) * P.rows + j, gd = gt + k + 1;
+      cp_async4(&Q.fthr[slot][0], P.fthr + gt);
+      cp_async4(&Q.fthr[slot][1], P.fthr + gd);
+      cp_async4(&Q.ffirst[slot][0], P.ffirst + gt);
+      cp_async4(&Q.ffirst[slot][1], P.ffirst + gd);
+    }
   };
   if (lane == 0) put(0, next());
   __syncwarp();
@@ -274,6 +287,14 @@ __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
     cp_async_wait<S - 1>();
     __syncwarp();
     const DiagNorm nm = Q.nrm[n % kItemRing];  // landed with the item's commit group
+    float thr_t = 0.f, thr_d = 0.f;            // likewise
+    int first_t = -1, first_d = -1;
+    if constexpr (kFilt) {
+      thr_t = Q.fthr[n % kItemRing][0];
+      thr_d = Q.fthr[n % kItemRing][1];
+      first_t = Q.ffirst[n % kItemRing][0];
+      first_d = Q.ffirst[n % kItemRing][1];
+    }
     const unsigned char* st = ring + (n % S) * kStage;
     if (!nm.bad) {
       float amin = 0.f, apq = 0.f, best = -INFINITY;
@@ -287,6 +308,10 @@ __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
         float xt[8], xd[8], mn[8], pq[8];
         stage8<TT>(st, o, xt);
         stage8<TD>(st + kBT, o, xd);
+        if constexpr (kFilt) {
+          filt8(xt, c0 + o, thr_t, first_t);
+          filt8(xd, c0 + o, thr_d, first_d);
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float p = prob_of(xt[e], nm.Mt, c, nm.invSt);
@@ -370,7 +395,15 @@ __global__ void __launch_bounds__(kDiagThreads)
   if (lane == 0) {
     const int b = g / k, j = g % k;
     const TD* drow = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + j) * V;
-    const float aq = bidx < V ? prob_of(logit_at<TD>(drow, bidx), nm.Md, P.c, nm.invSd) : NAN;
+    float aq = NAN;
+    if (bidx < V) {
+      float xq = logit_at<TD>(drow, bidx);
+      if (P.fthr) {  // the draft row as its sampler filter leaves it
+        const int64_t gd = static_cast<int64_t>(b) * P.rows + k + 1 + j;
+        xq = filt1(xq, bidx, P.fthr[gd], P.ffirst[gd]);
+      }
+      aq = prob_of(xq, nm.Md, P.c, nm.invSd);
+    }
     write_diag(g, amin, apq, aq, min_sum, pq_sum, argmax_q);
   }
 }

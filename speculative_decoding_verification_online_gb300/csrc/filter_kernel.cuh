@@ -1,10 +1,10 @@
 // filter_kernel.cuh -- the sampler's filter chain before the softmax (mlxcel
 // PR #992, "What changed": temperature, top-k, top-p, min-p, then the softmax
-// of the survivors; top_k == 1 is greedy).  Each row's kept set is found here;
-// the verifying kernels then read every logit outside it as -inf, applying
-// the row's threshold as they load (the temperature softmax of a row masked
-// that way is exactly the filtered distribution).  The diagnostics read rows
-// as they are, so for them mask_kernel writes masked copies instead.
+// of the survivors; top_k == 1 is greedy).  Each row's kept set is found here
+// (and, for bf16 rows, in hist_kernel.cuh); the verifying and diagnostics
+// kernels then read every logit outside it as -inf, applying the row's
+// threshold as they load (the temperature softmax of a row masked that way is
+// exactly the filtered distribution).
 //
 // Each filter keeps the tokens at or above a logit threshold (ties kept), so a
 // row's kept set is {x : key(x) >= K} for one key K in an order-preserving
@@ -33,8 +33,6 @@ struct FilterParams {
   unsigned* key;        // [B * rows] threshold key of each row (kept: key >= K)
   int* first;           // [B * rows] top_k == 1: the index kept, else -1
   float* thr;           // [B * rows] the same threshold as a logit: kept x >= thr (-inf: all)
-  void* Lt_m;           // masked copies, same layouts and types as the inputs (null: none)
-  void* Ld_m;
   // top-k rows: the gathering pass before the selection (null: none) --
   // gbound [B * rows] each row's lower bound of fl(x c) over its top-k set
   // (+inf: not gathered), glist / gcount what the pass kept per chunk
@@ -53,7 +51,6 @@ __host__ __device__ inline bool gathers_row(const Filter& f, int nchunk) {
 }
 
 constexpr int kSelThreads = 512;
-constexpr int kMaskThreads = 256;  // threads of a masking CTA
 // A selecting CTA sweeps its row with one 16-byte load per thread per step,
 // used at once (its registers are at the two-CTAs-per-SM cap), so each step
 // would wait a full DRAM round trip; every thread therefore also pulls its
@@ -842,96 +839,6 @@ __global__ void __launch_bounds__(kSelThreads)
   };
   if (!draft) run(static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (P.k + 1) + r) * V);
   else run(static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * V);
-}
-
-// the masked copies: x where key(x) >= K of its row (or only at the kept index
-// for top_k == 1), -inf elsewhere.  Each side (target rows, draft rows) is one
-// flat row-major array; a thread takes 16-byte vectors of it (plain entries
-// when the rows are not 16-byte aligned).
-template <typename T>
-__device__ __forceinline__ bool mask_keep(float x, int v, unsigned K, int first) {
-  // a NaN stays, whatever its sign, so that the row is still rejected as invalid
-  return isnan(x) || (first >= 0 ? v == first : key_of(x) >= K);
-}
-
-// one 16-byte vector of row entries [v0, v0 + 16 / sizeof(T)), masked
-template <typename T>
-__device__ __forceinline__ uint4 mask_vec(uint4 u, int v0, unsigned K, int first) {
-  if constexpr (sizeof(T) == 2) {
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t lo = w[q] & 0xffffu, hi = w[q] >> 16;
-      if (!mask_keep<T>(__uint_as_float(lo << 16), v0 + 2 * q, K, first)) lo = 0xFF80u;
-      if (!mask_keep<T>(__uint_as_float(hi << 16), v0 + 2 * q + 1, K, first)) hi = 0xFF80u;
-      w[q] = lo | (hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  } else {
-    float x[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (!mask_keep<T>(x[q], v0 + q, K, first)) x[q] = -INFINITY;
-    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
-  }
-}
-
-// One row (index g in the per-row arrays) by one CTA: the threshold read
-// once, then every thread with four independent 16-byte vectors in flight.
-template <typename T>
-__device__ void mask_row(const T* __restrict__ src, T* __restrict__ dst, int V, bool vec, unsigned K,
-                         int first) {
-  constexpr int kVE = 16 / static_cast<int>(sizeof(T));
-  constexpr int kT = kMaskThreads;
-  if (vec) {  // V is a multiple of kVE (the row is 16-byte aligned and sized)
-    const int vpr = V / kVE;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-    int v = threadIdx.x;
-#pragma unroll 1
-    for (; v + 3 * kT < vpr; v += 4 * kT) {
-      uint4 u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = __ldg(s4 + v + q * kT);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) d4[v + q * kT] = mask_vec<T>(u[q], (v + q * kT) * kVE, K, first);
-    }
-#pragma unroll 1
-    for (; v < vpr; v += kT) d4[v] = mask_vec<T>(__ldg(s4 + v), v * kVE, K, first);
-  } else {
-#pragma unroll 1
-    for (int v = threadIdx.x; v < V; v += kT) {
-      const float x = row_at<T>(src, v);
-      const bool keep = mask_keep<T>(x, v, K, first);
-      if constexpr (sizeof(T) == 2) dst[v] = keep ? src[v] : static_cast<uint16_t>(0xFF80u);
-      else dst[v] = keep ? x : -INFINITY;
-    }
-  }
-}
-
-// The masked copies of every target and draft row: CTA i takes rows i,
-// i + grid, ... of the target rows followed by the draft rows.
-template <typename TT, typename TD>
-__global__ void __launch_bounds__(kMaskThreads) mask_kernel(const __grid_constant__ Params P,
-                                                             const __grid_constant__ FilterParams F) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int nt = P.B * (P.k + 1), nd = P.B * P.k;
-#pragma unroll 1
-  for (int row = blockIdx.x; row < nt + nd; row += gridDim.x) {
-    const bool draft = row >= nt;
-    const int rr = draft ? row - nt : row;
-    const int per = draft ? P.k : P.k + 1;
-    const int b = rr / per, j = rr - b * per;
-    const int g = b * P.rows + (draft ? P.k + 1 + j : j);  // index in the per-row arrays
-    const unsigned K = __ldg(F.key + g);
-    const int first = __ldg(F.first + g);
-    const int64_t o = static_cast<int64_t>(rr) * P.V;
-    if (draft)
-      mask_row<TD>(static_cast<const TD*>(P.Ld) + o, static_cast<TD*>(F.Ld_m) + o, P.V, P.vec_d != 0, K, first);
-    else
-      mask_row<TT>(static_cast<const TT*>(P.Lt) + o, static_cast<TT*>(F.Lt_m) + o, P.V, P.vec_t != 0, K, first);
-  }
 }
 
 }  // namespace sv

@@ -36,14 +36,11 @@ struct spec_verify_s {
   int n_sched = 0;
   float sched[SV_MAX_K] = {};
   float min_cum = 0.f;
-  // sampler filters (spec_verify_set_filters) and their buffers, allocated on
-  // first use: each row's kept set (every filtered call), masked copies of
-  // the logits (filtered diagnostics only)
+  // sampler filters (spec_verify_set_filters) and their buffer, allocated on
+  // first use: each row's kept set
   sv::Filter filt[2] = {{0, 1.f, 0.f}, {0, 1.f, 0.f}};
   void* fbuf = nullptr;
   size_t fbuf_bytes = 0;
-  void* fcopy = nullptr;
-  size_t fcopy_bytes = 0;
 };
 
 namespace sv {

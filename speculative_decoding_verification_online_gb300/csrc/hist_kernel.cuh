@@ -162,8 +162,11 @@ __device__ __forceinline__ void hist_visit(const uint4& u, unsigned& mx, HistSha
       // d + 0x7400 has bit 15 set; any other word goes out of line whole
       const uint32_t d2 = (w[e] & 0x7fff7fffu) - (kMagLo | (kMagLo << 16));
       if (((d2 | (d2 + 0x74007400u)) & 0x80008000u) == 0u) {
-        atomicAdd(&sh.cnt[(d2 & 0xffffu) + ((w[e] & 0x8000u) ? 0u : kHSide)], 1u);
-        atomicAdd(&sh.cnt[(d2 >> 16) + ((w[e] & 0x80000000u) ? 0u : kHSide)], 1u);
+        // both counters at once: kHSide added to each positive half (the sum
+        // stays below 2 kHSide, so nothing carries between the halves)
+        const uint32_t i2 = d2 + ((~w[e] >> 15) & 0x00010001u) * static_cast<uint32_t>(kHSide);
+        atomicAdd(&sh.cnt[i2 & 0xffffu], 1u);
+        atomicAdd(&sh.cnt[i2 >> 16], 1u);
       } else {
         rare |= 3u << (2 * e);
       }

@@ -55,7 +55,13 @@ cudaError_t configure(int* blocks_per_sm, int fin_spread_smem) {
     e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeGather, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pair_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(stream_kernel<TT, TD, kModeStats, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pair_kernel<TT, TD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pair_smem<TT, TD>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pair_kernel<TT, TD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              pair_smem<TT, TD>());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(select_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -171,11 +177,13 @@ sv_status launch(spec_verify_t h, const Params& P, int blocks_per_sm, bool dense
 
 // the acceptance diagnostics: the stream pass, the per-position merge, and
 // (temperature > 0) the pair sweep and its reduction, each launch a
-// programmatic dependent of the one before
-template <typename TT, typename TD, bool kGreedy>
+// programmatic dependent of the one before (kFilt: the rows as the sampler
+// filters leave them, applied as logits load)
+template <typename TT, typename TD, bool kGreedy, bool kFilt>
 sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float* min_sum,
                       float* pq_sum, float* argmax_q, cudaStream_t st) {
-  const sv_status rs = launch_stream<TT, TD, kGreedy ? kModeGreedy : kModeStats, false>(h, P, blocks_per_sm, st);
+  static_assert(!(kGreedy && kFilt), "a greedy call is one-hot already");
+  const sv_status rs = launch_stream<TT, TD, kGreedy ? kModeGreedy : kModeStats, kFilt>(h, P, blocks_per_sm, st);
   if (rs != SV_OK) return rs;
   const unsigned npos = static_cast<unsigned>(P.B * P.k);
   const unsigned small_grid = (npos + kDiagWarps - 1) / kDiagWarps;
@@ -188,7 +196,7 @@ sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float
     long long grid = h->num_sms;
     const long long need = (static_cast<long long>(total) + kW - 1) / kW;
     if (grid > need) grid = need;
-    if (launch_dependent(pair_kernel<TT, TD>, static_cast<unsigned>(grid),
+    if (launch_dependent(pair_kernel<TT, TD, kFilt>, static_cast<unsigned>(grid),
                          PairStages<TT, TD>::kThreadsPerCta, pair_smem<TT, TD>(), st, P,
                          static_cast<const DiagNorm*>(h->dnorm), total) != cudaSuccess)
       return SV_ECUDA;
@@ -236,13 +244,11 @@ sv_status launch_selection(spec_verify_t h, const Params& P, FilterParams& F, in
 // top_k = 1, the kept index).  When every filtered side holds bf16 logits and
 // none is top_k = 1, hist_kernel finds it from one read of each row;
 // otherwise the statistics pass of the raw rows, then (top-k rows) the
-// gathering passes, then select_kernel.  A verifying call then applies them
-// on the fly (P.fthr, P.ffirst: its stream and finishing kernels mask every
-// logit they load).  With `copies` (the diagnostics, whose kernels read rows
-// as they are) mask_kernel also writes masked copies of the logits and P
-// reads those instead.
+// gathering passes, then select_kernel.  The call's kernels then apply them on
+// the fly (P.fthr, P.ffirst: every logit outside a row's kept set reads as
+// -inf).
 template <typename TT, typename TD>
-sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool copies, cudaStream_t st) {
+sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, cudaStream_t st) {
   const size_t rows_all = static_cast<size_t>(h->max_B) * (2 * h->k + 1);
   const size_t chunks_all = rows_all * h->nchunk;
   const size_t o_key = 0, o_first = align_up(rows_all * sizeof(unsigned), 256);
@@ -259,16 +265,6 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
     }
     h->fbuf_bytes = need;
   }
-  if (copies && !h->fcopy) {
-    // masked copies sized for max_B and fp32 (the larger element type)
-    const size_t bt = static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float);
-    const size_t bd = static_cast<size_t>(h->max_B) * h->k * h->V * sizeof(float);
-    if (cudaMalloc(&h->fcopy, align_up(bt, 256) + bd) != cudaSuccess) {
-      h->fcopy = nullptr;
-      return SV_ENOMEM;
-    }
-    h->fcopy_bytes = align_up(bt, 256) + bd;
-  }
   char* base = static_cast<char*>(h->fbuf);
   FilterParams F;
   F.f[0] = h->filt[0];
@@ -280,10 +276,6 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
   F.gcount = nullptr;
   F.glist = nullptr;
   F.done = nullptr;
-  F.Lt_m = copies ? h->fcopy : nullptr;
-  F.Ld_m = copies ? static_cast<char*>(h->fcopy) +
-                        align_up(static_cast<size_t>(h->max_B) * (h->k + 1) * h->V * sizeof(float), 256)
-                  : nullptr;
   const unsigned nrows = static_cast<unsigned>(P.B * P.rows);
   if (hist_selects(F.f[0], sizeof(TT) == 2) && hist_selects(F.f[1], sizeof(TD) == 2)) {
     if (launch_dependent(hist_kernel<TT, TD>, nrows, kHThreads, 0, st, P, F) != cudaSuccess) return SV_ECUDA;
@@ -293,22 +285,8 @@ sv_status launch_filters(spec_verify_t h, Params& P, int blocks_per_sm, bool cop
     rs = launch_selection<TT, TD>(h, P, F, blocks_per_sm, base + o_gc, base + o_gl, base + o_done, st);
     if (rs != SV_OK) return rs;
   }
-  if (copies) {
-    // one CTA per row at a time, at most eight per SM
-    long long grid = static_cast<long long>(P.B) * P.rows;
-    if (grid > 8ll * h->num_sms) grid = 8ll * h->num_sms;
-    if (grid < 1) grid = 1;
-    if (launch_dependent(mask_kernel<TT, TD>, static_cast<unsigned>(grid), static_cast<unsigned>(kMaskThreads),
-                         0, st, P, F) != cudaSuccess)
-      return SV_ECUDA;
-    P.Lt = F.Lt_m;
-    P.Ld = F.Ld_m;
-    P.vec_t = (static_cast<size_t>(P.V) * sizeof(TT)) % 16 == 0;
-    P.vec_d = (static_cast<size_t>(P.V) * sizeof(TD)) % 16 == 0;
-  } else {
-    P.fthr = F.thr;
-    P.ffirst = F.first;
-  }
+  P.fthr = F.thr;
+  P.ffirst = F.first;
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
@@ -320,7 +298,7 @@ sv_status verify_pair(spec_verify_t h, Params& P, int mode, int bps, bool dense_
                       cudaStream_t st) {
   if (mode == kModeGreedy) return launch<TT, TD, kModeGreedy, false>(h, P, bps, false, st);
   if (filtered) {
-    const sv_status rs = launch_filters<TT, TD>(h, P, bps, false, st);
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
     if (rs != SV_OK) return rs;
     if (mode == kModePolicy) return launch<TT, TD, kModePolicy, true>(h, P, bps, dense_likely, st);
     return launch<TT, TD, kModeSample, true>(h, P, bps, dense_likely, st);
@@ -333,12 +311,13 @@ sv_status verify_pair(spec_verify_t h, Params& P, int mode, int bps, bool dense_
 template <typename TT, typename TD>
 sv_status diag_pair(spec_verify_t h, Params& P, int bps, bool filtered, float* min_sum, float* pq_sum,
                     float* argmax_q, cudaStream_t st) {
+  if (P.greedy) return launch_diag<TT, TD, true, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
   if (filtered) {
-    const sv_status rs = launch_filters<TT, TD>(h, P, bps, true, st);
+    const sv_status rs = launch_filters<TT, TD>(h, P, bps, st);
     if (rs != SV_OK) return rs;
+    return launch_diag<TT, TD, false, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
   }
-  if (P.greedy) return launch_diag<TT, TD, true>(h, P, bps, min_sum, pq_sum, argmax_q, st);
-  return launch_diag<TT, TD, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
+  return launch_diag<TT, TD, false, false>(h, P, bps, min_sum, pq_sum, argmax_q, st);
 }
 
 }  // namespace

@@ -425,7 +425,6 @@ sv_status spec_verify_free(spec_verify_t h) {
     if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = SV_ECUDA;
     if (h->stage && cudaFree(h->stage) != cudaSuccess) rc = SV_ECUDA;
     if (h->fbuf && cudaFree(h->fbuf) != cudaSuccess) rc = SV_ECUDA;
-    if (h->fcopy && cudaFree(h->fcopy) != cudaSuccess) rc = SV_ECUDA;
   }
   delete h;
   return rc;
