@@ -161,6 +161,32 @@ def test_filtered_diagnostics(sv):
     ver.close()
 
 
+@pytest.mark.parametrize("dtype,filt", [
+    ("f32", ((25, 0.9, 0.0), (0, 1.0, 0.05))),   # the statistics path, both rows masked as they load
+    ("bf16", ((1, 1.0, 0.0), (12, 0.9, 0.0))),   # a top_k = 1 target: one kept index
+    ("f32", ((0, 0.8, 0.0), (1, 1.0, 0.0))),     # a top_k = 1 draft: q one-hot
+])
+def test_filtered_diagnostics_paths(sv, dtype, filt):
+    # the diagnostics read each row as its sampler filter leaves it, the
+    # threshold (or the one kept index) applied as logits load
+    B, k, V = 20, 3, 6000
+    w = peaked_workload(B, k, V, dtype, seed=23 + (dtype == "f32"), gate=(np.arange(B) % 2), tau=0.3)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = ver.diagnostics(w.Lt, w.Ld, w.D, w.T, gate_mode=sv.SV_GATED_MU, threshold=0.5,
+                          gate_per_seq=w.gate, threshold_per_seq=w.tau)
+    torch.cuda.synchronize()
+    ref = O.diagnostics(workloads.to_numpy_logits(w.Lt), workloads.to_numpy_logits(w.Ld), w.D.cpu().numpy(),
+                        w.T, w.gate.cpu().numpy(), w.tau.cpu().numpy().astype(np.float64), filters=filt,
+                        nthreads=16)
+    keep = ref["margin"] >= 1e-6
+    for key in ("min_sum", "pq_sum", "argmax_q"):
+        np.testing.assert_allclose(out[key].cpu().numpy()[keep], ref[key][keep], rtol=2e-5, atol=2e-6,
+                                   err_msg=key)
+    assert keep.sum() >= B // 2
+    ver.close()
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_filters_with_a_gate_policy(sv, dtype):
     # the features compose: filtered p and q, a per-step schedule and a
@@ -374,4 +400,23 @@ def test_degenerate_gated_residual_on_the_candidate_path(sv):
     compare(w, out, ref, what="degenerate gated", filters=filt)
     assert int(cnt[sv.SV_CNT_DEGENERATE]) == int(ref["degenerate"].sum()) == B
     assert (out["tokens"][:, 0] >= 0).all()
+    ver.close()
+
+
+@pytest.mark.parametrize("V", [1, 8, 67, 2047])
+def test_histogram_selection_small_vocabularies(sv, V):
+    # one logit, one 16-byte vector, the scalar read (rows not 16-byte
+    # multiples), and top_k at or above V (no top-k)
+    filt = ((3, 0.9, 0.0), (0, 0.8, 0.1))
+    B, k = 16, 3
+    w = peaked_workload(B, k, V, "bf16", seed=900 + V, gate=(np.arange(B) % 2), tau=0.3, T=0.9)
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w, filters=filt)
+    st = compare(w, out, ref, what=f"histogram small V={V}", filters=filt)
+    ok = ref["margin"] >= 1e-6
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
+    assert st["compared"] >= B // 2
     ver.close()
