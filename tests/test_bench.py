@@ -50,3 +50,26 @@ def test_cpu_oracle_rate_on_one_thread_and_a_pool():
         rate, reps, el = b["cpu_oracle_rate"](w, 0.05, threads)
         assert rate > 0 and reps >= 1 and el >= 0.05
         assert abs(rate - reps * w.B * w.k / el) < 1e-9 * rate
+
+
+def test_filter_launch_counts_follow_the_selection_route():
+    # the launches a filtered call adds in front of its own (the bench line's
+    # gpu_launches counts them): the histogram selection (1) when every
+    # filtered side is bf16 and none is top_k = 1, else the statistics pass
+    # and select_kernel (2), plus bound, gathering and list selection (3) when
+    # a side gathers its top-k set (2 <= top_k <= chunks <= 512); within the
+    # header's bound of 7 launches per filtered verifying call
+    fl = _bench()["filter_launches"]
+    OFF = (0, 1.0, 0.0)
+    V = 128256  # 63 chunks
+    assert fl(((50, 0.9, 0.0), (40, 0.95, 0.0)), V, ("bf16", "bf16")) == 1
+    assert fl(((0, 0.9, 0.0), OFF), V, ("bf16", "f32")) == 1  # the f32 side is unfiltered
+    assert fl(((0, 1.0, 0.05), OFF), V, ("bf16", "bf16")) == 1
+    assert fl(((1, 1.0, 0.0), OFF), V, ("bf16", "bf16")) == 2  # top_k = 1: select_kernel's kept index
+    assert fl(((0, 0.9, 0.0), OFF), V, ("f32", "f32")) == 2
+    assert fl(((50, 0.9, 0.0), OFF), V, ("f32", "f32")) == 5  # gathered top-k
+    assert fl(((64, 0.9, 0.0), OFF), V, ("f32", "f32")) == 2  # k above the 63 chunks: not gathered
+    assert fl(((50, 0.9, 0.0), (1, 1.0, 0.0)), V, ("bf16", "bf16")) == 5
+    for filt in (((50, 0.9, 0.0), (40, 0.95, 0.0)), ((1, 1.0, 0.0), (3, 1.0, 0.0))):
+        for dts in (("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32")):
+            assert fl(filt, V, dts) + 2 <= 7
