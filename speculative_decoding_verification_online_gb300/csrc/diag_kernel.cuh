@@ -193,7 +193,7 @@ struct PairQueue {
 };
 
 // partial record of chunk pair (b, j, ch): (sum min(p, mu), sum p q, largest
-// target logit, first index holding it), over the chunk statistics' storage
+// target logit, unused), over the chunk statistics' storage
 __device__ __forceinline__ float4* pair_partials(const Params& P) { return reinterpret_cast<float4*>(P.part); }
 
 template <typename T>
@@ -298,48 +298,44 @@ __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
     const unsigned char* st = ring + (n % S) * kStage;
     if (!nm.bad) {
       float amin = 0.f, apq = 0.f, best = -INFINITY;
-      int bidx = 0x7fffffff;
       const int c0 = it.z * kChunk;
-      // lane l takes entries (32 g + l) 8 .. + 7, g = 0..7: in index order,
-      // so a strict > keeps its first largest logit
+      // lane l takes entries (32 g + l) 8 .. + 7, g = 0..7; the terms use the
+      // fast exp2 (the sums' tolerance is far above its error), and without a
+      // cumulative floor the gate is one compare
+      auto sweep = [&](auto cum) {
 #pragma unroll 2
-      for (int g = 0; g < kChunk / 256; ++g) {
-        const int o = (32 * g + lane) * 8;
-        float xt[8], xd[8], mn[8], pq[8];
-        stage8<TT>(st, o, xt);
-        stage8<TD>(st + kBT, o, xd);
-        if constexpr (kFilt) {
-          filt8(xt, c0 + o, thr_t, first_t);
-          filt8(xd, c0 + o, thr_d, first_d);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float p = prob_of(xt[e], nm.Mt, c, nm.invSt);
-          const float q = prob_of(xd[e], nm.Md, c, nm.invSd);
-          const float mu = (q >= nm.tau_e && nm.cprev * q >= nm.mc_e) ? q : 0.f;
-          mn[e] = fminf(p, mu);
-          pq[e] = p * q;
-          if (xt[e] > best) {
-            best = xt[e];
-            bidx = c0 + o + e;
+        for (int g = 0; g < kChunk / 256; ++g) {
+          const int o = (32 * g + lane) * 8;
+          float xt[8], xd[8], mn[8], pq[8];
+          stage8<TT>(st, o, xt);
+          stage8<TD>(st + kBT, o, xd);
+          if constexpr (kFilt) {
+            filt8(xt, c0 + o, thr_t, first_t);
+            filt8(xd, c0 + o, thr_d, first_d);
           }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float p = ex2_approx(fmaf(xt[e], c, -nm.Mt)) * nm.invSt;
+            const float q = ex2_approx(fmaf(xd[e], c, -nm.Md)) * nm.invSd;
+            bool adm = q >= nm.tau_e;
+            if constexpr (decltype(cum)::value) adm = adm && nm.cprev * q >= nm.mc_e;
+            mn[e] = fminf(p, adm ? q : 0.f);
+            pq[e] = p * q;
+            best = fmaxf(best, xt[e]);
+          }
+          amin += ((mn[0] + mn[1]) + (mn[2] + mn[3])) + ((mn[4] + mn[5]) + (mn[6] + mn[7]));
+          apq += ((pq[0] + pq[1]) + (pq[2] + pq[3])) + ((pq[4] + pq[5]) + (pq[6] + pq[7]));
         }
-        amin += ((mn[0] + mn[1]) + (mn[2] + mn[3])) + ((mn[4] + mn[5]) + (mn[6] + mn[7]));
-        apq += ((pq[0] + pq[1]) + (pq[2] + pq[3])) + ((pq[4] + pq[5]) + (pq[6] + pq[7]));
-      }
+      };
+      if (nm.mc_e >= 0.f) sweep(std::true_type{});
+      else sweep(std::false_type{});
       amin = warp_sum(amin);
       apq = warp_sum(apq);
-#pragma unroll
-      for (int s = 16; s > 0; s >>= 1) {
-        const float ob = __shfl_xor_sync(0xffffffffu, best, s);
-        const int oi = __shfl_xor_sync(0xffffffffu, bidx, s);
-        if (ob > best || (ob == best && oi < bidx)) {
-          best = ob;
-          bidx = oi;
-        }
-      }
+      best = warp_max(best);
+      // the chunk's largest target logit; the reduction finds the first index
+      // of the row's largest in the first chunk that holds it
       if (lane == 0)
-        out[(static_cast<int64_t>(it.x) * k + it.y) * nch + it.z] = make_float4(amin, apq, best, __int_as_float(bidx));
+        out[(static_cast<int64_t>(it.x) * k + it.y) * nch + it.z] = make_float4(amin, apq, best, 0.f);
     }
     __syncwarp();
   }
@@ -348,7 +344,7 @@ __global__ void __launch_bounds__(PairStages<TT, TD>::kThreadsPerCta, 1)
 
 // launch 4: one warp per (sequence b, position j): the partials added in
 // chunk order, the argmax's q looked up
-template <typename TD>
+template <typename TT, typename TD>
 __global__ void __launch_bounds__(kDiagThreads)
     diag_reduce_kernel(const __grid_constant__ Params P, const DiagNorm* __restrict__ norm, float* min_sum,
                        float* pq_sum, float* argmax_q) {
@@ -365,7 +361,7 @@ __global__ void __launch_bounds__(kDiagThreads)
   }
   const float4* part = pair_partials(P) + static_cast<int64_t>(g) * nch;
   float amin = 0.f, apq = 0.f, best = -INFINITY;
-  int bidx = 0x7fffffff;
+  int bch = 0x7fffffff;  // the first chunk holding the row's largest target logit
   // the same trip count on every lane: the shuffles below run converged
   const int niter = (nch + 31) >> 5;
 #pragma unroll 1
@@ -375,10 +371,9 @@ __global__ void __launch_bounds__(kDiagThreads)
     const float4 r = __ldcg(part + ch);
     amin += r.x;
     apq += r.y;
-    const int ri = __float_as_int(r.w);
-    if (r.z > best || (r.z == best && ri < bidx)) {
+    if (r.z > best) {  // chunks in increasing order per lane: the first one kept
       best = r.z;
-      bidx = ri;
+      bch = ch;
     }
   }
   amin = warp_sum(amin);
@@ -386,14 +381,33 @@ __global__ void __launch_bounds__(kDiagThreads)
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) {
     const float ob = __shfl_xor_sync(0xffffffffu, best, s);
-    const int oi = __shfl_xor_sync(0xffffffffu, bidx, s);
-    if (ob > best || (ob == best && oi < bidx)) {
+    const int oc = __shfl_xor_sync(0xffffffffu, bch, s);
+    if (ob > best || (ob == best && oc < bch)) {
       best = ob;
-      bidx = oi;
+      bch = oc;
     }
   }
+  // the first index of that logit in that chunk of the target row (the
+  // largest logit is kept by every sampler filter, so the raw row serves)
+  const int b = g / k, j = g % k;
+  int bidx = 0x7fffffff;
+  if (bch < nch) {
+    // lane l holds entries [64 l, 64 l + 64) of the chunk, loaded at once
+    // (entries past V read as -inf)
+    const TT* trow = static_cast<const TT*>(P.Lt) + (static_cast<int64_t>(b) * (k + 1) + j) * V;
+    const int v0 = bch * kChunk + 64 * lane;
+    float x[8][8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) load8<TT>(trow, v0 + 8 * h, V, P.vec_t != 0, x[h]);
+#pragma unroll
+    for (int h = 7; h >= 0; --h)
+#pragma unroll
+      for (int e = 7; e >= 0; --e)
+        if (x[h][e] == best) bidx = v0 + 8 * h + e;  // the last assignment is the first index
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) bidx = min(bidx, __shfl_xor_sync(0xffffffffu, bidx, s));
+  }
   if (lane == 0) {
-    const int b = g / k, j = g % k;
     const TD* drow = static_cast<const TD*>(P.Ld) + (static_cast<int64_t>(b) * k + j) * V;
     float aq = NAN;
     if (bidx < V) {

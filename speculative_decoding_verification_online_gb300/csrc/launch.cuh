@@ -200,7 +200,7 @@ sv_status launch_diag(spec_verify_t h, const Params& P, int blocks_per_sm, float
                          PairStages<TT, TD>::kThreadsPerCta, pair_smem<TT, TD>(), st, P,
                          static_cast<const DiagNorm*>(h->dnorm), total) != cudaSuccess)
       return SV_ECUDA;
-    if (launch_dependent(diag_reduce_kernel<TD>, small_grid, kDiagThreads, 0, st, P,
+    if (launch_dependent(diag_reduce_kernel<TT, TD>, small_grid, kDiagThreads, 0, st, P,
                          static_cast<const DiagNorm*>(h->dnorm), min_sum, pq_sum, argmax_q) != cudaSuccess)
       return SV_ECUDA;
   }
