@@ -603,6 +603,52 @@ __device__ __forceinline__ void put_item(const Params& P, Queue& Q, int slot, un
   }
 }
 
+// a hint: the line holding p is brought into L2 (no data returned, no effect
+// on what any later load reads)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// How many of a CTA's first chunks the stream pass prefetches into L2 before
+// its programmatic wait, per warp.  While the previous call's finishing pass
+// runs and this grid's wait is released, DRAM is nearly idle; each warp's
+// first copy then finds its lines in L2.  Measured on the 128K-vocabulary
+// batch (64 sequences, k = 5, bf16): 39.3 us per step without, 38.8 us with
+// one chunk per warp, 39.0 us with two (a full ring), 40.3 us with four --
+// deeper prefetches slow the step.
+constexpr int kPrefetchPerWarp = 1;
+
+// Warp `warp` of the CTA prefetches chunks i = warp, warp + W, ... < n of the
+// CTA's share (chunk index blockIdx.x + i gridDim.x), one 128-byte line per
+// lane and step, every address inside the chunk's row.  The addresses come
+// from the launch arguments alone: nothing is read.
+template <typename TT, typename TD>
+__device__ __forceinline__ void prefetch_first_chunks(const Params& P, int n, int warp, int lane) {
+  constexpr int W = Stages<TT, TD>::kWarpsPerCta;
+  for (int i = warp; i < n; i += W) {
+    const unsigned long long x = blockIdx.x + static_cast<unsigned long long>(i) * gridDim.x;
+    if (x >= P.total_chunks) break;
+    const unsigned rg = fastdiv(static_cast<unsigned>(x), P.div_nchunk);
+    const int ch = static_cast<int>(static_cast<unsigned>(x) - rg * static_cast<unsigned>(P.nchunk));
+    const unsigned b = fastdiv(rg, P.div_rows);
+    const int r = static_cast<int>(rg - b * static_cast<unsigned>(P.rows));
+    const int c0 = ch * kChunk;
+    const int len = min(kChunk, P.V - c0);
+    const char* base;
+    int bytes;
+    if (r <= P.k) {
+      base = static_cast<const char*>(P.Lt) +
+             ((static_cast<int64_t>(b) * (P.k + 1) + r) * P.V + c0) * static_cast<int64_t>(sizeof(TT));
+      bytes = len * static_cast<int>(sizeof(TT));
+    } else {
+      base = static_cast<const char*>(P.Ld) +
+             ((static_cast<int64_t>(b) * P.k + (r - P.k - 1)) * P.V + c0) * static_cast<int64_t>(sizeof(TD));
+      bytes = len * static_cast<int>(sizeof(TD));
+    }
+    for (int o = lane * 128; o < bytes; o += 32 * 128) prefetch_l2(base + o);
+  }
+}
+
 template <typename TT, typename TD>
 __device__ __forceinline__ void issue_chunk(const Params& P, int b, int r, int ch, unsigned char* stage,
                                             int lane) {
@@ -798,7 +844,11 @@ __global__ void __launch_bounds__(Stages<TT, TD>::kThreadsPerCta, Stages<TT, TD>
   // This grid is itself a programmatic dependent launch: its CTAs may be
   // resident while the previous kernel in the stream (the producer of the
   // logits, or the previous call's finishing pass, which reads the workspace)
-  // drains, and touch no global memory before that kernel has completed.
+  // drains, and read no global memory before that kernel has completed.  Only
+  // L2 prefetches of the first chunks go out before: a prefetch returns no
+  // data, and a load after the wait reads what the producer wrote whether or
+  // not the line was prefetched (L2 is where device writes become visible).
+  prefetch_first_chunks<TT, TD>(P, kPrefetchPerWarp * Stages<TT, TD>::kWarpsPerCta, warp, lane);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // Then the finishing grid may launch: its CTAs take SMs as this grid's CTAs
   // retire, run their input-only prologue (the inputs are complete: see the
@@ -1003,10 +1053,6 @@ __device__ __forceinline__ void residual8(const ResidualEval& e, const float (&x
 // what the finishing pass of sequence b needs from the inputs alone: drafted
 // tokens, the Philox draws (or the explicit uniforms), the gate.  Runs before
 // the wait on the stream pass.
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 template <int kMode>
 __device__ __forceinline__ void finish_prologue(const Params& P, int b, FinishShared& sh, bool dry) {
   const int tid = threadIdx.x, k = P.k;
