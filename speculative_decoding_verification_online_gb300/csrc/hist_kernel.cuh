@@ -15,7 +15,9 @@
 // 0 < |x| < 2^-15 (kept in a short list, each with its own mass), and
 // |x| >= 2^9 (counted, with the largest of the negative ones).  The row's
 // maximum comes from the same read (packed bf16 maxima); min-p alone needs
-// nothing else, and its rows count nothing.  A row whose answer lies outside
+// nothing else, and its rows count nothing.  A top-k row counts its first
+// logits in full and then only the logits at or above their k-th largest
+// (hist_sweep_cut): the decisions never look below the row's k-th largest.  A row whose answer lies outside
 // the exact counters -- a logit >= 2^9, a threshold among the tiny values or
 // below -2^9, a tiny list over its cap, or logits below -2^9 whose masses are
 // not all zero under top-p -- is selected by a radix descent over its 16-bit
@@ -70,6 +72,7 @@ struct alignas(16) HistShared {  // (16-byte loads of the counters)
   unsigned nbelow, kbelow;  // logits <= -2^9 (-inf too) and their largest 16-bit key
   unsigned nabove;          // finite logits >= 2^9
   int bad;                  // a NaN or +inf: an invalid row
+  uint4 queue[kHWarps][2 * 32];  // per warp: vectors at or above a top-k row's cut, to count
   unsigned bcnt[kHNBlk];    // per block of 32 ranks: counts and masses
   unsigned long long bmass[kHNBlk];
   unsigned long long wsum[kHWarps];  // per warp: its blocks' mass
@@ -144,6 +147,21 @@ static __device__ __noinline__ void hist_some8(uint4 u, unsigned bits, HistShare
   }
 }
 
+// packed bf16 maximum that keeps a NaN (either operand NaN: NaN)
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// both bf16 halves of v below the same halves of t (ordered: a NaN is not below)
+__device__ __forceinline__ bool both_below(uint32_t v, uint32_t t) {
+  uint32_t r;
+  asm("{\n\t.reg .pred p, q;\n\tsetp.lt.bf16x2 p|q, %1, %2;\n\tand.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(t));
+  return r != 0u;
+}
+
 // What a sweep does with each 16-byte vector (eight logits): kMaxOnly the
 // packed maximum alone; kCountAll the maximum and every logit into its counter.
 enum : int { kMaxOnly = 0, kCountAll = 1 };
@@ -153,7 +171,7 @@ __device__ __forceinline__ void hist_visit(const uint4& u, unsigned& mx, HistSha
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) mx = bmax2(mx, w[e]);
-  if constexpr (kHow == kCountAll) {
+  if constexpr (kHow != kMaxOnly) {
     unsigned rare = 0u;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -184,10 +202,10 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
   return v;
 }
 
-// the row's vectors [0, nv): two sets of four 16-byte vectors per thread, one
-// in flight while the other is visited
+// the row's vectors [first, nv) (first: this thread's first vector): two sets
+// of four 16-byte vectors per thread, one in flight while the other is visited
 template <int kHow>
-__device__ __forceinline__ void hist_sweep(const uint4* r4, int nv, unsigned& mx, HistShared& sh) {
+__device__ __forceinline__ void hist_sweep(const uint4* r4, int nv, unsigned& mx, HistShared& sh, int first) {
   // past nv: -inf, which does not raise the maximum (a count skips them)
   const uint4 none = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   uint4 a[4], b[4];
@@ -203,7 +221,7 @@ __device__ __forceinline__ void hist_sweep(const uint4* r4, int nv, unsigned& mx
     for (int q = 0; q < 4; ++q)
       if (kHow == kMaxOnly || base + q * kHThreads < nv) hist_visit<kHow>(u[q], mx, sh);
   };
-  int base = static_cast<int>(threadIdx.x);
+  int base = first;
   load4(base, a);
   load4(base + 4 * kHThreads, b);
 #pragma unroll 1
@@ -396,6 +414,95 @@ static __device__ void hist_cross(bool by_mass, bool masses, unsigned long long 
   __syncthreads();
 }
 
+// A top-k row's read in two parts.  The first set of vectors (four per
+// thread: the row's first 8192 logits) is counted in full; the k-th largest of
+// those logits is at most the row's k-th largest, so every rank the top-k and
+// top-p decisions look at -- those at or above the row's k-th largest, whose
+// values are then all at or above the cut -- is counted whole when the rest of
+// the read counts only the vectors holding a logit at or above the cut.
+// Counters below the cut stay partial, and nothing reads them: the counts'
+// crossing lies at or above the row's k-th largest, and the top-p target is a
+// fraction of the mass through it.  A crossing among the first logits outside
+// the exact ranks (none, or a tiny class) sets no cut.
+//
+// Few vectors reach the cut (about one in twenty on Zipf-like rows), spread at
+// random, so a lane that meets one does not count it alone -- the warp would
+// issue the whole count for it -- but appends it to its warp's queue (a ballot
+// and its prefix count place it); each time 32 are queued the warp counts
+// them, one vector per lane.  A vector holding a NaN is never below the cut,
+// so an invalid row is still seen.
+static __device__ void hist_sweep_cut(const uint4* r4, int nv, int top_k, unsigned& mx, HistShared& sh) {
+  const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
+  const uint4 none = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  {
+    uint4 a[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = tid + q * kHThreads;
+      a[q] = i < nv ? ldg_stream(r4 + i) : none;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (tid + q * kHThreads < nv) hist_visit<kCountAll>(a[q], mx, sh);
+  }
+  __syncthreads();  // the first logits' counts are in
+  hist_block_sums(false, 0.f, 0.f, sh);
+  int bk;
+  unsigned long long unused;
+  hist_cross(false, false, static_cast<unsigned long long>(top_k), 0.f, 0.f, sh, &bk, &unused);
+  uint32_t cut2 = 0xff80ff80u;  // -inf: no vector is below it
+  if (bk >= 0 && !rank_tiny(bk)) {
+    const uint32_t t = rank_bits(bk);
+    cut2 = t | (t << 16);
+  }
+  uint4* queue = sh.queue[warp];
+  int qn = 0;  // vectors queued (the same on every lane)
+  const unsigned lt = (1u << lane) - 1u;
+  auto take = [&](const uint4& u, bool in) {
+    const uint32_t v = bmax2_nan(bmax2_nan(u.x, u.y), bmax2_nan(u.z, u.w));
+    mx = bmax2(mx, v);  // (a NaN half leaves mx's half; the row is invalid anyway)
+    const bool hit = in && !both_below(v, cut2);
+    const unsigned ball = __ballot_sync(0xffffffffu, hit);
+    if (ball) {
+      if (hit) queue[qn + __popc(ball & lt)] = u;
+      qn += __popc(ball);
+      if (qn >= 32) {
+        __syncwarp();
+        qn -= 32;
+        hist_visit<kCountAll>(queue[qn + lane], mx, sh);
+        __syncwarp();
+      }
+    }
+  };
+  // the rest, from the thread's fifth vector, two sets of four in flight; the
+  // loop runs on the warp's first lane's position, so every lane takes every
+  // ballot (lanes past the row take nothing)
+  uint4 a[4], b[4];
+  auto load4 = [&](int base, uint4(&u)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = base + q * kHThreads;
+      u[q] = i < nv ? ldg_stream(r4 + i) : none;
+    }
+  };
+  auto take4 = [&](int base, const uint4(&u)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) take(u[q], base + q * kHThreads < nv);
+  };
+  int base = tid + 4 * kHThreads;
+  load4(base, a);
+  load4(base + 4 * kHThreads, b);
+#pragma unroll 1
+  for (; base - lane < nv; base += 8 * kHThreads) {
+    take4(base, a);
+    load4(base + 8 * kHThreads, a);
+    take4(base + 4 * kHThreads, b);
+    load4(base + 12 * kHThreads, b);
+  }
+  __syncwarp();
+  if (lane < qn) hist_visit<kCountAll>(queue[lane], mx, sh);
+}
+
 __device__ __forceinline__ unsigned long long ceil_target(double t) {
   const double tc = ceil(t);
   return tc <= 0.0 ? 0ull : (tc >= 1.8e19 ? ~0ull : static_cast<unsigned long long>(tc));
@@ -582,8 +689,9 @@ __global__ void __launch_bounds__(kHThreads, 5)
       unsigned mx = 0xff80ff80u;  // packed running maximum (max.bf16x2 passes NaN over)
       if (vec) {
         const uint4* r4 = reinterpret_cast<const uint4*>(row);
-        if (count) hist_sweep<kCountAll>(r4, V >> 3, mx, sh);
-        else hist_sweep<kMaxOnly>(r4, V >> 3, mx, sh);
+        if (use_k) hist_sweep_cut(r4, V >> 3, f.top_k, mx, sh);
+        else if (count) hist_sweep<kCountAll>(r4, V >> 3, mx, sh, tid);
+        else hist_sweep<kMaxOnly>(r4, V >> 3, mx, sh, tid);
       } else {
 #pragma unroll 4
         for (int v = tid; v < V; v += kHThreads) {
