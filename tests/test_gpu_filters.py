@@ -342,6 +342,81 @@ def test_histogram_selection_edge_rows(sv, kind):
     ver.close()
 
 
+# Top-k rows count their first 8192 logits in full and, past them, only the
+# vectors holding a logit at or above the k-th largest of those (queued per
+# warp).  These rows (V = 20000, the vector path) put what that must not miss
+# past the first 8192: a NaN or +inf (an invalid row), logits >= 2^9 (the
+# radix fallback), the row's largest logits (a low cut: most vectors queued),
+# and a first 8192 of signed zeros, so that the cut is zero and top-k ends in
+# zeros of both signs.
+CUT_KINDS = {
+    "late_nan": ((50, 0.9, 0.0), (40, 0.95, 0.0)),
+    "late_posinf": ((50, 0.9, 0.0), (40, 1.0, 0.0)),
+    "late_above_2^9": ((50, 0.9, 0.0), (30, 0.8, 0.0)),
+    "largest_late": ((200, 0.9, 0.0), (64, 0.95, 0.0)),
+    "zero_cut": ((6000, 0.9, 0.0), (3000, 1.0, 0.0)),
+}
+
+
+def _cut_workload(kind, B, k, V, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    R = B * (2 * k + 1)
+    x = torch.randn(R, V, generator=g, device="cuda")
+    late = 8192 + torch.randint(0, V - 8192, (R,), generator=g, device="cuda")
+    rows = torch.arange(R, device="cuda")
+    some = rows % 5 == 1  # a fifth of the rows, leaving sequences 1, 4, 6, 9, 11 whole
+    if kind == "late_nan":
+        x[rows[some], late[some]] = float("nan")
+    elif kind == "late_posinf":
+        x[rows[some], late[some]] = float("inf")
+    elif kind == "late_above_2^9":
+        x[rows[some], late[some]] = 700.0
+    elif kind == "largest_late":
+        x[:, :8192] -= 3.0
+        x[:, 8192:] += 3.0
+    elif kind == "zero_cut":
+        x = torch.randint(-2, 3, (R, V), generator=g, device="cuda").float()
+        x[:, :8192] = 0.0
+        neg = torch.rand(R, V, generator=g, device="cuda") < 0.5
+        x = torch.where((x == 0) & neg, torch.full_like(x, -0.0), x)
+    Lt = x[: B * (k + 1)].reshape(B, k + 1, V).to(torch.bfloat16)
+    Ld = x[B * (k + 1):].reshape(B, k, V).to(torch.bfloat16)
+    u = torch.rand(B, k, V, generator=g, device="cuda").clamp_(1e-30, 1 - 1e-7)
+    xd = torch.nan_to_num(Ld.float(), nan=0.0, posinf=0.0)
+    D = torch.argmax(xd - torch.log(-torch.log(u)), dim=2).to(torch.int32)
+    gate = torch.as_tensor((np.arange(B) % 2).astype(np.uint8), device="cuda")
+    return workloads.Workload(name=kind, Lt=Lt, Ld=Ld, D=D, T=1.0, gate=gate,
+                              tau=torch.full((B,), 0.3, device="cuda"), philox_seed=seed + 1, B=B, k=k, V=V,
+                              dtype="bf16")
+
+
+@pytest.mark.parametrize("kind", sorted(CUT_KINDS))
+def test_histogram_selection_cut_rows(sv, kind):
+    filt = CUT_KINDS[kind]
+    B, k, V = 12, 2, 20000
+    w = _cut_workload(kind, B, k, V, seed=900 + sorted(CUT_KINDS).index(kind))
+    ver = sv.SpecVerifier(B, k, V, device=0)
+    ver.set_filters(*filt)
+    out = _run(sv, ver, w, row_stats=True)
+    ref = oracle_for(w, filters=filt)
+    st = compare(w, out, ref, what=f"histogram cut rows {kind}", filters=filt)
+    invalid = ref["accepted_len"] < 0
+    if kind in ("late_nan", "late_posinf"):
+        # sequences with a NaN or +inf in one of their rows are invalid on both sides
+        assert invalid.any()
+        assert np.array_equal(out["accepted_len"].cpu().numpy() < 0, invalid)
+    else:
+        assert not invalid.any()
+    # the filtered rows' statistics pin every valid row's kept set
+    ok = (ref["margin"] >= 1e-6) & ~invalid
+    rs = out["row_stats"].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(rs[ok][..., 0], ref["row_stats"][ok][..., 0], rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(rs[ok][..., 1], ref["row_stats"][ok][..., 1], rtol=1e-5, atol=1e-5)
+    assert st["compared"] >= 2 and ok.sum() >= 2
+    ver.close()
+
+
 def _same_rows_workload(B, k, V, dtype, x, gate, tau, seed):
     """Draft rows equal to the target rows (p = q at every position) and each
     drafted token the smallest draft logit, outside any filtered set: every
